@@ -1,0 +1,211 @@
+"""Seeded synthetic inputs shared by the tests, the bench and the oracle's callers.
+
+The generator is defined once in ``synth_core.h`` (SplitMix64 counter stream ->
+Irwin-Hall twelve-uniform normal approximation -> one IEEE rounding per
+operation -> optional Bernoulli outlier scaling -> bf16 round-to-nearest-even
+for activations).  ``libmtsynth_host.so`` evaluates it on the host and
+``libmtsynth_dev.so`` on the GPU; both give the same bits for the same element
+index.  Nothing here computes any part of the decode MLP itself.
+
+The workloads below stand in for the Llama/Qwen-shaped layers the meTile
+"MLX-LM Backend" page measures (no checkpoints are used or needed): every
+tensor is drawn from the generator with the distribution stated per workload.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass, field
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_HOST_SO = os.path.join(_HERE, "libmtsynth_host.so")
+_DEV_SO = os.path.join(_HERE, "libmtsynth_dev.so")
+_lock = threading.Lock()
+_host = None
+_dev = None
+
+# tensor ids inside one layer's seed space
+T_VALUES, T_RESIDUAL, T_NORM_W, T_WG, T_WU, T_WD, T_X, T_H, T_RES3 = range(9)
+
+OUTLIER_P32_1PCT = 42949673  # round(0.01 * 2**32)
+
+
+def seed_for(workload_id: int, layer: int, tensor: int) -> int:
+    """Seed of one tensor: 0x5EED0000 + 16*workload + tensor, layer in the high word."""
+    return (0x5EED0000 + 16 * workload_id + tensor + (layer << 32)) & 0xFFFFFFFFFFFFFFFF
+
+
+def _newer(dst: str, srcs) -> bool:
+    return os.path.exists(dst) and all(os.path.getmtime(dst) >= os.path.getmtime(s) for s in srcs)
+
+
+def build(force: bool = False, device: bool = True) -> None:
+    """Compile the host (gcc) and device (nvcc, sm_103a) generator libraries."""
+    hdr = os.path.join(_HERE, "synth_core.h")
+    hsrc = os.path.join(_HERE, "synth_host.c")
+    if force or not _newer(_HOST_SO, [hdr, hsrc]):
+        subprocess.check_call(
+            ["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-o", _HOST_SO, hsrc],
+            cwd=_HERE)
+    if device:
+        dsrc = os.path.join(_HERE, "synth_dev.cu")
+        if force or not _newer(_DEV_SO, [hdr, dsrc]):
+            subprocess.check_call(
+                ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
+                 "-Xcompiler", "-fPIC", "-shared", "-o", _DEV_SO, dsrc],
+                cwd=_HERE)
+
+
+def _host_lib():
+    global _host
+    with _lock:
+        if _host is None:
+            build(device=False)
+            lib = ctypes.CDLL(_HOST_SO)
+            for name, ptr_t in (("syn_fill_f32_host", ctypes.c_void_p),
+                                ("syn_fill_bf16_host", ctypes.c_void_p)):
+                fn = getattr(lib, name)
+                fn.restype = None
+                fn.argtypes = [ptr_t, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                               ctypes.c_float, ctypes.c_float, ctypes.c_uint32, ctypes.c_float]
+            _host = lib
+    return _host
+
+
+def _dev_lib():
+    global _dev
+    with _lock:
+        if _dev is None:
+            if not os.path.exists(_DEV_SO):
+                raise RuntimeError("synth device library missing: run synth.build()")
+            lib = ctypes.CDLL(_DEV_SO)
+            for name in ("syn_fill_f32_device", "syn_fill_bf16_device"):
+                fn = getattr(lib, name)
+                fn.restype = ctypes.c_int
+                fn.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                               ctypes.c_float, ctypes.c_float, ctypes.c_uint32, ctypes.c_float,
+                               ctypes.c_void_p]
+            _dev = lib
+    return _dev
+
+
+@dataclass(frozen=True)
+class Dist:
+    """Distribution of one tensor: normal(mean, std) with optional outliers."""
+    mean: float = 0.0
+    std: float = 1.0
+    outlier_p32: int = 0
+    outlier_scale: float = 1.0
+
+    def args(self):
+        return (float(np.float32(self.mean)), float(np.float32(self.std)),
+                int(self.outlier_p32), float(np.float32(self.outlier_scale)))
+
+
+ACT = Dist(0.0, 1.0)
+NORM_W = Dist(1.0, 0.1)
+WEIGHT = Dist(0.0, 0.02)
+WEIGHT_OUTLIERS = Dist(0.0, 0.02, OUTLIER_P32_1PCT, 20.0)
+
+
+def host_f32(n: int, seed: int, dist: Dist, offset: int = 0) -> np.ndarray:
+    out = np.empty(n, dtype=np.float32)
+    _host_lib().syn_fill_f32_host(out.ctypes.data, n, seed, offset, *dist.args())
+    return out
+
+
+def host_bf16(n: int, seed: int, dist: Dist, offset: int = 0) -> np.ndarray:
+    """bf16 values as their uint16 bit patterns."""
+    out = np.empty(n, dtype=np.uint16)
+    _host_lib().syn_fill_bf16_host(out.ctypes.data, n, seed, offset, *dist.args())
+    return out
+
+
+def device_f32(tensor, seed: int, dist: Dist, offset: int = 0, stream=None) -> None:
+    """Fill a contiguous float32 CUDA tensor in place."""
+    import torch
+    assert tensor.is_cuda and tensor.dtype == torch.float32 and tensor.is_contiguous()
+    s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    rc = _dev_lib().syn_fill_f32_device(tensor.data_ptr(), tensor.numel(), seed, offset,
+                                        *dist.args(), s)
+    if rc != 0:
+        raise RuntimeError(f"syn_fill_f32_device failed: cudaError {rc}")
+
+
+def device_bf16(tensor, seed: int, dist: Dist, offset: int = 0, stream=None) -> None:
+    """Fill a contiguous bfloat16 (or int16/uint16) CUDA tensor in place."""
+    import torch
+    assert tensor.is_cuda and tensor.element_size() == 2 and tensor.is_contiguous()
+    s = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    rc = _dev_lib().syn_fill_bf16_device(tensor.data_ptr(), tensor.numel(), seed, offset,
+                                         *dist.args(), s)
+    if rc != 0:
+        raise RuntimeError(f"syn_fill_bf16_device failed: cudaError {rc}")
+
+
+# ---------------------------------------------------------------------------
+# Workloads (shapes and distributions of the five measured layer shapes)
+# ---------------------------------------------------------------------------
+FMT_BF16, FMT_AFFINE8, FMT_AFFINE4 = 0, 1, 2
+FMT_NAMES = {FMT_BF16: "bf16", FMT_AFFINE8: "affine8", FMT_AFFINE4: "affine4"}
+
+
+@dataclass(frozen=True)
+class Workload:
+    wid: int            # seed-space id
+    name: str
+    d: int              # hidden size
+    f: int              # intermediate size
+    M: int              # rows
+    fmt: int            # weight format
+    group: int          # affine group along K (0 for bf16)
+    eps: float
+    layers: int = 1
+    weight_dist: Dist = WEIGHT
+    out_f32: bool = False
+
+    @property
+    def bits(self) -> int:
+        return {FMT_BF16: 16, FMT_AFFINE8: 8, FMT_AFFINE4: 4}[self.fmt]
+
+    def weight_bytes(self) -> int:
+        """Packed weight + scale/bias bytes of one layer (gate, up, down)."""
+        n_w = 3 * self.d * self.f
+        wb = n_w * self.bits // 8
+        sb = 0 if self.fmt == FMT_BF16 else 2 * 2 * (n_w // self.group)
+        return wb + sb
+
+    def act_bytes(self) -> int:
+        """Activation bytes of one layer: K1 reads v, r (2*M*d bf16) and the norm
+        weight (d), writes out_sum and out_norm (2*M*d); K2 reads x (M*d), writes
+        h (M*f); K3 reads h (M*f) and the residual (M*d), writes y (M*d)."""
+        M, d, f = self.M, self.d, self.f
+        return 2 * (7 * M * d + 2 * M * f + d)
+
+    def layer_bytes(self) -> int:
+        return self.weight_bytes() + self.act_bytes()
+
+    def with_(self, **kw) -> "Workload":
+        from dataclasses import replace
+        return replace(self, **kw)
+
+
+TINY = Workload(1, "tiny d256 f768 affine8 g64", 256, 768, 1, FMT_AFFINE8, 64, 1e-5)
+LLAMA1B = Workload(2, "llama3.2-1b layer d2048 f8192 affine4 g64", 2048, 8192, 1, FMT_AFFINE4, 64, 1e-5)
+QWEN15 = Workload(3, "qwen2.5-1.5b layer d1536 f8960 bf16", 1536, 8960, 1, FMT_BF16, 0, 1e-6)
+QWEN8B = Workload(4, "qwen3-8b stack d4096 f12288 affine8 g128 x36", 4096, 12288, 1, FMT_AFFINE8, 128,
+                  1e-6, layers=36)
+
+
+def sweep_point(group: int, M: int) -> Workload:
+    return Workload(5, f"sweep d2048 f8192 affine8 g{group} M{M} outliers", 2048, 8192, M,
+                    FMT_AFFINE8, group, 1e-5, weight_dist=WEIGHT_OUTLIERS)
+
+
+SWEEP = [sweep_point(g, m) for g in (32, 64, 128) for m in (1, 2, 4, 8)]
+ALL = [TINY, LLAMA1B, QWEN15, QWEN8B] + SWEEP

@@ -1,0 +1,442 @@
+"""Pins of the float64 CPU oracle to facts that do not come from the oracle.
+
+Each oracle function is tied to at least one of: hand-derived fixtures
+(tests/golden), IEEE-754 textbook cases, a library routine on the special case
+where it applies (torch's fp32 -> bf16 conversion), exact rational brute force
+(fractions.Fraction) on tiny shapes, closed forms and invariants.  Shapes are
+non-square and M > 1 where it matters, so a transposed operand, a swapped gate
+and up, a wrong group index or a dropped term fails a test.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------- helpers
+def torch_bf16_bits_from_f32(x32: np.ndarray) -> np.ndarray:
+    """Library conversion fp32 -> bf16 (round to nearest even) as uint16 bits."""
+    t = torch.from_numpy(np.ascontiguousarray(x32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def torch_f64_from_bf16(bits: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16))
+    return t.view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def frac_bf16(bits: int) -> Fraction:
+    return Fraction(float(torch_f64_from_bf16(np.array([bits], dtype=np.uint16))[0]))
+
+
+def bf16_neighbours_nearest(value: Fraction, bits: int) -> bool:
+    """True if bf16 `bits` is a nearest bf16 to the exact `value` (checks the
+    two adjacent bf16 patterns of the same sign)."""
+    c = frac_bf16(bits)
+    d = abs(c - value)
+    for nb in (bits - 1, bits + 1):
+        if 0 <= nb < 0x10000 and (nb & 0x7F80) != 0x7F80:
+            if abs(frac_bf16(nb) - value) < d:
+                return False
+    return True
+
+
+def gen_bf16(n, seed, dist=synth.ACT):
+    return synth.host_bf16(n, seed, dist)
+
+
+# ------------------------------------------------------------------ bf16
+def _read_bf16_cases():
+    rows = []
+    with open(os.path.join(GOLD, "bf16_cases.txt")) as fh:
+        for line in fh:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            a, b = line.split()[:2]
+            rows.append((float.fromhex(a) if a not in ("inf", "-inf", "nan") else float(a), int(b, 16)))
+    return rows
+
+
+@pytest.mark.parametrize("x,expect", _read_bf16_cases())
+def test_bf16_textbook_cases(x, expect):
+    got = int(oracle.bf16_from_f64(np.array([x]))[0])
+    assert got == expect, f"{x!r}: {got:04x} != {expect:04x}"
+
+
+def test_bf16_matches_library_on_fp32_values():
+    # For inputs that are binary32 values a single rounding from binary64 and
+    # torch's fp32 -> bf16 conversion must agree bit for bit.
+    rng = np.random.default_rng(1)
+    u = rng.integers(0, 2**32, size=200000, dtype=np.uint64).astype(np.uint32)
+    x32 = u.view(np.float32)
+    x32 = x32[np.isfinite(x32)]
+    # add exact ties and near-ties around bf16 rounding boundaries
+    base = rng.integers(0, 2**16, size=20000, dtype=np.uint32) << 16
+    ties = (base | 0x8000).view(np.float32)
+    near = (base | 0x7FFF).view(np.float32)
+    x32 = np.concatenate([x32, ties[np.isfinite(ties)], near[np.isfinite(near)]])
+    got = oracle.bf16_from_f64(x32.astype(np.float64))
+    exp = torch_bf16_bits_from_f32(x32)
+    assert np.array_equal(got, exp)
+
+
+def test_bf16_decode_matches_library_all_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.f64_from_bf16(bits)
+    exp = torch_f64_from_bf16(bits)
+    nan = np.isnan(exp)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], exp[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(exp[~nan]))
+
+
+def test_bf16_round_trip_identity():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.f64_from_bf16(bits)
+    ok = ~np.isnan(vals)
+    assert np.array_equal(oracle.bf16_from_f64(vals[ok]), bits[ok])
+
+
+# ------------------------------------------------------------- quantiser
+def _read_quant_groups():
+    groups, cur = [], None
+    with open(os.path.join(GOLD, "quant_groups.txt")) as fh:
+        for line in fh:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            tok = line.split()
+            if tok[0] == "group":
+                cur = dict(name=tok[1], bits=int(tok[2].split("=")[1]), vals=[], codes=[])
+                groups.append(cur)
+            elif tok[0] in ("scale", "bias"):
+                cur[tok[0]] = int(tok[1], 16)
+            else:
+                cur["vals"].append(float.fromhex(tok[0]))
+                cur["codes"].append(int(tok[1]))
+    return groups
+
+
+@pytest.mark.parametrize("grp", _read_quant_groups(), ids=lambda g: g["name"])
+def test_quantizer_hand_built_groups(grp):
+    g = 32
+    vals = grp["vals"] + [grp["vals"][0]] * (g - len(grp["vals"]))
+    codes_exp = grp["codes"] + [grp["codes"][0]] * (g - len(grp["codes"]))
+    W = np.array([vals], dtype=np.float32)
+    assert np.array_equal(W.astype(np.float64)[0], np.array(vals))  # all exact in fp32
+    codes, s, b = oracle.quantize(W, g, grp["bits"])
+    assert list(codes[0]) == codes_exp
+    assert int(s[0, 0]) == grp["scale"]
+    assert int(b[0, 0]) == grp["bias"]
+
+
+def test_quantizer_grid_round_trip_exact():
+    # scale 2^-8 / 2^-4 exactly: dequantised values reproduce the inputs
+    for bits, step in ((8, 2.0 ** -8), (4, 2.0 ** -4)):
+        qmax = (1 << bits) - 1
+        k = np.arange(64) % (qmax + 1)
+        k[0], k[1] = 0, qmax
+        W = (k * step).astype(np.float32)[None, :].repeat(3, 0)
+        codes, s, b = oracle.quantize(W, 64, bits)
+        assert np.array_equal(codes[0], k)
+        wd = oracle.dequant(codes, s, b, 64)
+        assert np.array_equal(wd, W.astype(np.float64))
+
+
+def test_quantizer_against_brute_force_argmin():
+    rng = np.random.default_rng(7)
+    for bits, group in ((8, 32), (4, 32), (8, 64), (4, 128)):
+        qmax = (1 << bits) - 1
+        N, K = 3, 2 * group
+        W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+        W[1, 5] *= 20.0  # an outlier inside one group
+        codes, s, b = oracle.quantize(W, group, bits)
+        assert codes.shape == (N, K) and s.shape == (N, K // group)
+        for n in range(N):
+            for gi in range(K // group):
+                seg = W[n, gi * group:(gi + 1) * group].astype(np.float64)
+                mn, mx = Fraction(float(seg.min())), Fraction(float(seg.max()))
+                # bias: nearest bf16 to min (library conversion of an fp32 value)
+                assert int(b[n, gi]) == int(torch_bf16_bits_from_f32(np.array([seg.min()], np.float32))[0])
+                # scale: a nearest bf16 to (max - min) / qmax
+                assert bf16_neighbours_nearest((mx - mn) / qmax, int(s[n, gi]))
+                sc, bi = frac_bf16(int(s[n, gi])), frac_bf16(int(b[n, gi]))
+                for k in range(group):
+                    w = Fraction(float(seg[k]))
+                    errs = [abs(w - (sc * c + bi)) for c in range(qmax + 1)]
+                    best = min(errs)
+                    cands = [c for c in range(qmax + 1) if errs[c] == best]
+                    exp_c = cands[0] if len(cands) == 1 else [c for c in cands if c % 2 == 0][0]
+                    assert codes[n, gi * group + k] == exp_c
+
+
+def test_quantizer_error_bound():
+    # |w - w'| <= scale/2 + |bias - min| + qmax*|scale - (max-min)/qmax| (closed form)
+    W = synth.host_f32(16 * 256, 99, synth.WEIGHT_OUTLIERS).reshape(16, 256)
+    for bits in (8, 4):
+        qmax = (1 << bits) - 1
+        codes, s, b = oracle.quantize(W, 64, bits)
+        wd = oracle.dequant(codes, s, b, 64)
+        sv = oracle.f64_from_bf16(s).repeat(64, axis=1)
+        bv = oracle.f64_from_bf16(b).repeat(64, axis=1)
+        Wg = W.astype(np.float64).reshape(16, 4, 64)
+        mn = Wg.min(-1).repeat(64, axis=1)
+        mx = Wg.max(-1).repeat(64, axis=1)
+        bound = sv / 2 + np.abs(bv - mn) + qmax * np.abs(sv - (mx - mn) / qmax)
+        assert np.all(np.abs(W - wd) <= bound * (1 + 1e-12))
+
+
+def test_quantizer_constant_and_zero_groups():
+    W = np.zeros((2, 64), dtype=np.float32)
+    W[1, :] = -0.75
+    codes, s, b = oracle.quantize(W, 32, 8)
+    assert not codes.any() and not s.any()
+    assert list(b[0]) == [0, 0] and list(b[1]) == [0xBF40, 0xBF40]
+    assert np.array_equal(oracle.dequant(codes, s, b, 32), W.astype(np.float64))
+
+
+def test_groups_run_along_k_not_n():
+    # Row 0 uses a small range, row 1 a large one, and the two halves of each
+    # row differ: scales must be indexed [n][k / group].
+    W = np.zeros((2, 64), dtype=np.float32)
+    W[0, :32] = np.linspace(0, 1, 32)
+    W[0, 32:] = np.linspace(0, 2, 32)
+    W[1, :32] = np.linspace(0, 4, 32)
+    W[1, 32:] = np.linspace(0, 8, 32)
+    _, s, _ = oracle.quantize(W, 32, 8)
+    vals = oracle.f64_from_bf16(s)
+    assert vals[0, 0] < vals[0, 1] < vals[1, 0] < vals[1, 1]
+
+
+def test_pack_codes_layout():
+    codes = np.array([[1, 2, 3, 4, 15, 0], [0, 15, 7, 8, 9, 10]], dtype=np.uint8)
+    p4 = oracle.pack_codes(codes, 4)
+    assert p4.tolist() == [[0x21, 0x43, 0x0F], [0xF0, 0x87, 0xA9]]
+    p8 = oracle.pack_codes(codes, 8)
+    assert np.array_equal(p8, codes)
+    with pytest.raises(ValueError):
+        oracle.pack_codes(np.array([[16, 0]], dtype=np.uint8), 4)
+
+
+def test_dequant_exact_rational():
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 256, size=(3, 64)).astype(np.uint8)
+    s = torch_bf16_bits_from_f32(rng.uniform(1e-4, 1e-2, size=(3, 2)).astype(np.float32))
+    b = torch_bf16_bits_from_f32(rng.uniform(-0.1, 0.0, size=(3, 2)).astype(np.float32))
+    wd = oracle.dequant(codes, s, b, 32)
+    for n in range(3):
+        for k in range(64):
+            exp = frac_bf16(int(s[n, k // 32])) * int(codes[n, k]) + frac_bf16(int(b[n, k // 32]))
+            assert Fraction(float(wd[n, k])) == exp
+
+
+# --------------------------------------------------------------- RMSNorm
+def _read_rms_cases():
+    rows = []
+    with open(os.path.join(GOLD, "rmsnorm_worked.txt")) as fh:
+        for line in fh:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            name, eps, v, r, w, exp = line.split()
+            hx = lambda t: np.array([int(x, 16) for x in t.split(",")], dtype=np.uint16)
+            rows.append((name, float(eps), hx(v), hx(r), hx(w), np.array([float(x) for x in exp.split(",")])))
+    return rows
+
+
+@pytest.mark.parametrize("case", _read_rms_cases(), ids=lambda c: c[0])
+def test_rmsnorm_worked_vectors(case):
+    _, eps, v, r, w, exp = case
+    out_sum, norm = oracle.add_rmsnorm(v, r, w, eps)
+    np.testing.assert_allclose(norm[0], exp, rtol=2e-16 * 8, atol=0)
+    assert np.array_equal(out_sum[0], oracle.bf16_from_f64(oracle.f64_from_bf16(v) + oracle.f64_from_bf16(r)))
+
+
+def test_rmsnorm_constant_vector_closed_form():
+    for c_bits, eps in ((0x4040, 1e-5), (0x3C00, 1e-6), (0xC2C8, 1e-5)):
+        d = 96
+        v = np.full(d, c_bits, dtype=np.uint16)
+        r = np.zeros(d, dtype=np.uint16)
+        w = gen_bf16(d, 5, synth.NORM_W)
+        _, norm = oracle.add_rmsnorm(v, r, w, eps)
+        c = float(oracle.f64_from_bf16(np.array([c_bits]))[0])
+        exp = c * oracle.f64_from_bf16(w) / math.sqrt(c * c + eps)
+        np.testing.assert_allclose(norm[0], exp, rtol=1e-14)
+
+
+def test_add_rmsnorm_brute_force_and_fusion_invariance():
+    M, d = 3, 40
+    v = gen_bf16(M * d, 11).reshape(M, d)
+    r = gen_bf16(M * d, 12).reshape(M, d)
+    w = gen_bf16(d, 13, synth.NORM_W)
+    eps = 1e-5
+    out_sum, norm = oracle.add_rmsnorm(v, r, w, eps)
+    vf, rf, wf = torch_f64_from_bf16(v), torch_f64_from_bf16(r), torch_f64_from_bf16(w)
+    # summed output = bf16(values + residual); for these operands the fp32 sum
+    # is exact, so the library conversion of it is the reference
+    assert np.array_equal(out_sum, torch_bf16_bits_from_f32((vf + rf).astype(np.float32)))
+    sf = torch_f64_from_bf16(out_sum)
+    for m in range(M):
+        ms = sum(Fraction(float(x)) ** 2 for x in sf[m]) / d
+        den = math.sqrt(float(ms) + eps)
+        exp = [float(sf[m, i]) * float(wf[i]) / den for i in range(d)]
+        np.testing.assert_allclose(norm[m], exp, rtol=1e-14)
+    # rows are independent: permuting rows permutes both outputs
+    perm = [2, 0, 1]
+    s2, n2 = oracle.add_rmsnorm(v[perm], r[perm], w, eps)
+    assert np.array_equal(s2, out_sum[perm]) and np.array_equal(n2, norm[perm])
+
+
+def test_rmsnorm_scale_invariance():
+    d = 64
+    v = gen_bf16(d, 21)
+    r = np.zeros(d, dtype=np.uint16)
+    w = gen_bf16(d, 22, synth.NORM_W)
+    v4 = oracle.bf16_from_f64(oracle.f64_from_bf16(v) * 4.0)  # exact power-of-two scaling
+    _, n1 = oracle.add_rmsnorm(v, r, w, 1e-12)
+    _, n4 = oracle.add_rmsnorm(v4, r, w, 1e-12)
+    np.testing.assert_allclose(n1, n4, rtol=1e-10)
+
+
+# ---------------------------------------------------------------- SwiGLU
+def _weight(fmt_bits, N, K, group, seed, dist=synth.WEIGHT):
+    W32 = synth.host_f32(N * K, seed, dist).reshape(N, K)
+    return oracle.Weight.from_f32(W32, fmt_bits, group)
+
+
+def _frac_dense(w: oracle.Weight):
+    if w.fmt == oracle.FMT_BF16:
+        return [[Fraction(float(x)) for x in row] for row in torch_f64_from_bf16(w.W)]
+    out = []
+    G = w.W.shape[1] // w.group
+    for n in range(w.W.shape[0]):
+        row = []
+        for k in range(w.W.shape[1]):
+            sc = frac_bf16(int(w.scales[n, k // w.group]))
+            bi = frac_bf16(int(w.biases[n, k // w.group]))
+            row.append(sc * int(w.W[n, k]) + bi)
+        out.append(row)
+    return out
+
+
+@pytest.mark.parametrize("fmt_bits,group", [(8, 32), (4, 64), (16, 0)])
+def test_swiglu_gateup_brute_force(fmt_bits, group):
+    M, K, N = 2, 128, 5
+    x = gen_bf16(M * K, 31).reshape(M, K)
+    Wg = _weight(fmt_bits, N, K, group, 32)
+    Wu = _weight(fmt_bits, N, K, group, 33)
+    h, g, u = oracle.swiglu_gateup(x, Wg, Wu, return_gu=True)
+    xf = [[Fraction(float(t)) for t in row] for row in torch_f64_from_bf16(x)]
+    Gd, Ud = _frac_dense(Wg), _frac_dense(Wu)
+    for m in range(M):
+        for n in range(N):
+            ge = sum(a * b for a, b in zip(xf[m], Gd[n]))
+            ue = sum(a * b for a, b in zip(xf[m], Ud[n]))
+            scale = float(sum(abs(a * b) for a, b in zip(xf[m], Gd[n])))
+            assert abs(g[m, n] - float(ge)) <= 1e-14 * scale
+            assert abs(u[m, n] - float(ue)) <= 1e-14 * float(sum(abs(a * b) for a, b in zip(xf[m], Ud[n])))
+            hb = float(ge) / (1.0 + math.exp(-float(ge))) * float(ue)
+            assert abs(h[m, n] - hb) <= 1e-13 * max(1.0, abs(hb))
+    # gate and up are not interchangeable
+    h_swapped = oracle.swiglu_gateup(x, Wu, Wg)
+    assert not np.allclose(h, h_swapped)
+
+
+def _const_weight(N, K, group, scale_bits, bias_bits, code):
+    G = K // group
+    return oracle.Weight(oracle.FMT_CODES, np.full((N, K), code, np.uint8),
+                         np.full((N, G), scale_bits, np.uint16), np.full((N, G), bias_bits, np.uint16),
+                         group)
+
+
+def test_silu_special_cases():
+    assert oracle.silu(0.0) == 0.0
+    assert abs(oracle.silu(20.0) - 20.0) <= 20.0 * 2.1e-9
+    assert 0 > oracle.silu(-20.0) > -20.0 * math.exp(-20.0) * 1.0000001
+    K, N = 64, 3
+    x = gen_bf16(K, 41)[None, :]
+    zero = _const_weight(N, K, 32, 0, 0, 0)                 # all-zero gate rows
+    Wu = _weight(8, N, K, 32, 42)
+    h = oracle.swiglu_gateup(x, zero, Wu)
+    assert np.all(h == 0.0)
+    # g = 20 exactly: x = 1 everywhere (bf16 0x3F80), gate weights 20/64 = 0.3125
+    ones = np.full((1, K), 0x3F80, np.uint16)
+    gate20 = _const_weight(N, K, 32, 0x3EA0, 0, 1)           # scale 0.3125 * q(=1)
+    h, g, u = oracle.swiglu_gateup(ones, gate20, Wu, return_gu=True)
+    assert np.all(g == 20.0)
+    np.testing.assert_allclose(h, 20.0 * u, rtol=2.1e-9)
+    gate_m20 = _const_weight(N, K, 32, 0, 0xBEA0, 0)         # bias -0.3125
+    h, g, u = oracle.swiglu_gateup(ones, gate_m20, Wu, return_gu=True)
+    assert np.all(g == -20.0)
+    assert np.all(np.abs(h) <= 20.0 * math.exp(-20.0) * np.abs(u) * 1.0000001)
+
+
+# ------------------------------------------------------------ down + res
+@pytest.mark.parametrize("fmt_bits,group", [(8, 64), (4, 32), (16, 0)])
+def test_down_residual_brute_force(fmt_bits, group):
+    M, K, N = 2, 192, 7
+    h = gen_bf16(M * K, 51).reshape(M, K)
+    res = gen_bf16(M * N, 52).reshape(M, N)
+    Wd = _weight(fmt_bits, N, K, group, 53)
+    y = oracle.down_residual(h, Wd, res)
+    hf = [[Fraction(float(t)) for t in row] for row in torch_f64_from_bf16(h)]
+    rf = torch_f64_from_bf16(res)
+    D = _frac_dense(Wd)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(a * b for a, b in zip(hf[m], D[n])) + Fraction(float(rf[m, n]))
+            scale = float(sum(abs(a * b) for a, b in zip(hf[m], D[n]))) + abs(float(rf[m, n]))
+            assert abs(y[m, n] - float(exact)) <= 1e-14 * scale
+
+
+def test_down_residual_zero_weights_and_identity():
+    M, K = 2, 64
+    h = gen_bf16(M * K, 61).reshape(M, K)
+    res = gen_bf16(M * K, 62).reshape(M, K)
+    zero = _const_weight(K, K, 32, 0, 0, 0)
+    y = oracle.down_residual(h, zero, res)
+    assert np.array_equal(y, torch_f64_from_bf16(res))
+    eye = oracle.Weight(oracle.FMT_BF16, np.where(np.eye(K, dtype=bool), 0x3F80, 0).astype(np.uint16))
+    y = oracle.down_residual(h, eye, res)
+    assert np.array_equal(y, torch_f64_from_bf16(h) + torch_f64_from_bf16(res))
+    # a non-square projection with one non-zero column per row picks h[:, k]
+    N = 5
+    sel = np.zeros((N, K), np.uint16)
+    for n in range(N):
+        sel[n, 3 * n + 1] = 0x4000  # weight 2.0
+    y = oracle.down_residual(h, oracle.Weight(oracle.FMT_BF16, sel), np.zeros((M, N), np.uint16))
+    hf = torch_f64_from_bf16(h)
+    assert np.array_equal(y, 2.0 * hf[:, [3 * n + 1 for n in range(N)]])
+
+
+# ----------------------------------------------------------- composition
+def test_mlp_layer_and_stack_composition():
+    d, f, M, g = 64, 96, 2, 32
+    rng_seed = 70
+    v = [gen_bf16(M * d, rng_seed + i).reshape(M, d) for i in range(2)]
+    r0 = gen_bf16(M * d, rng_seed + 5).reshape(M, d)
+    layers = []
+    for l in range(2):
+        layers.append((gen_bf16(d, 80 + l, synth.NORM_W), _weight(8, f, d, g, 90 + l),
+                       _weight(8, f, d, g, 95 + l), _weight(8, d, f, g, 99 + l)))
+    out = oracle.mlp_stack(v, r0, layers, 1e-5)
+    r = r0
+    for l in range(2):
+        w, Wg, Wu, Wd = layers[l]
+        s, nx = oracle.add_rmsnorm(v[l], r, w, 1e-5)
+        hx = oracle.swiglu_gateup(oracle.bf16_from_f64(nx), Wg, Wu)
+        yx = oracle.down_residual(oracle.bf16_from_f64(hx), Wd, s)
+        assert np.array_equal(out[l]["out_sum"], s)
+        assert np.array_equal(out[l]["h"], oracle.bf16_from_f64(hx))
+        assert np.array_equal(out[l]["y_x"], yx)
+        r = oracle.bf16_from_f64(yx)
+    assert not np.array_equal(out[0]["y"], out[1]["y"])

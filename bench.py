@@ -1,0 +1,473 @@
+"""Benchmark of the one-row decode MLP on GB300.
+
+Default workload: the Qwen3-8B-shaped decode stack (d=4096, f=12288, one row,
+36 layers with distinct weights, affine INT8 group 128, ~5.6 GB streamed per
+step -- larger than L2, so no flush is needed between steps).  A step is one
+pass over the whole stack: per layer add+RMSNorm, gate/up GEMV + SwiGLU, down
+GEMV + residual, each a call of the C ABI.  The step is captured once into a
+CUDA graph (the calls keep their programmatic-dependent-launch attributes) and
+replayed.
+
+Printed JSON line (one per run, rank 0):
+  value       effective HBM GB/s = algorithmic bytes of the step / step time
+  e2e         the same metric with the step's inputs copied host->device from
+              pinned memory and the output read back, inside the timed region
+  roofline    the dominant kernel (gate/up + SwiGLU) timed alone over the 36
+              layers with CUDA events, against the measured HBM peak
+  cpu_baseline the float64 CPU oracle timed on one layer of the same workload
+  clocks      SM clocks / throttle reasons sampled during the timed region
+
+``--impl reference`` times the CPU oracle (the only reference this method
+has: the pages describe Apple-GPU Metal kernels that cannot run here).
+Multi-GPU (torchrun): independent replicas, one stack per GPU, no collective
+on the data path; value = total bytes of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per decode MLP layer and effective HBM GB/s (fraction of ~8 TB/s peak)"
+GATEUP_PROFILE = os.path.join(ROOT, "profiles", "gateup_affine8_qwen3-8b.txt")
+KERNEL_SOURCES = ["k_gemv.cuh", "k_gemv_run.cuh", "k_gemv_a8.cu", "mt_device.cuh"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "quantized_gemv_epilogues_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the gate/up kernel from the committed ncu
+    summary, or None when the summary is missing or the kernel changed."""
+    if not os.path.exists(GATEUP_PROFILE):
+        return None
+    kv = {}
+    with open(GATEUP_PROFILE) as fh:
+        for line in fh:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("kernel_sources_sha256_16") != kernel_hash():
+        return None
+    try:
+        return int(kv["dram_bytes_per_launch_full"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ stack
+class Stack:
+    """Device-resident packed weights and activation buffers of a decode stack."""
+
+    def __init__(self, wl, device, layers=None):
+        import torch
+        import synth
+        import quantized_gemv_epilogues_gb300 as mt
+        self.mt, self.torch = mt, torch
+        self.wl = wl
+        self.L = layers or wl.layers
+        d, f, M, g = wl.d, wl.f, wl.M, wl.group
+        self.dev = device
+        bf = torch.bfloat16
+        tmp = torch.empty(max(d * f, 1), dtype=torch.float32, device=device)
+        self.layers = []
+        for l in range(self.L):
+            sd = lambda t: synth.seed_for(wl.wid, l, t)
+            w_norm = torch.empty(d, dtype=bf, device=device)
+            synth.device_bf16(w_norm, sd(synth.T_NORM_W), synth.NORM_W)
+            if wl.fmt == synth.FMT_BF16:
+                Wg = torch.empty(f, d, dtype=bf, device=device)
+                Wu = torch.empty(f, d, dtype=bf, device=device)
+                Wd = torch.empty(d, f, dtype=bf, device=device)
+                synth.device_bf16(Wg, sd(synth.T_WG), wl.weight_dist)
+                synth.device_bf16(Wu, sd(synth.T_WU), wl.weight_dist)
+                synth.device_bf16(Wd, sd(synth.T_WD), wl.weight_dist)
+                sgu = bgu = sdn = bdn = None
+            else:
+                bits = wl.bits
+                Wg = torch.empty(f, d * bits // 8, dtype=torch.uint8, device=device)
+                Wu = torch.empty_like(Wg)
+                Wd = torch.empty(d, f * bits // 8, dtype=torch.uint8, device=device)
+                sgu = torch.empty(2, f, d // g, dtype=bf, device=device)
+                bgu = torch.empty_like(sgu)
+                sdn = torch.empty(d, f // g, dtype=bf, device=device)
+                bdn = torch.empty_like(sdn)
+                for (dst, s_, b_, N, K, t) in ((Wg, sgu[0], bgu[0], f, d, synth.T_WG),
+                                               (Wu, sgu[1], bgu[1], f, d, synth.T_WU),
+                                               (Wd, sdn, bdn, d, f, synth.T_WD)):
+                    W32 = tmp[:N * K].view(N, K)
+                    synth.device_f32(W32, sd(t), wl.weight_dist)
+                    mt.mt_pack_affine(W32, N, K, g, bits, dst, s_, b_)
+            values = torch.empty(M, d, dtype=bf, device=device)
+            synth.device_bf16(values, sd(synth.T_VALUES), synth.ACT)
+            self.layers.append(dict(w=w_norm, Wg=Wg, Wu=Wu, Wd=Wd, sgu=sgu, bgu=bgu, sd=sdn,
+                                    bd=bdn, values=values))
+        del tmp
+        self.r0 = torch.empty(M, d, dtype=bf, device=device)
+        synth.device_bf16(self.r0, synth.seed_for(wl.wid, 0, synth.T_RESIDUAL), synth.ACT)
+        self.resid = torch.empty(M, d, dtype=bf, device=device)
+        self.norm = torch.empty(M, d, dtype=bf, device=device)
+        self.h = torch.empty(M, wl.f, dtype=bf, device=device)
+        torch.cuda.synchronize()
+
+    def step(self):
+        """One pass over the stack (3 C-ABI calls per layer)."""
+        mt, wl = self.mt, self.wl
+        self.resid.copy_(self.r0)
+        for L in self.layers:
+            mt.mt_add_rmsnorm(L["values"], self.resid, L["w"], wl.eps, self.resid, self.norm)
+            mt.mt_swiglu_gateup(self.norm, L["Wg"], L["Wu"], L["sgu"], L["bgu"], wl.group, self.h,
+                                fmt=wl.fmt)
+            mt.mt_down_residual(self.h, L["Wd"], L["sd"], L["bd"], wl.group, self.resid, self.resid,
+                                fmt=wl.fmt)
+
+    def gateup_only(self):
+        mt, wl = self.mt, self.wl
+        for L in self.layers:
+            mt.mt_swiglu_gateup(self.norm, L["Wg"], L["Wu"], L["sgu"], L["bgu"], wl.group, self.h,
+                                fmt=wl.fmt)
+
+    def gateup_bytes(self):
+        wl = self.wl
+        n = 2 * wl.f * wl.d
+        w = n * wl.bits // 8 + (0 if wl.fmt == 0 else 4 * n // wl.group)
+        return w + 2 * wl.M * wl.d + 2 * wl.M * wl.f
+
+
+def capture(fn, torch):
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # warm (plans, attributes) outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, n, torch):
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(st)
+        for _ in range(n):
+            g.replay()
+        e1.record(st)
+        e1.synchronize()
+    return e0.elapsed_time(e1) / n  # ms
+
+
+# ------------------------------------------------------------------ CPU oracle
+class OracleLayer:
+    """One layer of `wl` for the float64 CPU oracle: weights generated and
+    quantised once (outside any timed region); run() is one oracle pass."""
+
+    def __init__(self, wl):
+        import oracle
+        import synth
+        self.oracle, self.wl = oracle, wl
+        d, f, M, g = wl.d, wl.f, wl.M, wl.group
+        sd = lambda t: synth.seed_for(wl.wid, 0, t)
+        gen = lambda N, K, t: synth.host_f32(N * K, sd(t), wl.weight_dist).reshape(N, K)
+        self.Wg = oracle.Weight.from_f32(gen(f, d, synth.T_WG), wl.bits, g)
+        self.Wu = oracle.Weight.from_f32(gen(f, d, synth.T_WU), wl.bits, g)
+        self.Wd = oracle.Weight.from_f32(gen(d, f, synth.T_WD), wl.bits, g)
+        self.v = synth.host_bf16(M * d, sd(synth.T_VALUES), synth.ACT).reshape(M, d)
+        self.r = synth.host_bf16(M * d, sd(synth.T_RESIDUAL), synth.ACT).reshape(M, d)
+        self.w = synth.host_bf16(d, sd(synth.T_NORM_W), synth.NORM_W)
+
+    def run(self):
+        return self.oracle.mlp_layer(self.v, self.r, self.w, self.wl.eps, self.Wg, self.Wu, self.Wd)
+
+
+def oracle_layer_timing(wl, budget_s: float = 12.0, max_reps: int = 64):
+    """Times the CPU oracle on one layer of `wl` for about `budget_s` seconds.
+    Returns (us_per_layer, reps)."""
+    lay = OracleLayer(wl)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        lay.run()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= max_reps:
+            break
+    return el / reps * 1e6, reps
+
+
+def workload_config(wl, n_gpus):
+    return {"workload": wl.name, "d": wl.d, "f": wl.f, "rows_M": wl.M, "layers": wl.layers,
+            "weights": {0: "bf16", 1: "affine8", 2: "affine4"}[wl.fmt], "group": wl.group,
+            "eps": wl.eps, "bytes_per_layer": wl.layer_bytes(),
+            "l2": "inputs larger than L2: each step streams all layers' weights once "
+                  f"({wl.layer_bytes() * wl.layers / 1e9:.2f} GB per step vs 129 MB L2)",
+            "graph": "one CUDA graph per step, PDL between kernels",
+            "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, ws: int, torch, device=None):
+    """Max over ranks (gloo on CPU or nccl on GPU)."""
+    if ws == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args):
+    """The reference arm: the float64 CPU oracle, one layer of the Qwen3-8B
+    stack per step (a bounded sample of the workload), on the host cores."""
+    import synth
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = synth.QWEN8B
+    lay = OracleLayer(wl)
+    for _ in range(max(0, args.warmup)):
+        lay.run()
+    times = []
+    for _ in range(max(1, args.steps)):
+        t0 = time.perf_counter()
+        lay.run()
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    us = total / len(times) * 1e6
+    gbs = wl.layer_bytes() / (us * 1e-6) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+            "us_per_layer": round(us, 1), "n_gpus": args.gpus, "steps": len(times),
+            "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, 1),
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"one {wl.d}x{wl.f} affine8 g128 layer per step "
+                                       "(a bounded sample of the 36-layer stack), single-threaded "
+                                       "binary64 C oracle"},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="mt", choices=["mt", "reference"])
+    ap.add_argument("--workload", default="qwen3-8b",
+                    choices=["qwen3-8b", "tiny", "llama1b", "qwen15", "sweep"])
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--gateup-only", action="store_true",
+                    help="profiling aid: run only the gate/up kernels of the stack")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import synth
+    import quantized_gemv_epilogues_gb300 as mt
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if args.no_pdl:
+        mt.mt_set_option(mt.MT_OPT_PDL, 0)
+
+    wl = {"qwen3-8b": synth.QWEN8B, "tiny": synth.TINY, "llama1b": synth.LLAMA1B,
+          "qwen15": synth.QWEN15, "sweep": synth.sweep_point(64, 1)}[args.workload]
+    if args.layers:
+        wl = wl.with_(layers=args.layers)
+    stack = Stack(wl, dev)
+
+    if args.gateup_only:
+        for _ in range(max(3, args.warmup)):
+            stack.gateup_only()
+        for _ in range(args.steps):
+            stack.gateup_only()
+        torch.cuda.synchronize()
+        return 0
+
+    g_step = capture(stack.step, torch)
+    for _ in range(max(3, args.warmup)):
+        g_step.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms = time_graph(g_step, args.steps, torch)
+    torch.cuda.synchronize()
+    ms = reduce_max(ms, ws, torch, dev)
+    step_bytes = wl.layer_bytes() * wl.layers
+    value = ws * step_bytes / (ms * 1e-3) / 1e9
+    us_layer = ms * 1e3 / wl.layers
+
+    # ---- dominant kernel alone (gate/up + SwiGLU over the 36 layers' weights)
+    g_gu = capture(stack.gateup_only, torch)
+    for _ in range(3):
+        g_gu.replay()
+    ms_gu = time_graph(g_gu, max(5, args.steps // 2), torch)
+    gu_launch_s = ms_gu * 1e-3 / wl.layers
+    gu_bytes = stack.gateup_bytes()
+    peak, peak_kind = measured_peaks()
+    achieved = gu_bytes / gu_launch_s / 1e9
+
+    # ---- end to end: pinned host inputs -> device, graph, result -> host
+    h_vals = [torch.empty_like(L["values"], device="cpu").pin_memory() for L in stack.layers]
+    for hv, L in zip(h_vals, stack.layers):
+        hv.copy_(L["values"])
+    h_r0 = stack.r0.cpu().pin_memory()
+    h_out = torch.empty_like(stack.resid, device="cpu").pin_memory()
+
+    def e2e_step():
+        for hv, L in zip(h_vals, stack.layers):
+            L["values"].copy_(hv, non_blocking=True)
+        stack.r0.copy_(h_r0, non_blocking=True)
+        g_step.replay()
+        h_out.copy_(stack.resid, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = reduce_max((time.perf_counter() - t0) / args.steps, ws, torch, dev)
+    h2d = sum(hv.numel() * 2 for hv in h_vals) + h_r0.numel() * 2
+    d2h = h_out.numel() * 2
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s",
+            "us_per_layer": round(us_layer, 3), "frac_of_8TBs": round(value / ws / 8000.0, 4),
+            "frac_of_measured_hbm": round(value / ws / peak, 4),
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": {0: "bf16", 1: "u8", 2: "u4"}[wl.fmt] + "-weights/f32-acc",
+            "data": "synthetic", "config": workload_config(wl, ws),
+            "gpu_launches": 3 * wl.layers * args.steps,
+            "roofline": {"bound": "hbm", "kernel": "gemv_kernel gate/up+SwiGLU (affine8 M=1)",
+                         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                         "bytes_per_launch": gu_bytes, "us_per_launch": round(gu_launch_s * 1e6, 3),
+                         "traffic": profiled_traffic()},
+            "e2e": {"value": round(ws * step_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
+                    "us_per_layer": round(e2e_s * 1e6 / wl.layers, 3),
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "clocks": clk.summary()}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and wl.name == synth.QWEN8B.name:
+        us_cpu, reps = oracle_layer_timing(wl)
+        line["cpu_baseline"] = {"value": round(wl.layer_bytes() / (us_cpu * 1e-6) / 1e9, 4),
+                                "unit": "GB/s", "us_per_layer": round(us_cpu, 1), "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"{reps} passes of one layer ({wl.d}x{wl.f}, affine8 g128) "
+                                          "of the same workload, binary64 C oracle, one thread"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

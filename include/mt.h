@@ -1,0 +1,195 @@
+/*
+ * mt.h - C ABI of the GB300 (sm_103a) one-row decode-MLP library.
+ *
+ * One decode MLP layer is three stream-ordered calls:
+ *
+ *   mt_add_rmsnorm    summed = values + residual, normalized = rms_norm(summed,
+ *                     weight, eps); both are outputs (one multi-output kernel).
+ *                     meTile docs, "Compute-Graph Fusion", opening example.
+ *   mt_swiglu_gateup  g = x @ Wg^T, u = x @ Wu^T over group-wise affine weights
+ *                     (or dense bf16), h = silu(g) * u applied on-chip before
+ *                     the only store.  meTile docs, "Compute-Graph Fusion",
+ *                     Automatic Gated Epilogues; "MLX-LM Backend", Dispatch
+ *                     Policy (affine INT8/4-bit groups 32/64/128, dense BF16
+ *                     paired gate/up QMV).
+ *   mt_down_residual  y = h @ Wd^T + residual with the residual added in the
+ *                     GEMV's epilogue.  meTile docs, "Compute-Graph Fusion",
+ *                     Automatic Gated Epilogues ("a second composable
+ *                     epilogue adds the transformer residual to the down
+ *                     projection"); "MLX-LM Backend", Dispatch Policy
+ *                     ("values @ weight.T + residual").
+ *
+ * plus the offline packer mt_pack_affine (affine group quantisation of fp32
+ * weights into the stored layout).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Layouts.  Activations are row-major [M][.] bf16 (M = rows, 1..8).  A
+ *   weight is stored output-major [N][K] with K contiguous ("x[.., K] @ W[N, K]
+ *   stored transposed", ANEForge docs, "The optimizer and the cost model", The
+ *   roofline).  Gate/up: N = f, K = d.  Down: N = d, K = f.
+ *   MT_W_BF16    : W is bf16 [N][K].
+ *   MT_W_AFFINE8 : W is uint8 [N][K], one code q per byte.
+ *   MT_W_AFFINE4 : W is uint8 [N][K/2], byte j of a row holds code 2j in bits
+ *                  0..3 and code 2j+1 in bits 4..7.
+ *   Affine weights are w[n][k] = scale[n][k/group] * q[n][k] + bias[n][k/group]
+ *   with bf16 scales and biases [N][K/group], row-major.  For
+ *   mt_swiglu_gateup one scales array and one biases array hold two planes
+ *   [2][f][d/group]: plane 0 belongs to Wg, plane 1 to Wu.
+ * - Pointers.  Every tensor pointer is a DEVICE pointer (cudaMalloc, or memory
+ *   the device can address), 16-byte aligned.  The caller owns every buffer;
+ *   the hot calls allocate nothing and never synchronise.
+ * - Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *   default stream).  All work is enqueued on it in call order.
+ * - Errors.  Arguments are validated before anything is launched; on an
+ *   invalid argument nothing is launched and the matching MT_ERR_* is
+ *   returned.  A failed launch returns MT_ERR_CUDA (mt_last_cuda_error()
+ *   gives the cudaError_t).  Faults during execution surface at the caller's
+ *   next synchronisation, as for any CUDA kernel.
+ * - Aliasing.  Outputs must not overlap inputs, except: out_sum may equal
+ *   residual in mt_add_rmsnorm, and out_y may equal residual in
+ *   mt_down_residual (each element is read and then written by the same
+ *   thread).  Other overlaps return MT_ERR_ALIAS.
+ * - Programmatic dependent launch.  By default the three hot calls are
+ *   launched so that each kernel may start while the previous kernel on the
+ *   stream finishes; before waiting for that kernel a call reads only its
+ *   weights, scales, biases and RMSNorm weight.  Those must therefore not be
+ *   written by work still running on the stream (upload or pack them, then
+ *   synchronise or record an event, before the first call that reads them).
+ *   mt_set_option(MT_OPT_PDL, 0) turns this off.
+ */
+#ifndef MT_H
+#define MT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mt_status {
+  MT_OK = 0,
+  MT_ERR_NULL = 1,    /* a required pointer is NULL */
+  MT_ERR_SHAPE = 2,   /* a size is out of range or not divisible as required */
+  MT_ERR_GROUP = 3,   /* group not in {32, 64, 128} for affine, not 0 for bf16 */
+  MT_ERR_ALIGN = 4,   /* a pointer is not 16-byte aligned */
+  MT_ERR_FORMAT = 5,  /* unknown weight format, dtype, bit width or option */
+  MT_ERR_ALIAS = 6,   /* an output overlaps an input it may not overlap */
+  MT_ERR_CUDA = 7,    /* a CUDA runtime call failed (see mt_last_cuda_error) */
+  MT_ERR_TIMEOUT = 8  /* reserved: a bounded device-side wait expired */
+} mt_status;
+
+/* Output element type of a call.  Inputs are always bf16. */
+typedef enum mt_dtype { MT_BF16 = 0, MT_F32 = 1 } mt_dtype;
+
+/* Weight storage format. */
+typedef enum mt_wfmt { MT_W_BF16 = 0, MT_W_AFFINE8 = 1, MT_W_AFFINE4 = 2 } mt_wfmt;
+
+/* Library options (mt_set_option / mt_get_option). */
+typedef enum mt_option {
+  MT_OPT_PDL = 0 /* 1 (default): launch with programmatic stream serialization */
+} mt_option;
+
+/*
+ * Residual add + RMSNorm as one multi-output kernel.
+ *   values, residual : bf16 [M][d]
+ *   weight           : bf16 [d] (RMSNorm gain)
+ *   out_sum          : bf16 [M][d], out_sum = bf16(values + residual)
+ *   out_norm         : [M][d] of norm_dtype,
+ *                      out_norm = out_sum * weight / sqrt(mean(out_sum^2) + eps)
+ *                      computed from the rounded out_sum with fp32 accumulation.
+ * Limits: 1 <= M <= 8, 8 <= d <= 65536, d % 8 == 0, eps >= 0.
+ * meTile docs, "Compute-Graph Fusion" (opening example: the residual value
+ * remains a graph output); "MLX-LM Backend", Dispatch Policy (RMSNorm with FP32
+ * accumulation, residual-add followed by RMSNorm kept as two outputs).
+ */
+mt_status mt_add_rmsnorm(const void* values, const void* residual, const void* weight,
+                         float eps, void* out_sum, void* out_norm, int M, int d,
+                         mt_dtype norm_dtype, void* stream);
+
+/*
+ * Gate/up GEMV with the SwiGLU epilogue.
+ *   x        : bf16 [M][d]
+ *   Wg, Wu   : [f][d] in format fmt (see Layouts)
+ *   scales   : bf16 [2][f][d/group]  (NULL for MT_W_BF16)
+ *   biases   : bf16 [2][f][d/group]  (NULL for MT_W_BF16)
+ *   group    : 32, 64 or 128 for affine formats, 0 for MT_W_BF16
+ *   out_h    : [M][f] of out_dtype, h = silu(g) * u, silu(g) = g / (1 + e^-g),
+ *              g = x . Wg[n], u = x . Wu[n], fp32 accumulation, one rounding.
+ * Limits: 1 <= M <= 8; d % group == 0 (affine), d % 8 == 0 (bf16);
+ *         1 <= f; d <= 32768.
+ * meTile docs, "Compute-Graph Fusion", Automatic Gated Epilogues (two matmuls
+ * sharing the activation, silu(gate) * up applied on-chip); "MLX-LM Backend",
+ * Dispatch Policy (gate and up dot products share each activation load and
+ * apply the SwiGLU epilogue before the only output write).
+ */
+mt_status mt_swiglu_gateup(const void* x, const void* Wg, const void* Wu,
+                           const void* scales, const void* biases, int group,
+                           void* out_h, int M, int d, int f,
+                           mt_wfmt fmt, mt_dtype out_dtype, void* stream);
+
+/*
+ * Down GEMV with the residual epilogue.
+ *   h        : bf16 [M][f]
+ *   Wd       : [d][f] in format fmt
+ *   scales   : bf16 [d][f/group] (NULL for MT_W_BF16)
+ *   biases   : bf16 [d][f/group] (NULL for MT_W_BF16)
+ *   residual : bf16 [M][d]
+ *   out_y    : [M][d] of out_dtype, y = h . Wd[n] + residual[n], fp32
+ *              accumulation, one rounding.  out_y may equal residual.
+ * Limits: 1 <= M <= 8; f % group == 0 (affine), f % 8 == 0 (bf16);
+ *         1 <= d; f <= 32768.
+ * meTile docs, "Compute-Graph Fusion", Automatic Gated Epilogues (residual
+ * added to the down projection in the same kernel); "MLX-LM Backend",
+ * Dispatch Policy (typed store adds the transformer residual without
+ * materialising the unfused projection).
+ */
+mt_status mt_down_residual(const void* h, const void* Wd, const void* scales,
+                           const void* biases, int group, const void* residual,
+                           void* out_y, int M, int f, int d,
+                           mt_wfmt fmt, mt_dtype out_dtype, void* stream);
+
+/*
+ * Affine group quantiser and packer (offline preparation; stream-ordered).
+ *   W        : fp32 [N][K], device
+ *   bits     : 8 or 4;  group : 32, 64 or 128;  K % group == 0
+ *   q        : uint8 [N][K] (bits 8) or [N][K/2] (bits 4), device
+ *   scales   : bf16 [N][K/group], biases : bf16 [N][K/group], device
+ * Per group of `group` consecutive elements along K, in binary64:
+ *   bias  = bf16(min),  scale = bf16((max - min) / (2^bits - 1)),
+ *   q     = clamp(round_half_even((w - bias) / scale), 0, 2^bits - 1),
+ *   and q = 0 when scale == 0.  bf16() rounds to nearest even.
+ * meTile docs, "MLX-LM Backend": affine INT8 and 4-bit "affine nibbles,
+ * scales, and biases" with group sizes 32, 64 and 128 prepared ahead of time.
+ * The formula itself is not printed there; this is the min/max reading.
+ */
+mt_status mt_pack_affine(const float* W, int N, int K, int group, int bits,
+                         void* q, void* scales, void* biases, void* stream);
+
+/*
+ * Dequantise packed affine weights to fp32 [N][K] (w = scale * q + bias,
+ * rounded once to fp32).  Stream-ordered, device pointers.  For layout checks.
+ */
+mt_status mt_unpack_affine(const void* q, const void* scales, const void* biases,
+                           int N, int K, int group, int bits, float* W, void* stream);
+
+/* Library options.  Returns MT_ERR_FORMAT for an unknown option. */
+mt_status mt_set_option(mt_option opt, int value);
+int mt_get_option(mt_option opt);
+
+/* Static description of a status code (never NULL). */
+const char* mt_status_string(mt_status s);
+
+/* cudaError_t of the last failed CUDA call made by the library in this
+ * thread (0 if none). */
+int mt_last_cuda_error(void);
+
+/* Library ABI version: (major << 16) | minor. */
+int mt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MT_H */

@@ -1,0 +1,12 @@
+// k_gemv_a4.cu - instantiations of the GEMV kernels for one weight format
+// (compiled as a separate translation unit to build in parallel).
+#include "k_gemv_run.cuh"
+
+namespace mt {
+
+mt_status launch_gemv_a4(const GemvProblem& p, const Launch& l) {
+  if (p.kind == Kind::GateUp) return dispatch_rows<FMT_A4, 0>(p, l);
+  return dispatch_rows<FMT_A4, 1>(p, l);
+}
+
+}  // namespace mt

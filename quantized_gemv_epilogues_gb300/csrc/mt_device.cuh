@@ -1,0 +1,81 @@
+// mt_device.cuh - device helpers shared by the library's kernels (sm_103a).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mt {
+
+// ---------------------------------------------------------------- PTX wrappers
+
+// Programmatic dependent launch: wait for the preceding kernel on the stream
+// (and the visibility of its writes); no-op when launched without the
+// programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allow the next kernel on the stream to begin launching its CTAs.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 128-bit streaming load of read-only data that is used once: no L1
+// allocation, L2 prefetch hint of 256 B.
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint4 ldg_nc(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint16_t ldg_u16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// Ampere-style asynchronous 16-byte global -> shared copy (LDGSTS).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// ------------------------------------------------------------ conversions
+
+// bf16 bit pattern (low or high half of a 32-bit word) -> fp32, exact.
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+// fp32 -> bf16 round-to-nearest-even (the CUDA intrinsic).
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
+}
+
+// Exponent-bias ("magic number") integer -> float conversion: placing an
+// 8-bit integer q in the low mantissa bits of 2^23 (bit pattern 0x4B0000qq)
+// gives the float 2^23 + q exactly, because the spacing of floats in
+// [2^23, 2^24) is 1; subtracting 2^23 leaves q exactly.  This is the
+// conversion used for fast INT8/INT4 dequantisation by Kim et al., "Who Says
+// Elephants Can't Run: Bringing Large Scale MoE Models into Cloud Scale
+// Production" (2022), there with the fp16 bias 0x6400.  `sel` picks byte
+// 0..3 of w.  Tested against cvt.rn.f32.u32 in the test suite.
+__device__ __forceinline__ float u8_to_f32(uint32_t w, int sel) {
+  const uint32_t m = __byte_perm(w, 0x4B000000u, 0x7540u | (uint32_t)sel);
+  return __uint_as_float(m) - 8388608.0f;
+}
+
+}  // namespace mt

@@ -1,0 +1,168 @@
+"""Host-side checks of the C-ABI library: it builds, loads, exports every
+function include/mt.h declares, and rejects invalid arguments with the
+documented status before touching the GPU (no device is needed: validation
+happens before any CUDA call)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_gemv_epilogues_gb300 import _build
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(HEADER_DIR)):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(mt_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_hot_path_calls():
+    names = declared_functions()
+    for n in ("mt_add_rmsnorm", "mt_swiglu_gateup", "mt_down_residual", "mt_pack_affine"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (mt_[a-z0-9_]+)", out))
+    assert set(declared_functions()) <= exported
+
+
+def test_header_compiles_as_c():
+    src = '#include "mt.h"\nint main(void){ return (int)MT_OK; }\n'
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", HEADER_DIR, "-x", "c", "-",
+                        "-o", os.devnull], input=src, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+# fake, 16-byte aligned, non-overlapping "device" addresses: never dereferenced,
+# because every case below fails validation first
+A = [0x10000000 * (i + 1) for i in range(12)]
+P = ctypes.c_void_p
+
+
+def _rms(lib, *a):
+    f = lib.mt_add_rmsnorm
+    f.restype = ctypes.c_int
+    f.argtypes = [P, P, P, ctypes.c_float, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
+    return f(*a)
+
+
+def _gu(lib, *a):
+    f = lib.mt_swiglu_gateup
+    f.restype = ctypes.c_int
+    f.argtypes = [P, P, P, P, P, ctypes.c_int, P] + [ctypes.c_int] * 5 + [P]
+    return f(*a)
+
+
+def _dn(lib, *a):
+    f = lib.mt_down_residual
+    f.restype = ctypes.c_int
+    f.argtypes = [P, P, P, P, ctypes.c_int, P, P] + [ctypes.c_int] * 5 + [P]
+    return f(*a)
+
+
+def _pk(lib, *a):
+    f = lib.mt_pack_affine
+    f.restype = ctypes.c_int
+    f.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P]
+    return f(*a)
+
+
+NULL, SHAPE, GROUP, ALIGN, FORMAT, ALIAS = 1, 2, 3, 4, 5, 6
+
+
+def test_add_rmsnorm_validation(lib):
+    v, r, w, s, n = A[:5]
+    assert _rms(lib, None, r, w, 1e-5, s, n, 1, 256, 0, None) == NULL
+    assert _rms(lib, v, r, w, 1e-5, s, n, 0, 256, 0, None) == SHAPE
+    assert _rms(lib, v, r, w, 1e-5, s, n, 9, 256, 0, None) == SHAPE
+    assert _rms(lib, v, r, w, 1e-5, s, n, 1, 260, 0, None) == SHAPE
+    assert _rms(lib, v, r, w, -1.0, s, n, 1, 256, 0, None) == SHAPE
+    assert _rms(lib, v, r, w, float("nan"), s, n, 1, 256, 0, None) == SHAPE
+    assert _rms(lib, v, r, w, 1e-5, s, n, 1, 256, 7, None) == FORMAT
+    assert _rms(lib, v + 2, r, w, 1e-5, s, n, 1, 256, 0, None) == ALIGN
+    assert _rms(lib, v, r, w, 1e-5, v, n, 1, 256, 0, None) == ALIAS     # out_sum == values
+    assert _rms(lib, v, r, w, 1e-5, s, r, 1, 256, 0, None) == ALIAS     # out_norm == residual
+    assert _rms(lib, v, r, w, 1e-5, s, s + 16, 1, 256, 0, None) == ALIAS  # outputs overlap
+
+
+def test_swiglu_gateup_validation(lib):
+    x, wg, wu, sc, bi, h = A[:6]
+    ok = dict(M=1, d=256, f=768, fmt=1, od=0)
+
+    def call(x=x, wg=wg, wu=wu, sc=sc, bi=bi, g=64, h=h, M=1, d=256, f=768, fmt=1, od=0):
+        return _gu(lib, x, wg, wu, sc, bi, g, h, M, d, f, fmt, od, None)
+
+    assert call(x=None) == NULL
+    assert call(sc=None) == NULL
+    assert call(g=48) == GROUP
+    assert call(fmt=0, g=64, sc=None, bi=None) == GROUP      # bf16 takes group 0
+    assert call(d=200) == SHAPE                              # 200 % 64 != 0
+    assert call(M=0) == SHAPE
+    assert call(M=9) == SHAPE
+    assert call(f=0) == SHAPE
+    assert call(fmt=3) == FORMAT
+    assert call(od=2) == FORMAT
+    assert call(wu=wu + 8) == ALIGN
+    assert call(h=x) == ALIAS
+    assert call(h=sc) == ALIAS
+    assert call(fmt=0, g=0, sc=None, bi=None, d=260) == SHAPE  # bf16 needs d % 8 == 0
+
+
+def test_down_residual_validation(lib):
+    h, wd, sc, bi, res, y = A[:6]
+
+    def call(h=h, wd=wd, sc=sc, bi=bi, g=128, res=res, y=y, M=1, f=12288, d=4096, fmt=1, od=0):
+        return _dn(lib, h, wd, sc, bi, g, res, y, M, f, d, fmt, od, None)
+
+    assert call(res=None) == NULL
+    assert call(g=16) == GROUP
+    assert call(f=1000) == SHAPE
+    assert call(f=40000) == SHAPE
+    assert call(fmt=-1) == FORMAT
+    assert call(y=y + 4) == ALIGN
+    assert call(y=h) == ALIAS
+    assert call(y=res + 16) == ALIAS          # partial overlap with the residual
+    assert call(y=res, od=1) == ALIAS         # in place only with the same element size
+
+
+def test_pack_validation(lib):
+    W, q, s, b = A[:4]
+    assert _pk(lib, None, 4, 256, 64, 8, q, s, b, None) == NULL
+    assert _pk(lib, W, 4, 256, 64, 5, q, s, b, None) == FORMAT
+    assert _pk(lib, W, 4, 256, 100, 8, q, s, b, None) == GROUP
+    assert _pk(lib, W, 4, 250, 64, 8, q, s, b, None) == SHAPE
+    assert _pk(lib, W, 4, 256, 64, 8, q, q, b, None) == ALIAS
+    assert _pk(lib, W + 4, 4, 256, 64, 8, q, s, b, None) == ALIGN
+
+
+def test_status_strings_and_options(lib):
+    f = lib.mt_status_string
+    f.restype = ctypes.c_char_p
+    for s in range(9):
+        assert f(s)
+    assert f(99) == b"unknown mt_status"
+    lib.mt_set_option.restype = ctypes.c_int
+    lib.mt_get_option.restype = ctypes.c_int
+    assert lib.mt_set_option(0, 0) == 0 and lib.mt_get_option(0) == 0
+    assert lib.mt_set_option(0, 1) == 0 and lib.mt_get_option(0) == 1
+    assert lib.mt_set_option(5, 1) == FORMAT
+    assert lib.mt_version() >> 16 == 1

@@ -15,8 +15,8 @@ HEADER_DIR = os.path.join(ROOT, "include")
 
 @pytest.fixture(scope="module")
 def lib():
-    from quantized_gemv_epilogues_gb300 import _build
-    path = _build.build()
+    import __graft_entry__
+    path = __graft_entry__._libbuild().build()
     return ctypes.CDLL(path)
 
 

@@ -208,6 +208,23 @@ class Stack:
             mt.mt_swiglu_gateup(self.norm, L["Wg"], L["Wu"], L["sgu"], L["bgu"], wl.group, self.h,
                                 fmt=wl.fmt)
 
+    def down_only(self):
+        mt, wl = self.mt, self.wl
+        for L in self.layers:
+            mt.mt_down_residual(self.h, L["Wd"], L["sd"], L["bd"], wl.group, self.resid, self.resid,
+                                fmt=wl.fmt)
+
+    def rmsnorm_only(self):
+        mt, wl = self.mt, self.wl
+        for L in self.layers:
+            mt.mt_add_rmsnorm(L["values"], self.resid, L["w"], wl.eps, self.resid, self.norm)
+
+    def down_bytes(self):
+        wl = self.wl
+        n = wl.f * wl.d
+        w = n * wl.bits // 8 + (0 if wl.fmt == 0 else 4 * n // wl.group)
+        return w + 2 * wl.M * wl.f + 4 * wl.M * wl.d
+
     def gateup_bytes(self):
         wl = self.wl
         n = 2 * wl.f * wl.d
@@ -343,7 +360,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mt", choices=["mt", "reference"])
     ap.add_argument("--workload", default="qwen3-8b",
@@ -401,12 +418,16 @@ def main():
     value = ws * step_bytes / (ms * 1e-3) / 1e9
     us_layer = ms * 1e3 / wl.layers
 
-    # ---- dominant kernel alone (gate/up + SwiGLU over the 36 layers' weights)
-    g_gu = capture(stack.gateup_only, torch)
-    for _ in range(3):
-        g_gu.replay()
-    ms_gu = time_graph(g_gu, max(5, args.steps // 2), torch)
-    gu_launch_s = ms_gu * 1e-3 / wl.layers
+    # ---- each kernel alone, over the 36 layers' weights (one graph per kind)
+    per_kernel = {}
+    for name, fn in (("gateup", stack.gateup_only), ("down", stack.down_only),
+                     ("add_rmsnorm", stack.rmsnorm_only)):
+        g_k = capture(fn, torch)
+        for _ in range(3):
+            g_k.replay()
+        per_kernel[name] = time_graph(g_k, max(5, args.steps // 4), torch) * 1e3 / wl.layers
+        del g_k
+    gu_launch_s = per_kernel["gateup"] * 1e-6
     gu_bytes = stack.gateup_bytes()
     peak, peak_kind = measured_peaks()
     achieved = gu_bytes / gu_launch_s / 1e9
@@ -451,6 +472,8 @@ def main():
                          "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                          "bytes_per_launch": gu_bytes, "us_per_launch": round(gu_launch_s * 1e6, 3),
                          "traffic": profiled_traffic()},
+            "kernels_us_per_layer": {k: round(v, 3) for k, v in per_kernel.items()},
+            "down_gbs_alone": round(stack.down_bytes() / (per_kernel["down"] * 1e-6) / 1e9, 1),
             "e2e": {"value": round(ws * step_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
                     "us_per_layer": round(e2e_s * 1e6 / wl.layers, 3),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -368,6 +368,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--gemv", default="tma", choices=["tma", "regs"],
+                    help="one-row GEMV kernel: TMA bulk-copy pipeline or register pipeline")
     ap.add_argument("--gateup-only", action="store_true",
                     help="profiling aid: run only the gate/up kernels of the stack")
     args = ap.parse_args()
@@ -386,6 +388,7 @@ def main():
     dev = torch.device("cuda", local)
     if args.no_pdl:
         mt.mt_set_option(mt.MT_OPT_PDL, 0)
+    mt.mt_set_option(mt.MT_OPT_GEMV, 0 if args.gemv == "tma" else 1)
 
     wl = {"qwen3-8b": synth.QWEN8B, "tiny": synth.TINY, "llama1b": synth.LLAMA1B,
           "qwen15": synth.QWEN15, "sweep": synth.sweep_point(64, 1)}[args.workload]
@@ -467,7 +470,10 @@ def main():
             "vs_baseline": None, "dtype": {0: "bf16", 1: "u8", 2: "u4"}[wl.fmt] + "-weights/f32-acc",
             "data": "synthetic", "config": workload_config(wl, ws),
             "gpu_launches": 3 * wl.layers * args.steps,
-            "roofline": {"bound": "hbm", "kernel": "gemv_kernel gate/up+SwiGLU (affine8 M=1)",
+            "device_error": mt.mt_device_error(),
+            "roofline": {"bound": "hbm",
+                         "kernel": ("gemv_tma_kernel" if args.gemv == "tma" else "gemv_kernel")
+                                   + " gate/up+SwiGLU (affine8, one row)",
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                          "bytes_per_launch": gu_bytes, "us_per_launch": round(gu_launch_s * 1e6, 3),

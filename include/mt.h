@@ -88,7 +88,9 @@ typedef enum mt_wfmt { MT_W_BF16 = 0, MT_W_AFFINE8 = 1, MT_W_AFFINE4 = 2 } mt_wf
 
 /* Library options (mt_set_option / mt_get_option). */
 typedef enum mt_option {
-  MT_OPT_PDL = 0 /* 1 (default): launch with programmatic stream serialization */
+  MT_OPT_PDL = 0, /* 1 (default): launch with programmatic stream serialization */
+  MT_OPT_GEMV = 1 /* one-row GEMV kernel: 0 (default) TMA bulk-copy pipeline,
+                     1 register-pipelined kernel (the one used for M > 1) */
 } mt_option;
 
 /*
@@ -177,6 +179,11 @@ mt_status mt_unpack_affine(const void* q, const void* scales, const void* biases
 /* Library options.  Returns MT_ERR_FORMAT for an unknown option. */
 mt_status mt_set_option(mt_option opt, int value);
 int mt_get_option(mt_option opt);
+
+/* Device error word: MT_ERR_TIMEOUT if a kernel's bounded wait expired since
+ * the word was last cleared, 0 otherwise, -1 if it cannot be read.  Reading it
+ * synchronises with the device (cudaMemcpyFromSymbol); clear != 0 resets it. */
+int mt_device_error(int clear);
 
 /* Static description of a status code (never NULL). */
 const char* mt_status_string(mt_status s);

@@ -36,7 +36,7 @@ MT_OK, MT_ERR_NULL, MT_ERR_SHAPE, MT_ERR_GROUP, MT_ERR_ALIGN = 0, 1, 2, 3, 4
 MT_ERR_FORMAT, MT_ERR_ALIAS, MT_ERR_CUDA, MT_ERR_TIMEOUT = 5, 6, 7, 8
 MT_BF16, MT_F32 = 0, 1
 MT_W_BF16, MT_W_AFFINE8, MT_W_AFFINE4 = 0, 1, 2
-MT_OPT_PDL = 0
+MT_OPT_PDL, MT_OPT_GEMV = 0, 1
 
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _SIGS = {
@@ -49,6 +49,7 @@ _SIGS = {
     "mt_get_option": (_I, [_I]),
     "mt_status_string": (ctypes.c_char_p, [_I]),
     "mt_last_cuda_error": (_I, []),
+    "mt_device_error": (_I, [_I]),
     "mt_version": (_I, []),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -166,6 +167,10 @@ def mt_status_string(status: int) -> str:
 
 def mt_last_cuda_error() -> int:
     return _lib.mt_last_cuda_error()
+
+
+def mt_device_error(clear: bool = False) -> int:
+    return _lib.mt_device_error(1 if clear else 0)
 
 
 def mt_version() -> int:

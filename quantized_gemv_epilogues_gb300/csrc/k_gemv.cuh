@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs a) {
   constexpr int V = R * NW * MR;           // partial sums per thread per tile
   constexpr bool FACTOR = AFF && MR == 1;  // s * sum(q x) + b * sum(x) per chunk
 
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                       // [MR][K] bf16
   float* sxs = reinterpret_cast<float*>(smem + (size_t)MR * a.K * 2);     // [CPR] (FACTOR)
   uint32_t* sbs = reinterpret_cast<uint32_t*>(

@@ -99,7 +99,7 @@ mt_status run_gemv(const GemvProblem& p, const Launch& l) {
   int rows_per = (N + grid - 1) / grid;
   const size_t budget = (size_t)di->max_smem_optin;
   if (base_smem + sb_row_bytes * (size_t)((rows_per + R - 1) / R * R) > budget) {
-    if (base_smem + sb_row_bytes * R > budget) return MT_ERR_SHAPE;
+    if (sb_row_bytes == 0 || base_smem + sb_row_bytes * R > budget) return MT_ERR_SHAPE;
     const int cap = (int)((budget - base_smem) / sb_row_bytes) / R * R;
     grid = (N + cap - 1) / cap;
     rows_per = (N + grid - 1) / grid;
@@ -113,9 +113,18 @@ mt_status run_gemv(const GemvProblem& p, const Launch& l) {
   return launch(kern, dim3(grid), dim3(block), smem, l, a);
 }
 
-// Chooses the row-count instantiation for one (format, kind).
+template <int FMT, int KIND, int R>
+mt_status run_gemv_tma(const GemvProblem& p, const Launch& l);
+
+// Chooses the kernel for one (format, kind): the TMA pipeline for one row
+// (unless MT_OPT_GEMV selects the register kernel or the shape does not fit
+// its shared memory), else the register-pipelined kernel by row count.
 template <int FMT, int KIND>
 mt_status dispatch_rows(const GemvProblem& p, const Launch& l) {
+  if (p.M == 1 && gemv_choice() == 0) {
+    const mt_status st = run_gemv_tma<FMT, KIND, KIND == 0 ? 1 : 2>(p, l);
+    if (st != MT_ERR_SHAPE) return st;
+  }
   if (p.M <= 1) return run_gemv<FMT, KIND, 1, 4>(p, l);
   if (p.M <= 2) return run_gemv<FMT, KIND, 2, 4>(p, l);
   if (p.M <= 4) return run_gemv<FMT, KIND, 4, 2>(p, l);

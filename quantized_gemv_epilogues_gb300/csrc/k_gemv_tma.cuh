@@ -1,0 +1,443 @@
+// k_gemv_tma.cuh - one-row (M == 1) GEMV with the SwiGLU or residual
+// epilogue, fed by a TMA bulk-copy pipeline.
+//
+// meTile docs, "Compute-Graph Fusion", Automatic Gated Epilogues (gate and up
+// share the activation, silu(gate) * up before the only store; the down
+// projection adds the residual in its epilogue); "MLX-LM Backend", Dispatch
+// Policy (affine w = scale * q + bias per group of 32/64/128 along K).
+//
+// GB300 design:
+//  * One persistent CTA per SM owns a contiguous range of output rows.
+//  * Warp specialisation: one producer lane streams the CTA's weight rows
+//    into a ring of shared-memory slots with cp.async.bulk (TMA, evict-first
+//    L2 policy), each slot signalled by a "full" mbarrier with a transaction
+//    count; eight consumer warps each take whole tasks (R rows x one piece of
+//    the row) and release the slot through an "empty" mbarrier.  The ring
+//    holds 100+ KB per SM in flight, independent of register pressure.
+//  * The first slots are requested before waiting on the preceding kernel
+//    (programmatic dependent launch): weights do not depend on it.
+//  * x is staged once as fp32 in shared memory with a bank swizzle, so each
+//    lane's 16-byte reads of its chunk are conflict-free; scales and biases
+//    are staged as fp32.  The affine term is factored as
+//      sum_k (s q_k + b) x_k = sum_chunks s * (sum q_k x_k) + sum_groups b * X_g
+//    with X_g the sum of x over group g, so the per-weight work is one byte
+//    permute (exponent-bias conversion) plus half a packed fp32x2 add and half
+//    a packed fp32x2 FMA.
+//  * Each task is reduced inside its warp (shuffles); a row split into P
+//    pieces is combined by whichever warp finishes its last piece (a
+//    shared-memory counter; no waiting).
+//  * Every mbarrier wait is bounded (~1 s); on expiry the kernel records
+//    MT_ERR_TIMEOUT in a device error word, stops, waits (bounded) for its
+//    own copies in flight and returns.
+#pragma once
+#include "k_gemv.cuh"
+
+namespace mt {
+
+constexpr int TMA_CWARPS = 8;  // consumer warps per CTA
+
+struct TmaArgs {
+  const uint16_t* x;
+  const uint8_t* W0;
+  const uint8_t* W1;
+  const uint16_t* s0;
+  const uint16_t* b0;
+  const uint16_t* s1;
+  const uint16_t* b1;
+  const uint16_t* res;
+  void* out;
+  int K, N;
+  int group, G;          // group size and groups per row (affine)
+  int row_bytes;         // bytes of one weight row
+  int rows_base, rows_extra;
+  int P;                 // pieces per row
+  int B;                 // bytes per piece (multiple of 16)
+  int CPP;               // 16-byte chunks per piece
+  int GPP;               // groups per piece (affine)
+  int S;                 // ring slots (multiple of TMA_CWARPS)
+  int slot_bytes;        // R * NW * B
+  int rows_alloc;        // rows of the staged scale/bias/part arrays
+  int out_f32;
+  int* err;              // device error word
+};
+
+// Position (in floats) of element e of x in the swizzled fp32 staging layout:
+// chunk c = e / EPC holds U = EPC/4 float4 units; unit k of chunk c is stored
+// at unit k ^ swz(c), which spreads the 8 lanes of a shared-memory wavefront
+// over all 32 banks when consecutive lanes read consecutive chunks.
+template <int EPC>
+__device__ __forceinline__ int x_swz_index(int e) {
+  constexpr int U = EPC / 4;
+  constexpr int SH = U == 2 ? 2 : (U == 4 ? 1 : 0);
+  const int c = e / EPC;
+  const int k = (e % EPC) >> 2;
+  const int ks = k ^ ((c >> SH) & (U - 1));
+  return (c * U + ks) * 4 + (e & 3);
+}
+
+template <int EPC>
+__device__ __forceinline__ float4 x_unit(const float* xs, int c, int k) {
+  constexpr int U = EPC / 4;
+  constexpr int SH = U == 2 ? 2 : (U == 4 ? 1 : 0);
+  const int ks = k ^ ((c >> SH) & (U - 1));
+  return *reinterpret_cast<const float4*>(xs + (c * U + ks) * 4);
+}
+
+// Dot product of one 16-byte weight chunk with its EPC activations, as a
+// pair of partial sums (packed fp32x2).
+template <int FMT>
+__device__ __forceinline__ float2 chunk_dot(const uint4 w, const float* xs, int c) {
+  using T = FmtTraits<FMT>;
+  constexpr int EPC = T::EPC;
+  const float2 neg = make_float2(-8388608.0f, -8388608.0f);
+  float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
+  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  if constexpr (FMT == FMT_A8) {
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      const float4 xv = x_unit<EPC>(xs, c, wi);
+      const uint32_t m0 = __byte_perm(ww[wi], 0x4B000000u, 0x7540u);
+      const uint32_t m1 = __byte_perm(ww[wi], 0x4B000000u, 0x7541u);
+      const uint32_t m2 = __byte_perm(ww[wi], 0x4B000000u, 0x7542u);
+      const uint32_t m3 = __byte_perm(ww[wi], 0x4B000000u, 0x7543u);
+      const float2 qa = __fadd2_rn(make_float2(__uint_as_float(m0), __uint_as_float(m1)), neg);
+      const float2 qb = __fadd2_rn(make_float2(__uint_as_float(m2), __uint_as_float(m3)), neg);
+      if (wi & 1) {
+        d1 = __ffma2_rn(qa, make_float2(xv.x, xv.y), d1);
+        d1 = __ffma2_rn(qb, make_float2(xv.z, xv.w), d1);
+      } else {
+        d0 = __ffma2_rn(qa, make_float2(xv.x, xv.y), d0);
+        d0 = __ffma2_rn(qb, make_float2(xv.z, xv.w), d0);
+      }
+    }
+  } else if constexpr (FMT == FMT_A4) {
+    // word wi holds elements 8wi..8wi+7: byte j = (2j low nibble, 2j+1 high)
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      const uint32_t lo = ww[wi] & 0x0F0F0F0Fu, hi = (ww[wi] >> 4) & 0x0F0F0F0Fu;
+      const float4 xa = x_unit<EPC>(xs, c, 2 * wi);      // elements 8wi .. 8wi+3
+      const float4 xb = x_unit<EPC>(xs, c, 2 * wi + 1);  // elements 8wi+4 .. 8wi+7
+      const float2 q01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7540u)),
+                                                __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7540u))), neg);
+      const float2 q23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7541u)),
+                                                __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7541u))), neg);
+      const float2 q45 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7542u)),
+                                                __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7542u))), neg);
+      const float2 q67 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7543u)),
+                                                __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7543u))), neg);
+      d0 = __ffma2_rn(q01, make_float2(xa.x, xa.y), d0);
+      d1 = __ffma2_rn(q23, make_float2(xa.z, xa.w), d1);
+      d0 = __ffma2_rn(q45, make_float2(xb.x, xb.y), d0);
+      d1 = __ffma2_rn(q67, make_float2(xb.z, xb.w), d1);
+    }
+  } else {
+    // dense bf16: word wi holds elements 2wi (low half) and 2wi+1 (high half)
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float4 xv = x_unit<EPC>(xs, c, u);
+      const float2 wa = make_float2(bf16lo(ww[2 * u]), bf16hi(ww[2 * u]));
+      const float2 wb = make_float2(bf16lo(ww[2 * u + 1]), bf16hi(ww[2 * u + 1]));
+      d0 = __ffma2_rn(wa, make_float2(xv.x, xv.y), d0);
+      d1 = __ffma2_rn(wb, make_float2(xv.z, xv.w), d1);
+    }
+  }
+  return __fadd2_rn(d0, d1);
+}
+
+template <int FMT, int KIND, int R>
+__global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(const TmaArgs a) {
+  using T = FmtTraits<FMT>;
+  constexpr int EPC = T::EPC;
+  constexpr bool AFF = T::AFFINE;
+  constexpr int NW = KIND == 0 ? 2 : 1;
+  constexpr int V = R * NW;
+  constexpr int NCT = TMA_CWARPS * 32;  // consumer threads
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int S = a.S;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);               // full[S], empty[S]
+  const size_t bar_bytes = ((size_t)16 * S + 127) / 128 * 128;
+  unsigned char* ring = smem + bar_bytes;
+  float* xs = reinterpret_cast<float*>(ring + (size_t)S * a.slot_bytes);  // [K] swizzled
+  float* gsum = xs + a.K;                                                // [G]
+  float* ssc = gsum + (AFF ? a.G : 0);                                   // [rows][NW][G]
+  float* sbi = ssc + (AFF ? (size_t)a.rows_alloc * NW * a.G : 0);        // [rows][NW][G]
+  float* parts = sbi + (AFF ? (size_t)a.rows_alloc * NW * a.G : 0);      // [rows][P][NW]
+  int* cnt = reinterpret_cast<int*>(parts + (a.P > 1 ? (size_t)a.rows_alloc * a.P * NW : 0));
+  __shared__ volatile int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cta = blockIdx.x;
+  const int r_begin = cta * a.rows_base + min(cta, a.rows_extra);
+  const int rows = a.rows_base + (cta < a.rows_extra ? 1 : 0);
+  const int groups = (rows + R - 1) / R;
+  const int T_tasks = groups * a.P;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
+
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+  pdl_trigger();
+
+  if (warp == TMA_CWARPS) {
+    // ------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      const uint32_t ring_s = smem_u32(ring);
+      int issued = 0;
+      for (int t = 0; t < T_tasks; ++t) {
+        const int s = t % S;
+        if (t >= S && !mbar_wait_bounded(empty0 + 8 * s, ((t / S) - 1) & 1)) {
+          abort_flag = 1;
+          atomicExch(a.err, (int)MT_ERR_TIMEOUT);
+          break;
+        }
+        if (abort_flag) break;
+        const int rg = t / a.P, p = t - rg * a.P;
+        const int nvalid = min(R, rows - rg * R);
+        mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)(nvalid * NW * a.B));
+        for (int i = 0; i < nvalid; ++i) {
+          const size_t src = (size_t)(r_begin + rg * R + i) * a.row_bytes + (size_t)p * a.B;
+#pragma unroll
+          for (int m = 0; m < NW; ++m)
+            bulk_g2s(ring_s + (uint32_t)(s * a.slot_bytes + (i * NW + m) * a.B),
+                     (m ? a.W1 : a.W0) + src, (uint32_t)a.B, full0 + 8 * s, pol);
+        }
+        issued = t + 1;
+      }
+      // never leave the CTA with copies in flight
+      for (int t = max(0, issued - S); t < issued; ++t)
+        (void)mbar_wait_bounded(full0 + 8 * (t % S), (t / S) & 1);
+    }
+    return;
+  }
+
+  // --------------------------------------------------------- consumers
+  const int ctid = tid;  // 0 .. NCT-1
+  if constexpr (AFF) {
+    // scales and biases of the CTA's rows as fp32 (static: before the wait)
+    const int n_sb = rows * NW * a.G;
+    for (int i = ctid; i < n_sb; i += NCT) {
+      const int rl = i / (NW * a.G);
+      const int rem = i - rl * NW * a.G;
+      const int m = rem / a.G, g = rem - m * a.G;
+      const size_t gi = (size_t)(r_begin + rl) * a.G + g;
+      ssc[i] = bf16f(ldg_u16((m ? a.s1 : a.s0) + gi));
+      sbi[i] = bf16f(ldg_u16((m ? a.b1 : a.b0) + gi));
+    }
+  }
+  if (a.P > 1)
+    for (int i = ctid; i < rows; i += NCT) cnt[i] = 0;
+  pdl_wait();  // x and the residual come from the preceding kernels
+  for (int i = ctid; i < a.K / 8; i += NCT) {
+    const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)i * 8);
+    const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      xs[x_swz_index<EPC>(i * 8 + 2 * j)] = bf16lo(vw[j]);
+      xs[x_swz_index<EPC>(i * 8 + 2 * j + 1)] = bf16hi(vw[j]);
+    }
+  }
+  team_barrier(1, NCT);
+  if constexpr (AFF) {
+    // X_g = sum of x over group g (one warp per group)
+    for (int g = warp; g < a.G; g += TMA_CWARPS) {
+      float sum = 0.f;
+      for (int e = lane; e < a.group; e += 32) sum += xs[x_swz_index<EPC>(g * a.group + e)];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      if (lane == 0) gsum[g] = sum;
+    }
+    team_barrier(1, NCT);
+  }
+
+  for (int t = warp; t < T_tasks; t += TMA_CWARPS) {
+    const int s = t % S;
+    if (abort_flag) break;
+    if (!mbar_wait_bounded(full0 + 8 * s, (t / S) & 1)) {
+      abort_flag = 1;
+      atomicExch(a.err, (int)MT_ERR_TIMEOUT);
+      break;
+    }
+    const int rg = t / a.P, p = t - rg * a.P;
+    const int rl0 = rg * R;
+    const unsigned char* slot = ring + (size_t)s * a.slot_bytes;
+    float2 acc[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] = make_float2(0.f, 0.f);
+
+    for (int j = lane; j < a.CPP; j += 32) {
+      const int c = p * a.CPP + j;
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        if (rl0 + i >= rows) break;
+#pragma unroll
+        for (int m = 0; m < NW; ++m) {
+          const uint4 w = *reinterpret_cast<const uint4*>(slot + (i * NW + m) * a.B + j * 16);
+          const float2 d = chunk_dot<FMT>(w, xs, c);
+          if constexpr (AFF) {
+            const float sc = ssc[((rl0 + i) * NW + m) * a.G + (c * EPC) / a.group];
+            acc[i * NW + m] = __ffma2_rn(make_float2(sc, sc), d, acc[i * NW + m]);
+          } else {
+            acc[i * NW + m] = __fadd2_rn(acc[i * NW + m], d);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);  // slot consumed
+
+    float vals[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) vals[v] = acc[v].x + acc[v].y;
+    if constexpr (AFF) {
+      // bias terms of the groups in this piece: sum_g b_g * X_g
+      for (int gl = lane; gl < a.GPP; gl += 32) {
+        const int g = p * a.GPP + gl;
+        const float xg = gsum[g];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          if (rl0 + i >= rows) break;
+#pragma unroll
+          for (int m = 0; m < NW; ++m) vals[i * NW + m] = fmaf(sbi[((rl0 + i) * NW + m) * a.G + g], xg, vals[i * NW + m]);
+        }
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) vals[v] += __shfl_xor_sync(0xffffffffu, vals[v], off);
+
+    // lane i finishes row i of the task
+    if (lane < R && rl0 + lane < rows) {
+      const int rl = rl0 + lane;
+      float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < R; ++i)
+        if (i == lane) { v0 = vals[i * NW]; if (NW == 2) v1 = vals[i * NW + NW - 1]; }
+      bool finish = true;
+      if (a.P > 1) {
+        parts[((size_t)rl * a.P + p) * NW] = v0;
+        if (NW == 2) parts[((size_t)rl * a.P + p) * NW + 1] = v1;
+        __threadfence_block();
+        finish = atomicAdd(&cnt[rl], 1) == a.P - 1;
+        if (finish) {
+          __threadfence_block();
+          v0 = 0.f; v1 = 0.f;
+          for (int q = 0; q < a.P; ++q) {  // fixed order: deterministic
+            v0 += parts[((size_t)rl * a.P + q) * NW];
+            if (NW == 2) v1 += parts[((size_t)rl * a.P + q) * NW + 1];
+          }
+        }
+      }
+      if (finish) {
+        const int n = r_begin + rl;
+        float outv;
+        if constexpr (KIND == 0) {
+          outv = v0 / (1.0f + expf(-v0)) * v1;  // silu(gate) * up
+        } else {
+          outv = v0 + bf16f(a.res[n]);  // + residual
+        }
+        if (a.out_f32)
+          static_cast<float*>(a.out)[n] = outv;
+        else
+          static_cast<uint16_t*>(a.out)[n] = f2bf(outv);
+      }
+    }
+  }
+}
+
+}  // namespace mt
+
+namespace mt {
+
+// Host plan and launch of the TMA pipeline for one (format, kind, rows per
+// task).  Returns MT_ERR_SHAPE when the problem does not fit its shared
+// memory layout (the caller then uses the register-pipelined kernel).
+template <int FMT, int KIND, int R>
+mt_status run_gemv_tma(const GemvProblem& p, const Launch& l) {
+  using T = FmtTraits<FMT>;
+  constexpr int EPC = T::EPC;
+  constexpr bool AFF = T::AFFINE;
+  constexpr int NW = KIND == 0 ? 2 : 1;
+  if (p.M != 1) return MT_ERR_SHAPE;
+  static OccCache cache;  // only the attribute flags are used
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  int derr = 0;
+  const DeviceInfo* di = device_info(&derr);
+  if (!di) return cuda_fail((cudaError_t)derr);
+
+  TmaArgs a = {};
+  a.x = p.x;
+  a.W0 = static_cast<const uint8_t*>(p.W0);
+  a.W1 = static_cast<const uint8_t*>(p.W1);
+  a.s0 = p.s0; a.b0 = p.b0; a.s1 = p.s1; a.b1 = p.b1;
+  a.res = p.res;
+  a.out = p.out;
+  a.K = p.K; a.N = p.N;
+  a.group = AFF ? p.group : 1;
+  a.G = AFF ? p.K / p.group : 0;
+  a.row_bytes = FMT == FMT_BF16 ? p.K * 2 : (FMT == FMT_A8 ? p.K : p.K / 2);
+  a.out_f32 = p.out_f32 ? 1 : 0;
+  a.err = device_error_ptr();
+  if (!a.err) return cuda_fail(cudaErrorInvalidSymbol);
+  const int CPR = p.K / EPC;
+
+  // Pieces per row: the fewest that keep a piece at <= 4 KB, dividing both
+  // the row's chunks and (affine) its groups, so pieces hold whole groups.
+  int P = 1;
+  for (int q = 1; q <= CPR; ++q) {
+    if (CPR % q || (AFF && a.G % q)) continue;
+    P = q;
+    if (a.row_bytes / q <= 4096) break;
+  }
+  a.P = P;
+  a.B = a.row_bytes / P;
+  a.CPP = CPR / P;
+  a.GPP = AFF ? a.G / P : 0;
+  a.slot_bytes = R * NW * a.B;
+
+  const int N = p.N;
+  int grid = di->sm_count;
+  if (grid > N) grid = N;
+  a.rows_base = N / grid;
+  a.rows_extra = N % grid;
+  const int rows_max = a.rows_base + (a.rows_extra ? 1 : 0);
+  a.rows_alloc = (rows_max + R - 1) / R * R;
+
+  const size_t fixed = (size_t)p.K * 4 +
+                       (AFF ? (size_t)a.G * 4 + (size_t)2 * a.rows_alloc * NW * a.G * 4 : 0) +
+                       (P > 1 ? (size_t)a.rows_alloc * P * NW * 4 + (size_t)a.rows_alloc * 4 : 0);
+  const size_t budget = (size_t)di->max_smem_optin - 1024;  // static smem and slack
+  if (fixed + 128 + (size_t)TMA_CWARPS * a.slot_bytes > budget) return MT_ERR_SHAPE;
+  int S = (int)((budget - fixed - 128) / ((size_t)a.slot_bytes + 16));
+  S = S / TMA_CWARPS * TMA_CWARPS;
+  if (S > 64) S = 64;
+  if (S < TMA_CWARPS) return MT_ERR_SHAPE;
+  a.S = S;
+  const size_t bar_bytes = ((size_t)16 * S + 127) / 128 * 128;
+  const size_t smem = bar_bytes + (size_t)S * a.slot_bytes + fixed;
+  if (smem > budget) return MT_ERR_SHAPE;
+
+  auto kern = gemv_tma_kernel<FMT, KIND, R>;
+  {
+    std::lock_guard<std::mutex> g(cache.mu);
+    if (dev < 64 && !cache.attr_set[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           di->max_smem_optin);
+      if (e != cudaSuccess) return cuda_fail(e);
+      cache.attr_set[dev] = 1;
+    }
+  }
+  return launch(kern, dim3(grid), dim3((TMA_CWARPS + 1) * 32), smem, l, a);
+}
+
+}  // namespace mt

@@ -12,6 +12,26 @@ namespace mt {
 
 static thread_local int g_last_cuda_error = 0;
 static std::atomic<int> g_opt_pdl{1};
+static std::atomic<int> g_opt_gemv{0};
+
+// Device error word: kernels with bounded waits record MT_ERR_TIMEOUT here.
+__device__ int g_device_error;
+
+int* device_error_ptr() {
+  static std::mutex mu;
+  static int* ptr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> g(mu);
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptr[dev] = static_cast<int*>(p);
+  }
+  return ptr[dev];
+}
+
+int gemv_choice() { return g_opt_gemv.load(); }
 
 mt_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = (int)e;
@@ -226,12 +246,28 @@ mt_status mt_set_option(mt_option opt, int value) {
     g_opt_pdl.store(value ? 1 : 0);
     return MT_OK;
   }
+  if (opt == MT_OPT_GEMV) {
+    if (value < 0 || value > 1) return MT_ERR_FORMAT;
+    g_opt_gemv.store(value);
+    return MT_OK;
+  }
   return MT_ERR_FORMAT;
 }
 
 int mt_get_option(mt_option opt) {
   if (opt == MT_OPT_PDL) return g_opt_pdl.load();
+  if (opt == MT_OPT_GEMV) return g_opt_gemv.load();
   return -1;
+}
+
+int mt_device_error(int clear) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return -1;
+  if (clear && v) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return -1;
+  }
+  return v;
 }
 
 const char* mt_status_string(mt_status s) {

@@ -23,6 +23,13 @@ struct Launch {
 // Records a CUDA error for mt_last_cuda_error() and returns MT_ERR_CUDA.
 mt_status cuda_fail(cudaError_t e);
 
+// Device address of the library's device error word (set by kernels whose
+// bounded waits expire); nullptr if it cannot be resolved.
+int* device_error_ptr();
+
+// Which GEMV kernel family to use for one-row problems (MT_OPT_GEMV).
+int gemv_choice();
+
 // Launches `kernel` with (grid, block, smem) on l.stream, adding the
 // programmatic-stream-serialization attribute when l.pdl is set.
 template <typename... KArgs, typename... Args>

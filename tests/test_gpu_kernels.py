@@ -27,6 +27,16 @@ def mt():
     return m
 
 
+@pytest.fixture(params=["tma", "regs"])
+def gemv(request, mt):
+    """Runs a test with each one-row GEMV kernel (TMA pipeline / register
+    pipeline); M > 1 always uses the register kernel."""
+    mt.mt_set_option(mt.MT_OPT_GEMV, 0 if request.param == "tma" else 1)
+    yield request.param
+    mt.mt_set_option(mt.MT_OPT_GEMV, 0)
+    assert mt.mt_device_error(clear=True) == 0, "a bounded device wait expired"
+
+
 # ------------------------------------------------------------------ helpers
 def gen_w32(N, K, seed, dist=synth.WEIGHT):
     return synth.host_f32(N * K, seed, dist).reshape(N, K)
@@ -123,6 +133,11 @@ SHAPES = [  # (fmt, group, M, d, f)
     (0, 0, 1, 1536, 300),
     (0, 0, 2, 1000, 77),
     (0, 0, 8, 512, 40),
+    (1, 128, 1, 12288, 161),   # 12 KB rows: split into pieces
+    (1, 32, 1, 4096, 1000),    # many rows per CTA
+    (2, 64, 1, 8192, 153),     # one more row than SMs
+    (0, 0, 1, 8960, 40),       # 17.5 KB bf16 rows
+    (1, 64, 1, 64, 7),         # rows shorter than a warp's stride
 ]
 
 
@@ -133,7 +148,7 @@ def _ids(p):
 
 @pytest.mark.parametrize("shape", SHAPES, ids=_ids)
 @pytest.mark.parametrize("out_f32", [False, True])
-def test_swiglu_gateup(mt, shape, out_f32):
+def test_swiglu_gateup(mt, gemv, shape, out_f32):
     fmt, group, M, d, f = shape
     seed = 3000 + fmt * 97 + M * 13 + d + f
     x = synth.host_bf16(M * d, seed, synth.ACT).reshape(M, d)
@@ -158,7 +173,7 @@ def test_swiglu_gateup(mt, shape, out_f32):
 
 @pytest.mark.parametrize("shape", SHAPES, ids=_ids)
 @pytest.mark.parametrize("out_f32", [False, True])
-def test_down_residual(mt, shape, out_f32):
+def test_down_residual(mt, gemv, shape, out_f32):
     fmt, group, M, d, f = shape
     # the down projection reads [M][f] and writes [M][d]; reuse the shape list
     # with the roles of d and f swapped so K = f covers the same K values
@@ -178,7 +193,7 @@ def test_down_residual(mt, shape, out_f32):
         assert_bf16_close(host_bits(y), ref, "y bf16")
 
 
-def test_down_residual_in_place(mt):
+def test_down_residual_in_place(mt, gemv):
     M, K, N, g = 1, 4096, 1024, 128
     hin = synth.host_bf16(M * K, 91, synth.ACT).reshape(M, K)
     res = synth.host_bf16(M * N, 92, synth.ACT).reshape(M, N)
@@ -206,7 +221,7 @@ def _exact_affine(N, K, group, bits, rng, bias_lo=-32, bias_hi=32):
 @pytest.mark.parametrize("bits,group,M,K,N", [(8, 32, 1, 128, 45), (8, 64, 2, 512, 33),
                                               (8, 128, 8, 384, 17), (4, 32, 1, 256, 23),
                                               (4, 64, 3, 512, 16), (4, 128, 1, 384, 9)])
-def test_indexing_down_bit_exact(mt, bits, group, M, K, N):
+def test_indexing_down_bit_exact(mt, gemv, bits, group, M, K, N):
     rng = np.random.default_rng(bits * 1000 + group + K + N + M)
     codes, s, b = _exact_affine(N, K, group, bits, rng)
     x = oracle.bf16_from_f64(rng.integers(-4, 5, size=(M, K)).astype(np.float64))
@@ -222,7 +237,7 @@ def test_indexing_down_bit_exact(mt, bits, group, M, K, N):
 
 @pytest.mark.parametrize("bits,group,M,K,N", [(8, 32, 1, 256, 31), (8, 128, 2, 512, 20),
                                               (4, 64, 1, 512, 12), (4, 32, 8, 256, 10)])
-def test_indexing_gateup_bit_exact(mt, bits, group, M, K, N):
+def test_indexing_gateup_bit_exact(mt, gemv, bits, group, M, K, N):
     # gate rows give g >= 40, where silu(g) == g in both binary64 and fp32, so
     # h = g * u is one rounding of an exact product on both sides
     rng = np.random.default_rng(bits * 77 + group + K + N + M)
@@ -243,7 +258,7 @@ def test_indexing_gateup_bit_exact(mt, bits, group, M, K, N):
     assert np.array_equal(h.cpu().numpy(), (g_ref * u_ref).astype(np.float32))
 
 
-def test_indexing_bf16_weights_bit_exact(mt):
+def test_indexing_bf16_weights_bit_exact(mt, gemv):
     rng = np.random.default_rng(5)
     M, K, N = 2, 1000, 37
     W = oracle.bf16_from_f64(rng.integers(-64, 65, size=(N, K)) * 2.0 ** -6)
@@ -257,7 +272,7 @@ def test_indexing_bf16_weights_bit_exact(mt):
 
 
 # ------------------------------------------------------------------ layer
-def test_tiny_layer_chained(mt):
+def test_tiny_layer_chained(mt, gemv):
     wl = synth.TINY
     d, f, M, g = wl.d, wl.f, wl.M, wl.group
     sd = lambda t: synth.seed_for(wl.wid, 0, t)

@@ -431,8 +431,9 @@ mt_status run_gemv_tma(const GemvProblem& p, const Launch& l) {
   {
     std::lock_guard<std::mutex> g(cache.mu);
     if (dev < 64 && !cache.attr_set[dev]) {
+      // dynamic + static shared memory must stay within the opt-in limit
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           di->max_smem_optin);
+                                           (int)budget);
       if (e != cudaSuccess) return cuda_fail(e);
       cache.attr_set[dev] = 1;
     }

@@ -57,6 +57,8 @@ struct TmaArgs {
   int S;                 // ring slots (multiple of TMA_CWARPS)
   int slot_bytes;        // R * NW * B
   int rows_alloc;        // rows of the staged scale/bias/part arrays
+  int sb_stride;         // elements per staged scale or bias array (multiple of 8)
+  int sb_tma;            // 1: scales/biases are bulk-copied (G % 8 == 0)
   int out_f32;
   int* err;              // device error word
 };
@@ -155,14 +157,16 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
 
   extern __shared__ __align__(128) unsigned char smem[];
   const int S = a.S;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);               // full[S], empty[S]
-  const size_t bar_bytes = ((size_t)16 * S + 127) / 128 * 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[S], empty[S], sb, x
+  const size_t bar_bytes = ((size_t)8 * (2 * S + 2) + 127) / 128 * 128;
   unsigned char* ring = smem + bar_bytes;
-  float* xs = reinterpret_cast<float*>(ring + (size_t)S * a.slot_bytes);  // [K] swizzled
-  float* gsum = xs + a.K;                                                // [G]
-  float* ssc = gsum + (AFF ? a.G : 0);                                   // [rows][NW][G]
-  float* sbi = ssc + (AFF ? (size_t)a.rows_alloc * NW * a.G : 0);        // [rows][NW][G]
-  float* parts = sbi + (AFF ? (size_t)a.rows_alloc * NW * a.G : 0);      // [rows][P][NW]
+  uint16_t* xraw = reinterpret_cast<uint16_t*>(ring + (size_t)S * a.slot_bytes);  // [K] bf16
+  float* xs = reinterpret_cast<float*>(xraw + a.K);                               // [K] swizzled
+  float* gsum = xs + a.K;                                                         // [G]
+  uint16_t* sbr = reinterpret_cast<uint16_t*>(gsum + (AFF ? (a.G + 3) / 4 * 4 : 0));
+  // sbr: 2*NW arrays of sb_stride bf16: array 2m = scales, 2m+1 = biases of matrix m,
+  // each [rows][G]
+  float* parts = reinterpret_cast<float*>(sbr + (AFF ? (size_t)2 * NW * a.sb_stride : 0));
   int* cnt = reinterpret_cast<int*>(parts + (a.P > 1 ? (size_t)a.rows_alloc * a.P * NW : 0));
   __shared__ volatile int abort_flag;
 
@@ -173,6 +177,8 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
   const int groups = (rows + R - 1) / R;
   const int T_tasks = groups * a.P;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
+  const uint32_t bar_sb = smem_u32(bars + 2 * S), bar_x = smem_u32(bars + 2 * S + 1);
+  const bool sb_tma = AFF && a.sb_tma;
 
   if (tid == 0) {
     abort_flag = 0;
@@ -180,6 +186,8 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
+    mbar_init(bar_sb, 1);
+    mbar_init(bar_x, 1);
     mbar_fence_init();
   }
   __syncthreads();
@@ -189,10 +197,32 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
     // ------------------------------------------------------- producer
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
+      const uint64_t keep = l2_evict_last_policy();
       const uint32_t ring_s = smem_u32(ring);
+      if (sb_tma) {
+        // the CTA's scales and biases: contiguous [rows][G] blocks
+        const uint32_t bytes = (uint32_t)(rows * a.G * 2);
+        mbar_arrive_expect_tx(bar_sb, (uint32_t)(2 * NW) * bytes);
+#pragma unroll
+        for (int m = 0; m < NW; ++m) {
+          const size_t off = (size_t)r_begin * a.G;
+          bulk_g2s(smem_u32(sbr + (size_t)(2 * m) * a.sb_stride), (m ? a.s1 : a.s0) + off, bytes,
+                   bar_sb, keep);
+          bulk_g2s(smem_u32(sbr + (size_t)(2 * m + 1) * a.sb_stride), (m ? a.b1 : a.b0) + off,
+                   bytes, bar_sb, keep);
+        }
+      }
       int issued = 0;
+      bool x_issued = false;
       for (int t = 0; t < T_tasks; ++t) {
         const int s = t % S;
+        if (t == S) {
+          // the ring is full: fetch x once the preceding kernel is done
+          pdl_wait();
+          mbar_arrive_expect_tx(bar_x, (uint32_t)(a.K * 2));
+          bulk_g2s(smem_u32(xraw), a.x, (uint32_t)(a.K * 2), bar_x, keep);
+          x_issued = true;
+        }
         if (t >= S && !mbar_wait_bounded(empty0 + 8 * s, ((t / S) - 1) & 1)) {
           abort_flag = 1;
           atomicExch(a.err, (int)MT_ERR_TIMEOUT);
@@ -211,32 +241,42 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
         }
         issued = t + 1;
       }
+      if (!x_issued) {
+        pdl_wait();
+        mbar_arrive_expect_tx(bar_x, (uint32_t)(a.K * 2));
+        bulk_g2s(smem_u32(xraw), a.x, (uint32_t)(a.K * 2), bar_x, keep);
+      }
       // never leave the CTA with copies in flight
       for (int t = max(0, issued - S); t < issued; ++t)
         (void)mbar_wait_bounded(full0 + 8 * (t % S), (t / S) & 1);
+      (void)mbar_wait_bounded(bar_x, 0);
+      if (sb_tma) (void)mbar_wait_bounded(bar_sb, 0);
     }
     return;
   }
 
   // --------------------------------------------------------- consumers
   const int ctid = tid;  // 0 .. NCT-1
-  if constexpr (AFF) {
-    // scales and biases of the CTA's rows as fp32 (static: before the wait)
-    const int n_sb = rows * NW * a.G;
+  if (AFF && !sb_tma) {
+    // scales/biases whose blocks are not 16-byte aligned: plain loads
+    const int n_sb = rows * a.G;
     for (int i = ctid; i < n_sb; i += NCT) {
-      const int rl = i / (NW * a.G);
-      const int rem = i - rl * NW * a.G;
-      const int m = rem / a.G, g = rem - m * a.G;
-      const size_t gi = (size_t)(r_begin + rl) * a.G + g;
-      ssc[i] = bf16f(ldg_u16((m ? a.s1 : a.s0) + gi));
-      sbi[i] = bf16f(ldg_u16((m ? a.b1 : a.b0) + gi));
+      const size_t gi = (size_t)r_begin * a.G + i;
+#pragma unroll
+      for (int m = 0; m < NW; ++m) {
+        sbr[(size_t)(2 * m) * a.sb_stride + i] = ldg_u16((m ? a.s1 : a.s0) + gi);
+        sbr[(size_t)(2 * m + 1) * a.sb_stride + i] = ldg_u16((m ? a.b1 : a.b0) + gi);
+      }
     }
   }
   if (a.P > 1)
     for (int i = ctid; i < rows; i += NCT) cnt[i] = 0;
-  pdl_wait();  // x and the residual come from the preceding kernels
+  if (!mbar_wait_bounded(bar_x, 0)) {
+    abort_flag = 1;
+    atomicExch(a.err, (int)MT_ERR_TIMEOUT);
+  }
   for (int i = ctid; i < a.K / 8; i += NCT) {
-    const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)i * 8);
+    const uint4 v = *reinterpret_cast<const uint4*>(xraw + (size_t)i * 8);
     const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -254,8 +294,13 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
       for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
       if (lane == 0) gsum[g] = sum;
     }
+    if (sb_tma && !mbar_wait_bounded(bar_sb, 0)) {
+      abort_flag = 1;
+      atomicExch(a.err, (int)MT_ERR_TIMEOUT);
+    }
     team_barrier(1, NCT);
   }
+  pdl_wait();  // the residual and the output buffer belong to the preceding kernels' chain
 
   for (int t = warp; t < T_tasks; t += TMA_CWARPS) {
     const int s = t % S;
@@ -282,7 +327,7 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
           const uint4 w = *reinterpret_cast<const uint4*>(slot + (i * NW + m) * a.B + j * 16);
           const float2 d = chunk_dot<FMT>(w, xs, c);
           if constexpr (AFF) {
-            const float sc = ssc[((rl0 + i) * NW + m) * a.G + (c * EPC) / a.group];
+            const float sc = bf16f(sbr[(size_t)(2 * m) * a.sb_stride + (rl0 + i) * a.G + (c * EPC) / a.group]);
             acc[i * NW + m] = __ffma2_rn(make_float2(sc, sc), d, acc[i * NW + m]);
           } else {
             acc[i * NW + m] = __fadd2_rn(acc[i * NW + m], d);
@@ -305,7 +350,10 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
         for (int i = 0; i < R; ++i) {
           if (rl0 + i >= rows) break;
 #pragma unroll
-          for (int m = 0; m < NW; ++m) vals[i * NW + m] = fmaf(sbi[((rl0 + i) * NW + m) * a.G + g], xg, vals[i * NW + m]);
+          for (int m = 0; m < NW; ++m)
+            vals[i * NW + m] =
+                fmaf(bf16f(sbr[(size_t)(2 * m + 1) * a.sb_stride + (rl0 + i) * a.G + g]), xg,
+                     vals[i * NW + m]);
         }
       }
     }
@@ -413,17 +461,19 @@ mt_status run_gemv_tma(const GemvProblem& p, const Launch& l) {
   const int rows_max = a.rows_base + (a.rows_extra ? 1 : 0);
   a.rows_alloc = (rows_max + R - 1) / R * R;
 
-  const size_t fixed = (size_t)p.K * 4 +
-                       (AFF ? (size_t)a.G * 4 + (size_t)2 * a.rows_alloc * NW * a.G * 4 : 0) +
+  a.sb_stride = AFF ? (a.rows_alloc * a.G + 7) / 8 * 8 : 0;
+  a.sb_tma = (AFF && a.G % 8 == 0) ? 1 : 0;
+  const size_t fixed = (size_t)p.K * 2 + (size_t)p.K * 4 +
+                       (AFF ? (size_t)(a.G + 3) / 4 * 16 + (size_t)2 * NW * a.sb_stride * 2 : 0) +
                        (P > 1 ? (size_t)a.rows_alloc * P * NW * 4 + (size_t)a.rows_alloc * 4 : 0);
   const size_t budget = (size_t)di->max_smem_optin - 1024;  // static smem and slack
-  if (fixed + 128 + (size_t)TMA_CWARPS * a.slot_bytes > budget) return MT_ERR_SHAPE;
-  int S = (int)((budget - fixed - 128) / ((size_t)a.slot_bytes + 16));
+  if (fixed + 256 + (size_t)TMA_CWARPS * a.slot_bytes > budget) return MT_ERR_SHAPE;
+  int S = (int)((budget - fixed - 256) / ((size_t)a.slot_bytes + 16));
   S = S / TMA_CWARPS * TMA_CWARPS;
   if (S > 64) S = 64;
   if (S < TMA_CWARPS) return MT_ERR_SHAPE;
   a.S = S;
-  const size_t bar_bytes = ((size_t)16 * S + 127) / 128 * 128;
+  const size_t bar_bytes = ((size_t)8 * (2 * S + 2) + 127) / 128 * 128;
   const size_t smem = bar_bytes + (size_t)S * a.slot_bytes + fixed;
   if (smem > budget) return MT_ERR_SHAPE;
 

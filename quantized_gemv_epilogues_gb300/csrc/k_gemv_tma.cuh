@@ -1,5 +1,5 @@
 // k_gemv_tma.cuh - one-row (M == 1) GEMV with the SwiGLU or residual
-// epilogue, fed by a TMA bulk-copy pipeline.
+// epilogue, fed by TMA bulk copies into shared memory.
 //
 // meTile docs, "Compute-Graph Fusion", Automatic Gated Epilogues (gate and up
 // share the activation, silu(gate) * up before the only store; the down
@@ -7,25 +7,29 @@
 // Policy (affine w = scale * q + bias per group of 32/64/128 along K).
 //
 // GB300 design:
-//  * One persistent CTA per SM owns a contiguous range of output rows.
-//  * Warp specialisation: one producer lane streams the CTA's weight rows
-//    into a ring of shared-memory slots with cp.async.bulk (TMA, evict-first
-//    L2 policy), each slot signalled by a "full" mbarrier with a transaction
-//    count; eight consumer warps each take whole tasks (R rows x one piece of
-//    the row) and release the slot through an "empty" mbarrier.  The ring
-//    holds 100+ KB per SM in flight, independent of register pressure.
-//  * The first slots are requested before waiting on the preceding kernel
-//    (programmatic dependent launch): weights do not depend on it.
-//  * x is staged once as fp32 in shared memory with a bank swizzle, so each
-//    lane's 16-byte reads of its chunk are conflict-free; scales and biases
-//    are staged as fp32.  The affine term is factored as
+//  * One persistent CTA per SM owns a contiguous range of output rows; its
+//    work is split into tasks (R rows x one piece of B bytes of each row).
+//  * Sixteen warps, each feeding itself: a warp owns D slots of a shared
+//    memory ring and streams its own tasks into them with cp.async.bulk (TMA,
+//    evict-first L2 policy), one "full" mbarrier per slot carrying the
+//    transaction count.  As soon as a warp has consumed a slot it requests
+//    its task D steps ahead into the same slot.  Sixteen issuing threads per
+//    SM keep >100 KB in flight (one thread issuing 4 KB copies measured only
+//    ~1.7 TB/s on GB300; 4-16 issuers reach 6.7-7.2 TB/s).
+//  * The first D tasks of every warp are requested before waiting on the
+//    preceding kernel (programmatic dependent launch): weights, scales and
+//    biases do not depend on it; x is fetched right after the wait.
+//  * x is staged once as fp32 in a unit-transposed layout (16-byte unit k of
+//    chunk c at index k*CPR + c), so the lanes of a warp read consecutive
+//    16-byte words: conflict-free.  The affine term is factored as
 //      sum_k (s q_k + b) x_k = sum_chunks s * (sum q_k x_k) + sum_groups b * X_g
-//    with X_g the sum of x over group g, so the per-weight work is one byte
-//    permute (exponent-bias conversion) plus half a packed fp32x2 add and half
-//    a packed fp32x2 FMA.
+//    with X_g the sum of x over group g: per weight one byte permute
+//    (exponent-bias conversion), half a packed fp32x2 add, half a packed
+//    fp32x2 FMA.
 //  * Each task is reduced inside its warp (shuffles); a row split into P
-//    pieces is combined by whichever warp finishes its last piece (a
-//    shared-memory counter; no waiting).
+//    pieces is completed by whichever warp finishes its last piece (a
+//    shared-memory counter, no waiting; the pieces are summed in a fixed
+//    order, so results are deterministic).
 //  * Every mbarrier wait is bounded (~1 s); on expiry the kernel records
 //    MT_ERR_TIMEOUT in a device error word, stops, waits (bounded) for its
 //    own copies in flight and returns.
@@ -34,7 +38,7 @@
 
 namespace mt {
 
-constexpr int TMA_CWARPS = 8;  // consumer warps per CTA
+constexpr int TMA_WARPS = 16;  // warps per CTA (each consumes and issues)
 
 struct TmaArgs {
   const uint16_t* x;
@@ -47,78 +51,58 @@ struct TmaArgs {
   const uint16_t* res;
   void* out;
   int K, N;
-  int group, G;          // group size and groups per row (affine)
-  int row_bytes;         // bytes of one weight row
+  int group, lg_group, G;  // group size, log2(group), groups per row (affine)
+  int CPR;                 // 16-byte chunks per row
+  int row_bytes;           // bytes of one weight row
   int rows_base, rows_extra;
-  int P;                 // pieces per row
-  int B;                 // bytes per piece (multiple of 16)
-  int CPP;               // 16-byte chunks per piece
-  int GPP;               // groups per piece (affine)
-  int S;                 // ring slots (multiple of TMA_CWARPS)
-  int slot_bytes;        // R * NW * B
-  int rows_alloc;        // rows of the staged scale/bias/part arrays
-  int sb_stride;         // elements per staged scale or bias array (multiple of 8)
-  int sb_tma;            // 1: scales/biases are bulk-copied (G % 8 == 0)
+  int P;                   // pieces per row
+  int B;                   // bytes per piece (multiple of 16)
+  int CPP;                 // 16-byte chunks per piece
+  int GPP;                 // groups per piece (affine)
+  int D;                   // ring slots per warp
+  int slot_bytes;          // R * NW * B
+  int rows_alloc;          // rows of the staged scale/bias/part arrays
+  int sb_stride;           // elements per staged scale or bias array (multiple of 8)
+  int sb_tma;              // 1: scales/biases are bulk-copied (G % 8 == 0)
   int out_f32;
-  int* err;              // device error word
+  int* err;                // device error word
 };
 
-// Position (in floats) of element e of x in the swizzled fp32 staging layout:
-// chunk c = e / EPC holds U = EPC/4 float4 units; unit k of chunk c is stored
-// at unit k ^ swz(c), which spreads the 8 lanes of a shared-memory wavefront
-// over all 32 banks when consecutive lanes read consecutive chunks.
+// Float index of element e of x in the unit-transposed staging layout.
 template <int EPC>
-__device__ __forceinline__ int x_swz_index(int e) {
-  constexpr int U = EPC / 4;
-  constexpr int SH = U == 2 ? 2 : (U == 4 ? 1 : 0);
+__device__ __forceinline__ int xt_index(int e, int CPR) {
   const int c = e / EPC;
   const int k = (e % EPC) >> 2;
-  const int ks = k ^ ((c >> SH) & (U - 1));
-  return (c * U + ks) * 4 + (e & 3);
+  return (k * CPR + c) * 4 + (e & 3);
 }
 
-template <int EPC>
-__device__ __forceinline__ float4 x_unit(const float* xs, int c, int k) {
-  constexpr int U = EPC / 4;
-  constexpr int SH = U == 2 ? 2 : (U == 4 ? 1 : 0);
-  const int ks = k ^ ((c >> SH) & (U - 1));
-  return *reinterpret_cast<const float4*>(xs + (c * U + ks) * 4);
-}
-
-// Dot product of one 16-byte weight chunk with its EPC activations, as a
-// pair of partial sums (packed fp32x2).
+// Dot product of one 16-byte weight chunk (chunk c of its row) with its EPC
+// activations, as a pair of partial sums (packed fp32x2).
 template <int FMT>
-__device__ __forceinline__ float2 chunk_dot(const uint4 w, const float* xs, int c) {
-  using T = FmtTraits<FMT>;
-  constexpr int EPC = T::EPC;
+__device__ __forceinline__ float2 chunk_dot(const uint4 w, const float4* __restrict__ xt, int c,
+                                            int CPR) {
   const float2 neg = make_float2(-8388608.0f, -8388608.0f);
   float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
   const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
   if constexpr (FMT == FMT_A8) {
+    // word wi holds elements 4wi..4wi+3, one byte each
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
-      const float4 xv = x_unit<EPC>(xs, c, wi);
-      const uint32_t m0 = __byte_perm(ww[wi], 0x4B000000u, 0x7540u);
-      const uint32_t m1 = __byte_perm(ww[wi], 0x4B000000u, 0x7541u);
-      const uint32_t m2 = __byte_perm(ww[wi], 0x4B000000u, 0x7542u);
-      const uint32_t m3 = __byte_perm(ww[wi], 0x4B000000u, 0x7543u);
-      const float2 qa = __fadd2_rn(make_float2(__uint_as_float(m0), __uint_as_float(m1)), neg);
-      const float2 qb = __fadd2_rn(make_float2(__uint_as_float(m2), __uint_as_float(m3)), neg);
-      if (wi & 1) {
-        d1 = __ffma2_rn(qa, make_float2(xv.x, xv.y), d1);
-        d1 = __ffma2_rn(qb, make_float2(xv.z, xv.w), d1);
-      } else {
-        d0 = __ffma2_rn(qa, make_float2(xv.x, xv.y), d0);
-        d0 = __ffma2_rn(qb, make_float2(xv.z, xv.w), d0);
-      }
+      const float4 xv = xt[wi * CPR + c];
+      const float2 qa = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(ww[wi], 0x4B000000u, 0x7540u)),
+                                               __uint_as_float(__byte_perm(ww[wi], 0x4B000000u, 0x7541u))), neg);
+      const float2 qb = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(ww[wi], 0x4B000000u, 0x7542u)),
+                                               __uint_as_float(__byte_perm(ww[wi], 0x4B000000u, 0x7543u))), neg);
+      d0 = __ffma2_rn(qa, make_float2(xv.x, xv.y), d0);
+      d1 = __ffma2_rn(qb, make_float2(xv.z, xv.w), d1);
     }
   } else if constexpr (FMT == FMT_A4) {
     // word wi holds elements 8wi..8wi+7: byte j = (2j low nibble, 2j+1 high)
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
       const uint32_t lo = ww[wi] & 0x0F0F0F0Fu, hi = (ww[wi] >> 4) & 0x0F0F0F0Fu;
-      const float4 xa = x_unit<EPC>(xs, c, 2 * wi);      // elements 8wi .. 8wi+3
-      const float4 xb = x_unit<EPC>(xs, c, 2 * wi + 1);  // elements 8wi+4 .. 8wi+7
+      const float4 xa = xt[(2 * wi) * CPR + c];      // elements 8wi .. 8wi+3
+      const float4 xb = xt[(2 * wi + 1) * CPR + c];  // elements 8wi+4 .. 8wi+7
       const float2 q01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7540u)),
                                                 __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7540u))), neg);
       const float2 q23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7541u)),
@@ -136,36 +120,33 @@ __device__ __forceinline__ float2 chunk_dot(const uint4 w, const float* xs, int 
     // dense bf16: word wi holds elements 2wi (low half) and 2wi+1 (high half)
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const float4 xv = x_unit<EPC>(xs, c, u);
-      const float2 wa = make_float2(bf16lo(ww[2 * u]), bf16hi(ww[2 * u]));
-      const float2 wb = make_float2(bf16lo(ww[2 * u + 1]), bf16hi(ww[2 * u + 1]));
-      d0 = __ffma2_rn(wa, make_float2(xv.x, xv.y), d0);
-      d1 = __ffma2_rn(wb, make_float2(xv.z, xv.w), d1);
+      const float4 xv = xt[u * CPR + c];
+      d0 = __ffma2_rn(make_float2(bf16lo(ww[2 * u]), bf16hi(ww[2 * u])), make_float2(xv.x, xv.y), d0);
+      d1 = __ffma2_rn(make_float2(bf16lo(ww[2 * u + 1]), bf16hi(ww[2 * u + 1])), make_float2(xv.z, xv.w), d1);
     }
   }
   return __fadd2_rn(d0, d1);
 }
 
 template <int FMT, int KIND, int R>
-__global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(const TmaArgs a) {
+__global__ void __launch_bounds__(TMA_WARPS * 32, 1) gemv_tma_kernel(const TmaArgs a) {
   using T = FmtTraits<FMT>;
   constexpr int EPC = T::EPC;
   constexpr bool AFF = T::AFFINE;
   constexpr int NW = KIND == 0 ? 2 : 1;
   constexpr int V = R * NW;
-  constexpr int NCT = TMA_CWARPS * 32;  // consumer threads
 
   extern __shared__ __align__(128) unsigned char smem[];
-  const int S = a.S;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[S], empty[S], sb, x
-  const size_t bar_bytes = ((size_t)8 * (2 * S + 2) + 127) / 128 * 128;
+  const int S = TMA_WARPS * a.D;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[S], x, sb
+  const size_t bar_bytes = ((size_t)8 * (S + 2) + 127) / 128 * 128;
   unsigned char* ring = smem + bar_bytes;
   uint16_t* xraw = reinterpret_cast<uint16_t*>(ring + (size_t)S * a.slot_bytes);  // [K] bf16
-  float* xs = reinterpret_cast<float*>(xraw + a.K);                               // [K] swizzled
-  float* gsum = xs + a.K;                                                         // [G]
+  float4* xt = reinterpret_cast<float4*>(xraw + a.K);                             // [K/4]
+  float* gsum = reinterpret_cast<float*>(xt + a.K / 4);                           // [G]
   uint16_t* sbr = reinterpret_cast<uint16_t*>(gsum + (AFF ? (a.G + 3) / 4 * 4 : 0));
-  // sbr: 2*NW arrays of sb_stride bf16: array 2m = scales, 2m+1 = biases of matrix m,
-  // each [rows][G]
+  // sbr: 2*NW arrays of sb_stride bf16: array 2m = scales, 2m+1 = biases of
+  // matrix m, each [rows][G]
   float* parts = reinterpret_cast<float*>(sbr + (AFF ? (size_t)2 * NW * a.sb_stride : 0));
   int* cnt = reinterpret_cast<int*>(parts + (a.P > 1 ? (size_t)a.rows_alloc * a.P * NW : 0));
   __shared__ volatile int abort_flag;
@@ -174,93 +155,62 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
   const int cta = blockIdx.x;
   const int r_begin = cta * a.rows_base + min(cta, a.rows_extra);
   const int rows = a.rows_base + (cta < a.rows_extra ? 1 : 0);
-  const int groups = (rows + R - 1) / R;
-  const int T_tasks = groups * a.P;
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
-  const uint32_t bar_sb = smem_u32(bars + 2 * S), bar_x = smem_u32(bars + 2 * S + 1);
+  const int T_tasks = (rows + R - 1) / R * a.P;
+  const int my_n = warp < T_tasks ? (T_tasks - warp + TMA_WARPS - 1) / TMA_WARPS : 0;
+  const int D = a.D;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t bar_x = smem_u32(bars + S), bar_sb = smem_u32(bars + S + 1);
   const bool sb_tma = AFF && a.sb_tma;
 
   if (tid == 0) {
     abort_flag = 0;
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
-    }
-    mbar_init(bar_sb, 1);
-    mbar_init(bar_x, 1);
+    for (int s = 0; s < S + 2; ++s) mbar_init(full0 + 8 * s, 1);
     mbar_fence_init();
   }
   __syncthreads();
   pdl_trigger();
 
-  if (warp == TMA_CWARPS) {
-    // ------------------------------------------------------- producer
-    if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();
-      const uint64_t keep = l2_evict_last_policy();
-      const uint32_t ring_s = smem_u32(ring);
-      if (sb_tma) {
-        // the CTA's scales and biases: contiguous [rows][G] blocks
-        const uint32_t bytes = (uint32_t)(rows * a.G * 2);
-        mbar_arrive_expect_tx(bar_sb, (uint32_t)(2 * NW) * bytes);
+  const uint64_t pol = l2_evict_first_policy();
+  // i-th task of this warp into its slot (i % D); lane 0 only
+  auto issue = [&](int i) {
+    const int t = warp + i * TMA_WARPS;
+    const int slot = warp * D + i % D;
+    const int rg = t / a.P, p = t - rg * a.P;
+    const int nvalid = min(R, rows - rg * R);
+    const uint32_t bar = full0 + 8 * slot;
+    mbar_arrive_expect_tx(bar, (uint32_t)(nvalid * NW * a.B));
+    const uint32_t dst = smem_u32(ring + (size_t)slot * a.slot_bytes);
+    for (int ii = 0; ii < nvalid; ++ii) {
+      const size_t src = (size_t)(r_begin + rg * R + ii) * a.row_bytes + (size_t)p * a.B;
 #pragma unroll
-        for (int m = 0; m < NW; ++m) {
-          const size_t off = (size_t)r_begin * a.G;
-          bulk_g2s(smem_u32(sbr + (size_t)(2 * m) * a.sb_stride), (m ? a.s1 : a.s0) + off, bytes,
-                   bar_sb, keep);
-          bulk_g2s(smem_u32(sbr + (size_t)(2 * m + 1) * a.sb_stride), (m ? a.b1 : a.b0) + off,
-                   bytes, bar_sb, keep);
-        }
-      }
-      int issued = 0;
-      bool x_issued = false;
-      for (int t = 0; t < T_tasks; ++t) {
-        const int s = t % S;
-        if (t == S) {
-          // the ring is full: fetch x once the preceding kernel is done
-          pdl_wait();
-          mbar_arrive_expect_tx(bar_x, (uint32_t)(a.K * 2));
-          bulk_g2s(smem_u32(xraw), a.x, (uint32_t)(a.K * 2), bar_x, keep);
-          x_issued = true;
-        }
-        if (t >= S && !mbar_wait_bounded(empty0 + 8 * s, ((t / S) - 1) & 1)) {
-          abort_flag = 1;
-          atomicExch(a.err, (int)MT_ERR_TIMEOUT);
-          break;
-        }
-        if (abort_flag) break;
-        const int rg = t / a.P, p = t - rg * a.P;
-        const int nvalid = min(R, rows - rg * R);
-        mbar_arrive_expect_tx(full0 + 8 * s, (uint32_t)(nvalid * NW * a.B));
-        for (int i = 0; i < nvalid; ++i) {
-          const size_t src = (size_t)(r_begin + rg * R + i) * a.row_bytes + (size_t)p * a.B;
-#pragma unroll
-          for (int m = 0; m < NW; ++m)
-            bulk_g2s(ring_s + (uint32_t)(s * a.slot_bytes + (i * NW + m) * a.B),
-                     (m ? a.W1 : a.W0) + src, (uint32_t)a.B, full0 + 8 * s, pol);
-        }
-        issued = t + 1;
-      }
-      if (!x_issued) {
-        pdl_wait();
-        mbar_arrive_expect_tx(bar_x, (uint32_t)(a.K * 2));
-        bulk_g2s(smem_u32(xraw), a.x, (uint32_t)(a.K * 2), bar_x, keep);
-      }
-      // never leave the CTA with copies in flight
-      for (int t = max(0, issued - S); t < issued; ++t)
-        (void)mbar_wait_bounded(full0 + 8 * (t % S), (t / S) & 1);
-      (void)mbar_wait_bounded(bar_x, 0);
-      if (sb_tma) (void)mbar_wait_bounded(bar_sb, 0);
+      for (int m = 0; m < NW; ++m)
+        bulk_g2s(dst + (uint32_t)((ii * NW + m) * a.B), (m ? a.W1 : a.W0) + src, (uint32_t)a.B,
+                 bar, pol);
     }
-    return;
+  };
+  int issued = 0;
+  if (lane == 0) {
+    issued = min(D, my_n);
+    for (int i = 0; i < issued; ++i) issue(i);
   }
-
-  // --------------------------------------------------------- consumers
-  const int ctid = tid;  // 0 .. NCT-1
+  if (tid == 0 && sb_tma) {
+    // the CTA's scales and biases: contiguous [rows][G] blocks
+    const uint64_t keep = l2_evict_last_policy();
+    const uint32_t bytes = (uint32_t)(rows * a.G * 2);
+    const size_t off = (size_t)r_begin * a.G;
+    mbar_arrive_expect_tx(bar_sb, (uint32_t)(2 * NW) * bytes);
+#pragma unroll
+    for (int m = 0; m < NW; ++m) {
+      bulk_g2s(smem_u32(sbr + (size_t)(2 * m) * a.sb_stride), (m ? a.s1 : a.s0) + off, bytes,
+               bar_sb, keep);
+      bulk_g2s(smem_u32(sbr + (size_t)(2 * m + 1) * a.sb_stride), (m ? a.b1 : a.b0) + off, bytes,
+               bar_sb, keep);
+    }
+  }
   if (AFF && !sb_tma) {
-    // scales/biases whose blocks are not 16-byte aligned: plain loads
+    // scale/bias blocks that are not 16-byte aligned: plain loads
     const int n_sb = rows * a.G;
-    for (int i = ctid; i < n_sb; i += NCT) {
+    for (int i = tid; i < n_sb; i += TMA_WARPS * 32) {
       const size_t gi = (size_t)r_begin * a.G + i;
 #pragma unroll
       for (int m = 0; m < NW; ++m) {
@@ -270,26 +220,34 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
     }
   }
   if (a.P > 1)
-    for (int i = ctid; i < rows; i += NCT) cnt[i] = 0;
+    for (int i = tid; i < rows; i += TMA_WARPS * 32) cnt[i] = 0;
+
+  pdl_wait();  // x, the residual and the output buffer follow the preceding kernel
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_x, (uint32_t)(a.K * 2));
+    bulk_g2s(smem_u32(xraw), a.x, (uint32_t)(a.K * 2), bar_x, l2_evict_last_policy());
+  }
   if (!mbar_wait_bounded(bar_x, 0)) {
     abort_flag = 1;
     atomicExch(a.err, (int)MT_ERR_TIMEOUT);
   }
-  for (int i = ctid; i < a.K / 8; i += NCT) {
+  for (int i = tid; i < a.K / 8; i += TMA_WARPS * 32) {
     const uint4 v = *reinterpret_cast<const uint4*>(xraw + (size_t)i * 8);
     const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+    float* xf = reinterpret_cast<float*>(xt);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      xs[x_swz_index<EPC>(i * 8 + 2 * j)] = bf16lo(vw[j]);
-      xs[x_swz_index<EPC>(i * 8 + 2 * j + 1)] = bf16hi(vw[j]);
+      xf[xt_index<EPC>(i * 8 + 2 * j, a.CPR)] = bf16lo(vw[j]);
+      xf[xt_index<EPC>(i * 8 + 2 * j + 1, a.CPR)] = bf16hi(vw[j]);
     }
   }
-  team_barrier(1, NCT);
+  __syncthreads();
   if constexpr (AFF) {
     // X_g = sum of x over group g (one warp per group)
-    for (int g = warp; g < a.G; g += TMA_CWARPS) {
+    const float* xf = reinterpret_cast<const float*>(xt);
+    for (int g = warp; g < a.G; g += TMA_WARPS) {
       float sum = 0.f;
-      for (int e = lane; e < a.group; e += 32) sum += xs[x_swz_index<EPC>(g * a.group + e)];
+      for (int e = lane; e < a.group; e += 32) sum += xf[xt_index<EPC>(g * a.group + e, a.CPR)];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
       if (lane == 0) gsum[g] = sum;
@@ -298,45 +256,51 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
       abort_flag = 1;
       atomicExch(a.err, (int)MT_ERR_TIMEOUT);
     }
-    team_barrier(1, NCT);
+    __syncthreads();
   }
-  pdl_wait();  // the residual and the output buffer belong to the preceding kernels' chain
 
-  for (int t = warp; t < T_tasks; t += TMA_CWARPS) {
-    const int s = t % S;
+  for (int i = 0; i < my_n; ++i) {
     if (abort_flag) break;
-    if (!mbar_wait_bounded(full0 + 8 * s, (t / S) & 1)) {
+    const int slot = warp * D + i % D;
+    if (!mbar_wait_bounded(full0 + 8 * slot, (i / D) & 1)) {
       abort_flag = 1;
       atomicExch(a.err, (int)MT_ERR_TIMEOUT);
       break;
     }
+    const int t = warp + i * TMA_WARPS;
     const int rg = t / a.P, p = t - rg * a.P;
     const int rl0 = rg * R;
-    const unsigned char* slot = ring + (size_t)s * a.slot_bytes;
+    const unsigned char* sl = ring + (size_t)slot * a.slot_bytes;
     float2 acc[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] = make_float2(0.f, 0.f);
 
     for (int j = lane; j < a.CPP; j += 32) {
       const int c = p * a.CPP + j;
+      const int gi = AFF ? (c * EPC) >> a.lg_group : 0;
 #pragma unroll
-      for (int i = 0; i < R; ++i) {
-        if (rl0 + i >= rows) break;
+      for (int ii = 0; ii < R; ++ii) {
+        if (rl0 + ii >= rows) break;
 #pragma unroll
         for (int m = 0; m < NW; ++m) {
-          const uint4 w = *reinterpret_cast<const uint4*>(slot + (i * NW + m) * a.B + j * 16);
-          const float2 d = chunk_dot<FMT>(w, xs, c);
+          const uint4 w = *reinterpret_cast<const uint4*>(sl + (ii * NW + m) * a.B + j * 16);
+          const float2 d = chunk_dot<FMT>(w, xt, c, a.CPR);
           if constexpr (AFF) {
-            const float sc = bf16f(sbr[(size_t)(2 * m) * a.sb_stride + (rl0 + i) * a.G + (c * EPC) / a.group]);
-            acc[i * NW + m] = __ffma2_rn(make_float2(sc, sc), d, acc[i * NW + m]);
+            const float sc = bf16f(sbr[(size_t)(2 * m) * a.sb_stride + (rl0 + ii) * a.G + gi]);
+            acc[ii * NW + m] = __ffma2_rn(make_float2(sc, sc), d, acc[ii * NW + m]);
           } else {
-            acc[i * NW + m] = __fadd2_rn(acc[i * NW + m], d);
+            acc[ii * NW + m] = __fadd2_rn(acc[ii * NW + m], d);
           }
         }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * s);  // slot consumed
+    if (lane == 0 && i + D < my_n && !abort_flag) {
+      // every lane has finished reading the slot: refill it (async proxy)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(i + D);
+      issued = i + D + 1;
+    }
 
     float vals[V];
 #pragma unroll
@@ -347,13 +311,13 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
         const int g = p * a.GPP + gl;
         const float xg = gsum[g];
 #pragma unroll
-        for (int i = 0; i < R; ++i) {
-          if (rl0 + i >= rows) break;
+        for (int ii = 0; ii < R; ++ii) {
+          if (rl0 + ii >= rows) break;
 #pragma unroll
           for (int m = 0; m < NW; ++m)
-            vals[i * NW + m] =
-                fmaf(bf16f(sbr[(size_t)(2 * m + 1) * a.sb_stride + (rl0 + i) * a.G + g]), xg,
-                     vals[i * NW + m]);
+            vals[ii * NW + m] =
+                fmaf(bf16f(sbr[(size_t)(2 * m + 1) * a.sb_stride + (rl0 + ii) * a.G + g]), xg,
+                     vals[ii * NW + m]);
         }
       }
     }
@@ -362,13 +326,16 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) vals[v] += __shfl_xor_sync(0xffffffffu, vals[v], off);
 
-    // lane i finishes row i of the task
+    // lane ii finishes row ii of the task
     if (lane < R && rl0 + lane < rows) {
       const int rl = rl0 + lane;
       float v0 = 0.f, v1 = 0.f;
 #pragma unroll
-      for (int i = 0; i < R; ++i)
-        if (i == lane) { v0 = vals[i * NW]; if (NW == 2) v1 = vals[i * NW + NW - 1]; }
+      for (int ii = 0; ii < R; ++ii)
+        if (ii == lane) {
+          v0 = vals[ii * NW];
+          if (NW == 2) v1 = vals[ii * NW + NW - 1];
+        }
       bool finish = true;
       if (a.P > 1) {
         parts[((size_t)rl * a.P + p) * NW] = v0;
@@ -377,7 +344,8 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
         finish = atomicAdd(&cnt[rl], 1) == a.P - 1;
         if (finish) {
           __threadfence_block();
-          v0 = 0.f; v1 = 0.f;
+          v0 = 0.f;
+          v1 = 0.f;
           for (int q = 0; q < a.P; ++q) {  // fixed order: deterministic
             v0 += parts[((size_t)rl * a.P + q) * NW];
             if (NW == 2) v1 += parts[((size_t)rl * a.P + q) * NW + 1];
@@ -399,11 +367,12 @@ __global__ void __launch_bounds__((TMA_CWARPS + 1) * 32, 1) gemv_tma_kernel(cons
       }
     }
   }
+  // never leave the CTA with copies in flight (only matters after a timeout)
+  if (lane == 0) {
+    for (int i = max(0, issued - D); i < issued; ++i)
+      (void)mbar_wait_bounded(full0 + 8 * (warp * D + i % D), (i / D) & 1);
+  }
 }
-
-}  // namespace mt
-
-namespace mt {
 
 // Host plan and launch of the TMA pipeline for one (format, kind, rows per
 // task).  Returns MT_ERR_SHAPE when the problem does not fit its shared
@@ -432,24 +401,27 @@ mt_status run_gemv_tma(const GemvProblem& p, const Launch& l) {
   a.out = p.out;
   a.K = p.K; a.N = p.N;
   a.group = AFF ? p.group : 1;
+  a.lg_group = AFF ? (p.group == 32 ? 5 : (p.group == 64 ? 6 : 7)) : 0;
   a.G = AFF ? p.K / p.group : 0;
   a.row_bytes = FMT == FMT_BF16 ? p.K * 2 : (FMT == FMT_A8 ? p.K : p.K / 2);
   a.out_f32 = p.out_f32 ? 1 : 0;
   a.err = device_error_ptr();
   if (!a.err) return cuda_fail(cudaErrorInvalidSymbol);
-  const int CPR = p.K / EPC;
+  a.CPR = p.K / EPC;
 
-  // Pieces per row: the fewest that keep a piece at <= 4 KB, dividing both
-  // the row's chunks and (affine) its groups, so pieces hold whole groups.
+  // Pieces per row: the fewest that keep a task's slot (R rows x NW
+  // matrices x one piece) at <= 4 KB, dividing both the row's chunks and
+  // (affine) its groups, so a piece holds whole groups.
+  const int max_piece = 4096 / (R * NW);
   int P = 1;
-  for (int q = 1; q <= CPR; ++q) {
-    if (CPR % q || (AFF && a.G % q)) continue;
+  for (int q = 1; q <= a.CPR; ++q) {
+    if (a.CPR % q || (AFF && a.G % q)) continue;
     P = q;
-    if (a.row_bytes / q <= 4096) break;
+    if (a.row_bytes / q <= max_piece) break;
   }
   a.P = P;
   a.B = a.row_bytes / P;
-  a.CPP = CPR / P;
+  a.CPP = a.CPR / P;
   a.GPP = AFF ? a.G / P : 0;
   a.slot_bytes = R * NW * a.B;
 
@@ -460,20 +432,21 @@ mt_status run_gemv_tma(const GemvProblem& p, const Launch& l) {
   a.rows_extra = N % grid;
   const int rows_max = a.rows_base + (a.rows_extra ? 1 : 0);
   a.rows_alloc = (rows_max + R - 1) / R * R;
-
   a.sb_stride = AFF ? (a.rows_alloc * a.G + 7) / 8 * 8 : 0;
   a.sb_tma = (AFF && a.G % 8 == 0) ? 1 : 0;
+
   const size_t fixed = (size_t)p.K * 2 + (size_t)p.K * 4 +
                        (AFF ? (size_t)(a.G + 3) / 4 * 16 + (size_t)2 * NW * a.sb_stride * 2 : 0) +
                        (P > 1 ? (size_t)a.rows_alloc * P * NW * 4 + (size_t)a.rows_alloc * 4 : 0);
   const size_t budget = (size_t)di->max_smem_optin - 1024;  // static smem and slack
-  if (fixed + 256 + (size_t)TMA_CWARPS * a.slot_bytes > budget) return MT_ERR_SHAPE;
-  int S = (int)((budget - fixed - 256) / ((size_t)a.slot_bytes + 16));
-  S = S / TMA_CWARPS * TMA_CWARPS;
-  if (S > 64) S = 64;
-  if (S < TMA_CWARPS) return MT_ERR_SHAPE;
-  a.S = S;
-  const size_t bar_bytes = ((size_t)8 * (2 * S + 2) + 127) / 128 * 128;
+  const size_t bars_max = ((size_t)8 * (TMA_WARPS * 8 + 2) + 127) / 128 * 128;
+  if (fixed + bars_max + (size_t)2 * TMA_WARPS * a.slot_bytes > budget) return MT_ERR_SHAPE;
+  int D = (int)((budget - fixed - bars_max) / ((size_t)TMA_WARPS * a.slot_bytes));
+  if (D > 8) D = 8;
+  if (D < 2) return MT_ERR_SHAPE;
+  a.D = D;
+  const int S = TMA_WARPS * D;
+  const size_t bar_bytes = ((size_t)8 * (S + 2) + 127) / 128 * 128;
   const size_t smem = bar_bytes + (size_t)S * a.slot_bytes + fixed;
   if (smem > budget) return MT_ERR_SHAPE;
 
@@ -488,7 +461,7 @@ mt_status run_gemv_tma(const GemvProblem& p, const Launch& l) {
       cache.attr_set[dev] = 1;
     }
   }
-  return launch(kern, dim3(grid), dim3((TMA_CWARPS + 1) * 32), smem, l, a);
+  return launch(kern, dim3(grid), dim3(TMA_WARPS * 32), smem, l, a);
 }
 
 }  // namespace mt

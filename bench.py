@@ -39,7 +39,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "µs per decode MLP layer and effective HBM GB/s (fraction of ~8 TB/s peak)"
 GATEUP_PROFILE = os.path.join(ROOT, "profiles", "gateup_affine8_qwen3-8b.txt")
-KERNEL_SOURCES = ["k_gemv.cuh", "k_gemv_run.cuh", "k_gemv_a8.cu", "mt_device.cuh"]
+KERNEL_SOURCES = ["k_gemv.cuh", "k_gemv_warp.cuh", "k_gemv_run.cuh", "k_gemv_a8.cu", "mt_device.cuh"]
 
 
 def kernel_hash() -> str:
@@ -368,8 +368,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true")
-    ap.add_argument("--gemv", default="tma", choices=["tma", "regs"],
-                    help="one-row GEMV kernel: TMA bulk-copy pipeline or register pipeline")
+    ap.add_argument("--gemv", default="warp", choices=["warp", "team"],
+                    help="one-row GEMV kernel: warp-task kernel (default) or team kernel")
     ap.add_argument("--gateup-only", action="store_true",
                     help="profiling aid: run only the gate/up kernels of the stack")
     args = ap.parse_args()
@@ -388,7 +388,7 @@ def main():
     dev = torch.device("cuda", local)
     if args.no_pdl:
         mt.mt_set_option(mt.MT_OPT_PDL, 0)
-    mt.mt_set_option(mt.MT_OPT_GEMV, 0 if args.gemv == "tma" else 1)
+    mt.mt_set_option(mt.MT_OPT_GEMV, 0 if args.gemv == "warp" else 1)
 
     wl = {"qwen3-8b": synth.QWEN8B, "tiny": synth.TINY, "llama1b": synth.LLAMA1B,
           "qwen15": synth.QWEN15, "sweep": synth.sweep_point(64, 1)}[args.workload]
@@ -472,7 +472,7 @@ def main():
             "gpu_launches": 3 * wl.layers * args.steps,
             "device_error": mt.mt_device_error(),
             "roofline": {"bound": "hbm",
-                         "kernel": ("gemv_tma_kernel" if args.gemv == "tma" else "gemv_kernel")
+                         "kernel": ("gemv_warp_kernel" if args.gemv == "warp" else "gemv_kernel")
                                    + " gate/up+SwiGLU (affine8, one row)",
                          "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_kind": peak_kind,

@@ -89,8 +89,8 @@ typedef enum mt_wfmt { MT_W_BF16 = 0, MT_W_AFFINE8 = 1, MT_W_AFFINE4 = 2 } mt_wf
 /* Library options (mt_set_option / mt_get_option). */
 typedef enum mt_option {
   MT_OPT_PDL = 0, /* 1 (default): launch with programmatic stream serialization */
-  MT_OPT_GEMV = 1 /* one-row GEMV kernel: 0 (default) TMA bulk-copy pipeline,
-                     1 register-pipelined kernel (the one used for M > 1) */
+  MT_OPT_GEMV = 1 /* one-row GEMV kernel: 0 (default) warp-task kernel,
+                     1 team kernel (the one always used for M > 1) */
 } mt_option;
 
 /*

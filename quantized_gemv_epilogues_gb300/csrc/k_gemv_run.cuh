@@ -113,16 +113,16 @@ mt_status run_gemv(const GemvProblem& p, const Launch& l) {
   return launch(kern, dim3(grid), dim3(block), smem, l, a);
 }
 
-template <int FMT, int KIND, int R>
-mt_status run_gemv_tma(const GemvProblem& p, const Launch& l);
+template <int FMT, int KIND>
+mt_status run_gemv_warp(const GemvProblem& p, const Launch& l);
 
-// Chooses the kernel for one (format, kind): the TMA pipeline for one row
-// (unless MT_OPT_GEMV selects the register kernel or the shape does not fit
-// its shared memory), else the register-pipelined kernel by row count.
+// Chooses the kernel for one (format, kind): the warp-task kernel for one
+// row (unless MT_OPT_GEMV selects the team kernel or the shape does not fit
+// its shared memory), else the team kernel by row count.
 template <int FMT, int KIND>
 mt_status dispatch_rows(const GemvProblem& p, const Launch& l) {
   if (p.M == 1 && gemv_choice() == 0) {
-    const mt_status st = run_gemv_tma<FMT, KIND, KIND == 0 ? 1 : 2>(p, l);
+    const mt_status st = run_gemv_warp<FMT, KIND>(p, l);
     if (st != MT_ERR_SHAPE) return st;
   }
   if (p.M <= 1) return run_gemv<FMT, KIND, 1, 4>(p, l);

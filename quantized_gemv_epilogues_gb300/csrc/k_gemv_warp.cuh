@@ -1,46 +1,45 @@
-// k_gemv_tma.cuh - one-row (M == 1) GEMV with the SwiGLU or residual
-// epilogue, fed by TMA bulk copies into shared memory.
+// k_gemv_warp.cuh - one-row (M == 1) GEMV with the SwiGLU or residual
+// epilogue: warp-task register pipeline.
 //
 // meTile docs, "Compute-Graph Fusion", Automatic Gated Epilogues (gate and up
 // share the activation, silu(gate) * up before the only store; the down
 // projection adds the residual in its epilogue); "MLX-LM Backend", Dispatch
 // Policy (affine w = scale * q + bias per group of 32/64/128 along K).
 //
-// GB300 design:
-//  * One persistent CTA per SM owns a contiguous range of output rows; its
-//    work is split into tasks (R rows x one piece of B bytes of each row).
-//  * Sixteen warps, each feeding itself: a warp owns D slots of a shared
-//    memory ring and streams its own tasks into them with cp.async.bulk (TMA,
-//    evict-first L2 policy), one "full" mbarrier per slot carrying the
-//    transaction count.  As soon as a warp has consumed a slot it requests
-//    its task D steps ahead into the same slot.  Sixteen issuing threads per
-//    SM keep >100 KB in flight (one thread issuing 4 KB copies measured only
-//    ~1.7 TB/s on GB300; 4-16 issuers reach 6.7-7.2 TB/s).
-//  * The first D tasks of every warp are requested before waiting on the
-//    preceding kernel (programmatic dependent launch): weights, scales and
-//    biases do not depend on it; x is fetched right after the wait.
-//  * x is staged once as fp32 in a unit-transposed layout (16-byte unit k of
-//    chunk c at index k*CPR + c), so the lanes of a warp read consecutive
-//    16-byte words: conflict-free.  The affine term is factored as
+// GB300 design (each choice measured on this part; see the design notes):
+//  * One persistent CTA of 16 warps per SM owns a contiguous range of output
+//    rows.  The range is cut into tasks of one row piece (B bytes of each of
+//    the NW weight matrices), handed out dynamically through a shared-memory
+//    counter, so warps finish within about one task of each other.
+//  * A warp streams its next task's weights into registers with 128-bit
+//    evict-first loads while it computes the current one (register double
+//    buffer, up to 8 x 16 B per lane per task): ~128 KB in flight per SM
+//    with no per-copy issue cost.  (Bulk TMA copies cost the issuing thread
+//    ~350 cycles each on this part, which capped a TMA-ring design near
+//    3.5 TB/s for 2-4 KB pieces.)  The first task is requested before
+//    waiting on the preceding kernel (programmatic dependent launch).
+//  * x (fp32, unit-transposed: 16-byte unit k of chunk c at index k*CPR + c,
+//    so the lanes of a warp read consecutive words) and the CTA's scales and
+//    biases (bf16) are staged once in shared memory with TMA bulk copies.
+//  * The affine term is factored as
 //      sum_k (s q_k + b) x_k = sum_chunks s * (sum q_k x_k) + sum_groups b * X_g
 //    with X_g the sum of x over group g: per weight one byte permute
-//    (exponent-bias conversion), half a packed fp32x2 add, half a packed
+//    (exponent-bias conversion), half a packed fp32x2 add and half a packed
 //    fp32x2 FMA.
-//  * Each task is reduced inside its warp (shuffles); a row split into P
-//    pieces is completed by whichever warp finishes its last piece (a
-//    shared-memory counter, no waiting; the pieces are summed in a fixed
-//    order, so results are deterministic).
-//  * Every mbarrier wait is bounded (~1 s); on expiry the kernel records
-//    MT_ERR_TIMEOUT in a device error word, stops, waits (bounded) for its
-//    own copies in flight and returns.
+//  * A task's partial sums are reduced inside the warp (shuffles) and stored
+//    per piece in shared memory; after one barrier, one thread per row adds
+//    the pieces in a fixed order (deterministic) and runs the epilogue.
+//  * The staging waits are bounded (~1 s); on expiry the kernel records
+//    MT_ERR_TIMEOUT in a device error word and skips its main loop.
 #pragma once
 #include "k_gemv.cuh"
 
 namespace mt {
 
-constexpr int TMA_WARPS = 16;  // warps per CTA (each consumes and issues)
+constexpr int WARP_TASK_WARPS = 16;  // warps per CTA
+constexpr int WARP_TASK_UPL = 8;     // 16-byte loads per lane per task (all matrices)
 
-struct TmaArgs {
+struct WarpArgs {
   const uint16_t* x;
   const uint8_t* W0;
   const uint8_t* W1;
@@ -57,11 +56,9 @@ struct TmaArgs {
   int rows_base, rows_extra;
   int P;                   // pieces per row
   int B;                   // bytes per piece (multiple of 16)
-  int CPP;                 // 16-byte chunks per piece
+  int CPP;                 // 16-byte chunks per piece (<= 32 * UPL / NW)
   int GPP;                 // groups per piece (affine)
-  int D;                   // ring slots per warp
-  int slot_bytes;          // R * NW * B
-  int rows_alloc;          // rows of the staged scale/bias/part arrays
+  int rows_alloc;          // rows of the staged arrays
   int sb_stride;           // elements per staged scale or bias array (multiple of 8)
   int sb_tma;              // 1: scales/biases are bulk-copied (G % 8 == 0)
   int out_f32;
@@ -128,71 +125,69 @@ __device__ __forceinline__ float2 chunk_dot(const uint4 w, const float4* __restr
   return __fadd2_rn(d0, d1);
 }
 
-template <int FMT, int KIND, int R>
-__global__ void __launch_bounds__(TMA_WARPS * 32, 1) gemv_tma_kernel(const TmaArgs a) {
+template <int FMT, int KIND>
+__global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(const WarpArgs a) {
   using T = FmtTraits<FMT>;
   constexpr int EPC = T::EPC;
   constexpr bool AFF = T::AFFINE;
   constexpr int NW = KIND == 0 ? 2 : 1;
-  constexpr int V = R * NW;
+  constexpr int CL = WARP_TASK_UPL / NW;  // chunks per lane per matrix per task
+  constexpr int NT = WARP_TASK_WARPS * 32;
 
   extern __shared__ __align__(128) unsigned char smem[];
-  const int S = TMA_WARPS * a.D;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[S], x, sb
-  const size_t bar_bytes = ((size_t)8 * (S + 2) + 127) / 128 * 128;
-  unsigned char* ring = smem + bar_bytes;
-  uint16_t* xraw = reinterpret_cast<uint16_t*>(ring + (size_t)S * a.slot_bytes);  // [K] bf16
-  float4* xt = reinterpret_cast<float4*>(xraw + a.K);                             // [K/4]
-  float* gsum = reinterpret_cast<float*>(xt + a.K / 4);                           // [G]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);            // x, sb
+  uint16_t* xraw = reinterpret_cast<uint16_t*>(smem + 128);       // [K] bf16
+  float4* xt = reinterpret_cast<float4*>(xraw + a.K);             // [K/4]
+  float* gsum = reinterpret_cast<float*>(xt + a.K / 4);           // [G]
   uint16_t* sbr = reinterpret_cast<uint16_t*>(gsum + (AFF ? (a.G + 3) / 4 * 4 : 0));
-  // sbr: 2*NW arrays of sb_stride bf16: array 2m = scales, 2m+1 = biases of
-  // matrix m, each [rows][G]
-  float* parts = reinterpret_cast<float*>(sbr + (AFF ? (size_t)2 * NW * a.sb_stride : 0));
-  int* cnt = reinterpret_cast<int*>(parts + (a.P > 1 ? (size_t)a.rows_alloc * a.P * NW : 0));
+  // sbr: 2*NW arrays of sb_stride bf16: 2m = scales, 2m+1 = biases of matrix m
+  float* parts = reinterpret_cast<float*>(sbr + (AFF ? (size_t)2 * NW * a.sb_stride : 0));  // [rows][P][NW]
+  __shared__ int task_ctr;
   __shared__ volatile int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
   const int r_begin = cta * a.rows_base + min(cta, a.rows_extra);
   const int rows = a.rows_base + (cta < a.rows_extra ? 1 : 0);
-  const int T_tasks = (rows + R - 1) / R * a.P;
-  const int my_n = warp < T_tasks ? (T_tasks - warp + TMA_WARPS - 1) / TMA_WARPS : 0;
-  const int D = a.D;
-  const uint32_t full0 = smem_u32(bars);
-  const uint32_t bar_x = smem_u32(bars + S), bar_sb = smem_u32(bars + S + 1);
+  const int T_tasks = rows * a.P;
+  const uint32_t bar_x = smem_u32(bars), bar_sb = smem_u32(bars + 1);
   const bool sb_tma = AFF && a.sb_tma;
 
   if (tid == 0) {
     abort_flag = 0;
-    for (int s = 0; s < S + 2; ++s) mbar_init(full0 + 8 * s, 1);
+    task_ctr = WARP_TASK_WARPS;  // tasks 0..W-1 are taken statically below
+    mbar_init(bar_x, 1);
+    mbar_init(bar_sb, 1);
     mbar_fence_init();
   }
   __syncthreads();
   pdl_trigger();
 
   const uint64_t pol = l2_evict_first_policy();
-  // i-th task of this warp into its slot (i % D); lane 0 only
-  auto issue = [&](int i) {
-    const int t = warp + i * TMA_WARPS;
-    const int slot = warp * D + i % D;
-    const int rg = t / a.P, p = t - rg * a.P;
-    const int nvalid = min(R, rows - rg * R);
-    const uint32_t bar = full0 + 8 * slot;
-    mbar_arrive_expect_tx(bar, (uint32_t)(nvalid * NW * a.B));
-    const uint32_t dst = smem_u32(ring + (size_t)slot * a.slot_bytes);
-    for (int ii = 0; ii < nvalid; ++ii) {
-      const size_t src = (size_t)(r_begin + rg * R + ii) * a.row_bytes + (size_t)p * a.B;
+  auto load_task = [&](int t, uint4 (&buf)[NW][CL]) {
+    const bool ok = t < T_tasks;
+    const int rl = ok ? t / a.P : 0, p = ok ? t - rl * a.P : 0;
+    const size_t base = (size_t)(r_begin + rl) * a.row_bytes + (size_t)p * a.B;
 #pragma unroll
-      for (int m = 0; m < NW; ++m)
-        bulk_g2s(dst + (uint32_t)((ii * NW + m) * a.B), (m ? a.W1 : a.W0) + src, (uint32_t)a.B,
-                 bar, pol);
-    }
+    for (int m = 0; m < NW; ++m)
+#pragma unroll
+      for (int k = 0; k < CL; ++k) {
+        const int j = lane + 32 * k;
+        buf[m][k] = (ok && j < a.CPP) ? ldg_stream_pol((m ? a.W1 : a.W0) + base + (size_t)j * 16, pol)
+                                      : make_uint4(0, 0, 0, 0);
+      }
   };
-  int issued = 0;
-  if (lane == 0) {
-    issued = min(D, my_n);
-    for (int i = 0; i < issued; ++i) issue(i);
-  }
+  auto next_task = [&]() -> int {
+    int t = 0;
+    if (lane == 0) t = atomicAdd(&task_ctr, 1);
+    return __shfl_sync(0xffffffffu, t, 0);
+  };
+
+  // first task of each warp: static weights, requested before the wait
+  uint4 bufA[NW][CL], bufB[NW][CL];
+  int tA = warp;
+  load_task(tA, bufA);
+
   if (tid == 0 && sb_tma) {
     // the CTA's scales and biases: contiguous [rows][G] blocks
     const uint64_t keep = l2_evict_last_policy();
@@ -210,7 +205,7 @@ __global__ void __launch_bounds__(TMA_WARPS * 32, 1) gemv_tma_kernel(const TmaAr
   if (AFF && !sb_tma) {
     // scale/bias blocks that are not 16-byte aligned: plain loads
     const int n_sb = rows * a.G;
-    for (int i = tid; i < n_sb; i += TMA_WARPS * 32) {
+    for (int i = tid; i < n_sb; i += NT) {
       const size_t gi = (size_t)r_begin * a.G + i;
 #pragma unroll
       for (int m = 0; m < NW; ++m) {
@@ -219,8 +214,6 @@ __global__ void __launch_bounds__(TMA_WARPS * 32, 1) gemv_tma_kernel(const TmaAr
       }
     }
   }
-  if (a.P > 1)
-    for (int i = tid; i < rows; i += TMA_WARPS * 32) cnt[i] = 0;
 
   pdl_wait();  // x, the residual and the output buffer follow the preceding kernel
   if (tid == 0) {
@@ -231,7 +224,7 @@ __global__ void __launch_bounds__(TMA_WARPS * 32, 1) gemv_tma_kernel(const TmaAr
     abort_flag = 1;
     atomicExch(a.err, (int)MT_ERR_TIMEOUT);
   }
-  for (int i = tid; i < a.K / 8; i += TMA_WARPS * 32) {
+  for (int i = tid; i < a.K / 8; i += NT) {
     const uint4 v = *reinterpret_cast<const uint4*>(xraw + (size_t)i * 8);
     const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
     float* xf = reinterpret_cast<float*>(xt);
@@ -245,7 +238,7 @@ __global__ void __launch_bounds__(TMA_WARPS * 32, 1) gemv_tma_kernel(const TmaAr
   if constexpr (AFF) {
     // X_g = sum of x over group g (one warp per group)
     const float* xf = reinterpret_cast<const float*>(xt);
-    for (int g = warp; g < a.G; g += TMA_WARPS) {
+    for (int g = warp; g < a.G; g += WARP_TASK_WARPS) {
       float sum = 0.f;
       for (int e = lane; e < a.group; e += 32) sum += xf[xt_index<EPC>(g * a.group + e, a.CPR)];
 #pragma unroll
@@ -259,130 +252,102 @@ __global__ void __launch_bounds__(TMA_WARPS * 32, 1) gemv_tma_kernel(const TmaAr
     __syncthreads();
   }
 
-  for (int i = 0; i < my_n; ++i) {
-    if (abort_flag) break;
-    const int slot = warp * D + i % D;
-    if (!mbar_wait_bounded(full0 + 8 * slot, (i / D) & 1)) {
-      abort_flag = 1;
-      atomicExch(a.err, (int)MT_ERR_TIMEOUT);
-      break;
-    }
-    const int t = warp + i * TMA_WARPS;
-    const int rg = t / a.P, p = t - rg * a.P;
-    const int rl0 = rg * R;
-    const unsigned char* sl = ring + (size_t)slot * a.slot_bytes;
-    float2 acc[V];
+  // computes task t from the weights in buf and stores its partial sums
+  auto compute_task = [&](int t, const uint4 (&buf)[NW][CL]) {
+    const int rl = t / a.P, p = t - rl * a.P;
+    float2 acc[NW];
 #pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] = make_float2(0.f, 0.f);
-
-    for (int j = lane; j < a.CPP; j += 32) {
-      const int c = p * a.CPP + j;
-      const int gi = AFF ? (c * EPC) >> a.lg_group : 0;
+    for (int m = 0; m < NW; ++m) acc[m] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int ii = 0; ii < R; ++ii) {
-        if (rl0 + ii >= rows) break;
+    for (int k = 0; k < CL; ++k) {
+      const int j = lane + 32 * k;
+      if (j < a.CPP) {
+        const int c = p * a.CPP + j;
 #pragma unroll
         for (int m = 0; m < NW; ++m) {
-          const uint4 w = *reinterpret_cast<const uint4*>(sl + (ii * NW + m) * a.B + j * 16);
-          const float2 d = chunk_dot<FMT>(w, xt, c, a.CPR);
+          const float2 d = chunk_dot<FMT>(buf[m][k], xt, c, a.CPR);
           if constexpr (AFF) {
-            const float sc = bf16f(sbr[(size_t)(2 * m) * a.sb_stride + (rl0 + ii) * a.G + gi]);
-            acc[ii * NW + m] = __ffma2_rn(make_float2(sc, sc), d, acc[ii * NW + m]);
+            const int gi = (c * EPC) >> a.lg_group;
+            const float sc = bf16f(sbr[(size_t)(2 * m) * a.sb_stride + rl * a.G + gi]);
+            acc[m] = __ffma2_rn(make_float2(sc, sc), d, acc[m]);
           } else {
-            acc[ii * NW + m] = __fadd2_rn(acc[ii * NW + m], d);
+            acc[m] = __fadd2_rn(acc[m], d);
           }
         }
       }
     }
-    __syncwarp();
-    if (lane == 0 && i + D < my_n && !abort_flag) {
-      // every lane has finished reading the slot: refill it (async proxy)
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(i + D);
-      issued = i + D + 1;
-    }
-
-    float vals[V];
+    float vals[NW];
 #pragma unroll
-    for (int v = 0; v < V; ++v) vals[v] = acc[v].x + acc[v].y;
+    for (int m = 0; m < NW; ++m) vals[m] = acc[m].x + acc[m].y;
     if constexpr (AFF) {
       // bias terms of the groups in this piece: sum_g b_g * X_g
       for (int gl = lane; gl < a.GPP; gl += 32) {
         const int g = p * a.GPP + gl;
         const float xg = gsum[g];
 #pragma unroll
-        for (int ii = 0; ii < R; ++ii) {
-          if (rl0 + ii >= rows) break;
-#pragma unroll
-          for (int m = 0; m < NW; ++m)
-            vals[ii * NW + m] =
-                fmaf(bf16f(sbr[(size_t)(2 * m + 1) * a.sb_stride + (rl0 + ii) * a.G + g]), xg,
-                     vals[ii * NW + m]);
-        }
+        for (int m = 0; m < NW; ++m)
+          vals[m] = fmaf(bf16f(sbr[(size_t)(2 * m + 1) * a.sb_stride + rl * a.G + g]), xg, vals[m]);
       }
     }
 #pragma unroll
-    for (int v = 0; v < V; ++v)
+    for (int m = 0; m < NW; ++m)
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) vals[v] += __shfl_xor_sync(0xffffffffu, vals[v], off);
+      for (int off = 16; off > 0; off >>= 1) vals[m] += __shfl_xor_sync(0xffffffffu, vals[m], off);
+    if (lane < NW) {
+      float v = vals[0];
+#pragma unroll
+      for (int m = 1; m < NW; ++m)
+        if (lane == m) v = vals[m];
+      parts[((size_t)rl * a.P + p) * NW + lane] = v;
+    }
+  };
 
-    // lane ii finishes row ii of the task
-    if (lane < R && rl0 + lane < rows) {
-      const int rl = rl0 + lane;
-      float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-      for (int ii = 0; ii < R; ++ii)
-        if (ii == lane) {
-          v0 = vals[ii * NW];
-          if (NW == 2) v1 = vals[ii * NW + NW - 1];
-        }
-      bool finish = true;
-      if (a.P > 1) {
-        parts[((size_t)rl * a.P + p) * NW] = v0;
-        if (NW == 2) parts[((size_t)rl * a.P + p) * NW + 1] = v1;
-        __threadfence_block();
-        finish = atomicAdd(&cnt[rl], 1) == a.P - 1;
-        if (finish) {
-          __threadfence_block();
-          v0 = 0.f;
-          v1 = 0.f;
-          for (int q = 0; q < a.P; ++q) {  // fixed order: deterministic
-            v0 += parts[((size_t)rl * a.P + q) * NW];
-            if (NW == 2) v1 += parts[((size_t)rl * a.P + q) * NW + 1];
-          }
-        }
-      }
-      if (finish) {
-        const int n = r_begin + rl;
-        float outv;
-        if constexpr (KIND == 0) {
-          outv = v0 / (1.0f + expf(-v0)) * v1;  // silu(gate) * up
-        } else {
-          outv = v0 + bf16f(a.res[n]);  // + residual
-        }
-        if (a.out_f32)
-          static_cast<float*>(a.out)[n] = outv;
-        else
-          static_cast<uint16_t*>(a.out)[n] = f2bf(outv);
-      }
+  if (!abort_flag) {
+    // register ping-pong: the next task's loads are in flight while the
+    // current one is computed; two tasks per iteration keep indices static
+    while (tA < T_tasks) {
+      const int tB = next_task();
+      load_task(tB, bufB);
+      compute_task(tA, bufA);
+      if (tB >= T_tasks) break;
+      tA = next_task();
+      load_task(tA, bufA);
+      compute_task(tB, bufB);
     }
   }
-  // never leave the CTA with copies in flight (only matters after a timeout)
-  if (lane == 0) {
-    for (int i = max(0, issued - D); i < issued; ++i)
-      (void)mbar_wait_bounded(full0 + 8 * (warp * D + i % D), (i / D) & 1);
+  __syncthreads();
+
+  // epilogue: one thread per row adds the pieces in a fixed order
+  for (int rl = tid; rl < rows; rl += NT) {
+    float v0 = 0.f, v1 = 0.f;
+    for (int q = 0; q < a.P; ++q) {
+      v0 += parts[((size_t)rl * a.P + q) * NW];
+      if (NW == 2) v1 += parts[((size_t)rl * a.P + q) * NW + 1];
+    }
+    const int n = r_begin + rl;
+    float outv;
+    if constexpr (KIND == 0) {
+      outv = v0 / (1.0f + expf(-v0)) * v1;  // silu(gate) * up
+    } else {
+      outv = v0 + bf16f(a.res[n]);  // + residual
+    }
+    if (a.out_f32)
+      static_cast<float*>(a.out)[n] = outv;
+    else
+      static_cast<uint16_t*>(a.out)[n] = f2bf(outv);
   }
 }
 
-// Host plan and launch of the TMA pipeline for one (format, kind, rows per
-// task).  Returns MT_ERR_SHAPE when the problem does not fit its shared
-// memory layout (the caller then uses the register-pipelined kernel).
-template <int FMT, int KIND, int R>
-mt_status run_gemv_tma(const GemvProblem& p, const Launch& l) {
+// Host plan and launch of the warp-task kernel for one (format, kind).
+// Returns MT_ERR_SHAPE when the problem does not fit its shared-memory
+// layout (the caller then uses the team kernel).
+template <int FMT, int KIND>
+mt_status run_gemv_warp(const GemvProblem& p, const Launch& l) {
   using T = FmtTraits<FMT>;
   constexpr int EPC = T::EPC;
   constexpr bool AFF = T::AFFINE;
   constexpr int NW = KIND == 0 ? 2 : 1;
+  constexpr int CL = WARP_TASK_UPL / NW;
   if (p.M != 1) return MT_ERR_SHAPE;
   static OccCache cache;  // only the attribute flags are used
   int dev = 0;
@@ -392,7 +357,7 @@ mt_status run_gemv_tma(const GemvProblem& p, const Launch& l) {
   const DeviceInfo* di = device_info(&derr);
   if (!di) return cuda_fail((cudaError_t)derr);
 
-  TmaArgs a = {};
+  WarpArgs a = {};
   a.x = p.x;
   a.W0 = static_cast<const uint8_t*>(p.W0);
   a.W1 = static_cast<const uint8_t*>(p.W1);
@@ -409,21 +374,19 @@ mt_status run_gemv_tma(const GemvProblem& p, const Launch& l) {
   if (!a.err) return cuda_fail(cudaErrorInvalidSymbol);
   a.CPR = p.K / EPC;
 
-  // Pieces per row: the fewest that keep a task's slot (R rows x NW
-  // matrices x one piece) at <= 4 KB, dividing both the row's chunks and
-  // (affine) its groups, so a piece holds whole groups.
-  const int max_piece = 4096 / (R * NW);
-  int P = 1;
+  // Pieces per row: the fewest whose chunks fit the lanes' register buffer
+  // (32 * CL chunks per matrix), dividing the row's chunks and (affine) its
+  // groups, so a piece holds whole groups.
+  int P = 0;
   for (int q = 1; q <= a.CPR; ++q) {
     if (a.CPR % q || (AFF && a.G % q)) continue;
-    P = q;
-    if (a.row_bytes / q <= max_piece) break;
+    if (a.CPR / q <= 32 * CL) { P = q; break; }
   }
+  if (P == 0) return MT_ERR_SHAPE;
   a.P = P;
   a.B = a.row_bytes / P;
   a.CPP = a.CPR / P;
   a.GPP = AFF ? a.G / P : 0;
-  a.slot_bytes = R * NW * a.B;
 
   const int N = p.N;
   int grid = di->sm_count;
@@ -431,37 +394,27 @@ mt_status run_gemv_tma(const GemvProblem& p, const Launch& l) {
   a.rows_base = N / grid;
   a.rows_extra = N % grid;
   const int rows_max = a.rows_base + (a.rows_extra ? 1 : 0);
-  a.rows_alloc = (rows_max + R - 1) / R * R;
+  a.rows_alloc = rows_max;
   a.sb_stride = AFF ? (a.rows_alloc * a.G + 7) / 8 * 8 : 0;
   a.sb_tma = (AFF && a.G % 8 == 0) ? 1 : 0;
 
-  const size_t fixed = (size_t)p.K * 2 + (size_t)p.K * 4 +
-                       (AFF ? (size_t)(a.G + 3) / 4 * 16 + (size_t)2 * NW * a.sb_stride * 2 : 0) +
-                       (P > 1 ? (size_t)a.rows_alloc * P * NW * 4 + (size_t)a.rows_alloc * 4 : 0);
+  const size_t smem = 128 + (size_t)p.K * 2 + (size_t)p.K * 4 +
+                      (AFF ? (size_t)(a.G + 3) / 4 * 16 + (size_t)2 * NW * a.sb_stride * 2 : 0) +
+                      (size_t)a.rows_alloc * P * NW * 4;
   const size_t budget = (size_t)di->max_smem_optin - 1024;  // static smem and slack
-  const size_t bars_max = ((size_t)8 * (TMA_WARPS * 8 + 2) + 127) / 128 * 128;
-  if (fixed + bars_max + (size_t)2 * TMA_WARPS * a.slot_bytes > budget) return MT_ERR_SHAPE;
-  int D = (int)((budget - fixed - bars_max) / ((size_t)TMA_WARPS * a.slot_bytes));
-  if (D > 8) D = 8;
-  if (D < 2) return MT_ERR_SHAPE;
-  a.D = D;
-  const int S = TMA_WARPS * D;
-  const size_t bar_bytes = ((size_t)8 * (S + 2) + 127) / 128 * 128;
-  const size_t smem = bar_bytes + (size_t)S * a.slot_bytes + fixed;
   if (smem > budget) return MT_ERR_SHAPE;
 
-  auto kern = gemv_tma_kernel<FMT, KIND, R>;
+  auto kern = gemv_warp_kernel<FMT, KIND>;
   {
     std::lock_guard<std::mutex> g(cache.mu);
     if (dev < 64 && !cache.attr_set[dev]) {
-      // dynamic + static shared memory must stay within the opt-in limit
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)budget);
       if (e != cudaSuccess) return cuda_fail(e);
       cache.attr_set[dev] = 1;
     }
   }
-  return launch(kern, dim3(grid), dim3(TMA_WARPS * 32), smem, l, a);
+  return launch(kern, dim3(grid), dim3(WARP_TASK_WARPS * 32), smem, l, a);
 }
 
 }  // namespace mt

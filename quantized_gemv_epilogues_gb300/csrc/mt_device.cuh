@@ -28,6 +28,17 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   return v;
 }
 
+// 128-bit streaming load with an explicit L2 eviction policy (from
+// createpolicy), no L1 allocation.
+__device__ __forceinline__ uint4 ldg_stream_pol(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p), "l"(pol));
+  return v;
+}
+
 __device__ __forceinline__ uint4 ldg_nc(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -27,11 +27,11 @@ def mt():
     return m
 
 
-@pytest.fixture(params=["tma", "regs"])
+@pytest.fixture(params=["warp", "team"])
 def gemv(request, mt):
-    """Runs a test with each one-row GEMV kernel (TMA pipeline / register
-    pipeline); M > 1 always uses the register kernel."""
-    mt.mt_set_option(mt.MT_OPT_GEMV, 0 if request.param == "tma" else 1)
+    """Runs a test with each one-row GEMV kernel (warp-task / team kernel);
+    M > 1 always uses the team kernel."""
+    mt.mt_set_option(mt.MT_OPT_GEMV, 0 if request.param == "warp" else 1)
     yield request.param
     mt.mt_set_option(mt.MT_OPT_GEMV, 0)
     assert mt.mt_device_error(clear=True) == 0, "a bounded device wait expired"

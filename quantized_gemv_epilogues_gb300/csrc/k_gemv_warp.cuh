@@ -11,16 +11,20 @@
 //    rows.  The range is cut into tasks of one row piece (B bytes of each of
 //    the NW weight matrices), handed out dynamically through a shared-memory
 //    counter, so warps finish within about one task of each other.
-//  * A warp streams its next task's weights into registers with 128-bit
-//    evict-first loads while it computes the current one (register double
-//    buffer, up to 8 x 16 B per lane per task): ~128 KB in flight per SM
-//    with no per-copy issue cost.  (Bulk TMA copies cost the issuing thread
-//    ~350 cycles each on this part, which capped a TMA-ring design near
-//    3.5 TB/s for 2-4 KB pieces.)  The first task is requested before
-//    waiting on the preceding kernel (programmatic dependent launch).
+//  * A warp holds a small queue of task ids: the lines of the tasks two and
+//    three ahead are prefetched into L2 (one prefetch per lane), the next
+//    task's weights are loaded into registers with 128-bit evict-first loads
+//    while the current one is computed (register double buffer, up to 8 x
+//    16 B per lane per task).  HBM sees ~200 KB in flight per SM while the
+//    register pipeline only has to cover L2 latency, with no per-copy issue
+//    cost (bulk TMA copies cost the issuing thread ~350 cycles each on this
+//    part, which capped a TMA-ring design near 3.5 TB/s for 2-4 KB pieces).
+//    The first tasks are requested before waiting on the preceding kernel
+//    (programmatic dependent launch).
 //  * x (fp32, unit-transposed: 16-byte unit k of chunk c at index k*CPR + c,
 //    so the lanes of a warp read consecutive words) and the CTA's scales and
-//    biases (bf16) are staged once in shared memory with TMA bulk copies.
+//    biases (bf16) are staged once in shared memory with cp.async 16-byte
+//    copies issued by every thread.
 //  * The affine term is factored as
 //      sum_k (s q_k + b) x_k = sum_chunks s * (sum q_k x_k) + sum_groups b * X_g
 //    with X_g the sum of x over group g: per weight one byte permute
@@ -29,8 +33,8 @@
 //  * A task's partial sums are reduced inside the warp (shuffles) and stored
 //    per piece in shared memory; after one barrier, one thread per row adds
 //    the pieces in a fixed order (deterministic) and runs the epilogue.
-//  * The staging waits are bounded (~1 s); on expiry the kernel records
-//    MT_ERR_TIMEOUT in a device error word and skips its main loop.
+//  * No thread waits on another CTA or on a flag: the only waits are
+//    cp.async group completions and CTA barriers.
 #pragma once
 #include "k_gemv.cuh"
 
@@ -60,9 +64,8 @@ struct WarpArgs {
   int GPP;                 // groups per piece (affine)
   int rows_alloc;          // rows of the staged arrays
   int sb_stride;           // elements per staged scale or bias array (multiple of 8)
-  int sb_tma;              // 1: scales/biases are bulk-copied (G % 8 == 0)
+  int sb_vec;              // 1: scales/biases are staged in 16-byte copies (G % 8 == 0)
   int out_f32;
-  int* err;                // device error word
 };
 
 // Float index of element e of x in the unit-transposed staging layout.
@@ -135,31 +138,21 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
   constexpr int NT = WARP_TASK_WARPS * 32;
 
   extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);            // x, sb
-  uint16_t* xraw = reinterpret_cast<uint16_t*>(smem + 128);       // [K] bf16
+  uint16_t* xraw = reinterpret_cast<uint16_t*>(smem);             // [K] bf16
   float4* xt = reinterpret_cast<float4*>(xraw + a.K);             // [K/4]
   float* gsum = reinterpret_cast<float*>(xt + a.K / 4);           // [G]
   uint16_t* sbr = reinterpret_cast<uint16_t*>(gsum + (AFF ? (a.G + 3) / 4 * 4 : 0));
   // sbr: 2*NW arrays of sb_stride bf16: 2m = scales, 2m+1 = biases of matrix m
   float* parts = reinterpret_cast<float*>(sbr + (AFF ? (size_t)2 * NW * a.sb_stride : 0));  // [rows][P][NW]
   __shared__ int task_ctr;
-  __shared__ volatile int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
   const int r_begin = cta * a.rows_base + min(cta, a.rows_extra);
   const int rows = a.rows_base + (cta < a.rows_extra ? 1 : 0);
   const int T_tasks = rows * a.P;
-  const uint32_t bar_x = smem_u32(bars), bar_sb = smem_u32(bars + 1);
-  const bool sb_tma = AFF && a.sb_tma;
 
-  if (tid == 0) {
-    abort_flag = 0;
-    task_ctr = WARP_TASK_WARPS;  // tasks 0..W-1 are taken statically below
-    mbar_init(bar_x, 1);
-    mbar_init(bar_sb, 1);
-    mbar_fence_init();
-  }
+  if (tid == 0) task_ctr = WARP_TASK_WARPS;  // tasks 0..W-1 are taken statically
   __syncthreads();
   pdl_trigger();
 
@@ -177,53 +170,63 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
                                       : make_uint4(0, 0, 0, 0);
       }
   };
+  // one L2 prefetch per lane per 128-byte line of task t
+  const int lines_pm = (a.B + 127) >> 7;
+  auto prefetch_task = [&](int t) {
+    if (t >= T_tasks) return;
+    const int rl = t / a.P, p = t - rl * a.P;
+    const size_t base = (size_t)(r_begin + rl) * a.row_bytes + (size_t)p * a.B;
+    for (int li = lane; li < NW * lines_pm; li += 32) {
+      const int m = li / lines_pm;
+      prefetch_l2((m ? a.W1 : a.W0) + base + (size_t)(li - m * lines_pm) * 128);
+    }
+  };
   auto next_task = [&]() -> int {
     int t = 0;
     if (lane == 0) t = atomicAdd(&task_ctr, 1);
     return __shfl_sync(0xffffffffu, t, 0);
   };
 
-  // first task of each warp: static weights, requested before the wait
+  // the first tasks: static weights, requested before the wait
   uint4 bufA[NW][CL], bufB[NW][CL];
-  int tA = warp;
-  load_task(tA, bufA);
+  int tc = warp;
+  load_task(tc, bufA);
+  int tl = next_task(), tp1 = next_task(), tp2 = next_task();
+  prefetch_task(tl);
+  prefetch_task(tp1);
+  prefetch_task(tp2);
 
-  if (tid == 0 && sb_tma) {
-    // the CTA's scales and biases: contiguous [rows][G] blocks
-    const uint64_t keep = l2_evict_last_policy();
-    const uint32_t bytes = (uint32_t)(rows * a.G * 2);
-    const size_t off = (size_t)r_begin * a.G;
-    mbar_arrive_expect_tx(bar_sb, (uint32_t)(2 * NW) * bytes);
+  if constexpr (AFF) {
+    // the CTA's scales and biases (contiguous [rows][G] blocks)
+    if (a.sb_vec) {
+      const int n16 = rows * a.G / 8;
+      const size_t off = (size_t)r_begin * a.G;
+      for (int i = tid; i < n16; i += NT) {
 #pragma unroll
-    for (int m = 0; m < NW; ++m) {
-      bulk_g2s(smem_u32(sbr + (size_t)(2 * m) * a.sb_stride), (m ? a.s1 : a.s0) + off, bytes,
-               bar_sb, keep);
-      bulk_g2s(smem_u32(sbr + (size_t)(2 * m + 1) * a.sb_stride), (m ? a.b1 : a.b0) + off, bytes,
-               bar_sb, keep);
-    }
-  }
-  if (AFF && !sb_tma) {
-    // scale/bias blocks that are not 16-byte aligned: plain loads
-    const int n_sb = rows * a.G;
-    for (int i = tid; i < n_sb; i += NT) {
-      const size_t gi = (size_t)r_begin * a.G + i;
+        for (int m = 0; m < NW; ++m) {
+          cp_async16(sbr + (size_t)(2 * m) * a.sb_stride + i * 8, (m ? a.s1 : a.s0) + off + i * 8);
+          cp_async16(sbr + (size_t)(2 * m + 1) * a.sb_stride + i * 8, (m ? a.b1 : a.b0) + off + i * 8);
+        }
+      }
+      cp_async_commit();
+    } else {
+      const int n_sb = rows * a.G;
+      for (int i = tid; i < n_sb; i += NT) {
+        const size_t gi = (size_t)r_begin * a.G + i;
 #pragma unroll
-      for (int m = 0; m < NW; ++m) {
-        sbr[(size_t)(2 * m) * a.sb_stride + i] = ldg_u16((m ? a.s1 : a.s0) + gi);
-        sbr[(size_t)(2 * m + 1) * a.sb_stride + i] = ldg_u16((m ? a.b1 : a.b0) + gi);
+        for (int m = 0; m < NW; ++m) {
+          sbr[(size_t)(2 * m) * a.sb_stride + i] = ldg_u16((m ? a.s1 : a.s0) + gi);
+          sbr[(size_t)(2 * m + 1) * a.sb_stride + i] = ldg_u16((m ? a.b1 : a.b0) + gi);
+        }
       }
     }
   }
 
   pdl_wait();  // x, the residual and the output buffer follow the preceding kernel
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar_x, (uint32_t)(a.K * 2));
-    bulk_g2s(smem_u32(xraw), a.x, (uint32_t)(a.K * 2), bar_x, l2_evict_last_policy());
-  }
-  if (!mbar_wait_bounded(bar_x, 0)) {
-    abort_flag = 1;
-    atomicExch(a.err, (int)MT_ERR_TIMEOUT);
-  }
+  for (int i = tid; i < a.K / 8; i += NT) cp_async16(xraw + (size_t)i * 8, a.x + (size_t)i * 8);
+  cp_async_commit();
+  cp_async_wait_all();
+  __syncthreads();
   for (int i = tid; i < a.K / 8; i += NT) {
     const uint4 v = *reinterpret_cast<const uint4*>(xraw + (size_t)i * 8);
     const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
@@ -244,10 +247,6 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
       if (lane == 0) gsum[g] = sum;
-    }
-    if (sb_tma && !mbar_wait_bounded(bar_sb, 0)) {
-      abort_flag = 1;
-      atomicExch(a.err, (int)MT_ERR_TIMEOUT);
     }
     __syncthreads();
   }
@@ -302,18 +301,18 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
     }
   };
 
-  if (!abort_flag) {
-    // register ping-pong: the next task's loads are in flight while the
-    // current one is computed; two tasks per iteration keep indices static
-    while (tA < T_tasks) {
-      const int tB = next_task();
-      load_task(tB, bufB);
-      compute_task(tA, bufA);
-      if (tB >= T_tasks) break;
-      tA = next_task();
-      load_task(tA, bufA);
-      compute_task(tB, bufB);
-    }
+  // register ping-pong: the next task's loads are in flight while the
+  // current one is computed; two tasks per iteration keep indices static
+  while (tc < T_tasks) {
+    load_task(tl, bufB);
+    compute_task(tc, bufA);
+    tc = tl; tl = tp1; tp1 = tp2; tp2 = next_task();
+    prefetch_task(tp2);
+    if (tc >= T_tasks) break;
+    load_task(tl, bufA);
+    compute_task(tc, bufB);
+    tc = tl; tl = tp1; tp1 = tp2; tp2 = next_task();
+    prefetch_task(tp2);
   }
   __syncthreads();
 
@@ -370,8 +369,6 @@ mt_status run_gemv_warp(const GemvProblem& p, const Launch& l) {
   a.G = AFF ? p.K / p.group : 0;
   a.row_bytes = FMT == FMT_BF16 ? p.K * 2 : (FMT == FMT_A8 ? p.K : p.K / 2);
   a.out_f32 = p.out_f32 ? 1 : 0;
-  a.err = device_error_ptr();
-  if (!a.err) return cuda_fail(cudaErrorInvalidSymbol);
   a.CPR = p.K / EPC;
 
   // Pieces per row: the fewest whose chunks fit the lanes' register buffer
@@ -396,9 +393,9 @@ mt_status run_gemv_warp(const GemvProblem& p, const Launch& l) {
   const int rows_max = a.rows_base + (a.rows_extra ? 1 : 0);
   a.rows_alloc = rows_max;
   a.sb_stride = AFF ? (a.rows_alloc * a.G + 7) / 8 * 8 : 0;
-  a.sb_tma = (AFF && a.G % 8 == 0) ? 1 : 0;
+  a.sb_vec = (AFF && a.G % 8 == 0) ? 1 : 0;
 
-  const size_t smem = 128 + (size_t)p.K * 2 + (size_t)p.K * 4 +
+  const size_t smem = (size_t)p.K * 2 + (size_t)p.K * 4 +
                       (AFF ? (size_t)(a.G + 3) / 4 * 16 + (size_t)2 * NW * a.sb_stride * 2 : 0) +
                       (size_t)a.rows_alloc * P * NW * 4;
   const size_t budget = (size_t)di->max_smem_optin - 1024;  // static smem and slack

@@ -100,7 +100,8 @@ mt_status run_gemv(const GemvProblem& p, const Launch& l) {
   const size_t budget = (size_t)di->max_smem_optin;
   if (base_smem + sb_row_bytes * (size_t)((rows_per + R - 1) / R * R) > budget) {
     if (sb_row_bytes == 0 || base_smem + sb_row_bytes * R > budget) return MT_ERR_SHAPE;
-    const int cap = (int)((budget - base_smem) / sb_row_bytes) / R * R;
+    const size_t per_row = sb_row_bytes ? sb_row_bytes : 1;  // nonzero here
+    const int cap = (int)((budget - base_smem) / per_row) / R * R;
     grid = (N + cap - 1) / cap;
     rows_per = (N + grid - 1) / grid;
   }

@@ -11,25 +11,28 @@
 //    rows.  The range is cut into tasks of one row piece (B bytes of each of
 //    the NW weight matrices), handed out dynamically through a shared-memory
 //    counter, so warps finish within about one task of each other.
-//  * A warp holds a small queue of task ids: the lines of the tasks two and
-//    three ahead are prefetched into L2 (one prefetch per lane), the next
-//    task's weights are loaded into registers with 128-bit evict-first loads
-//    while the current one is computed (register double buffer, up to 8 x
-//    16 B per lane per task).  HBM sees ~200 KB in flight per SM while the
-//    register pipeline only has to cover L2 latency, with no per-copy issue
-//    cost (bulk TMA copies cost the issuing thread ~350 cycles each on this
-//    part, which capped a TMA-ring design near 3.5 TB/s for 2-4 KB pieces).
-//    The first tasks are requested before waiting on the preceding kernel
-//    (programmatic dependent launch).
-//  * x (fp32, unit-transposed: 16-byte unit k of chunk c at index k*CPR + c,
-//    so the lanes of a warp read consecutive words) and the CTA's scales and
-//    biases (bf16) are staged once in shared memory with cp.async 16-byte
-//    copies issued by every thread.
+//  * A warp loads its next task's weights into registers with 128-bit
+//    evict-first loads while it computes the current one (register double
+//    buffer, up to 8 x 16 B per lane per task), ~64-128 KB in flight per SM
+//    with no per-copy issue cost.  (Bulk TMA copies cost the issuing thread
+//    ~350 cycles each on this part, which capped a TMA-ring design near
+//    3.5 TB/s for 2-4 KB pieces.)  The first task is requested before
+//    waiting on the preceding kernel (programmatic dependent launch).
+//  * The CTA's scales and biases (bf16) and x are staged once in shared
+//    memory with cp.async 16-byte copies issued by every thread.  x is then
+//    laid out unit-transposed (the x words of chunk c for word k at index
+//    k*CPR + c) so the lanes of a warp read consecutive words.
 //  * The affine term is factored as
 //      sum_k (s q_k + b) x_k = sum_chunks s * (sum q_k x_k) + sum_groups b * X_g
-//    with X_g the sum of x over group g: per weight one byte permute
-//    (exponent-bias conversion), half a packed fp32x2 add and half a packed
-//    fp32x2 FMA.
+//    with X_g the sum of x over group g (fp32, from the bf16 values).  The
+//    codes are turned into fp16 with the exponent-bias trick (a byte permute
+//    or a mask builds 1024 + q, one packed fp16 subtract leaves q exactly),
+//    and each product q * x is one mixed-precision FMA (fp16 x fp16, exact
+//    product, fp32 accumulation).  x enters that FMA as fp16 after an exact
+//    power-of-two scaling chosen per CTA from max|x| (so nothing overflows;
+//    only elements below ~2^-24 of the scaled maximum lose bits); the scale is
+//    divided out of the partial sums.  Dense bf16 weights use the bf16 form of
+//    the same FMA with x unchanged.  About two instructions per weight.
 //  * A task's partial sums are reduced inside the warp (shuffles) and stored
 //    per piece in shared memory; after one barrier, one thread per row adds
 //    the pieces in a fixed order (deterministic) and runs the epilogue.
@@ -59,6 +62,7 @@ struct WarpArgs {
   int row_bytes;           // bytes of one weight row
   int rows_base, rows_extra;
   int P;                   // pieces per row
+  unsigned long long p_mul;  // ceil(2^32 / P): t / P == (t * p_mul) >> 32 for t < 2^32 / P
   int B;                   // bytes per piece (multiple of 16)
   int CPP;                 // 16-byte chunks per piece (<= 32 * UPL / NW)
   int GPP;                 // groups per piece (affine)
@@ -68,64 +72,92 @@ struct WarpArgs {
   int out_f32;
 };
 
-// Float index of element e of x in the unit-transposed staging layout.
-template <int EPC>
-__device__ __forceinline__ int xt_index(int e, int CPR) {
-  const int c = e / EPC;
-  const int k = (e % EPC) >> 2;
-  return (k * CPR + c) * 4 + (e & 3);
+// Position (in 16-bit elements) of element e of x in the staging layout.
+// A8: word wi of chunk c is 4 fp16 (elements 4wi..4wi+3) at unit wi*CPR + c.
+// A4: word wi of chunk c is 8 fp16 at unit wi*CPR + c, in the order
+//     {0,4,1,5,2,6,3,7} that matches the nibble pairs of one weight word.
+// BF16: words 2u, 2u+1 of chunk c read 4 bf16 (elements 4u..4u+3) at unit
+//     u*CPR + c.
+template <int FMT>
+__device__ __forceinline__ int xs_index(int e, int CPR) {
+  using T = FmtTraits<FMT>;
+  const int c = e / T::EPC, r = e % T::EPC;
+  if constexpr (FMT == FMT_A4) {
+    const int wi = r >> 3, t = r & 7;
+    return (wi * CPR + c) * 8 + (t < 4 ? 2 * t : 2 * (t - 4) + 1);
+  } else {
+    return ((r >> 2) * CPR + c) * 4 + (r & 3);
+  }
 }
 
-// Dot product of one 16-byte weight chunk (chunk c of its row) with its EPC
-// activations, as a pair of partial sums (packed fp32x2).
+// acc_lo += lo(a) * lo(b), acc_hi += hi(a) * hi(b): fp16 x fp16 products
+// (exact in fp32) accumulated in fp32.
+__device__ __forceinline__ void fma2_f16_f32(float& lo, float& hi, uint32_t a, uint32_t b) {
+  asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+      "mov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+      "fma.rn.f32.f16 %0, a0, b0, %0;\n\tfma.rn.f32.f16 %1, a1, b1, %1;\n\t}"
+      : "+f"(lo), "+f"(hi)
+      : "r"(a), "r"(b));
+}
+
+// The same with bf16 operands (exact products in fp32).
+__device__ __forceinline__ void fma2_bf16_f32(float& lo, float& hi, uint32_t a, uint32_t b) {
+  asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"
+      "mov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t}"
+      : "+f"(lo), "+f"(hi)
+      : "r"(a), "r"(b));
+}
+
+// Two fp16 codes 1024 + q (built with the exponent-bias trick) -> q, exactly.
+__device__ __forceinline__ uint32_t unbias_f16x2(uint32_t h) {
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(h) : "r"(0x64006400u));
+  return h;
+}
+
+// Dot product of one 16-byte weight chunk (chunk c of its row) with its
+// activations from the staging layout: sum of q * x (affine, x scaled) or of
+// w * x (bf16).
 template <int FMT>
-__device__ __forceinline__ float2 chunk_dot(const uint4 w, const float4* __restrict__ xt, int c,
-                                            int CPR) {
-  const float2 neg = make_float2(-8388608.0f, -8388608.0f);
-  float2 d0 = make_float2(0.f, 0.f), d1 = make_float2(0.f, 0.f);
+__device__ __forceinline__ float chunk_dot(const uint4 w, const uint16_t* __restrict__ xs, int c,
+                                           int CPR) {
   const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   if constexpr (FMT == FMT_A8) {
-    // word wi holds elements 4wi..4wi+3, one byte each
+    const uint2* xu = reinterpret_cast<const uint2*>(xs);
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
-      const float4 xv = xt[wi * CPR + c];
-      const float2 qa = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(ww[wi], 0x4B000000u, 0x7540u)),
-                                               __uint_as_float(__byte_perm(ww[wi], 0x4B000000u, 0x7541u))), neg);
-      const float2 qb = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(ww[wi], 0x4B000000u, 0x7542u)),
-                                               __uint_as_float(__byte_perm(ww[wi], 0x4B000000u, 0x7543u))), neg);
-      d0 = __ffma2_rn(qa, make_float2(xv.x, xv.y), d0);
-      d1 = __ffma2_rn(qb, make_float2(xv.z, xv.w), d1);
+      const uint2 xv = xu[wi * CPR + c];
+      const uint32_t h01 = unbias_f16x2(__byte_perm(ww[wi], 0x64646464u, 0x5140u));
+      const uint32_t h23 = unbias_f16x2(__byte_perm(ww[wi], 0x64646464u, 0x7342u));
+      fma2_f16_f32(a0, a1, h01, xv.x);
+      fma2_f16_f32(a2, a3, h23, xv.y);
     }
   } else if constexpr (FMT == FMT_A4) {
-    // word wi holds elements 8wi..8wi+7: byte j = (2j low nibble, 2j+1 high)
+    const uint4* xu = reinterpret_cast<const uint4*>(xs);
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
-      const uint32_t lo = ww[wi] & 0x0F0F0F0Fu, hi = (ww[wi] >> 4) & 0x0F0F0F0Fu;
-      const float4 xa = xt[(2 * wi) * CPR + c];      // elements 8wi .. 8wi+3
-      const float4 xb = xt[(2 * wi + 1) * CPR + c];  // elements 8wi+4 .. 8wi+7
-      const float2 q01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7540u)),
-                                                __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7540u))), neg);
-      const float2 q23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7541u)),
-                                                __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7541u))), neg);
-      const float2 q45 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7542u)),
-                                                __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7542u))), neg);
-      const float2 q67 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7543u)),
-                                                __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7543u))), neg);
-      d0 = __ffma2_rn(q01, make_float2(xa.x, xa.y), d0);
-      d1 = __ffma2_rn(q23, make_float2(xa.z, xa.w), d1);
-      d0 = __ffma2_rn(q45, make_float2(xb.x, xb.y), d0);
-      d1 = __ffma2_rn(q67, make_float2(xb.z, xb.w), d1);
+      const uint4 xv = xu[wi * CPR + c];
+      const uint32_t v = ww[wi];
+      const uint32_t p0 = unbias_f16x2((v & 0x000F000Fu) | 0x64006400u);          // q0, q4
+      const uint32_t p1 = unbias_f16x2(((v >> 4) & 0x000F000Fu) | 0x64006400u);   // q1, q5
+      const uint32_t p2 = unbias_f16x2(((v >> 8) & 0x000F000Fu) | 0x64006400u);   // q2, q6
+      const uint32_t p3 = unbias_f16x2(((v >> 12) & 0x000F000Fu) | 0x64006400u);  // q3, q7
+      fma2_f16_f32(a0, a1, p0, xv.x);
+      fma2_f16_f32(a2, a3, p1, xv.y);
+      fma2_f16_f32(a0, a1, p2, xv.z);
+      fma2_f16_f32(a2, a3, p3, xv.w);
     }
   } else {
-    // dense bf16: word wi holds elements 2wi (low half) and 2wi+1 (high half)
+    const uint2* xu = reinterpret_cast<const uint2*>(xs);
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const float4 xv = xt[u * CPR + c];
-      d0 = __ffma2_rn(make_float2(bf16lo(ww[2 * u]), bf16hi(ww[2 * u])), make_float2(xv.x, xv.y), d0);
-      d1 = __ffma2_rn(make_float2(bf16lo(ww[2 * u + 1]), bf16hi(ww[2 * u + 1])), make_float2(xv.z, xv.w), d1);
+      const uint2 xv = xu[u * CPR + c];
+      fma2_bf16_f32(a0, a1, ww[2 * u], xv.x);
+      fma2_bf16_f32(a2, a3, ww[2 * u + 1], xv.y);
     }
   }
-  return __fadd2_rn(d0, d1);
+  return (a0 + a1) + (a2 + a3);
 }
 
 template <int FMT, int KIND>
@@ -139,12 +171,13 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint16_t* xraw = reinterpret_cast<uint16_t*>(smem);             // [K] bf16
-  float4* xt = reinterpret_cast<float4*>(xraw + a.K);             // [K/4]
-  float* gsum = reinterpret_cast<float*>(xt + a.K / 4);           // [G]
+  uint16_t* xs = xraw + a.K;                                      // [K] staging layout
+  float* gsum = reinterpret_cast<float*>(xs + a.K);               // [G]
   uint16_t* sbr = reinterpret_cast<uint16_t*>(gsum + (AFF ? (a.G + 3) / 4 * 4 : 0));
   // sbr: 2*NW arrays of sb_stride bf16: 2m = scales, 2m+1 = biases of matrix m
   float* parts = reinterpret_cast<float*>(sbr + (AFF ? (size_t)2 * NW * a.sb_stride : 0));  // [rows][P][NW]
   __shared__ int task_ctr;
+  __shared__ float red_max[WARP_TASK_WARPS];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
@@ -159,7 +192,8 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
   const uint64_t pol = l2_evict_first_policy();
   auto load_task = [&](int t, uint4 (&buf)[NW][CL]) {
     const bool ok = t < T_tasks;
-    const int rl = ok ? t / a.P : 0, p = ok ? t - rl * a.P : 0;
+    const int q = (int)(((unsigned long long)(unsigned)t * a.p_mul) >> 32);
+    const int rl = ok ? q : 0, p = ok ? t - q * a.P : 0;
     const size_t base = (size_t)(r_begin + rl) * a.row_bytes + (size_t)p * a.B;
 #pragma unroll
     for (int m = 0; m < NW; ++m)
@@ -169,17 +203,6 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
         buf[m][k] = (ok && j < a.CPP) ? ldg_stream_pol((m ? a.W1 : a.W0) + base + (size_t)j * 16, pol)
                                       : make_uint4(0, 0, 0, 0);
       }
-  };
-  // one L2 prefetch per lane per 128-byte line of task t
-  const int lines_pm = (a.B + 127) >> 7;
-  auto prefetch_task = [&](int t) {
-    if (t >= T_tasks) return;
-    const int rl = t / a.P, p = t - rl * a.P;
-    const size_t base = (size_t)(r_begin + rl) * a.row_bytes + (size_t)p * a.B;
-    for (int li = lane; li < NW * lines_pm; li += 32) {
-      const int m = li / lines_pm;
-      prefetch_l2((m ? a.W1 : a.W0) + base + (size_t)(li - m * lines_pm) * 128);
-    }
   };
   auto next_task = [&]() -> int {
     int t = 0;
@@ -191,10 +214,6 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
   uint4 bufA[NW][CL], bufB[NW][CL];
   int tc = warp;
   load_task(tc, bufA);
-  int tl = next_task(), tp1 = next_task(), tp2 = next_task();
-  prefetch_task(tl);
-  prefetch_task(tp1);
-  prefetch_task(tp2);
 
   if constexpr (AFF) {
     // the CTA's scales and biases (contiguous [rows][G] blocks)
@@ -227,36 +246,56 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
   cp_async_commit();
   cp_async_wait_all();
   __syncthreads();
-  for (int i = tid; i < a.K / 8; i += NT) {
-    const uint4 v = *reinterpret_cast<const uint4*>(xraw + (size_t)i * 8);
-    const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-    float* xf = reinterpret_cast<float*>(xt);
+  // x scale (affine): 2^e with max|x| * 2^e in [2^14, 2^15), exact
+  float xscale = 1.f, xinv = 1.f;
+  if constexpr (AFF) {
+    float mx = 0.f;
+    for (int i = tid; i < a.K / 2; i += NT) {
+      const uint32_t v = reinterpret_cast<const uint32_t*>(xraw)[i];
+      mx = fmaxf(mx, fmaxf(fabsf(bf16lo(v)), fabsf(bf16hi(v))));
+    }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      xf[xt_index<EPC>(i * 8 + 2 * j, a.CPR)] = bf16lo(vw[j]);
-      xf[xt_index<EPC>(i * 8 + 2 * j + 1, a.CPR)] = bf16hi(vw[j]);
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red_max[warp] = mx;
+    __syncthreads();
+    mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < WARP_TASK_WARPS; ++w) mx = fmaxf(mx, red_max[w]);
+    if (mx > 0.f && mx < 3.0e38f) {
+      const int ex = max(-126, min(126, 14 - ilogbf(mx)));
+      xscale = ldexpf(1.f, ex);
+      xinv = ldexpf(1.f, -ex);
     }
   }
-  __syncthreads();
+  for (int i = tid; i < a.K / 2; i += NT) {
+    const uint32_t v = reinterpret_cast<const uint32_t*>(xraw)[i];
+    if constexpr (AFF) {
+      xs[xs_index<FMT>(2 * i, a.CPR)] = __half_as_ushort(__float2half_rn(bf16lo(v) * xscale));
+      xs[xs_index<FMT>(2 * i + 1, a.CPR)] = __half_as_ushort(__float2half_rn(bf16hi(v) * xscale));
+    } else {
+      xs[xs_index<FMT>(2 * i, a.CPR)] = (uint16_t)(v & 0xFFFFu);
+      xs[xs_index<FMT>(2 * i + 1, a.CPR)] = (uint16_t)(v >> 16);
+    }
+  }
   if constexpr (AFF) {
-    // X_g = sum of x over group g (one warp per group)
-    const float* xf = reinterpret_cast<const float*>(xt);
+    // X_g = sum of x over group g (fp32, unscaled; one warp per group)
     for (int g = warp; g < a.G; g += WARP_TASK_WARPS) {
       float sum = 0.f;
-      for (int e = lane; e < a.group; e += 32) sum += xf[xt_index<EPC>(g * a.group + e, a.CPR)];
+      for (int e = lane; e < a.group; e += 32) sum += bf16f(xraw[g * a.group + e]);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
       if (lane == 0) gsum[g] = sum;
     }
-    __syncthreads();
   }
+  __syncthreads();
 
   // computes task t from the weights in buf and stores its partial sums
   auto compute_task = [&](int t, const uint4 (&buf)[NW][CL]) {
-    const int rl = t / a.P, p = t - rl * a.P;
-    float2 acc[NW];
+    const int rl = (int)(((unsigned long long)(unsigned)t * a.p_mul) >> 32);
+    const int p = t - rl * a.P;
+    float acc[NW];
 #pragma unroll
-    for (int m = 0; m < NW; ++m) acc[m] = make_float2(0.f, 0.f);
+    for (int m = 0; m < NW; ++m) acc[m] = 0.f;
 #pragma unroll
     for (int k = 0; k < CL; ++k) {
       const int j = lane + 32 * k;
@@ -264,20 +303,19 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
         const int c = p * a.CPP + j;
 #pragma unroll
         for (int m = 0; m < NW; ++m) {
-          const float2 d = chunk_dot<FMT>(buf[m][k], xt, c, a.CPR);
+          const float d = chunk_dot<FMT>(buf[m][k], xs, c, a.CPR);
           if constexpr (AFF) {
             const int gi = (c * EPC) >> a.lg_group;
-            const float sc = bf16f(sbr[(size_t)(2 * m) * a.sb_stride + rl * a.G + gi]);
-            acc[m] = __ffma2_rn(make_float2(sc, sc), d, acc[m]);
+            acc[m] = fmaf(bf16f(sbr[(size_t)(2 * m) * a.sb_stride + rl * a.G + gi]), d, acc[m]);
           } else {
-            acc[m] = __fadd2_rn(acc[m], d);
+            acc[m] += d;
           }
         }
       }
     }
     float vals[NW];
 #pragma unroll
-    for (int m = 0; m < NW; ++m) vals[m] = acc[m].x + acc[m].y;
+    for (int m = 0; m < NW; ++m) vals[m] = acc[m] * xinv;
     if constexpr (AFF) {
       // bias terms of the groups in this piece: sum_g b_g * X_g
       for (int gl = lane; gl < a.GPP; gl += 32) {
@@ -304,15 +342,13 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
   // register ping-pong: the next task's loads are in flight while the
   // current one is computed; two tasks per iteration keep indices static
   while (tc < T_tasks) {
-    load_task(tl, bufB);
+    const int tB = next_task();
+    load_task(tB, bufB);
     compute_task(tc, bufA);
-    tc = tl; tl = tp1; tp1 = tp2; tp2 = next_task();
-    prefetch_task(tp2);
-    if (tc >= T_tasks) break;
-    load_task(tl, bufA);
-    compute_task(tc, bufB);
-    tc = tl; tl = tp1; tp1 = tp2; tp2 = next_task();
-    prefetch_task(tp2);
+    if (tB >= T_tasks) break;
+    tc = next_task();
+    load_task(tc, bufA);
+    compute_task(tB, bufB);
   }
   __syncthreads();
 
@@ -381,6 +417,7 @@ mt_status run_gemv_warp(const GemvProblem& p, const Launch& l) {
   }
   if (P == 0) return MT_ERR_SHAPE;
   a.P = P;
+  a.p_mul = ((1ull << 32) + (unsigned long long)P - 1) / (unsigned long long)P;
   a.B = a.row_bytes / P;
   a.CPP = a.CPR / P;
   a.GPP = AFF ? a.G / P : 0;
@@ -395,7 +432,7 @@ mt_status run_gemv_warp(const GemvProblem& p, const Launch& l) {
   a.sb_stride = AFF ? (a.rows_alloc * a.G + 7) / 8 * 8 : 0;
   a.sb_vec = (AFF && a.G % 8 == 0) ? 1 : 0;
 
-  const size_t smem = (size_t)p.K * 2 + (size_t)p.K * 4 +
+  const size_t smem = (size_t)p.K * 2 + (size_t)p.K * 2 +
                       (AFF ? (size_t)(a.G + 3) / 4 * 16 + (size_t)2 * NW * a.sb_stride * 2 : 0) +
                       (size_t)a.rows_alloc * P * NW * 4;
   const size_t budget = (size_t)di->max_smem_optin - 1024;  // static smem and slack

@@ -1,5 +1,6 @@
 // mt_device.cuh - device helpers shared by the library's kernels (sm_103a).
 #pragma once
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 

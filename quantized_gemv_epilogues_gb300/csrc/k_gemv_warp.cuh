@@ -72,23 +72,12 @@ struct WarpArgs {
   int out_f32;
 };
 
-// Position (in 16-bit elements) of element e of x in the staging layout.
+// Staging layout of x (16-bit elements), read by chunk_dot:
 // A8: word wi of chunk c is 4 fp16 (elements 4wi..4wi+3) at unit wi*CPR + c.
 // A4: word wi of chunk c is 8 fp16 at unit wi*CPR + c, in the order
 //     {0,4,1,5,2,6,3,7} that matches the nibble pairs of one weight word.
 // BF16: words 2u, 2u+1 of chunk c read 4 bf16 (elements 4u..4u+3) at unit
 //     u*CPR + c.
-template <int FMT>
-__device__ __forceinline__ int xs_index(int e, int CPR) {
-  using T = FmtTraits<FMT>;
-  const int c = e / T::EPC, r = e % T::EPC;
-  if constexpr (FMT == FMT_A4) {
-    const int wi = r >> 3, t = r & 7;
-    return (wi * CPR + c) * 8 + (t < 4 ? 2 * t : 2 * (t - 4) + 1);
-  } else {
-    return ((r >> 2) * CPR + c) * 4 + (r & 3);
-  }
-}
 
 // acc_lo += lo(a) * lo(b), acc_hi += hi(a) * hi(b): fp16 x fp16 products
 // (exact in fp32) accumulated in fp32.
@@ -250,13 +239,27 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
   float xscale = 1.f, xinv = 1.f;
   if constexpr (AFF) {
     float mx = 0.f;
-    for (int i = tid; i < a.K / 2; i += NT) {
-      const uint32_t v = reinterpret_cast<const uint32_t*>(xraw)[i];
-      mx = fmaxf(mx, fmaxf(fabsf(bf16lo(v)), fabsf(bf16hi(v))));
+    for (int i = tid; i < a.K / 8; i += NT) {
+      const uint4 v = reinterpret_cast<const uint4*>(xraw)[i];
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16lo(v.x)), fabsf(bf16hi(v.x))),
+                           fmaxf(fabsf(bf16lo(v.y)), fabsf(bf16hi(v.y)))));
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16lo(v.z)), fabsf(bf16hi(v.z))),
+                           fmaxf(fabsf(bf16lo(v.w)), fabsf(bf16hi(v.w)))));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     if (lane == 0) red_max[warp] = mx;
+    // X_g = sum of x over group g (fp32, unscaled; one warp per group)
+    for (int g = warp; g < a.G; g += WARP_TASK_WARPS) {
+      float sum = 0.f;
+      for (int e = 4 * lane; e < a.group; e += 128) {
+        const uint2 v = *reinterpret_cast<const uint2*>(xraw + g * a.group + e);
+        sum += (bf16lo(v.x) + bf16hi(v.x)) + (bf16lo(v.y) + bf16hi(v.y));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      if (lane == 0) gsum[g] = sum;
+    }
     __syncthreads();
     mx = 0.f;
 #pragma unroll
@@ -267,24 +270,46 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
       xinv = ldexpf(1.f, -ex);
     }
   }
-  for (int i = tid; i < a.K / 2; i += NT) {
-    const uint32_t v = reinterpret_cast<const uint32_t*>(xraw)[i];
-    if constexpr (AFF) {
-      xs[xs_index<FMT>(2 * i, a.CPR)] = __half_as_ushort(__float2half_rn(bf16lo(v) * xscale));
-      xs[xs_index<FMT>(2 * i + 1, a.CPR)] = __half_as_ushort(__float2half_rn(bf16hi(v) * xscale));
-    } else {
-      xs[xs_index<FMT>(2 * i, a.CPR)] = (uint16_t)(v & 0xFFFFu);
-      xs[xs_index<FMT>(2 * i + 1, a.CPR)] = (uint16_t)(v >> 16);
-    }
-  }
-  if constexpr (AFF) {
-    // X_g = sum of x over group g (fp32, unscaled; one warp per group)
-    for (int g = warp; g < a.G; g += WARP_TASK_WARPS) {
-      float sum = 0.f;
-      for (int e = lane; e < a.group; e += 32) sum += bf16f(xraw[g * a.group + e]);
+  // staging layout: consecutive threads write consecutive words
+  {
+    const int CPR = a.CPR;
+    if constexpr (FMT == FMT_A4) {
+#pragma unroll 1
+      for (int k = 0; k < 4; ++k)
+        for (int c = tid; c < CPR; c += NT) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xraw + c * 32 + 8 * k);  // elements 0..7 of word k
+          const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+          float f[8];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      if (lane == 0) gsum[g] = sum;
+          for (int j = 0; j < 4; ++j) {
+            f[2 * j] = bf16lo(vw[j]) * xscale;
+            f[2 * j + 1] = bf16hi(vw[j]) * xscale;
+          }
+          // order {0,4,1,5,2,6,3,7}
+          uint4 o;
+          o.x = (uint32_t)__half_as_ushort(__float2half_rn(f[0])) | ((uint32_t)__half_as_ushort(__float2half_rn(f[4])) << 16);
+          o.y = (uint32_t)__half_as_ushort(__float2half_rn(f[1])) | ((uint32_t)__half_as_ushort(__float2half_rn(f[5])) << 16);
+          o.z = (uint32_t)__half_as_ushort(__float2half_rn(f[2])) | ((uint32_t)__half_as_ushort(__float2half_rn(f[6])) << 16);
+          o.w = (uint32_t)__half_as_ushort(__float2half_rn(f[3])) | ((uint32_t)__half_as_ushort(__float2half_rn(f[7])) << 16);
+          reinterpret_cast<uint4*>(xs)[k * CPR + c] = o;
+        }
+    } else {
+      constexpr int U = EPC / 4;  // words of 4 elements per chunk
+#pragma unroll 1
+      for (int k = 0; k < U; ++k)
+        for (int c = tid; c < CPR; c += NT) {
+          const uint2 v = *reinterpret_cast<const uint2*>(xraw + c * EPC + 4 * k);
+          uint2 o;
+          if constexpr (AFF) {
+            o.x = (uint32_t)__half_as_ushort(__float2half_rn(bf16lo(v.x) * xscale)) |
+                  ((uint32_t)__half_as_ushort(__float2half_rn(bf16hi(v.x) * xscale)) << 16);
+            o.y = (uint32_t)__half_as_ushort(__float2half_rn(bf16lo(v.y) * xscale)) |
+                  ((uint32_t)__half_as_ushort(__float2half_rn(bf16hi(v.y) * xscale)) << 16);
+          } else {
+            o = v;
+          }
+          reinterpret_cast<uint2*>(xs)[k * CPR + c] = o;
+        }
     }
   }
   __syncthreads();

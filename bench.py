@@ -232,7 +232,21 @@ class Stack:
         return w + 2 * wl.M * wl.d + 2 * wl.M * wl.f
 
 
-def capture(fn, torch):
+class DirectLaunch:
+    """Stands in for a captured graph: replay() calls the launches directly."""
+
+    def __init__(self, fn):
+        self.fn = fn
+
+    def replay(self):
+        self.fn()
+
+
+def capture(fn, torch, direct=False):
+    if direct:
+        fn()
+        torch.cuda.synchronize()
+        return DirectLaunch(fn)
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -302,7 +316,7 @@ def workload_config(wl, n_gpus):
             "eps": wl.eps, "bytes_per_layer": wl.layer_bytes(),
             "l2": "inputs larger than L2: each step streams all layers' weights once "
                   f"({wl.layer_bytes() * wl.layers / 1e9:.2f} GB per step vs 129 MB L2)",
-            "graph": "one CUDA graph per step, PDL between kernels",
+            "graph": "one CUDA graph per step, PDL between kernels",  # overwritten below when direct
             "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU"}
 
 
@@ -368,6 +382,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the step's kernels directly instead of replaying a CUDA graph")
     ap.add_argument("--gemv", default="warp", choices=["warp", "team"],
                     help="one-row GEMV kernel: warp-task kernel (default) or team kernel")
     ap.add_argument("--gateup-only", action="store_true",
@@ -404,7 +420,7 @@ def main():
         torch.cuda.synchronize()
         return 0
 
-    g_step = capture(stack.step, torch)
+    g_step = capture(stack.step, torch, direct=args.no_graph)
     for _ in range(max(3, args.warmup)):
         g_step.replay()
     torch.cuda.synchronize()
@@ -425,7 +441,7 @@ def main():
     per_kernel = {}
     for name, fn in (("gateup", stack.gateup_only), ("down", stack.down_only),
                      ("add_rmsnorm", stack.rmsnorm_only)):
-        g_k = capture(fn, torch)
+        g_k = capture(fn, torch, direct=args.no_graph)
         for _ in range(3):
             g_k.replay()
         per_kernel[name] = time_graph(g_k, max(5, args.steps // 4), torch) * 1e3 / wl.layers
@@ -484,6 +500,8 @@ def main():
                     "us_per_layer": round(e2e_s * 1e6 / wl.layers, 3),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "clocks": clk.summary()}
+    line["config"]["graph"] = ("direct launches" if args.no_graph else "one CUDA graph per step") + \
+        (", no PDL" if args.no_pdl else ", PDL between kernels")
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and wl.name == synth.QWEN8B.name:
         us_cpu, reps = oracle_layer_timing(wl)
         line["cpu_baseline"] = {"value": round(wl.layer_bytes() / (us_cpu * 1e-6) / 1e9, 4),

@@ -8,9 +8,11 @@
 //
 // GB300 design (each choice measured on this part; see the design notes):
 //  * One persistent CTA of 16 warps per SM owns a contiguous range of output
-//    rows.  The range is cut into tasks of one row piece (B bytes of each of
-//    the NW weight matrices), handed out dynamically through a shared-memory
-//    counter, so warps finish within about one task of each other.
+//    rows.  The range is cut into tasks of two weight streams of B bytes
+//    that share their activations: gate and up of one row (gate/up), or two
+//    consecutive rows (down).  Tasks are handed out dynamically through a
+//    shared-memory counter, so warps finish within about one task of each
+//    other.
 //  * A warp loads its next task's weights into registers with 128-bit
 //    evict-first loads while it computes the current one (register double
 //    buffer, up to 8 x 16 B per lane per task), ~64-128 KB in flight per SM
@@ -64,7 +66,7 @@ struct WarpArgs {
   int P;                   // pieces per row
   unsigned long long p_mul;  // ceil(2^32 / P): t / P == (t * p_mul) >> 32 for t < 2^32 / P
   int B;                   // bytes per piece (multiple of 16)
-  int CPP;                 // 16-byte chunks per piece (<= 32 * UPL / NW)
+  int CPP;                 // 16-byte chunks per piece (<= 32 * UPL / 2)
   int GPP;                 // groups per piece (affine)
   int rows_alloc;          // rows of the staged arrays
   int sb_stride;           // elements per staged scale or bias array (multiple of 8)
@@ -154,8 +156,10 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
   using T = FmtTraits<FMT>;
   constexpr int EPC = T::EPC;
   constexpr bool AFF = T::AFFINE;
-  constexpr int NW = KIND == 0 ? 2 : 1;
-  constexpr int CL = WARP_TASK_UPL / NW;  // chunks per lane per matrix per task
+  constexpr int NW = KIND == 0 ? 2 : 1;   // weight matrices
+  constexpr int RW = KIND == 0 ? 1 : 2;   // rows per task
+  constexpr int NS = 2;                   // weight streams per task: NW * RW
+  constexpr int CL = WARP_TASK_UPL / NS;  // chunks per lane per stream per task
   constexpr int NT = WARP_TASK_WARPS * 32;
 
   extern __shared__ __align__(128) unsigned char smem[];
@@ -172,26 +176,29 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
   const int cta = blockIdx.x;
   const int r_begin = cta * a.rows_base + min(cta, a.rows_extra);
   const int rows = a.rows_base + (cta < a.rows_extra ? 1 : 0);
-  const int T_tasks = rows * a.P;
+  const int T_tasks = (rows + RW - 1) / RW * a.P;
 
   if (tid == 0) task_ctr = WARP_TASK_WARPS;  // tasks 0..W-1 are taken statically
   __syncthreads();
   pdl_trigger();
 
   const uint64_t pol = l2_evict_first_policy();
-  auto load_task = [&](int t, uint4 (&buf)[NW][CL]) {
-    const bool ok = t < T_tasks;
-    const int q = (int)(((unsigned long long)(unsigned)t * a.p_mul) >> 32);
-    const int rl = ok ? q : 0, p = ok ? t - q * a.P : 0;
-    const size_t base = (size_t)(r_begin + rl) * a.row_bytes + (size_t)p * a.B;
+  // stream v of a task: matrix v of row rl0 (gate/up) or row rl0 + v (down)
+  auto load_task = [&](int t, uint4 (&buf)[NS][CL]) {
+    const int rg = (int)(((unsigned long long)(unsigned)t * a.p_mul) >> 32);
+    const int p = t - rg * a.P;
 #pragma unroll
-    for (int m = 0; m < NW; ++m)
+    for (int v = 0; v < NS; ++v) {
+      const int rl = rg * RW + (KIND == 0 ? 0 : v);
+      const bool ok = t < T_tasks && rl < rows;
+      const uint8_t* src = (KIND == 0 && v ? a.W1 : a.W0) +
+                           (size_t)(r_begin + (ok ? rl : 0)) * a.row_bytes + (size_t)p * a.B;
 #pragma unroll
       for (int k = 0; k < CL; ++k) {
         const int j = lane + 32 * k;
-        buf[m][k] = (ok && j < a.CPP) ? ldg_stream_pol((m ? a.W1 : a.W0) + base + (size_t)j * 16, pol)
-                                      : make_uint4(0, 0, 0, 0);
+        buf[v][k] = (ok && j < a.CPP) ? ldg_stream_pol(src + (size_t)j * 16, pol) : make_uint4(0, 0, 0, 0);
       }
+    }
   };
   auto next_task = [&]() -> int {
     int t = 0;
@@ -200,7 +207,7 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
   };
 
   // the first tasks: static weights, requested before the wait
-  uint4 bufA[NW][CL], bufB[NW][CL];
+  uint4 bufA[NS][CL], bufB[NS][CL];
   int tc = warp;
   load_task(tc, bufA);
 
@@ -315,52 +322,57 @@ __global__ void __launch_bounds__(WARP_TASK_WARPS * 32, 1) gemv_warp_kernel(cons
   __syncthreads();
 
   // computes task t from the weights in buf and stores its partial sums
-  auto compute_task = [&](int t, const uint4 (&buf)[NW][CL]) {
-    const int rl = (int)(((unsigned long long)(unsigned)t * a.p_mul) >> 32);
-    const int p = t - rl * a.P;
-    float acc[NW];
+  auto compute_task = [&](int t, const uint4 (&buf)[NS][CL]) {
+    const int rg = (int)(((unsigned long long)(unsigned)t * a.p_mul) >> 32);
+    const int p = t - rg * a.P;
+    const int rl0 = rg * RW;
+    float acc[NS];
 #pragma unroll
-    for (int m = 0; m < NW; ++m) acc[m] = 0.f;
+    for (int v = 0; v < NS; ++v) acc[v] = 0.f;
 #pragma unroll
     for (int k = 0; k < CL; ++k) {
       const int j = lane + 32 * k;
       if (j < a.CPP) {
         const int c = p * a.CPP + j;
 #pragma unroll
-        for (int m = 0; m < NW; ++m) {
-          const float d = chunk_dot<FMT>(buf[m][k], xs, c, a.CPR);
+        for (int v = 0; v < NS; ++v) {
+          const float d = chunk_dot<FMT>(buf[v][k], xs, c, a.CPR);
           if constexpr (AFF) {
+            const int m = KIND == 0 ? v : 0, rl = min(rl0 + (KIND == 0 ? 0 : v), rows - 1);
             const int gi = (c * EPC) >> a.lg_group;
-            acc[m] = fmaf(bf16f(sbr[(size_t)(2 * m) * a.sb_stride + rl * a.G + gi]), d, acc[m]);
+            acc[v] = fmaf(bf16f(sbr[(size_t)(2 * m) * a.sb_stride + rl * a.G + gi]), d, acc[v]);
           } else {
-            acc[m] += d;
+            acc[v] += d;
           }
         }
       }
     }
-    float vals[NW];
+    float vals[NS];
 #pragma unroll
-    for (int m = 0; m < NW; ++m) vals[m] = acc[m] * xinv;
+    for (int v = 0; v < NS; ++v) vals[v] = acc[v] * xinv;
     if constexpr (AFF) {
       // bias terms of the groups in this piece: sum_g b_g * X_g
       for (int gl = lane; gl < a.GPP; gl += 32) {
         const int g = p * a.GPP + gl;
         const float xg = gsum[g];
 #pragma unroll
-        for (int m = 0; m < NW; ++m)
-          vals[m] = fmaf(bf16f(sbr[(size_t)(2 * m + 1) * a.sb_stride + rl * a.G + g]), xg, vals[m]);
+        for (int v = 0; v < NS; ++v) {
+          const int m = KIND == 0 ? v : 0, rl = min(rl0 + (KIND == 0 ? 0 : v), rows - 1);
+          vals[v] = fmaf(bf16f(sbr[(size_t)(2 * m + 1) * a.sb_stride + rl * a.G + g]), xg, vals[v]);
+        }
       }
     }
 #pragma unroll
-    for (int m = 0; m < NW; ++m)
+    for (int v = 0; v < NS; ++v)
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) vals[m] += __shfl_xor_sync(0xffffffffu, vals[m], off);
-    if (lane < NW) {
-      float v = vals[0];
+      for (int off = 16; off > 0; off >>= 1) vals[v] += __shfl_xor_sync(0xffffffffu, vals[v], off);
+    if (lane < NS) {
+      float val = vals[0];
 #pragma unroll
-      for (int m = 1; m < NW; ++m)
-        if (lane == m) v = vals[m];
-      parts[((size_t)rl * a.P + p) * NW + lane] = v;
+      for (int v = 1; v < NS; ++v)
+        if (lane == v) val = vals[v];
+      const int m = KIND == 0 ? lane : 0, rl = rl0 + (KIND == 0 ? 0 : lane);
+      if (rl < rows) parts[((size_t)rl * a.P + p) * NW + m] = val;
     }
   };
 
@@ -407,7 +419,7 @@ mt_status run_gemv_warp(const GemvProblem& p, const Launch& l) {
   constexpr int EPC = T::EPC;
   constexpr bool AFF = T::AFFINE;
   constexpr int NW = KIND == 0 ? 2 : 1;
-  constexpr int CL = WARP_TASK_UPL / NW;
+  constexpr int CL = WARP_TASK_UPL / 2;  // chunks per lane per stream
   if (p.M != 1) return MT_ERR_SHAPE;
   static OccCache cache;  // only the attribute flags are used
   int dev = 0;
@@ -433,7 +445,7 @@ mt_status run_gemv_warp(const GemvProblem& p, const Launch& l) {
   a.CPR = p.K / EPC;
 
   // Pieces per row: the fewest whose chunks fit the lanes' register buffer
-  // (32 * CL chunks per matrix), dividing the row's chunks and (affine) its
+  // (32 * CL chunks per stream), dividing the row's chunks and (affine) its
   // groups, so a piece holds whole groups.
   int P = 0;
   for (int q = 1; q <= a.CPR; ++q) {

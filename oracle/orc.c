@@ -24,7 +24,8 @@
  * design notes of this repository):
  *  - bf16 values are rounded to nearest-even directly from binary64, only
  *    where a tensor crosses a call boundary (out_sum, out_norm, h, y).
- *  - quantiser: bias = bf16(min), scale = bf16((max - min) / (2^bits - 1)),
+ *  - quantiser: bias = bf16(min) (+0 for a zero minimum),
+ *    scale = bf16((max - min) / (2^bits - 1)),
  *    q = clamp(round_half_even((w - bias) / scale), 0, 2^bits - 1), computed
  *    against the bf16-rounded scale and bias; a zero scale gives q = 0.
  *  - 4-bit packing: code 2j in the low nibble and code 2j+1 in the high
@@ -128,6 +129,7 @@ int orc_quantize(const float* W, long N, long K, int group, int bits,
         if (v < mn) mn = v;
         if (v > mx) mx = v;
       }
+      if (mn == 0.0) mn = 0.0; /* a zero minimum gives the bias +0 */
       uint16_t b16 = orc_bf16_from_f64(mn);
       uint16_t s16 = orc_bf16_from_f64((mx - mn) / qmax);
       double bias = orc_f64_from_bf16(b16);

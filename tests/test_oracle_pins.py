@@ -204,6 +204,14 @@ def test_quantizer_constant_and_zero_groups():
     assert np.array_equal(oracle.dequant(codes, s, b, 32), W.astype(np.float64))
 
 
+def test_zero_minimum_gives_positive_zero_bias():
+    W = np.full((1, 32), 0.5, dtype=np.float32)
+    W[0, 3] = -0.0
+    W[0, 7] = 0.0
+    _, _, b = oracle.quantize(W, 32, 8)
+    assert int(b[0, 0]) == 0x0000
+
+
 def test_groups_run_along_k_not_n():
     # Row 0 uses a small range, row 1 a large one, and the two halves of each
     # row differ: scales must be indexed [n][k / group].

@@ -4,16 +4,19 @@ Default workload: the Qwen3-8B-shaped decode stack (d=4096, f=12288, one row,
 36 layers with distinct weights, affine INT8 group 128, ~5.6 GB streamed per
 step -- larger than L2, so no flush is needed between steps).  A step is one
 pass over the whole stack: per layer add+RMSNorm, gate/up GEMV + SwiGLU, down
-GEMV + residual, each a call of the C ABI.  The step is captured once into a
-CUDA graph (the calls keep their programmatic-dependent-launch attributes) and
-replayed.
+GEMV + residual.  Default path: the warmed executor (mt_mlp_plan_run: one
+persistent cooperative kernel for the whole stack).  --path calls times the
+three single-call C-ABI kernels per layer instead (captured into one CUDA
+graph, programmatic dependent launch between them); its time is also
+reported beside the executor's as ``calls_path``.
 
 Printed JSON line (one per run, rank 0):
   value       effective HBM GB/s = algorithmic bytes of the step / step time
   e2e         the same metric with the step's inputs copied host->device from
               pinned memory and the output read back, inside the timed region
-  roofline    the dominant kernel (gate/up + SwiGLU) timed alone over the 36
-              layers with CUDA events, against the measured HBM peak
+  roofline    the dominant kernel (the stack kernel; with --path calls the
+              gate/up + SwiGLU kernel timed alone over the 36 layers) with CUDA
+              events, against the measured HBM peak
   cpu_baseline the float64 CPU oracle timed on one layer of the same workload
   clocks      SM clocks / throttle reasons sampled during the timed region
 
@@ -38,13 +41,20 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "µs per decode MLP layer and effective HBM GB/s (fraction of ~8 TB/s peak)"
-GATEUP_PROFILE = os.path.join(ROOT, "profiles", "gateup_affine8_qwen3-8b.txt")
-KERNEL_SOURCES = ["k_gemv.cuh", "k_gemv_warp.cuh", "k_gemv_run.cuh", "k_gemv_a8.cu", "mt_device.cuh"]
+# ncu summaries under profiles/ and the sources of the kernel each covers (the
+# traffic figure is used only while the kernel is unchanged)
+PROFILES = {
+    "gateup": (os.path.join(ROOT, "profiles", "gateup_affine8_qwen3-8b.txt"),
+               ["k_gemv.cuh", "k_phase.cuh", "k_gemv_warp.cuh", "k_gemv_run.cuh", "k_gemv_a8.cu",
+                "mt_device.cuh"]),
+    "stack": (os.path.join(ROOT, "profiles", "stack_affine8_qwen3-8b.txt"),
+              ["k_gemv.cuh", "k_phase.cuh", "k_stack.cu", "mt_device.cuh"]),
+}
 
 
-def kernel_hash() -> str:
+def kernel_hash(kind: str) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in PROFILES[kind][1]:
         with open(os.path.join(ROOT, "quantized_gemv_epilogues_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -59,18 +69,19 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def profiled_traffic():
-    """Per-launch DRAM bytes of the gate/up kernel from the committed ncu
-    summary, or None when the summary is missing or the kernel changed."""
-    if not os.path.exists(GATEUP_PROFILE):
+def profiled_traffic(kind: str):
+    """Per-launch DRAM bytes of a kernel from its committed ncu summary, or
+    None when the summary is missing or the kernel changed since."""
+    path = PROFILES[kind][0]
+    if not os.path.exists(path):
         return None
     kv = {}
-    with open(GATEUP_PROFILE) as fh:
+    with open(path) as fh:
         for line in fh:
             if ":" in line:
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
-    if kv.get("kernel_sources_sha256_16") != kernel_hash():
+    if kv.get("kernel_sources_sha256_16") != kernel_hash(kind):
         return None
     try:
         return int(kv["dram_bytes_per_launch_full"])
@@ -151,6 +162,7 @@ class Stack:
         self.dev = device
         bf = torch.bfloat16
         tmp = torch.empty(max(d * f, 1), dtype=torch.float32, device=device)
+        self.values = torch.empty(self.L, M, d, dtype=bf, device=device)  # per-layer addends
         self.layers = []
         for l in range(self.L):
             sd = lambda t: synth.seed_for(wl.wid, l, t)
@@ -179,7 +191,7 @@ class Stack:
                     W32 = tmp[:N * K].view(N, K)
                     synth.device_f32(W32, sd(t), wl.weight_dist)
                     mt.mt_pack_affine(W32, N, K, g, bits, dst, s_, b_)
-            values = torch.empty(M, d, dtype=bf, device=device)
+            values = self.values[l]
             synth.device_bf16(values, sd(synth.T_VALUES), synth.ACT)
             self.layers.append(dict(w=w_norm, Wg=Wg, Wu=Wu, Wd=Wd, sgu=sgu, bgu=bgu, sd=sdn,
                                     bd=bdn, values=values))
@@ -189,9 +201,25 @@ class Stack:
         self.resid = torch.empty(M, d, dtype=bf, device=device)
         self.norm = torch.empty(M, d, dtype=bf, device=device)
         self.h = torch.empty(M, wl.f, dtype=bf, device=device)
+        self.out_y = torch.empty(M, d, dtype=bf, device=device)
+        self.plan = None
+        if M == 1:
+            self.plan = mt.mt_mlp_plan_create(
+                [dict(norm_weight=L["w"], Wg=L["Wg"], Wu=L["Wu"], gu_scales=L["sgu"],
+                      gu_biases=L["bgu"], Wd=L["Wd"], d_scales=L["sd"], d_biases=L["bd"])
+                 for L in self.layers], d, f, g, wl.fmt, wl.eps)
         torch.cuda.synchronize()
 
-    def step(self):
+    def close(self):
+        if self.plan is not None:
+            self.mt.mt_mlp_plan_destroy(self.plan)
+            self.plan = None
+
+    def step_executor(self):
+        """One pass over the stack: one mt_mlp_plan_run (one kernel)."""
+        self.mt.mt_mlp_plan_run(self.plan, self.values, self.r0, self.out_y)
+
+    def step_calls(self):
         """One pass over the stack (3 C-ABI calls per layer)."""
         mt, wl = self.mt, self.wl
         self.resid.copy_(self.r0)
@@ -254,8 +282,13 @@ def capture(fn, torch, direct=False):
         fn()  # warm (plans, attributes) outside capture
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
-    with torch.cuda.graph(g):
-        fn()
+    try:
+        with torch.cuda.graph(g):
+            fn()
+    except RuntimeError as e:  # a launch kind the graph cannot hold: launch directly
+        print(f"bench: graph capture failed ({e}); launching directly", file=sys.stderr)
+        torch.cuda.synchronize()
+        return DirectLaunch(fn)
     torch.cuda.synchronize()
     return g
 
@@ -380,14 +413,17 @@ def main():
     ap.add_argument("--workload", default="qwen3-8b",
                     choices=["qwen3-8b", "tiny", "llama1b", "qwen15", "sweep"])
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
+    ap.add_argument("--path", default="executor", choices=["executor", "calls"],
+                    help="timed step: the warmed executor (one kernel per step, default) or "
+                         "three single-call kernels per layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the step's kernels directly instead of replaying a CUDA graph")
     ap.add_argument("--gemv", default="warp", choices=["warp", "team"],
-                    help="one-row GEMV kernel: warp-task kernel (default) or team kernel")
-    ap.add_argument("--gateup-only", action="store_true",
-                    help="profiling aid: run only the gate/up kernels of the stack")
+                    help="single-call one-row GEMV kernel: warp-task kernel (default) or team kernel")
+    ap.add_argument("--only", default=None, choices=["gateup", "executor"],
+                    help="profiling aid: run only these kernels (no timing, no JSON line)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -411,16 +447,18 @@ def main():
     if args.layers:
         wl = wl.with_(layers=args.layers)
     stack = Stack(wl, dev)
+    use_exec = args.path == "executor" and stack.plan is not None
 
-    if args.gateup_only:
-        for _ in range(max(3, args.warmup)):
-            stack.gateup_only()
-        for _ in range(args.steps):
-            stack.gateup_only()
+    if args.only:
+        fn = stack.gateup_only if args.only == "gateup" else stack.step_executor
+        for _ in range(max(3, args.warmup) + args.steps):
+            fn()
         torch.cuda.synchronize()
+        stack.close()
         return 0
 
-    g_step = capture(stack.step, torch, direct=args.no_graph)
+    step_fn = stack.step_executor if use_exec else stack.step_calls
+    g_step = capture(step_fn, torch, direct=args.no_graph)
     for _ in range(max(3, args.warmup)):
         g_step.replay()
     torch.cuda.synchronize()
@@ -436,34 +474,54 @@ def main():
     step_bytes = wl.layer_bytes() * wl.layers
     value = ws * step_bytes / (ms * 1e-3) / 1e9
     us_layer = ms * 1e3 / wl.layers
+    peak, peak_kind = measured_peaks()
 
-    # ---- each kernel alone, over the 36 layers' weights (one graph per kind)
+    # ---- the single-call path, and each of its kernels alone over the layers
     per_kernel = {}
+    kernel_reps = max(5, args.steps // 4)
+    g_calls = g_step if not use_exec else capture(stack.step_calls, torch, direct=args.no_graph)
+    for _ in range(3):
+        g_calls.replay()
+    calls_us = time_graph(g_calls, kernel_reps, torch) * 1e3 / wl.layers
+    del g_calls
     for name, fn in (("gateup", stack.gateup_only), ("down", stack.down_only),
                      ("add_rmsnorm", stack.rmsnorm_only)):
         g_k = capture(fn, torch, direct=args.no_graph)
         for _ in range(3):
             g_k.replay()
-        per_kernel[name] = time_graph(g_k, max(5, args.steps // 4), torch) * 1e3 / wl.layers
+        per_kernel[name] = time_graph(g_k, kernel_reps, torch) * 1e3 / wl.layers
         del g_k
-    gu_launch_s = per_kernel["gateup"] * 1e-6
-    gu_bytes = stack.gateup_bytes()
-    peak, peak_kind = measured_peaks()
-    achieved = gu_bytes / gu_launch_s / 1e9
 
-    # ---- end to end: pinned host inputs -> device, graph, result -> host
-    h_vals = [torch.empty_like(L["values"], device="cpu").pin_memory() for L in stack.layers]
-    for hv, L in zip(h_vals, stack.layers):
-        hv.copy_(L["values"])
+    if use_exec:
+        # the stack kernel is the whole step (plus a 128-byte memset node)
+        roof = {"bound": "hbm", "kernel": f"mlp_stack_kernel ({wl.layers} layers, one row)",
+                "achieved": round(step_bytes / (ms * 1e-3) / 1e9, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4), "peak_kind": peak_kind,
+                "bytes_per_launch": step_bytes, "us_per_launch": round(ms * 1e3, 3),
+                "traffic": profiled_traffic("stack")}
+    else:
+        gu_launch_s = per_kernel["gateup"] * 1e-6
+        gu_bytes = stack.gateup_bytes()
+        achieved = gu_bytes / gu_launch_s / 1e9
+        roof = {"bound": "hbm",
+                "kernel": ("gemv_warp_kernel" if args.gemv == "warp" else "gemv_kernel")
+                          + " gate/up+SwiGLU (one row)",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                "bytes_per_launch": gu_bytes, "us_per_launch": round(gu_launch_s * 1e6, 3),
+                "traffic": profiled_traffic("gateup")}
+
+    # ---- end to end: pinned host inputs -> device, step, result -> host
+    h_vals = stack.values.cpu().pin_memory()
     h_r0 = stack.r0.cpu().pin_memory()
-    h_out = torch.empty_like(stack.resid, device="cpu").pin_memory()
+    out_dev = stack.out_y if use_exec else stack.resid
+    h_out = torch.empty_like(out_dev, device="cpu").pin_memory()
 
     def e2e_step():
-        for hv, L in zip(h_vals, stack.layers):
-            L["values"].copy_(hv, non_blocking=True)
+        stack.values.copy_(h_vals, non_blocking=True)
         stack.r0.copy_(h_r0, non_blocking=True)
         g_step.replay()
-        h_out.copy_(stack.resid, non_blocking=True)
+        h_out.copy_(out_dev, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -475,7 +533,7 @@ def main():
         e2e_step()
     torch.cuda.synchronize()
     e2e_s = reduce_max((time.perf_counter() - t0) / args.steps, ws, torch, dev)
-    h2d = sum(hv.numel() * 2 for hv in h_vals) + h_r0.numel() * 2
+    h2d = h_vals.numel() * 2 + h_r0.numel() * 2
     d2h = h_out.numel() * 2
 
     line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s",
@@ -485,23 +543,25 @@ def main():
             "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": {0: "bf16", 1: "u8", 2: "u4"}[wl.fmt] + "-weights/f32-acc",
             "data": "synthetic", "config": workload_config(wl, ws),
-            "gpu_launches": 3 * wl.layers * args.steps,
+            "gpu_launches": (1 if use_exec else 3 * wl.layers) * args.steps,
             "device_error": mt.mt_device_error(),
-            "roofline": {"bound": "hbm",
-                         "kernel": ("gemv_warp_kernel" if args.gemv == "warp" else "gemv_kernel")
-                                   + " gate/up+SwiGLU (affine8, one row)",
-                         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                         "bytes_per_launch": gu_bytes, "us_per_launch": round(gu_launch_s * 1e6, 3),
-                         "traffic": profiled_traffic()},
+            "roofline": roof,
+            "calls_path": {"us_per_layer": round(calls_us, 3),
+                           "gbs": round(wl.layer_bytes() / (calls_us * 1e-6) / 1e9, 1)},
             "kernels_us_per_layer": {k: round(v, 3) for k, v in per_kernel.items()},
             "down_gbs_alone": round(stack.down_bytes() / (per_kernel["down"] * 1e-6) / 1e9, 1),
+            "gateup_gbs_alone": round(stack.gateup_bytes() / (per_kernel["gateup"] * 1e-6) / 1e9, 1),
             "e2e": {"value": round(ws * step_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
                     "us_per_layer": round(e2e_s * 1e6 / wl.layers, 3),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "clocks": clk.summary()}
-    line["config"]["graph"] = ("direct launches" if args.no_graph else "one CUDA graph per step") + \
-        (", no PDL" if args.no_pdl else ", PDL between kernels")
+    if use_exec:
+        line["config"]["path"] = "warmed executor: mt_mlp_plan_run, one cooperative kernel per step"
+    else:
+        line["config"]["path"] = "single calls: mt_add_rmsnorm + mt_swiglu_gateup + mt_down_residual " \
+                                 "per layer" + (", no PDL" if args.no_pdl else ", PDL between kernels")
+    line["config"]["graph"] = "direct launches" if isinstance(g_step, DirectLaunch) else \
+        "one CUDA graph per step"
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and wl.name == synth.QWEN8B.name:
         us_cpu, reps = oracle_layer_timing(wl)
         line["cpu_baseline"] = {"value": round(wl.layer_bytes() / (us_cpu * 1e-6) / 1e9, 4),
@@ -509,6 +569,7 @@ def main():
                                 "kind": "oracle",
                                 "sample": f"{reps} passes of one layer ({wl.d}x{wl.f}, affine8 g128) "
                                           "of the same workload, binary64 C oracle, one thread"}
+    stack.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -20,7 +20,8 @@
  *                     ("values @ weight.T + residual").
  *
  * plus the offline packer mt_pack_affine (affine group quantisation of fp32
- * weights into the stored layout).
+ * weights into the stored layout), and the warmed executor mt_mlp_plan_*
+ * that runs L such layers back to back as one persistent kernel.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -77,7 +78,7 @@ typedef enum mt_status {
   MT_ERR_FORMAT = 5,  /* unknown weight format, dtype, bit width or option */
   MT_ERR_ALIAS = 6,   /* an output overlaps an input it may not overlap */
   MT_ERR_CUDA = 7,    /* a CUDA runtime call failed (see mt_last_cuda_error) */
-  MT_ERR_TIMEOUT = 8  /* reserved: a bounded device-side wait expired */
+  MT_ERR_TIMEOUT = 8  /* a bounded device-side wait expired (mt_device_error) */
 } mt_status;
 
 /* Output element type of a call.  Inputs are always bf16. */
@@ -175,6 +176,83 @@ mt_status mt_pack_affine(const float* W, int N, int K, int group, int bits,
  */
 mt_status mt_unpack_affine(const void* q, const void* scales, const void* biases,
                            int N, int K, int group, int bits, float* W, void* stream);
+
+/*
+ * Warmed decode-MLP executor (one row, M = 1): L layers run back to back by
+ * one persistent kernel.  Layer l (l = 0 .. L-1) computes, with r_0 = residual:
+ *   summed_l = bf16(values[l] + r_l)
+ *   x_l      = bf16(summed_l * norm_weight_l / sqrt(mean(summed_l^2) + eps))
+ *   h_l      = bf16(silu(x_l . Wg_l[n]) * (x_l . Wu_l[n]))      n < f
+ *   y_l      = bf16(h_l . Wd_l[n] + summed_l[n])                 n < d
+ *   r_{l+1}  = y_l
+ * i.e. exactly the tensors of L rounds of mt_add_rmsnorm, mt_swiglu_gateup and
+ * mt_down_residual with bf16 outputs (fp32 accumulation, each tensor rounded
+ * once where it crosses a call boundary); out_y = y_{L-1}.
+ * meTile docs, "Compute-Graph Fusion", Automatic Gated Epilogues (the selected
+ * gate/up and down/residual stages are bound once into a warmed MLP executor);
+ * "MLX-LM Backend", Dispatch Policy (residual add + RMSNorm keeps the residual
+ * as a second output; steady-state decode does not go through a per-call
+ * wrapper).
+ *
+ * mt_mlp_plan_create binds the layers' weights (device pointers, layouts as
+ * for the single calls; one format and group size for all layers) and plans
+ * the kernel for the CURRENT device.  It allocates the plan's device memory
+ * (a layer table of 80 * L bytes and a workspace of about 4 * (d + f) bytes
+ * plus 2 KB) with cudaMalloc, uploads the table synchronously and returns the
+ * plan in *plan.
+ * The weights stay owned by the caller and must outlive the plan; they must
+ * not be written while a run that reads them may execute.
+ *   layers : host array of L layer descriptions (copied; may be freed after)
+ *   d, f   : hidden and intermediate sizes, 8 <= d, f <= 32768, multiples of 8
+ *            and (affine) of group
+ *   Limits : 1 <= L <= 4096; the kernel's shared-memory layout must fit one SM
+ *            (MT_ERR_SHAPE otherwise; d = 4096, f = 12288 fits).
+ * mt_mlp_plan_run enqueues one pass over the L layers on `stream` (a memset of
+ * the plan's workspace and one cooperative kernel launch).  It allocates
+ * nothing and does not synchronise.
+ *   values   : bf16 [L][d], values[l] is layer l's addend (device)
+ *   residual : bf16 [d], r_0 (device)
+ *   out_y    : bf16 [d], y_{L-1} (device); may equal residual
+ *   trace    : NULL, or per-layer copies of the intermediate tensors, each
+ *              NULL or a device buffer: out_sum [L][d] (summed_l), out_norm
+ *              [L][d] (x_l), h [L][f], y [L][d].
+ *   The device current at the call must be the plan's (else MT_ERR_CUDA with
+ *   cudaErrorInvalidDevice).  Runs of one plan share its workspace: they must
+ *   not execute concurrently (enqueue them on one stream, or order them with
+ *   events); different plans are independent.  The run's kernel keeps one
+ *   CTA resident on every SM for its whole duration (cooperative launch);
+ *   kernels running concurrently on other streams can delay its CTAs.
+ *   A wait for another CTA's data that expires (bounded at about one
+ *   second) makes every CTA return: mt_device_error() then reports
+ *   MT_ERR_TIMEOUT and out_y is undefined.
+ * mt_mlp_plan_destroy frees the plan's device memory (cudaFree, which
+ * synchronises the device) and the plan.
+ */
+typedef struct mt_mlp_layer {
+  const void* norm_weight; /* bf16 [d] RMSNorm gain */
+  const void* Wg;          /* [f][d] in the plan's format */
+  const void* Wu;          /* [f][d] */
+  const void* gu_scales;   /* bf16 [2][f][d/group] (plane 0 Wg, 1 Wu); NULL for MT_W_BF16 */
+  const void* gu_biases;   /* bf16 [2][f][d/group]; NULL for MT_W_BF16 */
+  const void* Wd;          /* [d][f] */
+  const void* d_scales;    /* bf16 [d][f/group]; NULL for MT_W_BF16 */
+  const void* d_biases;    /* bf16 [d][f/group]; NULL for MT_W_BF16 */
+} mt_mlp_layer;
+
+typedef struct mt_mlp_trace {
+  void* out_sum;  /* bf16 [L][d] or NULL */
+  void* out_norm; /* bf16 [L][d] or NULL */
+  void* h;        /* bf16 [L][f] or NULL */
+  void* y;        /* bf16 [L][d] or NULL */
+} mt_mlp_trace;
+
+typedef struct mt_mlp_plan mt_mlp_plan;
+
+mt_status mt_mlp_plan_create(const mt_mlp_layer* layers, int L, int d, int f, int group,
+                             mt_wfmt fmt, float eps, mt_mlp_plan** plan);
+mt_status mt_mlp_plan_run(const mt_mlp_plan* plan, const void* values, const void* residual,
+                          void* out_y, const mt_mlp_trace* trace, void* stream);
+mt_status mt_mlp_plan_destroy(mt_mlp_plan* plan);
 
 /* Library options.  Returns MT_ERR_FORMAT for an unknown option. */
 mt_status mt_set_option(mt_option opt, int value);

@@ -12,6 +12,8 @@ Calls (same names as the C ABI):
 * :func:`mt_swiglu_gateup` -- gate/up GEMV with the silu(gate) * up epilogue.
 * :func:`mt_down_residual` -- down GEMV with the residual added in its epilogue.
 * :func:`mt_pack_affine` / :func:`mt_unpack_affine` -- affine group packer.
+* :func:`mt_mlp_plan_create` / :func:`mt_mlp_plan_run` / :func:`mt_mlp_plan_destroy`
+  -- the warmed executor: L one-row layers as one persistent kernel.
 
 Tensors are ``torch.Tensor`` on the current CUDA device (bf16 activations,
 uint8 packed codes, bf16 scales/biases); raw integer device pointers are also
@@ -51,11 +53,25 @@ _SIGS = {
     "mt_last_cuda_error": (_I, []),
     "mt_device_error": (_I, [_I]),
     "mt_version": (_I, []),
+    "mt_mlp_plan_create": (_I, [_P, _I, _I, _I, _I, _I, _F, _P]),
+    "mt_mlp_plan_run": (_I, [_P, _P, _P, _P, _P, _P]),
+    "mt_mlp_plan_destroy": (_I, [_P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
     _fn.restype = _res
     _fn.argtypes = _args
+
+
+class MlpLayer(ctypes.Structure):
+    """``mt_mlp_layer``: one layer's device pointers."""
+    _fields_ = [(n, _P) for n in ("norm_weight", "Wg", "Wu", "gu_scales", "gu_biases", "Wd",
+                                  "d_scales", "d_biases")]
+
+
+class MlpTrace(ctypes.Structure):
+    """``mt_mlp_trace``: optional per-layer outputs (device pointers or NULL)."""
+    _fields_ = [(n, _P) for n in ("out_sum", "out_norm", "h", "y")]
 
 
 class MTError(RuntimeError):
@@ -151,6 +167,35 @@ def mt_pack_affine(W, N, K, group, bits, q, scales, biases, stream=None):
 def mt_unpack_affine(q, scales, biases, N, K, group, bits, W, stream=None):
     _check(_lib.mt_unpack_affine(_ptr(q), _ptr(scales), _ptr(biases), int(N), int(K), int(group),
                                  int(bits), _ptr(W), _stream(stream)), "mt_unpack_affine")
+
+
+def mt_mlp_plan_create(layers, d, f, group, fmt, eps) -> int:
+    """Binds L layers (each a mapping with the ``mt_mlp_layer`` field names to
+    tensors or device pointers; scale/bias fields may be None for bf16) and
+    returns the plan handle (an int)."""
+    arr = (MlpLayer * len(layers))()
+    for i, ly in enumerate(layers):
+        for name, _ in MlpLayer._fields_:
+            setattr(arr[i], name, _ptr(ly.get(name)))
+    plan = ctypes.c_void_p()
+    _check(_lib.mt_mlp_plan_create(arr, len(layers), int(d), int(f), int(group), int(fmt),
+                                   float(eps), ctypes.byref(plan)), "mt_mlp_plan_create")
+    return plan.value
+
+
+def mt_mlp_plan_run(plan, values, residual, out_y, trace=None, stream=None) -> None:
+    """One pass over the plan's layers.  trace: None or a mapping with some of
+    out_sum / out_norm / h / y (tensors [L][.] or device pointers)."""
+    tr = None
+    if trace is not None:
+        tr = MlpTrace(*[_ptr(trace.get(n)) for n, _ in MlpTrace._fields_])
+    _check(_lib.mt_mlp_plan_run(plan, _ptr(values), _ptr(residual), _ptr(out_y),
+                                ctypes.byref(tr) if tr is not None else None, _stream(stream)),
+           "mt_mlp_plan_run")
+
+
+def mt_mlp_plan_destroy(plan) -> None:
+    _check(_lib.mt_mlp_plan_destroy(plan), "mt_mlp_plan_destroy")
 
 
 def mt_set_option(opt: int, value: int) -> None:

@@ -1,0 +1,745 @@
+// k_stack.cu - the warmed decode-MLP executor: L one-row layers
+//   summed_l = values_l + r_l, x_l = rms_norm(summed_l), h_l = silu(x_l Wg^T) * (x_l Wu^T),
+//   y_l = h_l Wd^T + summed_l, r_{l+1} = y_l
+// run by ONE persistent cooperative kernel.
+//
+// meTile docs, "Compute-Graph Fusion", Automatic Gated Epilogues (the gate/up
+// stage with its SwiGLU epilogue and the down stage with its residual
+// epilogue are combined into a warmed MLP executor that binds the selected
+// stages once); "MLX-LM Backend", Dispatch Policy (residual add + RMSNorm
+// with the summed residual kept as a second output; steady-state decode does
+// not pass through a per-call wrapper).
+//
+// GB300 design.  The three single-call kernels of a layer each pay a launch,
+// a prologue (x staging, scales) and a tail in which the SMs drain; with
+// one CTA per SM, programmatic dependent launch cannot overlap them.  Here
+// one CTA per SM stays resident for the whole stack and walks, per layer:
+//   norm    every CTA rebuilds x_l = rms_norm(summed_l) for the whole vector
+//           from summed_l and the per-CTA partial sums of squares,
+//   gate/up the CTA's rows of Wg/Wu (warp-task phase, k_phase.cuh),
+//           publishing its rows of h,
+//   down    the CTA's rows of Wd with x = h; the epilogue adds the residual
+//           and publishes its rows of summed_{l+1} = values_{l+1} + y_l and
+//           their sum of squares.
+// Hand-offs between CTAs use no grid barrier.  Every published value travels
+// in a flag-in-data word: 64 bits holding 32 bits of payload (two bf16, or
+// one fp32) and the 32-bit number of the tensor's layer plus one, written
+// and read as single 64-bit accesses (single-copy atomic), so a reader that
+// sees the expected number also has the payload; it re-reads a word until the
+// number matches.  After publishing its rows a CTA writes one tagged "done"
+// word (for summed, the word of its partial sum of squares); in each CTA a
+// single warp polls the grid's done words, then every thread reads its data
+// words once (re-reading, with a short sleep, the rare word that is still in
+// flight).  A hand-off thus costs about two round trips to L2 instead of the
+// four or five of a barrier (release, arrival, polls) followed by the load,
+// which measured 3-5 us per hand-off on this two-die part; letting every
+// thread poll its own data words instead flooded L2 with re-reads.  Reuse is safe without barriers: a CTA overwrites a published buffer
+// only after consuming a tensor that every other CTA published after it had
+// read that buffer.  Rows are dealt out to CTAs in pairs so that every word
+// has one writer.  The words are zeroed before each run.  Every wait is
+// bounded (~1 s): on expiry the thread records MT_ERR_TIMEOUT in the device
+// error word and raises an abort flag that every other wait also watches,
+// and every CTA returns.
+//
+// Between hand-offs a CTA asks L2 for the first rows of its next phase's
+// weights with bulk (TMA) prefetches and stages that phase's scales, biases
+// and RMSNorm gain, so HBM keeps streaming while the hand-off completes.
+#include <math.h>
+
+#include <mutex>
+#include <new>
+
+#include "k_phase.cuh"
+
+namespace mt {
+
+constexpr int STACK_MAX_GRID = 256;  // CTAs (one per SM)
+// Bytes of each weight stream a CTA asks L2 for before a phase: about what
+// HBM delivers to one SM during a hand-off and the staging that follows.
+constexpr int STACK_PRE_GATEUP = 96 * 1024;  // per gate and per up stream
+constexpr int STACK_PRE_DOWN = 160 * 1024;
+
+// One layer's device pointers.
+struct StackLayerDev {
+  const uint16_t* wn;  // RMSNorm gain [d]
+  const uint8_t* Wg;
+  const uint8_t* Wu;
+  const uint8_t* Wd;
+  const uint16_t* sg;
+  const uint16_t* bg;
+  const uint16_t* su;
+  const uint16_t* bu;
+  const uint16_t* sd;
+  const uint16_t* bd;
+};
+
+// Run state (one 128-byte line, zeroed before every run with the words).
+struct StackCtl {
+  int abort;  // set when a wait expired
+  int pad[31];
+};
+
+struct StackArgs {
+  PhaseGeom gu, dn;
+  const StackLayerDev* layers;
+  int L, d, f;
+  float eps;
+  const uint16_t* values;    // [L][d]
+  const uint16_t* residual;  // [d]
+  uint16_t* out_y;           // [d]
+  StackCtl* ctl;
+  uint64_t* hw;   // [f/2]  h_l words: h[2k], h[2k+1] | l + 1
+  uint64_t* sw;   // [d/2]  summed_l words: summed[2k], summed[2k+1] | l + 1
+  uint64_t* qw;   // [grid] partial sums of squares of summed_l: fp32 | l + 1
+  uint64_t* hd;   // [grid] "h_l rows published": 0 | l + 1
+  int* err;
+  int pre_g, pre_d;   // bytes per weight stream asked of L2 ahead of a phase
+  uint16_t* tr_sum;   // optional [L][d]
+  uint16_t* tr_norm;  // optional [L][d]
+  uint16_t* tr_h;     // optional [L][f]
+  uint16_t* tr_y;     // optional [L][d]
+  // shared-memory carve-up (byte offsets)
+  int off_xs, off_gsum_g, off_sbr_g, off_parts_g, off_gsum_d, off_sbr_d, off_parts_d;
+  int off_wn, off_ssm;
+};
+
+// ---- flag-in-data words
+
+// GPU-scope relaxed accesses (system scope would also order against the
+// host, which this data never meets).
+__device__ __forceinline__ void word_store(uint64_t* p, uint32_t payload, uint32_t tag) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(((uint64_t)tag << 32) | payload)
+               : "memory");
+}
+__device__ __forceinline__ void words_load2(const uint64_t* p, uint64_t& w0, uint64_t& w1) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(p) : "memory");
+}
+__device__ __forceinline__ uint64_t word_load(const uint64_t* p) {
+  uint64_t w;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+__device__ __forceinline__ bool tag_is(uint64_t w, uint32_t tag) { return (uint32_t)(w >> 32) == tag; }
+
+// Bounded re-reading.  A wait (begin(), then again() before each re-read)
+// gives up after about 2^31 SM cycles (~1 s) or when another thread has given
+// up; the first to give up records MT_ERR_TIMEOUT.  After giving up, every
+// later wait of the thread gives up at once.
+struct Waiter {
+  StackCtl* ctl;
+  int* err;
+  long long t0;
+  unsigned spins;
+  bool ok;
+  __device__ __forceinline__ void begin() { spins = 0; }
+  __device__ __forceinline__ bool again() {  // false: stop waiting
+    if (!ok) return false;
+    if (spins++ == 0) t0 = clock64();
+    if ((spins & 63u) == 0) {
+      if (ld_relaxed_gpu(&ctl->abort)) { ok = false; return false; }
+      if (clock64() - t0 > (1ll << 31)) {
+        atomicExch(&ctl->abort, 1);
+        atomicExch(err, (int)MT_ERR_TIMEOUT);
+        ok = false;
+        return false;
+      }
+    }
+    return true;
+  }
+};
+
+// One warp: waits until the n (<= 256) words p[0 .. n-1] all carry `tag`,
+// re-reading every word still missing in each round; lane l receives the
+// payloads of words l + 32k in v[k] (0 beyond n).
+__device__ __forceinline__ void warp_wait_done(const uint64_t* p, int n, uint32_t tag, uint32_t (&v)[8],
+                                               Waiter& wt, int lane) {
+  uint64_t q[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int i = lane + 32 * k;
+    q[k] = i < n ? word_load(p + i) : ((uint64_t)tag << 32);
+  }
+  wt.begin();
+  for (;;) {
+    bool have = true;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) have = have && tag_is(q[k], tag);
+    if (__all_sync(0xffffffffu, have) || !wt.again()) break;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (!tag_is(q[k], tag)) q[k] = word_load(p + lane + 32 * k);
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) v[k] = (uint32_t)q[k];
+}
+
+// Reads NB x units of a published bf16 vector (unit i = words 4i .. 4i+3 =
+// elements 8i .. 8i+7): units base0 + k * WT_THREADS + lane for k < NB
+// (units >= nu are skipped).  Issues every read first, then re-reads (after a
+// short sleep) the units whose words do not yet all carry `tag`, until none
+// is left.  Used after the producers' done words were seen, so re-reads are
+// rare.
+template <int NB>
+__device__ __forceinline__ void read_units(const uint64_t* words, int base0, int nu, uint32_t tag,
+                                           uint4 (&out)[NB], Waiter& wt, int lane) {
+  uint64_t w[NB][4];
+#pragma unroll
+  for (int k = 0; k < NB; ++k) {
+    const int i = base0 + k * WT_THREADS + lane;
+    if (i < nu) {
+      words_load2(words + 4 * i, w[k][0], w[k][1]);
+      words_load2(words + 4 * i + 2, w[k][2], w[k][3]);
+    } else {
+      w[k][0] = w[k][1] = w[k][2] = w[k][3] = (uint64_t)tag << 32;
+    }
+  }
+  wt.begin();
+  for (;;) {
+    bool have = true;
+#pragma unroll
+    for (int k = 0; k < NB; ++k)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) have = have && tag_is(w[k][j], tag);
+    if (have || !wt.again()) break;
+    __nanosleep(64);
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+      const int i = base0 + k * WT_THREADS + lane;
+      if (i < nu && !(tag_is(w[k][0], tag) && tag_is(w[k][1], tag) && tag_is(w[k][2], tag) &&
+                      tag_is(w[k][3], tag))) {
+        words_load2(words + 4 * i, w[k][0], w[k][1]);
+        words_load2(words + 4 * i + 2, w[k][2], w[k][3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < NB; ++k)
+    out[k] = make_uint4((uint32_t)w[k][0], (uint32_t)w[k][1], (uint32_t)w[k][2], (uint32_t)w[k][3]);
+}
+
+__device__ __forceinline__ PhaseW gateup_w(const StackLayerDev& L) {
+  PhaseW w;
+  w.W0 = L.Wg; w.W1 = L.Wu;
+  w.s0 = L.sg; w.b0 = L.bg; w.s1 = L.su; w.b1 = L.bu;
+  return w;
+}
+__device__ __forceinline__ PhaseW down_w(const StackLayerDev& L) {
+  PhaseW w;
+  w.W0 = L.Wd; w.W1 = nullptr;
+  w.s0 = L.sd; w.b0 = L.bd; w.s1 = nullptr; w.b1 = nullptr;
+  return w;
+}
+
+// Sum over the CTA of one float per thread, in a fixed order; thread 0
+// receives the total.  red: WARP_TASK_WARPS floats of shared memory, free on
+// entry.
+__device__ __forceinline__ float cta_sum(float v, float* red, int tid) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  if ((tid & 31) == 0) red[tid >> 5] = v;
+  __syncthreads();
+  float t = 0.f;
+  if (tid == 0)
+    for (int w = 0; w < WARP_TASK_WARPS; ++w) t += red[w];
+  return t;
+}
+
+__device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
+
+template <int FMT>
+__global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArgs a) {
+  constexpr bool AFF = FmtTraits<FMT>::AFFINE;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int task_ctr;
+  __shared__ float red[WARP_TASK_WARPS];
+  __shared__ float s_inv;
+  __shared__ __align__(16) StackLayerDev lay_s[2];  // layers l and l + 1
+  static_assert(sizeof(StackLayerDev) % 16 == 0, "layer table entries are copied in 16-byte units");
+  constexpr int LAY_UNITS = (int)(sizeof(StackLayerDev) / 16);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cta = blockIdx.x;
+  const int d = a.d, f = a.f;
+
+  PhaseSmem smG, smD;
+  smG.xraw = smD.xraw = reinterpret_cast<uint16_t*>(smem);
+  smG.xs = smD.xs = reinterpret_cast<uint4*>(smem + a.off_xs);
+  smG.gsum = reinterpret_cast<float*>(smem + a.off_gsum_g);
+  smG.sbr = reinterpret_cast<uint16_t*>(smem + a.off_sbr_g);
+  smG.parts = reinterpret_cast<float*>(smem + a.off_parts_g);
+  smD.gsum = reinterpret_cast<float*>(smem + a.off_gsum_d);
+  smD.sbr = reinterpret_cast<uint16_t*>(smem + a.off_sbr_d);
+  smD.parts = reinterpret_cast<float*>(smem + a.off_parts_d);
+  uint16_t* wn = reinterpret_cast<uint16_t*>(smem + a.off_wn);    // [d] RMSNorm gain
+  uint16_t* ssm = reinterpret_cast<uint16_t*>(smem + a.off_ssm);  // [d] summed_l
+
+  const PhaseCta cg = phase_cta<0>(a.gu, cta);
+  const PhaseCta cd = phase_cta<1>(a.dn, cta);
+  const uint64_t pol = l2_evict_first_policy();
+  uint4 bufA[WT_NS][WT_CL], bufB[WT_NS][WT_CL];
+  const int tA = warp, tB = warp + WARP_TASK_WARPS;
+  Waiter wt{a.ctl, a.err, 0, 0, true};
+
+  // Copies layer l's pointer table entry into lay_s[l & 1] (cp.async; the
+  // caller commits and waits).
+  auto fetch_layer = [&](int l) {
+    if (tid < LAY_UNITS && l < a.L)
+      cp_async16(reinterpret_cast<uint4*>(&lay_s[l & 1]) + tid,
+                 reinterpret_cast<const uint4*>(a.layers + l) + tid);
+  };
+  // Asks L2 for the first `pre` bytes of the CTA's (contiguous) rows of W:
+  // one bulk prefetch, issued by the calling thread.
+  auto l2_ahead = [&](const PhaseGeom& g, const PhaseCta& c, const uint8_t* W, int pre) {
+    const size_t all = (size_t)c.rows * g.row_bytes;
+    const uint32_t n = (uint32_t)(all < (size_t)pre ? all : (size_t)pre);
+    if (n) bulk_prefetch_l2(W + (size_t)c.r_begin * g.row_bytes, n);
+  };
+  // What a phase needs that does not depend on the hand-off before it is
+  // requested early, so that only the hand-off's own traffic is in flight
+  // while a CTA waits: its scales and biases and (gate/up) the RMSNorm gain
+  // go to shared memory at the start of the PREVIOUS phase's task loop
+  // (stage_*_smem; the copies are small next to the weight stream), and its
+  // first rows' weights go to L2 with bulk prefetches right after the CTA has
+  // published its part of the hand-off (prefetch_*).  lay_s[l & 1] must be
+  // complete and visible.  The caller commits the copies.
+  auto stage_gateup_smem = [&](int l) {
+    const StackLayerDev& Ly = lay_s[l & 1];
+    if constexpr (AFF) stage_sb<0>(a.gu, gateup_w(Ly), cg, smG.sbr, tid, WT_THREADS);
+    for (int i = tid; i < d / 8; i += WT_THREADS) cp_async16(wn + (size_t)i * 8, Ly.wn + (size_t)i * 8);
+  };
+  auto stage_down_smem = [&](int l) {
+    const StackLayerDev& Ly = lay_s[l & 1];
+    if constexpr (AFF) stage_sb<1>(a.dn, down_w(Ly), cd, smD.sbr, tid, WT_THREADS);
+  };
+  auto prefetch_gateup = [&](int l) {
+    const StackLayerDev& Ly = lay_s[l & 1];
+    if (tid == 32) l2_ahead(a.gu, cg, Ly.Wg, a.pre_g);
+    if (tid == 64) l2_ahead(a.gu, cg, Ly.Wu, a.pre_g);
+  };
+  auto prefetch_down = [&](int l) {
+    const StackLayerDev& Ly = lay_s[l & 1];
+    if (tid == 32) l2_ahead(a.dn, cd, Ly.Wd, a.pre_d);
+  };
+  // This CTA's rows of summed_l = values_l + r (bf16 sum of two bf16, one
+  // rounding): pair j (rows 2j, 2j+1 of the CTA's down rows) is computed by
+  // thread j, published, and its squares folded into the CTA's partial sum,
+  // which thread 0 publishes.  r2: the pair of r.
+  auto publish_summed = [&](int l, uint32_t v2, uint32_t r2, bool have) {
+    float ss = 0.f;
+    if (have) {
+      const uint16_t s0 = f2bf(bf16lo(v2) + bf16lo(r2));
+      const uint16_t s1 = f2bf(bf16hi(v2) + bf16hi(r2));
+      word_store(a.sw + (cd.r_begin >> 1) + tid, pack2(s0, s1), (uint32_t)l + 1);
+      ss = fmaf(bf16f(s0), bf16f(s0), bf16f(s1) * bf16f(s1));
+    }
+    ss = cta_sum(ss, red, tid);
+    if (tid == 0) word_store(a.qw + cta, __float_as_uint(ss), (uint32_t)l + 1);
+  };
+
+  const int npair_d = cd.rows >> 1, npair_g = cg.rows >> 1;
+
+  // ---- prologue: layer 0's table entry, its gate/up staging, summed_0
+  fetch_layer(0);
+  cp_async_commit();
+  cp_async_wait_all();
+  __syncthreads();
+  {
+    const bool have = tid < npair_d;
+    uint32_t v2 = 0, r2 = 0;
+    if (have) {
+      v2 = *reinterpret_cast<const uint32_t*>(a.values + cd.r_begin + 2 * tid);
+      r2 = *reinterpret_cast<const uint32_t*>(a.residual + cd.r_begin + 2 * tid);
+    }
+    publish_summed(0, v2, r2, have);
+  }
+  prefetch_gateup(0);
+  stage_gateup_smem(0);
+  cp_async_commit();
+
+  for (int l = 0; l < a.L; ++l) {
+    const StackLayerDev& Ly = lay_s[l & 1];
+    const uint32_t tag = (uint32_t)l + 1;
+    fetch_layer(l + 1);  // waited for with the RMSNorm gain below
+    cp_async_commit();
+    // values_{l+1} of this thread's pair of down rows, for the down epilogue
+    uint32_t vnx = 0;
+    if (l + 1 < a.L && tid < npair_d)
+      vnx = *reinterpret_cast<const uint32_t*>(a.values + (size_t)(l + 1) * d + cd.r_begin + 2 * tid);
+
+    // ---- add + RMSNorm of the whole vector (every CTA)
+    float xinv;
+    {
+      const int nu = d / 8;  // x units of 8 elements = 4 summed words
+      static_assert(STACK_MAX_GRID <= 256, "warp_wait_done reads at most 256 words");
+      if (warp == 0) {  // the partial sums of squares, in one fixed order
+        uint32_t v[8];
+        warp_wait_done(a.qw, (int)gridDim.x, tag, v, wt, lane);
+        float tot = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) tot += __uint_as_float(v[k]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+        if (lane == 0) s_inv = rsqrtf(tot / (float)d + a.eps);
+      }
+      cp_async_wait_all();
+      if (!__syncthreads_and(wt.ok)) return;  // gain, scales, next table entry, s_inv
+      const float inv = s_inv;
+      // this thread's first two units of summed_l
+      uint4 u[2];
+      read_units<2>(a.sw, warp * 32, nu, tag, u, wt, lane);
+      // x = bf16(summed * inv * w), unit by unit, into the first staging pass
+      float mx = 0.f;
+      auto norm_unit = [&](int base, const uint4 sv) {
+        const int i = base + lane < nu ? base + lane : -1;
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (i >= 0) {
+          const uint4 w = reinterpret_cast<const uint4*>(wn)[i];
+          const uint32_t* sp = &sv.x;
+          const uint32_t* wp = &w.x;
+          uint32_t* op = &o.x;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float lo = bf16lo(sp[j]) * inv * bf16lo(wp[j]);
+            const float hi = bf16hi(sp[j]) * inv * bf16hi(wp[j]);
+            op[j] = pack2(f2bf(lo), f2bf(hi));
+          }
+          reinterpret_cast<uint4*>(ssm)[i] = sv;
+        }
+        x_unit<FMT>(a.gu, smG, i, o, mx);
+      };
+      if (warp * 32 < nu) norm_unit(warp * 32, u[0]);
+      if (warp * 32 + WT_THREADS < nu) norm_unit(warp * 32 + WT_THREADS, u[1]);
+      for (int base = warp * 32 + 2 * WT_THREADS; base < nu; base += WT_THREADS) {  // d > 8192
+        uint4 uw[1];
+        read_units<1>(a.sw, base, nu, tag, uw, wt, lane);
+        norm_unit(base, uw[0]);
+      }
+      // the first two gate/up tasks (mostly L2 hits after stage_gateup), in
+      // flight during the second staging pass
+      {
+        const PhaseW w = gateup_w(Ly);
+        wt_load<0>(a.gu, w, cg, tA, bufA, pol, lane);
+        wt_load<0>(a.gu, w, cg, tB, bufB, pol, lane);
+        wt_prefetch<0>(a.gu, w, cg, tA + 2 * WARP_TASK_WARPS, lane);
+        wt_prefetch<0>(a.gu, w, cg, tB + 2 * WARP_TASK_WARPS, lane);
+      }
+      if (tid == 0) task_ctr = 2 * WARP_TASK_WARPS;  // tasks 0..2W-1 are taken statically
+      xinv = x_convert<FMT>(a.gu, smG, mx, red, tid);
+      stage_down_smem(l);  // for the next phase, during this one's loop
+      cp_async_commit();
+      if (a.tr_sum || a.tr_norm)
+        for (int rl = tid; rl < cd.rows; rl += WT_THREADS) {
+          const int n = cd.r_begin + rl;
+          if (a.tr_sum) a.tr_sum[(size_t)l * d + n] = ssm[n];
+          if (a.tr_norm) a.tr_norm[(size_t)l * d + n] = smG.xraw[n];
+        }
+    }
+    // ---- gate/up with the SwiGLU epilogue; h is published pair by pair
+    {
+      wt_run<FMT, 0>(a.gu, gateup_w(Ly), cg, smG, bufA, bufB, tA, tB, &task_ctr, xinv, pol, lane);
+      __syncthreads();
+      for (int j = tid; j < npair_g; j += WT_THREADS) {
+        uint16_t hb[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float g = row_total<2>(a.gu, smG.parts, 2 * j + e, 0);
+          const float u = row_total<2>(a.gu, smG.parts, 2 * j + e, 1);
+          hb[e] = f2bf(g / (1.0f + expf(-g)) * u);
+        }
+        word_store(a.hw + (cg.r_begin >> 1) + j, pack2(hb[0], hb[1]), tag);
+        if (a.tr_h) *reinterpret_cast<uint32_t*>(a.tr_h + (size_t)l * f + cg.r_begin + 2 * j) = pack2(hb[0], hb[1]);
+      }
+      __syncthreads();
+      if (tid == 0) word_store(a.hd + cta, 0u, tag);
+    }
+    // ---- down
+    {
+      prefetch_down(l);
+      if (tid == 0) task_ctr = 2 * WARP_TASK_WARPS;
+      if (warp == 0) {
+        uint32_t v[8];
+        warp_wait_done(a.hd, (int)gridDim.x, tag, v, wt, lane);
+      }
+      if (!__syncthreads_and(wt.ok)) { cp_async_wait_all(); return; }
+      // h (every unit of a batch read before anything else is requested) and
+      // the first staging pass over it
+      const PhaseW w = down_w(Ly);
+      const int nu = f / 8;
+      constexpr int HB = 4;  // units per thread and batch: f <= 16384 in one batch
+      float mx = 0.f;
+      for (int base0 = warp * 32; base0 < nu; base0 += HB * WT_THREADS) {
+        uint4 hv[HB];
+        read_units<HB>(a.hw, base0, nu, tag, hv, wt, lane);
+#pragma unroll
+        for (int k = 0; k < HB; ++k) {
+          const int base = base0 + k * WT_THREADS;
+          if (base < nu) x_unit<FMT>(a.dn, smD, base + lane < nu ? base + lane : -1, hv[k], mx);
+        }
+      }
+      // the first two tasks, in flight during the second staging pass
+      wt_load<1>(a.dn, w, cd, tA, bufA, pol, lane);
+      wt_load<1>(a.dn, w, cd, tB, bufB, pol, lane);
+      wt_prefetch<1>(a.dn, w, cd, tA + 2 * WARP_TASK_WARPS, lane);
+      wt_prefetch<1>(a.dn, w, cd, tB + 2 * WARP_TASK_WARPS, lane);
+      cp_async_wait_all();  // scales and biases (long complete)
+      if (!__syncthreads_and(wt.ok)) return;
+      const float xinv = x_convert<FMT>(a.dn, smD, mx, red, tid);
+      if (l + 1 < a.L) {  // the next gate/up phase's, during this loop
+        stage_gateup_smem(l + 1);
+        cp_async_commit();
+      }
+      wt_run<FMT, 1>(a.dn, w, cd, smD, bufA, bufB, tA, tB, &task_ctr, xinv, pol, lane);
+      __syncthreads();
+      // epilogue: y = h . Wd[n] + summed_l[n]; summed_{l+1} = values_{l+1} + y
+      const bool last = l + 1 == a.L;
+      const bool have = tid < npair_d;
+      uint32_t y2 = 0;
+      if (have) {
+        uint16_t yb[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int n = cd.r_begin + 2 * tid + e;
+          yb[e] = f2bf(row_total<1>(a.dn, smD.parts, 2 * tid + e, 0) + bf16f(ssm[n]));
+        }
+        y2 = pack2(yb[0], yb[1]);
+        if (a.tr_y) *reinterpret_cast<uint32_t*>(a.tr_y + (size_t)l * d + cd.r_begin + 2 * tid) = y2;
+        if (last) *reinterpret_cast<uint32_t*>(a.out_y + cd.r_begin + 2 * tid) = y2;
+      }
+      if (last) break;
+      publish_summed(l + 1, vnx, y2, have);
+      prefetch_gateup(l + 1);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+struct StackPlanImpl {
+  int dev;
+  int L, d, f, group, fmt;
+  float eps;
+  int grid;
+  size_t smem;
+  StackArgs base;       // geometry, layer table, workspace and smem offsets
+  void* alloc;          // device allocation owned by the plan
+  void* run_state;      // start of what is zeroed before each run (control line + words)
+  size_t run_state_bytes;
+  const void* kernel;   // mlp_stack_kernel<FMT>
+};
+
+template <int FMT>
+static bool plan_stack(StackPlanImpl* P, const DeviceInfo* di) {
+  size_t pg = 0, pd = 0;
+  const int grid = di->sm_count;
+  if (grid > STACK_MAX_GRID) return false;
+  StackArgs& a = P->base;
+  // rows in pairs: every published word has one writer
+  if (!plan_phase<FMT, 0>(P->d, P->f, P->group, grid, &a.gu, &pg, 2)) return false;
+  if (!plan_phase<FMT, 1>(P->f, P->d, P->group, grid, &a.dn, &pd, 2)) return false;
+  if (a.dn.rows_alloc > 2 * WT_THREADS) return false;  // one pair of down rows per thread
+  const int Kmax = P->d > P->f ? P->d : P->f;
+  size_t off = (size_t)Kmax * 2;  // xraw
+  a.off_xs = (int)off; off += xs_bytes<FMT>(Kmax);
+  // gate/up arrays: gsum, sbr, parts (plan_phase's sizes, 16-byte multiples)
+  const bool AFF = FmtTraits<FMT>::AFFINE;
+  const size_t gsum_g = AFF ? (size_t)(a.gu.G + 3) / 4 * 16 : 0;
+  const size_t sbr_g = AFF ? (size_t)4 * a.gu.sb_stride * 2 : 0;
+  a.off_gsum_g = (int)off; off += gsum_g;
+  a.off_sbr_g = (int)off; off += sbr_g;
+  a.off_parts_g = (int)off; off += pg - gsum_g - sbr_g;
+  const size_t gsum_d = AFF ? (size_t)(a.dn.G + 3) / 4 * 16 : 0;
+  const size_t sbr_d = AFF ? (size_t)2 * a.dn.sb_stride * 2 : 0;
+  a.off_gsum_d = (int)off; off += gsum_d;
+  a.off_sbr_d = (int)off; off += sbr_d;
+  a.off_parts_d = (int)off; off += pd - gsum_d - sbr_d;
+  a.off_wn = (int)off; off += (size_t)P->d * 2;
+  a.off_ssm = (int)off; off += (size_t)P->d * 2;
+  P->smem = off;
+  P->grid = grid;
+  P->kernel = reinterpret_cast<const void*>(mlp_stack_kernel<FMT>);
+  return true;
+}
+
+static bool is16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace mt
+
+struct mt_mlp_plan {
+  mt::StackPlanImpl impl;
+};
+
+using namespace mt;
+
+extern "C" mt_status mt_mlp_plan_create(const mt_mlp_layer* layers, int L, int d, int f,
+                                        int group, mt_wfmt fmt, float eps, mt_mlp_plan** plan) {
+  if (!plan) return MT_ERR_NULL;
+  *plan = nullptr;
+  if (!layers) return MT_ERR_NULL;
+  if (fmt != MT_W_BF16 && fmt != MT_W_AFFINE8 && fmt != MT_W_AFFINE4) return MT_ERR_FORMAT;
+  if (L < 1 || L > 4096 || d < 8 || f < 8 || d > 32768 || f > 32768 || d % 8 || f % 8)
+    return MT_ERR_SHAPE;
+  if (!(eps >= 0.f) || !isfinite(eps)) return MT_ERR_SHAPE;
+  if (fmt == MT_W_BF16) {
+    if (group != 0) return MT_ERR_GROUP;
+  } else {
+    if (group != 32 && group != 64 && group != 128) return MT_ERR_GROUP;
+    if (d % group || f % group) return MT_ERR_SHAPE;
+  }
+  const bool aff = fmt != MT_W_BF16;
+  for (int l = 0; l < L; ++l) {
+    const mt_mlp_layer& y = layers[l];
+    if (!y.norm_weight || !y.Wg || !y.Wu || !y.Wd) return MT_ERR_NULL;
+    if (aff && (!y.gu_scales || !y.gu_biases || !y.d_scales || !y.d_biases)) return MT_ERR_NULL;
+    if (!is16(y.norm_weight) || !is16(y.Wg) || !is16(y.Wu) || !is16(y.Wd)) return MT_ERR_ALIGN;
+    if (aff && (!is16(y.gu_scales) || !is16(y.gu_biases) || !is16(y.d_scales) || !is16(y.d_biases)))
+      return MT_ERR_ALIGN;
+  }
+  int derr = 0;
+  const DeviceInfo* di = device_info(&derr);
+  if (!di) return cuda_fail((cudaError_t)derr);
+
+  StackPlanImpl P = {};
+  cudaError_t ce = cudaGetDevice(&P.dev);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  P.L = L; P.d = d; P.f = f; P.group = aff ? group : 0; P.fmt = fmt; P.eps = eps;
+  bool ok = false;
+  if (fmt == MT_W_AFFINE8) ok = plan_stack<FMT_A8>(&P, di);
+  else if (fmt == MT_W_AFFINE4) ok = plan_stack<FMT_A4>(&P, di);
+  else ok = plan_stack<FMT_BF16>(&P, di);
+  if (!ok) return MT_ERR_SHAPE;
+  const size_t budget = (size_t)di->max_smem_optin - 1024;  // static smem and slack
+  if (P.smem > budget) return MT_ERR_SHAPE;
+  // the opt-in maximum, so that plans of different sizes never shrink it
+  ce = cudaFuncSetAttribute(P.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  int occ = 0;
+  ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, P.kernel, WT_THREADS, P.smem);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  if (occ < 1) return MT_ERR_SHAPE;
+
+  // device memory: [layer table | control line | qw | sw | hw | hd]; everything
+  // after the table is zeroed before each run
+  const size_t tab = ((size_t)L * sizeof(StackLayerDev) + 127) / 128 * 128;
+  const size_t o_ctl = tab, o_qw = o_ctl + 128;
+  const size_t o_sw = o_qw + ((size_t)P.grid * 8 + 127) / 128 * 128;
+  const size_t o_hw = o_sw + ((size_t)d / 2 * 8 + 127) / 128 * 128;
+  const size_t o_hd = o_hw + ((size_t)f / 2 * 8 + 127) / 128 * 128;
+  const size_t total = o_hd + ((size_t)P.grid * 8 + 127) / 128 * 128;
+  StackLayerDev* host_tab = new (std::nothrow) StackLayerDev[L];
+  if (!host_tab) return MT_ERR_SHAPE;
+  for (int l = 0; l < L; ++l) {
+    const mt_mlp_layer& y = layers[l];
+    StackLayerDev& t = host_tab[l];
+    t.wn = (const uint16_t*)y.norm_weight;
+    t.Wg = (const uint8_t*)y.Wg; t.Wu = (const uint8_t*)y.Wu; t.Wd = (const uint8_t*)y.Wd;
+    if (aff) {
+      const size_t plane = (size_t)f * (d / group);
+      t.sg = (const uint16_t*)y.gu_scales; t.su = t.sg + plane;
+      t.bg = (const uint16_t*)y.gu_biases; t.bu = t.bg + plane;
+      t.sd = (const uint16_t*)y.d_scales; t.bd = (const uint16_t*)y.d_biases;
+    } else {
+      t.sg = t.su = t.bg = t.bu = t.sd = t.bd = nullptr;
+    }
+  }
+  void* mem = nullptr;
+  ce = cudaMalloc(&mem, total);
+  if (ce != cudaSuccess) { delete[] host_tab; return cuda_fail(ce); }
+  ce = cudaMemcpy(mem, host_tab, (size_t)L * sizeof(StackLayerDev), cudaMemcpyHostToDevice);
+  delete[] host_tab;
+  if (ce == cudaSuccess) ce = cudaMemset(static_cast<char*>(mem) + o_ctl, 0, total - o_ctl);
+  if (ce != cudaSuccess) { cudaFree(mem); return cuda_fail(ce); }
+  int* err = device_error_ptr();
+  if (!err) { cudaFree(mem); return cuda_fail(cudaErrorInvalidSymbol); }
+
+  StackArgs& a = P.base;
+  char* base = static_cast<char*>(mem);
+  a.layers = reinterpret_cast<const StackLayerDev*>(base);
+  a.ctl = reinterpret_cast<StackCtl*>(base + o_ctl);
+  a.qw = reinterpret_cast<uint64_t*>(base + o_qw);
+  a.sw = reinterpret_cast<uint64_t*>(base + o_sw);
+  a.hw = reinterpret_cast<uint64_t*>(base + o_hw);
+  a.hd = reinterpret_cast<uint64_t*>(base + o_hd);
+  P.run_state = base + o_ctl;
+  P.run_state_bytes = total - o_ctl;
+  a.L = L; a.d = d; a.f = f; a.eps = eps;
+  a.pre_g = STACK_PRE_GATEUP;
+  a.pre_d = STACK_PRE_DOWN;
+  a.err = err;
+  P.alloc = mem;
+
+  mt_mlp_plan* out = new (std::nothrow) mt_mlp_plan;
+  if (!out) { cudaFree(mem); return MT_ERR_SHAPE; }
+  out->impl = P;
+  *plan = out;
+  return MT_OK;
+}
+
+extern "C" mt_status mt_mlp_plan_run(const mt_mlp_plan* plan, const void* values,
+                                     const void* residual, void* out_y, const mt_mlp_trace* trace,
+                                     void* stream) {
+  if (!plan || !values || !residual || !out_y) return MT_ERR_NULL;
+  const StackPlanImpl& P = plan->impl;
+  if (!is16(values) || !is16(residual) || !is16(out_y)) return MT_ERR_ALIGN;
+  StackArgs a = P.base;
+  a.values = (const uint16_t*)values;
+  a.residual = (const uint16_t*)residual;
+  a.out_y = (uint16_t*)out_y;
+  if (trace) {
+    a.tr_sum = (uint16_t*)trace->out_sum;
+    a.tr_norm = (uint16_t*)trace->out_norm;
+    a.tr_h = (uint16_t*)trace->h;
+    a.tr_y = (uint16_t*)trace->y;
+  }
+  // out_y may equal residual; no other overlap among inputs and outputs
+  const uintptr_t yb = (uintptr_t)out_y, ye = yb + (size_t)P.d * 2;
+  auto hits = [&](const void* p, size_t n) {
+    const uintptr_t b = (uintptr_t)p;
+    return p && b < ye && yb < b + n;
+  };
+  if (hits(values, (size_t)P.L * P.d * 2)) return MT_ERR_ALIAS;
+  if (hits(residual, (size_t)P.d * 2) && residual != out_y) return MT_ERR_ALIAS;
+  if (trace) {
+    const void* tr[4] = {trace->out_sum, trace->out_norm, trace->h, trace->y};
+    const size_t tn[4] = {(size_t)P.L * P.d * 2, (size_t)P.L * P.d * 2, (size_t)P.L * P.f * 2,
+                          (size_t)P.L * P.d * 2};
+    for (int i = 0; i < 4; ++i) {
+      if (tr[i] && !is16(tr[i])) return MT_ERR_ALIGN;
+      if (hits(tr[i], tn[i])) return MT_ERR_ALIAS;
+      const uintptr_t b = (uintptr_t)tr[i];
+      const uintptr_t vb = (uintptr_t)values, rb = (uintptr_t)residual;
+      if (tr[i] && ((b < vb + (size_t)P.L * P.d * 2 && vb < b + tn[i]) ||
+                    (b < rb + (size_t)P.d * 2 && rb < b + tn[i])))
+        return MT_ERR_ALIAS;
+    }
+  }
+  int dev = -1;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  if (dev != P.dev) return cuda_fail(cudaErrorInvalidDevice);
+  cudaStream_t s = (cudaStream_t)stream;
+  ce = cudaMemsetAsync(P.run_state, 0, P.run_state_bytes, s);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P.grid);
+  cfg.blockDim = dim3(WT_THREADS);
+  cfg.dynamicSmemBytes = P.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&a};
+  ce = cudaLaunchKernelExC(&cfg, P.kernel, args);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  return MT_OK;
+}
+
+extern "C" mt_status mt_mlp_plan_destroy(mt_mlp_plan* plan) {
+  if (!plan) return MT_ERR_NULL;
+  cudaError_t ce = cudaSuccess;
+  if (plan->impl.alloc) ce = cudaFree(plan->impl.alloc);
+  delete plan;
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  return MT_OK;
+}

@@ -166,3 +166,50 @@ def test_status_strings_and_options(lib):
     assert lib.mt_set_option(0, 1) == 0 and lib.mt_get_option(0) == 1
     assert lib.mt_set_option(5, 1) == FORMAT
     assert lib.mt_version() >> 16 == 1
+
+
+class _Layer(ctypes.Structure):
+    _fields_ = [(n, P) for n in ("norm_weight", "Wg", "Wu", "gu_scales", "gu_biases", "Wd",
+                                 "d_scales", "d_biases")]
+
+
+def _create(lib, layers, L, d=256, f=768, g=64, fmt=1, eps=1e-5, plan=True):
+    fn = lib.mt_mlp_plan_create
+    fn.restype = ctypes.c_int
+    fn.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_float, P]
+    out = P()
+    return fn(layers, L, d, f, g, fmt, eps, ctypes.byref(out) if plan else None)
+
+
+def test_mlp_plan_validation(lib):
+    """mt_mlp_plan_create / run / destroy refuse invalid arguments before any
+    CUDA call (so these run without a device)."""
+    arr = (_Layer * 2)()
+    for i in range(2):
+        for j, (name, _) in enumerate(_Layer._fields_):
+            setattr(arr[i], name, A[j] + 0x1000 * i)
+    assert _create(lib, arr, 2, plan=False) == NULL
+    assert _create(lib, None, 2) == NULL
+    assert _create(lib, arr, 0) == SHAPE
+    assert _create(lib, arr, 2, d=260) == SHAPE          # d % 8 != 0
+    assert _create(lib, arr, 2, f=40000) == SHAPE
+    assert _create(lib, arr, 2, d=96) == SHAPE           # d % group != 0
+    assert _create(lib, arr, 2, eps=-1.0) == SHAPE
+    assert _create(lib, arr, 2, g=48) == GROUP
+    assert _create(lib, arr, 2, fmt=0) == GROUP          # bf16 takes group 0
+    assert _create(lib, arr, 2, fmt=4) == FORMAT
+    arr[1].Wd = None
+    assert _create(lib, arr, 2) == NULL
+    arr[1].Wd = A[5] + 0x1000
+    arr[1].d_scales = None
+    assert _create(lib, arr, 2) == NULL
+    arr[1].d_scales = A[6] + 0x1008                        # misaligned scales
+    assert _create(lib, arr, 2) == ALIGN
+    run = lib.mt_mlp_plan_run
+    run.restype = ctypes.c_int
+    run.argtypes = [P, P, P, P, P, P]
+    assert run(None, A[0], A[1], A[2], None, None) == NULL
+    lib.mt_mlp_plan_destroy.restype = ctypes.c_int
+    lib.mt_mlp_plan_destroy.argtypes = [P]
+    assert lib.mt_mlp_plan_destroy(None) == NULL

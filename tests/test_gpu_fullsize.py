@@ -13,6 +13,7 @@ import torch
 
 import oracle
 import synth
+from gpu_layers import DevLayer, full_oracle_layer, host_acts, run_layer
 from parity_util import assert_bf16_close, assert_f32_close, dev_bf16, host_bits, host_f64
 
 pytestmark = pytest.mark.gpu
@@ -27,90 +28,15 @@ def mt():
     return m
 
 
-class DevLayer:
-    """One layer's weights generated on the device and packed by the library."""
-
-    def __init__(self, mt, wl, layer):
-        self.wl, self.l = wl, layer
-        d, f, g = wl.d, wl.f, wl.group
-        sd = lambda t: synth.seed_for(wl.wid, layer, t)
-        self.sd = sd
-        bf = torch.bfloat16
-        self.w = torch.empty(d, dtype=bf, device="cuda")
-        synth.device_bf16(self.w, sd(synth.T_NORM_W), synth.NORM_W)
-        if wl.fmt == synth.FMT_BF16:
-            self.Wg = torch.empty(f, d, dtype=bf, device="cuda")
-            self.Wu = torch.empty(f, d, dtype=bf, device="cuda")
-            self.Wd = torch.empty(d, f, dtype=bf, device="cuda")
-            for W, t in ((self.Wg, synth.T_WG), (self.Wu, synth.T_WU), (self.Wd, synth.T_WD)):
-                synth.device_bf16(W, sd(t), wl.weight_dist)
-            self.sgu = self.bgu = self.sdn = self.bdn = None
-        else:
-            b = wl.bits
-            self.Wg = torch.empty(f, d * b // 8, dtype=torch.uint8, device="cuda")
-            self.Wu = torch.empty_like(self.Wg)
-            self.Wd = torch.empty(d, f * b // 8, dtype=torch.uint8, device="cuda")
-            self.sgu = torch.empty(2, f, d // g, dtype=bf, device="cuda")
-            self.bgu = torch.empty_like(self.sgu)
-            self.sdn = torch.empty(d, f // g, dtype=bf, device="cuda")
-            self.bdn = torch.empty_like(self.sdn)
-            tmp = torch.empty(d * f, dtype=torch.float32, device="cuda")
-            for (dst, s_, b_, N, K, t) in ((self.Wg, self.sgu[0], self.bgu[0], f, d, synth.T_WG),
-                                           (self.Wu, self.sgu[1], self.bgu[1], f, d, synth.T_WU),
-                                           (self.Wd, self.sdn, self.bdn, d, f, synth.T_WD)):
-                W32 = tmp[:N * K].view(N, K)
-                synth.device_f32(W32, sd(t), wl.weight_dist)
-                mt.mt_pack_affine(W32, N, K, g, b, dst, s_, b_)
-            del tmp
-        torch.cuda.synchronize()
-
-    def oracle_rows(self, tensor, rows, N, K):
-        """Oracle-side weight rows [rows] of matrix `tensor` ([N][K])."""
-        wl = self.wl
-        W32 = np.stack([synth.host_f32(K, self.sd(tensor), wl.weight_dist, offset=int(n) * K) for n in rows])
-        return oracle.Weight.from_f32(W32, wl.bits, wl.group)
-
-
-def _run_layer(mt, L, v, r, M):
-    wl = L.wl
-    d, f = wl.d, wl.f
-    out_sum = torch.empty(M, d, dtype=torch.bfloat16, device="cuda")
-    out_norm = torch.empty_like(out_sum)
-    h = torch.empty(M, f, dtype=torch.bfloat16, device="cuda")
-    y = torch.empty(M, d, dtype=torch.bfloat16, device="cuda")
-    mt.mt_add_rmsnorm(v, r, L.w, wl.eps, out_sum, out_norm)
-    mt.mt_swiglu_gateup(out_norm, L.Wg, L.Wu, L.sgu, L.bgu, wl.group, h, fmt=wl.fmt)
-    mt.mt_down_residual(h, L.Wd, L.sdn, L.bdn, wl.group, out_sum, y, fmt=wl.fmt)
-    torch.cuda.synchronize()
-    return out_sum, out_norm, h, y
-
-
-def _host_acts(wl, layer, M):
-    sd = lambda t: synth.seed_for(wl.wid, layer, t)
-    v = synth.host_bf16(M * wl.d, sd(synth.T_VALUES), synth.ACT).reshape(M, wl.d)
-    r = synth.host_bf16(M * wl.d, synth.seed_for(wl.wid, 0, synth.T_RESIDUAL), synth.ACT).reshape(M, wl.d)
-    w = synth.host_bf16(wl.d, sd(synth.T_NORM_W), synth.NORM_W)
-    return v, r, w
-
-
-def _full_oracle_layer(L, v, r, w):
-    wl = L.wl
-    d, f = wl.d, wl.f
-    Wg = L.oracle_rows(synth.T_WG, range(f), f, d)
-    Wu = L.oracle_rows(synth.T_WU, range(f), f, d)
-    Wd = L.oracle_rows(synth.T_WD, range(d), d, f)
-    return oracle.mlp_layer(v, r, w, wl.eps, Wg, Wu, Wd), (Wg, Wu, Wd)
-
-
 @pytest.mark.parametrize("wl", [synth.LLAMA1B, synth.QWEN15, synth.TINY], ids=lambda w: w.name.split()[0])
 def test_layer_full(mt, wl):
     """Every output of one layer: the chained layer, and each kernel on the
     oracle's own inputs (so each kernel is judged on its own error)."""
     M = wl.M
     L = DevLayer(mt, wl, 0)
-    v, r, w = _host_acts(wl, 0, M)
-    ref, (Wg, Wu, Wd) = _full_oracle_layer(L, v, r, w)
-    out_sum, out_norm, h, y = _run_layer(mt, L, dev_bf16(v), dev_bf16(r), M)
+    v, r, w = host_acts(wl, 0, M)
+    ref, (Wg, Wu, Wd) = full_oracle_layer(L, v, r, w)
+    out_sum, out_norm, h, y = run_layer(mt, L, dev_bf16(v), dev_bf16(r), M)
     assert np.array_equal(host_bits(L.w), w), "device and host generators differ"
     assert np.array_equal(host_bits(out_sum), ref["out_sum"])
     assert_bf16_close(host_bits(out_norm), ref["norm_x"], "out_norm")
@@ -133,9 +59,9 @@ def test_qwen3_8b_stack_layers(mt):
     wl = synth.QWEN8B
     d, f, M, g = wl.d, wl.f, wl.M, wl.group
     L0 = DevLayer(mt, wl, 0)
-    v, r, w = _host_acts(wl, 0, M)
-    ref, (Wg, Wu, Wd) = _full_oracle_layer(L0, v, r, w)
-    out_sum, out_norm, h, y = _run_layer(mt, L0, dev_bf16(v), dev_bf16(r), M)
+    v, r, w = host_acts(wl, 0, M)
+    ref, (Wg, Wu, Wd) = full_oracle_layer(L0, v, r, w)
+    out_sum, out_norm, h, y = run_layer(mt, L0, dev_bf16(v), dev_bf16(r), M)
     assert np.array_equal(host_bits(out_sum), ref["out_sum"])
     assert_bf16_close(host_bits(out_norm), ref["norm_x"], "out_norm")
     assert_bf16_close(host_bits(y), ref["y_x"], "y (chained)")

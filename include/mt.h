@@ -254,6 +254,38 @@ mt_status mt_mlp_plan_run(const mt_mlp_plan* plan, const void* values, const voi
                           void* out_y, const mt_mlp_trace* trace, void* stream);
 mt_status mt_mlp_plan_destroy(mt_mlp_plan* plan);
 
+/*
+ * The same L-layer pass as mt_mlp_plan_run, for callers that cannot let the
+ * library allocate device memory: engines that reserve the device's memory up
+ * front for their own pool (an allocation by the library would fail or take
+ * memory the engine has already planned) and code that must not synchronise
+ * the device (cudaMalloc and cudaFree may).  The meTile pages have no
+ * counterpart to this call: their executor is built once together with its
+ * memory.
+ *   layers, L, d, f, group, fmt, eps : as for mt_mlp_plan_create (layers is a
+ *            host array, read during the call; it may be freed afterwards)
+ *   values, residual, out_y, stream  : as for mt_mlp_plan_run (no trace)
+ * Scratch.  The layer table and the hand-off words live in one static device
+ * array of MT_STACK_SCRATCH_BYTES bytes per device:
+ *   128*ceil(80 L / 128) + 128 + 2 * 128*ceil(8 S / 128)
+ *     + 128*ceil(4 d / 128) + 128*ceil(4 f / 128)      bytes, S = SM count
+ * (71,168 bytes for 36 layers of d = 4096, f = 12288 on 152 SMs).  Larger
+ * problems return MT_ERR_SHAPE.  Each call uploads the table
+ * (cudaMemcpyAsync from host memory) and zeroes the rest (cudaMemsetAsync) on
+ * `stream` before the kernel; it calls no allocating routine.
+ * Set-up.  The first call on a device, made with that device current, looks
+ * up the array's device address (cudaGetSymbolAddress) and sets the kernel's
+ * shared-memory limit; make that first call before any stream capture.
+ * Concurrency.  Every call on a device uses the same array: calls that can
+ * overlap in time (other streams, or calls not ordered by the caller) race
+ * and give undefined results.
+ * Errors.  As for mt_mlp_plan_create and mt_mlp_plan_run.
+ */
+#define MT_STACK_SCRATCH_BYTES 262144
+mt_status mt_mlp_stack_run_noalloc(const mt_mlp_layer* layers, int L, int d, int f, int group,
+                                   mt_wfmt fmt, float eps, const void* values,
+                                   const void* residual, void* out_y, void* stream);
+
 /* Library options.  Returns MT_ERR_FORMAT for an unknown option. */
 mt_status mt_set_option(mt_option opt, int value);
 int mt_get_option(mt_option opt);

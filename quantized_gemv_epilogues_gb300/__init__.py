@@ -14,6 +14,7 @@ Calls (same names as the C ABI):
 * :func:`mt_pack_affine` / :func:`mt_unpack_affine` -- affine group packer.
 * :func:`mt_mlp_plan_create` / :func:`mt_mlp_plan_run` / :func:`mt_mlp_plan_destroy`
   -- the warmed executor: L one-row layers as one persistent kernel.
+* :func:`mt_mlp_stack_run_noalloc` -- the same pass without any allocation.
 
 Tensors are ``torch.Tensor`` on the current CUDA device (bf16 activations,
 uint8 packed codes, bf16 scales/biases); raw integer device pointers are also
@@ -56,6 +57,7 @@ _SIGS = {
     "mt_mlp_plan_create": (_I, [_P, _I, _I, _I, _I, _I, _F, _P]),
     "mt_mlp_plan_run": (_I, [_P, _P, _P, _P, _P, _P]),
     "mt_mlp_plan_destroy": (_I, [_P]),
+    "mt_mlp_stack_run_noalloc": (_I, [_P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -196,6 +198,19 @@ def mt_mlp_plan_run(plan, values, residual, out_y, trace=None, stream=None) -> N
 
 def mt_mlp_plan_destroy(plan) -> None:
     _check(_lib.mt_mlp_plan_destroy(plan), "mt_mlp_plan_destroy")
+
+
+def mt_mlp_stack_run_noalloc(layers, d, f, group, fmt, eps, values, residual, out_y,
+                             stream=None) -> None:
+    """The stack pass with the library's static scratch instead of a plan's
+    memory (see include/mt.h)."""
+    arr = (MlpLayer * len(layers))()
+    for i, ly in enumerate(layers):
+        for name, _ in MlpLayer._fields_:
+            setattr(arr[i], name, _ptr(ly.get(name)))
+    _check(_lib.mt_mlp_stack_run_noalloc(arr, len(layers), int(d), int(f), int(group), int(fmt),
+                                         float(eps), _ptr(values), _ptr(residual), _ptr(out_y),
+                                         _stream(stream)), "mt_mlp_stack_run_noalloc")
 
 
 def mt_set_option(opt: int, value: int) -> None:

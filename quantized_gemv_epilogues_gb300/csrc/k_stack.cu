@@ -743,3 +743,178 @@ extern "C" mt_status mt_mlp_plan_destroy(mt_mlp_plan* plan) {
   if (ce != cudaSuccess) return cuda_fail(ce);
   return MT_OK;
 }
+
+// ------------------------------------------- the stack without any allocation
+//
+// mt_mlp_stack_run_noalloc runs the same kernel as mt_mlp_plan_run, but its
+// layer table and hand-off words live in a file-scope static device array
+// instead of memory a plan allocates.  It is for callers that cannot let the
+// library allocate device memory: engines that reserve the device's memory up
+// front for their own pool (a cudaMalloc by the library would fail, or carve
+// memory out of a budget the engine has already planned) and code that must
+// not synchronise the device (cudaMalloc and cudaFree may).  The array is
+// shared by every call on a device, so calls that overlap in time race.
+static __device__ __align__(256) unsigned char g_stack_scratch[MT_STACK_SCRATCH_BYTES];
+
+namespace mt {
+
+// Per-device one-time set-up: the scratch's device address (with the device
+// current) and the kernel's shared-memory limit.  Guarded by a mutex.
+struct NoallocState {
+  std::mutex mu;
+  void* scratch[64];
+  bool attr_set[3][64];
+};
+static NoallocState g_noalloc;
+
+static mt_status noalloc_setup(int dev, int fmt, const void* kernel, size_t smem_limit,
+                               void** scratch) {
+  if (dev < 0 || dev >= 64) return cuda_fail(cudaErrorInvalidDevice);
+  std::lock_guard<std::mutex> g(g_noalloc.mu);
+  if (!g_noalloc.scratch[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_stack_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_noalloc.scratch[dev] = p;
+  }
+  if (!g_noalloc.attr_set[fmt][dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_limit);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_noalloc.attr_set[fmt][dev] = true;
+  }
+  *scratch = g_noalloc.scratch[dev];
+  return MT_OK;
+}
+
+static size_t round128(size_t n) { return (n + 127) / 128 * 128; }
+
+}  // namespace mt
+
+extern "C" mt_status mt_mlp_stack_run_noalloc(const mt_mlp_layer* layers, int L, int d, int f,
+                                              int group, mt_wfmt fmt, float eps,
+                                              const void* values, const void* residual,
+                                              void* out_y, void* stream) {
+  // ---- arguments (nothing touches the device before these pass)
+  if (!layers || !values || !residual || !out_y) return MT_ERR_NULL;
+  if (fmt != MT_W_BF16 && fmt != MT_W_AFFINE8 && fmt != MT_W_AFFINE4) return MT_ERR_FORMAT;
+  if (L < 1 || L > 4096 || d < 8 || f < 8 || d > 32768 || f > 32768 || d % 8 || f % 8)
+    return MT_ERR_SHAPE;
+  if (!(eps >= 0.f) || !isfinite(eps)) return MT_ERR_SHAPE;
+  if (fmt == MT_W_BF16) {
+    if (group != 0) return MT_ERR_GROUP;
+  } else {
+    if (group != 32 && group != 64 && group != 128) return MT_ERR_GROUP;
+    if (d % group || f % group) return MT_ERR_SHAPE;
+  }
+  const bool aff = fmt != MT_W_BF16;
+  for (int l = 0; l < L; ++l) {
+    const mt_mlp_layer& y = layers[l];
+    if (!y.norm_weight || !y.Wg || !y.Wu || !y.Wd) return MT_ERR_NULL;
+    if (aff && (!y.gu_scales || !y.gu_biases || !y.d_scales || !y.d_biases)) return MT_ERR_NULL;
+    if (!is16(y.norm_weight) || !is16(y.Wg) || !is16(y.Wu) || !is16(y.Wd)) return MT_ERR_ALIGN;
+    if (aff && (!is16(y.gu_scales) || !is16(y.gu_biases) || !is16(y.d_scales) || !is16(y.d_biases)))
+      return MT_ERR_ALIGN;
+  }
+  if (!is16(values) || !is16(residual) || !is16(out_y)) return MT_ERR_ALIGN;
+  {
+    const uintptr_t yb = (uintptr_t)out_y, ye = yb + (size_t)d * 2;
+    const uintptr_t vb = (uintptr_t)values, ve = vb + (size_t)L * d * 2;
+    const uintptr_t rb = (uintptr_t)residual, re = rb + (size_t)d * 2;
+    if (vb < ye && yb < ve) return MT_ERR_ALIAS;
+    if (rb < ye && yb < re && residual != out_y) return MT_ERR_ALIAS;
+  }
+
+  // ---- geometry (host arithmetic) and the scratch it needs
+  int derr = 0;
+  const DeviceInfo* di = device_info(&derr);
+  if (!di) return cuda_fail((cudaError_t)derr);
+  StackPlanImpl P = {};
+  cudaError_t ce = cudaGetDevice(&P.dev);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  P.L = L; P.d = d; P.f = f; P.group = aff ? group : 0; P.fmt = fmt; P.eps = eps;
+  bool ok = false;
+  if (fmt == MT_W_AFFINE8) ok = plan_stack<FMT_A8>(&P, di);
+  else if (fmt == MT_W_AFFINE4) ok = plan_stack<FMT_A4>(&P, di);
+  else ok = plan_stack<FMT_BF16>(&P, di);
+  if (!ok) return MT_ERR_SHAPE;
+  const size_t budget = (size_t)di->max_smem_optin - 1024;  // static smem and slack
+  if (P.smem > budget) return MT_ERR_SHAPE;
+  // scratch layout: [layer table | control line | qw | sw | hw | hd]
+  const size_t o_ctl = round128((size_t)L * sizeof(StackLayerDev));
+  const size_t o_qw = o_ctl + 128;
+  const size_t o_sw = o_qw + round128((size_t)P.grid * 8);
+  const size_t o_hw = o_sw + round128((size_t)d / 2 * 8);
+  const size_t o_hd = o_hw + round128((size_t)f / 2 * 8);
+  const size_t total = o_hd + round128((size_t)P.grid * 8);
+  if (total > (size_t)MT_STACK_SCRATCH_BYTES) return MT_ERR_SHAPE;
+
+  // ---- one-time set-up of this device, then the launch
+  void* scratch = nullptr;
+  const mt_status st = noalloc_setup(P.dev, (int)fmt, P.kernel, budget, &scratch);
+  if (st != MT_OK) return st;
+  int occ = 0;
+  ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, P.kernel, WT_THREADS, P.smem);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  if (occ < 1) return MT_ERR_SHAPE;
+  int* err = device_error_ptr();
+  if (!err) return cuda_fail(cudaErrorInvalidSymbol);
+  cudaStream_t s = (cudaStream_t)stream;
+  char* base = static_cast<char*>(scratch);
+  // the layer table, converted in chunks on the host stack; copies from
+  // pageable memory are staged before cudaMemcpyAsync returns
+  constexpr int CHUNK = 32;
+  for (int l0 = 0; l0 < L; l0 += CHUNK) {
+    StackLayerDev tab[CHUNK];
+    const int n = L - l0 < CHUNK ? L - l0 : CHUNK;
+    for (int i = 0; i < n; ++i) {
+      const mt_mlp_layer& y = layers[l0 + i];
+      StackLayerDev& t = tab[i];
+      t.wn = (const uint16_t*)y.norm_weight;
+      t.Wg = (const uint8_t*)y.Wg; t.Wu = (const uint8_t*)y.Wu; t.Wd = (const uint8_t*)y.Wd;
+      if (aff) {
+        const size_t plane = (size_t)f * (d / group);
+        t.sg = (const uint16_t*)y.gu_scales; t.su = t.sg + plane;
+        t.bg = (const uint16_t*)y.gu_biases; t.bu = t.bg + plane;
+        t.sd = (const uint16_t*)y.d_scales; t.bd = (const uint16_t*)y.d_biases;
+      } else {
+        t.sg = t.su = t.bg = t.bu = t.sd = t.bd = nullptr;
+      }
+    }
+    ce = cudaMemcpyAsync(base + (size_t)l0 * sizeof(StackLayerDev), tab,
+                         (size_t)n * sizeof(StackLayerDev), cudaMemcpyHostToDevice, s);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+  }
+  // the control line and the hand-off words must start at zero
+  ce = cudaMemsetAsync(base + o_ctl, 0, total - o_ctl, s);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+
+  StackArgs a = P.base;
+  a.layers = reinterpret_cast<const StackLayerDev*>(base);
+  a.ctl = reinterpret_cast<StackCtl*>(base + o_ctl);
+  a.qw = reinterpret_cast<uint64_t*>(base + o_qw);
+  a.sw = reinterpret_cast<uint64_t*>(base + o_sw);
+  a.hw = reinterpret_cast<uint64_t*>(base + o_hw);
+  a.hd = reinterpret_cast<uint64_t*>(base + o_hd);
+  a.L = L; a.d = d; a.f = f; a.eps = eps;
+  a.err = err;
+  a.pre_g = STACK_PRE_GATEUP;
+  a.pre_d = STACK_PRE_DOWN;
+  a.values = (const uint16_t*)values;
+  a.residual = (const uint16_t*)residual;
+  a.out_y = (uint16_t*)out_y;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P.grid);
+  cfg.blockDim = dim3(WT_THREADS);
+  cfg.dynamicSmemBytes = P.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&a};
+  ce = cudaLaunchKernelExC(&cfg, P.kernel, args);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  return MT_OK;
+}

@@ -213,3 +213,29 @@ def test_mlp_plan_validation(lib):
     lib.mt_mlp_plan_destroy.restype = ctypes.c_int
     lib.mt_mlp_plan_destroy.argtypes = [P]
     assert lib.mt_mlp_plan_destroy(None) == NULL
+
+
+def test_noalloc_validation(lib):
+    """mt_mlp_stack_run_noalloc refuses invalid arguments before any CUDA call."""
+    fn = lib.mt_mlp_stack_run_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_float, P, P, P, P]
+    arr = (_Layer * 2)()
+    for i in range(2):
+        for j, (name, _) in enumerate(_Layer._fields_):
+            setattr(arr[i], name, A[j] + 0x1000 * i)
+    v, r, y = A[9], A[10], A[11]
+
+    def call(layers=arr, L=2, d=256, f=768, g=64, fmt=1, eps=1e-5, v=v, r=r, y=y):
+        return fn(layers, L, d, f, g, fmt, eps, v, r, y, None)
+
+    assert call(layers=None) == NULL
+    assert call(v=None) == NULL
+    assert call(L=0) == SHAPE
+    assert call(d=260) == SHAPE
+    assert call(g=48) == GROUP
+    assert call(fmt=7) == FORMAT
+    assert call(y=y + 8) == ALIGN
+    assert call(y=v) == ALIAS                 # out_y inside values
+    assert call(y=r + 16) == ALIAS           # partial overlap with the residual

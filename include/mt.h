@@ -197,8 +197,8 @@ mt_status mt_unpack_affine(const void* q, const void* scales, const void* biases
  * mt_mlp_plan_create binds the layers' weights (device pointers, layouts as
  * for the single calls; one format and group size for all layers) and plans
  * the kernel for the CURRENT device.  It allocates the plan's device memory
- * (a layer table of 80 * L bytes and a workspace of about 4 * (d + f) bytes
- * plus 2 KB) with cudaMalloc, uploads the table synchronously and returns the
+ * (a layer table of 80 * L bytes and a workspace of about 2 * (d + f) bytes
+ * plus 1 KB) with cudaMalloc, uploads the table synchronously and returns the
  * plan in *plan.
  * The weights stay owned by the caller and must outlive the plan; they must
  * not be written while a run that reads them may execute.
@@ -207,8 +207,8 @@ mt_status mt_unpack_affine(const void* q, const void* scales, const void* biases
  *            and (affine) of group
  *   Limits : 1 <= L <= 4096; the kernel's shared-memory layout must fit one SM
  *            (MT_ERR_SHAPE otherwise; d = 4096, f = 12288 fits).
- * mt_mlp_plan_run enqueues one pass over the L layers on `stream` (a memset of
- * the plan's workspace and one cooperative kernel launch).  It allocates
+ * mt_mlp_plan_run enqueues one pass over the L layers on `stream` (a 128-byte
+ * memset of the plan's barrier line and one cooperative kernel launch).  It allocates
  * nothing and does not synchronise.
  *   values   : bf16 [L][d], values[l] is layer l's addend (device)
  *   residual : bf16 [d], r_0 (device)
@@ -222,9 +222,9 @@ mt_status mt_unpack_affine(const void* q, const void* scales, const void* biases
  *   events); different plans are independent.  The run's kernel keeps one
  *   CTA resident on every SM for its whole duration (cooperative launch);
  *   kernels running concurrently on other streams can delay its CTAs.
- *   A wait for another CTA's data that expires (bounded at about one
- *   second) makes every CTA return: mt_device_error() then reports
- *   MT_ERR_TIMEOUT and out_y is undefined.
+ *   A grid-wide wait that expires (bounded at about one second) makes every
+ *   CTA return: mt_device_error() then reports MT_ERR_TIMEOUT and out_y is
+ *   undefined.
  * mt_mlp_plan_destroy frees the plan's device memory (cudaFree, which
  * synchronises the device) and the plan.
  */
@@ -267,11 +267,11 @@ mt_status mt_mlp_plan_destroy(mt_mlp_plan* plan);
  *   values, residual, out_y, stream  : as for mt_mlp_plan_run (no trace)
  * Scratch.  The layer table and the hand-off words live in one static device
  * array of MT_STACK_SCRATCH_BYTES bytes per device:
- *   128*ceil(80 L / 128) + 128 + 2 * 128*ceil(8 S / 128)
- *     + 128*ceil(4 d / 128) + 128*ceil(4 f / 128)      bytes, S = SM count
- * (71,168 bytes for 36 layers of d = 4096, f = 12288 on 152 SMs).  Larger
+ *   128*ceil(80 L / 128) + 128 + 128*ceil(4 S / 128)
+ *     + 128*ceil(2 d / 128) + 128*ceil(2 f / 128)      bytes, S = SM count
+ * (36,480 bytes for 36 layers of d = 4096, f = 12288 on 152 SMs).  Larger
  * problems return MT_ERR_SHAPE.  Each call uploads the table
- * (cudaMemcpyAsync from host memory) and zeroes the rest (cudaMemsetAsync) on
+ * (cudaMemcpyAsync from host memory) and zeroes the barrier line (cudaMemsetAsync) on
  * `stream` before the kernel; it calls no allocating routine.
  * Set-up.  The first call on a device, made with that device current, looks
  * up the array's device address (cudaGetSymbolAddress) and sets the kernel's

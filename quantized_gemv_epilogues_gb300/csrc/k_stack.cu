@@ -21,24 +21,18 @@
 //   down    the CTA's rows of Wd with x = h; the epilogue adds the residual
 //           and publishes its rows of summed_{l+1} = values_{l+1} + y_l and
 //           their sum of squares.
-// Hand-offs between CTAs use no grid barrier.  Every published value travels
-// in a flag-in-data word: 64 bits holding 32 bits of payload (two bf16, or
-// one fp32) and the 32-bit number of the tensor's layer plus one, written
-// and read as single 64-bit accesses (single-copy atomic), so a reader that
-// sees the expected number also has the payload; it re-reads a word until the
-// number matches.  After publishing its rows a CTA writes one tagged "done"
-// word (for summed, the word of its partial sum of squares); in each CTA a
-// single warp polls the grid's done words, then every thread reads its data
-// words once (re-reading, with a short sleep, the rare word that is still in
-// flight).  A hand-off thus costs about two round trips to L2 instead of the
-// four or five of a barrier (release, arrival, polls) followed by the load,
-// which measured 3-5 us per hand-off on this two-die part; letting every
-// thread poll its own data words instead flooded L2 with re-reads.  Reuse is safe without barriers: a CTA overwrites a published buffer
-// only after consuming a tensor that every other CTA published after it had
-// read that buffer.  Rows are dealt out to CTAs in pairs so that every word
-// has one writer.  The words are zeroed before each run.  Every wait is
+// A hand-off between CTAs is a grid barrier split in two halves.  A CTA
+// stores its rows (plain stores), passes a CTA barrier, and thread 0 adds
+// the CTA's arrival to one counter with a release reduction (no reply is
+// awaited); the CTA then requests what its next phase needs that does not
+// depend on the hand-off, and thread 0 polls the counter with acquire loads
+// until every CTA has arrived; after a second CTA barrier every thread reads
+// the published rows from L2.  (Tagged per-word data polled by one warp per
+// CTA measured about 2 us slower per hand-off on this two-die part than the
+// single counter; letting every thread poll its own words flooded L2.)  The
+// counter and an abort flag are zeroed before each run.  Every wait is
 // bounded (~1 s): on expiry the thread records MT_ERR_TIMEOUT in the device
-// error word and raises an abort flag that every other wait also watches,
+// error word and raises the abort flag that every other wait also watches,
 // and every CTA returns.
 //
 // Between hand-offs a CTA asks L2 for the first rows of its next phase's
@@ -56,8 +50,8 @@ namespace mt {
 constexpr int STACK_MAX_GRID = 256;  // CTAs (one per SM)
 // Bytes of each weight stream a CTA asks L2 for before a phase: about what
 // HBM delivers to one SM during a hand-off and the staging that follows.
-constexpr int STACK_PRE_GATEUP = 96 * 1024;  // per gate and per up stream
-constexpr int STACK_PRE_DOWN = 160 * 1024;
+constexpr int STACK_PRE_GATEUP = 64 * 1024;  // per gate and per up stream (swept: 0-192 KB)
+constexpr int STACK_PRE_DOWN = 160 * 1024;   // (swept: 0-256 KB)
 
 // One layer's device pointers.
 struct StackLayerDev {
@@ -73,10 +67,11 @@ struct StackLayerDev {
   const uint16_t* bd;
 };
 
-// Run state (one 128-byte line, zeroed before every run with the words).
+// Run state (one 128-byte line, zeroed before every run).
 struct StackCtl {
-  int abort;  // set when a wait expired
-  int pad[31];
+  unsigned count;  // barrier arrivals so far (barrier k completes at (k + 1) * grid)
+  int abort;       // set when a wait expired
+  int pad[30];
 };
 
 struct StackArgs {
@@ -88,10 +83,9 @@ struct StackArgs {
   const uint16_t* residual;  // [d]
   uint16_t* out_y;           // [d]
   StackCtl* ctl;
-  uint64_t* hw;   // [f/2]  h_l words: h[2k], h[2k+1] | l + 1
-  uint64_t* sw;   // [d/2]  summed_l words: summed[2k], summed[2k+1] | l + 1
-  uint64_t* qw;   // [grid] partial sums of squares of summed_l: fp32 | l + 1
-  uint64_t* hd;   // [grid] "h_l rows published": 0 | l + 1
+  uint16_t* hbuf;  // [f]    h of the current layer
+  uint16_t* sbuf;  // [d]    summed of the next layer
+  float* ssq;      // [grid] per-CTA partial sums of squares of sbuf
   int* err;
   int pre_g, pre_d;   // bytes per weight stream asked of L2 ahead of a phase
   uint16_t* tr_sum;   // optional [L][d]
@@ -103,118 +97,28 @@ struct StackArgs {
   int off_wn, off_ssm;
 };
 
-// ---- flag-in-data words
+// ---- grid barrier halves
 
-// GPU-scope relaxed accesses (system scope would also order against the
-// host, which this data never meets).
-__device__ __forceinline__ void word_store(uint64_t* p, uint32_t payload, uint32_t tag) {
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(((uint64_t)tag << 32) | payload)
-               : "memory");
-}
-__device__ __forceinline__ void words_load2(const uint64_t* p, uint64_t& w0, uint64_t& w1) {
-  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(p) : "memory");
-}
-__device__ __forceinline__ uint64_t word_load(const uint64_t* p) {
-  uint64_t w;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
-  return w;
-}
-__device__ __forceinline__ bool tag_is(uint64_t w, uint32_t tag) { return (uint32_t)(w >> 32) == tag; }
+// Thread 0, right after a CTA barrier that follows the CTA's global stores.
+__device__ __forceinline__ void grid_arrive(StackCtl* ctl) { red_release_gpu_add(&ctl->count, 1u); }
 
-// Bounded re-reading.  A wait (begin(), then again() before each re-read)
-// gives up after about 2^31 SM cycles (~1 s) or when another thread has given
-// up; the first to give up records MT_ERR_TIMEOUT.  After giving up, every
-// later wait of the thread gives up at once.
-struct Waiter {
-  StackCtl* ctl;
-  int* err;
-  long long t0;
-  unsigned spins;
-  bool ok;
-  __device__ __forceinline__ void begin() { spins = 0; }
-  __device__ __forceinline__ bool again() {  // false: stop waiting
-    if (!ok) return false;
-    if (spins++ == 0) t0 = clock64();
+// Thread 0: polls until all CTAs have arrived at barrier k (bounded).  The
+// caller follows with a CTA barrier that also spreads the verdict.
+__device__ __forceinline__ bool grid_poll(StackCtl* ctl, unsigned k, int* err) {
+  const unsigned target = (k + 1) * gridDim.x;
+  if (ld_acquire_gpu(&ctl->count) >= target) return true;
+  const long long t0 = clock64();
+  for (unsigned spins = 1;; ++spins) {
+    if (ld_acquire_gpu(&ctl->count) >= target) return true;
     if ((spins & 63u) == 0) {
-      if (ld_relaxed_gpu(&ctl->abort)) { ok = false; return false; }
+      if (ld_relaxed_gpu(&ctl->abort)) return false;
       if (clock64() - t0 > (1ll << 31)) {
         atomicExch(&ctl->abort, 1);
         atomicExch(err, (int)MT_ERR_TIMEOUT);
-        ok = false;
         return false;
       }
     }
-    return true;
   }
-};
-
-// One warp: waits until the n (<= 256) words p[0 .. n-1] all carry `tag`,
-// re-reading every word still missing in each round; lane l receives the
-// payloads of words l + 32k in v[k] (0 beyond n).
-__device__ __forceinline__ void warp_wait_done(const uint64_t* p, int n, uint32_t tag, uint32_t (&v)[8],
-                                               Waiter& wt, int lane) {
-  uint64_t q[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int i = lane + 32 * k;
-    q[k] = i < n ? word_load(p + i) : ((uint64_t)tag << 32);
-  }
-  wt.begin();
-  for (;;) {
-    bool have = true;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) have = have && tag_is(q[k], tag);
-    if (__all_sync(0xffffffffu, have) || !wt.again()) break;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (!tag_is(q[k], tag)) q[k] = word_load(p + lane + 32 * k);
-  }
-#pragma unroll
-  for (int k = 0; k < 8; ++k) v[k] = (uint32_t)q[k];
-}
-
-// Reads NB x units of a published bf16 vector (unit i = words 4i .. 4i+3 =
-// elements 8i .. 8i+7): units base0 + k * WT_THREADS + lane for k < NB
-// (units >= nu are skipped).  Issues every read first, then re-reads (after a
-// short sleep) the units whose words do not yet all carry `tag`, until none
-// is left.  Used after the producers' done words were seen, so re-reads are
-// rare.
-template <int NB>
-__device__ __forceinline__ void read_units(const uint64_t* words, int base0, int nu, uint32_t tag,
-                                           uint4 (&out)[NB], Waiter& wt, int lane) {
-  uint64_t w[NB][4];
-#pragma unroll
-  for (int k = 0; k < NB; ++k) {
-    const int i = base0 + k * WT_THREADS + lane;
-    if (i < nu) {
-      words_load2(words + 4 * i, w[k][0], w[k][1]);
-      words_load2(words + 4 * i + 2, w[k][2], w[k][3]);
-    } else {
-      w[k][0] = w[k][1] = w[k][2] = w[k][3] = (uint64_t)tag << 32;
-    }
-  }
-  wt.begin();
-  for (;;) {
-    bool have = true;
-#pragma unroll
-    for (int k = 0; k < NB; ++k)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) have = have && tag_is(w[k][j], tag);
-    if (have || !wt.again()) break;
-    __nanosleep(64);
-#pragma unroll
-    for (int k = 0; k < NB; ++k) {
-      const int i = base0 + k * WT_THREADS + lane;
-      if (i < nu && !(tag_is(w[k][0], tag) && tag_is(w[k][1], tag) && tag_is(w[k][2], tag) &&
-                      tag_is(w[k][3], tag))) {
-        words_load2(words + 4 * i, w[k][0], w[k][1]);
-        words_load2(words + 4 * i + 2, w[k][2], w[k][3]);
-      }
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < NB; ++k)
-    out[k] = make_uint4((uint32_t)w[k][0], (uint32_t)w[k][1], (uint32_t)w[k][2], (uint32_t)w[k][3]);
 }
 
 __device__ __forceinline__ PhaseW gateup_w(const StackLayerDev& L) {
@@ -252,7 +156,6 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int task_ctr;
   __shared__ float red[WARP_TASK_WARPS];
-  __shared__ float s_inv;
   __shared__ __align__(16) StackLayerDev lay_s[2];  // layers l and l + 1
   static_assert(sizeof(StackLayerDev) % 16 == 0, "layer table entries are copied in 16-byte units");
   constexpr int LAY_UNITS = (int)(sizeof(StackLayerDev) / 16);
@@ -278,7 +181,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
   const uint64_t pol = l2_evict_first_policy();
   uint4 bufA[WT_NS][WT_CL], bufB[WT_NS][WT_CL];
   const int tA = warp, tB = warp + WARP_TASK_WARPS;
-  Waiter wt{a.ctl, a.err, 0, 0, true};
+  unsigned nbar = 0;  // grid barriers passed
 
   // Copies layer l's pointer table entry into lay_s[l & 1] (cp.async; the
   // caller commits and waits).
@@ -300,8 +203,8 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
   // go to shared memory at the start of the PREVIOUS phase's task loop
   // (stage_*_smem; the copies are small next to the weight stream), and its
   // first rows' weights go to L2 with bulk prefetches right after the CTA has
-  // published its part of the hand-off (prefetch_*).  lay_s[l & 1] must be
-  // complete and visible.  The caller commits the copies.
+  // arrived at the hand-off (prefetch_*).  lay_s[l & 1] must be complete and
+  // visible.  The caller commits the copies.
   auto stage_gateup_smem = [&](int l) {
     const StackLayerDev& Ly = lay_s[l & 1];
     if constexpr (AFF) stage_sb<0>(a.gu, gateup_w(Ly), cg, smG.sbr, tid, WT_THREADS);
@@ -320,25 +223,37 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
     const StackLayerDev& Ly = lay_s[l & 1];
     if (tid == 32) l2_ahead(a.dn, cd, Ly.Wd, a.pre_d);
   };
+  // Completes barrier nbar: thread 0 polls, then every thread learns the
+  // verdict.  (Thread 0 issues no other loads between its arrival and here:
+  // polls queued behind loads from HBM took microseconds longer.)
+  auto grid_wait = [&]() -> bool {
+    int ok = 1;
+    if (tid == 0) ok = grid_poll(a.ctl, nbar, a.err) ? 1 : 0;
+    ++nbar;
+    return __syncthreads_and(ok) != 0;
+  };
   // This CTA's rows of summed_l = values_l + r (bf16 sum of two bf16, one
-  // rounding): pair j (rows 2j, 2j+1 of the CTA's down rows) is computed by
-  // thread j, published, and its squares folded into the CTA's partial sum,
-  // which thread 0 publishes.  r2: the pair of r.
-  auto publish_summed = [&](int l, uint32_t v2, uint32_t r2, bool have) {
+  // rounding): pair j (rows 2j, 2j+1 of the CTA's down rows) is computed and
+  // stored by thread j, its squares folded into the CTA's partial sum, which
+  // thread 0 stores before arriving at the barrier.  r2: the pair of r.
+  auto publish_summed = [&](uint32_t v2, uint32_t r2, bool have) {
     float ss = 0.f;
     if (have) {
       const uint16_t s0 = f2bf(bf16lo(v2) + bf16lo(r2));
       const uint16_t s1 = f2bf(bf16hi(v2) + bf16hi(r2));
-      word_store(a.sw + (cd.r_begin >> 1) + tid, pack2(s0, s1), (uint32_t)l + 1);
+      *reinterpret_cast<uint32_t*>(a.sbuf + cd.r_begin + 2 * tid) = pack2(s0, s1);
       ss = fmaf(bf16f(s0), bf16f(s0), bf16f(s1) * bf16f(s1));
     }
-    ss = cta_sum(ss, red, tid);
-    if (tid == 0) word_store(a.qw + cta, __float_as_uint(ss), (uint32_t)l + 1);
+    ss = cta_sum(ss, red, tid);  // its CTA barrier orders the summed stores
+    if (tid == 0) {
+      a.ssq[cta] = ss;
+      grid_arrive(a.ctl);
+    }
   };
 
   const int npair_d = cd.rows >> 1, npair_g = cg.rows >> 1;
 
-  // ---- prologue: layer 0's table entry, its gate/up staging, summed_0
+  // ---- prologue: layer 0's table entry and staging, summed_0
   fetch_layer(0);
   cp_async_commit();
   cp_async_wait_all();
@@ -350,16 +265,18 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       v2 = *reinterpret_cast<const uint32_t*>(a.values + cd.r_begin + 2 * tid);
       r2 = *reinterpret_cast<const uint32_t*>(a.residual + cd.r_begin + 2 * tid);
     }
-    publish_summed(0, v2, r2, have);
+    publish_summed(v2, r2, have);
   }
   prefetch_gateup(0);
-  stage_gateup_smem(0);
+  if (warp > 0) stage_gateup_smem(0);
+  cp_async_commit();
+  if (!grid_wait()) { cp_async_wait_all(); return; }
+  if (warp == 0) stage_gateup_smem(0);  // warp 0's share, after its polls
   cp_async_commit();
 
   for (int l = 0; l < a.L; ++l) {
     const StackLayerDev& Ly = lay_s[l & 1];
-    const uint32_t tag = (uint32_t)l + 1;
-    fetch_layer(l + 1);  // waited for with the RMSNorm gain below
+    fetch_layer(l + 1);  // waited for below
     cp_async_commit();
     // values_{l+1} of this thread's pair of down rows, for the down epilogue
     uint32_t vnx = 0;
@@ -369,24 +286,26 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
     // ---- add + RMSNorm of the whole vector (every CTA)
     float xinv;
     {
-      const int nu = d / 8;  // x units of 8 elements = 4 summed words
-      static_assert(STACK_MAX_GRID <= 256, "warp_wait_done reads at most 256 words");
-      if (warp == 0) {  // the partial sums of squares, in one fixed order
-        uint32_t v[8];
-        warp_wait_done(a.qw, (int)gridDim.x, tag, v, wt, lane);
-        float tot = 0.f;
+      const int nu = d / 8;  // x units of 8 elements
+      // the per-CTA partial sums of squares (every warp reads all of them,
+      // in one fixed order) and this thread's first two units of summed_l
+      float q[STACK_MAX_GRID / 32];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) tot += __uint_as_float(v[k]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-        if (lane == 0) s_inv = rsqrtf(tot / (float)d + a.eps);
+      for (int k = 0; k < STACK_MAX_GRID / 32; ++k) {
+        const int i = lane + 32 * k;
+        q[k] = i < (int)gridDim.x ? ldg_cg_f32(a.ssq + i) : 0.f;
       }
+      uint4 u0 = make_uint4(0, 0, 0, 0), u1 = u0;
+      if (tid < nu) u0 = ldg_cg(a.sbuf + (size_t)tid * 8);
+      if (tid + WT_THREADS < nu) u1 = ldg_cg(a.sbuf + (size_t)(tid + WT_THREADS) * 8);
+      float tot = 0.f;
+#pragma unroll
+      for (int k = 0; k < STACK_MAX_GRID / 32; ++k) tot += q[k];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+      const float inv = rsqrtf(tot / (float)d + a.eps);
       cp_async_wait_all();
-      if (!__syncthreads_and(wt.ok)) return;  // gain, scales, next table entry, s_inv
-      const float inv = s_inv;
-      // this thread's first two units of summed_l
-      uint4 u[2];
-      read_units<2>(a.sw, warp * 32, nu, tag, u, wt, lane);
+      __syncthreads();  // the RMSNorm gain, the scales and the next table entry
       // x = bf16(summed * inv * w), unit by unit, into the first staging pass
       float mx = 0.f;
       auto norm_unit = [&](int base, const uint4 sv) {
@@ -407,15 +326,15 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
         }
         x_unit<FMT>(a.gu, smG, i, o, mx);
       };
-      if (warp * 32 < nu) norm_unit(warp * 32, u[0]);
-      if (warp * 32 + WT_THREADS < nu) norm_unit(warp * 32 + WT_THREADS, u[1]);
+      if (warp * 32 < nu) norm_unit(warp * 32, u0);
+      if (warp * 32 + WT_THREADS < nu) norm_unit(warp * 32 + WT_THREADS, u1);
       for (int base = warp * 32 + 2 * WT_THREADS; base < nu; base += WT_THREADS) {  // d > 8192
-        uint4 uw[1];
-        read_units<1>(a.sw, base, nu, tag, uw, wt, lane);
-        norm_unit(base, uw[0]);
+        const int i = base + lane;
+        norm_unit(base, i < nu ? ldg_cg(a.sbuf + (size_t)i * 8) : make_uint4(0, 0, 0, 0));
       }
-      // the first two gate/up tasks (mostly L2 hits after stage_gateup), in
-      // flight during the second staging pass
+      if (tid == 0) task_ctr = 2 * WARP_TASK_WARPS;  // tasks 0..2W-1 are taken statically
+      xinv = x_convert<FMT>(a.gu, smG, mx, red, tid);
+      // the first two gate/up tasks (mostly L2 hits after prefetch_gateup)
       {
         const PhaseW w = gateup_w(Ly);
         wt_load<0>(a.gu, w, cg, tA, bufA, pol, lane);
@@ -423,8 +342,6 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
         wt_prefetch<0>(a.gu, w, cg, tA + 2 * WARP_TASK_WARPS, lane);
         wt_prefetch<0>(a.gu, w, cg, tB + 2 * WARP_TASK_WARPS, lane);
       }
-      if (tid == 0) task_ctr = 2 * WARP_TASK_WARPS;  // tasks 0..2W-1 are taken statically
-      xinv = x_convert<FMT>(a.gu, smG, mx, red, tid);
       stage_down_smem(l);  // for the next phase, during this one's loop
       cp_async_commit();
       if (a.tr_sum || a.tr_norm)
@@ -434,7 +351,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
           if (a.tr_norm) a.tr_norm[(size_t)l * d + n] = smG.xraw[n];
         }
     }
-    // ---- gate/up with the SwiGLU epilogue; h is published pair by pair
+    // ---- gate/up with the SwiGLU epilogue; h rows published in pairs
     {
       wt_run<FMT, 0>(a.gu, gateup_w(Ly), cg, smG, bufA, bufB, tA, tB, &task_ctr, xinv, pol, lane);
       __syncthreads();
@@ -446,44 +363,43 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
           const float u = row_total<2>(a.gu, smG.parts, 2 * j + e, 1);
           hb[e] = f2bf(g / (1.0f + expf(-g)) * u);
         }
-        word_store(a.hw + (cg.r_begin >> 1) + j, pack2(hb[0], hb[1]), tag);
+        *reinterpret_cast<uint32_t*>(a.hbuf + cg.r_begin + 2 * j) = pack2(hb[0], hb[1]);
         if (a.tr_h) *reinterpret_cast<uint32_t*>(a.tr_h + (size_t)l * f + cg.r_begin + 2 * j) = pack2(hb[0], hb[1]);
       }
       __syncthreads();
-      if (tid == 0) word_store(a.hd + cta, 0u, tag);
+      if (tid == 0) grid_arrive(a.ctl);  // h is published
     }
     // ---- down
     {
       prefetch_down(l);
       if (tid == 0) task_ctr = 2 * WARP_TASK_WARPS;
-      if (warp == 0) {
-        uint32_t v[8];
-        warp_wait_done(a.hd, (int)gridDim.x, tag, v, wt, lane);
-      }
-      if (!__syncthreads_and(wt.ok)) { cp_async_wait_all(); return; }
-      // h (every unit of a batch read before anything else is requested) and
-      // the first staging pass over it
+      if (!grid_wait()) { cp_async_wait_all(); return; }
+      // h (every unit of a batch read before it is used) and the first
+      // staging pass over it
       const PhaseW w = down_w(Ly);
       const int nu = f / 8;
       constexpr int HB = 4;  // units per thread and batch: f <= 16384 in one batch
       float mx = 0.f;
       for (int base0 = warp * 32; base0 < nu; base0 += HB * WT_THREADS) {
         uint4 hv[HB];
-        read_units<HB>(a.hw, base0, nu, tag, hv, wt, lane);
+#pragma unroll
+        for (int k = 0; k < HB; ++k) {
+          const int i = base0 + k * WT_THREADS + lane;
+          hv[k] = i < nu ? ldg_cg(a.hbuf + (size_t)i * 8) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
         for (int k = 0; k < HB; ++k) {
           const int base = base0 + k * WT_THREADS;
           if (base < nu) x_unit<FMT>(a.dn, smD, base + lane < nu ? base + lane : -1, hv[k], mx);
         }
       }
-      // the first two tasks, in flight during the second staging pass
+      cp_async_wait_all();  // scales and biases (long complete)
+      const float xinv = x_convert<FMT>(a.dn, smD, mx, red, tid);
+      // the first two tasks (mostly L2 hits after prefetch_down)
       wt_load<1>(a.dn, w, cd, tA, bufA, pol, lane);
       wt_load<1>(a.dn, w, cd, tB, bufB, pol, lane);
       wt_prefetch<1>(a.dn, w, cd, tA + 2 * WARP_TASK_WARPS, lane);
       wt_prefetch<1>(a.dn, w, cd, tB + 2 * WARP_TASK_WARPS, lane);
-      cp_async_wait_all();  // scales and biases (long complete)
-      if (!__syncthreads_and(wt.ok)) return;
-      const float xinv = x_convert<FMT>(a.dn, smD, mx, red, tid);
       if (l + 1 < a.L) {  // the next gate/up phase's, during this loop
         stage_gateup_smem(l + 1);
         cp_async_commit();
@@ -506,8 +422,9 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
         if (last) *reinterpret_cast<uint32_t*>(a.out_y + cd.r_begin + 2 * tid) = y2;
       }
       if (last) break;
-      publish_summed(l + 1, vnx, y2, have);
+      publish_summed(vnx, y2, have);
       prefetch_gateup(l + 1);
+      if (!grid_wait()) { cp_async_wait_all(); return; }
     }
   }
 }
@@ -522,7 +439,7 @@ struct StackPlanImpl {
   size_t smem;
   StackArgs base;       // geometry, layer table, workspace and smem offsets
   void* alloc;          // device allocation owned by the plan
-  void* run_state;      // start of what is zeroed before each run (control line + words)
+  void* run_state;      // what is zeroed before each run (the control line)
   size_t run_state_bytes;
   const void* kernel;   // mlp_stack_kernel<FMT>
 };
@@ -617,14 +534,13 @@ extern "C" mt_status mt_mlp_plan_create(const mt_mlp_layer* layers, int L, int d
   if (ce != cudaSuccess) return cuda_fail(ce);
   if (occ < 1) return MT_ERR_SHAPE;
 
-  // device memory: [layer table | control line | qw | sw | hw | hd]; everything
-  // after the table is zeroed before each run
+  // device memory: [layer table | control line | ssq | sbuf | hbuf]; the
+  // control line is zeroed before each run
   const size_t tab = ((size_t)L * sizeof(StackLayerDev) + 127) / 128 * 128;
-  const size_t o_ctl = tab, o_qw = o_ctl + 128;
-  const size_t o_sw = o_qw + ((size_t)P.grid * 8 + 127) / 128 * 128;
-  const size_t o_hw = o_sw + ((size_t)d / 2 * 8 + 127) / 128 * 128;
-  const size_t o_hd = o_hw + ((size_t)f / 2 * 8 + 127) / 128 * 128;
-  const size_t total = o_hd + ((size_t)P.grid * 8 + 127) / 128 * 128;
+  const size_t o_ctl = tab, o_ssq = o_ctl + 128;
+  const size_t o_sbuf = o_ssq + ((size_t)P.grid * 4 + 127) / 128 * 128;
+  const size_t o_hbuf = o_sbuf + ((size_t)d * 2 + 127) / 128 * 128;
+  const size_t total = o_hbuf + ((size_t)f * 2 + 127) / 128 * 128;
   StackLayerDev* host_tab = new (std::nothrow) StackLayerDev[L];
   if (!host_tab) return MT_ERR_SHAPE;
   for (int l = 0; l < L; ++l) {
@@ -655,12 +571,11 @@ extern "C" mt_status mt_mlp_plan_create(const mt_mlp_layer* layers, int L, int d
   char* base = static_cast<char*>(mem);
   a.layers = reinterpret_cast<const StackLayerDev*>(base);
   a.ctl = reinterpret_cast<StackCtl*>(base + o_ctl);
-  a.qw = reinterpret_cast<uint64_t*>(base + o_qw);
-  a.sw = reinterpret_cast<uint64_t*>(base + o_sw);
-  a.hw = reinterpret_cast<uint64_t*>(base + o_hw);
-  a.hd = reinterpret_cast<uint64_t*>(base + o_hd);
+  a.ssq = reinterpret_cast<float*>(base + o_ssq);
+  a.sbuf = reinterpret_cast<uint16_t*>(base + o_sbuf);
+  a.hbuf = reinterpret_cast<uint16_t*>(base + o_hbuf);
   P.run_state = base + o_ctl;
-  P.run_state_bytes = total - o_ctl;
+  P.run_state_bytes = 128;
   a.L = L; a.d = d; a.f = f; a.eps = eps;
   a.pre_g = STACK_PRE_GATEUP;
   a.pre_d = STACK_PRE_DOWN;
@@ -840,13 +755,12 @@ extern "C" mt_status mt_mlp_stack_run_noalloc(const mt_mlp_layer* layers, int L,
   if (!ok) return MT_ERR_SHAPE;
   const size_t budget = (size_t)di->max_smem_optin - 1024;  // static smem and slack
   if (P.smem > budget) return MT_ERR_SHAPE;
-  // scratch layout: [layer table | control line | qw | sw | hw | hd]
+  // scratch layout: [layer table | control line | ssq | sbuf | hbuf]
   const size_t o_ctl = round128((size_t)L * sizeof(StackLayerDev));
-  const size_t o_qw = o_ctl + 128;
-  const size_t o_sw = o_qw + round128((size_t)P.grid * 8);
-  const size_t o_hw = o_sw + round128((size_t)d / 2 * 8);
-  const size_t o_hd = o_hw + round128((size_t)f / 2 * 8);
-  const size_t total = o_hd + round128((size_t)P.grid * 8);
+  const size_t o_ssq = o_ctl + 128;
+  const size_t o_sbuf = o_ssq + round128((size_t)P.grid * 4);
+  const size_t o_hbuf = o_sbuf + round128((size_t)d * 2);
+  const size_t total = o_hbuf + round128((size_t)f * 2);
   if (total > (size_t)MT_STACK_SCRATCH_BYTES) return MT_ERR_SHAPE;
 
   // ---- one-time set-up of this device, then the launch
@@ -885,17 +799,16 @@ extern "C" mt_status mt_mlp_stack_run_noalloc(const mt_mlp_layer* layers, int L,
                          (size_t)n * sizeof(StackLayerDev), cudaMemcpyHostToDevice, s);
     if (ce != cudaSuccess) return cuda_fail(ce);
   }
-  // the control line and the hand-off words must start at zero
-  ce = cudaMemsetAsync(base + o_ctl, 0, total - o_ctl, s);
+  // the control line (barrier counter, abort flag) must start at zero
+  ce = cudaMemsetAsync(base + o_ctl, 0, 128, s);
   if (ce != cudaSuccess) return cuda_fail(ce);
 
   StackArgs a = P.base;
   a.layers = reinterpret_cast<const StackLayerDev*>(base);
   a.ctl = reinterpret_cast<StackCtl*>(base + o_ctl);
-  a.qw = reinterpret_cast<uint64_t*>(base + o_qw);
-  a.sw = reinterpret_cast<uint64_t*>(base + o_sw);
-  a.hw = reinterpret_cast<uint64_t*>(base + o_hw);
-  a.hd = reinterpret_cast<uint64_t*>(base + o_hd);
+  a.ssq = reinterpret_cast<float*>(base + o_ssq);
+  a.sbuf = reinterpret_cast<uint16_t*>(base + o_sbuf);
+  a.hbuf = reinterpret_cast<uint16_t*>(base + o_hbuf);
   a.L = L; a.d = d; a.f = f; a.eps = eps;
   a.err = err;
   a.pre_g = STACK_PRE_GATEUP;

@@ -36,16 +36,15 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
   PhaseSmem sm;
   sm.xraw = reinterpret_cast<uint16_t*>(smem);
   sm.xs = reinterpret_cast<uint4*>(smem + (size_t)g.K * 2);
-  sm.gsum = reinterpret_cast<float*>(smem + (size_t)g.K * 2 + xs_bytes<FMT>(g.K));
-  sm.sbr = reinterpret_cast<uint16_t*>(sm.gsum + (AFF ? (g.G + 3) / 4 * 4 : 0));
-  sm.parts = reinterpret_cast<float*>(sm.sbr + (AFF ? (size_t)2 * NW * g.sb_stride : 0));
+  phase_tail_carve<FMT, KIND>(g, smem + (size_t)g.K * 2 + xs_bytes<FMT>(g.K), sm);
   __shared__ int task_ctr;
-  __shared__ float red_max[WARP_TASK_WARPS];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PhaseCta c = phase_cta<KIND>(g, blockIdx.x);
 
   if (tid == 0) task_ctr = 2 * WARP_TASK_WARPS;  // tasks 0..2W-1 are taken statically
+  if constexpr (AFF)
+    for (int p = tid; p < g.P; p += WT_THREADS) sm.pmax[p] = 0;
   __syncthreads();
   pdl_trigger();
 
@@ -62,17 +61,16 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
   }
 
   pdl_wait();  // x, the residual and the output buffer follow the preceding kernel
-  float mx = 0.f;
   for (int base = warp * 32; base < g.K / 8; base += WT_THREADS) {
     const int i = base + lane < g.K / 8 ? base + lane : -1;
     // plain (coherent) loads: x was written by the preceding kernel
     const uint4 v = i >= 0 ? *reinterpret_cast<const uint4*>(a.x + (size_t)i * 8) : make_uint4(0, 0, 0, 0);
-    x_unit<FMT>(g, sm, i, v, mx);
+    x_unit<FMT>(g, sm, i, v);
   }
   cp_async_wait_all();  // scales and biases
-  const float xinv = x_convert<FMT>(g, sm, mx, red_max, tid);
+  x_convert<FMT>(g, sm, tid);
 
-  wt_run<FMT, KIND>(g, a.w, c, sm, bufA, bufB, tA, tB, &task_ctr, xinv, pol, lane);
+  wt_run<FMT, KIND>(g, a.w, c, sm, bufA, bufB, tA, tB, &task_ctr, pol, lane);
   __syncthreads();
 
   // epilogue: one thread per row adds the pieces in a fixed order

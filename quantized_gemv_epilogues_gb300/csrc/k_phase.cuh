@@ -30,9 +30,10 @@
 //      sum_k (s q_k + b) x_k = sum_chunks s * (sum q_k x_k) + sum_groups b * X_g
 //    with X_g the sum of x over group g (fp32, from the bf16 values).  The
 //    chunk sums sum q_k x_k are EXACT integer arithmetic: x is held as a
-//    24-bit fixed-point integer X = round(x * 2^e) (2^e chosen per CTA from
-//    max|x| so that |X| < 2^22; every element within 2^14 of the maximum is
-//    exact, smaller ones are rounded to 2^-22 of the maximum) and split into
+//    24-bit fixed-point integer X = round(x * 2^e) (2^e chosen per piece of
+//    the row from that piece's max|x| so that |X| <= 2^22; every element
+//    within 2^14 of its piece's maximum is exact, smaller ones are rounded to
+//    2^-22 of that maximum) and split into
 //    three byte planes, X = 65536 X2 + 256 X1 + X0 (X2 signed).  The packed
 //    codes are used as they are stored: one dp4a (four u8 x s8/u8 products
 //    added to an int32) per weight word and plane, so a 16-byte chunk of INT8
@@ -71,6 +72,8 @@ struct PhaseGeom {
   unsigned long long p_mul;  // ceil(2^32 / P): t / P == (t * p_mul) >> 32 for t < 2^32 / P
   int B;                     // bytes per piece (multiple of 16)
   int CPP;                   // 16-byte chunks per piece (<= 32 * WT_CL)
+  int upp;                   // 8-element x units per piece (K / 8 / P)
+  unsigned long long upp_mul;  // ceil(2^32 / upp): i / upp == (i * upp_mul) >> 32 for i < K / 8
   int GPP;                   // groups per piece (affine)
   int sb_stride;             // elements per staged scale or bias array (multiple of 8)
   int sb_vec;                // 1: scales/biases are staged in 16-byte copies (G % 8 == 0)
@@ -91,9 +94,43 @@ struct PhaseSmem {
   uint16_t* xraw;  // [K] bf16 activations
   uint4* xs;       // staging layout of x (see below), xs_bytes<FMT>(K) bytes
   float* gsum;     // [G] X_g (affine)
+  int* pmax;       // [P] max |x| of each piece, as float bits (affine)
+  float* xinv;     // [P] 1 / 2^e_p, undoing the piece's x scale (affine)
   uint16_t* sbr;   // 2*NW arrays of sb_stride bf16: 2m = scales, 2m+1 = biases of matrix m
   float* parts;    // [rows][P][NW] partial sums of the pieces
 };
+
+// Bytes of a phase's shared arrays other than xraw and xs, in the order gsum,
+// pmax, xinv, sbr, parts (each a multiple of 16 bytes).
+template <int FMT, int KIND>
+__host__ __device__ inline size_t phase_tail_bytes(const PhaseGeom& g) {
+  constexpr bool AFF = FmtTraits<FMT>::AFFINE;
+  constexpr int NW = KIND == 0 ? 2 : 1;
+  size_t n = 0;
+  if (AFF) {
+    n += (size_t)(g.G + 3) / 4 * 16;
+    n += (size_t)(2 * g.P + 3) / 4 * 16;
+    n += (size_t)2 * NW * g.sb_stride * 2;
+  }
+  n += ((size_t)g.rows_alloc * g.P * NW * 4 + 15) / 16 * 16;
+  return n;
+}
+
+// Points sm's gsum, pmax, xinv, sbr and parts into the tail at p (16-byte
+// aligned, phase_tail_bytes long).
+template <int FMT, int KIND>
+__device__ __forceinline__ void phase_tail_carve(const PhaseGeom& g, unsigned char* p, PhaseSmem& sm) {
+  constexpr bool AFF = FmtTraits<FMT>::AFFINE;
+  constexpr int NW = KIND == 0 ? 2 : 1;
+  sm.gsum = reinterpret_cast<float*>(p);
+  if (AFF) p += (size_t)(g.G + 3) / 4 * 16;
+  sm.pmax = reinterpret_cast<int*>(p);
+  sm.xinv = reinterpret_cast<float*>(p) + g.P;
+  if (AFF) p += (size_t)(2 * g.P + 3) / 4 * 16;
+  sm.sbr = reinterpret_cast<uint16_t*>(p);
+  if (AFF) p += (size_t)2 * NW * g.sb_stride * 2;
+  sm.parts = reinterpret_cast<float*>(p);
+}
 
 // The rows a CTA owns in one phase and its task count.
 struct PhaseCta {
@@ -276,15 +313,20 @@ __device__ __forceinline__ void stage_sb(const PhaseGeom& g, const PhaseW& w, co
 
 // Staging of x, in two passes over 8-element units (one uint4 of bf16).
 //
-// Pass 1, x_unit: unit i of x (0 <= i < K/8) is stored in sm.xraw, its |x|
-// folded into the calling thread's running maximum and (affine) its sum added
-// into the group sum X_g (fp32).  Every lane of a warp calls it together for
-// units base + lane (base a multiple of 32; i = -1 for a lane without a
-// unit), so the group/8 units of a group sit in consecutive lanes and are
-// summed with a fixed shuffle tree.
+// The piece of x unit i.
+__device__ __forceinline__ int unit_piece(const PhaseGeom& g, int i) {
+  return (int)(((unsigned long long)(unsigned)i * g.upp_mul) >> 32);
+}
+
+// Pass 1, x_unit: unit i of x (0 <= i < K/8) is stored in sm.xraw and
+// (affine) its |x| folded into its piece's maximum sm.pmax (a shared-memory
+// max on the float bits, which order like the non-negative floats) and its
+// sum added into the group sum X_g (fp32).  sm.pmax must start at zero.
+// Every lane of a warp calls it together for units base + lane (base a
+// multiple of 32; i = -1 for a lane without a unit), so the group/8 units of a
+// group sit in consecutive lanes and are summed with a fixed shuffle tree.
 template <int FMT>
-__device__ __forceinline__ void x_unit(const PhaseGeom& g, const PhaseSmem& sm, int i, const uint4 v,
-                                       float& mx) {
+__device__ __forceinline__ void x_unit(const PhaseGeom& g, const PhaseSmem& sm, int i, const uint4 v) {
   if (i >= 0) reinterpret_cast<uint4*>(sm.xraw)[i] = v;
   if constexpr (FmtTraits<FMT>::AFFINE) {
     float sum = 0.f, m = 0.f;
@@ -297,7 +339,14 @@ __device__ __forceinline__ void x_unit(const PhaseGeom& g, const PhaseSmem& sm, 
         m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
       }
     }
-    mx = fmaxf(mx, m);
+    if (g.upp % 32 == 0) {  // the warp's 32 units lie in one piece
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      const int i0 = __shfl_sync(0xffffffffu, i, 0);
+      if ((threadIdx.x & 31) == 0 && i0 >= 0) atomicMax(sm.pmax + unit_piece(g, i0), __float_as_int(m));
+    } else if (i >= 0) {
+      atomicMax(sm.pmax + unit_piece(g, i), __float_as_int(m));
+    }
     const int upg = g.group >> 3;  // units per group: 4, 8 or 16
     for (int off = 1; off < upg; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
     if (i >= 0 && (i & (upg - 1)) == 0) sm.gsum[i / upg] = sum;
@@ -310,19 +359,20 @@ __device__ __forceinline__ uint32_t byte_plane(uint32_t a, uint32_t b, uint32_t 
   return __byte_perm(__byte_perm(a, b, sel), __byte_perm(c, d, sel), 0x5410);
 }
 
-// Pass 2, after every thread's pass-1 calls: the power-of-two scale 2^e with
-// max|x| * 2^e in [2^21, 2^22) (affine) and the staging layout of every unit.
-// mx: the thread's running maximum.  red_max: WARP_TASK_WARPS floats of
-// shared memory.  Begins and ends with a CTA barrier.  Returns 1 / 2^e (1 for
-// bf16).
+// 2^e for an integer e in [-126, 126] (exact).
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
+
+// Pass 2, after every thread's pass-1 calls: per piece p, the power-of-two
+// scale 2^e_p with max|x| * 2^e_p in [2^21, 2^22) (affine; the fixed-point X =
+// round(x * 2^e_p) then has |X| <= 2^22) and the staging layout of every unit;
+// sm.xinv[p] = 2^-e_p, and sm.pmax is reset to zero for the next use.  Begins
+// and ends with a CTA barrier (the reset follows the second).
 template <int FMT>
-__device__ __forceinline__ float x_convert(const PhaseGeom& g, const PhaseSmem& sm, float mx,
-                                           float* red_max, int tid) {
+__device__ __forceinline__ void x_convert(const PhaseGeom& g, const PhaseSmem& sm, int tid) {
   using T = FmtTraits<FMT>;
-  const int warp = tid >> 5, lane = tid & 31;
   const int CPR = g.CPR, NU = g.K / 8;
+  __syncthreads();
   if constexpr (!T::AFFINE) {
-    __syncthreads();
     // bf16: a unit is a chunk; its words 2u, 2u+1 go to 8-byte unit u*CPR + c
     for (int i = tid; i < NU; i += WT_THREADS) {
       const uint4 v = reinterpret_cast<const uint4*>(sm.xraw)[i];
@@ -330,20 +380,18 @@ __device__ __forceinline__ float x_convert(const PhaseGeom& g, const PhaseSmem& 
       reinterpret_cast<uint2*>(sm.xs)[CPR + i] = make_uint2(v.z, v.w);
     }
     __syncthreads();
-    return 1.f;
   } else {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0) red_max[warp] = mx;
+    // per piece: the exponent from the maximum's bits (a subnormal or zero
+    // maximum gives the largest exponent, 126), then pmax[p] holds the scale
+    for (int p = tid; p < g.P; p += WT_THREADS) {
+      const int mb = sm.pmax[p];
+      const int ex = (mb >> 23) >= 255 ? 0 : max(-126, min(126, 21 - ((mb >> 23) - 127)));
+      sm.xinv[p] = exp2i(-ex);
+      sm.pmax[p] = __float_as_int(exp2i(ex));
+    }
     __syncthreads();
-    mx = 0.f;
-#pragma unroll
-    for (int w = 0; w < WARP_TASK_WARPS; ++w) mx = fmaxf(mx, red_max[w]);
-    // X = round(x * 2^e), |X| <= 2^22
-    int ex = 0;
-    if (mx > 0.f && mx < 3.0e38f) ex = max(-126, min(126, 21 - ilogbf(mx)));
-    const float xscale = ldexpf(1.f, ex);
     for (int i = tid; i < NU; i += WT_THREADS) {
+      const float xscale = __int_as_float(sm.pmax[unit_piece(g, i)]);
       const uint4 v = reinterpret_cast<const uint4*>(sm.xraw)[i];
       const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
       uint32_t X[8];
@@ -372,7 +420,7 @@ __device__ __forceinline__ float x_convert(const PhaseGeom& g, const PhaseSmem& 
       }
     }
     __syncthreads();
-    return ldexpf(1.f, -ex);
+    for (int p = tid; p < g.P; p += WT_THREADS) sm.pmax[p] = 0;
   }
 }
 
@@ -381,7 +429,7 @@ __device__ __forceinline__ float x_convert(const PhaseGeom& g, const PhaseSmem& 
 template <int FMT, int KIND>
 __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c,
                                            const PhaseSmem& sm, int t,
-                                           const uint4 (&buf)[WT_NS][WT_CL], float xinv, int lane) {
+                                           const uint4 (&buf)[WT_NS][WT_CL], int lane) {
   using T = FmtTraits<FMT>;
   constexpr int EPC = T::EPC;
   constexpr bool AFF = T::AFFINE;
@@ -413,7 +461,7 @@ __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c
   }
   float vals[WT_NS];
 #pragma unroll
-  for (int v = 0; v < WT_NS; ++v) vals[v] = acc[v] * xinv;
+  for (int v = 0; v < WT_NS; ++v) vals[v] = AFF ? acc[v] * sm.xinv[p] : acc[v];
   if constexpr (AFF) {
     // bias terms of the groups in this piece: sum_g b_g * X_g
     for (int gl = lane; gl < g.GPP; gl += 32) {
@@ -449,7 +497,7 @@ template <int FMT, int KIND>
 __device__ __forceinline__ void wt_run(const PhaseGeom& g, const PhaseW& w, const PhaseCta& c,
                                        const PhaseSmem& sm, uint4 (&bufA)[WT_NS][WT_CL],
                                        uint4 (&bufB)[WT_NS][WT_CL], int tA, int tB, int* task_ctr,
-                                       float xinv, uint64_t pol, int lane) {
+                                       uint64_t pol, int lane) {
   auto next_task = [&]() -> int {
     int t = 0;
     if (lane == 0) t = atomicAdd(task_ctr, 1);
@@ -458,12 +506,12 @@ __device__ __forceinline__ void wt_run(const PhaseGeom& g, const PhaseW& w, cons
   constexpr int AHEAD = 2 * WARP_TASK_WARPS;  // L2 lookahead in tasks
   for (;;) {
     if (tA >= c.T) break;  // tA < tB here
-    wt_compute<FMT, KIND>(g, c, sm, tA, bufA, xinv, lane);
+    wt_compute<FMT, KIND>(g, c, sm, tA, bufA, lane);
     tA = next_task();
     wt_load<KIND>(g, w, c, tA, bufA, pol, lane);
     wt_prefetch<KIND>(g, w, c, tA + AHEAD, lane);
     if (tB >= c.T) break;  // tB < tA here
-    wt_compute<FMT, KIND>(g, c, sm, tB, bufB, xinv, lane);
+    wt_compute<FMT, KIND>(g, c, sm, tB, bufB, lane);
     tB = next_task();
     wt_load<KIND>(g, w, c, tB, bufB, pol, lane);
     wt_prefetch<KIND>(g, w, c, tB + AHEAD, lane);
@@ -486,7 +534,7 @@ __device__ __forceinline__ float row_total(const PhaseGeom& g, const float* part
 // groups.  The N rows are dealt out to the CTAs in contiguous ranges of whole
 // units of row_unit rows (N % row_unit == 0).  Returns false if no such cut
 // exists.  *smem_parts receives the bytes of the phase's shared arrays other
-// than x (gsum, sbr, parts).
+// than x (phase_tail_bytes).
 template <int FMT, int KIND>
 bool plan_phase(int K, int N, int group, int grid, PhaseGeom* out, size_t* smem_parts,
                 int row_unit = 1) {
@@ -512,6 +560,8 @@ bool plan_phase(int K, int N, int group, int grid, PhaseGeom* out, size_t* smem_
   g.p_mul = ((1ull << 32) + (unsigned long long)P - 1) / (unsigned long long)P;
   g.B = g.row_bytes / P;
   g.CPP = g.CPR / P;
+  g.upp = K / 8 / P;
+  g.upp_mul = ((1ull << 32) + (unsigned long long)g.upp - 1) / (unsigned long long)g.upp;
   g.GPP = AFF ? g.G / P : 0;
   g.row_unit = row_unit;
   g.rows_base = N / row_unit / grid;
@@ -520,8 +570,7 @@ bool plan_phase(int K, int N, int group, int grid, PhaseGeom* out, size_t* smem_
   g.sb_stride = AFF ? (g.rows_alloc * g.G + 7) / 8 * 8 : 0;
   g.sb_vec = (AFF && g.G % 8 == 0) ? 1 : 0;
   *out = g;
-  *smem_parts = (AFF ? (size_t)(g.G + 3) / 4 * 16 + (size_t)2 * NW * g.sb_stride * 2 : 0) +
-                ((size_t)g.rows_alloc * P * NW * 4 + 15) / 16 * 16;
+  *smem_parts = phase_tail_bytes<FMT, KIND>(g);
   return true;
 }
 

@@ -93,7 +93,7 @@ struct StackArgs {
   uint16_t* tr_h;     // optional [L][f]
   uint16_t* tr_y;     // optional [L][d]
   // shared-memory carve-up (byte offsets)
-  int off_xs, off_gsum_g, off_sbr_g, off_parts_g, off_gsum_d, off_sbr_d, off_parts_d;
+  int off_xs, off_tail_g, off_tail_d;
   int off_wn, off_ssm;
 };
 
@@ -167,12 +167,8 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
   PhaseSmem smG, smD;
   smG.xraw = smD.xraw = reinterpret_cast<uint16_t*>(smem);
   smG.xs = smD.xs = reinterpret_cast<uint4*>(smem + a.off_xs);
-  smG.gsum = reinterpret_cast<float*>(smem + a.off_gsum_g);
-  smG.sbr = reinterpret_cast<uint16_t*>(smem + a.off_sbr_g);
-  smG.parts = reinterpret_cast<float*>(smem + a.off_parts_g);
-  smD.gsum = reinterpret_cast<float*>(smem + a.off_gsum_d);
-  smD.sbr = reinterpret_cast<uint16_t*>(smem + a.off_sbr_d);
-  smD.parts = reinterpret_cast<float*>(smem + a.off_parts_d);
+  phase_tail_carve<FMT, 0>(a.gu, smem + a.off_tail_g, smG);
+  phase_tail_carve<FMT, 1>(a.dn, smem + a.off_tail_d, smD);
   uint16_t* wn = reinterpret_cast<uint16_t*>(smem + a.off_wn);    // [d] RMSNorm gain
   uint16_t* ssm = reinterpret_cast<uint16_t*>(smem + a.off_ssm);  // [d] summed_l
 
@@ -254,6 +250,10 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
   const int npair_d = cd.rows >> 1, npair_g = cg.rows >> 1;
 
   // ---- prologue: layer 0's table entry and staging, summed_0
+  if constexpr (AFF) {
+    for (int p = tid; p < a.gu.P; p += WT_THREADS) smG.pmax[p] = 0;
+    for (int p = tid; p < a.dn.P; p += WT_THREADS) smD.pmax[p] = 0;
+  }
   fetch_layer(0);
   cp_async_commit();
   cp_async_wait_all();
@@ -284,7 +284,6 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       vnx = *reinterpret_cast<const uint32_t*>(a.values + (size_t)(l + 1) * d + cd.r_begin + 2 * tid);
 
     // ---- add + RMSNorm of the whole vector (every CTA)
-    float xinv;
     {
       const int nu = d / 8;  // x units of 8 elements
       // the per-CTA partial sums of squares (every warp reads all of them,
@@ -307,7 +306,6 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       cp_async_wait_all();
       __syncthreads();  // the RMSNorm gain, the scales and the next table entry
       // x = bf16(summed * inv * w), unit by unit, into the first staging pass
-      float mx = 0.f;
       auto norm_unit = [&](int base, const uint4 sv) {
         const int i = base + lane < nu ? base + lane : -1;
         uint4 o = make_uint4(0, 0, 0, 0);
@@ -324,7 +322,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
           }
           reinterpret_cast<uint4*>(ssm)[i] = sv;
         }
-        x_unit<FMT>(a.gu, smG, i, o, mx);
+        x_unit<FMT>(a.gu, smG, i, o);
       };
       if (warp * 32 < nu) norm_unit(warp * 32, u0);
       if (warp * 32 + WT_THREADS < nu) norm_unit(warp * 32 + WT_THREADS, u1);
@@ -333,7 +331,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
         norm_unit(base, i < nu ? ldg_cg(a.sbuf + (size_t)i * 8) : make_uint4(0, 0, 0, 0));
       }
       if (tid == 0) task_ctr = 2 * WARP_TASK_WARPS;  // tasks 0..2W-1 are taken statically
-      xinv = x_convert<FMT>(a.gu, smG, mx, red, tid);
+      x_convert<FMT>(a.gu, smG, tid);
       // the first two gate/up tasks (mostly L2 hits after prefetch_gateup)
       {
         const PhaseW w = gateup_w(Ly);
@@ -353,7 +351,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
     }
     // ---- gate/up with the SwiGLU epilogue; h rows published in pairs
     {
-      wt_run<FMT, 0>(a.gu, gateup_w(Ly), cg, smG, bufA, bufB, tA, tB, &task_ctr, xinv, pol, lane);
+      wt_run<FMT, 0>(a.gu, gateup_w(Ly), cg, smG, bufA, bufB, tA, tB, &task_ctr, pol, lane);
       __syncthreads();
       for (int j = tid; j < npair_g; j += WT_THREADS) {
         uint16_t hb[2];
@@ -379,7 +377,6 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       const PhaseW w = down_w(Ly);
       const int nu = f / 8;
       constexpr int HB = 4;  // units per thread and batch: f <= 16384 in one batch
-      float mx = 0.f;
       for (int base0 = warp * 32; base0 < nu; base0 += HB * WT_THREADS) {
         uint4 hv[HB];
 #pragma unroll
@@ -390,11 +387,11 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
 #pragma unroll
         for (int k = 0; k < HB; ++k) {
           const int base = base0 + k * WT_THREADS;
-          if (base < nu) x_unit<FMT>(a.dn, smD, base + lane < nu ? base + lane : -1, hv[k], mx);
+          if (base < nu) x_unit<FMT>(a.dn, smD, base + lane < nu ? base + lane : -1, hv[k]);
         }
       }
       cp_async_wait_all();  // scales and biases (long complete)
-      const float xinv = x_convert<FMT>(a.dn, smD, mx, red, tid);
+      x_convert<FMT>(a.dn, smD, tid);
       // the first two tasks (mostly L2 hits after prefetch_down)
       wt_load<1>(a.dn, w, cd, tA, bufA, pol, lane);
       wt_load<1>(a.dn, w, cd, tB, bufB, pol, lane);
@@ -404,7 +401,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
         stage_gateup_smem(l + 1);
         cp_async_commit();
       }
-      wt_run<FMT, 1>(a.dn, w, cd, smD, bufA, bufB, tA, tB, &task_ctr, xinv, pol, lane);
+      wt_run<FMT, 1>(a.dn, w, cd, smD, bufA, bufB, tA, tB, &task_ctr, pol, lane);
       __syncthreads();
       // epilogue: y = h . Wd[n] + summed_l[n]; summed_{l+1} = values_{l+1} + y
       const bool last = l + 1 == a.L;
@@ -457,18 +454,8 @@ static bool plan_stack(StackPlanImpl* P, const DeviceInfo* di) {
   const int Kmax = P->d > P->f ? P->d : P->f;
   size_t off = (size_t)Kmax * 2;  // xraw
   a.off_xs = (int)off; off += xs_bytes<FMT>(Kmax);
-  // gate/up arrays: gsum, sbr, parts (plan_phase's sizes, 16-byte multiples)
-  const bool AFF = FmtTraits<FMT>::AFFINE;
-  const size_t gsum_g = AFF ? (size_t)(a.gu.G + 3) / 4 * 16 : 0;
-  const size_t sbr_g = AFF ? (size_t)4 * a.gu.sb_stride * 2 : 0;
-  a.off_gsum_g = (int)off; off += gsum_g;
-  a.off_sbr_g = (int)off; off += sbr_g;
-  a.off_parts_g = (int)off; off += pg - gsum_g - sbr_g;
-  const size_t gsum_d = AFF ? (size_t)(a.dn.G + 3) / 4 * 16 : 0;
-  const size_t sbr_d = AFF ? (size_t)2 * a.dn.sb_stride * 2 : 0;
-  a.off_gsum_d = (int)off; off += gsum_d;
-  a.off_sbr_d = (int)off; off += sbr_d;
-  a.off_parts_d = (int)off; off += pd - gsum_d - sbr_d;
+  a.off_tail_g = (int)off; off += pg;  // plan_phase's phase_tail_bytes (16-byte multiples)
+  a.off_tail_d = (int)off; off += pd;
   a.off_wn = (int)off; off += (size_t)P->d * 2;
   a.off_ssm = (int)off; off += (size_t)P->d * 2;
   P->smem = off;

@@ -404,6 +404,54 @@ def run_reference(args):
     return 0
 
 
+def run_sweep(args, torch, synth, mt, dev):
+    """Config 5: one d=2048, f=8192 affine INT8 layer (1 % x20 outliers) per
+    point, group in {32, 64, 128} x rows M in {1, 2, 4, 8}: us per layer
+    (add+RMSNorm, gate/up+SwiGLU, down+residual as single calls in one CUDA
+    graph) and effective GB/s per point.  The JSON line's value is the
+    geometric mean GB/s over the points."""
+    points = []
+    peak, peak_kind = measured_peaks()
+    for g in (32, 64, 128):
+        for M in (1, 2, 4, 8):
+            wl = synth.sweep_point(g, M)
+            st = Stack(wl, dev)
+            gr = capture(st.step_calls, torch, direct=args.no_graph)
+            for _ in range(max(3, args.warmup)):
+                gr.replay()
+            ms = time_graph(gr, args.steps, torch)
+            per = {}
+            for name, fn in (("gateup", st.gateup_only), ("down", st.down_only)):
+                gk = capture(fn, torch, direct=args.no_graph)
+                for _ in range(3):
+                    gk.replay()
+                per[name] = time_graph(gk, max(5, args.steps // 2), torch) * 1e3
+                del gk
+            points.append({"group": g, "M": M, "us_per_layer": round(ms * 1e3, 3),
+                           "gbs": round(wl.layer_bytes() / (ms * 1e-3) / 1e9, 1),
+                           "gateup_us": round(per["gateup"], 3),
+                           "gateup_gbs": round(st.gateup_bytes() / (per["gateup"] * 1e-6) / 1e9, 1),
+                           "down_us": round(per["down"], 3),
+                           "down_gbs": round(st.down_bytes() / (per["down"] * 1e-6) / 1e9, 1),
+                           "bytes_per_layer": wl.layer_bytes()})
+            del gr, st
+            torch.cuda.empty_cache()
+    import math
+    gm = math.exp(sum(math.log(p["gbs"]) for p in points) / len(points))
+    wl = synth.sweep_point(64, 1)
+    line = {"metric": METRIC, "value": round(gm, 2), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u8-weights/f32-acc",
+            "data": "synthetic",
+            "config": {"workload": "sweep d2048 f8192 affine8 (1 % x20 outliers), "
+                                   "group {32,64,128} x M {1,2,4,8}, one layer per point",
+                       "l2": "weights 50 MB per layer fit in L2: hot-L2 numbers"},
+            "peak": peak, "peak_kind": peak_kind, "points": points,
+            "device_error": mt.mt_device_error()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -411,7 +459,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mt", choices=["mt", "reference"])
     ap.add_argument("--workload", default="qwen3-8b",
-                    choices=["qwen3-8b", "tiny", "llama1b", "qwen15", "sweep"])
+                    choices=["qwen3-8b", "tiny", "llama1b", "qwen15", "sweep"],
+                    help="sweep: every group x M point of the d=2048, f=8192 sweep, one line")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
     ap.add_argument("--path", default="executor", choices=["executor", "calls"],
                     help="timed step: the warmed executor (one kernel per step, default) or "
@@ -442,8 +491,10 @@ def main():
         mt.mt_set_option(mt.MT_OPT_PDL, 0)
     mt.mt_set_option(mt.MT_OPT_GEMV, 0 if args.gemv == "warp" else 1)
 
+    if args.workload == "sweep":
+        return run_sweep(args, torch, synth, mt, dev)
     wl = {"qwen3-8b": synth.QWEN8B, "tiny": synth.TINY, "llama1b": synth.LLAMA1B,
-          "qwen15": synth.QWEN15, "sweep": synth.sweep_point(64, 1)}[args.workload]
+          "qwen15": synth.QWEN15}[args.workload]
     if args.layers:
         wl = wl.with_(layers=args.layers)
     stack = Stack(wl, dev)

@@ -88,6 +88,7 @@ struct StackArgs {
   float* ssq;      // [grid] per-CTA partial sums of squares of sbuf
   int* err;
   int pre_g, pre_d;   // bytes per weight stream asked of L2 ahead of a phase
+  unsigned bar_extra; // arrivals a barrier waits for beyond the grid (0; > 0 only in tests)
   uint16_t* tr_sum;   // optional [L][d]
   uint16_t* tr_norm;  // optional [L][d]
   uint16_t* tr_h;     // optional [L][f]
@@ -104,8 +105,8 @@ __device__ __forceinline__ void grid_arrive(StackCtl* ctl) { red_release_gpu_add
 
 // Thread 0: polls until all CTAs have arrived at barrier k (bounded).  The
 // caller follows with a CTA barrier that also spreads the verdict.
-__device__ __forceinline__ bool grid_poll(StackCtl* ctl, unsigned k, int* err) {
-  const unsigned target = (k + 1) * gridDim.x;
+__device__ __forceinline__ bool grid_poll(StackCtl* ctl, unsigned k, unsigned extra, int* err) {
+  const unsigned target = (k + 1) * gridDim.x + extra;
   if (ld_acquire_gpu(&ctl->count) >= target) return true;
   const long long t0 = clock64();
   for (unsigned spins = 1;; ++spins) {
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
   // polls queued behind loads from HBM took microseconds longer.)
   auto grid_wait = [&]() -> bool {
     int ok = 1;
-    if (tid == 0) ok = grid_poll(a.ctl, nbar, a.err) ? 1 : 0;
+    if (tid == 0) ok = grid_poll(a.ctl, nbar, a.bar_extra, a.err) ? 1 : 0;
     ++nbar;
     return __syncthreads_and(ok) != 0;
   };
@@ -586,6 +587,7 @@ extern "C" mt_status mt_mlp_plan_run(const mt_mlp_plan* plan, const void* values
   a.values = (const uint16_t*)values;
   a.residual = (const uint16_t*)residual;
   a.out_y = (uint16_t*)out_y;
+  a.bar_extra = (unsigned)test_barrier_extra();
   if (trace) {
     a.tr_sum = (uint16_t*)trace->out_sum;
     a.tr_norm = (uint16_t*)trace->out_norm;
@@ -803,6 +805,7 @@ extern "C" mt_status mt_mlp_stack_run_noalloc(const mt_mlp_layer* layers, int L,
   a.values = (const uint16_t*)values;
   a.residual = (const uint16_t*)residual;
   a.out_y = (uint16_t*)out_y;
+  a.bar_extra = (unsigned)test_barrier_extra();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(P.grid);
   cfg.blockDim = dim3(WT_THREADS);

@@ -13,6 +13,7 @@ namespace mt {
 static thread_local int g_last_cuda_error = 0;
 static std::atomic<int> g_opt_pdl{1};
 static std::atomic<int> g_opt_gemv{0};
+static std::atomic<int> g_opt_barrier_extra{0};
 
 // Device error word: kernels with bounded waits record MT_ERR_TIMEOUT here.
 __device__ int g_device_error;
@@ -32,6 +33,7 @@ int* device_error_ptr() {
 }
 
 int gemv_choice() { return g_opt_gemv.load(); }
+int test_barrier_extra() { return g_opt_barrier_extra.load(); }
 
 mt_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = (int)e;
@@ -251,12 +253,18 @@ mt_status mt_set_option(mt_option opt, int value) {
     g_opt_gemv.store(value);
     return MT_OK;
   }
+  if (opt == MT_OPT_TEST_BARRIER_EXTRA) {
+    if (value < 0 || value > 8) return MT_ERR_FORMAT;
+    g_opt_barrier_extra.store(value);
+    return MT_OK;
+  }
   return MT_ERR_FORMAT;
 }
 
 int mt_get_option(mt_option opt) {
   if (opt == MT_OPT_PDL) return g_opt_pdl.load();
   if (opt == MT_OPT_GEMV) return g_opt_gemv.load();
+  if (opt == MT_OPT_TEST_BARRIER_EXTRA) return g_opt_barrier_extra.load();
   return -1;
 }
 

@@ -30,6 +30,10 @@ int* device_error_ptr();
 // Which GEMV kernel family to use for one-row problems (MT_OPT_GEMV).
 int gemv_choice();
 
+// Phantom arrivals the executor's grid barriers wait for
+// (MT_OPT_TEST_BARRIER_EXTRA; 0 except in failure-detection tests).
+int test_barrier_extra();
+
 // Launches `kernel` with (grid, block, smem) on l.stream, adding the
 // programmatic-stream-serialization attribute when l.pdl is set.
 template <typename... KArgs, typename... Args>

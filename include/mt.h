@@ -90,8 +90,10 @@ typedef enum mt_wfmt { MT_W_BF16 = 0, MT_W_AFFINE8 = 1, MT_W_AFFINE4 = 2 } mt_wf
 /* Library options (mt_set_option / mt_get_option). */
 typedef enum mt_option {
   MT_OPT_PDL = 0, /* 1 (default): launch with programmatic stream serialization */
-  MT_OPT_GEMV = 1, /* one-row GEMV kernel: 0 (default) warp-task kernel,
-                      1 team kernel (the one always used for M > 1) */
+  MT_OPT_GEMV = 1, /* GEMV kernel family: 0 (default) warp-task kernel for
+                      M = 1 and tensor-core kernel for M > 1; 1 team kernel
+                      for every M; 2 tensor-core kernel for every M (shapes
+                      a kernel cannot hold fall back to the team kernel) */
   MT_OPT_TEST_BARRIER_EXTRA = 2 /* test hook for failure detection, 0 (default)
                       to 8: executor runs started while it is n > 0 make
                       every grid barrier wait for n arrivals that never come,

@@ -1,6 +1,7 @@
 // k_gemv_bf16.cu - instantiations of the GEMV kernels for one weight format
 // (compiled as a separate translation unit to build in parallel).
 #include "k_gemv_run.cuh"
+#include "k_gemv_mma.cuh"
 #include "k_gemv_warp.cuh"
 
 namespace mt {

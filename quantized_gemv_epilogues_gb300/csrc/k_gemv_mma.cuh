@@ -1,0 +1,659 @@
+// k_gemv_mma.cuh - multi-row GEMV (1 <= M <= 8 activation rows) with the
+// SwiGLU or residual epilogue, its dot products on the tensor cores.
+//
+// meTile docs, "Compute-Graph Fusion", Automatic Gated Epilogues (gate and up
+// share the activation; silu(gate) * up and the residual add are epilogues
+// before the only store); "MLX-LM Backend", Dispatch Policy (affine
+// w = scale * q + bias per group of 32/64/128 along K, fp32 accumulation).
+//
+// GB300 design:
+//  * Dot products are mma.sync m16n8k16 with fp32 accumulators: A = 16
+//    weight rows x 16 K, B = 16 K x 8 activation rows (B columns >= M repeat
+//    row M-1 and their results are dropped).  Each weight is read once for
+//    all M rows, and the per-weight work does not grow with M.
+//  * Affine codes enter A exactly as fp16 subnormals: the 16-bit pattern
+//    0x00qq is the fp16 value q * 2^-24 (exponent field zero, spacing
+//    2^-24), so one mask or byte permute per two codes places them, with no
+//    arithmetic.  A high INT4 nibble stays in place as 16 q * 2^-24, and the
+//    x it meets is staged divided by 16.  Products with x (fp16 up to 2^15)
+//    are exact in the fp32 accumulator; the 2^24 goes into the staged group
+//    scale.  Each group's fp32 accumulator is then scaled by the row's group
+//    scale and the bias enters as b * X_g, both in
+//    fp32; X_g, the group sum of x, comes from one more mma per k step with
+//    an all-ones A (the tensor pipe is otherwise idle most of the time).
+//    Dense bf16 weights are A as stored.
+//  * x enters B as fp16 scaled per quantisation group by a power of two 2^e
+//    (max|x| 2^e in [2^14, 2^15) over the group): a bf16 value is exact in
+//    fp16 unless it lies below 2^-28 of its group's maximum (those are
+//    flushed); the scale is divided out at each group's fp32 flush.  Every
+//    CTA stages and converts all of x: asynchronous 16-byte copies, then one
+//    pass of packed bf16 maxima and an integer re-biasing of the
+//    bf16 exponent (bf16x2_to_f16x2).  Dense bf16 weights take x as stored
+//    (bf16 mma).
+//  * K order: a dot product does not depend on which physical K index meets
+//    which mma k slot, as long as A and B agree.  A lane takes WPL
+//    consecutive 4-byte words of its row with one 16-, 8- or 4-byte load and
+//    uses them in register order; x is staged in shared memory in the same
+//    order, so a lane reads its B fragments with 16-byte loads and no
+//    shuffles.  The 16 K indices of one k step lie in one quantisation group
+//    (the load width is chosen from the group size).
+//  * Work split: one CTA of 16 warps per SM owns a contiguous range of output
+//    rows (within one row of every other CTA), cut into tiles of at most 16
+//    rows.  A unit is one tile x UK of K: 32 words (128 bytes) per lane.  The
+//    CTA's units are dealt to its warps in contiguous ranges; a warp
+//    accumulates along K in registers and writes one partial per tile it
+//    touched, and the epilogue adds a row's partials in warp order
+//    (deterministic).  Two units are in flight per warp (register double
+//    buffer) and the unit after them is asked of L2.
+#pragma once
+#include <algorithm>
+
+#include "k_gemv_run.cuh"
+
+namespace mt {
+
+constexpr int MMA_WARPS = 16;
+constexpr int MMA_THREADS = 32 * MMA_WARPS;
+constexpr int MMA_WORDS = 32;  // 4-byte weight words per lane per unit
+
+struct MmaArgs {
+  const uint16_t* x;
+  const uint8_t* W0;
+  const uint8_t* W1;
+  const uint16_t* s0;
+  const uint16_t* b0;
+  const uint16_t* s1;
+  const uint16_t* b1;
+  const uint16_t* res;
+  void* out;
+  int out_f32;
+  int M, K, N;
+  int group, lg_group, G;
+  int row_bytes;
+  int rows_base, rows_extra;  // CTA i owns rows_base + (i < rows_extra) rows
+  int KB;                     // units per tile along K: ceil(K / UK)
+  int NS;                     // partial slots per warp
+  int xstride;                // bytes per staged x row
+  int raw_vec;                // 1: raw scales/biases are copied in 16-byte pieces
+  // shared-memory byte offsets
+  int off_sbf, off_ginv, off_raw, off_parts, off_tstart;
+};
+
+// Compile-time shape of one (format, kind, load width) instantiation.
+template <int FMT, int KIND, int WPL>
+struct MmaCfg {
+  static constexpr int NW = KIND == 0 ? 2 : 1;                               // weight matrices
+  static constexpr int EPW = FMT == FMT_A8 ? 4 : (FMT == FMT_A4 ? 8 : 2);    // codes per word
+  static constexpr int CPL = WPL * EPW;  // codes per lane per chunk
+  static constexpr int CW = 4 * CPL;     // codes of a row per chunk (4 lanes)
+  static constexpr int LB = 2 * CPL;     // bytes of staged x per lane per chunk
+  static constexpr int CPU = MMA_WORDS / (NW * 2 * WPL);  // chunks per unit
+  static constexpr int UK = CPU * CW;                       // K per unit
+  static constexpr int KSC = FMT == FMT_A8 ? WPL : (FMT == FMT_A4 ? 2 * WPL : WPL / 2);  // k steps per chunk
+  static_assert(CPU >= 1 && KSC >= 1, "load width");
+};
+
+// Byte offset of code k within a weight row.
+template <int FMT>
+__host__ __device__ constexpr size_t code_bytes(int k) {
+  return FMT == FMT_A8 ? (size_t)k : (FMT == FMT_A4 ? (size_t)k / 2 : (size_t)k * 2);
+}
+
+// Streaming loads of WPL words (no L1 allocation, L2 policy).
+template <int WPL>
+__device__ __forceinline__ void ldw(uint32_t (&d)[WPL], const uint8_t* p, uint64_t pol) {
+  if constexpr (WPL == 4) {
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+                 : "l"(p), "l"(pol));
+  } else if constexpr (WPL == 2) {
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
+                 : "=r"(d[0]), "=r"(d[1])
+                 : "l"(p), "l"(pol));
+  } else {
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;"
+                 : "=r"(d[0])
+                 : "l"(p), "l"(pol));
+  }
+}
+
+// Packed bf16 maxima.  On non-negative finite values the bf16 order is the
+// order of the 16-bit patterns, so this is also a packed unsigned 16-bit
+// maximum of such patterns.
+__device__ __forceinline__ uint32_t hmax2_bf16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// fp16 bit patterns of x * 2^e for the two bf16 values of w, by integer
+// arithmetic on the bit fields: an fp16 exponent field is the bf16 one minus
+// 112 plus e, and the 7 bf16 fraction bits become the top 7 of the 10.  thr2
+// holds (112 - e) << 7 in both halves (0 <= 112 - e < 256): a packed
+// maximum clamps magnitudes below 2^-15 after scaling to that threshold, so
+// the subtraction never borrows across halves and they come out as zero (or,
+// in [2^-15, 2^-14), as some value below 2^-14).  Exact for every |x 2^e| in
+// [2^-14, 2^15); the caller's e keeps the group's maximum below 2^15.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, uint32_t thr2) {
+  const uint32_t t = hmax2_bf16(w & 0x7FFF7FFFu, thr2) - thr2;
+  return (t << 3) | (w & 0x80008000u);
+}
+
+// d += A * B for one m16n8k16 tile, fp32 accumulation; A/B fp16 or bf16.
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (BF16) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+// The two A registers of k step ks (within its chunk) from one row's words:
+// lo holds the codes of mma k slots (2t, 2t+1), hi those of (2t+8, 2t+9).
+//   A8:   word ks = codes c0..c3;   lo = (c0, c1), hi = (c2, c3)
+//   A4:   word ks/2 = codes c0..c7 (byte b: c_2b low nibble, c_2b+1 high);
+//         even ks: lo = (c0, c4), hi = (c1, c5); odd ks: lo = (c2, c6), hi = (c3, c7)
+//   BF16: words 2ks, 2ks+1 as stored (elements in order)
+// The staged x of a lane's chunk follows the same order (A8 and bf16: the
+// elements in order; A4: permuted within each 8), and when a lane's
+// block is 64 bytes (A4 with 16-byte loads) lanes t = 2, 3 keep its 16-byte
+// pieces swapped in pairs (piece q at q ^ 1), so the quarter-warps of a
+// 16-byte shared load hit distinct banks.
+template <int FMT, int WPL>
+__device__ __forceinline__ void a_regs(const uint32_t (&w)[WPL], int ks, uint32_t& lo, uint32_t& hi) {
+  if constexpr (FMT == FMT_A8) {
+    const uint32_t v = w[ks];
+    lo = __byte_perm(v, 0u, 0x4140);  // (c0, c1) * 2^-24
+    hi = __byte_perm(v, 0u, 0x4342);  // (c2, c3) * 2^-24
+  } else if constexpr (FMT == FMT_A4) {
+    const uint32_t v = (ks & 1) ? (w[ks >> 1] >> 8) : w[ks >> 1];
+    lo = v & 0x000F000Fu;  // (c0, c4) * 2^-24
+    hi = v & 0x00F000F0u;  // (c1, c5) * 2^-20: B holds x / 16 in these slots
+  } else {
+    lo = w[2 * ks];
+    hi = w[2 * ks + 1];
+  }
+}
+
+// Bytes added to a staged x row so that rows gid and gid + 1 start 16, 32 or
+// 64 bytes apart modulo 128 (conflict-free 16-byte B-fragment loads).
+template <int LB>
+__host__ __device__ constexpr int mma_row_pad() {
+  return LB == 16 ? 64 : (LB == 32 ? 16 : 32);
+}
+
+template <int FMT, int KIND, int WPL>
+__global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs a) {
+  using C = MmaCfg<FMT, KIND, WPL>;
+  constexpr int NW = C::NW, CPU = C::CPU, UK = C::UK, CW = C::CW, LB = C::LB, KSC = C::KSC;
+  constexpr bool AFF = FmtTraits<FMT>::AFFINE;
+  constexpr bool BF = FMT == FMT_BF16;
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* xs = smem;                                                   // [M][xstride]
+  float4* sbf = reinterpret_cast<float4*>(smem + a.off_sbf);                  // [NW][RT][G][8]
+  uint16_t* raw = reinterpret_cast<uint16_t*>(smem + a.off_raw);              // [NW][2][rows*G]
+  float* parts = reinterpret_cast<float*>(smem + a.off_parts);                // [W][NS][16][M][NW]
+  float* ginv = reinterpret_cast<float*>(smem + a.off_ginv);                  // [G][8] 2^-e_g
+  int* tstart = reinterpret_cast<int*>(smem + a.off_tstart);                  // [RT + 1]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gid = lane >> 2, t = lane & 3;
+  const int cta = blockIdx.x;
+  const int r_begin = cta * a.rows_base + min(cta, a.rows_extra);
+  const int rows = a.rows_base + (cta < a.rows_extra ? 1 : 0);
+  const int RT = (rows + 15) >> 4;
+  const int KB = a.KB, M = a.M, K = a.K, G = a.G;
+  const int U = RT * KB;
+  const int u0 = (int)((long)warp * U / MMA_WARPS), u1 = (int)((long)(warp + 1) * U / MMA_WARPS);
+
+  if (tid <= RT) tstart[tid] = tid * rows / RT;
+  __syncthreads();
+  pdl_trigger();
+
+  const uint64_t pol = l2_evict_first_policy();
+
+  // Unit cursors: tile j, K block kb, units left in the warp's range.
+  struct Cur {
+    int j, kb, left;
+  };
+  auto advance = [&](Cur& c) {
+    if (++c.kb == KB) { c.kb = 0; ++c.j; }
+    --c.left;
+  };
+
+  auto load_unit = [&](const Cur& c, uint32_t (&buf)[NW][2][CPU][WPL]) {
+    if (c.left <= 0) return;
+    const int j = c.j, k0 = c.kb * UK;
+    const int tr0 = tstart[j], tr1 = tstart[j + 1];
+#pragma unroll
+    for (int mat = 0; mat < NW; ++mat)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int rl = tr0 + gid + 8 * h;
+        const bool okr = rl < tr1;
+        const uint8_t* src = (mat ? a.W1 : a.W0) + (size_t)(r_begin + (okr ? rl : tr0)) * a.row_bytes +
+                             code_bytes<FMT>(k0) + t * WPL * 4;
+#pragma unroll
+        for (int ch = 0; ch < CPU; ++ch) {
+          if (okr && k0 + ch * CW < K) {
+            ldw<WPL>(buf[mat][h][ch], src + code_bytes<FMT>(ch * CW), pol);
+          } else {
+#pragma unroll
+            for (int i = 0; i < WPL; ++i) buf[mat][h][ch][i] = 0u;
+          }
+        }
+      }
+  };
+  // one 128-byte line per lane: the unit's 16 rows x UK codes of each matrix
+  auto prefetch_unit = [&](const Cur& c) {
+    if (c.left <= 0) return;
+    const int j = c.j, k0 = c.kb * UK;
+    const int tr0 = tstart[j], tr1 = tstart[j + 1];
+    constexpr int LPR = (int)(code_bytes<FMT>(UK) / 128);  // lines per row and matrix
+    const int mat = NW == 2 ? (lane >> 4) : 0;
+    const int idx = NW == 2 ? (lane & 15) : lane;
+    const int rl = tr0 + idx / LPR, line = idx % LPR;
+    if (rl < tr1 && (size_t)line * 128 < code_bytes<FMT>(K) - code_bytes<FMT>(k0))
+      prefetch_l2_normal((mat ? a.W1 : a.W0) + (size_t)(r_begin + rl) * a.row_bytes + code_bytes<FMT>(k0) + line * 128);
+  };
+
+  // cc: the unit computed next; cl: the next unit to load; cp: the next unit
+  // asked of L2 (two ahead of cl)
+  Cur cc = {u0 / KB, u0 % KB, u1 - u0};
+  Cur cl = cc, cp;
+  uint32_t bufA[NW][2][CPU][WPL], bufB[NW][2][CPU][WPL];
+  load_unit(cl, bufA);
+  advance(cl);
+  load_unit(cl, bufB);
+  advance(cl);
+  cp = cl;
+  prefetch_unit(cp);
+  advance(cp);
+  prefetch_unit(cp);
+  advance(cp);
+
+  // raw scales and biases of the CTA's rows (static data: before the wait)
+  if constexpr (AFF) {
+    const int n = rows * G;  // per array
+    const size_t off = (size_t)r_begin * G;
+#pragma unroll
+    for (int mat = 0; mat < NW; ++mat) {
+      const uint16_t* s = mat ? a.s1 : a.s0;
+      const uint16_t* b = mat ? a.b1 : a.b0;
+      uint16_t* rs = raw + (size_t)(2 * mat) * n;
+      uint16_t* rb = rs + n;
+      if (a.raw_vec) {
+        for (int i = tid; i < n / 8; i += MMA_THREADS) {
+          cp_async16(rs + i * 8, s + off + i * 8);
+          cp_async16(rb + i * 8, b + off + i * 8);
+        }
+      } else {
+        for (int i = tid; i < n; i += MMA_THREADS) {
+          rs[i] = ldg_u16(s + off + i);
+          rb[i] = ldg_u16(b + off + i);
+        }
+      }
+    }
+    cp_async_commit();
+  }
+
+  pdl_wait();  // x, the residual and the output follow the preceding kernel
+
+  // ---- x: raw bf16 rows into shared memory (16-byte asynchronous copies,
+  // all in flight together)
+  const int U8 = K / 8;  // 8-element units per row
+  {
+    int m = 0, u = tid;
+    while (m < M && u >= U8) { u -= U8; ++m; }
+    while (m < M) {
+      cp_async16(xs + (size_t)m * a.xstride + (size_t)u * 16, a.x + (size_t)m * K + (size_t)u * 8);
+      u += MMA_THREADS;
+      while (m < M && u >= U8) { u -= U8; ++m; }
+    }
+    cp_async_commit();
+  }
+  cp_async_wait_all();  // x (and the raw scales/biases)
+  __syncthreads();
+
+  if constexpr (AFF) {
+    // ---- x as fp16 in place, scaled per quantisation group by 2^e_g with
+    // max|x| 2^e_g in [2^14, 2^15) (a zero or tiny maximum gives 2^112);
+    // ginv[g][m] = 2^-e_g.  One lane block per lane, in the order of a_regs:
+    // in order (A8); (c0, c4), (c1, c5), (c2, c6), (c3, c7) per 8 codes (A4).  A group's blocks sit in BPG
+    // consecutive lanes; its maximum is the packed bf16 maximum of the
+    // magnitudes (sign bits cleared), combined over those lanes by shuffles.
+    constexpr int CPL = C::CPL;
+    const int nblk = K / CPL;
+    const int BPG = a.group / CPL;  // lane blocks per group: 4 or 8
+    // one lane block: raw bf16 in, fp16 out (in place)
+    auto convert = [&](int m, int bk, const uint4 (&raw)[LB / 16], int e) {
+      // A4: the odd codes of each byte pair sit 16x high in A (see a_regs), so
+      // their x is scaled by 2^(e-4)
+      const uint32_t thr = (uint32_t)(112 - e) << 7, thr_odd = (uint32_t)(116 - e) << 7;
+      const uint32_t t2 = thr | (thr << 16), t2_odd = thr_odd | (thr_odd << 16);
+      // lanes t = 2, 3 of a chunk (block bk & 3) keep their 16-byte pieces
+      // swapped when a lane block is 64 bytes
+      const int sw = (FMT == FMT_A4 && WPL == 4) ? ((bk >> 1) & 1) : 0;
+      uint4* blk = reinterpret_cast<uint4*>(xs + (size_t)m * a.xstride + (size_t)bk * LB);
+      uint32_t in[CPL / 2], ow[CPL / 2];
+#pragma unroll
+      for (int q = 0; q < LB / 16; ++q) {
+        in[4 * q] = raw[q].x; in[4 * q + 1] = raw[q].y; in[4 * q + 2] = raw[q].z; in[4 * q + 3] = raw[q].w;
+      }
+      if constexpr (FMT == FMT_A8) {
+#pragma unroll
+        for (int j = 0; j < CPL / 2; ++j) ow[j] = bf16x2_to_f16x2(in[j], t2);
+      } else {
+        // words (x0,x1) (x2,x3) (x4,x5) (x6,x7) -> (x0,x4) (x1,x5) (x2,x6) (x3,x7)
+#pragma unroll
+        for (int j = 0; j < CPL / 2; j += 4) {
+          ow[j] = bf16x2_to_f16x2(__byte_perm(in[j], in[j + 2], 0x5410), t2);
+          ow[j + 1] = bf16x2_to_f16x2(__byte_perm(in[j], in[j + 2], 0x7632), t2_odd);
+          ow[j + 2] = bf16x2_to_f16x2(__byte_perm(in[j + 1], in[j + 3], 0x5410), t2);
+          ow[j + 3] = bf16x2_to_f16x2(__byte_perm(in[j + 1], in[j + 3], 0x7632), t2_odd);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < LB / 16; ++q)
+        blk[q ^ sw] = make_uint4(ow[4 * q], ow[4 * q + 1], ow[4 * q + 2], ow[4 * q + 3]);
+    };
+    auto load_raw = [&](int m, int bk, uint4 (&raw)[LB / 16]) {
+      const uint4* blk = reinterpret_cast<const uint4*>(xs + (size_t)m * a.xstride + (size_t)bk * LB);
+#pragma unroll
+      for (int q = 0; q < LB / 16; ++q) raw[q] = blk[q];
+    };
+    // warp tasks of (row, 32 x 2 lane blocks): both blocks' loads first
+    constexpr int PB = 2;
+    const int csegs = (nblk + 32 * PB - 1) / (32 * PB);
+    for (int task = warp; task < M * csegs; task += MMA_WARPS) {  // warp-uniform
+      const int m = task / csegs, sg = task - m * csegs;
+      uint4 raw[PB][LB / 16];
+#pragma unroll
+      for (int j = 0; j < PB; ++j) {
+        const int bk = (sg * PB + j) * 32 + lane;
+        if (bk < nblk) {
+          load_raw(m, bk, raw[j]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < LB / 16; ++q) raw[j][q] = make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < PB; ++j) {
+        const int bk = (sg * PB + j) * 32 + lane;
+        uint32_t mx = 0;
+#pragma unroll
+        for (int q = 0; q < LB / 16; ++q)
+          mx = hmax2_bf16(mx, hmax2_bf16(hmax2_bf16(raw[j][q].x & 0x7FFF7FFFu, raw[j][q].y & 0x7FFF7FFFu),
+                                         hmax2_bf16(raw[j][q].z & 0x7FFF7FFFu, raw[j][q].w & 0x7FFF7FFFu)));
+        mx = max(mx & 0xFFFFu, mx >> 16);
+        for (int off = 1; off < BPG; off <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        // mx: bf16 bits of the group's max|x|; e <= 112 keeps the threshold
+        // of bf16x2_to_f16x2 non-negative (groups below 2^-98 lose precision)
+        const int e = max(-126, min(112, 14 - ((int)(mx >> 7) - 127)));
+        if (bk < nblk) {
+          convert(m, bk, raw[j], e);
+          if ((lane & (BPG - 1)) == 0) ginv[(bk / BPG) * 8 + m] = exp2i(-e);
+        }
+      }
+    }
+    const int n = rows * G, ne = RT * G * 8;
+    for (int i = tid; i < NW * ne; i += MMA_THREADS) {
+      const int mat = i / ne, rem = i - mat * ne;
+      const int jg = rem >> 3, gi = rem & 7;
+      const int j = jg / G, g = jg - j * G;
+      const int tr0 = tstart[j], tr1 = tstart[j + 1];
+      const uint16_t* rs = raw + (size_t)(2 * mat) * n;
+      const uint16_t* rb = rs + n;
+      const int ra = tr0 + gi, rbw = tr0 + gi + 8;
+      float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
+      constexpr float TWO24 = 16777216.f;  // the codes enter the mma as q * 2^-24
+      if (ra < tr1) { e.x = bf16f(rs[ra * G + g]) * TWO24; e.z = bf16f(rb[ra * G + g]); }
+      if (rbw < tr1) { e.y = bf16f(rs[rbw * G + g]) * TWO24; e.w = bf16f(rb[rbw * G + g]); }
+      sbf[(size_t)mat * ne + rem] = e;
+    }
+    __syncthreads();
+  }
+
+  // ---- mainloop
+  float acc[NW][4];
+#pragma unroll
+  for (int mat = 0; mat < NW; ++mat)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[mat][i] = 0.f;
+  const unsigned char* xrow = xs + (size_t)min(gid, M - 1) * a.xstride + t * LB;
+  const int ne = RT * G * 8;
+
+  const int jfirst = u0 / KB;
+  auto compute_unit = [&](const Cur& c, const uint32_t (&buf)[NW][2][CPU][WPL]) {
+    const int j = c.j, kb = c.kb, k0 = kb * UK;
+    float d[NW][4] = {}, d1[4] = {};  // d1: group sums of B (A = ones)
+#pragma unroll
+    for (int ch = 0; ch < CPU; ++ch) {
+      const int kc = k0 + ch * CW;
+      if (kc >= K) break;
+      if constexpr (AFF) {
+        if ((kc & (a.group - 1)) == 0) {
+#pragma unroll
+          for (int mat = 0; mat < NW; ++mat)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d[mat][i] = 0.f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d1[i] = 0.f;
+        }
+      }
+      // A4 with 16-byte loads: lanes t = 2, 3 hold their pieces swapped
+      constexpr bool SWP = FMT == FMT_A4 && WPL == 4;
+      uint32_t xr[LB / 4];
+#pragma unroll
+      for (int q = 0; q < LB / 16; ++q) {
+        const int pos = SWP ? (q ^ ((t >> 1) & 1)) : q;
+        const uint4 v = *reinterpret_cast<const uint4*>(xrow + (size_t)kc * 2 + pos * 16);
+        xr[4 * q] = v.x; xr[4 * q + 1] = v.y; xr[4 * q + 2] = v.z; xr[4 * q + 3] = v.w;
+      }
+#pragma unroll
+      for (int ks = 0; ks < KSC; ++ks) {
+        const uint32_t b0 = xr[2 * ks], b1 = xr[2 * ks + 1];
+        if constexpr (AFF) {  // sum of x over the group: A = 1 (16 where B holds x / 16)
+          constexpr uint32_t ONE = 0x3C003C00u, HI = FMT == FMT_A4 ? 0x4C004C00u : ONE;
+          mma16816<false>(d1, ONE, ONE, HI, HI, b0, b1);
+        }
+#pragma unroll
+        for (int mat = 0; mat < NW; ++mat) {
+          uint32_t lo0, hi0, lo1, hi1;
+          a_regs<FMT, WPL>(buf[mat][0][ch], ks, lo0, hi0);
+          a_regs<FMT, WPL>(buf[mat][1][ch], ks, lo1, hi1);
+          if constexpr (AFF)
+            mma16816<false>(d[mat], lo0, lo1, hi0, hi1, b0, b1);
+          else
+            mma16816<BF>(acc[mat], lo0, lo1, hi0, hi1, b0, b1);
+        }
+      }
+      if constexpr (AFF) {
+        if (((kc + CW) & (a.group - 1)) == 0) {  // the group ends with this chunk
+          const int g = kc >> a.lg_group;
+          // s * sum(q x) + b * X_g in the group's x scale, then undone
+          const float2 gi = *reinterpret_cast<const float2*>(ginv + g * 8 + 2 * t);
+#pragma unroll
+          for (int mat = 0; mat < NW; ++mat) {
+            const float4 sb = sbf[(size_t)mat * ne + (j * G + g) * 8 + gid];
+            acc[mat][0] = fmaf(fmaf(sb.x, d[mat][0], sb.z * d1[0]), gi.x, acc[mat][0]);
+            acc[mat][1] = fmaf(fmaf(sb.x, d[mat][1], sb.z * d1[1]), gi.y, acc[mat][1]);
+            acc[mat][2] = fmaf(fmaf(sb.y, d[mat][2], sb.w * d1[0]), gi.x, acc[mat][2]);
+            acc[mat][3] = fmaf(fmaf(sb.y, d[mat][3], sb.w * d1[1]), gi.y, acc[mat][3]);
+          }
+        }
+      }
+    }
+    if (c.left == 1 || kb + 1 == KB) {  // last unit of this warp in tile j
+      const int slot = j - jfirst;
+      float* pp = parts + (size_t)(warp * a.NS + slot) * 16 * M * NW;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int m = 2 * t + c;
+        if (m < M) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int mat = 0; mat < NW; ++mat)
+              pp[((gid + 8 * h) * M + m) * NW + mat] = acc[mat][2 * h + c];
+        }
+      }
+#pragma unroll
+      for (int mat = 0; mat < NW; ++mat)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[mat][i] = 0.f;
+    }
+  };
+
+  // register ping-pong: two units per iteration keep the buffer indices static
+  while (cc.left > 0) {
+    compute_unit(cc, bufA);
+    advance(cc);
+    load_unit(cl, bufA);
+    advance(cl);
+    prefetch_unit(cp);
+    advance(cp);
+    if (cc.left <= 0) break;
+    compute_unit(cc, bufB);
+    advance(cc);
+    load_unit(cl, bufB);
+    advance(cl);
+    prefetch_unit(cp);
+    advance(cp);
+  }
+  __syncthreads();
+
+  // ---- epilogue: one thread per (activation row, output row); a row's
+  // partials are added in warp order
+  for (int o = tid; o < rows * M; o += MMA_THREADS) {
+    const int m = o / rows, rl = o - m * rows;
+    int j = min(RT - 1, rl * RT / rows);
+    while (j > 0 && tstart[j] > rl) --j;
+    while (j + 1 < RT && tstart[j + 1] <= rl) ++j;
+    const int i = rl - tstart[j];
+    float v[NW];
+#pragma unroll
+    for (int mat = 0; mat < NW; ++mat) v[mat] = 0.f;
+    for (int w = 0; w < MMA_WARPS; ++w) {
+      const int w0 = (int)((long)w * U / MMA_WARPS), w1 = (int)((long)(w + 1) * U / MMA_WARPS);
+      if (w1 > w0 && w0 < (j + 1) * KB && w1 > j * KB) {
+        const float* pp = parts + ((size_t)(w * a.NS + (j - w0 / KB)) * 16 + i) * M * NW + m * NW;
+#pragma unroll
+        for (int mat = 0; mat < NW; ++mat) v[mat] += pp[mat];
+      }
+    }
+    const int n = r_begin + rl;
+    float outv;
+    if constexpr (KIND == 0) {
+      outv = v[0] / (1.0f + expf(-v[0])) * v[NW - 1];  // silu(gate) * up
+    } else {
+      outv = v[0] + bf16f(a.res[(size_t)m * a.N + n]);  // + residual
+    }
+    if (a.out_f32)
+      static_cast<float*>(a.out)[(size_t)m * a.N + n] = outv;
+    else
+      static_cast<uint16_t*>(a.out)[(size_t)m * a.N + n] = f2bf(outv);
+  }
+}
+
+// Host plan and launch of the tensor-core kernel for one (format, kind, load
+// width).  Returns MT_ERR_SHAPE when the problem does not fit its layout
+// (K not a multiple of a chunk, or the shared arrays over the budget); the
+// caller then uses the team kernel.
+template <int FMT, int KIND, int WPL>
+mt_status run_gemv_mma(const GemvProblem& p, const Launch& l) {
+  using C = MmaCfg<FMT, KIND, WPL>;
+  constexpr bool AFF = FmtTraits<FMT>::AFFINE;
+  constexpr int NW = C::NW;
+  static OccCache cache;  // only the attribute flags are used
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  int derr = 0;
+  const DeviceInfo* di = device_info(&derr);
+  if (!di) return cuda_fail((cudaError_t)derr);
+  if (p.M < 1 || p.M > 8 || p.K % C::CW) return MT_ERR_SHAPE;
+  if (AFF && (p.group % C::CW || p.K % p.group)) return MT_ERR_SHAPE;
+
+  MmaArgs a = {};
+  a.x = p.x;
+  a.W0 = static_cast<const uint8_t*>(p.W0);
+  a.W1 = static_cast<const uint8_t*>(p.W1);
+  a.s0 = p.s0; a.b0 = p.b0; a.s1 = p.s1; a.b1 = p.b1;
+  a.res = p.res;
+  a.out = p.out;
+  a.out_f32 = p.out_f32 ? 1 : 0;
+  a.M = p.M; a.K = p.K; a.N = p.N;
+  a.group = AFF ? p.group : 1;
+  a.lg_group = AFF ? (p.group == 32 ? 5 : (p.group == 64 ? 6 : 7)) : 0;
+  a.G = AFF ? p.K / p.group : 0;
+  a.row_bytes = (int)code_bytes<FMT>(p.K);
+
+  const int grid = di->sm_count < p.N ? di->sm_count : p.N;
+  a.rows_base = p.N / grid;
+  a.rows_extra = p.N % grid;
+  const int rows_max = a.rows_base + (a.rows_extra ? 1 : 0);
+  const int RT = (rows_max + 15) / 16;
+  if (RT > 64) return MT_ERR_SHAPE;  // the tile-start table holds 65 entries
+  a.KB = (p.K + C::UK - 1) / C::UK;
+  const long U = (long)RT * a.KB;
+  const long len = (U + MMA_WARPS - 1) / MMA_WARPS;  // longest warp range
+  a.NS = (int)std::min<long>(RT, (len - 1 + a.KB - 1) / a.KB + 1);
+  a.xstride = (p.K * 2 + 127) / 128 * 128 + mma_row_pad<C::LB>();
+  a.raw_vec = (AFF && a.G % 8 == 0) ? 1 : 0;
+
+  auto al16 = [](size_t v) { return (v + 15) / 16 * 16; };
+  size_t off = al16((size_t)p.M * a.xstride);
+  a.off_sbf = (int)off;
+  if (AFF) off += (size_t)NW * RT * a.G * 8 * 16;
+  a.off_ginv = (int)off;
+  if (AFF) off += (size_t)a.G * 8 * 4;
+  const size_t raw_bytes = AFF ? al16((size_t)NW * 2 * rows_max * a.G * 2) : 0;
+  const size_t parts_bytes = (size_t)MMA_WARPS * a.NS * 16 * p.M * NW * 4;
+  a.off_raw = (int)off;    // the raw scales/biases are dead once the
+  a.off_parts = (int)off;  // mainloop writes its first partial
+  off += std::max(raw_bytes, parts_bytes);
+  a.off_tstart = (int)al16(off);
+  const size_t smem = a.off_tstart + 80 * 4;  // tile starts
+  const size_t budget = (size_t)di->max_smem_optin - 1024;
+  if (smem > budget) return MT_ERR_SHAPE;
+
+  auto kern = gemv_mma_kernel<FMT, KIND, WPL>;
+  {
+    std::lock_guard<std::mutex> g(cache.mu);
+    if (dev < 64 && !cache.attr_set[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
+      if (e != cudaSuccess) return cuda_fail(e);
+      cache.attr_set[dev] = 1;
+    }
+  }
+  return launch(kern, dim3(grid), dim3(MMA_THREADS), smem, l, a);
+}
+
+// The load width for a format and group size: a k step's 16 K indices (4
+// lanes x WPL words) must lie in one group.
+template <int FMT, int KIND>
+mt_status dispatch_mma(const GemvProblem& p, const Launch& l) {
+  if constexpr (FMT == FMT_A8) {
+    if (p.group == 32) return run_gemv_mma<FMT, KIND, 2>(p, l);
+    return run_gemv_mma<FMT, KIND, 4>(p, l);
+  } else if constexpr (FMT == FMT_A4) {
+    if (p.group == 32) return run_gemv_mma<FMT, KIND, 1>(p, l);
+    if (p.group == 64) return run_gemv_mma<FMT, KIND, 2>(p, l);
+    return run_gemv_mma<FMT, KIND, 4>(p, l);
+  } else {
+    return run_gemv_mma<FMT, KIND, 4>(p, l);
+  }
+}
+
+}  // namespace mt

@@ -116,14 +116,23 @@ mt_status run_gemv(const GemvProblem& p, const Launch& l) {
 
 template <int FMT, int KIND>
 mt_status run_gemv_warp(const GemvProblem& p, const Launch& l);
+template <int FMT, int KIND>
+mt_status dispatch_mma(const GemvProblem& p, const Launch& l);
 
-// Chooses the kernel for one (format, kind): the warp-task kernel for one
-// row (unless MT_OPT_GEMV selects the team kernel or the shape does not fit
-// its shared memory), else the team kernel by row count.
+// Chooses the kernel for one (format, kind) by MT_OPT_GEMV: 0 (default) the
+// warp-task kernel for one row and the tensor-core kernel for M > 1; 1 the
+// team kernel for every M; 2 the tensor-core kernel for every M.  A shape
+// that does not fit the chosen kernel's shared memory falls back to the team
+// kernel by row count.
 template <int FMT, int KIND>
 mt_status dispatch_rows(const GemvProblem& p, const Launch& l) {
-  if (p.M == 1 && gemv_choice() == 0) {
+  const int choice = gemv_choice();
+  if (p.M == 1 && choice == 0) {
     const mt_status st = run_gemv_warp<FMT, KIND>(p, l);
+    if (st != MT_ERR_SHAPE) return st;
+  }
+  if ((p.M > 1 && choice == 0) || choice == 2) {
+    const mt_status st = dispatch_mma<FMT, KIND>(p, l);
     if (st != MT_ERR_SHAPE) return st;
   }
   if (p.M <= 1) return run_gemv<FMT, KIND, 1, 4>(p, l);

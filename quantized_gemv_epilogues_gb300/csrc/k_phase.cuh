@@ -359,9 +359,6 @@ __device__ __forceinline__ uint32_t byte_plane(uint32_t a, uint32_t b, uint32_t 
   return __byte_perm(__byte_perm(a, b, sel), __byte_perm(c, d, sel), 0x5410);
 }
 
-// 2^e for an integer e in [-126, 126] (exact).
-__device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
-
 // Pass 2, after every thread's pass-1 calls: per piece p, the power-of-two
 // scale 2^e_p with max|x| * 2^e_p in [2^21, 2^22) (affine; the fixed-point X =
 // round(x * 2^e_p) then has |X| <= 2^22) and the staging layout of every unit;

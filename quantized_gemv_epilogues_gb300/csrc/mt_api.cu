@@ -249,7 +249,7 @@ mt_status mt_set_option(mt_option opt, int value) {
     return MT_OK;
   }
   if (opt == MT_OPT_GEMV) {
-    if (value < 0 || value > 1) return MT_ERR_FORMAT;
+    if (value < 0 || value > 2) return MT_ERR_FORMAT;
     g_opt_gemv.store(value);
     return MT_OK;
   }

@@ -195,6 +195,9 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
+// 2^e for an integer e in [-126, 126] (exact).
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
+
 // fp32 -> bf16 round-to-nearest-even (the CUDA intrinsic).
 __device__ __forceinline__ uint16_t f2bf(float f) {
   uint16_t r;

@@ -165,6 +165,9 @@ def test_status_strings_and_options(lib):
     assert lib.mt_set_option(0, 0) == 0 and lib.mt_get_option(0) == 0
     assert lib.mt_set_option(0, 1) == 0 and lib.mt_get_option(0) == 1
     assert lib.mt_set_option(5, 1) == FORMAT
+    assert lib.mt_set_option(1, 2) == 0 and lib.mt_get_option(1) == 2
+    assert lib.mt_set_option(1, 3) == FORMAT and lib.mt_get_option(1) == 2
+    assert lib.mt_set_option(1, 0) == 0
     assert lib.mt_set_option(2, 9) == FORMAT and lib.mt_set_option(2, -1) == FORMAT
     assert lib.mt_set_option(2, 0) == 0 and lib.mt_get_option(2) == 0
     assert lib.mt_version() >> 16 == 1

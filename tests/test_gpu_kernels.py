@@ -27,11 +27,12 @@ def mt():
     return m
 
 
-@pytest.fixture(params=["warp", "team"])
+@pytest.fixture(params=["default", "team", "mma"])
 def gemv(request, mt):
-    """Runs a test with each one-row GEMV kernel (warp-task / team kernel);
-    M > 1 always uses the team kernel."""
-    mt.mt_set_option(mt.MT_OPT_GEMV, 0 if request.param == "warp" else 1)
+    """Runs a test with each GEMV kernel family: the default choice (warp-task
+    kernel for M = 1, tensor-core kernel for M > 1), the team kernel for every
+    M, and the tensor-core kernel for every M."""
+    mt.mt_set_option(mt.MT_OPT_GEMV, {"default": 0, "team": 1, "mma": 2}[request.param])
     yield request.param
     mt.mt_set_option(mt.MT_OPT_GEMV, 0)
     assert mt.mt_device_error(clear=True) == 0, "a bounded device wait expired"
@@ -138,6 +139,11 @@ SHAPES = [  # (fmt, group, M, d, f)
     (2, 64, 1, 8192, 153),     # one more row than SMs
     (0, 0, 1, 8960, 40),       # 17.5 KB bf16 rows
     (1, 64, 1, 64, 7),         # rows shorter than a warp's stride
+    (1, 32, 8, 2048, 1000),    # multi-row: several 16-row tiles per CTA
+    (1, 64, 7, 768, 500),
+    (2, 128, 5, 1024, 300),
+    (2, 32, 2, 256, 170),
+    (0, 0, 6, 1536, 350),
 ]
 
 

@@ -446,8 +446,8 @@ def run_sweep(args, torch, synth, mt, dev):
         del gk
         return us
 
-    for g in (32, 64, 128):
-        for M in (1, 2, 4, 8):
+    for g in ((args.sweep_group,) if args.sweep_group else (32, 64, 128)):
+        for M in ((args.sweep_rows,) if args.sweep_rows else (1, 2, 4, 8)):
             wl = synth.sweep_point(g, M)
             n_cold = int(math.ceil(2 * l2 / wl.layer_bytes())) + 1
             st = Stack(wl, dev, layers=n_cold)
@@ -514,6 +514,10 @@ def main():
                     choices=["qwen3-8b", "tiny", "llama1b", "qwen15", "sweep"],
                     help="sweep: every group x M point of the d=2048, f=8192 sweep, one line")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
+    ap.add_argument("--sweep-group", type=int, default=None, choices=[32, 64, 128],
+                    help="sweep: only this group size")
+    ap.add_argument("--sweep-rows", type=int, default=None, choices=[1, 2, 4, 8],
+                    help="sweep: only this row count M")
     ap.add_argument("--path", default="executor", choices=["executor", "calls"],
                     help="timed step: the warmed executor (one kernel per step, default) or "
                          "three single-call kernels per layer")

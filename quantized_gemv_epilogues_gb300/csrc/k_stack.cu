@@ -332,8 +332,9 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
         norm_unit(base, i < nu ? ldg_cg(a.sbuf + (size_t)i * 8) : make_uint4(0, 0, 0, 0));
       }
       if (tid == 0) task_ctr = 2 * WARP_TASK_WARPS;  // tasks 0..2W-1 are taken statically
-      x_convert<FMT>(a.gu, smG, tid);
-      // the first two gate/up tasks (mostly L2 hits after prefetch_gateup)
+      // the first two gate/up tasks (mostly L2 hits after prefetch_gateup),
+      // in flight while x is converted (shared memory only; requested before
+      // the hand-off instead, they slowed the barrier itself)
       {
         const PhaseW w = gateup_w(Ly);
         wt_load<0>(a.gu, w, cg, tA, bufA, pol, lane);
@@ -341,6 +342,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
         wt_prefetch<0>(a.gu, w, cg, tA + 2 * WARP_TASK_WARPS, lane);
         wt_prefetch<0>(a.gu, w, cg, tB + 2 * WARP_TASK_WARPS, lane);
       }
+      x_convert<FMT>(a.gu, smG, tid);
       stage_down_smem(l);  // for the next phase, during this one's loop
       cp_async_commit();
       if (a.tr_sum || a.tr_norm)
@@ -392,12 +394,13 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
         }
       }
       cp_async_wait_all();  // scales and biases (long complete)
-      x_convert<FMT>(a.dn, smD, tid);
-      // the first two tasks (mostly L2 hits after prefetch_down)
+      // the first two tasks (mostly L2 hits after prefetch_down), in flight
+      // while h is converted (shared memory only)
       wt_load<1>(a.dn, w, cd, tA, bufA, pol, lane);
       wt_load<1>(a.dn, w, cd, tB, bufB, pol, lane);
       wt_prefetch<1>(a.dn, w, cd, tA + 2 * WARP_TASK_WARPS, lane);
       wt_prefetch<1>(a.dn, w, cd, tB + 2 * WARP_TASK_WARPS, lane);
+      x_convert<FMT>(a.dn, smD, tid);
       if (l + 1 < a.L) {  // the next gate/up phase's, during this loop
         stage_gateup_smem(l + 1);
         cp_async_commit();

@@ -327,99 +327,94 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
   if constexpr (AFF) {
     // ---- x as fp16 in place, scaled per quantisation group by 2^e_g with
     // max|x| 2^e_g in [2^14, 2^15) (a zero or tiny maximum gives 2^112);
-    // ginv[g][m] = 2^-e_g.  One lane block per lane, in the order of a_regs:
-    // in order (A8); (c0, c4), (c1, c5), (c2, c6), (c3, c7) per 8 codes (A4).  A group's blocks sit in BPG
-    // consecutive lanes; its maximum is the packed bf16 maximum of the
-    // magnitudes (sign bits cleared), combined over those lanes by shuffles.
-    constexpr int CPL = C::CPL;
-    const int nblk = K / CPL;
-    const int BPG = a.group / CPL;  // lane blocks per group: 4 or 8
-    // one lane block: raw bf16 in, fp16 out (in place)
-    auto convert = [&](int m, int bk, const uint4 (&raw)[LB / 16], int e) {
-      // A4: the odd codes of each byte pair sit 16x high in A (see a_regs), so
-      // their x is scaled by 2^(e-4)
-      const uint32_t thr = (uint32_t)(112 - e) << 7, thr_odd = (uint32_t)(116 - e) << 7;
-      const uint32_t t2 = thr | (thr << 16), t2_odd = thr_odd | (thr_odd << 16);
-      // lanes t = 2, 3 of a chunk (block bk & 3) keep their 16-byte pieces
-      // swapped when a lane block is 64 bytes
-      const int sw = (FMT == FMT_A4 && WPL == 4) ? ((bk >> 1) & 1) : 0;
-      uint4* blk = reinterpret_cast<uint4*>(xs + (size_t)m * a.xstride + (size_t)bk * LB);
-      uint32_t in[CPL / 2], ow[CPL / 2];
+    // ginv[g][m] = 2^-e_g.  One 16-byte unit (8 elements) per lane and step,
+    // consecutive lanes on consecutive units (conflict-free shared accesses):
+    // a group's upg = group / 8 units sit in consecutive lanes and its
+    // maximum (packed bf16 maxima of the magnitudes) is combined by shuffles.
+    // Element order within a unit as a_regs reads it: in order (A8); (c0, c4),
+    // (c1, c5), (c2, c6), (c3, c7) (A4), and with 64-byte lane blocks (A4,
+    // 16-byte loads) the units of lanes t = 2, 3 of each chunk swapped in
+    // pairs; the swap partner is the neighbouring lane, whose load precedes
+    // both stores.
+    const int upg = a.group >> 3, lg_upg = a.lg_group - 3;
+    // units per lane and task: the most (up to 4) that still give every warp
+    // a task
+    constexpr int PU = 4;
+    int pu = PU;
+    while (pu > 1 && M * ((U8 + 32 * pu - 1) / (32 * pu)) < MMA_WARPS) pu >>= 1;
+    const int usegs = (U8 + 32 * pu - 1) / (32 * pu);
+    for (int task = warp; task < M * usegs; task += MMA_WARPS) {  // warp-uniform
+      const int m = task / usegs, sg = task - m * usegs;
+      unsigned char* row = xs + (size_t)m * a.xstride;
+      uint4 v[PU];
 #pragma unroll
-      for (int q = 0; q < LB / 16; ++q) {
-        in[4 * q] = raw[q].x; in[4 * q + 1] = raw[q].y; in[4 * q + 2] = raw[q].z; in[4 * q + 3] = raw[q].w;
+      for (int j = 0; j < PU; ++j) {
+        const int u = (sg * pu + j) * 32 + lane;
+        v[j] = (j < pu && u < U8) ? *reinterpret_cast<const uint4*>(row + (size_t)u * 16)
+                                  : make_uint4(0, 0, 0, 0);
       }
-      if constexpr (FMT == FMT_A8) {
+      // the PU units' maxima advance in lockstep (independent shuffle chains)
+      uint32_t mx[PU];
 #pragma unroll
-        for (int j = 0; j < CPL / 2; ++j) ow[j] = bf16x2_to_f16x2(in[j], t2);
-      } else {
-        // words (x0,x1) (x2,x3) (x4,x5) (x6,x7) -> (x0,x4) (x1,x5) (x2,x6) (x3,x7)
-#pragma unroll
-        for (int j = 0; j < CPL / 2; j += 4) {
-          ow[j] = bf16x2_to_f16x2(__byte_perm(in[j], in[j + 2], 0x5410), t2);
-          ow[j + 1] = bf16x2_to_f16x2(__byte_perm(in[j], in[j + 2], 0x7632), t2_odd);
-          ow[j + 2] = bf16x2_to_f16x2(__byte_perm(in[j + 1], in[j + 3], 0x5410), t2);
-          ow[j + 3] = bf16x2_to_f16x2(__byte_perm(in[j + 1], in[j + 3], 0x7632), t2_odd);
-        }
+      for (int j = 0; j < PU; ++j) {
+        mx[j] = hmax2_bf16(hmax2_bf16(v[j].x & 0x7FFF7FFFu, v[j].y & 0x7FFF7FFFu),
+                           hmax2_bf16(v[j].z & 0x7FFF7FFFu, v[j].w & 0x7FFF7FFFu));
+        mx[j] = max(mx[j] & 0xFFFFu, mx[j] >> 16);
       }
+      for (int off = 1; off < upg; off <<= 1) {
 #pragma unroll
-      for (int q = 0; q < LB / 16; ++q)
-        blk[q ^ sw] = make_uint4(ow[4 * q], ow[4 * q + 1], ow[4 * q + 2], ow[4 * q + 3]);
-    };
-    auto load_raw = [&](int m, int bk, uint4 (&raw)[LB / 16]) {
-      const uint4* blk = reinterpret_cast<const uint4*>(xs + (size_t)m * a.xstride + (size_t)bk * LB);
-#pragma unroll
-      for (int q = 0; q < LB / 16; ++q) raw[q] = blk[q];
-    };
-    // warp tasks of (row, 32 x 2 lane blocks): both blocks' loads first
-    constexpr int PB = 2;
-    const int csegs = (nblk + 32 * PB - 1) / (32 * PB);
-    for (int task = warp; task < M * csegs; task += MMA_WARPS) {  // warp-uniform
-      const int m = task / csegs, sg = task - m * csegs;
-      uint4 raw[PB][LB / 16];
-#pragma unroll
-      for (int j = 0; j < PB; ++j) {
-        const int bk = (sg * PB + j) * 32 + lane;
-        if (bk < nblk) {
-          load_raw(m, bk, raw[j]);
-        } else {
-#pragma unroll
-          for (int q = 0; q < LB / 16; ++q) raw[j][q] = make_uint4(0, 0, 0, 0);
-        }
+        for (int j = 0; j < PU; ++j) mx[j] = max(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], off));
       }
 #pragma unroll
-      for (int j = 0; j < PB; ++j) {
-        const int bk = (sg * PB + j) * 32 + lane;
-        uint32_t mx = 0;
-#pragma unroll
-        for (int q = 0; q < LB / 16; ++q)
-          mx = hmax2_bf16(mx, hmax2_bf16(hmax2_bf16(raw[j][q].x & 0x7FFF7FFFu, raw[j][q].y & 0x7FFF7FFFu),
-                                         hmax2_bf16(raw[j][q].z & 0x7FFF7FFFu, raw[j][q].w & 0x7FFF7FFFu)));
-        mx = max(mx & 0xFFFFu, mx >> 16);
-        for (int off = 1; off < BPG; off <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      for (int j = 0; j < PU; ++j) {
+        const int u = (sg * pu + j) * 32 + lane;
         // mx: bf16 bits of the group's max|x|; e <= 112 keeps the threshold
         // of bf16x2_to_f16x2 non-negative (groups below 2^-98 lose precision)
-        const int e = max(-126, min(112, 14 - ((int)(mx >> 7) - 127)));
-        if (bk < nblk) {
-          convert(m, bk, raw[j], e);
-          if ((lane & (BPG - 1)) == 0) ginv[(bk / BPG) * 8 + m] = exp2i(-e);
+        const int e = max(-126, min(112, 14 - ((int)(mx[j] >> 7) - 127)));
+        const uint32_t thr = (uint32_t)(112 - e) << 7, t2 = thr | (thr << 16);
+        uint4 o;
+        if constexpr (FMT == FMT_A8) {
+          o = make_uint4(bf16x2_to_f16x2(v[j].x, t2), bf16x2_to_f16x2(v[j].y, t2),
+                         bf16x2_to_f16x2(v[j].z, t2), bf16x2_to_f16x2(v[j].w, t2));
+        } else {
+          // (x0,x1) (x2,x3) (x4,x5) (x6,x7) -> (x0,x4) (x1,x5) (x2,x6) (x3,x7);
+          // the odd codes of each byte pair sit 16x high in A (see a_regs), so
+          // their x is scaled by 2^(e-4)
+          const uint32_t to = (uint32_t)(116 - e) << 7, t2o = to | (to << 16);
+          o = make_uint4(bf16x2_to_f16x2(__byte_perm(v[j].x, v[j].z, 0x5410), t2),
+                         bf16x2_to_f16x2(__byte_perm(v[j].x, v[j].z, 0x7632), t2o),
+                         bf16x2_to_f16x2(__byte_perm(v[j].y, v[j].w, 0x5410), t2),
+                         bf16x2_to_f16x2(__byte_perm(v[j].y, v[j].w, 0x7632), t2o));
+        }
+        if (j < pu && u < U8) {
+          const int ud = (FMT == FMT_A4 && WPL == 4) ? (u ^ ((u >> 3) & 1)) : u;
+          *reinterpret_cast<uint4*>(row + (size_t)ud * 16) = o;
+          if ((u & (upg - 1)) == 0) ginv[(u >> lg_upg) * 8 + m] = exp2i(-e);
         }
       }
     }
+    // scales and biases: entry (mat, tile j, group g, gid) at thread i; the
+    // thread's next entry is MMA_THREADS further (gid stays: 8 | MMA_THREADS)
     const int n = rows * G, ne = RT * G * 8;
-    for (int i = tid; i < NW * ne; i += MMA_THREADS) {
-      const int mat = i / ne, rem = i - mat * ne;
-      const int jg = rem >> 3, gi = rem & 7;
-      const int j = jg / G, g = jg - j * G;
-      const int tr0 = tstart[j], tr1 = tstart[j + 1];
-      const uint16_t* rs = raw + (size_t)(2 * mat) * n;
-      const uint16_t* rb = rs + n;
-      const int ra = tr0 + gi, rbw = tr0 + gi + 8;
-      float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
-      constexpr float TWO24 = 16777216.f;  // the codes enter the mma as q * 2^-24
-      if (ra < tr1) { e.x = bf16f(rs[ra * G + g]) * TWO24; e.z = bf16f(rb[ra * G + g]); }
-      if (rbw < tr1) { e.y = bf16f(rs[rbw * G + g]) * TWO24; e.w = bf16f(rb[rbw * G + g]); }
-      sbf[(size_t)mat * ne + rem] = e;
+    {
+      const int gi = tid & 7;
+      int g = tid >> 3, j = 0, mat = 0;
+      while (g >= G) { g -= G; ++j; }
+      while (j >= RT) { j -= RT; ++mat; }
+      for (int i = tid; i < NW * ne; i += MMA_THREADS) {
+        const int tr0 = tstart[j], tr1 = tstart[j + 1];
+        const uint16_t* rs = raw + (size_t)(2 * mat) * n;
+        const uint16_t* rb = rs + n;
+        const int ra = tr0 + gi, rbw = tr0 + gi + 8;
+        float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
+        constexpr float TWO24 = 16777216.f;  // the codes enter the mma as q * 2^-24
+        if (ra < tr1) { e.x = bf16f(rs[ra * G + g]) * TWO24; e.z = bf16f(rb[ra * G + g]); }
+        if (rbw < tr1) { e.y = bf16f(rs[rbw * G + g]) * TWO24; e.w = bf16f(rb[rbw * G + g]); }
+        sbf[i] = e;
+        g += MMA_THREADS / 8;
+        while (g >= G) { g -= G; ++j; }
+        while (j >= RT) { j -= RT; ++mat; }
+      }
     }
     __syncthreads();
   }

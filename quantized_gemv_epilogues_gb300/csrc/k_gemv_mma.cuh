@@ -37,9 +37,12 @@
 //    order, so a lane reads its B fragments with 16-byte loads and no
 //    shuffles.  The 16 K indices of one k step lie in one quantisation group
 //    (the load width is chosen from the group size).
-//  * Work split: one CTA of 16 warps per SM owns a contiguous range of output
-//    rows (within one row of every other CTA), cut into tiles of at most 16
-//    rows.  A unit is one tile x UK of K: 32 words (128 bytes) per lane.  The
+//  * Work split: one CTA of 16 warps per SM.  A contiguous range of output
+//    rows (within one row of every other range) belongs to a cluster of two
+//    CTAs that take one half of K each (each stages and converts half of x;
+//    their totals meet through distributed shared memory), or to one CTA
+//    when K does not halve into whole groups; a range is cut into tiles of
+//    at most 16 rows.  A unit is one tile x UK of K: 32 words (128 bytes) per lane.  The
 //    CTA's units are dealt to its warps in contiguous ranges; a warp
 //    accumulates along K in registers and writes one partial per tile it
 //    touched, and the epilogue adds a row's partials in warp order
@@ -69,14 +72,16 @@ struct MmaArgs {
   int out_f32;
   int M, K, N;
   int group, lg_group, G;
+  int ck;      // CTAs per cluster sharing a row range: 1, or 2 (each takes half of K)
+  int Kc, Gc;  // K and groups per CTA (K / ck, G / ck)
   int row_bytes;
-  int rows_base, rows_extra;  // CTA i owns rows_base + (i < rows_extra) rows
+  int rows_base, rows_extra;  // row range r owns rows_base + (r < rows_extra) rows
   int KB;                     // units per tile along K: ceil(K / UK)
   int NS;                     // partial slots per warp
   int xstride;                // bytes per staged x row
   int raw_vec;                // 1: raw scales/biases are copied in 16-byte pieces
   // shared-memory byte offsets
-  int off_sbf, off_ginv, off_raw, off_parts, off_tstart;
+  int off_sbf, off_ginv, off_raw, off_parts, off_tstart, off_tot;
 };
 
 // Compile-time shape of one (format, kind, load width) instantiation.
@@ -115,6 +120,27 @@ __device__ __forceinline__ void ldw(uint32_t (&d)[WPL], const uint8_t* p, uint64
                  : "=r"(d[0])
                  : "l"(p), "l"(pol));
   }
+}
+
+// Thread-block cluster helpers (distributed shared memory).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster: the shared-memory writes before
+// it are visible to every CTA after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The float at this CTA's shared address p, read from the same address in
+// the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ float ld_cluster_f32(const float* p, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(p)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
 }
 
 // Packed bf16 maxima.  On non-negative finite values the bf16 order is the
@@ -202,16 +228,21 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
   float4* sbf = reinterpret_cast<float4*>(smem + a.off_sbf);                  // [NW][RT][G][8]
   uint16_t* raw = reinterpret_cast<uint16_t*>(smem + a.off_raw);              // [NW][2][rows*G]
   float* parts = reinterpret_cast<float*>(smem + a.off_parts);                // [W][NS][16][M][NW]
-  float* ginv = reinterpret_cast<float*>(smem + a.off_ginv);                  // [G][8] 2^-e_g
+  float* ginv = reinterpret_cast<float*>(smem + a.off_ginv);                  // [Gc][8] 2^-e_g
   int* tstart = reinterpret_cast<int*>(smem + a.off_tstart);                  // [RT + 1]
+  float* tot = reinterpret_cast<float*>(smem + a.off_tot);                    // [rows][M][NW] (ck 2)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, t = lane & 3;
-  const int cta = blockIdx.x;
-  const int r_begin = cta * a.rows_base + min(cta, a.rows_extra);
-  const int rows = a.rows_base + (cta < a.rows_extra ? 1 : 0);
+  // a cluster of ck CTAs owns a row range; CTA `rank` of it takes the K
+  // range [rank Kc, (rank + 1) Kc) of every row
+  const int rr = blockIdx.x / a.ck;
+  const int rank = a.ck == 2 ? (int)cluster_ctarank() : 0;
+  const int r_begin = rr * a.rows_base + min(rr, a.rows_extra);
+  const int rows = a.rows_base + (rr < a.rows_extra ? 1 : 0);
   const int RT = (rows + 15) >> 4;
   const int KB = a.KB, M = a.M, K = a.K, G = a.G;
+  const int Kc = a.Kc, Gc = a.Gc, K_lo = rank * Kc, g_lo = rank * Gc;
   const int U = RT * KB;
   const int u0 = (int)((long)warp * U / MMA_WARPS), u1 = (int)((long)(warp + 1) * U / MMA_WARPS);
 
@@ -241,10 +272,10 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
         const int rl = tr0 + gid + 8 * h;
         const bool okr = rl < tr1;
         const uint8_t* src = (mat ? a.W1 : a.W0) + (size_t)(r_begin + (okr ? rl : tr0)) * a.row_bytes +
-                             code_bytes<FMT>(k0) + t * WPL * 4;
+                             code_bytes<FMT>(K_lo + k0) + t * WPL * 4;
 #pragma unroll
         for (int ch = 0; ch < CPU; ++ch) {
-          if (okr && k0 + ch * CW < K) {
+          if (okr && k0 + ch * CW < Kc) {
             ldw<WPL>(buf[mat][h][ch], src + code_bytes<FMT>(ch * CW), pol);
           } else {
 #pragma unroll
@@ -262,8 +293,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
     const int mat = NW == 2 ? (lane >> 4) : 0;
     const int idx = NW == 2 ? (lane & 15) : lane;
     const int rl = tr0 + idx / LPR, line = idx % LPR;
-    if (rl < tr1 && (size_t)line * 128 < code_bytes<FMT>(K) - code_bytes<FMT>(k0))
-      prefetch_l2_normal((mat ? a.W1 : a.W0) + (size_t)(r_begin + rl) * a.row_bytes + code_bytes<FMT>(k0) + line * 128);
+    if (rl < tr1 && (size_t)line * 128 < code_bytes<FMT>(Kc) - code_bytes<FMT>(k0))
+      prefetch_l2_normal((mat ? a.W1 : a.W0) + (size_t)(r_begin + rl) * a.row_bytes +
+                         code_bytes<FMT>(K_lo + k0) + line * 128);
   };
 
   // cc: the unit computed next; cl: the next unit to load; cp: the next unit
@@ -283,23 +315,28 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
 
   // raw scales and biases of the CTA's rows (static data: before the wait)
   if constexpr (AFF) {
-    const int n = rows * G;  // per array
-    const size_t off = (size_t)r_begin * G;
+    // [rows][Gc] per array: this CTA's groups of each of its rows
+    const int n = rows * Gc;
 #pragma unroll
     for (int mat = 0; mat < NW; ++mat) {
       const uint16_t* s = mat ? a.s1 : a.s0;
       const uint16_t* b = mat ? a.b1 : a.b0;
       uint16_t* rs = raw + (size_t)(2 * mat) * n;
       uint16_t* rb = rs + n;
-      if (a.raw_vec) {
+      if (a.raw_vec) {  // Gc % 8 == 0: 16-byte pieces
+        const int upr = Gc >> 3;
         for (int i = tid; i < n / 8; i += MMA_THREADS) {
-          cp_async16(rs + i * 8, s + off + i * 8);
-          cp_async16(rb + i * 8, b + off + i * 8);
+          const int rl = i / upr, c = i - rl * upr;
+          const size_t src = (size_t)(r_begin + rl) * G + g_lo + c * 8;
+          cp_async16(rs + i * 8, s + src);
+          cp_async16(rb + i * 8, b + src);
         }
       } else {
         for (int i = tid; i < n; i += MMA_THREADS) {
-          rs[i] = ldg_u16(s + off + i);
-          rb[i] = ldg_u16(b + off + i);
+          const int rl = i / Gc, c = i - rl * Gc;
+          const size_t src = (size_t)(r_begin + rl) * G + g_lo + c;
+          rs[i] = ldg_u16(s + src);
+          rb[i] = ldg_u16(b + src);
         }
       }
     }
@@ -310,12 +347,12 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
 
   // ---- x: raw bf16 rows into shared memory (16-byte asynchronous copies,
   // all in flight together)
-  const int U8 = K / 8;  // 8-element units per row
+  const int U8 = Kc / 8;  // 8-element units of this CTA's K range
   {
     int m = 0, u = tid;
     while (m < M && u >= U8) { u -= U8; ++m; }
     while (m < M) {
-      cp_async16(xs + (size_t)m * a.xstride + (size_t)u * 16, a.x + (size_t)m * K + (size_t)u * 8);
+      cp_async16(xs + (size_t)m * a.xstride + (size_t)u * 16, a.x + (size_t)m * K + K_lo + (size_t)u * 8);
       u += MMA_THREADS;
       while (m < M && u >= U8) { u -= U8; ++m; }
     }
@@ -395,11 +432,11 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
     }
     // scales and biases: entry (mat, tile j, group g, gid) at thread i; the
     // thread's next entry is MMA_THREADS further (gid stays: 8 | MMA_THREADS)
-    const int n = rows * G, ne = RT * G * 8;
+    const int n = rows * Gc, ne = RT * Gc * 8;
     {
       const int gi = tid & 7;
       int g = tid >> 3, j = 0, mat = 0;
-      while (g >= G) { g -= G; ++j; }
+      while (g >= Gc) { g -= Gc; ++j; }
       while (j >= RT) { j -= RT; ++mat; }
       for (int i = tid; i < NW * ne; i += MMA_THREADS) {
         const int tr0 = tstart[j], tr1 = tstart[j + 1];
@@ -408,11 +445,11 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
         const int ra = tr0 + gi, rbw = tr0 + gi + 8;
         float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
         constexpr float TWO24 = 16777216.f;  // the codes enter the mma as q * 2^-24
-        if (ra < tr1) { e.x = bf16f(rs[ra * G + g]) * TWO24; e.z = bf16f(rb[ra * G + g]); }
-        if (rbw < tr1) { e.y = bf16f(rs[rbw * G + g]) * TWO24; e.w = bf16f(rb[rbw * G + g]); }
+        if (ra < tr1) { e.x = bf16f(rs[ra * Gc + g]) * TWO24; e.z = bf16f(rb[ra * Gc + g]); }
+        if (rbw < tr1) { e.y = bf16f(rs[rbw * Gc + g]) * TWO24; e.w = bf16f(rb[rbw * Gc + g]); }
         sbf[i] = e;
         g += MMA_THREADS / 8;
-        while (g >= G) { g -= G; ++j; }
+        while (g >= Gc) { g -= Gc; ++j; }
         while (j >= RT) { j -= RT; ++mat; }
       }
     }
@@ -426,7 +463,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[mat][i] = 0.f;
   const unsigned char* xrow = xs + (size_t)min(gid, M - 1) * a.xstride + t * LB;
-  const int ne = RT * G * 8;
+  const int ne = RT * Gc * 8;
 
   const int jfirst = u0 / KB;
   auto compute_unit = [&](const Cur& c, const uint32_t (&buf)[NW][2][CPU][WPL]) {
@@ -435,7 +472,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
 #pragma unroll
     for (int ch = 0; ch < CPU; ++ch) {
       const int kc = k0 + ch * CW;
-      if (kc >= K) break;
+      if (kc >= Kc) break;
       if constexpr (AFF) {
         if ((kc & (a.group - 1)) == 0) {
 #pragma unroll
@@ -480,7 +517,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
           const float2 gi = *reinterpret_cast<const float2*>(ginv + g * 8 + 2 * t);
 #pragma unroll
           for (int mat = 0; mat < NW; ++mat) {
-            const float4 sb = sbf[(size_t)mat * ne + (j * G + g) * 8 + gid];
+            const float4 sb = sbf[(size_t)mat * ne + (j * Gc + g) * 8 + gid];
             acc[mat][0] = fmaf(fmaf(sb.x, d[mat][0], sb.z * d1[0]), gi.x, acc[mat][0]);
             acc[mat][1] = fmaf(fmaf(sb.x, d[mat][1], sb.z * d1[1]), gi.y, acc[mat][1]);
             acc[mat][2] = fmaf(fmaf(sb.y, d[mat][2], sb.w * d1[0]), gi.x, acc[mat][2]);
@@ -528,15 +565,15 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
   }
   __syncthreads();
 
-  // ---- epilogue: one thread per (activation row, output row); a row's
-  // partials are added in warp order
-  for (int o = tid; o < rows * M; o += MMA_THREADS) {
-    const int m = o / rows, rl = o - m * rows;
+  // ---- epilogue: per (activation row, output row), this CTA's partials of
+  // the row added in warp order; with a cluster of two, each CTA keeps its
+  // K-half totals, and after a cluster barrier the two CTAs finish one half
+  // of the rows each, adding rank 0's total then rank 1's (deterministic)
+  auto cta_total = [&](int rl, int m, float (&v)[NW]) {
     int j = min(RT - 1, rl * RT / rows);
     while (j > 0 && tstart[j] > rl) --j;
     while (j + 1 < RT && tstart[j + 1] <= rl) ++j;
     const int i = rl - tstart[j];
-    float v[NW];
 #pragma unroll
     for (int mat = 0; mat < NW; ++mat) v[mat] = 0.f;
     for (int w = 0; w < MMA_WARPS; ++w) {
@@ -547,6 +584,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
         for (int mat = 0; mat < NW; ++mat) v[mat] += pp[mat];
       }
     }
+  };
+  auto finish = [&](int rl, int m, const float (&v)[NW]) {
     const int n = r_begin + rl;
     float outv;
     if constexpr (KIND == 0) {
@@ -558,7 +597,67 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
       static_cast<float*>(a.out)[(size_t)m * a.N + n] = outv;
     else
       static_cast<uint16_t*>(a.out)[(size_t)m * a.N + n] = f2bf(outv);
+  };
+  if (a.ck == 1) {
+    for (int o = tid; o < rows * M; o += MMA_THREADS) {
+      const int m = o / rows, rl = o - m * rows;
+      float v[NW];
+      cta_total(rl, m, v);
+      finish(rl, m, v);
+    }
+  } else {
+    for (int o = tid; o < rows * M; o += MMA_THREADS) {
+      const int m = o / rows, rl = o - m * rows;
+      float v[NW];
+      cta_total(rl, m, v);
+#pragma unroll
+      for (int mat = 0; mat < NW; ++mat) tot[((size_t)rl * M + m) * NW + mat] = v[mat];
+    }
+    cluster_sync_all();
+    const int half = (rows + 1) >> 1;
+    const int rl0 = rank ? half : 0, nr = rank ? rows - half : half;
+    for (int o = tid; o < nr * M; o += MMA_THREADS) {
+      const int m = o / nr, rl = rl0 + (o - m * nr);
+      float v[NW];
+#pragma unroll
+      for (int mat = 0; mat < NW; ++mat) {
+        const float* q = tot + ((size_t)rl * M + m) * NW + mat;
+        v[mat] = ld_cluster_f32(q, 0) + ld_cluster_f32(q, 1);
+      }
+      finish(rl, m, v);
+    }
+    cluster_sync_all();  // the peer may still read this CTA's totals
   }
+}
+
+// Launches a gemv_mma_kernel instantiation: programmatic stream
+// serialization when l.pdl is set, clusters of ck CTAs when ck == 2.
+template <typename KernelT>
+mt_status launch_mma(KernelT kern, int grid, size_t smem, const Launch& l, const MmaArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(MMA_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = l.stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (l.pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (a.ck == 2) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MT_OK;
 }
 
 // Host plan and launch of the tensor-core kernel for one (format, kind, load
@@ -594,34 +693,59 @@ mt_status run_gemv_mma(const GemvProblem& p, const Launch& l) {
   a.G = AFF ? p.K / p.group : 0;
   a.row_bytes = (int)code_bytes<FMT>(p.K);
 
-  const int grid = di->sm_count < p.N ? di->sm_count : p.N;
-  a.rows_base = p.N / grid;
-  a.rows_extra = p.N % grid;
-  const int rows_max = a.rows_base + (a.rows_extra ? 1 : 0);
-  const int RT = (rows_max + 15) / 16;
-  if (RT > 64) return MT_ERR_SHAPE;  // the tile-start table holds 65 entries
-  a.KB = (p.K + C::UK - 1) / C::UK;
-  const long U = (long)RT * a.KB;
-  const long len = (U + MMA_WARPS - 1) / MMA_WARPS;  // longest warp range
-  a.NS = (int)std::min<long>(RT, (len - 1 + a.KB - 1) / a.KB + 1);
-  a.xstride = (p.K * 2 + 127) / 128 * 128 + mma_row_pad<C::LB>();
-  a.raw_vec = (AFF && a.G % 8 == 0) ? 1 : 0;
-
-  auto al16 = [](size_t v) { return (v + 15) / 16 * 16; };
-  size_t off = al16((size_t)p.M * a.xstride);
-  a.off_sbf = (int)off;
-  if (AFF) off += (size_t)NW * RT * a.G * 8 * 16;
-  a.off_ginv = (int)off;
-  if (AFF) off += (size_t)a.G * 8 * 4;
-  const size_t raw_bytes = AFF ? al16((size_t)NW * 2 * rows_max * a.G * 2) : 0;
-  const size_t parts_bytes = (size_t)MMA_WARPS * a.NS * 16 * p.M * NW * 4;
-  a.off_raw = (int)off;    // the raw scales/biases are dead once the
-  a.off_parts = (int)off;  // mainloop writes its first partial
-  off += std::max(raw_bytes, parts_bytes);
-  a.off_tstart = (int)al16(off);
-  const size_t smem = a.off_tstart + 80 * 4;  // tile starts
+  // The geometry for ck CTAs per row range (1, or a cluster of 2 that
+  // splits K); returns the dynamic shared memory it needs (0: no tile table).
+  const int sms = di->sm_count;
+  int grid = 0;
+  auto plan = [&](int ck) -> size_t {
+    a.ck = ck;
+    a.Kc = p.K / ck;
+    a.Gc = a.G / ck;
+    const int nrange = std::min(sms / ck, p.N);  // row ranges (clusters)
+    grid = nrange * ck;
+    a.rows_base = p.N / nrange;
+    a.rows_extra = p.N % nrange;
+    const int rows_max = a.rows_base + (a.rows_extra ? 1 : 0);
+    const int RT = (rows_max + 15) / 16;
+    if (RT > 64) return 0;  // the tile-start table holds 65 entries
+    a.KB = (a.Kc + C::UK - 1) / C::UK;
+    const long U = (long)RT * a.KB;
+    const long len = (U + MMA_WARPS - 1) / MMA_WARPS;  // longest warp range
+    a.NS = (int)std::min<long>(RT, (len - 1 + a.KB - 1) / a.KB + 1);
+    a.xstride = (a.Kc * 2 + 127) / 128 * 128 + mma_row_pad<C::LB>();
+    a.raw_vec = (AFF && a.Gc % 8 == 0) ? 1 : 0;
+    auto al16 = [](size_t v) { return (v + 15) / 16 * 16; };
+    size_t off = al16((size_t)p.M * a.xstride);
+    a.off_sbf = (int)off;
+    if (AFF) off += (size_t)NW * RT * a.Gc * 8 * 16;
+    a.off_ginv = (int)off;
+    if (AFF) off += (size_t)a.Gc * 8 * 4;
+    const size_t raw_bytes = AFF ? al16((size_t)NW * 2 * rows_max * a.Gc * 2) : 0;
+    const size_t parts_bytes = (size_t)MMA_WARPS * a.NS * 16 * p.M * NW * 4;
+    a.off_raw = (int)off;    // the raw scales/biases are dead once the
+    a.off_parts = (int)off;  // mainloop writes its first partial
+    off += std::max(raw_bytes, parts_bytes);
+    a.off_tstart = (int)al16(off);
+    off = a.off_tstart + 80 * 4;  // tile starts
+    a.off_tot = (int)al16(off);
+    if (ck == 2) off = a.off_tot + (size_t)rows_max * p.M * NW * 4;
+    return off;
+  };
+  // Clusters of two take half of K each when K halves into whole groups and
+  // chunks and a row range stays at least a tile high, and either x would
+  // not fit one CTA's shared memory or it is large next to the CTA's
+  // weights (staging and converting x costs every CTA; measured: a win for
+  // the down projection at M = 8, a loss when x is under ~2/3 of the bytes of
+  // the CTA's weight rows).
   const size_t budget = (size_t)di->max_smem_optin - 1024;
-  if (smem > budget) return MT_ERR_SHAPE;
+  const int Kh = p.K / 2;
+  const bool can2 = sms % 2 == 0 && p.K % 2 == 0 && Kh % C::CW == 0 &&
+                    (!AFF || Kh % p.group == 0) && p.N >= 16 * (sms / 2);
+  size_t smem = plan(1);
+  const double x_bytes = 2.0 * p.M * p.K;
+  const double w_bytes = (double)p.N / sms * (double)a.row_bytes * NW;
+  if (can2 && (smem == 0 || smem > budget || x_bytes * 3 > w_bytes * 2)) smem = plan(2);
+  if (smem == 0 || smem > budget) return MT_ERR_SHAPE;
 
   auto kern = gemv_mma_kernel<FMT, KIND, WPL>;
   {
@@ -632,7 +756,7 @@ mt_status run_gemv_mma(const GemvProblem& p, const Launch& l) {
       cache.attr_set[dev] = 1;
     }
   }
-  return launch(kern, dim3(grid), dim3(MMA_THREADS), smem, l, a);
+  return launch_mma(kern, grid, smem, l, a);
 }
 
 // The load width for a format and group size: a k step's 16 K indices (4

@@ -144,6 +144,10 @@ SHAPES = [  # (fmt, group, M, d, f)
     (2, 128, 5, 1024, 300),
     (2, 32, 2, 256, 170),
     (0, 0, 6, 1536, 350),
+    (1, 64, 3, 512, 1300),     # row ranges shared by clusters of two CTAs (K halves)
+    (1, 128, 8, 768, 1229),
+    (2, 32, 5, 256, 1500),
+    (0, 0, 4, 384, 1250),
 ]
 
 

@@ -199,9 +199,10 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
   // while a CTA waits: its scales and biases and (gate/up) the RMSNorm gain
   // go to shared memory at the start of the PREVIOUS phase's task loop
   // (stage_*_smem; the copies are small next to the weight stream), and its
-  // first rows' weights go to L2 with bulk prefetches right after the CTA has
-  // arrived at the hand-off (prefetch_*).  lay_s[l & 1] must be complete and
-  // visible.  The caller commits the copies.
+  // first rows' weights go to L2 with bulk prefetches as soon as the
+  // hand-off's barrier has passed (prefetch_*; issued between the arrival
+  // and the barrier, their traffic slowed the barrier itself).  lay_s[l & 1]
+  // must be complete and visible.  The caller commits the copies.
   auto stage_gateup_smem = [&](int l) {
     const StackLayerDev& Ly = lay_s[l & 1];
     if constexpr (AFF) stage_sb<0>(a.gu, gateup_w(Ly), cg, smG.sbr, tid, WT_THREADS);
@@ -372,9 +373,9 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
     }
     // ---- down
     {
-      prefetch_down(l);
       if (tid == 0) task_ctr = 2 * WARP_TASK_WARPS;
       if (!grid_wait()) { cp_async_wait_all(); return; }
+      prefetch_down(l);  // after the barrier: its traffic would slow the barrier
       // h (every unit of a batch read before it is used) and the first
       // staging pass over it
       const PhaseW w = down_w(Ly);
@@ -424,8 +425,8 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       }
       if (last) break;
       publish_summed(vnx, y2, have);
-      prefetch_gateup(l + 1);
       if (!grid_wait()) { cp_async_wait_all(); return; }
+      prefetch_gateup(l + 1);
     }
   }
 }

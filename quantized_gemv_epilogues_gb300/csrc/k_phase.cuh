@@ -394,8 +394,9 @@ __device__ __forceinline__ void x_convert(const PhaseGeom& g, const PhaseSmem& s
       uint32_t X[8];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        X[2 * j] = (uint32_t)__float2int_rn(bf16lo(vw[j]) * xscale);
-        X[2 * j + 1] = (uint32_t)__float2int_rn(bf16hi(vw[j]) * xscale);
+        // |x * xscale| < 2^22 by the choice of the piece's scale
+        X[2 * j] = (uint32_t)round_small_to_int(bf16lo(vw[j]) * xscale);
+        X[2 * j + 1] = (uint32_t)round_small_to_int(bf16hi(vw[j]) * xscale);
       }
       if constexpr (FMT == FMT_A8) {
         // unit i = words 2(i&1), 2(i&1)+1 of chunk i>>1; plane p byte 2-p of X

@@ -218,4 +218,12 @@ __device__ __forceinline__ float u8_to_f32(uint32_t w, int sel) {
   return __uint_as_float(m) - 8388608.0f;
 }
 
+// The integer nearest to v (ties to even) for |v| < 2^22, by the same
+// exponent bias run the other way: in [2^23, 2^24) floats are spaced 1, so
+// the fp32 sum v + 1.5 * 2^23 is that integer plus 0x4B400000 in its bit
+// pattern (the addition rounds to nearest even, like cvt.rni).
+__device__ __forceinline__ int round_small_to_int(float v) {
+  return __float_as_int(v + 12582912.0f) - 0x4B400000;
+}
+
 }  // namespace mt

@@ -422,21 +422,16 @@ def run_reference(args):
 SWEEP_REPS = 24  # layers per timed graph in the sweep
 
 
-def run_sweep(args, torch, synth, mt, dev):
-    """Config 5: one d=2048, f=8192 affine INT8 layer (1 % x20 outliers) per
-    point, group in {32, 64, 128} x rows M in {1, 2, 4, 8}: us per layer
-    (add+RMSNorm, gate/up+SwiGLU, down+residual as single calls) and effective
-    GB/s per point, hot and cold.  Hot: the same layer SWEEP_REPS times in one
-    CUDA graph (its 50 MB of weights stay in L2).  Cold: the graph cycles
-    through enough distinct copies of the layer (different seeds) to exceed
-    twice the L2 size, so each layer's weights come from HBM.  One-row points
-    also time the warmed executor (one kernel for all the layers of a plan).
-    The JSON line's value is the geometric mean of the cold GB/s."""
+def measure_layer(wl, args, torch, mt, dev, reps=None):
+    """One layer shape, hot and cold: us per layer of the three single calls
+    (and of each GEMV alone) and, for one row, of the warmed executor.  Hot:
+    the same layer `reps` times in one CUDA graph (weights resident in L2 when
+    they fit).  Cold: the graph cycles through enough distinct copies of the
+    layer (different seeds) to exceed twice the L2 size, so each layer's
+    weights come from HBM."""
     import math
-    reps = SWEEP_REPS
+    reps = reps or SWEEP_REPS
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    points = []
-    peak, peak_kind = measured_peaks()
 
     def timed(fn, n_layers, steps):
         gk = capture(fn, torch, direct=args.no_graph)
@@ -446,48 +441,62 @@ def run_sweep(args, torch, synth, mt, dev):
         del gk
         return us
 
+    n_cold = int(math.ceil(2 * l2 / wl.layer_bytes())) + 1
+    st = Stack(wl, dev, layers=n_cold)
+    hot = [0] * reps
+    cold = list(range(n_cold)) * max(1, reps // n_cold)
+    pt = {"bytes_per_layer": wl.layer_bytes(), "cold_copies": n_cold}
+    for tag, seq in (("", hot), ("_cold", cold)):
+        us = timed(lambda: st.run_layers(seq), len(seq), args.steps)
+        gu = timed(lambda: st.run_layers(seq, ("gateup",)), len(seq), max(5, args.steps // 2))
+        dn = timed(lambda: st.run_layers(seq, ("down",)), len(seq), max(5, args.steps // 2))
+        pt.update({"us_per_layer" + tag: round(us, 3),
+                   "gbs" + tag: round(wl.layer_bytes() / (us * 1e-6) / 1e9, 1),
+                   "gateup_us" + tag: round(gu, 3),
+                   "gateup_gbs" + tag: round(st.gateup_bytes() / (gu * 1e-6) / 1e9, 1),
+                   "down_us" + tag: round(dn, 3),
+                   "down_gbs" + tag: round(st.down_bytes() / (dn * 1e-6) / 1e9, 1)})
+    if wl.M == 1:
+        # executor: a plan of the same layer `reps` times (hot) and the stack
+        # plan over the distinct copies (cold)
+        lay = st.layers[0]
+        hot_plan = mt.mt_mlp_plan_create(
+            [dict(norm_weight=lay["w"], Wg=lay["Wg"], Wu=lay["Wu"], gu_scales=lay["sgu"],
+                  gu_biases=lay["bgu"], Wd=lay["Wd"], d_scales=lay["sd"], d_biases=lay["bd"])] * reps,
+            wl.d, wl.f, wl.group, wl.fmt, wl.eps)
+        vals = torch.zeros(reps, 1, wl.d, dtype=torch.bfloat16, device=dev)
+        vals.copy_(st.values[:1].expand(reps, 1, wl.d))
+        try:
+            us_h = timed(lambda: mt.mt_mlp_plan_run(hot_plan, vals, st.r0, st.out_y), reps, args.steps)
+        finally:
+            mt.mt_mlp_plan_destroy(hot_plan)
+        us_c = timed(st.step_executor, n_cold, args.steps)
+        pt.update({"executor_us": round(us_h, 3),
+                   "executor_gbs": round(wl.layer_bytes() / (us_h * 1e-6) / 1e9, 1),
+                   "executor_us_cold": round(us_c, 3),
+                   "executor_gbs_cold": round(wl.layer_bytes() / (us_c * 1e-6) / 1e9, 1)})
+    st.close()
+    del st
+    torch.cuda.empty_cache()
+    return pt
+
+
+def run_sweep(args, torch, synth, mt, dev):
+    """Config 5: one d=2048, f=8192 affine INT8 layer (1 % x20 outliers) per
+    point, group in {32, 64, 128} x rows M in {1, 2, 4, 8}: us per layer
+    (add+RMSNorm, gate/up+SwiGLU, down+residual as single calls) and effective
+    GB/s per point, hot and cold (measure_layer; one-row points also time the
+    warmed executor).  The JSON line's value is the geometric mean of the cold
+    GB/s."""
+    import math
+    reps = SWEEP_REPS
+    points = []
+    peak, peak_kind = measured_peaks()
     for g in ((args.sweep_group,) if args.sweep_group else (32, 64, 128)):
         for M in ((args.sweep_rows,) if args.sweep_rows else (1, 2, 4, 8)):
-            wl = synth.sweep_point(g, M)
-            n_cold = int(math.ceil(2 * l2 / wl.layer_bytes())) + 1
-            st = Stack(wl, dev, layers=n_cold)
-            hot = [0] * reps
-            cold = list(range(n_cold)) * max(1, reps // n_cold)
-            pt = {"group": g, "M": M, "bytes_per_layer": wl.layer_bytes(), "cold_copies": n_cold}
-            for tag, seq in (("", hot), ("_cold", cold)):
-                us = timed(lambda: st.run_layers(seq), len(seq), args.steps)
-                gu = timed(lambda: st.run_layers(seq, ("gateup",)), len(seq), max(5, args.steps // 2))
-                dn = timed(lambda: st.run_layers(seq, ("down",)), len(seq), max(5, args.steps // 2))
-                pt.update({"us_per_layer" + tag: round(us, 3),
-                           "gbs" + tag: round(wl.layer_bytes() / (us * 1e-6) / 1e9, 1),
-                           "gateup_us" + tag: round(gu, 3),
-                           "gateup_gbs" + tag: round(st.gateup_bytes() / (gu * 1e-6) / 1e9, 1),
-                           "down_us" + tag: round(dn, 3),
-                           "down_gbs" + tag: round(st.down_bytes() / (dn * 1e-6) / 1e9, 1)})
-            if M == 1:
-                # executor: a plan of the same layer `reps` times (hot) and the
-                # stack plan over the distinct copies (cold)
-                lay = st.layers[0]
-                hot_plan = mt.mt_mlp_plan_create(
-                    [dict(norm_weight=lay["w"], Wg=lay["Wg"], Wu=lay["Wu"], gu_scales=lay["sgu"],
-                          gu_biases=lay["bgu"], Wd=lay["Wd"], d_scales=lay["sd"], d_biases=lay["bd"])] * reps,
-                    wl.d, wl.f, g, wl.fmt, wl.eps)
-                vals = torch.zeros(reps, 1, wl.d, dtype=torch.bfloat16, device=dev)
-                vals.copy_(st.values[:1].expand(reps, 1, wl.d))
-                try:
-                    us_h = timed(lambda: mt.mt_mlp_plan_run(hot_plan, vals, st.r0, st.out_y), reps,
-                                 args.steps)
-                finally:
-                    mt.mt_mlp_plan_destroy(hot_plan)
-                us_c = timed(st.step_executor, n_cold, args.steps)
-                pt.update({"executor_us": round(us_h, 3),
-                           "executor_gbs": round(wl.layer_bytes() / (us_h * 1e-6) / 1e9, 1),
-                           "executor_us_cold": round(us_c, 3),
-                           "executor_gbs_cold": round(wl.layer_bytes() / (us_c * 1e-6) / 1e9, 1)})
+            pt = {"group": g, "M": M}
+            pt.update(measure_layer(synth.sweep_point(g, M), args, torch, mt, dev, reps))
             points.append(pt)
-            st.close()
-            del st
-            torch.cuda.empty_cache()
     gm = math.exp(sum(math.log(p["gbs_cold"]) for p in points) / len(points))
     gm_hot = math.exp(sum(math.log(p["gbs"]) for p in points) / len(points))
     line = {"metric": METRIC, "value": round(gm, 2), "unit": "GB/s", "n_gpus": 1,
@@ -504,6 +513,33 @@ def run_sweep(args, torch, synth, mt, dev):
     return 0
 
 
+def run_configs(args, torch, synth, mt, dev):
+    """Configs 1-3 (tiny, Llama-3.2-1B-shaped affine INT4, Qwen2.5-1.5B-shaped
+    bf16): each layer hot and cold through the single calls and the warmed
+    executor (measure_layer).  The JSON line's value is the geometric mean of
+    the cold GB/s of the single calls."""
+    import math
+    peak, peak_kind = measured_peaks()
+    points = []
+    for wl in (synth.TINY, synth.LLAMA1B, synth.QWEN15):
+        pt = {"workload": wl.name}
+        pt.update(measure_layer(wl, args, torch, mt, dev))
+        points.append(pt)
+    gm = math.exp(sum(math.log(p["gbs_cold"]) for p in points) / len(points))
+    line = {"metric": METRIC, "value": round(gm, 2), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "per-config weights/f32-acc",
+            "data": "synthetic",
+            "config": {"workload": "configs 1-3: tiny d256 f768 affine8 g64; llama3.2-1b layer d2048 "
+                                   "f8192 affine4 g64; qwen2.5-1.5b layer d1536 f8960 bf16; one row",
+                       "l2": "value: cold (distinct layer copies > 2x L2 cycled); hot: one layer x "
+                             f"{SWEEP_REPS} in one graph"},
+            "peak": peak, "peak_kind": peak_kind, "points": points,
+            "device_error": mt.mt_device_error()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -511,8 +547,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mt", choices=["mt", "reference"])
     ap.add_argument("--workload", default="qwen3-8b",
-                    choices=["qwen3-8b", "tiny", "llama1b", "qwen15", "sweep"],
-                    help="sweep: every group x M point of the d=2048, f=8192 sweep, one line")
+                    choices=["qwen3-8b", "tiny", "llama1b", "qwen15", "sweep", "configs"],
+                    help="sweep: every group x M point of the d=2048, f=8192 sweep, one line; "
+                         "configs: the tiny, Llama-3.2-1B and Qwen2.5-1.5B layers hot and cold, one line")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
     ap.add_argument("--sweep-group", type=int, default=None, choices=[32, 64, 128],
                     help="sweep: only this group size")
@@ -550,6 +587,8 @@ def main():
 
     if args.workload == "sweep":
         return run_sweep(args, torch, synth, mt, dev)
+    if args.workload == "configs":
+        return run_configs(args, torch, synth, mt, dev)
     wl = {"qwen3-8b": synth.QWEN8B, "tiny": synth.TINY, "llama1b": synth.LLAMA1B,
           "qwen15": synth.QWEN15}[args.workload]
     if args.layers:

@@ -148,6 +148,8 @@ SHAPES = [  # (fmt, group, M, d, f)
     (1, 128, 8, 768, 1229),
     (2, 32, 5, 256, 1500),
     (0, 0, 4, 384, 1250),
+    (1, 32, 6, 1024, 1400),    # clusters with 8-byte weight loads
+    (2, 64, 7, 512, 1600),
 ]
 
 

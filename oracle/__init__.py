@@ -23,6 +23,10 @@ What each function follows (meTile docs unless stated):
 * :func:`down_residual` -- values @ weight.T + residual, the down projection
   with the residual added in its epilogue ("Compute-Graph Fusion", Automatic
   Gated Epilogues; "MLX-LM Backend", Dispatch Policy).
+* :func:`linear_bias` -- values @ weight.T + bias for the attention
+  projections (q/k/v/o, bias kept) and the vocabulary projection, which run
+  the same one-row GEMV ("MLX-LM Backend", the attention-projection and
+  vocabulary compression passages before Dispatch Policy).
 * :func:`mlp_layer`, :func:`mlp_stack` -- the three steps composed; a stack
   layer takes the previous layer's output as its residual.
 
@@ -77,6 +81,7 @@ def _L():
                 "orc_silu": (D, [D]),
                 "orc_swiglu_gateup": (I, [P, L, L, L, I, P, P, P, P, P, P, I, P, P, P]),
                 "orc_down_residual": (I, [P, L, L, L, I, P, P, P, I, P, P]),
+                "orc_linear_bias": (I, [P, L, L, L, I, P, P, P, I, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -232,6 +237,25 @@ def down_residual(h, Wd: Weight, res):
                                 _p(Wd.biases), Wd.group, res.ctypes.data, y.ctypes.data)
     if rc:
         raise ValueError("orc_down_residual: bad arguments")
+    return y
+
+
+# ----------------------------------------------------------- projection
+def linear_bias(x, W: Weight, bias=None):
+    """y[m, n] = x[m] . W[n] + bias[n] (bias bf16 [N], or None for none),
+    exact float64 [M, N]."""
+    x = _c(np.atleast_2d(x), np.uint16)
+    M, K = x.shape
+    N, K2 = W.shape
+    assert K2 == K
+    if bias is not None:
+        bias = _c(bias, np.uint16).reshape(-1)
+        assert bias.shape == (N,)
+    y = np.empty((M, N), dtype=np.float64)
+    rc = _L().orc_linear_bias(x.ctypes.data, M, K, N, W.fmt, W.W.ctypes.data, _p(W.scales),
+                              _p(W.biases), W.group, _p(bias), y.ctypes.data)
+    if rc:
+        raise ValueError("orc_linear_bias: bad arguments")
     return y
 
 

@@ -17,6 +17,11 @@
  *    group-wise weights w = scale * q + bias with groups of 32/64/128 along K,
  *    INT8 and 4-bit "affine nibbles, scales, and biases", dense BF16 weights,
  *    and the exact "values @ weight.T + residual" down projection.
+ *  - "MLX-LM Backend", the attention-projection and vocabulary compression
+ *    passages before Dispatch Policy: the q/k/v/o projections of a layer and
+ *    the vocabulary projection (a tied embedding used as a linear map, or an
+ *    untied lm_head) run the same one-row GEMV, and the projection bias is
+ *    kept: y = x @ weight.T + bias.
  *  - ANEForge docs, "The optimizer and the cost model", The roofline: a weight
  *    is stored [N, K] (K contiguous) and x[.., K] @ W[N, K]^T gives [.., N].
  *
@@ -34,6 +39,8 @@
  *  - SwiGLU: h = silu(g) * u with silu(g) = g / (1 + exp(-g)), no rounding
  *    of g, u or the sigmoid before h.
  *  - down: y = sum_k h_k * W[n,k] + residual_n, rounded once.
+ *  - projection: y = sum_k x_k * W[n,k] + bias_n (bias bf16, absent = 0),
+ *    rounded once.
  */
 #include <math.h>
 #include <stddef.h>
@@ -272,6 +279,24 @@ int orc_down_residual(const uint16_t* hin, long M, long K, long N, int fmt,
       for (long k = 0; k < K; ++k)
         acc += orc_f64_from_bf16(hin[m * K + k]) * orc_weight(fmt, Wd, s, b, K, group, n, k);
       y[m * N + n] = acc + orc_f64_from_bf16(res[m * N + n]);
+    }
+  return 0;
+}
+
+/* ------------------------------------------------------- projection */
+
+/* y[m][n] = sum_k x[m][k] * W[n][k] + bias[n]  (exact, not rounded);
+ * bias is a bf16 vector [N] or NULL for a projection without bias. */
+int orc_linear_bias(const uint16_t* x, long M, long K, long N, int fmt,
+                    const void* W, const uint16_t* s, const uint16_t* b, int group,
+                    const uint16_t* bias, double* y) {
+  if (orc_check_fmt(fmt, K, group)) return -1;
+  for (long m = 0; m < M; ++m)
+    for (long n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (long k = 0; k < K; ++k)
+        acc += orc_f64_from_bf16(x[m * K + k]) * orc_weight(fmt, W, s, b, K, group, n, k);
+      y[m * N + n] = bias ? acc + orc_f64_from_bf16(bias[n]) : acc;
     }
   return 0;
 }

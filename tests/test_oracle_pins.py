@@ -426,6 +426,59 @@ def test_down_residual_zero_weights_and_identity():
     assert np.array_equal(y, 2.0 * hf[:, [3 * n + 1 for n in range(N)]])
 
 
+# ------------------------------------------------------------ projection
+@pytest.mark.parametrize("fmt_bits,group,with_bias", [(8, 32, True), (4, 128, True), (16, 0, True),
+                                                      (8, 64, False)])
+def test_linear_bias_brute_force(fmt_bits, group, with_bias):
+    M, K, N = 3, 256, 9
+    x = gen_bf16(M * K, 111).reshape(M, K)
+    W = _weight(fmt_bits, N, K, group, 112)
+    bias = gen_bf16(N, 113) if with_bias else None
+    y = oracle.linear_bias(x, W, bias)
+    xf = [[Fraction(float(t)) for t in row] for row in torch_f64_from_bf16(x)]
+    bf = torch_f64_from_bf16(bias) if with_bias else np.zeros(N)
+    D = _frac_dense(W)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(a * b for a, b in zip(xf[m], D[n])) + Fraction(float(bf[n]))
+            scale = float(sum(abs(a * b) for a, b in zip(xf[m], D[n]))) + abs(float(bf[n]))
+            assert abs(y[m, n] - float(exact)) <= 1e-14 * scale
+    if with_bias:
+        # the bias is indexed by the output column, not by the row
+        assert not np.allclose(y, oracle.linear_bias(x, W, bias[::-1].copy()))
+
+
+def test_linear_bias_zero_weights_and_selection():
+    M, K, N = 2, 128, 6
+    x = gen_bf16(M * K, 121).reshape(M, K)
+    bias = gen_bf16(N, 122)
+    zero = _const_weight(N, K, 64, 0, 0, 0)
+    y = oracle.linear_bias(x, zero, bias)
+    assert np.array_equal(y, np.broadcast_to(torch_f64_from_bf16(bias), (M, N)))
+    assert np.array_equal(oracle.linear_bias(x, zero), np.zeros((M, N)))
+    # one non-zero column per row: row n of W picks x[:, 5n + 2] times 0.5
+    sel = np.zeros((N, K), np.uint16)
+    for n in range(N):
+        sel[n, 5 * n + 2] = 0x3F00  # weight 0.5
+    y = oracle.linear_bias(x, oracle.Weight(oracle.FMT_BF16, sel), bias)
+    xf = torch_f64_from_bf16(x)
+    expect = 0.5 * xf[:, [5 * n + 2 for n in range(N)]] + torch_f64_from_bf16(bias)[None, :]
+    assert np.array_equal(y, expect)
+
+
+def test_linear_bias_tied_embedding_reading():
+    # A tied embedding used as the vocabulary projection: E [V, d] is the weight
+    # as stored ([N, K] = [V, d]), so a one-hot activation e_j returns column j
+    # of E for every vocabulary row, and the logit of row v is x . E[v].
+    V, d = 11, 64
+    E = _weight(8, V, d, 32, 131)
+    Ed = E.dense()
+    for j in (0, 17, d - 1):
+        x = np.zeros((1, d), np.uint16)
+        x[0, j] = 0x3F80  # 1.0
+        assert np.array_equal(oracle.linear_bias(x, E)[0], Ed[:, j])
+
+
 # ----------------------------------------------------------- composition
 def test_mlp_layer_and_stack_composition():
     d, f, M, g = 64, 96, 2, 32

@@ -540,6 +540,119 @@ def run_configs(args, torch, synth, mt, dev):
     return 0
 
 
+class ProjStack:
+    """Device-resident projection weights of one decode step: per layer the
+    stacked q/k/v weight (and bias) and the o weight, and one vocabulary
+    weight, generated by the seeded generator and packed by the library."""
+
+    def __init__(self, pw, device, M=None):
+        import torch
+        import synth
+        import quantized_gemv_epilogues_gb300 as mt
+        self.mt, self.pw = mt, pw
+        self.M = M or pw.M
+        bf = torch.bfloat16
+        biggest = max(p.N * p.K for p in pw.projs)
+        tmp = torch.empty(biggest if pw.fmt != synth.FMT_BF16 else 1, dtype=torch.float32, device=device)
+        self.items = []   # (projection, layer, W, s, b, bias, x, y)
+        self.x = {}
+        for p in pw.projs:
+            x = torch.empty(self.M, p.K, dtype=bf, device=device)
+            synth.device_bf16(x, synth.seed_for(pw.wid, 0, synth.T_X) + p.tensor, synth.ACT)
+            y = torch.empty(self.M, p.N, dtype=bf, device=device)
+            for l in range(pw.layers if p.per_layer else 1):
+                sd = lambda t: synth.seed_for(pw.wid, l, t)
+                if pw.fmt == synth.FMT_BF16:
+                    W = torch.empty(p.N, p.K, dtype=bf, device=device)
+                    synth.device_bf16(W, sd(p.tensor), pw.weight_dist)
+                    s = b = None
+                else:
+                    W = torch.empty(p.N, p.K * pw.bits // 8, dtype=torch.uint8, device=device)
+                    s = torch.empty(p.N, p.K // pw.group, dtype=bf, device=device)
+                    b = torch.empty_like(s)
+                    W32 = tmp[:p.N * p.K].view(p.N, p.K)
+                    synth.device_f32(W32, sd(p.tensor), pw.weight_dist)
+                    mt.mt_pack_affine(W32, p.N, p.K, pw.group, pw.bits, W, s, b)
+                bias = None
+                if p.bias is not None:
+                    bias = torch.empty(p.N, dtype=bf, device=device)
+                    synth.device_bf16(bias, sd(p.bias), synth.PROJ_BIAS)
+                self.items.append((p, l, W, s, b, bias, x, y))
+        del tmp
+        torch.cuda.synchronize()
+
+    def run(self, names=None):
+        mt, pw = self.mt, self.pw
+        for (p, l, W, s, b, bias, x, y) in self.items:
+            if names is None or p.name in names:
+                mt.mt_linear_bias(x, W, s, b, pw.group, bias, y, fmt=pw.fmt)
+
+    def launches(self, names=None):
+        return sum(1 for it in self.items if names is None or it[0].name in names)
+
+    def bytes(self, names=None):
+        pw = self.pw
+        tot = 0
+        for (p, l, *_rest) in self.items:
+            if names is None or p.name in names:
+                tot += pw.proj_weight_bytes(p) + 2 * self.M * (p.K + p.N)
+        return tot
+
+
+def run_projections(args, torch, synth, mt, dev):
+    """The projection GEMV (mt_linear_bias) over one decode step of each model:
+    per layer the stacked q/k/v projection (with its bias where the model has
+    one) and the o projection, then the vocabulary projection once.  Every
+    weight is distinct and the step's weights exceed the L2, so each launch
+    reads its weights from HBM.  Per model: us per step, effective GB/s of the
+    step and of each projection kind alone.  The JSON line's value is the
+    Qwen3-8B step's GB/s."""
+    peak, peak_kind = measured_peaks()
+    points = []
+    for pw in synth.PROJ_ALL:
+        M = args.rows or pw.M
+        ps = ProjStack(pw, dev, M)
+        pt = {"workload": pw.name, "M": M, "step_bytes": ps.bytes(), "launches": ps.launches()}
+        g = capture(ps.run, torch, direct=args.no_graph)
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+        steps = max(5, args.steps // 10)
+        with ClockSampler(dev.index or 0) as clk:
+            ms = time_graph(g, steps, torch)
+        del g
+        pt.update({"us_per_step": round(ms * 1e3, 2),
+                   "gbs": round(ps.bytes() / (ms * 1e-3) / 1e9, 1),
+                   "frac_of_measured_hbm": round(ps.bytes() / (ms * 1e-3) / 1e9 / peak, 4),
+                   "clocks": clk.summary()})
+        for p in pw.projs:
+            gk = capture(lambda: ps.run((p.name,)), torch, direct=args.no_graph)
+            for _ in range(3):
+                gk.replay()
+            us = time_graph(gk, steps, torch) * 1e3 / ps.launches((p.name,))
+            del gk
+            nb = ps.bytes((p.name,)) / ps.launches((p.name,))
+            pt[p.name] = {"K": p.K, "N": p.N, "bias": p.bias is not None, "us_per_launch": round(us, 3),
+                          "gbs": round(nb / (us * 1e-6) / 1e9, 1)}
+        points.append(pt)
+        del ps
+        torch.cuda.empty_cache()
+    head = points[0]
+    lm = head["lm_head"]
+    line = {"metric": "µs per decode step of the attention and vocabulary projections and effective HBM GB/s",
+            "value": head["gbs"], "unit": "GB/s", "n_gpus": 1,
+            "steps": max(5, args.steps // 10), "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "per-model weights/f32-acc",
+            "data": "synthetic",
+            "config": {"workload": "; ".join(pw.name for pw in synth.PROJ_ALL),
+                       "l2": "every weight distinct, step weights > L2"},
+            "roofline": {"bound": "hbm", "kernel": "gemv_warp_kernel lm_head 4096x151936 affine8 g128",
+                         "achieved": lm["gbs"], "peak": peak, "unit": "GB/s",
+                         "frac": round(lm["gbs"] / peak, 4), "peak_kind": peak_kind},
+            "points": points, "device_error": mt.mt_device_error()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -547,9 +660,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mt", choices=["mt", "reference"])
     ap.add_argument("--workload", default="qwen3-8b",
-                    choices=["qwen3-8b", "tiny", "llama1b", "qwen15", "sweep", "configs"],
+                    choices=["qwen3-8b", "tiny", "llama1b", "qwen15", "sweep", "configs", "projections"],
                     help="sweep: every group x M point of the d=2048, f=8192 sweep, one line; "
-                         "configs: the tiny, Llama-3.2-1B and Qwen2.5-1.5B layers hot and cold, one line")
+                         "configs: the tiny, Llama-3.2-1B and Qwen2.5-1.5B layers hot and cold, one line; "
+                         "projections: attention and vocabulary projections of a decode step per model")
+    ap.add_argument("--rows", type=int, default=None, choices=range(1, 9),
+                    help="projections: rows M (default one, decode)")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
     ap.add_argument("--sweep-group", type=int, default=None, choices=[32, 64, 128],
                     help="sweep: only this group size")
@@ -589,6 +705,8 @@ def main():
         return run_sweep(args, torch, synth, mt, dev)
     if args.workload == "configs":
         return run_configs(args, torch, synth, mt, dev)
+    if args.workload == "projections":
+        return run_projections(args, torch, synth, mt, dev)
     wl = {"qwen3-8b": synth.QWEN8B, "tiny": synth.TINY, "llama1b": synth.LLAMA1B,
           "qwen15": synth.QWEN15}[args.workload]
     if args.layers:

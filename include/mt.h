@@ -19,6 +19,15 @@
  *                     projection"); "MLX-LM Backend", Dispatch Policy
  *                     ("values @ weight.T + residual").
  *
+ * and, for the rest of a decode step, the same GEMV as a projection:
+ *
+ *   mt_linear_bias    y = x @ W^T (+ bias): the attention projections q/k/v/o
+ *                     (bias kept where the model has one) and the vocabulary
+ *                     projection (untied lm_head, or a tied embedding table
+ *                     used as the weight).  meTile docs, "MLX-LM Backend", the
+ *                     attention-projection and vocabulary compression passages
+ *                     before Dispatch Policy.
+ *
  * plus the offline packer mt_pack_affine (affine group quantisation of fp32
  * weights into the stored layout), and the warmed executor mt_mlp_plan_*
  * that runs L such layers back to back as one persistent kernel.
@@ -159,6 +168,32 @@ mt_status mt_down_residual(const void* h, const void* Wd, const void* scales,
                            const void* biases, int group, const void* residual,
                            void* out_y, int M, int f, int d,
                            mt_wfmt fmt, mt_dtype out_dtype, void* stream);
+
+/*
+ * Projection GEMV with an optional bias epilogue.
+ *   x        : bf16 [M][K]
+ *   W        : [N][K] in format fmt.  q, k and v of one layer share x, so a
+ *              caller may stack their rows into one [Nq + Nk + Nv][K] weight
+ *              (and one bias) and make one call.  A tied embedding table
+ *              [vocab][K] is used as W unchanged.
+ *   scales   : bf16 [N][K/group] (NULL for MT_W_BF16)
+ *   biases   : bf16 [N][K/group] (NULL for MT_W_BF16)
+ *   bias     : bf16 [N], added to every row, or NULL for a projection without
+ *              bias
+ *   out_y    : [M][N] of out_dtype, y = x . W[n] (+ bias[n]), fp32
+ *              accumulation, one rounding.
+ * Limits: 1 <= M <= 8; K % group == 0 (affine), K % 8 == 0 (bf16);
+ *         K <= 32768; 1 <= N <= 1048576.
+ * Aliasing: out_y overlaps no input.
+ * meTile docs, "MLX-LM Backend", the attention-projection compression passage
+ * (q_proj, k_proj, v_proj and o_proj per layer, projection biases preserved,
+ * one-row decode only) and the vocabulary compression passage (tied
+ * embedding's linear projection or untied lm_head, one-row decode only).
+ */
+mt_status mt_linear_bias(const void* x, const void* W, const void* scales,
+                         const void* biases, int group, const void* bias,
+                         void* out_y, int M, int K, int N,
+                         mt_wfmt fmt, mt_dtype out_dtype, void* stream);
 
 /*
  * Affine group quantiser and packer (offline preparation; stream-ordered).

@@ -11,6 +11,8 @@ Calls (same names as the C ABI):
 * :func:`mt_add_rmsnorm` -- residual add + RMSNorm, both outputs written.
 * :func:`mt_swiglu_gateup` -- gate/up GEMV with the silu(gate) * up epilogue.
 * :func:`mt_down_residual` -- down GEMV with the residual added in its epilogue.
+* :func:`mt_linear_bias` -- projection GEMV with an optional bias (attention
+  q/k/v/o, vocabulary projection).
 * :func:`mt_pack_affine` / :func:`mt_unpack_affine` -- affine group packer.
 * :func:`mt_mlp_plan_create` / :func:`mt_mlp_plan_run` / :func:`mt_mlp_plan_destroy`
   -- the warmed executor: L one-row layers as one persistent kernel.
@@ -46,6 +48,7 @@ _SIGS = {
     "mt_add_rmsnorm": (_I, [_P, _P, _P, _F, _P, _P, _I, _I, _I, _P]),
     "mt_swiglu_gateup": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "mt_down_residual": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "mt_linear_bias": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
     "mt_pack_affine": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "mt_unpack_affine": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "mt_set_option": (_I, [_I, _I]),
@@ -159,6 +162,20 @@ def mt_down_residual(h, Wd, scales, biases, group, residual, out_y, M=None, f=No
                                  _ptr(residual), _ptr(out_y), M, f, d, int(fmt), od,
                                  _stream(stream)),
            "mt_down_residual")
+
+
+def mt_linear_bias(x, W, scales, biases, group, bias, out_y, M=None, K=None, N=None, fmt=None,
+                   out_dtype=None, stream=None):
+    if M is None or K is None:
+        M, K = _rows_cols(x)
+    if N is None:
+        N = _rows_cols(out_y)[1]
+    if fmt is None:
+        raise TypeError("fmt (MT_W_BF16 / MT_W_AFFINE8 / MT_W_AFFINE4) is required")
+    od = _odt(out_y, out_dtype) if not isinstance(out_y, int) else (out_dtype or MT_BF16)
+    _check(_lib.mt_linear_bias(_ptr(x), _ptr(W), _ptr(scales), _ptr(biases), int(group),
+                               _ptr(bias), _ptr(out_y), M, K, N, int(fmt), od, _stream(stream)),
+           "mt_linear_bias")
 
 
 def mt_pack_affine(W, N, K, group, bits, q, scales, biases, stream=None):

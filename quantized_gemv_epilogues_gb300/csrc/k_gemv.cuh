@@ -44,7 +44,8 @@ struct GemvArgs {
   const uint16_t* b0;
   const uint16_t* s1;
   const uint16_t* b1;
-  const uint16_t* res;
+  const uint16_t* res;  // addend (residual or bias) or nullptr
+  int res_ld;           // its row stride in elements (0: one bias row for every m)
   void* out;
   int M, K, N;
   int group, G;         // group size along K and groups per row
@@ -307,7 +308,8 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvArgs a) {
         if constexpr (KIND == 0) {
           outv = v0 / (1.0f + expf(-v0)) * v1;  // silu(gate) * up
         } else {
-          outv = v0 + bf16f(a.res[(size_t)m * a.N + n]);  // + residual
+          if (a.res) outv = v0 + bf16f(a.res[(size_t)m * a.res_ld + n]);  // + residual or bias
+          else outv = v0;
         }
         if (a.out_f32)
           static_cast<float*>(a.out)[(size_t)m * a.N + n] = outv;

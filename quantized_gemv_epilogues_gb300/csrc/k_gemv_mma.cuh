@@ -67,7 +67,8 @@ struct MmaArgs {
   const uint16_t* b0;
   const uint16_t* s1;
   const uint16_t* b1;
-  const uint16_t* res;
+  const uint16_t* res;  // addend (residual or bias) or nullptr
+  int res_ld;           // its row stride in elements (0: one bias row for every m)
   void* out;
   int out_f32;
   int M, K, N;
@@ -591,7 +592,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
     if constexpr (KIND == 0) {
       outv = v[0] / (1.0f + expf(-v[0])) * v[NW - 1];  // silu(gate) * up
     } else {
-      outv = v[0] + bf16f(a.res[(size_t)m * a.N + n]);  // + residual
+      outv = a.res ? v[0] + bf16f(a.res[(size_t)m * a.res_ld + n]) : v[0];  // + residual or bias
     }
     if (a.out_f32)
       static_cast<float*>(a.out)[(size_t)m * a.N + n] = outv;
@@ -685,6 +686,7 @@ mt_status run_gemv_mma(const GemvProblem& p, const Launch& l) {
   a.W1 = static_cast<const uint8_t*>(p.W1);
   a.s0 = p.s0; a.b0 = p.b0; a.s1 = p.s1; a.b1 = p.b1;
   a.res = p.res;
+  a.res_ld = p.res_ld;
   a.out = p.out;
   a.out_f32 = p.out_f32 ? 1 : 0;
   a.M = p.M; a.K = p.K; a.N = p.N;

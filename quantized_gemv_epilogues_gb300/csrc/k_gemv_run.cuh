@@ -39,6 +39,7 @@ mt_status run_gemv(const GemvProblem& p, const Launch& l) {
   a.W1 = static_cast<const uint8_t*>(p.W1);
   a.s0 = p.s0; a.b0 = p.b0; a.s1 = p.s1; a.b1 = p.b1;
   a.res = p.res;
+  a.res_ld = p.res_ld;
   a.out = p.out;
   a.M = p.M; a.K = p.K; a.N = p.N;
   a.group = AFF ? p.group : 1;

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
       const float v1 = row_total<NW>(g, sm.parts, rl, 1);
       outv = v0 / (1.0f + expf(-v0)) * v1;  // silu(gate) * up
     } else {
-      outv = v0 + bf16f(a.res[n]);  // + residual
+      outv = a.res ? v0 + bf16f(a.res[n]) : v0;  // + residual or bias (one row)
     }
     if (a.out_f32)
       static_cast<float*>(a.out)[n] = outv;

@@ -203,6 +203,43 @@ mt_status mt_down_residual(const void* h, const void* Wd, const void* scales, co
   p.s0 = (const uint16_t*)scales;
   p.b0 = (const uint16_t*)biases;
   p.res = (const uint16_t*)residual;
+  p.res_ld = d;
+  p.out = out_y;
+  p.out_f32 = out_dtype == MT_F32;
+  return launch_gemv(p, make_launch(stream));
+}
+
+mt_status mt_linear_bias(const void* x, const void* W, const void* scales, const void* biases,
+                         int group, const void* bias, void* out_y, int M, int K, int N,
+                         mt_wfmt fmt, mt_dtype out_dtype, void* stream) {
+  if (fmt != MT_W_BF16 && fmt != MT_W_AFFINE8 && fmt != MT_W_AFFINE4) return MT_ERR_FORMAT;
+  if (out_dtype != MT_BF16 && out_dtype != MT_F32) return MT_ERR_FORMAT;
+  if (!x || !W || !out_y) return MT_ERR_NULL;
+  if (fmt != MT_W_BF16 && (!scales || !biases)) return MT_ERR_NULL;
+  if (M < 1 || M > 8 || K < 1 || K > 32768 || N < 1 || N > (1 << 20)) return MT_ERR_SHAPE;
+  mt_status st = MT_OK;
+  if (!valid_group(fmt, group, K, &st)) return st;
+  if (!aligned16(x) || !aligned16(W) || !aligned16(out_y) || (bias && !aligned16(bias)) ||
+      (fmt != MT_W_BF16 && (!aligned16(scales) || !aligned16(biases))))
+    return MT_ERR_ALIGN;
+  const size_t wb = weight_bytes(fmt, N, K);
+  const size_t sbb = fmt == MT_W_BF16 ? 0 : (size_t)N * (K / group) * 2;
+  const Range ro = rng(out_y, (size_t)M * N * (out_dtype == MT_F32 ? 4 : 2));
+  if (overlap(ro, rng(x, (size_t)M * K * 2)) || overlap(ro, rng(W, wb)) ||
+      (bias && overlap(ro, rng(bias, (size_t)N * 2))) ||
+      (sbb && (overlap(ro, rng(scales, sbb)) || overlap(ro, rng(biases, sbb)))))
+    return MT_ERR_ALIAS;
+  GemvProblem p = {};
+  p.kind = Kind::Down;
+  p.fmt = fmt;
+  p.M = M; p.K = K; p.N = N;
+  p.group = fmt == MT_W_BF16 ? 0 : group;
+  p.x = (const uint16_t*)x;
+  p.W0 = W; p.W1 = nullptr;
+  p.s0 = (const uint16_t*)scales;
+  p.b0 = (const uint16_t*)biases;
+  p.res = (const uint16_t*)bias;  // nullable; one row broadcast over M
+  p.res_ld = 0;
   p.out = out_y;
   p.out_f32 = out_dtype == MT_F32;
   return launch_gemv(p, make_launch(stream));

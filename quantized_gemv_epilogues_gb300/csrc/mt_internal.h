@@ -60,6 +60,8 @@ mt_status launch_add_rmsnorm(const uint16_t* v, const uint16_t* r, const uint16_
                              const Launch& l);
 
 // ---- K2 / K3: affine or bf16 GEMV with an epilogue
+// GateUp: silu(x.Wg) * (x.Wu).  Down: x.W plus an optional addend (the residual
+// of the down projection, or the bias of an attention or vocabulary projection).
 enum class Kind { GateUp = 0, Down = 1 };
 
 struct GemvProblem {
@@ -74,7 +76,8 @@ struct GemvProblem {
   const uint16_t* b0;
   const uint16_t* s1;
   const uint16_t* b1;
-  const uint16_t* res;  // Down: residual [M][N]
+  const uint16_t* res;  // Down: residual [M][N], or a bias [N] (res_ld 0), or nullptr
+  int res_ld;           // elements between rows of res: N for a residual, 0 for a bias
   void* out;
   bool out_f32;
 };

@@ -31,6 +31,8 @@ _dev = None
 
 # tensor ids inside one layer's seed space
 T_VALUES, T_RESIDUAL, T_NORM_W, T_WG, T_WU, T_WD, T_X, T_H, T_RES3 = range(9)
+# projections: stacked q/k/v weight and bias, o weight, vocabulary weight
+T_WQKV, T_BQKV, T_WO, T_WVOCAB = range(9, 13)
 
 OUTLIER_P32_1PCT = 42949673  # round(0.01 * 2**32)
 
@@ -108,6 +110,7 @@ class Dist:
 
 
 ACT = Dist(0.0, 1.0)
+PROJ_BIAS = Dist(0.0, 0.5)
 NORM_W = Dist(1.0, 0.1)
 WEIGHT = Dist(0.0, 0.02)
 WEIGHT_OUTLIERS = Dist(0.0, 0.02, OUTLIER_P32_1PCT, 20.0)
@@ -209,3 +212,70 @@ def sweep_point(group: int, M: int) -> Workload:
 
 SWEEP = [sweep_point(g, m) for g in (32, 64, 128) for m in (1, 2, 4, 8)]
 ALL = [TINY, LLAMA1B, QWEN15, QWEN8B] + SWEEP
+
+
+# ---------------------------------------------------------------------------
+# Projection workloads: the attention projections of a decode step (q, k and v
+# stacked into one weight, as they share the activation, then o) and the
+# vocabulary projection, with the shapes of the models named.
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class Projection:
+    name: str
+    tensor: int                 # seed-space id of the weight
+    K: int
+    N: int
+    bias: Optional[int] = None  # seed-space id of the bias, None without one
+    per_layer: bool = True      # False: once per step (the vocabulary projection)
+
+
+@dataclass(frozen=True)
+class ProjWorkload:
+    wid: int
+    name: str
+    M: int
+    fmt: int
+    group: int
+    projs: tuple
+    layers: int = 1
+    weight_dist: Dist = WEIGHT
+
+    @property
+    def bits(self) -> int:
+        return {FMT_BF16: 16, FMT_AFFINE8: 8, FMT_AFFINE4: 4}[self.fmt]
+
+    def proj_weight_bytes(self, p: Projection) -> int:
+        wb = p.N * p.K * self.bits // 8
+        sb = 0 if self.fmt == FMT_BF16 else 2 * 2 * p.N * (p.K // self.group)
+        return wb + sb + (2 * p.N if p.bias is not None else 0)
+
+    def proj_act_bytes(self, p: Projection) -> int:
+        """x read (M*K bf16) and y written (M*N bf16)."""
+        return 2 * self.M * (p.K + p.N)
+
+    def step_bytes(self) -> int:
+        """Bytes one decode step's projections must move: per-layer projections
+        once per layer, the vocabulary projection once."""
+        tot = 0
+        for p in self.projs:
+            n = self.layers if p.per_layer else 1
+            tot += n * (self.proj_weight_bytes(p) + self.proj_act_bytes(p))
+        return tot
+
+
+QWEN8B_PROJ = ProjWorkload(
+    8, "qwen3-8b projections qkv 4096x6144 + o 4096x4096 x36, lm_head 4096x151936 affine8 g128",
+    1, FMT_AFFINE8, 128,
+    (Projection("qkv", T_WQKV, 4096, 6144), Projection("o", T_WO, 4096, 4096),
+     Projection("lm_head", T_WVOCAB, 4096, 151936, per_layer=False)), layers=36)
+QWEN15_PROJ = ProjWorkload(
+    9, "qwen2.5-1.5b projections qkv+bias 1536x2048 + o 1536x1536, tied vocab 1536x151936 bf16",
+    1, FMT_BF16, 0,
+    (Projection("qkv", T_WQKV, 1536, 2048, bias=T_BQKV), Projection("o", T_WO, 1536, 1536),
+     Projection("vocab", T_WVOCAB, 1536, 151936, per_layer=False)), layers=28)
+LLAMA1B_PROJ = ProjWorkload(
+    10, "llama3.2-1b projections qkv 2048x3072 + o 2048x2048, tied vocab 2048x128256 affine4 g64",
+    1, FMT_AFFINE4, 64,
+    (Projection("qkv", T_WQKV, 2048, 3072), Projection("o", T_WO, 2048, 2048),
+     Projection("vocab", T_WVOCAB, 2048, 128256, per_layer=False)), layers=16)
+PROJ_ALL = [QWEN8B_PROJ, QWEN15_PROJ, LLAMA1B_PROJ]

@@ -87,3 +87,53 @@ def plan_layer(L):
     """The layer as an ``mt_mlp_layer`` mapping for mt_mlp_plan_create."""
     return dict(norm_weight=L.w, Wg=L.Wg, Wu=L.Wu, gu_scales=L.sgu, gu_biases=L.bgu, Wd=L.Wd,
                 d_scales=L.sdn, d_biases=L.bdn)
+
+
+class DevProj:
+    """One projection's weight (and bias) generated on the device and packed by
+    the library, with oracle-side rows regenerated on the host."""
+
+    def __init__(self, mt, wl, p, layer=0):
+        self.wl, self.p, self.l = wl, p, layer
+        sd = lambda t: synth.seed_for(wl.wid, layer, t)
+        self.sd = sd
+        N, K, g = p.N, p.K, wl.group
+        bf = torch.bfloat16
+        if wl.fmt == synth.FMT_BF16:
+            self.W = torch.empty(N, K, dtype=bf, device="cuda")
+            synth.device_bf16(self.W, sd(p.tensor), wl.weight_dist)
+            self.s = self.b = None
+        else:
+            self.W = torch.empty(N, K * wl.bits // 8, dtype=torch.uint8, device="cuda")
+            self.s = torch.empty(N, K // g, dtype=bf, device="cuda")
+            self.b = torch.empty_like(self.s)
+            tmp = torch.empty(N, K, dtype=torch.float32, device="cuda")
+            synth.device_f32(tmp, sd(p.tensor), wl.weight_dist)
+            mt.mt_pack_affine(tmp, N, K, g, wl.bits, self.W, self.s, self.b)
+            del tmp
+        self.bias = None
+        if p.bias is not None:
+            self.bias = torch.empty(N, dtype=bf, device="cuda")
+            synth.device_bf16(self.bias, sd(p.bias), synth.PROJ_BIAS)
+        torch.cuda.synchronize()
+
+    def run(self, mt, x, out):
+        mt.mt_linear_bias(x, self.W, self.s, self.b, self.wl.group, self.bias, out, fmt=self.wl.fmt)
+
+    def oracle_rows(self, rows):
+        """Oracle-side weight rows and bias entries for output columns `rows`."""
+        wl, p = self.wl, self.p
+        K = p.K
+        if wl.fmt == synth.FMT_BF16:
+            W = np.stack([synth.host_bf16(K, self.sd(p.tensor), wl.weight_dist, offset=int(n) * K)
+                          for n in rows])
+            Wo = oracle.Weight(oracle.FMT_BF16, W)
+        else:
+            W32 = np.stack([synth.host_f32(K, self.sd(p.tensor), wl.weight_dist, offset=int(n) * K)
+                            for n in rows])
+            Wo = oracle.Weight.from_f32(W32, wl.bits, wl.group)
+        bias = None
+        if p.bias is not None:
+            full = synth.host_bf16(p.N, self.sd(p.bias), synth.PROJ_BIAS)
+            bias = full[np.asarray(list(rows), dtype=np.int64)]
+        return Wo, bias

@@ -33,7 +33,8 @@ def declared_functions():
 
 def test_header_declares_the_hot_path_calls():
     names = declared_functions()
-    for n in ("mt_add_rmsnorm", "mt_swiglu_gateup", "mt_down_residual", "mt_pack_affine"):
+    for n in ("mt_add_rmsnorm", "mt_swiglu_gateup", "mt_down_residual", "mt_linear_bias",
+              "mt_pack_affine"):
         assert n in names
 
 
@@ -74,6 +75,13 @@ def _gu(lib, *a):
 
 def _dn(lib, *a):
     f = lib.mt_down_residual
+    f.restype = ctypes.c_int
+    f.argtypes = [P, P, P, P, ctypes.c_int, P, P] + [ctypes.c_int] * 5 + [P]
+    return f(*a)
+
+
+def _lb(lib, *a):
+    f = lib.mt_linear_bias
     f.restype = ctypes.c_int
     f.argtypes = [P, P, P, P, ctypes.c_int, P, P] + [ctypes.c_int] * 5 + [P]
     return f(*a)
@@ -142,6 +150,32 @@ def test_down_residual_validation(lib):
     assert call(y=h) == ALIAS
     assert call(y=res + 16) == ALIAS          # partial overlap with the residual
     assert call(y=res, od=1) == ALIAS         # in place only with the same element size
+
+
+def test_linear_bias_validation(lib):
+    x, w, sc, bi, bias, y = A[:6]
+
+    def call(x=x, w=w, sc=sc, bi=bi, g=64, bias=bias, y=y, M=1, K=1536, N=2048, fmt=2, od=0):
+        return _lb(lib, x, w, sc, bi, g, bias, y, M, K, N, fmt, od, None)
+
+    assert call(x=None) == NULL
+    assert call(w=None) == NULL
+    assert call(bi=None) == NULL
+    assert call(g=96) == GROUP
+    assert call(fmt=0, g=64, sc=None, bi=None) == GROUP      # bf16 takes group 0
+    assert call(K=1000) == SHAPE                             # 1000 % 64 != 0
+    assert call(K=32832) == SHAPE                            # above 32768
+    assert call(N=0) == SHAPE
+    assert call(N=(1 << 20) + 1) == SHAPE
+    assert call(M=9) == SHAPE
+    assert call(fmt=3) == FORMAT
+    assert call(od=5) == FORMAT
+    assert call(bias=bias + 2) == ALIGN
+    assert call(y=y + 8) == ALIGN
+    assert call(y=x) == ALIAS
+    assert call(y=w + 64) == ALIAS
+    assert call(y=bias) == ALIAS
+    assert call(y=bi + 32) == ALIAS
 
 
 def test_pack_validation(lib):

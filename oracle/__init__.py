@@ -23,6 +23,12 @@ What each function follows (meTile docs unless stated):
 * :func:`down_residual` -- values @ weight.T + residual, the down projection
   with the residual added in its epilogue ("Compute-Graph Fusion", Automatic
   Gated Epilogues; "MLX-LM Backend", Dispatch Policy).
+* :func:`quantize_mx`, :func:`e4m3_value`, :func:`e2m1_value`,
+  :meth:`Weight.from_f32_mx` -- MXFP8 / MXFP4 block-scaled weights: E4M3 or
+  E2M1 elements with one E8M0 scale per 32 elements along K ("MLX-LM
+  Backend", Block-Scaled MLX Primitive; encodings and block size as in the
+  OCP Microscaling Formats (MX) v1.0 specification named by the format).
+  Every GEMV above accepts them.
 * :func:`linear_bias` -- values @ weight.T + bias for the attention
   projections (q/k/v/o, bias kept) and the vocabulary projection, which run
   the same one-row GEMV ("MLX-LM Backend", the attention-projection and
@@ -50,6 +56,9 @@ _lib = None
 
 FMT_BF16 = 0     # dense bf16 weights [N][K]
 FMT_CODES = 1    # affine codes [N][K], one code per byte, + scales/biases
+FMT_MXFP8 = 2    # E4M3 codes [N][K], one per byte, + E8M0 scales [N][K/32]
+FMT_MXFP4 = 3    # E2M1 codes [N][K], one per byte, + E8M0 scales [N][K/32]
+MX_BLOCK = 32
 
 
 def build(force: bool = False) -> str:
@@ -82,6 +91,11 @@ def _L():
                 "orc_swiglu_gateup": (I, [P, L, L, L, I, P, P, P, P, P, P, I, P, P, P]),
                 "orc_down_residual": (I, [P, L, L, L, I, P, P, P, I, P, P]),
                 "orc_linear_bias": (I, [P, L, L, L, I, P, P, P, I, P, P]),
+                "orc_e4m3_value": (D, [ctypes.c_uint8]),
+                "orc_e2m1_value": (D, [ctypes.c_uint8]),
+                "orc_e4m3_from_f64": (ctypes.c_uint8, [D]),
+                "orc_e2m1_from_f64": (ctypes.c_uint8, [D]),
+                "orc_quantize_mx": (I, [P, L, L, I, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -150,6 +164,45 @@ def pack_codes(codes, bits: int) -> np.ndarray:
     return out
 
 
+def e4m3_value(code: int) -> float:
+    """Value of an OCP FP8 E4M3 code (NaN for S.1111.111)."""
+    return _L().orc_e4m3_value(int(code))
+
+
+def e2m1_value(code: int) -> float:
+    """Value of an OCP FP4 E2M1 code (low four bits)."""
+    return _L().orc_e2m1_value(int(code))
+
+
+def e4m3_from_f64(v: float) -> int:
+    """Nearest E4M3 code (ties to even, saturating at 448, sign kept)."""
+    return int(_L().orc_e4m3_from_f64(float(v)))
+
+
+def e2m1_from_f64(v: float) -> int:
+    """Nearest E2M1 code (ties to even, saturating at 6, sign kept)."""
+    return int(_L().orc_e2m1_from_f64(float(v)))
+
+
+def quantize_mx(W, bits: int):
+    """MX quantisation of fp32 W [N, K] along K in blocks of 32: bits 8 =
+    MXFP8 (E4M3), bits 4 = MXFP4 (E2M1).  Returns (codes uint8 [N, K] one code
+    per byte, scales uint8 [N, K/32] E8M0 fields)."""
+    W = _c(W, np.float32)
+    N, K = W.shape
+    codes = np.empty((N, K), dtype=np.uint8)
+    s = np.empty((N, K // MX_BLOCK), dtype=np.uint8)
+    if _L().orc_quantize_mx(W.ctypes.data, N, K, bits, codes.ctypes.data, s.ctypes.data):
+        raise ValueError("orc_quantize_mx: bad arguments")
+    return codes, s
+
+
+def dequant_mx(codes, scales, bits: int) -> np.ndarray:
+    """Exact values of MX weights [N, K]: element value * 2^(E - 127)."""
+    W = Weight(FMT_MXFP8 if bits == 8 else FMT_MXFP4, codes, scales, None, MX_BLOCK)
+    return W.dense()
+
+
 def dequant(codes, scales, biases, group: int) -> np.ndarray:
     codes = _c(codes, np.uint8)
     N, K = codes.shape
@@ -183,9 +236,10 @@ class Weight:
     def __init__(self, fmt, W, scales=None, biases=None, group=0):
         self.fmt = fmt
         self.W = _c(W, np.uint16 if fmt == FMT_BF16 else np.uint8)
-        self.scales = None if scales is None else _c(scales, np.uint16)
-        self.biases = None if biases is None else _c(biases, np.uint16)
-        self.group = int(group)
+        mx = fmt in (FMT_MXFP8, FMT_MXFP4)
+        self.scales = None if scales is None else _c(scales, np.uint8 if mx else np.uint16)
+        self.biases = None if (biases is None or mx) else _c(biases, np.uint16)
+        self.group = MX_BLOCK if mx else int(group)
 
     @property
     def shape(self):
@@ -200,9 +254,22 @@ class Weight:
         codes, s, b = quantize(W32, group, fmt_bits)
         return cls(FMT_CODES, codes, s, b, group)
 
+    @classmethod
+    def from_f32_mx(cls, W32, bits: int):
+        """MX-quantise fp32 weights with the oracle's own quantiser (bits 8:
+        MXFP8, bits 4: MXFP4)."""
+        codes, s = quantize_mx(W32, bits)
+        return cls(FMT_MXFP8 if bits == 8 else FMT_MXFP4, codes, s, None, MX_BLOCK)
+
     def dense(self) -> np.ndarray:
         if self.fmt == FMT_BF16:
             return f64_from_bf16(self.W)
+        if self.fmt in (FMT_MXFP8, FMT_MXFP4):
+            val = e4m3_value if self.fmt == FMT_MXFP8 else e2m1_value
+            table = np.array([val(c) for c in range(256 if self.fmt == FMT_MXFP8 else 16)])
+            codes = self.W if self.fmt == FMT_MXFP8 else (self.W & 0xF)
+            scale = np.ldexp(1.0, self.scales.astype(np.int64) - 127)
+            return table[codes] * np.repeat(scale, MX_BLOCK, axis=1)
         return dequant(self.W, self.scales, self.biases, self.group)
 
 

@@ -22,6 +22,10 @@
  *    the vocabulary projection (a tied embedding used as a linear map, or an
  *    untied lm_head) run the same one-row GEMV, and the projection bias is
  *    kept: y = x @ weight.T + bias.
+ *  - "MLX-LM Backend", Block-Scaled MLX Primitive: MXFP8 and MXFP4 weights,
+ *    E4M3 or E2M1 element values with E8M0 block scales.  The element and
+ *    scale encodings and the block size of 32 follow the OCP Microscaling
+ *    Formats (MX) v1.0 specification, which the page's format names refer to.
  *  - ANEForge docs, "The optimizer and the cost model", The roofline: a weight
  *    is stored [N, K] (K contiguous) and x[.., K] @ W[N, K]^T gives [.., N].
  *
@@ -41,6 +45,13 @@
  *  - down: y = sum_k h_k * W[n,k] + residual_n, rounded once.
  *  - projection: y = sum_k x_k * W[n,k] + bias_n (bias bf16, absent = 0),
  *    rounded once.
+ *  - MX quantiser (per block of 32 consecutive elements along K): the shared
+ *    scale is 2^(floor(log2(amax)) - emax) with emax the element format's
+ *    largest exponent (8 for E4M3, 2 for E2M1), its E8M0 field clamped to
+ *    [0, 254] (an all-zero block takes field 0); each element is w / scale
+ *    rounded to nearest-even in the element format, magnitudes above the
+ *    largest finite value clamped to it, the sign kept (so a negative value
+ *    that rounds to zero gives the negative-zero code).
  */
 #include <math.h>
 #include <stddef.h>
@@ -192,11 +203,22 @@ int orc_dequant(const uint8_t* codes, const uint16_t* scales, const uint16_t* bi
 
 /* ------------------------------------------------------ weight operand */
 
+double orc_e4m3_value(uint8_t c);
+double orc_e2m1_value(uint8_t c);
+
 /* fmt 0: dense bf16 weights [N][K]; fmt 1: affine codes [N][K] (one code per
- * byte, any bit width) with bf16 scales/biases [N][K/group]. */
+ * byte, any bit width) with bf16 scales/biases [N][K/group]; fmt 2 / 3: MX
+ * element codes [N][K] (one E4M3 / E2M1 code per byte) with E8M0 scales
+ * [N][K/32] (passed as bytes through s; b unused). */
 static double orc_weight(int fmt, const void* W, const uint16_t* s, const uint16_t* b,
                          long K, int group, long n, long k) {
   if (fmt == 0) return orc_f64_from_bf16(((const uint16_t*)W)[n * K + k]);
+  if (fmt == 2 || fmt == 3) {
+    const uint8_t c = ((const uint8_t*)W)[n * K + k];
+    const uint8_t e = ((const uint8_t*)s)[n * (K / 32) + k / 32];
+    const double v = fmt == 2 ? orc_e4m3_value(c) : orc_e2m1_value(c);
+    return v * ldexp(1.0, (int)e - 127);
+  }
   const long G = K / group;
   double sc = orc_f64_from_bf16(s[n * G + k / group]);
   double bi = orc_f64_from_bf16(b[n * G + k / group]);
@@ -205,6 +227,7 @@ static double orc_weight(int fmt, const void* W, const uint16_t* s, const uint16
 
 static int orc_check_fmt(int fmt, long K, int group) {
   if (fmt == 0) return 0;
+  if (fmt == 2 || fmt == 3) return (group == 32 && K % 32 == 0) ? 0 : -1;
   if (fmt != 1 || group <= 0 || K % group != 0) return -1;
   return 0;
 }
@@ -297,6 +320,97 @@ int orc_linear_bias(const uint16_t* x, long M, long K, long N, int fmt,
       for (long k = 0; k < K; ++k)
         acc += orc_f64_from_bf16(x[m * K + k]) * orc_weight(fmt, W, s, b, K, group, n, k);
       y[m * N + n] = bias ? acc + orc_f64_from_bf16(bias[n]) : acc;
+    }
+  return 0;
+}
+
+/* ------------------------------------------------------ MX block scaling */
+
+/* Value of an OCP FP8 E4M3 code: sign, 4 exponent bits (bias 7), 3 fraction
+ * bits; exponent field 0 is subnormal (f * 2^-9); S.1111.111 is NaN and there
+ * are no infinities. */
+double orc_e4m3_value(uint8_t c) {
+  const int s = c >> 7, e = (c >> 3) & 15, f = c & 7;
+  double v;
+  if (e == 15 && f == 7)
+    v = NAN;
+  else if (e == 0)
+    v = ldexp((double)f, -9);
+  else
+    v = ldexp(8.0 + (double)f, e - 7 - 3);
+  return s ? -v : v;
+}
+
+/* Value of an OCP FP4 E2M1 code: sign, 2 exponent bits (bias 1), 1 fraction
+ * bit; exponent field 0 is subnormal (f * 0.5). */
+double orc_e2m1_value(uint8_t c) {
+  const int s = (c >> 3) & 1, e = (c >> 1) & 3, f = c & 1;
+  const double v = e == 0 ? 0.5 * (double)f : ldexp(2.0 + (double)f, e - 1 - 1);
+  return s ? -v : v;
+}
+
+/*
+ * Nearest code of a minifloat format with `mbits` fraction bits, exponent
+ * bias `bias`, largest finite magnitude `maxv` and the code of that magnitude
+ * `maxcode`, ties to even, magnitudes above maxv clamped to it, sign kept.
+ * Same scaling method as orc_bf16_from_f64: the value divided by the format's
+ * spacing at its exponent is rounded to an integer, then encoded.
+ */
+static uint8_t orc_minifloat(double v, int mbits, int ebits, int bias, double maxv, uint8_t maxcode) {
+  const uint8_t sign = (uint8_t)(signbit(v) ? 1u << (mbits + ebits) : 0u);
+  double a = fabs(v);
+  if (a >= maxv) return (uint8_t)(sign | maxcode);
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e);
+  int eu = e - 1;                            /* a in [2^eu, 2^(eu+1)) */
+  if (eu < 1 - bias) eu = 1 - bias;          /* subnormal spacing */
+  const double ulp = ldexp(1.0, eu - mbits);
+  const double q = nearbyint(a / ulp);       /* exact division; ties to even */
+  double r = q * ulp;
+  if (r > maxv) r = maxv;                    /* cannot happen below maxv; kept for clarity */
+  if (r < ldexp(1.0, 1 - bias)) {            /* subnormal (or zero): fraction = r / 2^(1-bias-mbits) */
+    return (uint8_t)(sign | (uint8_t)ldexp(r, bias - 1 + mbits));
+  }
+  int e2;
+  const double m2 = frexp(r, &e2);           /* r = m2 2^e2, m2 in [0.5, 1) */
+  const int be = e2 - 1 + bias;
+  const uint8_t frac = (uint8_t)(ldexp(m2, mbits + 1) - ldexp(1.0, mbits));
+  return (uint8_t)(sign | (uint8_t)(be << mbits) | frac);
+}
+
+uint8_t orc_e4m3_from_f64(double v) { return orc_minifloat(v, 3, 4, 7, 448.0, 0x7E); }
+uint8_t orc_e2m1_from_f64(double v) { return orc_minifloat(v, 1, 2, 1, 6.0, 0x7); }
+
+/*
+ * MX quantisation of W [N][K] (fp32) along K in blocks of 32: bits 8 gives
+ * MXFP8 (E4M3 elements), bits 4 MXFP4 (E2M1).  codes [N][K] (one code per
+ * byte), scales [N][K/32] as E8M0 fields.  Returns 0, or -1 on bad arguments.
+ */
+int orc_quantize_mx(const float* W, long N, long K, int bits, uint8_t* codes, uint8_t* scales) {
+  if (K % 32 != 0 || (bits != 8 && bits != 4)) return -1;
+  const int emax = bits == 8 ? 8 : 2;
+  const long B = K / 32;
+  for (long n = 0; n < N; ++n)
+    for (long bi = 0; bi < B; ++bi) {
+      const float* w = W + n * K + bi * 32;
+      double amax = 0.0;
+      for (int k = 0; k < 32; ++k)
+        if (fabs((double)w[k]) > amax) amax = fabs((double)w[k]);
+      int E = 0;
+      if (amax > 0.0) {
+        int e;
+        frexp(amax, &e);                     /* floor(log2(amax)) = e - 1 */
+        E = (e - 1) - emax + 127;
+        if (E < 0) E = 0;
+        if (E > 254) E = 254;
+      }
+      scales[n * B + bi] = (uint8_t)E;
+      const double X = ldexp(1.0, E - 127);
+      for (int k = 0; k < 32; ++k) {
+        const double v = (double)w[k] / X;   /* exact: X is a power of two */
+        codes[n * K + bi * 32 + k] = bits == 8 ? orc_e4m3_from_f64(v) : orc_e2m1_from_f64(v);
+      }
     }
   return 0;
 }

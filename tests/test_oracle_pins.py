@@ -479,6 +479,146 @@ def test_linear_bias_tied_embedding_reading():
         assert np.array_equal(oracle.linear_bias(x, E)[0], Ed[:, j])
 
 
+# ------------------------------------------------------------- MX formats
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # OCP MX v1.0, FP4 E2M1 values of codes 0..7
+
+
+def _read_mx_cases():
+    rows = []
+    with open(os.path.join(GOLD, "mx_cases.txt")) as fh:
+        for line in fh:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            kind, v, code = line.split()[:3]
+            rows.append((kind, float.fromhex(v), int(code, 16)))
+    return rows
+
+
+@pytest.mark.parametrize("kind,v,expect", _read_mx_cases())
+def test_mx_textbook_cases(kind, v, expect):
+    if kind == "e4m3":
+        assert oracle.e4m3_from_f64(v) == expect
+    elif kind == "e2m1":
+        assert oracle.e2m1_from_f64(v) == expect
+    else:
+        bits = 8 if kind == "scale8" else 4
+        W = np.zeros((1, 64), np.float32)
+        W[0, 5] = np.float32(v)          # block 0 holds the maximum
+        W[0, 40] = np.float32(-v) * 0.5  # block 1: half of it, negative
+        codes, s = oracle.quantize_mx(W, bits)
+        assert int(s[0, 0]) == expect
+        if v > 0:
+            # the second block's maximum is half: one field lower, unless clamped
+            assert int(s[0, 1]) == max(0, expect - 1) or expect == 0
+
+
+def test_e4m3_decode_matches_library_all_codes():
+    lib = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = np.array([oracle.e4m3_value(c) for c in range(256)])
+    assert np.array_equal(np.isnan(ours), np.isnan(lib))
+    ok = ~np.isnan(lib)
+    assert np.array_equal(ours[ok], lib[ok])
+    assert np.array_equal(np.signbit(ours[ok]), np.signbit(lib[ok]))
+
+
+def test_e2m1_decode_table():
+    for c in range(16):
+        mag = E2M1_TABLE[c & 7]
+        v = oracle.e2m1_value(c)
+        assert abs(v) == mag and (math.copysign(1.0, v) < 0) == bool(c & 8)
+
+
+def test_e4m3_encode_matches_library_in_range():
+    rng = np.random.default_rng(11)
+    vals = np.concatenate([
+        rng.uniform(-448, 448, 4000),
+        rng.normal(0, 1, 4000) * 2.0 ** rng.integers(-12, 8, 4000),
+        # every midpoint between neighbouring finite codes (ties)
+        [(oracle.e4m3_value(c) + oracle.e4m3_value(c + 1)) / 2 for c in range(0, 126)],
+    ]).astype(np.float32)
+    lib = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ours = np.array([oracle.e4m3_from_f64(float(v)) for v in vals], dtype=np.uint8)
+    assert np.array_equal(ours, lib)
+
+
+def test_e2m1_encode_brute_force():
+    rng = np.random.default_rng(12)
+    vals = list(rng.uniform(-7, 7, 3000)) + [m / 4 for m in range(-28, 29)]
+    for v in vals:
+        c = oracle.e2m1_from_f64(v)
+        a = min(abs(v), 6.0)
+        dist = [abs(a - t) for t in E2M1_TABLE]
+        best = min(dist)
+        cands = [i for i, dd in enumerate(dist) if dd == best]
+        want = cands[0] if len(cands) == 1 else [i for i in cands if i % 2 == 0][0]
+        assert c & 7 == want, (v, c)
+        assert bool(c & 8) == (math.copysign(1.0, v) < 0)
+
+
+def test_quantize_mx_round_trip_and_bound():
+    rng = np.random.default_rng(13)
+    # blocks whose values are all representable at scale 2^(E-127): exact
+    for bits, table in ((8, [oracle.e4m3_value(c) for c in range(0x7F)]), (4, E2M1_TABLE)):
+        E = 120
+        vals = np.array(table)[rng.integers(0, len(table), size=(4, 64))] * rng.choice([-1, 1], (4, 64))
+        vals[:, 0] = table[-1]  # each block's maximum is the largest finite element
+        vals[:, 32] = table[-1]
+        W = (vals * 2.0 ** (E - 127)).astype(np.float32)
+        codes, s = oracle.quantize_mx(W, bits)
+        emax = 8 if bits == 8 else 2
+        assert np.all(s == int(math.floor(math.log2(table[-1]))) - emax + 127 + (E - 127))
+        assert np.array_equal(oracle.dequant_mx(codes, s, bits), W.astype(np.float64))
+    # random blocks: error within half a spacing of the element format at the
+    # scaled value, or the clamp of values above the largest finite element
+    W = synth.host_f32(8 * 256, 14, synth.WEIGHT_OUTLIERS).reshape(8, 256)
+    for bits, mbits, lo_exp, maxv in ((8, 3, -6, 448.0), (4, 1, 0, 6.0)):
+        codes, s = oracle.quantize_mx(W, bits)
+        X = np.repeat(np.ldexp(1.0, s.astype(np.int64) - 127), 32, axis=1)
+        v = W.astype(np.float64) / X
+        back = oracle.dequant_mx(codes, s, bits) / X
+        a = np.minimum(np.abs(v), maxv)
+        e = np.floor(np.log2(np.maximum(a, 2.0 ** lo_exp)))
+        half = np.ldexp(0.5, (e - mbits).astype(int))
+        assert np.all(np.abs(np.sign(v) * a - back) <= half)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_mx_gemvs_brute_force(bits):
+    M, K, N = 2, 96, 5
+    x = gen_bf16(M * K, 141).reshape(M, K)
+    W32 = synth.host_f32(N * K, 142, synth.WEIGHT).reshape(N, K)
+    W = oracle.Weight.from_f32_mx(W32, bits)
+    # exact weight values from the library decode (E4M3) or the E2M1 table
+    if bits == 8:
+        dec = torch.from_numpy(W.W).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    else:
+        dec = np.array([[math.copysign(E2M1_TABLE[c & 7], -1.0 if c & 8 else 1.0) for c in row]
+                        for row in W.W])
+    D = [[Fraction(float(dec[n, k])) * Fraction(2) ** (int(W.scales[n, k // 32]) - 127) for k in range(K)]
+         for n in range(N)]
+    xf = [[Fraction(float(t)) for t in row] for row in torch_f64_from_bf16(x)]
+    bias = gen_bf16(N, 143)
+    y = oracle.linear_bias(x, W, bias)
+    res = gen_bf16(M * N, 144).reshape(M, N)
+    yd = oracle.down_residual(x, W, res)
+    for m in range(M):
+        for n in range(N):
+            dot = sum(a * b for a, b in zip(xf[m], D[n]))
+            scale = float(sum(abs(a * b) for a, b in zip(xf[m], D[n])))
+            exact = dot + Fraction(float(torch_f64_from_bf16(bias[n:n + 1])[0]))
+            assert abs(y[m, n] - float(exact)) <= 1e-14 * (scale + 1)
+            exact_d = dot + Fraction(float(torch_f64_from_bf16(res[m, n:n + 1])[0]))
+            assert abs(yd[m, n] - float(exact_d)) <= 1e-14 * (scale + 1)
+    # gate/up with two MX matrices
+    W2 = oracle.Weight.from_f32_mx(synth.host_f32(N * K, 145, synth.WEIGHT).reshape(N, K), bits)
+    h, g, u = oracle.swiglu_gateup(x, W, W2, return_gu=True)
+    for m in range(M):
+        for n in range(N):
+            ge = float(sum(a * b for a, b in zip(xf[m], D[n])))
+            assert abs(g[m, n] - ge) <= 1e-14 * (abs(ge) + float(sum(abs(a * b) for a, b in zip(xf[m], D[n]))))
+
+
 # ----------------------------------------------------------- composition
 def test_mlp_layer_and_stack_composition():
     d, f, M, g = 64, 96, 2, 32

@@ -178,19 +178,24 @@ class Stack:
                 sgu = bgu = sdn = bdn = None
             else:
                 bits = wl.bits
+                mx = synth.is_mx(wl.fmt)
+                sdt = torch.uint8 if mx else bf
                 Wg = torch.empty(f, d * bits // 8, dtype=torch.uint8, device=device)
                 Wu = torch.empty_like(Wg)
                 Wd = torch.empty(d, f * bits // 8, dtype=torch.uint8, device=device)
-                sgu = torch.empty(2, f, d // g, dtype=bf, device=device)
-                bgu = torch.empty_like(sgu)
-                sdn = torch.empty(d, f // g, dtype=bf, device=device)
-                bdn = torch.empty_like(sdn)
-                for (dst, s_, b_, N, K, t) in ((Wg, sgu[0], bgu[0], f, d, synth.T_WG),
-                                               (Wu, sgu[1], bgu[1], f, d, synth.T_WU),
+                sgu = torch.empty(2, f, d // g, dtype=sdt, device=device)
+                sdn = torch.empty(d, f // g, dtype=sdt, device=device)
+                bgu = None if mx else torch.empty_like(sgu)
+                bdn = None if mx else torch.empty_like(sdn)
+                for (dst, s_, b_, N, K, t) in ((Wg, sgu[0], None if mx else bgu[0], f, d, synth.T_WG),
+                                               (Wu, sgu[1], None if mx else bgu[1], f, d, synth.T_WU),
                                                (Wd, sdn, bdn, d, f, synth.T_WD)):
                     W32 = tmp[:N * K].view(N, K)
                     synth.device_f32(W32, sd(t), wl.weight_dist)
-                    mt.mt_pack_affine(W32, N, K, g, bits, dst, s_, b_)
+                    if mx:
+                        mt.mt_pack_mx(W32, N, K, bits, dst, s_)
+                    else:
+                        mt.mt_pack_affine(W32, N, K, g, bits, dst, s_, b_)
             values = self.values[l]
             synth.device_bf16(values, sd(synth.T_VALUES), synth.ACT)
             self.layers.append(dict(w=w_norm, Wg=Wg, Wu=Wu, Wd=Wd, sgu=sgu, bgu=bgu, sd=sdn,
@@ -203,7 +208,7 @@ class Stack:
         self.h = torch.empty(M, wl.f, dtype=bf, device=device)
         self.out_y = torch.empty(M, d, dtype=bf, device=device)
         self.plan = None
-        if M == 1:
+        if M == 1 and not synth.is_mx(wl.fmt):
             self.plan = mt.mt_mlp_plan_create(
                 [dict(norm_weight=L["w"], Wg=L["Wg"], Wu=L["Wu"], gu_scales=L["sgu"],
                       gu_biases=L["bgu"], Wd=L["Wd"], d_scales=L["sd"], d_biases=L["bd"])
@@ -263,15 +268,17 @@ class Stack:
             mt.mt_add_rmsnorm(L["values"], self.resid, L["w"], wl.eps, self.resid, self.norm)
 
     def down_bytes(self):
+        import synth
         wl = self.wl
         n = wl.f * wl.d
-        w = n * wl.bits // 8 + (0 if wl.fmt == 0 else 4 * n // wl.group)
+        w = n * wl.bits // 8 + synth.scale_bytes(wl.fmt, n, wl.group)
         return w + 2 * wl.M * wl.f + 4 * wl.M * wl.d
 
     def gateup_bytes(self):
+        import synth
         wl = self.wl
         n = 2 * wl.f * wl.d
-        w = n * wl.bits // 8 + (0 if wl.fmt == 0 else 4 * n // wl.group)
+        w = n * wl.bits // 8 + synth.scale_bytes(wl.fmt, n, wl.group)
         return w + 2 * wl.M * wl.d + 2 * wl.M * wl.f
 
 
@@ -456,7 +463,7 @@ def measure_layer(wl, args, torch, mt, dev, reps=None):
                    "gateup_gbs" + tag: round(st.gateup_bytes() / (gu * 1e-6) / 1e9, 1),
                    "down_us" + tag: round(dn, 3),
                    "down_gbs" + tag: round(st.down_bytes() / (dn * 1e-6) / 1e9, 1)})
-    if wl.M == 1:
+    if wl.M == 1 and st.plan is not None:
         # executor: a plan of the same layer `reps` times (hot) and the stack
         # plan over the distinct copies (cold)
         lay = st.layers[0]
@@ -653,6 +660,35 @@ def run_projections(args, torch, synth, mt, dev):
     return 0
 
 
+def run_mx(args, torch, synth, mt, dev):
+    """The Qwen3-8B-shaped layer (d=4096, f=12288) with MX block-scaled
+    weights (MXFP8, MXFP4), M = 1 and 4: us per layer of the single calls and
+    of each GEMV, hot and cold (measure_layer).  The JSON line's value is the
+    geometric mean of the cold GB/s."""
+    import math
+    peak, peak_kind = measured_peaks()
+    points = []
+    for wl in (synth.QWEN8B_MXFP8, synth.QWEN8B_MXFP4):
+        for M in ((args.rows,) if args.rows else (1, 4)):
+            w = wl.with_(M=M)
+            pt = {"workload": w.name, "M": M}
+            pt.update(measure_layer(w, args, torch, mt, dev))
+            points.append(pt)
+    gm = math.exp(sum(math.log(p["gbs_cold"]) for p in points) / len(points))
+    line = {"metric": METRIC, "value": round(gm, 2), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8/mxfp4-weights/f32-acc",
+            "data": "synthetic",
+            "config": {"workload": "qwen3-8b layer d4096 f12288 with MXFP8 and MXFP4 weights (E8M0 "
+                                   "scales per 32), M 1 and 4, single calls",
+                       "l2": "value: cold (distinct layer copies > 2x L2 cycled); hot: one layer x "
+                             f"{SWEEP_REPS} in one graph"},
+            "peak": peak, "peak_kind": peak_kind, "points": points,
+            "device_error": mt.mt_device_error()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -660,7 +696,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mt", choices=["mt", "reference"])
     ap.add_argument("--workload", default="qwen3-8b",
-                    choices=["qwen3-8b", "tiny", "llama1b", "qwen15", "sweep", "configs", "projections"],
+                    choices=["qwen3-8b", "tiny", "llama1b", "qwen15", "sweep", "configs", "projections", "mx"],
                     help="sweep: every group x M point of the d=2048, f=8192 sweep, one line; "
                          "configs: the tiny, Llama-3.2-1B and Qwen2.5-1.5B layers hot and cold, one line; "
                          "projections: attention and vocabulary projections of a decode step per model")
@@ -707,6 +743,8 @@ def main():
         return run_configs(args, torch, synth, mt, dev)
     if args.workload == "projections":
         return run_projections(args, torch, synth, mt, dev)
+    if args.workload == "mx":
+        return run_mx(args, torch, synth, mt, dev)
     wl = {"qwen3-8b": synth.QWEN8B, "tiny": synth.TINY, "llama1b": synth.LLAMA1B,
           "qwen15": synth.QWEN15}[args.workload]
     if args.layers:

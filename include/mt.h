@@ -43,9 +43,18 @@
  *   MT_W_AFFINE4 : W is uint8 [N][K/2], byte j of a row holds code 2j in bits
  *                  0..3 and code 2j+1 in bits 4..7.
  *   Affine weights are w[n][k] = scale[n][k/group] * q[n][k] + bias[n][k/group]
- *   with bf16 scales and biases [N][K/group], row-major.  For
- *   mt_swiglu_gateup one scales array and one biases array hold two planes
- *   [2][f][d/group]: plane 0 belongs to Wg, plane 1 to Wu.
+ *   with bf16 scales and biases [N][K/group], row-major.
+ *   MT_W_MXFP8   : W is uint8 [N][K], one OCP FP8 E4M3 code per byte.
+ *   MT_W_MXFP4   : W is uint8 [N][K/2], OCP FP4 E2M1 codes, nibble order as
+ *                  MT_W_AFFINE4.
+ *   MX weights are w[n][k] = value(code[n][k]) * 2^(E[n][k/32] - 127) with
+ *   uint8 E8M0 scale fields E [N][K/32] passed as `scales`, `biases` NULL
+ *   and group 32 (meTile docs, "MLX-LM Backend", Block-Scaled MLX Primitive;
+ *   encodings of the OCP Microscaling Formats v1.0).  They run on the
+ *   tensor-core kernel for every M; the executor (mt_mlp_plan_*) does not
+ *   take them.
+ *   For mt_swiglu_gateup one scales array and one biases array hold two
+ *   planes [2][f][d/group]: plane 0 belongs to Wg, plane 1 to Wu.
  * - Pointers.  Every tensor pointer is a DEVICE pointer (cudaMalloc, or memory
  *   the device can address), 16-byte aligned.  The caller owns every buffer;
  *   the hot calls allocate nothing and never synchronise.
@@ -94,7 +103,8 @@ typedef enum mt_status {
 typedef enum mt_dtype { MT_BF16 = 0, MT_F32 = 1 } mt_dtype;
 
 /* Weight storage format. */
-typedef enum mt_wfmt { MT_W_BF16 = 0, MT_W_AFFINE8 = 1, MT_W_AFFINE4 = 2 } mt_wfmt;
+typedef enum mt_wfmt { MT_W_BF16 = 0, MT_W_AFFINE8 = 1, MT_W_AFFINE4 = 2,
+                       MT_W_MXFP8 = 3, MT_W_MXFP4 = 4 } mt_wfmt;
 
 /* Library options (mt_set_option / mt_get_option). */
 typedef enum mt_option {
@@ -131,12 +141,12 @@ mt_status mt_add_rmsnorm(const void* values, const void* residual, const void* w
  * Gate/up GEMV with the SwiGLU epilogue.
  *   x        : bf16 [M][d]
  *   Wg, Wu   : [f][d] in format fmt (see Layouts)
- *   scales   : bf16 [2][f][d/group]  (NULL for MT_W_BF16)
- *   biases   : bf16 [2][f][d/group]  (NULL for MT_W_BF16)
+ *   scales   : bf16 [2][f][d/group] (NULL for MT_W_BF16; uint8 E8M0 for MX)
+ *   biases   : bf16 [2][f][d/group] (NULL for MT_W_BF16 and MX)
  *   group    : 32, 64 or 128 for affine formats, 0 for MT_W_BF16
  *   out_h    : [M][f] of out_dtype, h = silu(g) * u, silu(g) = g / (1 + e^-g),
  *              g = x . Wg[n], u = x . Wu[n], fp32 accumulation, one rounding.
- * Limits: 1 <= M <= 8; d % group == 0 (affine), d % 8 == 0 (bf16);
+ * Limits: 1 <= M <= 8; d % group == 0 (affine; group 32 for MX), d % 8 == 0 (bf16);
  *         1 <= f; d <= 32768.
  * meTile docs, "Compute-Graph Fusion", Automatic Gated Epilogues (two matmuls
  * sharing the activation, silu(gate) * up applied on-chip); "MLX-LM Backend",
@@ -152,12 +162,12 @@ mt_status mt_swiglu_gateup(const void* x, const void* Wg, const void* Wu,
  * Down GEMV with the residual epilogue.
  *   h        : bf16 [M][f]
  *   Wd       : [d][f] in format fmt
- *   scales   : bf16 [d][f/group] (NULL for MT_W_BF16)
- *   biases   : bf16 [d][f/group] (NULL for MT_W_BF16)
+ *   scales   : bf16 [d][f/group] (NULL for MT_W_BF16; uint8 E8M0 for MX)
+ *   biases   : bf16 [d][f/group] (NULL for MT_W_BF16 and MX)
  *   residual : bf16 [M][d]
  *   out_y    : [M][d] of out_dtype, y = h . Wd[n] + residual[n], fp32
  *              accumulation, one rounding.  out_y may equal residual.
- * Limits: 1 <= M <= 8; f % group == 0 (affine), f % 8 == 0 (bf16);
+ * Limits: 1 <= M <= 8; f % group == 0 (affine; group 32 for MX), f % 8 == 0 (bf16);
  *         1 <= d; f <= 32768.
  * meTile docs, "Compute-Graph Fusion", Automatic Gated Epilogues (residual
  * added to the down projection in the same kernel); "MLX-LM Backend",
@@ -176,13 +186,13 @@ mt_status mt_down_residual(const void* h, const void* Wd, const void* scales,
  *              caller may stack their rows into one [Nq + Nk + Nv][K] weight
  *              (and one bias) and make one call.  A tied embedding table
  *              [vocab][K] is used as W unchanged.
- *   scales   : bf16 [N][K/group] (NULL for MT_W_BF16)
- *   biases   : bf16 [N][K/group] (NULL for MT_W_BF16)
+ *   scales   : bf16 [N][K/group] (NULL for MT_W_BF16; uint8 E8M0 for MX)
+ *   biases   : bf16 [N][K/group] (NULL for MT_W_BF16 and MX)
  *   bias     : bf16 [N], added to every row, or NULL for a projection without
  *              bias
  *   out_y    : [M][N] of out_dtype, y = x . W[n] (+ bias[n]), fp32
  *              accumulation, one rounding.
- * Limits: 1 <= M <= 8; K % group == 0 (affine), K % 8 == 0 (bf16);
+ * Limits: 1 <= M <= 8; K % group == 0 (affine; group 32 for MX), K % 8 == 0 (bf16);
  *         K <= 32768; 1 <= N <= 1048576.
  * Aliasing: out_y overlaps no input.
  * meTile docs, "MLX-LM Backend", the attention-projection compression passage
@@ -211,6 +221,25 @@ mt_status mt_linear_bias(const void* x, const void* W, const void* scales,
  */
 mt_status mt_pack_affine(const float* W, int N, int K, int group, int bits,
                          void* q, void* scales, void* biases, void* stream);
+
+/*
+ * MX block-scaled quantiser and packer (offline preparation; stream-ordered).
+ *   W        : fp32 [N][K], device;  K % 32 == 0
+ *   bits     : 8 (MXFP8, E4M3 elements) or 4 (MXFP4, E2M1 elements)
+ *   q        : uint8 [N][K] (bits 8) or [N][K/2] (bits 4, code 2j in bits
+ *              0..3 of byte j, 2j+1 in bits 4..7), device
+ *   scales   : uint8 [N][K/32] E8M0 fields, device
+ * Per block of 32 consecutive elements along K: E = clamp(floor(log2(amax))
+ * - emax + 127, 0, 254) with emax = 8 (E4M3) or 2 (E2M1), E = 0 for an
+ * all-zero block; each element is w / 2^(E - 127) rounded to nearest-even
+ * in the element format, magnitudes above its largest finite value (448,
+ * 6) clamped to it, the sign kept.  Deterministic; bit-identical to the CPU
+ * oracle's quantiser.  meTile docs, "MLX-LM Backend", Block-Scaled MLX
+ * Primitive (MXFP8 / MXFP4 weights quantised ahead of time); the shared-scale
+ * rule and encodings are those of the OCP Microscaling Formats v1.0.
+ */
+mt_status mt_pack_mx(const float* W, int N, int K, int bits, void* q, void* scales,
+                     void* stream);
 
 /*
  * Dequantise packed affine weights to fp32 [N][K] (w = scale * q + bias,

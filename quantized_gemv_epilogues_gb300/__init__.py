@@ -14,6 +14,7 @@ Calls (same names as the C ABI):
 * :func:`mt_linear_bias` -- projection GEMV with an optional bias (attention
   q/k/v/o, vocabulary projection).
 * :func:`mt_pack_affine` / :func:`mt_unpack_affine` -- affine group packer.
+* :func:`mt_pack_mx` -- MXFP8 / MXFP4 block-scaled packer (E8M0 scales).
 * :func:`mt_mlp_plan_create` / :func:`mt_mlp_plan_run` / :func:`mt_mlp_plan_destroy`
   -- the warmed executor: L one-row layers as one persistent kernel.
 * :func:`mt_mlp_stack_run_noalloc` -- the same pass without any allocation.
@@ -40,7 +41,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 MT_OK, MT_ERR_NULL, MT_ERR_SHAPE, MT_ERR_GROUP, MT_ERR_ALIGN = 0, 1, 2, 3, 4
 MT_ERR_FORMAT, MT_ERR_ALIAS, MT_ERR_CUDA, MT_ERR_TIMEOUT = 5, 6, 7, 8
 MT_BF16, MT_F32 = 0, 1
-MT_W_BF16, MT_W_AFFINE8, MT_W_AFFINE4 = 0, 1, 2
+MT_W_BF16, MT_W_AFFINE8, MT_W_AFFINE4, MT_W_MXFP8, MT_W_MXFP4 = 0, 1, 2, 3, 4
 MT_OPT_PDL, MT_OPT_GEMV, MT_OPT_TEST_BARRIER_EXTRA = 0, 1, 2
 
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
@@ -51,6 +52,7 @@ _SIGS = {
     "mt_linear_bias": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
     "mt_pack_affine": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "mt_unpack_affine": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "mt_pack_mx": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "mt_set_option": (_I, [_I, _I]),
     "mt_get_option": (_I, [_I]),
     "mt_status_string": (ctypes.c_char_p, [_I]),
@@ -181,6 +183,11 @@ def mt_linear_bias(x, W, scales, biases, group, bias, out_y, M=None, K=None, N=N
 def mt_pack_affine(W, N, K, group, bits, q, scales, biases, stream=None):
     _check(_lib.mt_pack_affine(_ptr(W), int(N), int(K), int(group), int(bits), _ptr(q),
                                _ptr(scales), _ptr(biases), _stream(stream)), "mt_pack_affine")
+
+
+def mt_pack_mx(W, N, K, bits, q, scales, stream=None):
+    _check(_lib.mt_pack_mx(_ptr(W), int(N), int(K), int(bits), _ptr(q), _ptr(scales), _stream(stream)),
+           "mt_pack_mx")
 
 
 def mt_unpack_affine(q, scales, biases, N, K, group, bits, W, stream=None):

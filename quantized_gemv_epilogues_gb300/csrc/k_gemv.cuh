@@ -57,12 +57,17 @@ struct GemvArgs {
   int out_f32;
 };
 
-constexpr int FMT_BF16 = 0, FMT_A8 = 1, FMT_A4 = 2;
+// Weight formats (the values of mt_wfmt).  MX8 / MX4: OCP MX block-scaled
+// E4M3 / E2M1 elements with one E8M0 scale per 32 elements along K; only the
+// tensor-core kernel (k_gemv_mma.cuh) takes them.
+constexpr int FMT_BF16 = 0, FMT_A8 = 1, FMT_A4 = 2, FMT_MX8 = 3, FMT_MX4 = 4;
 
 template <int FMT> struct FmtTraits;
-template <> struct FmtTraits<FMT_BF16> { static constexpr int EPC = 8, EPW = 2; static constexpr bool AFFINE = false; };
-template <> struct FmtTraits<FMT_A8> { static constexpr int EPC = 16, EPW = 4; static constexpr bool AFFINE = true; };
-template <> struct FmtTraits<FMT_A4> { static constexpr int EPC = 32, EPW = 8; static constexpr bool AFFINE = true; };
+template <> struct FmtTraits<FMT_BF16> { static constexpr int EPC = 8, EPW = 2; static constexpr bool AFFINE = false, MX = false; };
+template <> struct FmtTraits<FMT_A8> { static constexpr int EPC = 16, EPW = 4; static constexpr bool AFFINE = true, MX = false; };
+template <> struct FmtTraits<FMT_A4> { static constexpr int EPC = 32, EPW = 8; static constexpr bool AFFINE = true, MX = false; };
+template <> struct FmtTraits<FMT_MX8> { static constexpr int EPC = 16, EPW = 4; static constexpr bool AFFINE = false, MX = true; };
+template <> struct FmtTraits<FMT_MX4> { static constexpr int EPC = 32, EPW = 8; static constexpr bool AFFINE = false, MX = true; };
 
 // Decodes word i of a 16-byte weight chunk into EPW floats: the raw codes q
 // (affine) or the bf16 weights.

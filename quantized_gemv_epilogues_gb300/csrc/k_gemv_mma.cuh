@@ -89,20 +89,20 @@ struct MmaArgs {
 template <int FMT, int KIND, int WPL>
 struct MmaCfg {
   static constexpr int NW = KIND == 0 ? 2 : 1;                               // weight matrices
-  static constexpr int EPW = FMT == FMT_A8 ? 4 : (FMT == FMT_A4 ? 8 : 2);    // codes per word
+  static constexpr int EPW = FmtTraits<FMT>::EPW;                           // codes per word
   static constexpr int CPL = WPL * EPW;  // codes per lane per chunk
   static constexpr int CW = 4 * CPL;     // codes of a row per chunk (4 lanes)
   static constexpr int LB = 2 * CPL;     // bytes of staged x per lane per chunk
   static constexpr int CPU = MMA_WORDS / (NW * 2 * WPL);  // chunks per unit
   static constexpr int UK = CPU * CW;                       // K per unit
-  static constexpr int KSC = FMT == FMT_A8 ? WPL : (FMT == FMT_A4 ? 2 * WPL : WPL / 2);  // k steps per chunk
+  static constexpr int KSC = EPW * WPL / 4;  // k steps per chunk (16 K indices = 4 per lane each)
   static_assert(CPU >= 1 && KSC >= 1, "load width");
 };
 
 // Byte offset of code k within a weight row.
 template <int FMT>
 __host__ __device__ constexpr size_t code_bytes(int k) {
-  return FMT == FMT_A8 ? (size_t)k : (FMT == FMT_A4 ? (size_t)k / 2 : (size_t)k * 2);
+  return FmtTraits<FMT>::EPW == 4 ? (size_t)k : (FmtTraits<FMT>::EPW == 8 ? (size_t)k / 2 : (size_t)k * 2);
 }
 
 // Streaming loads of WPL words (no L1 allocation, L2 policy).
@@ -183,20 +183,45 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
   }
 }
 
+// Exact fp16 values of block-scaled elements (the E8M0 block scale is applied
+// at the group flush): lo = codes (c0, c1), hi = (c2, c3) of the word's four
+// E4M3 bytes, or of the two E2M1 bytes in its low 16 bits (byte b holds
+// c_2b in bits 0..3 and c_2b+1 in bits 4..7).  Every E4M3 and E2M1 value is
+// an fp16 value.
+__device__ __forceinline__ void e4m3x2_to_f16x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(v));
+}
+__device__ __forceinline__ void e2m1x2_to_f16x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(v));
+}
+
 // The two A registers of k step ks (within its chunk) from one row's words:
 // lo holds the codes of mma k slots (2t, 2t+1), hi those of (2t+8, 2t+9).
 //   A8:   word ks = codes c0..c3;   lo = (c0, c1), hi = (c2, c3)
 //   A4:   word ks/2 = codes c0..c7 (byte b: c_2b low nibble, c_2b+1 high);
 //         even ks: lo = (c0, c4), hi = (c1, c5); odd ks: lo = (c2, c6), hi = (c3, c7)
 //   BF16: words 2ks, 2ks+1 as stored (elements in order)
-// The staged x of a lane's chunk follows the same order (A8 and bf16: the
-// elements in order; A4: permuted within each 8), and when a lane's
-// block is 64 bytes (A4 with 16-byte loads) lanes t = 2, 3 keep its 16-byte
+//   MX8:  as A8, the E4M3 codes converted to fp16 values
+//   MX4:  word ks/2, its low (even ks) or high (odd ks) 16 bits = codes
+//         c0..c3 of the step in order: lo = (c0, c1), hi = (c2, c3)
+// The staged x of a lane's chunk follows the same order (A8, MX8, MX4 and
+// bf16: the elements in order; A4: permuted within each 8), and when a lane's
+// block is 64 bytes (A4 or MX4 with 16-byte loads) lanes t = 2, 3 keep its 16-byte
 // pieces swapped in pairs (piece q at q ^ 1), so the quarter-warps of a
 // 16-byte shared load hit distinct banks.
 template <int FMT, int WPL>
 __device__ __forceinline__ void a_regs(const uint32_t (&w)[WPL], int ks, uint32_t& lo, uint32_t& hi) {
-  if constexpr (FMT == FMT_A8) {
+  if constexpr (FMT == FMT_MX8) {
+    e4m3x2_to_f16x2(w[ks], lo, hi);
+  } else if constexpr (FMT == FMT_MX4) {
+    e2m1x2_to_f16x2((ks & 1) ? (w[ks >> 1] >> 16) : w[ks >> 1], lo, hi);
+  } else if constexpr (FMT == FMT_A8) {
     const uint32_t v = w[ks];
     lo = __byte_perm(v, 0u, 0x4140);  // (c0, c1) * 2^-24
     hi = __byte_perm(v, 0u, 0x4342);  // (c2, c3) * 2^-24
@@ -222,12 +247,16 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
   using C = MmaCfg<FMT, KIND, WPL>;
   constexpr int NW = C::NW, CPU = C::CPU, UK = C::UK, CW = C::CW, LB = C::LB, KSC = C::KSC;
   constexpr bool AFF = FmtTraits<FMT>::AFFINE;
+  constexpr bool MX = FmtTraits<FMT>::MX;
+  constexpr bool GRP = AFF || MX;  // per-group flush (x scaled per group)
   constexpr bool BF = FMT == FMT_BF16;
 
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* xs = smem;                                                   // [M][xstride]
-  float4* sbf = reinterpret_cast<float4*>(smem + a.off_sbf);                  // [NW][RT][G][8]
-  uint16_t* raw = reinterpret_cast<uint16_t*>(smem + a.off_raw);              // [NW][2][rows*G]
+  float4* sbf = reinterpret_cast<float4*>(smem + a.off_sbf);                  // [NW][RT][G][8] (affine)
+  float2* sbf2 = reinterpret_cast<float2*>(smem + a.off_sbf);                 // [NW][RT][G][8] (MX)
+  uint16_t* raw = reinterpret_cast<uint16_t*>(smem + a.off_raw);              // [NW][2][rows*G] (affine)
+  uint8_t* raw8 = reinterpret_cast<uint8_t*>(smem + a.off_raw);               // [NW][rows*G] (MX)
   float* parts = reinterpret_cast<float*>(smem + a.off_parts);                // [W][NS][16][M][NW]
   float* ginv = reinterpret_cast<float*>(smem + a.off_ginv);                  // [Gc][8] 2^-e_g
   int* tstart = reinterpret_cast<int*>(smem + a.off_tstart);                  // [RT + 1]
@@ -343,6 +372,28 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
     }
     cp_async_commit();
   }
+  if constexpr (MX) {
+    // [rows][Gc] E8M0 bytes per matrix
+    const int n = rows * Gc;
+#pragma unroll
+    for (int mat = 0; mat < NW; ++mat) {
+      const uint8_t* s = reinterpret_cast<const uint8_t*>(mat ? a.s1 : a.s0);
+      uint8_t* rs = raw8 + (size_t)mat * n;
+      if (a.raw_vec) {  // Gc % 16 == 0: 16-byte pieces
+        const int upr = Gc >> 4;
+        for (int i = tid; i < n / 16; i += MMA_THREADS) {
+          const int rl = i / upr, c = i - rl * upr;
+          cp_async16(rs + i * 16, s + (size_t)(r_begin + rl) * G + g_lo + c * 16);
+        }
+      } else {
+        for (int i = tid; i < n; i += MMA_THREADS) {
+          const int rl = i / Gc, c = i - rl * Gc;
+          rs[i] = s[(size_t)(r_begin + rl) * G + g_lo + c];
+        }
+      }
+    }
+    cp_async_commit();
+  }
 
   pdl_wait();  // x, the residual and the output follow the preceding kernel
 
@@ -362,7 +413,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
   cp_async_wait_all();  // x (and the raw scales/biases)
   __syncthreads();
 
-  if constexpr (AFF) {
+  if constexpr (GRP) {
     // ---- x as fp16 in place, scaled per quantisation group by 2^e_g with
     // max|x| 2^e_g in [2^14, 2^15) (a zero or tiny maximum gives 2^112);
     // ginv[g][m] = 2^-e_g.  One 16-byte unit (8 elements) per lane and step,
@@ -411,7 +462,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
         const int e = max(-126, min(112, 14 - ((int)(mx[j] >> 7) - 127)));
         const uint32_t thr = (uint32_t)(112 - e) << 7, t2 = thr | (thr << 16);
         uint4 o;
-        if constexpr (FMT == FMT_A8) {
+        if constexpr (FMT != FMT_A4) {
           o = make_uint4(bf16x2_to_f16x2(v[j].x, t2), bf16x2_to_f16x2(v[j].y, t2),
                          bf16x2_to_f16x2(v[j].z, t2), bf16x2_to_f16x2(v[j].w, t2));
         } else {
@@ -425,7 +476,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
                          bf16x2_to_f16x2(__byte_perm(v[j].y, v[j].w, 0x7632), t2o));
         }
         if (j < pu && u < U8) {
-          const int ud = (FMT == FMT_A4 && WPL == 4) ? (u ^ ((u >> 3) & 1)) : u;
+          const int ud = (LB == 64) ? (u ^ ((u >> 3) & 1)) : u;
           *reinterpret_cast<uint4*>(row + (size_t)ud * 16) = o;
           if ((u & (upg - 1)) == 0) ginv[(u >> lg_upg) * 8 + m] = exp2i(-e);
         }
@@ -441,14 +492,24 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
       while (j >= RT) { j -= RT; ++mat; }
       for (int i = tid; i < NW * ne; i += MMA_THREADS) {
         const int tr0 = tstart[j], tr1 = tstart[j + 1];
-        const uint16_t* rs = raw + (size_t)(2 * mat) * n;
-        const uint16_t* rb = rs + n;
         const int ra = tr0 + gi, rbw = tr0 + gi + 8;
-        float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
-        constexpr float TWO24 = 16777216.f;  // the codes enter the mma as q * 2^-24
-        if (ra < tr1) { e.x = bf16f(rs[ra * Gc + g]) * TWO24; e.z = bf16f(rb[ra * Gc + g]); }
-        if (rbw < tr1) { e.y = bf16f(rs[rbw * Gc + g]) * TWO24; e.w = bf16f(rb[rbw * Gc + g]); }
-        sbf[i] = e;
+        if constexpr (MX) {
+          // E8M0 field E: 2^(E - 127) (E = 0: 2^-127, an fp32 subnormal)
+          const uint8_t* rs = raw8 + (size_t)mat * n;
+          auto e8m0 = [](uint32_t E) { return E ? __int_as_float((int)(E << 23)) : __int_as_float(0x00400000); };
+          float2 e = make_float2(0.f, 0.f);
+          if (ra < tr1) e.x = e8m0(rs[ra * Gc + g]);
+          if (rbw < tr1) e.y = e8m0(rs[rbw * Gc + g]);
+          sbf2[i] = e;
+        } else {
+          const uint16_t* rs = raw + (size_t)(2 * mat) * n;
+          const uint16_t* rb = rs + n;
+          float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
+          constexpr float TWO24 = 16777216.f;  // the codes enter the mma as q * 2^-24
+          if (ra < tr1) { e.x = bf16f(rs[ra * Gc + g]) * TWO24; e.z = bf16f(rb[ra * Gc + g]); }
+          if (rbw < tr1) { e.y = bf16f(rs[rbw * Gc + g]) * TWO24; e.w = bf16f(rb[rbw * Gc + g]); }
+          sbf[i] = e;
+        }
         g += MMA_THREADS / 8;
         while (g >= Gc) { g -= Gc; ++j; }
         while (j >= RT) { j -= RT; ++mat; }
@@ -474,7 +535,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
     for (int ch = 0; ch < CPU; ++ch) {
       const int kc = k0 + ch * CW;
       if (kc >= Kc) break;
-      if constexpr (AFF) {
+      if constexpr (GRP) {
         if ((kc & (a.group - 1)) == 0) {
 #pragma unroll
           for (int mat = 0; mat < NW; ++mat)
@@ -484,8 +545,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
           for (int i = 0; i < 4; ++i) d1[i] = 0.f;
         }
       }
-      // A4 with 16-byte loads: lanes t = 2, 3 hold their pieces swapped
-      constexpr bool SWP = FMT == FMT_A4 && WPL == 4;
+      // 64-byte lane blocks (A4, MX4 with 16-byte loads): lanes t = 2, 3 hold
+      // their pieces swapped
+      constexpr bool SWP = LB == 64;
       uint32_t xr[LB / 4];
 #pragma unroll
       for (int q = 0; q < LB / 16; ++q) {
@@ -505,10 +567,25 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) gemv_mma_kernel(const MmaArgs 
           uint32_t lo0, hi0, lo1, hi1;
           a_regs<FMT, WPL>(buf[mat][0][ch], ks, lo0, hi0);
           a_regs<FMT, WPL>(buf[mat][1][ch], ks, lo1, hi1);
-          if constexpr (AFF)
+          if constexpr (GRP)
             mma16816<false>(d[mat], lo0, lo1, hi0, hi1, b0, b1);
           else
             mma16816<BF>(acc[mat], lo0, lo1, hi0, hi1, b0, b1);
+        }
+      }
+      if constexpr (MX) {
+        if (((kc + CW) & (a.group - 1)) == 0) {  // the block ends with this chunk
+          const int g = kc >> a.lg_group;
+          // block scale * sum(w x) in the group's x scale, then undone
+          const float2 gi = *reinterpret_cast<const float2*>(ginv + g * 8 + 2 * t);
+#pragma unroll
+          for (int mat = 0; mat < NW; ++mat) {
+            const float2 sb = sbf2[(size_t)mat * ne + (j * Gc + g) * 8 + gid];
+            acc[mat][0] = fmaf(sb.x * d[mat][0], gi.x, acc[mat][0]);
+            acc[mat][1] = fmaf(sb.x * d[mat][1], gi.y, acc[mat][1]);
+            acc[mat][2] = fmaf(sb.y * d[mat][2], gi.x, acc[mat][2]);
+            acc[mat][3] = fmaf(sb.y * d[mat][3], gi.y, acc[mat][3]);
+          }
         }
       }
       if constexpr (AFF) {
@@ -669,6 +746,8 @@ template <int FMT, int KIND, int WPL>
 mt_status run_gemv_mma(const GemvProblem& p, const Launch& l) {
   using C = MmaCfg<FMT, KIND, WPL>;
   constexpr bool AFF = FmtTraits<FMT>::AFFINE;
+  constexpr bool MX = FmtTraits<FMT>::MX;
+  constexpr bool GRP = AFF || MX;
   constexpr int NW = C::NW;
   static OccCache cache;  // only the attribute flags are used
   int dev = 0;
@@ -678,7 +757,7 @@ mt_status run_gemv_mma(const GemvProblem& p, const Launch& l) {
   const DeviceInfo* di = device_info(&derr);
   if (!di) return cuda_fail((cudaError_t)derr);
   if (p.M < 1 || p.M > 8 || p.K % C::CW) return MT_ERR_SHAPE;
-  if (AFF && (p.group % C::CW || p.K % p.group)) return MT_ERR_SHAPE;
+  if (GRP && (p.group % C::CW || p.K % p.group)) return MT_ERR_SHAPE;
 
   MmaArgs a = {};
   a.x = p.x;
@@ -690,20 +769,21 @@ mt_status run_gemv_mma(const GemvProblem& p, const Launch& l) {
   a.out = p.out;
   a.out_f32 = p.out_f32 ? 1 : 0;
   a.M = p.M; a.K = p.K; a.N = p.N;
-  a.group = AFF ? p.group : 1;
-  a.lg_group = AFF ? (p.group == 32 ? 5 : (p.group == 64 ? 6 : 7)) : 0;
-  a.G = AFF ? p.K / p.group : 0;
+  a.group = GRP ? p.group : 1;
+  a.lg_group = GRP ? (p.group == 32 ? 5 : (p.group == 64 ? 6 : 7)) : 0;
+  a.G = GRP ? p.K / p.group : 0;
   a.row_bytes = (int)code_bytes<FMT>(p.K);
 
   // The geometry for ck CTAs per row range (1, or a cluster of 2 that
-  // splits K); returns the dynamic shared memory it needs (0: no tile table).
+  // splits K) and `waves` times as many row ranges as fit the SMs at once;
+  // returns the dynamic shared memory it needs (0: no tile table).
   const int sms = di->sm_count;
   int grid = 0;
-  auto plan = [&](int ck) -> size_t {
+  auto plan = [&](int ck, int waves) -> size_t {
     a.ck = ck;
     a.Kc = p.K / ck;
     a.Gc = a.G / ck;
-    const int nrange = std::min(sms / ck, p.N);  // row ranges (clusters)
+    const int nrange = std::min(sms / ck * waves, p.N);  // row ranges (clusters)
     grid = nrange * ck;
     a.rows_base = p.N / nrange;
     a.rows_extra = p.N % nrange;
@@ -715,14 +795,15 @@ mt_status run_gemv_mma(const GemvProblem& p, const Launch& l) {
     const long len = (U + MMA_WARPS - 1) / MMA_WARPS;  // longest warp range
     a.NS = (int)std::min<long>(RT, (len - 1 + a.KB - 1) / a.KB + 1);
     a.xstride = (a.Kc * 2 + 127) / 128 * 128 + mma_row_pad<C::LB>();
-    a.raw_vec = (AFF && a.Gc % 8 == 0) ? 1 : 0;
+    a.raw_vec = (AFF && a.Gc % 8 == 0) || (MX && a.Gc % 16 == 0) ? 1 : 0;
     auto al16 = [](size_t v) { return (v + 15) / 16 * 16; };
     size_t off = al16((size_t)p.M * a.xstride);
     a.off_sbf = (int)off;
-    if (AFF) off += (size_t)NW * RT * a.Gc * 8 * 16;
+    if (GRP) off += (size_t)NW * RT * a.Gc * 8 * (AFF ? 16 : 8);
     a.off_ginv = (int)off;
-    if (AFF) off += (size_t)a.Gc * 8 * 4;
-    const size_t raw_bytes = AFF ? al16((size_t)NW * 2 * rows_max * a.Gc * 2) : 0;
+    if (GRP) off += (size_t)a.Gc * 8 * 4;
+    const size_t raw_bytes = AFF ? al16((size_t)NW * 2 * rows_max * a.Gc * 2)
+                                 : (MX ? al16((size_t)NW * rows_max * a.Gc) : 0);
     const size_t parts_bytes = (size_t)MMA_WARPS * a.NS * 16 * p.M * NW * 4;
     a.off_raw = (int)off;    // the raw scales/biases are dead once the
     a.off_parts = (int)off;  // mainloop writes its first partial
@@ -739,14 +820,25 @@ mt_status run_gemv_mma(const GemvProblem& p, const Launch& l) {
   // weights (staging and converting x costs every CTA; measured: a win for
   // the down projection at M = 8, a loss when x is under ~2/3 of the bytes of
   // the CTA's weight rows).
+  // A row range too long for the tile table or the shared arrays is cut into
+  // more ranges than SMs (CTAs run in waves).
   const size_t budget = (size_t)di->max_smem_optin - 1024;
   const int Kh = p.K / 2;
   const bool can2 = sms % 2 == 0 && p.K % 2 == 0 && Kh % C::CW == 0 &&
-                    (!AFF || Kh % p.group == 0) && p.N >= 16 * (sms / 2);
-  size_t smem = plan(1);
+                    (!GRP || Kh % p.group == 0) && p.N >= 16 * (sms / 2);
   const double x_bytes = 2.0 * p.M * p.K;
   const double w_bytes = (double)p.N / sms * (double)a.row_bytes * NW;
-  if (can2 && (smem == 0 || smem > budget || x_bytes * 3 > w_bytes * 2)) smem = plan(2);
+  size_t smem = 0;
+  for (int waves = 1; waves <= 64; ++waves) {
+    smem = plan(1, waves);
+    if (can2 && (smem == 0 || smem > budget || x_bytes * 3 * waves > w_bytes * 2)) {
+      const size_t s2 = plan(2, waves);
+      if (s2 != 0 && s2 <= budget) { smem = s2; break; }
+      smem = plan(1, waves);
+    }
+    if (smem != 0 && smem <= budget) break;
+    if ((p.N + sms * waves - 1) / (sms * waves) <= 16) break;  // one tile per range already
+  }
   if (smem == 0 || smem > budget) return MT_ERR_SHAPE;
 
   auto kern = gemv_mma_kernel<FMT, KIND, WPL>;
@@ -765,7 +857,11 @@ mt_status run_gemv_mma(const GemvProblem& p, const Launch& l) {
 // lanes x WPL words) must lie in one group.
 template <int FMT, int KIND>
 mt_status dispatch_mma(const GemvProblem& p, const Launch& l) {
-  if constexpr (FMT == FMT_A8) {
+  if constexpr (FMT == FMT_MX8) {
+    return run_gemv_mma<FMT, KIND, 2>(p, l);  // blocks of 32: 4 lanes x 8 bytes
+  } else if constexpr (FMT == FMT_MX4) {
+    return run_gemv_mma<FMT, KIND, 1>(p, l);  // blocks of 32: 4 lanes x 4 bytes
+  } else if constexpr (FMT == FMT_A8) {
     if (p.group == 32) return run_gemv_mma<FMT, KIND, 2>(p, l);
     return run_gemv_mma<FMT, KIND, 4>(p, l);
   } else if constexpr (FMT == FMT_A4) {

@@ -159,4 +159,86 @@ mt_status launch_unpack_affine(const uint8_t* q, const uint16_t* s, const uint16
   return launch(unpack_affine_kernel<4>, dim3((unsigned)blocks), dim3(256), 0, l, q, s, b, N, K, group, W);
 }
 
+// ------------------------------------------------------------ MX packer
+//
+// meTile docs, "MLX-LM Backend", Block-Scaled MLX Primitive: MXFP8 / MXFP4
+// weights quantised ahead of time, E4M3 / E2M1 values with E8M0 scales.  The
+// encodings and the block of 32 elements along K are those of the OCP
+// Microscaling Formats (MX) v1.0 specification named by the format:
+//   scale field E = clamp(floor(log2(amax)) - emax + 127, 0, 254), emax the
+//                   element format's largest exponent (8 for E4M3, 2 for
+//                   E2M1); an all-zero block takes E = 0
+//   element       = w / 2^(E - 127) rounded to nearest-even in the element
+//                   format, magnitudes above its largest finite value clamped
+//                   to it, the sign kept.
+// One warp per block, one element per lane; the rounding is done in binary64
+// (the division by a power of two is exact there).
+
+// floor(log2(a)) of a positive finite float (subnormals included).
+__device__ __forceinline__ int floor_log2_pos(float a) {
+  const uint32_t u = __float_as_uint(a);
+  const int e = (int)(u >> 23);
+  return e ? e - 127 : (31 - __clz((int)u)) - 149;
+}
+
+// Nearest E4M3 code (sign, 4 exponent bits with bias 7, 3 fraction bits).
+__device__ uint8_t e4m3_rne(double v) {
+  const uint8_t sign = signbit(v) ? 0x80 : 0;
+  const double a = fabs(v);
+  if (!(a < 448.0)) return (uint8_t)(sign | 0x7E);  // the largest finite, 448
+  if (a < 0x1p-6) return (uint8_t)(sign | (int)rint(a * 512.0));  // multiples of 2^-9; 8 = 2^-6
+  int e = ilogb(a);                        // a in [2^e, 2^(e+1)), -6 <= e <= 8
+  int m = (int)rint(ldexp(a, 3 - e));      // 8 .. 16
+  if (m == 16) { m = 8; ++e; }
+  return (uint8_t)(sign | ((e + 7) << 3) | (m - 8));
+}
+
+// Nearest E2M1 code (sign, 2 exponent bits with bias 1, 1 fraction bit).
+__device__ uint8_t e2m1_rne(double v) {
+  const uint8_t sign = signbit(v) ? 8 : 0;
+  const double a = fabs(v);
+  if (!(a < 6.0)) return (uint8_t)(sign | 7);  // the largest finite, 6
+  if (a < 1.0) return (uint8_t)(sign | (int)rint(a * 2.0));  // 0, 0.5; 2 = 1.0
+  int e = ilogb(a);                        // 0 .. 2
+  int m = (int)rint(ldexp(a, 1 - e));      // 2 .. 4
+  if (m == 4) { m = 2; ++e; }
+  return (uint8_t)(sign | ((e + 1) << 1) | (m - 2));
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(256) pack_mx_kernel(const float* __restrict__ W, int N, int K,
+                                                       uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+  const int lane = threadIdx.x & 31;
+  const long long nb = (long long)N * (K / 32);
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long b = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < nb; b += warps) {
+    const long long n = b / (K / 32), kb = b - n * (K / 32);
+    const float w = W[n * K + kb * 32 + lane];
+    float amax = fabsf(w);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    constexpr int EMAX = BITS == 8 ? 8 : 2;
+    const int E = amax > 0.f ? max(0, min(254, floor_log2_pos(amax) - EMAX + 127)) : 0;
+    const double v = ldexp((double)w, 127 - E);
+    const uint32_t c = BITS == 8 ? e4m3_rne(v) : e2m1_rne(v);
+    if (BITS == 8) {
+      q[n * K + kb * 32 + lane] = (uint8_t)c;
+    } else {
+      const uint32_t hi = __shfl_down_sync(0xffffffffu, c, 1);
+      if ((lane & 1) == 0) q[n * (K / 2) + kb * 16 + (lane >> 1)] = (uint8_t)(c | (hi << 4));
+    }
+    if (lane == 0) s[b] = (uint8_t)E;
+  }
+}
+
+mt_status launch_pack_mx(const float* W, int N, int K, int bits, uint8_t* q, uint8_t* s,
+                         const Launch& l) {
+  const long long nb = (long long)N * (K / 32);
+  if (nb == 0) return MT_OK;
+  long long blocks = (nb + 7) / 8;
+  if (blocks > 152 * 64) blocks = 152 * 64;
+  if (bits == 8) return launch(pack_mx_kernel<8>, dim3((unsigned)blocks), dim3(256), 0, l, W, N, K, q, s);
+  return launch(pack_mx_kernel<4>, dim3((unsigned)blocks), dim3(256), 0, l, W, N, K, q, s);
+}
+
 }  // namespace mt

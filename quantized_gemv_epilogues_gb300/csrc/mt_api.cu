@@ -64,12 +64,16 @@ const DeviceInfo* device_info(int* err) {
 mt_status launch_gemv_bf16(const GemvProblem& p, const Launch& l);
 mt_status launch_gemv_a8(const GemvProblem& p, const Launch& l);
 mt_status launch_gemv_a4(const GemvProblem& p, const Launch& l);
+mt_status launch_gemv_mx8(const GemvProblem& p, const Launch& l);
+mt_status launch_gemv_mx4(const GemvProblem& p, const Launch& l);
 
 mt_status launch_gemv(const GemvProblem& p, const Launch& l) {
   switch (p.fmt) {
     case MT_W_BF16: return launch_gemv_bf16(p, l);
     case MT_W_AFFINE8: return launch_gemv_a8(p, l);
     case MT_W_AFFINE4: return launch_gemv_a4(p, l);
+    case MT_W_MXFP8: return launch_gemv_mx8(p, l);
+    case MT_W_MXFP4: return launch_gemv_mx4(p, l);
     default: return MT_ERR_FORMAT;
   }
 }
@@ -89,10 +93,28 @@ struct Range {
 Range rng(const void* p, size_t n) { return Range{(uintptr_t)p, (uintptr_t)p + n}; }
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
+bool is_mx(int fmt) { return fmt == MT_W_MXFP8 || fmt == MT_W_MXFP4; }
+bool valid_wfmt(int fmt) { return fmt >= MT_W_BF16 && fmt <= MT_W_MXFP4; }
+
 size_t weight_bytes(int fmt, long N, long K) {
   if (fmt == MT_W_BF16) return (size_t)N * K * 2;
-  if (fmt == MT_W_AFFINE8) return (size_t)N * K;
+  if (fmt == MT_W_AFFINE8 || fmt == MT_W_MXFP8) return (size_t)N * K;
   return (size_t)N * K / 2;
+}
+
+// Bytes of the scales of one [N][K] weight (and of its biases, affine).
+size_t sb_bytes(int fmt, long N, long K, int group) {
+  if (fmt == MT_W_BF16) return 0;
+  return (size_t)N * (K / group) * (is_mx(fmt) ? 1 : 2);
+}
+
+// Which of scales / biases a format takes: affine both, MX scales only (biases
+// must be NULL), bf16 neither.
+mt_status check_sb(int fmt, const void* scales, const void* biases) {
+  if (fmt == MT_W_BF16) return MT_OK;
+  if (!scales) return MT_ERR_NULL;
+  if (is_mx(fmt)) return biases ? MT_ERR_FORMAT : MT_OK;
+  return biases ? MT_OK : MT_ERR_NULL;
 }
 
 bool valid_group(int fmt, int group, long K, mt_status* st) {
@@ -101,6 +123,7 @@ bool valid_group(int fmt, int group, long K, mt_status* st) {
     if (K % 8 != 0) { *st = MT_ERR_SHAPE; return false; }
     return true;
   }
+  if (is_mx(fmt) && group != 32) { *st = MT_ERR_GROUP; return false; }
   if (group != 32 && group != 64 && group != 128) { *st = MT_ERR_GROUP; return false; }
   if (K % group != 0) { *st = MT_ERR_SHAPE; return false; }
   return true;
@@ -138,10 +161,10 @@ mt_status mt_add_rmsnorm(const void* values, const void* residual, const void* w
 mt_status mt_swiglu_gateup(const void* x, const void* Wg, const void* Wu, const void* scales,
                            const void* biases, int group, void* out_h, int M, int d, int f,
                            mt_wfmt fmt, mt_dtype out_dtype, void* stream) {
-  if (fmt != MT_W_BF16 && fmt != MT_W_AFFINE8 && fmt != MT_W_AFFINE4) return MT_ERR_FORMAT;
+  if (!valid_wfmt(fmt)) return MT_ERR_FORMAT;
   if (out_dtype != MT_BF16 && out_dtype != MT_F32) return MT_ERR_FORMAT;
   if (!x || !Wg || !Wu || !out_h) return MT_ERR_NULL;
-  if (fmt != MT_W_BF16 && (!scales || !biases)) return MT_ERR_NULL;
+  if (const mt_status sbst = check_sb(fmt, scales, biases)) return sbst;
   if (M < 1 || M > 8 || d < 1 || d > 32768 || f < 1) return MT_ERR_SHAPE;
   mt_status st = MT_OK;
   if (!valid_group(fmt, group, d, &st)) return st;
@@ -149,11 +172,11 @@ mt_status mt_swiglu_gateup(const void* x, const void* Wg, const void* Wu, const 
       (fmt != MT_W_BF16 && (!aligned16(scales) || !aligned16(biases))))
     return MT_ERR_ALIGN;
   const size_t wb = weight_bytes(fmt, f, d);
-  const size_t sbb = fmt == MT_W_BF16 ? 0 : (size_t)2 * f * (d / group) * 2;
+  const size_t sbb = 2 * sb_bytes(fmt, f, d, group);  // two planes
   const Range ro = rng(out_h, (size_t)M * f * (out_dtype == MT_F32 ? 4 : 2));
   if (overlap(ro, rng(x, (size_t)M * d * 2)) || overlap(ro, rng(Wg, wb)) ||
       overlap(ro, rng(Wu, wb)) ||
-      (sbb && (overlap(ro, rng(scales, sbb)) || overlap(ro, rng(biases, sbb)))))
+      (sbb && (overlap(ro, rng(scales, sbb)) || (biases && overlap(ro, rng(biases, sbb))))))
     return MT_ERR_ALIAS;
   GemvProblem p = {};
   p.kind = Kind::GateUp;
@@ -163,9 +186,13 @@ mt_status mt_swiglu_gateup(const void* x, const void* Wg, const void* Wu, const 
   p.x = (const uint16_t*)x;
   p.W0 = Wg; p.W1 = Wu;
   if (fmt != MT_W_BF16) {
-    const size_t plane = (size_t)f * (d / group);
-    p.s0 = (const uint16_t*)scales; p.s1 = (const uint16_t*)scales + plane;
-    p.b0 = (const uint16_t*)biases; p.b1 = (const uint16_t*)biases + plane;
+    const size_t plane = sb_bytes(fmt, f, d, group);  // bytes of one plane
+    p.s0 = (const uint16_t*)scales;
+    p.s1 = (const uint16_t*)((const char*)scales + plane);
+    if (biases) {
+      p.b0 = (const uint16_t*)biases;
+      p.b1 = (const uint16_t*)((const char*)biases + plane);
+    }
   }
   p.out = out_h;
   p.out_f32 = out_dtype == MT_F32;
@@ -175,10 +202,10 @@ mt_status mt_swiglu_gateup(const void* x, const void* Wg, const void* Wu, const 
 mt_status mt_down_residual(const void* h, const void* Wd, const void* scales, const void* biases,
                            int group, const void* residual, void* out_y, int M, int f, int d,
                            mt_wfmt fmt, mt_dtype out_dtype, void* stream) {
-  if (fmt != MT_W_BF16 && fmt != MT_W_AFFINE8 && fmt != MT_W_AFFINE4) return MT_ERR_FORMAT;
+  if (!valid_wfmt(fmt)) return MT_ERR_FORMAT;
   if (out_dtype != MT_BF16 && out_dtype != MT_F32) return MT_ERR_FORMAT;
   if (!h || !Wd || !residual || !out_y) return MT_ERR_NULL;
-  if (fmt != MT_W_BF16 && (!scales || !biases)) return MT_ERR_NULL;
+  if (const mt_status sbst = check_sb(fmt, scales, biases)) return sbst;
   if (M < 1 || M > 8 || f < 1 || f > 32768 || d < 1) return MT_ERR_SHAPE;
   mt_status st = MT_OK;
   if (!valid_group(fmt, group, f, &st)) return st;
@@ -186,11 +213,11 @@ mt_status mt_down_residual(const void* h, const void* Wd, const void* scales, co
       (fmt != MT_W_BF16 && (!aligned16(scales) || !aligned16(biases))))
     return MT_ERR_ALIGN;
   const size_t wb = weight_bytes(fmt, d, f);
-  const size_t sbb = fmt == MT_W_BF16 ? 0 : (size_t)d * (f / group) * 2;
+  const size_t sbb = sb_bytes(fmt, d, f, group);
   const Range ro = rng(out_y, (size_t)M * d * (out_dtype == MT_F32 ? 4 : 2));
   const Range rr = rng(residual, (size_t)M * d * 2);
   if (overlap(ro, rng(h, (size_t)M * f * 2)) || overlap(ro, rng(Wd, wb)) ||
-      (sbb && (overlap(ro, rng(scales, sbb)) || overlap(ro, rng(biases, sbb)))))
+      (sbb && (overlap(ro, rng(scales, sbb)) || (biases && overlap(ro, rng(biases, sbb))))))
     return MT_ERR_ALIAS;
   if (overlap(ro, rr) && !(out_y == residual && out_dtype == MT_BF16)) return MT_ERR_ALIAS;
   GemvProblem p = {};
@@ -212,10 +239,10 @@ mt_status mt_down_residual(const void* h, const void* Wd, const void* scales, co
 mt_status mt_linear_bias(const void* x, const void* W, const void* scales, const void* biases,
                          int group, const void* bias, void* out_y, int M, int K, int N,
                          mt_wfmt fmt, mt_dtype out_dtype, void* stream) {
-  if (fmt != MT_W_BF16 && fmt != MT_W_AFFINE8 && fmt != MT_W_AFFINE4) return MT_ERR_FORMAT;
+  if (!valid_wfmt(fmt)) return MT_ERR_FORMAT;
   if (out_dtype != MT_BF16 && out_dtype != MT_F32) return MT_ERR_FORMAT;
   if (!x || !W || !out_y) return MT_ERR_NULL;
-  if (fmt != MT_W_BF16 && (!scales || !biases)) return MT_ERR_NULL;
+  if (const mt_status sbst = check_sb(fmt, scales, biases)) return sbst;
   if (M < 1 || M > 8 || K < 1 || K > 32768 || N < 1 || N > (1 << 20)) return MT_ERR_SHAPE;
   mt_status st = MT_OK;
   if (!valid_group(fmt, group, K, &st)) return st;
@@ -223,11 +250,11 @@ mt_status mt_linear_bias(const void* x, const void* W, const void* scales, const
       (fmt != MT_W_BF16 && (!aligned16(scales) || !aligned16(biases))))
     return MT_ERR_ALIGN;
   const size_t wb = weight_bytes(fmt, N, K);
-  const size_t sbb = fmt == MT_W_BF16 ? 0 : (size_t)N * (K / group) * 2;
+  const size_t sbb = sb_bytes(fmt, N, K, group);
   const Range ro = rng(out_y, (size_t)M * N * (out_dtype == MT_F32 ? 4 : 2));
   if (overlap(ro, rng(x, (size_t)M * K * 2)) || overlap(ro, rng(W, wb)) ||
       (bias && overlap(ro, rng(bias, (size_t)N * 2))) ||
-      (sbb && (overlap(ro, rng(scales, sbb)) || overlap(ro, rng(biases, sbb)))))
+      (sbb && (overlap(ro, rng(scales, sbb)) || (biases && overlap(ro, rng(biases, sbb))))))
     return MT_ERR_ALIAS;
   GemvProblem p = {};
   p.kind = Kind::Down;
@@ -261,6 +288,18 @@ mt_status mt_pack_affine(const float* W, int N, int K, int group, int bits, void
     return MT_ERR_ALIAS;
   return launch_pack_affine(W, N, K, group, bits, (uint8_t*)q, (uint16_t*)scales,
                             (uint16_t*)biases, Launch{(cudaStream_t)stream, false});
+}
+
+mt_status mt_pack_mx(const float* W, int N, int K, int bits, void* q, void* scales, void* stream) {
+  if (!W || !q || !scales) return MT_ERR_NULL;
+  if (bits != 8 && bits != 4) return MT_ERR_FORMAT;
+  if (N < 0 || K < 0 || K % 32 != 0) return MT_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(q) || !aligned16(scales)) return MT_ERR_ALIGN;
+  const size_t qb = (size_t)N * K * bits / 8, sb = (size_t)N * (K / 32);
+  const Range rq = rng(q, qb), rs = rng(scales, sb), rw = rng(W, (size_t)N * K * 4);
+  if (overlap(rq, rs) || overlap(rw, rq) || overlap(rw, rs)) return MT_ERR_ALIAS;
+  return launch_pack_mx(W, N, K, bits, (uint8_t*)q, (uint8_t*)scales,
+                        Launch{(cudaStream_t)stream, false});
 }
 
 mt_status mt_unpack_affine(const void* q, const void* scales, const void* biases, int N, int K,

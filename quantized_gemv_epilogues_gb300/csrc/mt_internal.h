@@ -87,6 +87,8 @@ mt_status launch_gemv(const GemvProblem& p, const Launch& l);
 // ---- packer
 mt_status launch_pack_affine(const float* W, int N, int K, int group, int bits, uint8_t* q,
                              uint16_t* s, uint16_t* b, const Launch& l);
+mt_status launch_pack_mx(const float* W, int N, int K, int bits, uint8_t* q, uint8_t* s,
+                         const Launch& l);
 mt_status launch_unpack_affine(const uint8_t* q, const uint16_t* s, const uint16_t* b, int N,
                                int K, int group, int bits, float* W, const Launch& l);
 

@@ -154,8 +154,24 @@ def device_bf16(tensor, seed: int, dist: Dist, offset: int = 0, stream=None) -> 
 # ---------------------------------------------------------------------------
 # Workloads (shapes and distributions of the five measured layer shapes)
 # ---------------------------------------------------------------------------
-FMT_BF16, FMT_AFFINE8, FMT_AFFINE4 = 0, 1, 2
-FMT_NAMES = {FMT_BF16: "bf16", FMT_AFFINE8: "affine8", FMT_AFFINE4: "affine4"}
+FMT_BF16, FMT_AFFINE8, FMT_AFFINE4, FMT_MXFP8, FMT_MXFP4 = 0, 1, 2, 3, 4
+FMT_NAMES = {FMT_BF16: "bf16", FMT_AFFINE8: "affine8", FMT_AFFINE4: "affine4", FMT_MXFP8: "mxfp8",
+             FMT_MXFP4: "mxfp4"}
+_FMT_BITS = {FMT_BF16: 16, FMT_AFFINE8: 8, FMT_AFFINE4: 4, FMT_MXFP8: 8, FMT_MXFP4: 4}
+
+
+def is_mx(fmt: int) -> bool:
+    return fmt in (FMT_MXFP8, FMT_MXFP4)
+
+
+def scale_bytes(fmt: int, n_weights: int, group: int) -> int:
+    """Scale (and bias) bytes of n_weights weights: affine 2 bf16 per group,
+    MX one E8M0 byte per 32, bf16 none."""
+    if fmt == FMT_BF16:
+        return 0
+    if is_mx(fmt):
+        return n_weights // 32
+    return 2 * 2 * (n_weights // group)
 
 
 @dataclass(frozen=True)
@@ -174,14 +190,12 @@ class Workload:
 
     @property
     def bits(self) -> int:
-        return {FMT_BF16: 16, FMT_AFFINE8: 8, FMT_AFFINE4: 4}[self.fmt]
+        return _FMT_BITS[self.fmt]
 
     def weight_bytes(self) -> int:
         """Packed weight + scale/bias bytes of one layer (gate, up, down)."""
         n_w = 3 * self.d * self.f
-        wb = n_w * self.bits // 8
-        sb = 0 if self.fmt == FMT_BF16 else 2 * 2 * (n_w // self.group)
-        return wb + sb
+        return n_w * self.bits // 8 + scale_bytes(self.fmt, n_w, self.group)
 
     def act_bytes(self) -> int:
         """Activation bytes of one layer: K1 reads v, r (2*M*d bf16) and the norm
@@ -203,6 +217,14 @@ LLAMA1B = Workload(2, "llama3.2-1b layer d2048 f8192 affine4 g64", 2048, 8192, 1
 QWEN15 = Workload(3, "qwen2.5-1.5b layer d1536 f8960 bf16", 1536, 8960, 1, FMT_BF16, 0, 1e-6)
 QWEN8B = Workload(4, "qwen3-8b stack d4096 f12288 affine8 g128 x36", 4096, 12288, 1, FMT_AFFINE8, 128,
                   1e-6, layers=36)
+
+
+# the Qwen3-8B layer with MX block-scaled weights (OCP MXFP8 / MXFP4, E8M0
+# scales per 32): a stack of distinct layers, timed through the single calls
+QWEN8B_MXFP8 = Workload(11, "qwen3-8b layer d4096 f12288 mxfp8", 4096, 12288, 1, FMT_MXFP8, 32, 1e-6,
+                        layers=8)
+QWEN8B_MXFP4 = Workload(12, "qwen3-8b layer d4096 f12288 mxfp4", 4096, 12288, 1, FMT_MXFP4, 32, 1e-6,
+                        layers=8)
 
 
 def sweep_point(group: int, M: int) -> Workload:
@@ -242,11 +264,11 @@ class ProjWorkload:
 
     @property
     def bits(self) -> int:
-        return {FMT_BF16: 16, FMT_AFFINE8: 8, FMT_AFFINE4: 4}[self.fmt]
+        return _FMT_BITS[self.fmt]
 
     def proj_weight_bytes(self, p: Projection) -> int:
         wb = p.N * p.K * self.bits // 8
-        sb = 0 if self.fmt == FMT_BF16 else 2 * 2 * p.N * (p.K // self.group)
+        sb = scale_bytes(self.fmt, p.N * p.K, self.group)
         return wb + sb + (2 * p.N if p.bias is not None else 0)
 
     def proj_act_bytes(self, p: Projection) -> int:

@@ -28,20 +28,25 @@ class DevLayer:
             self.sgu = self.bgu = self.sdn = self.bdn = None
         else:
             b = wl.bits
+            mx = synth.is_mx(wl.fmt)
+            sdt = torch.uint8 if mx else bf
             self.Wg = torch.empty(f, d * b // 8, dtype=torch.uint8, device="cuda")
             self.Wu = torch.empty_like(self.Wg)
             self.Wd = torch.empty(d, f * b // 8, dtype=torch.uint8, device="cuda")
-            self.sgu = torch.empty(2, f, d // g, dtype=bf, device="cuda")
-            self.bgu = torch.empty_like(self.sgu)
-            self.sdn = torch.empty(d, f // g, dtype=bf, device="cuda")
-            self.bdn = torch.empty_like(self.sdn)
+            self.sgu = torch.empty(2, f, d // g, dtype=sdt, device="cuda")
+            self.sdn = torch.empty(d, f // g, dtype=sdt, device="cuda")
+            self.bgu = None if mx else torch.empty_like(self.sgu)
+            self.bdn = None if mx else torch.empty_like(self.sdn)
             tmp = torch.empty(d * f, dtype=torch.float32, device="cuda")
-            for (dst, s_, b_, N, K, t) in ((self.Wg, self.sgu[0], self.bgu[0], f, d, synth.T_WG),
-                                           (self.Wu, self.sgu[1], self.bgu[1], f, d, synth.T_WU),
+            for (dst, s_, b_, N, K, t) in ((self.Wg, self.sgu[0], None if mx else self.bgu[0], f, d, synth.T_WG),
+                                           (self.Wu, self.sgu[1], None if mx else self.bgu[1], f, d, synth.T_WU),
                                            (self.Wd, self.sdn, self.bdn, d, f, synth.T_WD)):
                 W32 = tmp[:N * K].view(N, K)
                 synth.device_f32(W32, sd(t), wl.weight_dist)
-                mt.mt_pack_affine(W32, N, K, g, b, dst, s_, b_)
+                if mx:
+                    mt.mt_pack_mx(W32, N, K, b, dst, s_)
+                else:
+                    mt.mt_pack_affine(W32, N, K, g, b, dst, s_, b_)
             del tmp
         torch.cuda.synchronize()
 
@@ -49,6 +54,8 @@ class DevLayer:
         """Oracle-side weight rows [rows] of matrix `tensor` ([N][K])."""
         wl = self.wl
         W32 = np.stack([synth.host_f32(K, self.sd(tensor), wl.weight_dist, offset=int(n) * K) for n in rows])
+        if synth.is_mx(wl.fmt):
+            return oracle.Weight.from_f32_mx(W32, wl.bits)
         return oracle.Weight.from_f32(W32, wl.bits, wl.group)
 
 

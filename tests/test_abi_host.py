@@ -176,6 +176,26 @@ def test_linear_bias_validation(lib):
     assert call(y=w + 64) == ALIAS
     assert call(y=bias) == ALIAS
     assert call(y=bi + 32) == ALIAS
+    # MX formats: group 32, scales only
+    assert call(fmt=3, g=64, bi=None) == GROUP
+    assert call(fmt=4, g=32) == FORMAT                      # biases must be NULL
+    assert call(fmt=4, g=32, sc=None, bi=None) == NULL
+    assert call(fmt=5, g=32, bi=None) == FORMAT
+    assert call(fmt=3, g=32, bi=None, K=1000) == SHAPE      # 1000 % 32 != 0
+    assert call(fmt=3, g=32, bi=None, y=sc + 16) == ALIAS   # E8M0 scales: N * K/32 bytes
+
+
+def test_pack_mx_validation(lib):
+    f = lib.mt_pack_mx
+    f.restype = ctypes.c_int
+    f.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P]
+    W, q, s = A[:3]
+    assert f(None, 4, 256, 8, q, s, None) == NULL
+    assert f(W, 4, 256, 8, q, None, None) == NULL
+    assert f(W, 4, 256, 6, q, s, None) == FORMAT
+    assert f(W, 4, 100, 8, q, s, None) == SHAPE
+    assert f(W, 4, 256, 8, q + 4, s, None) == ALIGN
+    assert f(W, 4, 256, 8, q, q + 256, None) == ALIAS
 
 
 def test_pack_validation(lib):

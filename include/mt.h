@@ -206,6 +206,47 @@ mt_status mt_linear_bias(const void* x, const void* W, const void* scales,
                          mt_wfmt fmt, mt_dtype out_dtype, void* stream);
 
 /*
+ * Multi-row prefill (M > 8 activation rows, any M >= 1) of the same three
+ * GEMV epilogues as tensor-core GEMMs (tcgen05 with tensor-memory
+ * accumulators, TMA-fed activation tiles): a 128-output x 64-row tile per
+ * CTA, the gate and up tiles of a row range computed together and the SwiGLU
+ * applied before the only store.  meTile docs, "MLX-LM Backend", Dispatch
+ * Policy (multi-row shapes: a row-tiled dual GEMM with the SwiGLU in
+ * registers); "Compute-Graph Fusion", Automatic Gated Epilogues.
+ *   Arguments, layouts and results as mt_swiglu_gateup / mt_down_residual /
+ *   mt_linear_bias, plus a caller-owned device workspace of at least
+ *   mt_prefill_workspace_bytes(M, K, group) bytes (16-byte aligned; K is d
+ *   for gate/up, f for down) that holds the activations converted for the
+ *   tensor cores; it must not overlap any argument.  The call allocates
+ *   nothing and never synchronises.
+ * Formats: MT_W_AFFINE8, MT_W_AFFINE4 (group 32, 64 or 128).
+ * Limits: 1 <= M <= 2^20; K % 64 == 0 and K % group == 0; 64 <= K <= 65536;
+ *         1 <= N <= 2^20.  A workspace below the required size is
+ *         MT_ERR_SHAPE.  out_y may equal residual (bf16 output).
+ * Accumulation: each quantisation group's code . x sum is exact products
+ * with fp32 accumulation on the tensor cores (codes as fp16 q * 2^-24; x as
+ * fp16 scaled per activation row by a power of two, exact for every bf16
+ * value above 2^-28 of the row's maximum); scales, biases and the total are
+ * fp32.
+ */
+size_t mt_prefill_workspace_bytes(int M, int K, int group);
+mt_status mt_prefill_swiglu_gateup(const void* x, const void* Wg, const void* Wu,
+                                   const void* scales, const void* biases, int group,
+                                   void* out_h, int M, int d, int f, mt_wfmt fmt,
+                                   mt_dtype out_dtype, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+mt_status mt_prefill_down_residual(const void* h, const void* Wd, const void* scales,
+                                   const void* biases, int group, const void* residual,
+                                   void* out_y, int M, int f, int d, mt_wfmt fmt,
+                                   mt_dtype out_dtype, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+mt_status mt_prefill_linear_bias(const void* x, const void* W, const void* scales,
+                                 const void* biases, int group, const void* bias,
+                                 void* out_y, int M, int K, int N, mt_wfmt fmt,
+                                 mt_dtype out_dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
  * Affine group quantiser and packer (offline preparation; stream-ordered).
  *   W        : fp32 [N][K], device
  *   bits     : 8 or 4;  group : 32, 64 or 128;  K % group == 0

@@ -13,6 +13,10 @@ Calls (same names as the C ABI):
 * :func:`mt_down_residual` -- down GEMV with the residual added in its epilogue.
 * :func:`mt_linear_bias` -- projection GEMV with an optional bias (attention
   q/k/v/o, vocabulary projection).
+* :func:`mt_prefill_swiglu_gateup`, :func:`mt_prefill_down_residual`,
+  :func:`mt_prefill_linear_bias` -- the same epilogues for many activation
+  rows (prefill) on the tcgen05 tensor cores, with a caller-owned workspace
+  of :func:`mt_prefill_workspace_bytes` bytes.
 * :func:`mt_pack_affine` / :func:`mt_unpack_affine` -- affine group packer.
 * :func:`mt_pack_mx` -- MXFP8 / MXFP4 block-scaled packer (E8M0 scales).
 * :func:`mt_mlp_plan_create` / :func:`mt_mlp_plan_run` / :func:`mt_mlp_plan_destroy`
@@ -53,6 +57,10 @@ _SIGS = {
     "mt_pack_affine": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "mt_unpack_affine": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "mt_pack_mx": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "mt_prefill_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
+    "mt_prefill_swiglu_gateup": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, ctypes.c_size_t, _P]),
+    "mt_prefill_down_residual": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, ctypes.c_size_t, _P]),
+    "mt_prefill_linear_bias": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, ctypes.c_size_t, _P]),
     "mt_set_option": (_I, [_I, _I]),
     "mt_get_option": (_I, [_I]),
     "mt_status_string": (ctypes.c_char_p, [_I]),
@@ -178,6 +186,66 @@ def mt_linear_bias(x, W, scales, biases, group, bias, out_y, M=None, K=None, N=N
     _check(_lib.mt_linear_bias(_ptr(x), _ptr(W), _ptr(scales), _ptr(biases), int(group),
                                _ptr(bias), _ptr(out_y), M, K, N, int(fmt), od, _stream(stream)),
            "mt_linear_bias")
+
+
+def mt_prefill_workspace_bytes(M, K, group):
+    return int(_lib.mt_prefill_workspace_bytes(int(M), int(K), int(group)))
+
+
+def _ws(workspace, M, K, group):
+    need = mt_prefill_workspace_bytes(M, K, group)
+    if workspace is None:
+        raise TypeError(f"a device workspace of at least {need} bytes is required")
+    nbytes = workspace.numel() * workspace.element_size() if not isinstance(workspace, int) else need
+    return _ptr(workspace), nbytes
+
+
+def mt_prefill_swiglu_gateup(x, Wg, Wu, scales, biases, group, out_h, workspace, M=None, d=None, f=None,
+                             fmt=None, out_dtype=None, workspace_bytes=None, stream=None):
+    if M is None or d is None:
+        M, d = _rows_cols(x)
+    if f is None:
+        f = _rows_cols(out_h)[1]
+    if fmt is None:
+        raise TypeError("fmt (MT_W_AFFINE8 / MT_W_AFFINE4) is required")
+    od = _odt(out_h, out_dtype) if not isinstance(out_h, int) else (out_dtype or MT_BF16)
+    wp, wb = _ws(workspace, M, d, group)
+    _check(_lib.mt_prefill_swiglu_gateup(_ptr(x), _ptr(Wg), _ptr(Wu), _ptr(scales), _ptr(biases), int(group),
+                                         _ptr(out_h), M, d, f, int(fmt), od, wp,
+                                         workspace_bytes if workspace_bytes is not None else wb, _stream(stream)),
+           "mt_prefill_swiglu_gateup")
+
+
+def mt_prefill_down_residual(h, Wd, scales, biases, group, residual, out_y, workspace, M=None, f=None, d=None,
+                             fmt=None, out_dtype=None, workspace_bytes=None, stream=None):
+    if M is None or f is None:
+        M, f = _rows_cols(h)
+    if d is None:
+        d = _rows_cols(out_y)[1]
+    if fmt is None:
+        raise TypeError("fmt (MT_W_AFFINE8 / MT_W_AFFINE4) is required")
+    od = _odt(out_y, out_dtype) if not isinstance(out_y, int) else (out_dtype or MT_BF16)
+    wp, wb = _ws(workspace, M, f, group)
+    _check(_lib.mt_prefill_down_residual(_ptr(h), _ptr(Wd), _ptr(scales), _ptr(biases), int(group),
+                                         _ptr(residual), _ptr(out_y), M, f, d, int(fmt), od, wp,
+                                         workspace_bytes if workspace_bytes is not None else wb, _stream(stream)),
+           "mt_prefill_down_residual")
+
+
+def mt_prefill_linear_bias(x, W, scales, biases, group, bias, out_y, workspace, M=None, K=None, N=None, fmt=None,
+                           out_dtype=None, workspace_bytes=None, stream=None):
+    if M is None or K is None:
+        M, K = _rows_cols(x)
+    if N is None:
+        N = _rows_cols(out_y)[1]
+    if fmt is None:
+        raise TypeError("fmt (MT_W_AFFINE8 / MT_W_AFFINE4) is required")
+    od = _odt(out_y, out_dtype) if not isinstance(out_y, int) else (out_dtype or MT_BF16)
+    wp, wb = _ws(workspace, M, K, group)
+    _check(_lib.mt_prefill_linear_bias(_ptr(x), _ptr(W), _ptr(scales), _ptr(biases), int(group), _ptr(bias),
+                                       _ptr(out_y), M, K, N, int(fmt), od, wp,
+                                       workspace_bytes if workspace_bytes is not None else wb, _stream(stream)),
+           "mt_prefill_linear_bias")
 
 
 def mt_pack_affine(W, N, K, group, bits, q, scales, biases, stream=None):

@@ -1,0 +1,673 @@
+// k_prefill.cu - multi-row prefill (M > 8 activation rows) of the gate/up +
+// SwiGLU, down + residual and projection + bias GEMMs over affine INT8/INT4
+// weights, on the fifth-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// meTile docs, "MLX-LM Backend", Dispatch Policy (multi-row shapes take a
+// row-tiled dual GEMM: the gate and up tiles share each activation tile and
+// the SwiGLU is applied in registers before the only store; affine
+// w = scale * q + bias per group of 32/64/128 along K, fp32 accumulation);
+// "Compute-Graph Fusion", Automatic Gated Epilogues (the residual and bias
+// epilogues).
+//
+// GB300 design:
+//  * One CTA computes a tile of 128 weight rows (output features) x 64
+//    activation rows (tokens): D[128 x 64] = W_tile[128 x K] . X_tile[64 x K]^T
+//    with tcgen05.mma (cta_group::1, M = 128, N = 64, K = 16, fp16 operands,
+//    fp32 accumulators in tensor memory), one accumulator per weight matrix
+//    (two for gate/up).
+//  * The affine codes enter the MMA exactly: the fp16 bit pattern 0x00qq is
+//    q * 2^-24 (a subnormal), so one byte permute per two codes (INT8) or a
+//    mask and permute (INT4) builds the operand.  Four converter warps load
+//    the codes from global memory (one weight row per thread, one K block
+//    ahead in registers) and write them into shared memory in the MMA's
+//    128-byte-swizzled K-major layout.
+//  * The activations are converted once per call (prefill_x_kernel) to fp16
+//    scaled per token row by 2^e_m (max|x_m| 2^e_m in [2^14, 2^15): every
+//    bf16 value above 2^-28 of its row's maximum is exact), and their group
+//    sums X'_g = sum_{k in g} x 2^e_m are kept in fp32.  TMA (2D tiled,
+//    SWIZZLE_128B) brings each 64 x 64 fp16 tile into shared memory.
+//  * Each quantisation group accumulates into its own tensor-memory buffer
+//    (two buffers, alternating): the epilogue warpgroup reads a finished
+//    group's accumulator with tcgen05.ld while the MMA fills the other, and
+//    adds s * 2^24 * D + b * X'_g into fp32 registers (one output row per
+//    thread, 64 tokens each).  At the end the row scale 2^-e_m is undone and
+//    the SwiGLU, residual or bias epilogue is applied before the only store.
+//  * Pipeline: four shared-memory stages of (x tile, weight tiles) with
+//    mbarriers: x_full (TMA transaction bytes), w_full (converters),
+//    stage_free (tcgen05.commit after the MMAs that read the stage); two
+//    accumulator buffers with acc_full (tcgen05.commit) and acc_free
+//    (epilogue).  Every wait is bounded (~1 s): on expiry the thread records
+//    MT_ERR_TIMEOUT in the device error word, the CTA stops, drains its
+//    outstanding copies and MMAs, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "k_gemv.cuh"
+
+namespace mt {
+
+constexpr int PF_ROWS = 128;       // weight rows per tile (MMA M)
+constexpr int PF_COLS = 64;        // activation rows per tile (MMA N)
+constexpr int PF_KB = 64;          // K per stage (one 128-byte swizzle row of fp16)
+constexpr int PF_STAGES = 4;
+constexpr int PF_EPI_WARPS = 4;    // warps 0-3: epilogue (tensor-memory lanes 0-127)
+constexpr int PF_CONV_WARPS = 4;   // warps 4-7: converters (+ the TMA producer thread)
+constexpr int PF_THREADS = 32 * (PF_EPI_WARPS + PF_CONV_WARPS + 1);  // + warp 8: MMA issuer
+constexpr int PF_X_TILE = PF_COLS * PF_KB * 2;   // 8 KB
+constexpr int PF_W_TILE = PF_ROWS * PF_KB * 2;   // 16 KB
+
+struct PrefillArgs {
+  const uint8_t* W0;  // gate (kind 0) or the weight (kind 1): codes [N][row_bytes]
+  const uint8_t* W1;  // up (kind 0)
+  const uint16_t* s0;
+  const uint16_t* b0;
+  const uint16_t* s1;
+  const uint16_t* b1;
+  const float* XgT;   // [G][Mp] group sums of the scaled activations (Mp = 64 n_ctiles)
+  const float* einv;  // [M] 2^-e_m
+  const uint16_t* res;  // addend (kind 1) or nullptr
+  int res_ld;           // its row stride in elements (0: one bias row for all m)
+  void* out;            // [M][N]
+  int out_f32;
+  int M, K, N, group, lg_group, G, KB, row_bytes;
+  int n_ctiles;         // ceil(M / 64)
+  int* err;             // device error word
+};
+
+// ------------------------------------------------------------- PTX wrappers
+
+// Shared-memory matrix descriptor of a K-major fp16 tile whose rows are 128
+// bytes, stored with the 128-byte swizzle (16-byte chunk c of row r at chunk
+// c ^ (r & 7)); 8-row core groups 1024 bytes apart.  The tile starts on a
+// 1024-byte boundary; a K step of 16 elements advances the start by 32 bytes.
+__device__ __forceinline__ uint64_t pf_desc_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                             // leading offset (unused here)
+  d |= (uint64_t)(1024 >> 4) << 32;                   // stride offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                             // descriptor version
+  d |= (uint64_t)2 << 61;                             // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: fp32 accumulator, fp16 A and B, both K-major,
+// N = 64, M = 128.
+constexpr uint32_t PF_IDESC = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(PF_COLS >> 3) << 17) |
+                              ((uint32_t)(PF_ROWS >> 4) << 24);
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(PF_IDESC), "r"(accumulate)
+      : "memory");
+}
+
+// The mbarrier tracks the completion of every tcgen05.mma this thread issued.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's tensor-memory lane at taddr
+// (and at taddr2), the wait for the loads inside the same statement so that
+// no use of the registers can be scheduled before it.
+__device__ __forceinline__ void tc_ld16_wait(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tc_ld16x2_wait(uint32_t ta, uint32_t tb, float (&va)[16], float (&vb)[16]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    va[i] = __uint_as_float(r[i]);
+    vb[i] = __uint_as_float(r[16 + i]);
+  }
+}
+
+// 2D tiled TMA load of box {64 elements, 64 rows} at (k0, m0), completing on bar.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int k0, int m0, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(k0), "r"(m0), "r"(bar)
+      : "memory");
+}
+
+// ---------------------------------------------------------- activations pass
+
+// One CTA per activation row m (grid: M rounded up to the column tile, Mp):
+// e_m from the row's maximum magnitude, the row as fp16 x * 2^e_m (round to
+// nearest), the group sums of x * 2^e_m (fp32, in a fixed order; [G][Mp]) and
+// 2^-e_m.
+__global__ void __launch_bounds__(256) prefill_x_kernel(const uint16_t* __restrict__ x, int M, int K, int group,
+                                                        __half* __restrict__ x16, float* __restrict__ XgT,
+                                                        float* __restrict__ einv) {
+  const int m = blockIdx.x;  // rows M .. Mp-1 only zero their group sums and scale
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = K / group, Mp = gridDim.x;
+  if (m >= M) {
+    for (int g = tid; g < G; g += 256) XgT[(size_t)g * Mp + m] = 0.f;
+    if (tid == 0) einv[m] = 0.f;
+    return;
+  }
+  const uint16_t* row = x + (size_t)m * K;
+  __shared__ uint32_t wmax[8];
+  uint32_t mx = 0;  // bf16 magnitude bits order like the magnitudes
+  for (int k = tid; k < K; k += 256) mx = max(mx, (uint32_t)(row[k] & 0x7FFFu));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) wmax[warp] = mx;
+  __syncthreads();
+  mx = wmax[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) mx = max(mx, wmax[w]);
+  // max in [2^(E-127), 2^(E-126)) for bf16 exponent field E: e = 14 - (E - 127)
+  const int E = (int)(mx >> 7);
+  const int e = (mx == 0 || E == 0xFF) ? 0 : max(-100, min(100, 14 - (E - 127)));
+  const float sc = exp2i(e);
+  for (int k = tid; k < K; k += 256) x16[(size_t)m * K + k] = __float2half_rn(bf16f(row[k]) * sc);
+  for (int g = warp; g < G; g += 8) {
+    float s = 0.f;
+    for (int j = lane; j < group; j += 32) s += bf16f(row[g * group + j]) * sc;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) XgT[(size_t)g * Mp + m] = s;
+  }
+  if (tid == 0) einv[m] = exp2i(-e);
+}
+
+// ------------------------------------------------------------- the GEMM
+
+// Codes of one weight row for one K block of 64 (INT8: 64 bytes, INT4: 32)
+// as fp16 subnormals q * 2^-24, written into the swizzled tile row r.
+template <int FMT>
+__device__ __forceinline__ void pf_convert_row(const uint4 (&c)[FMT == FMT_A8 ? 4 : 2], unsigned char* tile, int r) {
+  unsigned char* rowp = tile + r * 128;
+  const int sw = r & 7;
+  if constexpr (FMT == FMT_A8) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {  // 16 codes -> chunks 2u, 2u+1
+      const uint32_t w[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t a = w[2 * h], b = w[2 * h + 1];
+        const uint4 o = make_uint4(__byte_perm(a, 0u, 0x4140), __byte_perm(a, 0u, 0x4342),
+                                   __byte_perm(b, 0u, 0x4140), __byte_perm(b, 0u, 0x4342));
+        *reinterpret_cast<uint4*>(rowp + (((2 * u + h) ^ sw) << 4)) = o;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {  // 32 codes -> chunks 4u .. 4u+3 (one word each)
+      const uint32_t w[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        // byte j of w holds code 2j (bits 0..3) and 2j+1 (bits 4..7)
+        const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
+        const uint4 o = make_uint4(__byte_perm(lo, hi, 0x4400) & 0x00FF00FFu, __byte_perm(lo, hi, 0x5511) & 0x00FF00FFu,
+                                   __byte_perm(lo, hi, 0x6622) & 0x00FF00FFu, __byte_perm(lo, hi, 0x7733) & 0x00FF00FFu);
+        *reinterpret_cast<uint4*>(rowp + (((4 * u + i) ^ sw) << 4)) = o;
+      }
+    }
+  }
+}
+
+// Shape of the code registers of one converter thread.
+template <int FMT, int KIND>
+struct PfShape {
+  static constexpr int NW = KIND == 0 ? 2 : 1;  // weight matrices
+  static constexpr int CU = FMT == FMT_A8 ? 4 : 2;  // 16-byte code loads per row and K block
+};
+
+template <int FMT, int KIND>
+__global__ void __launch_bounds__(PF_THREADS, 1)
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillArgs a) {
+  using SH = PfShape<FMT, KIND>;
+  constexpr int NW = SH::NW;
+  constexpr int S = PF_STAGES;
+  constexpr int STAGE = PF_X_TILE + NW * PF_W_TILE;  // multiple of 1024
+  constexpr uint32_t NCOLS = 2 * NW * PF_COLS;       // two accumulator buffers
+  constexpr int CB = SH::CU * 16;                    // code bytes per row and K block
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  __shared__ __align__(8) uint64_t bars[3 * S + 5];
+  __shared__ uint32_t tmem_sh;
+  __shared__ int abort_sh;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rt = blockIdx.x / a.n_ctiles, ct = blockIdx.x - rt * a.n_ctiles;
+  const int n0 = rt * PF_ROWS, m0 = ct * PF_COLS;
+  const int KB = a.KB, G = a.G, Mp = a.n_ctiles * PF_COLS;
+  auto x_full = [&](int st) { return smem_u32(&bars[st]); };
+  auto w_full = [&](int st) { return smem_u32(&bars[S + st]); };
+  auto stage_free = [&](int st) { return smem_u32(&bars[2 * S + st]); };
+  auto acc_full = [&](int b) { return smem_u32(&bars[3 * S + b]); };
+  auto acc_free = [&](int b) { return smem_u32(&bars[3 * S + 2 + b]); };
+  const uint32_t mma_done = smem_u32(&bars[3 * S + 4]);
+  auto xtile = [&](int st) { return smem + (size_t)st * STAGE; };
+  auto wtile = [&](int st, int mat) { return smem + (size_t)st * STAGE + PF_X_TILE + mat * PF_W_TILE; };
+
+  if (tid == 0) {
+    for (int st = 0; st < S; ++st) {
+      mbar_init(x_full(st), 1);
+      mbar_init(w_full(st), 32 * PF_CONV_WARPS);
+      mbar_init(stage_free(st), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_free(b), 32 * PF_EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    abort_sh = 0;
+    mbar_fence_init();
+  }
+  if (warp == 8) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_sh)),
+                 "r"(NCOLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_sh;
+  volatile int* abort_flag = &abort_sh;
+  auto fail = [&]() {
+    atomicExch(a.err, (int)MT_ERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp >= PF_EPI_WARPS && warp < PF_EPI_WARPS + PF_CONV_WARPS) {
+    // ---- converters: weight row n0 + c of each matrix; thread c == 0 also
+    // issues the x tile copies
+    const int c = tid - 32 * PF_EPI_WARPS;
+    const int n = n0 + c;
+    const bool okr = n < a.N;
+    const uint8_t* wr[NW];
+#pragma unroll
+    for (int mat = 0; mat < NW; ++mat) wr[mat] = (mat ? a.W1 : a.W0) + (size_t)(okr ? n : 0) * a.row_bytes;
+    uint4 bufA[SH::NW][SH::CU], bufB[SH::NW][SH::CU];
+    auto load = [&](int kb, uint4 (&buf)[SH::NW][SH::CU]) {
+#pragma unroll
+      for (int mat = 0; mat < NW; ++mat)
+#pragma unroll
+        for (int u = 0; u < SH::CU; ++u)
+          buf[mat][u] = (okr && kb < KB) ? ldg_stream(wr[mat] + (size_t)kb * CB + u * 16) : make_uint4(0, 0, 0, 0);
+    };
+    int issued = 0;
+    auto step = [&](int kb, const uint4 (&cur)[SH::NW][SH::CU], uint4 (&nxt)[SH::NW][SH::CU]) -> bool {
+      load(kb + 1, nxt);
+      const int st = kb % S;
+      if (kb >= S && !mbar_wait_bounded(stage_free(st), ((kb / S) + 1) & 1)) return false;
+      if (c == 0) {
+        mbar_arrive_expect_tx(x_full(st), PF_X_TILE);
+        tma_load_2d(smem_u32(xtile(st)), &xmap, kb * PF_KB, m0, x_full(st));
+        ++issued;
+      }
+#pragma unroll
+      for (int mat = 0; mat < NW; ++mat) pf_convert_row<FMT>(cur[mat], wtile(st, mat), c);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor core reads
+      mbar_arrive(w_full(st));
+      return true;
+    };
+    load(0, bufA);
+    for (int kb = 0; kb < KB; kb += 2) {
+      if (*abort_flag) break;
+      if (!step(kb, bufA, bufB)) { fail(); break; }
+      if (kb + 1 >= KB) break;
+      if (*abort_flag) break;
+      if (!step(kb + 1, bufB, bufA)) { fail(); break; }
+    }
+    if (c == 0) {  // copies still in flight (only after an abort) land before the CTA ends
+      for (int kb = max(0, issued - S); kb < issued; ++kb) (void)mbar_wait_bounded(x_full(kb % S), (kb / S) & 1);
+    }
+  } else if (warp == 8) {
+    // ---- MMA issuer
+    if (lane == 0) {
+      const int group = a.group;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int st = kb % S;
+        const uint32_t ph = (kb / S) & 1;
+        if (!mbar_wait_bounded(x_full(st), ph) || !mbar_wait_bounded(w_full(st), ph)) { fail(); break; }
+        tc_fence_after();
+        const uint64_t xd = pf_desc_sw128(smem_u32(xtile(st)));
+        uint64_t wd[NW];
+#pragma unroll
+        for (int mat = 0; mat < NW; ++mat) wd[mat] = pf_desc_sw128(smem_u32(wtile(st, mat)));
+        bool ok = true;
+#pragma unroll
+        for (int j = 0; j < PF_KB / 16; ++j) {
+          const int k = kb * PF_KB + 16 * j;
+          const int gi = k >> a.lg_group, b = gi & 1;
+          const bool first = (k & (group - 1)) == 0;
+          if (first && gi >= 2) {
+            if (!mbar_wait_bounded(acc_free(b), ((gi >> 1) - 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int mat = 0; mat < NW; ++mat)
+            tc_mma(tbase + (uint32_t)((b * NW + mat) * PF_COLS), wd[mat] + 2 * j, xd + 2 * j, first ? 0u : 1u);
+          if (((k + 16) & (group - 1)) == 0) tc_commit(acc_full(b));
+        }
+        tc_commit(stage_free(st));
+        if (!ok) { fail(); break; }
+        if (*abort_flag) break;
+      }
+      tc_commit(mma_done);  // completes when every MMA issued above has
+      (void)mbar_wait_bounded(mma_done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue warpgroup: output row n0 + tid, 64 activation rows
+    const int n = n0 + tid;
+    const bool okr = n < a.N;
+    const size_t sbo = (size_t)(okr ? n : 0) * G;
+    float acc[NW][PF_COLS];
+#pragma unroll
+    for (int mat = 0; mat < NW; ++mat)
+#pragma unroll
+      for (int j = 0; j < PF_COLS; ++j) acc[mat][j] = 0.f;
+    const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
+    constexpr float TWO24 = 16777216.f;  // the codes enter the MMA as q * 2^-24
+    float sv[NW], bv[NW];
+#pragma unroll
+    for (int mat = 0; mat < NW; ++mat) {
+      sv[mat] = okr ? bf16f((mat ? a.s1 : a.s0)[sbo]) * TWO24 : 0.f;
+      bv[mat] = okr ? bf16f((mat ? a.b1 : a.b0)[sbo]) : 0.f;
+    }
+    bool aborted = false;
+    for (int gi = 0; gi < G; ++gi) {
+      const int b = gi & 1;
+      // the next group's scales and biases, ahead of the wait
+      float sn[NW], bn[NW];
+#pragma unroll
+      for (int mat = 0; mat < NW; ++mat) {
+        const bool more = okr && gi + 1 < G;
+        sn[mat] = more ? bf16f((mat ? a.s1 : a.s0)[sbo + gi + 1]) * TWO24 : 0.f;
+        bn[mat] = more ? bf16f((mat ? a.b1 : a.b0)[sbo + gi + 1]) : 0.f;
+      }
+      if (!mbar_wait_bounded(acc_full(b), (gi >> 1) & 1)) { fail(); aborted = true; break; }
+      tc_fence_after();
+      const float* xg = a.XgT + (size_t)gi * Mp + m0;
+#pragma unroll
+      for (int q = 0; q < PF_COLS / 16; ++q) {
+        float d0[16], d1[16];
+        const uint32_t t0 = lane_base + (uint32_t)(b * NW * PF_COLS + q * 16);
+        if constexpr (NW == 2)
+          tc_ld16x2_wait(t0, t0 + PF_COLS, d0, d1);
+        else
+          tc_ld16_wait(t0, d0);
+        float X[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(xg + q * 16) + i);
+          X[4 * i] = v.x; X[4 * i + 1] = v.y; X[4 * i + 2] = v.z; X[4 * i + 3] = v.w;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          acc[0][q * 16 + j] = fmaf(sv[0], d0[j], fmaf(bv[0], X[j], acc[0][q * 16 + j]));
+          if constexpr (NW == 2) acc[NW - 1][q * 16 + j] = fmaf(sv[NW - 1], d1[j], fmaf(bv[NW - 1], X[j], acc[NW - 1][q * 16 + j]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_free(b));
+#pragma unroll
+      for (int mat = 0; mat < NW; ++mat) { sv[mat] = sn[mat]; bv[mat] = bn[mat]; }
+      if (*abort_flag) { aborted = true; break; }
+    }
+    if (!aborted && okr) {
+#pragma unroll
+      for (int j = 0; j < PF_COLS; ++j) {
+        const int m = m0 + j;
+        if (m < a.M) {
+          const float ei = a.einv[m];
+          const float v0 = acc[0][j] * ei;
+          float outv;
+          if constexpr (KIND == 0) {
+            const float v1 = acc[NW - 1][j] * ei;
+            outv = v0 / (1.0f + expf(-v0)) * v1;  // silu(gate) * up
+          } else {
+            outv = a.res ? v0 + bf16f(a.res[(size_t)m * a.res_ld + n]) : v0;  // + residual or bias
+          }
+          if (a.out_f32)
+            static_cast<float*>(a.out)[(size_t)m * a.N + n] = outv;
+          else
+            static_cast<uint16_t*>(a.out)[(size_t)m * a.N + n] = f2bf(outv);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 8) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(NCOLS));
+}
+
+// ---------------------------------------------------------------- host side
+
+namespace {
+
+size_t al1k(size_t v) { return (v + 1023) / 1024 * 1024; }
+
+// Workspace: x16 [M][K] fp16, XgT [G][Mp] fp32, einv [Mp] fp32.
+size_t prefill_ws_bytes(long M, long K, long group) {
+  const long Mp = (M + PF_COLS - 1) / PF_COLS * PF_COLS;
+  return al1k((size_t)M * K * 2) + al1k((size_t)(K / group) * Mp * 4) + al1k((size_t)Mp * 4);
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+template <int FMT, int KIND>
+mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
+  constexpr int NW = KIND == 0 ? 2 : 1;
+  const int M = p.M, K = p.K, N = p.N, group = p.group;
+  const int n_ctiles = (M + PF_COLS - 1) / PF_COLS, Mp = n_ctiles * PF_COLS;
+  const int n_rtiles = (N + PF_ROWS - 1) / PF_ROWS;
+  const int G = K / group;
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  __half* x16 = reinterpret_cast<__half*>(w);
+  float* XgT = reinterpret_cast<float*>(w + al1k((size_t)M * K * 2));
+  float* einv = reinterpret_cast<float*>(w + al1k((size_t)M * K * 2) + al1k((size_t)G * Mp * 4));
+  int* err = device_error_ptr();
+  if (!err) return MT_ERR_CUDA;
+
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return cuda_fail(cudaErrorNotSupported);
+  CUtensorMap xmap;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)PF_KB, (cuuint32_t)PF_COLS};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+      CUDA_SUCCESS)
+    return cuda_fail(cudaErrorInvalidValue);
+
+  PrefillArgs a = {};
+  a.W0 = static_cast<const uint8_t*>(p.W0);
+  a.W1 = static_cast<const uint8_t*>(p.W1);
+  a.s0 = p.s0; a.b0 = p.b0; a.s1 = p.s1; a.b1 = p.b1;
+  a.XgT = XgT;
+  a.einv = einv;
+  a.res = p.res;
+  a.res_ld = p.res_ld;
+  a.out = p.out;
+  a.out_f32 = p.out_f32 ? 1 : 0;
+  a.M = M; a.K = K; a.N = N; a.group = group;
+  a.lg_group = group == 32 ? 5 : (group == 64 ? 6 : 7);
+  a.G = G;
+  a.KB = K / PF_KB;
+  a.row_bytes = FMT == FMT_A8 ? K : K / 2;
+  a.n_ctiles = n_ctiles;
+  a.err = err;
+
+  mt_status st = launch(prefill_x_kernel, dim3(Mp), dim3(256), 0, l, p.x, M, K, group, x16, XgT, einv);
+  if (st != MT_OK) return st;
+  const size_t smem = 1024 + (size_t)PF_STAGES * (PF_X_TILE + NW * PF_W_TILE);
+  auto kern = prefill_gemm_kernel<FMT, KIND>;
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (dev >= 64 || !attr_set[dev]) {
+      ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (ce != cudaSuccess) return cuda_fail(ce);
+      if (dev < 64) attr_set[dev] = true;
+    }
+  }
+  return launch(kern, dim3((unsigned)(n_rtiles * n_ctiles)), dim3(PF_THREADS), smem, l, xmap, a);
+}
+
+mt_status launch_prefill(const GemvProblem& p, void* ws, const Launch& l) {
+  if (p.fmt == MT_W_AFFINE8)
+    return p.kind == Kind::GateUp ? run_prefill<FMT_A8, 0>(p, ws, l) : run_prefill<FMT_A8, 1>(p, ws, l);
+  if (p.fmt == MT_W_AFFINE4)
+    return p.kind == Kind::GateUp ? run_prefill<FMT_A4, 0>(p, ws, l) : run_prefill<FMT_A4, 1>(p, ws, l);
+  return MT_ERR_FORMAT;
+}
+
+}  // namespace mt
+
+// ------------------------------------------------------------------ C ABI
+
+using namespace mt;
+
+namespace {
+
+bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+struct Rg {
+  uintptr_t lo, hi;
+};
+Rg rg(const void* p, size_t n) { return Rg{(uintptr_t)p, (uintptr_t)p + n}; }
+bool ovl(Rg a, Rg b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Shared validation and dispatch of the three prefill calls.  W1 is the up
+// matrix (gate/up) or nullptr; the addend is the residual (ld = N) or the
+// bias (ld = 0) or nullptr.
+mt_status prefill_call(Kind kind, const void* x, const void* W0, const void* W1, const void* scales,
+                       const void* biases, int group, const void* addend, int addend_ld, void* out, int M,
+                       int K, int N, mt_wfmt fmt, mt_dtype out_dtype, void* ws, size_t ws_bytes, void* stream) {
+  if (fmt != MT_W_AFFINE8 && fmt != MT_W_AFFINE4) return MT_ERR_FORMAT;
+  if (out_dtype != MT_BF16 && out_dtype != MT_F32) return MT_ERR_FORMAT;
+  if (!x || !W0 || (kind == Kind::GateUp && !W1) || !scales || !biases || !out || !ws) return MT_ERR_NULL;
+  if (group != 32 && group != 64 && group != 128) return MT_ERR_GROUP;
+  if (M < 1 || M > (1 << 20) || K < PF_KB || K > 65536 || K % PF_KB || K % group || N < 1 || N > (1 << 20))
+    return MT_ERR_SHAPE;
+  if (ws_bytes < prefill_ws_bytes(M, K, group)) return MT_ERR_SHAPE;
+  if (!al16(x) || !al16(W0) || !al16(W1) || !al16(scales) || !al16(biases) || !al16(out) || !al16(ws) ||
+      !al16(addend))
+    return MT_ERR_ALIGN;
+  const int NW = kind == Kind::GateUp ? 2 : 1;
+  const size_t wb = (size_t)N * K / (fmt == MT_W_AFFINE8 ? 1 : 2);
+  const size_t sbb = (size_t)NW * N * (K / group) * 2;
+  const Rg ro = rg(out, (size_t)M * N * (out_dtype == MT_F32 ? 4 : 2));
+  const Rg rw = rg(ws, prefill_ws_bytes(M, K, group));
+  const Rg rx = rg(x, (size_t)M * K * 2), rw0 = rg(W0, wb), rw1 = rg(W1, W1 ? wb : 0);
+  const Rg rs = rg(scales, sbb), rb = rg(biases, sbb);
+  const Rg ra = rg(addend, !addend ? 0 : (addend_ld ? (size_t)M * N * 2 : (size_t)N * 2));
+  if (ovl(ro, rx) || ovl(ro, rw0) || ovl(ro, rw1) || ovl(ro, rs) || ovl(ro, rb) || ovl(ro, rw)) return MT_ERR_ALIAS;
+  if (ovl(rw, rx) || ovl(rw, rw0) || ovl(rw, rw1) || ovl(rw, rs) || ovl(rw, rb) || ovl(rw, ra)) return MT_ERR_ALIAS;
+  // the residual may be the output itself (each element read, then written, by one thread)
+  if (ovl(ro, ra) && !(addend_ld && addend == out && out_dtype == MT_BF16)) return MT_ERR_ALIAS;
+  GemvProblem p = {};
+  p.kind = kind;
+  p.fmt = fmt;
+  p.M = M; p.K = K; p.N = N; p.group = group;
+  p.x = (const uint16_t*)x;
+  p.W0 = W0; p.W1 = W1;
+  const size_t plane = (size_t)N * (K / group);
+  p.s0 = (const uint16_t*)scales;
+  p.b0 = (const uint16_t*)biases;
+  if (kind == Kind::GateUp) {
+    p.s1 = (const uint16_t*)scales + plane;
+    p.b1 = (const uint16_t*)biases + plane;
+  }
+  p.res = (const uint16_t*)addend;
+  p.res_ld = addend_ld;
+  p.out = out;
+  p.out_f32 = out_dtype == MT_F32;
+  return launch_prefill(p, ws, Launch{(cudaStream_t)stream, false});
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mt_prefill_workspace_bytes(int M, int K, int group) {
+  if (M < 1 || K < 1 || (group != 32 && group != 64 && group != 128)) return 0;
+  return prefill_ws_bytes(M, K, group);
+}
+
+mt_status mt_prefill_swiglu_gateup(const void* x, const void* Wg, const void* Wu, const void* scales,
+                                   const void* biases, int group, void* out_h, int M, int d, int f,
+                                   mt_wfmt fmt, mt_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  return prefill_call(Kind::GateUp, x, Wg, Wu, scales, biases, group, nullptr, 0, out_h, M, d, f, fmt, out_dtype,
+                      workspace, workspace_bytes, stream);
+}
+
+mt_status mt_prefill_down_residual(const void* h, const void* Wd, const void* scales, const void* biases,
+                                   int group, const void* residual, void* out_y, int M, int f, int d,
+                                   mt_wfmt fmt, mt_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  if (!residual) return MT_ERR_NULL;
+  return prefill_call(Kind::Down, h, Wd, nullptr, scales, biases, group, residual, d, out_y, M, f, d, fmt,
+                      out_dtype, workspace, workspace_bytes, stream);
+}
+
+mt_status mt_prefill_linear_bias(const void* x, const void* W, const void* scales, const void* biases, int group,
+                                 const void* bias, void* out_y, int M, int K, int N, mt_wfmt fmt,
+                                 mt_dtype out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return prefill_call(Kind::Down, x, W, nullptr, scales, biases, group, bias, 0, out_y, M, K, N, fmt, out_dtype,
+                      workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"

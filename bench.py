@@ -660,6 +660,98 @@ def run_projections(args, torch, synth, mt, dev):
     return 0
 
 
+def bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["bf16_tflops"]), "measured (bf16 dense burst; fp16 runs at the same rate)"
+    return 1900.0, "fallback"
+
+
+def run_prefill(args, torch, synth, mt, dev):
+    """Multi-row prefill of the Qwen3-8B layer (d=4096, f=12288, affine INT8
+    g128) on the tcgen05 GEMMs: gate/up + SwiGLU and down + residual for M
+    activation rows, three distinct layers cycled (455 MB of weights, past the
+    L2).  Per M: us per layer, TFLOP/s (6 M d f flops per layer) and effective
+    GB/s.  The JSON line's value is the TFLOP/s at the largest M."""
+    hbm, hbm_kind = measured_peaks()
+    tpk, tpk_kind = bf16_peak()
+    points = []
+    n_layers = 3
+    for M in ((args.rows,) if args.rows else (16, 64, 256, 1024, 4096)):
+        wl = synth.QWEN8B.with_(M=M, layers=n_layers)
+        st = Stack(wl, dev)
+        d, f, g = wl.d, wl.f, wl.group
+        bf = torch.bfloat16
+        x = torch.empty(M, d, dtype=bf, device=dev)
+        hin = torch.empty(M, f, dtype=bf, device=dev)
+        res = torch.empty(M, d, dtype=bf, device=dev)
+        synth.device_bf16(x, synth.seed_for(wl.wid, M, synth.T_X), synth.ACT)
+        synth.device_bf16(hin, synth.seed_for(wl.wid, M, synth.T_H), synth.ACT)
+        synth.device_bf16(res, synth.seed_for(wl.wid, M, synth.T_RES3), synth.ACT)
+        h = torch.empty(M, f, dtype=bf, device=dev)
+        y = torch.empty(M, d, dtype=bf, device=dev)
+        ws = torch.empty(max(mt.mt_prefill_workspace_bytes(M, d, g), mt.mt_prefill_workspace_bytes(M, f, g)),
+                         dtype=torch.uint8, device=dev)
+
+        def gateup():
+            for L in st.layers:
+                mt.mt_prefill_swiglu_gateup(x, L["Wg"], L["Wu"], L["sgu"], L["bgu"], g, h, ws, fmt=wl.fmt)
+
+        def down():
+            for L in st.layers:
+                mt.mt_prefill_down_residual(hin, L["Wd"], L["sd"], L["bd"], g, res, y, ws, fmt=wl.fmt)
+
+        def both():
+            gateup()
+            down()
+
+        reps = max(3, min(args.steps // 10, 20))
+        res_us = {}
+        clk = None
+        for name, fn in (("layer", both), ("gateup", gateup), ("down", down)):
+            gk = capture(fn, torch, direct=args.no_graph)
+            for _ in range(max(3, args.warmup)):
+                gk.replay()
+            if name == "layer":
+                with ClockSampler(dev.index or 0) as clk:
+                    res_us[name] = time_graph(gk, reps, torch) * 1e3 / n_layers
+            else:
+                res_us[name] = time_graph(gk, reps, torch) * 1e3 / n_layers
+            del gk
+        fl_gu, fl_dn = 2.0 * M * d * (2 * f), 2.0 * M * f * d
+        by_gu = st.gateup_bytes()
+        by_dn = st.down_bytes()
+        pt = {"M": M, "us_per_layer": round(res_us["layer"], 2),
+              "tflops": round((fl_gu + fl_dn) / (res_us["layer"] * 1e-6) / 1e12, 1),
+              "gbs": round((by_gu + by_dn) / (res_us["layer"] * 1e-6) / 1e9, 1),
+              "gateup_us": round(res_us["gateup"], 2),
+              "gateup_tflops": round(fl_gu / (res_us["gateup"] * 1e-6) / 1e12, 1),
+              "down_us": round(res_us["down"], 2),
+              "down_tflops": round(fl_dn / (res_us["down"] * 1e-6) / 1e12, 1),
+              "clocks": clk.summary() if clk else None}
+        pt["frac_of_tensor_peak"] = round(pt["tflops"] / tpk, 4)
+        pt["frac_of_hbm_peak"] = round(pt["gbs"] / hbm, 4)
+        points.append(pt)
+        st.close()
+        del st, ws, x, hin, res, h, y
+        torch.cuda.empty_cache()
+    top = points[-1]
+    line = {"metric": "prefill TFLOP/s of the decode MLP layer's GEMMs (gate/up + SwiGLU, down + residual)",
+            "value": top["tflops"], "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8-weights/fp16-mma/f32-acc",
+            "data": "synthetic",
+            "config": {"workload": "qwen3-8b layer d4096 f12288 affine8 g128, M activation rows, 3 distinct layers cycled",
+                       "l2": "weights of 3 layers (467 MB) exceed the L2"},
+            "roofline": {"bound": "tensor", "kernel": f"prefill_gemm_kernel (M = {top['M']})",
+                         "achieved": top["tflops"], "peak": tpk, "unit": "TFLOP/s",
+                         "frac": top["frac_of_tensor_peak"], "peak_kind": tpk_kind},
+            "hbm_peak": hbm, "hbm_peak_kind": hbm_kind, "points": points, "device_error": mt.mt_device_error()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_mx(args, torch, synth, mt, dev):
     """The Qwen3-8B-shaped layer (d=4096, f=12288) with MX block-scaled
     weights (MXFP8, MXFP4), M = 1 and 4: us per layer of the single calls and
@@ -696,12 +788,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mt", choices=["mt", "reference"])
     ap.add_argument("--workload", default="qwen3-8b",
-                    choices=["qwen3-8b", "tiny", "llama1b", "qwen15", "sweep", "configs", "projections", "mx"],
+                    choices=["qwen3-8b", "tiny", "llama1b", "qwen15", "sweep", "configs", "projections", "mx",
+                             "prefill"],
                     help="sweep: every group x M point of the d=2048, f=8192 sweep, one line; "
                          "configs: the tiny, Llama-3.2-1B and Qwen2.5-1.5B layers hot and cold, one line; "
                          "projections: attention and vocabulary projections of a decode step per model")
-    ap.add_argument("--rows", type=int, default=None, choices=range(1, 9),
-                    help="projections: rows M (default one, decode)")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="projections / mx: rows M (1..8); prefill: one M instead of the list")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
     ap.add_argument("--sweep-group", type=int, default=None, choices=[32, 64, 128],
                     help="sweep: only this group size")
@@ -745,6 +838,8 @@ def main():
         return run_projections(args, torch, synth, mt, dev)
     if args.workload == "mx":
         return run_mx(args, torch, synth, mt, dev)
+    if args.workload == "prefill":
+        return run_prefill(args, torch, synth, mt, dev)
     wl = {"qwen3-8b": synth.QWEN8B, "tiny": synth.TINY, "llama1b": synth.LLAMA1B,
           "qwen15": synth.QWEN15}[args.workload]
     if args.layers:

@@ -53,13 +53,12 @@
 namespace mt {
 
 constexpr int PF_ROWS = 128;       // weight rows per tile (MMA M)
-constexpr int PF_COLS = 64;        // activation rows per tile (MMA N)
+constexpr int PF_COLS = 128;       // activation rows per tile (MMA N)
 constexpr int PF_KB = 64;          // K per stage (one 128-byte swizzle row of fp16)
-constexpr int PF_STAGES = 4;
-constexpr int PF_EPI_WARPS = 4;    // warps 0-3: epilogue (tensor-memory lanes 0-127)
-constexpr int PF_CONV_WARPS = 4;   // warps 4-7: converters (+ the TMA producer thread)
-constexpr int PF_THREADS = 32 * (PF_EPI_WARPS + PF_CONV_WARPS + 1);  // + warp 8: MMA issuer
-constexpr int PF_X_TILE = PF_COLS * PF_KB * 2;   // 8 KB
+constexpr int PF_EPI_WARPS = 8;    // warps 0-7: epilogue, two warpgroups (64 tile columns each)
+constexpr int PF_CONV_WARPS = 2;   // warps 8-9: converters
+constexpr int PF_THREADS = 32 * (PF_EPI_WARPS + PF_CONV_WARPS + 2);  // + warp 10: MMA, warp 11: TMA
+constexpr int PF_X_TILE = PF_COLS * PF_KB * 2;   // 16 KB
 constexpr int PF_W_TILE = PF_ROWS * PF_KB * 2;   // 16 KB
 
 struct PrefillArgs {
@@ -208,16 +207,22 @@ __global__ void __launch_bounds__(256) prefill_x_kernel(const uint16_t* __restri
 
 // ------------------------------------------------------------- the GEMM
 
-// Codes of one weight row for one K block of 64 (INT8: 64 bytes, INT4: 32)
-// as fp16 subnormals q * 2^-24, written into the swizzled tile row r.
+// Codes of weight row r for one K block of 64 (INT8: 64 bytes, INT4: 32),
+// read from the TMA-filled code tile (rows of CB bytes, 64- or 32-byte
+// swizzle: 16-byte chunk u of row r at u ^ ((r >> 1) & 3), resp. u ^ ((r >> 2)
+// & 1), so that eight consecutive rows read their chunk u from distinct
+// banks), written as fp16 subnormals q * 2^-24 into row r of the MMA tile
+// (128-byte rows, chunk j at j ^ (r & 7)).
 template <int FMT>
-__device__ __forceinline__ void pf_convert_row(const uint4 (&c)[FMT == FMT_A8 ? 4 : 2], unsigned char* tile, int r) {
-  unsigned char* rowp = tile + r * 128;
+__device__ __forceinline__ void pf_convert_row(const unsigned char* ctile, unsigned char* wtile, int r) {
+  unsigned char* rowp = wtile + r * 128;
   const int sw = r & 7;
   if constexpr (FMT == FMT_A8) {
+    const unsigned char* src = ctile + r * 64;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {  // 16 codes -> chunks 2u, 2u+1
-      const uint32_t w[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+      const uint4 v = *reinterpret_cast<const uint4*>(src + ((u ^ ((r >> 1) & 3)) << 4));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t a = w[2 * h], b = w[2 * h + 1];
@@ -227,9 +232,11 @@ __device__ __forceinline__ void pf_convert_row(const uint4 (&c)[FMT == FMT_A8 ? 
       }
     }
   } else {
+    const unsigned char* src = ctile + r * 32;
 #pragma unroll
     for (int u = 0; u < 2; ++u) {  // 32 codes -> chunks 4u .. 4u+3 (one word each)
-      const uint32_t w[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+      const uint4 v = *reinterpret_cast<const uint4*>(src + ((u ^ ((r >> 2) & 1)) << 4));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         // byte j of w holds code 2j (bits 0..3) and 2j+1 (bits 4..7)
@@ -242,57 +249,87 @@ __device__ __forceinline__ void pf_convert_row(const uint4 (&c)[FMT == FMT_A8 ? 
   }
 }
 
-// Shape of the code registers of one converter thread.
+// Shared-memory plan of one (format, kind).  Ring A (TMA): per slot the x
+// tile (128 rows x 128 B, 128-byte swizzle) and the code tiles of each matrix
+// (128 rows x CB bytes); ring B: the fp16 weight tiles the MMA reads.
 template <int FMT, int KIND>
 struct PfShape {
-  static constexpr int NW = KIND == 0 ? 2 : 1;  // weight matrices
-  static constexpr int CU = FMT == FMT_A8 ? 4 : 2;  // 16-byte code loads per row and K block
+  static constexpr int NW = KIND == 0 ? 2 : 1;          // weight matrices
+  static constexpr int CB = FMT == FMT_A8 ? 64 : 32;    // code bytes per row and K block
+  static constexpr int CTILE = PF_ROWS * CB;            // 8 or 4 KB
+  static constexpr int SA = NW == 2 ? 4 : 6;            // ring depths
+  static constexpr int SB = NW == 2 ? 2 : 3;
+  static constexpr int SLOT_A = PF_X_TILE + NW * CTILE;  // multiple of 1024
+  static constexpr int SLOT_B = NW * PF_W_TILE;
+  static constexpr size_t SMEM = 1024 + (size_t)SA * SLOT_A + (size_t)SB * SLOT_B;
+  static_assert(SMEM <= 200 * 1024, "shared memory plan");
 };
+
+// 1 in exactly one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+  return e != 0;
+}
 
 template <int FMT, int KIND>
 __global__ void __launch_bounds__(PF_THREADS, 1)
-    prefill_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const PrefillArgs a) {
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap0,
+                        const __grid_constant__ CUtensorMap wmap1, const PrefillArgs a) {
   using SH = PfShape<FMT, KIND>;
-  constexpr int NW = SH::NW;
-  constexpr int S = PF_STAGES;
-  constexpr int STAGE = PF_X_TILE + NW * PF_W_TILE;  // multiple of 1024
-  constexpr uint32_t NCOLS = 2 * NW * PF_COLS;       // two accumulator buffers
-  constexpr int CB = SH::CU * 16;                    // code bytes per row and K block
+  constexpr int NW = SH::NW, SA = SH::SA, SB = SH::SB;
+  constexpr uint32_t NCOLS = 2 * NW * PF_COLS;  // two accumulator buffers (256 or 512 columns)
+  constexpr int EPI = 32 * PF_EPI_WARPS;        // epilogue threads
+  constexpr int HALF = PF_COLS / 2;             // columns per epilogue warpgroup
 
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t bars[3 * S + 5];
+  // 1024-byte aligned start, by an offset on the shared array itself (so the
+  // compiler keeps shared-space loads and stores)
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) uint64_t bars[2 * SA + 2 * SB + 5];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
+  __shared__ __align__(16) float xg_sh[2][PF_COLS];  // X'_g of the tile's rows, two groups
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rt = blockIdx.x / a.n_ctiles, ct = blockIdx.x - rt * a.n_ctiles;
   const int n0 = rt * PF_ROWS, m0 = ct * PF_COLS;
   const int KB = a.KB, G = a.G, Mp = a.n_ctiles * PF_COLS;
-  auto x_full = [&](int st) { return smem_u32(&bars[st]); };
-  auto w_full = [&](int st) { return smem_u32(&bars[S + st]); };
-  auto stage_free = [&](int st) { return smem_u32(&bars[2 * S + st]); };
-  auto acc_full = [&](int b) { return smem_u32(&bars[3 * S + b]); };
-  auto acc_free = [&](int b) { return smem_u32(&bars[3 * S + 2 + b]); };
-  const uint32_t mma_done = smem_u32(&bars[3 * S + 4]);
-  auto xtile = [&](int st) { return smem + (size_t)st * STAGE; };
-  auto wtile = [&](int st, int mat) { return smem + (size_t)st * STAGE + PF_X_TILE + mat * PF_W_TILE; };
+  auto in_full = [&](int i) { return smem_u32(&bars[i]); };            // TMA bytes of slot i of ring A
+  auto a_free = [&](int i) { return smem_u32(&bars[SA + i]); };        // converters + MMA done with it
+  auto w_full = [&](int i) { return smem_u32(&bars[2 * SA + i]); };    // converters wrote slot i of ring B
+  auto b_free = [&](int i) { return smem_u32(&bars[2 * SA + SB + i]); };  // MMA done with it
+  auto acc_full = [&](int b) { return smem_u32(&bars[2 * SA + 2 * SB + b]); };
+  auto acc_free = [&](int b) { return smem_u32(&bars[2 * SA + 2 * SB + 2 + b]); };
+  const uint32_t mma_done = smem_u32(&bars[2 * SA + 2 * SB + 4]);
+  auto xslot = [&](int i) { return smem + (size_t)i * SH::SLOT_A; };
+  auto cslot = [&](int i, int mat) { return smem + (size_t)i * SH::SLOT_A + PF_X_TILE + mat * SH::CTILE; };
+  auto wslot = [&](int i, int mat) {
+    return smem + (size_t)SA * SH::SLOT_A + (size_t)i * SH::SLOT_B + mat * PF_W_TILE;
+  };
+  constexpr int CONV0 = PF_EPI_WARPS;                   // first converter warp
+  constexpr int MMA_WARP = PF_EPI_WARPS + PF_CONV_WARPS;
+  constexpr int TMA_WARP = MMA_WARP + 1;
+  constexpr int CONV = 32 * PF_CONV_WARPS;              // converter threads
 
   if (tid == 0) {
-    for (int st = 0; st < S; ++st) {
-      mbar_init(x_full(st), 1);
-      mbar_init(w_full(st), 32 * PF_CONV_WARPS);
-      mbar_init(stage_free(st), 1);
+    for (int i = 0; i < SA; ++i) {
+      mbar_init(in_full(i), 1);
+      mbar_init(a_free(i), CONV + 1);
+    }
+    for (int i = 0; i < SB; ++i) {
+      mbar_init(w_full(i), CONV);
+      mbar_init(b_free(i), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
-      mbar_init(acc_free(b), 32 * PF_EPI_WARPS);
+      mbar_init(acc_free(b), EPI);
     }
     mbar_init(mma_done, 1);
     abort_sh = 0;
     mbar_fence_init();
   }
-  if (warp == 8) {
+  if (warp == MMA_WARP) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_sh)),
                  "r"(NCOLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -307,97 +344,96 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     *abort_flag = 1;
   };
 
-  if (warp >= PF_EPI_WARPS && warp < PF_EPI_WARPS + PF_CONV_WARPS) {
-    // ---- converters: weight row n0 + c of each matrix; thread c == 0 also
-    // issues the x tile copies
-    const int c = tid - 32 * PF_EPI_WARPS;
-    const int n = n0 + c;
-    const bool okr = n < a.N;
-    const uint8_t* wr[NW];
-#pragma unroll
-    for (int mat = 0; mat < NW; ++mat) wr[mat] = (mat ? a.W1 : a.W0) + (size_t)(okr ? n : 0) * a.row_bytes;
-    uint4 bufA[SH::NW][SH::CU], bufB[SH::NW][SH::CU];
-    auto load = [&](int kb, uint4 (&buf)[SH::NW][SH::CU]) {
-#pragma unroll
-      for (int mat = 0; mat < NW; ++mat)
-#pragma unroll
-        for (int u = 0; u < SH::CU; ++u)
-          buf[mat][u] = (okr && kb < KB) ? ldg_stream(wr[mat] + (size_t)kb * CB + u * 16) : make_uint4(0, 0, 0, 0);
-    };
-    int issued = 0;
-    auto step = [&](int kb, const uint4 (&cur)[SH::NW][SH::CU], uint4 (&nxt)[SH::NW][SH::CU]) -> bool {
-      load(kb + 1, nxt);
-      const int st = kb % S;
-      if (kb >= S && !mbar_wait_bounded(stage_free(st), ((kb / S) + 1) & 1)) return false;
-      if (c == 0) {
-        mbar_arrive_expect_tx(x_full(st), PF_X_TILE);
-        tma_load_2d(smem_u32(xtile(st)), &xmap, kb * PF_KB, m0, x_full(st));
+  if (warp == TMA_WARP) {
+    // ---- producer: x tile and code tiles of each K block, SA blocks ahead
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int i = kb % SA;
+        if (kb >= SA && !mbar_wait_bounded(a_free(i), ((kb / SA) + 1) & 1)) { fail(); break; }
+        if (*abort_flag) break;
+        mbar_arrive_expect_tx(in_full(i), PF_X_TILE + NW * SH::CTILE);
+        tma_load_2d(smem_u32(xslot(i)), &xmap, kb * PF_KB, m0, in_full(i));
+        tma_load_2d(smem_u32(cslot(i, 0)), &wmap0, kb * SH::CB, n0, in_full(i));
+        if constexpr (NW == 2) tma_load_2d(smem_u32(cslot(i, 1)), &wmap1, kb * SH::CB, n0, in_full(i));
         ++issued;
       }
+      // copies still in flight (only after an abort) land before the CTA ends
+      for (int kb = max(0, issued - SA); kb < issued; ++kb) (void)mbar_wait_bounded(in_full(kb % SA), (kb / SA) & 1);
+    }
+    __syncwarp();
+  } else if (warp >= CONV0 && warp < MMA_WARP) {
+    // ---- converters: rows c, c + CONV, ... of each code tile into the fp16 tiles
+    const int c = tid - 32 * CONV0;
+    for (int kb = 0; kb < KB; ++kb) {
+      const int i = kb % SA, j = kb % SB;
+      if (!mbar_wait_bounded(in_full(i), (kb / SA) & 1)) { fail(); break; }
+      if (kb >= SB && !mbar_wait_bounded(b_free(j), ((kb / SB) + 1) & 1)) { fail(); break; }
 #pragma unroll
-      for (int mat = 0; mat < NW; ++mat) pf_convert_row<FMT>(cur[mat], wtile(st, mat), c);
+      for (int r = c; r < PF_ROWS; r += CONV)
+#pragma unroll
+        for (int mat = 0; mat < NW; ++mat) pf_convert_row<FMT>(cslot(i, mat), wslot(j, mat), r);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor core reads
-      mbar_arrive(w_full(st));
-      return true;
-    };
-    load(0, bufA);
-    for (int kb = 0; kb < KB; kb += 2) {
+      mbar_arrive(w_full(j));
+      mbar_arrive(a_free(i));
       if (*abort_flag) break;
-      if (!step(kb, bufA, bufB)) { fail(); break; }
-      if (kb + 1 >= KB) break;
-      if (*abort_flag) break;
-      if (!step(kb + 1, bufB, bufA)) { fail(); break; }
     }
-    if (c == 0) {  // copies still in flight (only after an abort) land before the CTA ends
-      for (int kb = max(0, issued - S); kb < issued; ++kb) (void)mbar_wait_bounded(x_full(kb % S), (kb / S) & 1);
-    }
-  } else if (warp == 8) {
-    // ---- MMA issuer
-    if (lane == 0) {
-      const int group = a.group;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int st = kb % S;
-        const uint32_t ph = (kb / S) & 1;
-        if (!mbar_wait_bounded(x_full(st), ph) || !mbar_wait_bounded(w_full(st), ph)) { fail(); break; }
-        tc_fence_after();
-        const uint64_t xd = pf_desc_sw128(smem_u32(xtile(st)));
-        uint64_t wd[NW];
+  } else if (warp == MMA_WARP) {
+    // ---- MMA issuer: the whole warp walks the loop, one elected lane issues
+    const int group = a.group;
+    bool ok = true;
+    for (int kb = 0; kb < KB && ok; ++kb) {
+      const int i = kb % SA, jb = kb % SB;
+      if (!mbar_wait_bounded(in_full(i), (kb / SA) & 1) || !mbar_wait_bounded(w_full(jb), (kb / SB) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t xd = pf_desc_sw128(smem_u32(xslot(i)));
+      uint64_t wd[NW];
 #pragma unroll
-        for (int mat = 0; mat < NW; ++mat) wd[mat] = pf_desc_sw128(smem_u32(wtile(st, mat)));
-        bool ok = true;
+      for (int mat = 0; mat < NW; ++mat) wd[mat] = pf_desc_sw128(smem_u32(wslot(jb, mat)));
 #pragma unroll
-        for (int j = 0; j < PF_KB / 16; ++j) {
-          const int k = kb * PF_KB + 16 * j;
-          const int gi = k >> a.lg_group, b = gi & 1;
-          const bool first = (k & (group - 1)) == 0;
-          if (first && gi >= 2) {
-            if (!mbar_wait_bounded(acc_free(b), ((gi >> 1) - 1) & 1)) { ok = false; break; }
-            tc_fence_after();
-          }
+      for (int j = 0; j < PF_KB / 16; ++j) {
+        const int k = kb * PF_KB + 16 * j;
+        const int gi = k >> a.lg_group, b = gi & 1;
+        const bool first = (k & (group - 1)) == 0;
+        if (first && gi >= 2) {
+          if (!mbar_wait_bounded(acc_free(b), ((gi >> 1) - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+        }
+        if (elect_one()) {
 #pragma unroll
           for (int mat = 0; mat < NW; ++mat)
             tc_mma(tbase + (uint32_t)((b * NW + mat) * PF_COLS), wd[mat] + 2 * j, xd + 2 * j, first ? 0u : 1u);
           if (((k + 16) & (group - 1)) == 0) tc_commit(acc_full(b));
         }
-        tc_commit(stage_free(st));
-        if (!ok) { fail(); break; }
-        if (*abort_flag) break;
+        __syncwarp();
       }
-      tc_commit(mma_done);  // completes when every MMA issued above has
-      (void)mbar_wait_bounded(mma_done, 0);
+      if (elect_one()) {
+        tc_commit(b_free(jb));
+        tc_commit(a_free(i));
+      }
+      __syncwarp();
+      if (*abort_flag) break;
     }
+    if (!ok) fail();
+    if (elect_one()) tc_commit(mma_done);  // completes when every MMA issued above has
     __syncwarp();
+    (void)mbar_wait_bounded(mma_done, 0);
   } else {
-    // ---- epilogue warpgroup: output row n0 + tid, 64 activation rows
-    const int n = n0 + tid;
+    // ---- epilogue: two warpgroups, output row n0 + (tid & 127), tile columns
+    // [wg * 64, wg * 64 + 64)
+    const int wg = warp >> 2, rl = tid & 127;
+    const int n = n0 + rl;
     const bool okr = n < a.N;
     const size_t sbo = (size_t)(okr ? n : 0) * G;
-    float acc[NW][PF_COLS];
+    float acc[NW][HALF];
 #pragma unroll
     for (int mat = 0; mat < NW; ++mat)
 #pragma unroll
-      for (int j = 0; j < PF_COLS; ++j) acc[mat][j] = 0.f;
-    const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
+      for (int j = 0; j < HALF; ++j) acc[mat][j] = 0.f;
+    const uint32_t lane_base = tbase + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(wg * HALF);
     constexpr float TWO24 = 16777216.f;  // the codes enter the MMA as q * 2^-24
     float sv[NW], bv[NW];
 #pragma unroll
@@ -405,9 +441,31 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       sv[mat] = okr ? bf16f((mat ? a.s1 : a.s0)[sbo]) * TWO24 : 0.f;
       bv[mat] = okr ? bf16f((mat ? a.b1 : a.b0)[sbo]) : 0.f;
     }
+    // X'_g of group gi for the tile's rows comes into xg_sh[gi & 1] by
+    // asynchronous copies one group ahead (threads 0-31, 16 bytes each)
+    auto fetch_xg = [&](int gi) {
+      if (tid < PF_COLS / 4) cp_async16(&xg_sh[gi & 1][4 * tid], a.XgT + (size_t)gi * Mp + m0 + 4 * tid);
+      cp_async_commit();
+    };
+    auto epi_sync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(EPI) : "memory"); };
+    // barrier of the epilogue warps that also ORs a flag over them (a uniform decision)
+    auto epi_sync_or = [&](bool v) -> bool {
+      uint32_t r;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+          "barrier.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+          : "=r"(r)
+          : "r"((uint32_t)v), "n"(EPI)
+          : "memory");
+      return r != 0;
+    };
+    fetch_xg(0);
+    cp_async_wait_all();
+    epi_sync();
     bool aborted = false;
     for (int gi = 0; gi < G; ++gi) {
       const int b = gi & 1;
+      if (gi + 1 < G) fetch_xg(gi + 1);
       // the next group's scales and biases, ahead of the wait
       float sn[NW], bn[NW];
 #pragma unroll
@@ -416,39 +474,45 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         sn[mat] = more ? bf16f((mat ? a.s1 : a.s0)[sbo + gi + 1]) * TWO24 : 0.f;
         bn[mat] = more ? bf16f((mat ? a.b1 : a.b0)[sbo + gi + 1]) : 0.f;
       }
-      if (!mbar_wait_bounded(acc_full(b), (gi >> 1) & 1)) { fail(); aborted = true; break; }
-      tc_fence_after();
-      const float* xg = a.XgT + (size_t)gi * Mp + m0;
+      if (!mbar_wait_bounded(acc_full(b), (gi >> 1) & 1)) { fail(); aborted = true; }
+      if (!aborted) {
+        tc_fence_after();
+        const float* xg = xg_sh[b] + wg * HALF;
 #pragma unroll
-      for (int q = 0; q < PF_COLS / 16; ++q) {
-        float d0[16], d1[16];
-        const uint32_t t0 = lane_base + (uint32_t)(b * NW * PF_COLS + q * 16);
-        if constexpr (NW == 2)
-          tc_ld16x2_wait(t0, t0 + PF_COLS, d0, d1);
-        else
-          tc_ld16_wait(t0, d0);
-        float X[16];
+        for (int q = 0; q < HALF / 16; ++q) {
+          float d0[16], d1[16];
+          const uint32_t t0 = lane_base + (uint32_t)(b * NW * PF_COLS + q * 16);
+          if constexpr (NW == 2)
+            tc_ld16x2_wait(t0, t0 + PF_COLS, d0, d1);
+          else
+            tc_ld16_wait(t0, d0);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 v = __ldg(reinterpret_cast<const float4*>(xg + q * 16) + i);
-          X[4 * i] = v.x; X[4 * i + 1] = v.y; X[4 * i + 2] = v.z; X[4 * i + 3] = v.w;
+          for (int i = 0; i < 4; ++i) {
+            const float4 X = *reinterpret_cast<const float4*>(xg + q * 16 + 4 * i);
+            const float Xv[4] = {X.x, X.y, X.z, X.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int jj = q * 16 + 4 * i + e;
+              acc[0][jj] = fmaf(sv[0], d0[4 * i + e], fmaf(bv[0], Xv[e], acc[0][jj]));
+              if constexpr (NW == 2) acc[NW - 1][jj] = fmaf(sv[NW - 1], d1[4 * i + e], fmaf(bv[NW - 1], Xv[e], acc[NW - 1][jj]));
+            }
+          }
         }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          acc[0][q * 16 + j] = fmaf(sv[0], d0[j], fmaf(bv[0], X[j], acc[0][q * 16 + j]));
-          if constexpr (NW == 2) acc[NW - 1][q * 16 + j] = fmaf(sv[NW - 1], d1[j], fmaf(bv[NW - 1], X[j], acc[NW - 1][q * 16 + j]));
-        }
+        tc_fence_before();
+        mbar_arrive(acc_free(b));
       }
-      tc_fence_before();
-      mbar_arrive(acc_free(b));
 #pragma unroll
       for (int mat = 0; mat < NW; ++mat) { sv[mat] = sn[mat]; bv[mat] = bn[mat]; }
-      if (*abort_flag) { aborted = true; break; }
+      // the next group's X'_g has landed and every thread is done with this
+      // one; the decision to stop is the same for every epilogue thread
+      cp_async_wait_all();
+      aborted = epi_sync_or(aborted || *abort_flag);
+      if (aborted) break;
     }
     if (!aborted && okr) {
 #pragma unroll
-      for (int j = 0; j < PF_COLS; ++j) {
-        const int m = m0 + j;
+      for (int j = 0; j < HALF; ++j) {
+        const int m = m0 + wg * HALF + j;
         if (m < a.M) {
           const float ei = a.einv[m];
           const float v0 = acc[0][j] * ei;
@@ -471,7 +535,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 8) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(NCOLS));
+  if (warp == MMA_WARP) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(NCOLS));
 }
 
 // ---------------------------------------------------------------- host side
@@ -527,6 +591,19 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
       CUDA_SUCCESS)
     return cuda_fail(cudaErrorInvalidValue);
+  // code tiles: 128 rows x CB bytes, 64-byte (INT8) or 32-byte (INT4) swizzle
+  using SH = PfShape<FMT, KIND>;
+  CUtensorMap wmap[2];
+  for (int mat = 0; mat < 2; ++mat) {
+    const void* W = (mat && NW == 2) ? p.W1 : p.W0;
+    const cuuint64_t wdims[2] = {(cuuint64_t)(FMT == FMT_A8 ? K : K / 2), (cuuint64_t)N};
+    const cuuint64_t wstr[1] = {wdims[0]};
+    const cuuint32_t wbox[2] = {(cuuint32_t)SH::CB, (cuuint32_t)PF_ROWS};
+    if (enc(&wmap[mat], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), wdims, wstr, wbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, FMT == FMT_A8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cuda_fail(cudaErrorInvalidValue);
+  }
 
   PrefillArgs a = {};
   a.W0 = static_cast<const uint8_t*>(p.W0);
@@ -548,7 +625,7 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
 
   mt_status st = launch(prefill_x_kernel, dim3(Mp), dim3(256), 0, l, p.x, M, K, group, x16, XgT, einv);
   if (st != MT_OK) return st;
-  const size_t smem = 1024 + (size_t)PF_STAGES * (PF_X_TILE + NW * PF_W_TILE);
+  const size_t smem = SH::SMEM;
   auto kern = prefill_gemm_kernel<FMT, KIND>;
   static std::mutex mu;
   static bool attr_set[64] = {};
@@ -563,7 +640,7 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
       if (dev < 64) attr_set[dev] = true;
     }
   }
-  return launch(kern, dim3((unsigned)(n_rtiles * n_ctiles)), dim3(PF_THREADS), smem, l, xmap, a);
+  return launch(kern, dim3((unsigned)(n_rtiles * n_ctiles)), dim3(PF_THREADS), smem, l, xmap, wmap[0], wmap[1], a);
 }
 
 mt_status launch_prefill(const GemvProblem& p, void* ws, const Launch& l) {

@@ -53,12 +53,12 @@
 namespace mt {
 
 constexpr int PF_ROWS = 128;       // weight rows per tile (MMA M)
-constexpr int PF_COLS = 128;       // activation rows per tile (MMA N)
+constexpr int PF_COLS = 256;       // activation rows per tile (MMA N)
 constexpr int PF_KB = 64;          // K per stage (one 128-byte swizzle row of fp16)
 constexpr int PF_EPI_WARPS = 8;    // warps 0-7: epilogue, two warpgroups (64 tile columns each)
 constexpr int PF_CONV_WARPS = 2;   // warps 8-9: converters
 constexpr int PF_THREADS = 32 * (PF_EPI_WARPS + PF_CONV_WARPS + 2);  // + warp 10: MMA, warp 11: TMA
-constexpr int PF_X_TILE = PF_COLS * PF_KB * 2;   // 16 KB
+constexpr int PF_X_TILE = PF_COLS * PF_KB * 2;   // 32 KB
 constexpr int PF_W_TILE = PF_ROWS * PF_KB * 2;   // 16 KB
 
 struct PrefillArgs {
@@ -249,20 +249,23 @@ __device__ __forceinline__ void pf_convert_row(const unsigned char* ctile, unsig
   }
 }
 
-// Shared-memory plan of one (format, kind).  Ring A (TMA): per slot the x
-// tile (128 rows x 128 B, 128-byte swizzle) and the code tiles of each matrix
-// (128 rows x CB bytes); ring B: the fp16 weight tiles the MMA reads.
+// Shared-memory plan of one (format, kind).  The MMA's A tile is 128 weight
+// rows: 128 output features (down / projection), or the gate rows (0-63) and
+// the up rows (64-127) of 64 output features (gate/up), so that one MMA per K
+// step covers both matrices.  Ring A (TMA): per slot the x tile (256 rows x
+// 128 B, 128-byte swizzle) and the code tile (128 rows x CB bytes); ring B:
+// the fp16 A tiles.
 template <int FMT, int KIND>
 struct PfShape {
-  static constexpr int NW = KIND == 0 ? 2 : 1;          // weight matrices
+  static constexpr int FT = KIND == 0 ? 64 : 128;       // output features per tile
   static constexpr int CB = FMT == FMT_A8 ? 64 : 32;    // code bytes per row and K block
   static constexpr int CTILE = PF_ROWS * CB;            // 8 or 4 KB
-  static constexpr int SA = NW == 2 ? 4 : 6;            // ring depths
-  static constexpr int SB = NW == 2 ? 2 : 3;
-  static constexpr int SLOT_A = PF_X_TILE + NW * CTILE;  // multiple of 1024
-  static constexpr int SLOT_B = NW * PF_W_TILE;
+  static constexpr int SA = 4, SB = 3;                  // ring depths
+  static constexpr int SLOT_A = PF_X_TILE + CTILE;      // multiple of 1024
+  static constexpr int SLOT_B = PF_W_TILE;
   static constexpr size_t SMEM = 1024 + (size_t)SA * SLOT_A + (size_t)SB * SLOT_B;
-  static_assert(SMEM <= 200 * 1024, "shared memory plan");
+  static_assert(SMEM <= 216 * 1024, "shared memory plan");
+  static_assert((size_t)SA * SLOT_A >= (size_t)64 * PF_COLS * 4, "gate/up exchange buffer");
 };
 
 // 1 in exactly one lane of the (converged) warp.
@@ -277,10 +280,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap0,
                         const __grid_constant__ CUtensorMap wmap1, const PrefillArgs a) {
   using SH = PfShape<FMT, KIND>;
-  constexpr int NW = SH::NW, SA = SH::SA, SB = SH::SB;
-  constexpr uint32_t NCOLS = 2 * NW * PF_COLS;  // two accumulator buffers (256 or 512 columns)
-  constexpr int EPI = 32 * PF_EPI_WARPS;        // epilogue threads
-  constexpr int HALF = PF_COLS / 2;             // columns per epilogue warpgroup
+  constexpr int SA = SH::SA, SB = SH::SB, FT = SH::FT;
+  constexpr uint32_t NCOLS = 2 * PF_COLS;   // two accumulator buffers of 256 columns
+  constexpr int EPI = 32 * PF_EPI_WARPS;    // epilogue threads
+  constexpr int HALF = PF_COLS / 2;         // tile columns per epilogue warpgroup (128)
 
   extern __shared__ unsigned char smem_raw[];
   // 1024-byte aligned start, by an offset on the shared array itself (so the
@@ -293,7 +296,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rt = blockIdx.x / a.n_ctiles, ct = blockIdx.x - rt * a.n_ctiles;
-  const int n0 = rt * PF_ROWS, m0 = ct * PF_COLS;
+  const int f0 = rt * FT, m0 = ct * PF_COLS;  // first output feature and activation row
   const int KB = a.KB, G = a.G, Mp = a.n_ctiles * PF_COLS;
   auto in_full = [&](int i) { return smem_u32(&bars[i]); };            // TMA bytes of slot i of ring A
   auto a_free = [&](int i) { return smem_u32(&bars[SA + i]); };        // converters + MMA done with it
@@ -303,10 +306,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   auto acc_free = [&](int b) { return smem_u32(&bars[2 * SA + 2 * SB + 2 + b]); };
   const uint32_t mma_done = smem_u32(&bars[2 * SA + 2 * SB + 4]);
   auto xslot = [&](int i) { return smem + (size_t)i * SH::SLOT_A; };
-  auto cslot = [&](int i, int mat) { return smem + (size_t)i * SH::SLOT_A + PF_X_TILE + mat * SH::CTILE; };
-  auto wslot = [&](int i, int mat) {
-    return smem + (size_t)SA * SH::SLOT_A + (size_t)i * SH::SLOT_B + mat * PF_W_TILE;
-  };
+  auto cslot = [&](int i) { return smem + (size_t)i * SH::SLOT_A + PF_X_TILE; };
+  auto wslot = [&](int i) { return smem + (size_t)SA * SH::SLOT_A + (size_t)i * SH::SLOT_B; };
   constexpr int CONV0 = PF_EPI_WARPS;                   // first converter warp
   constexpr int MMA_WARP = PF_EPI_WARPS + PF_CONV_WARPS;
   constexpr int TMA_WARP = MMA_WARP + 1;
@@ -345,17 +346,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   };
 
   if (warp == TMA_WARP) {
-    // ---- producer: x tile and code tiles of each K block, SA blocks ahead
+    // ---- producer: x tile and code tile of each K block, SA blocks ahead
     if (lane == 0) {
       int issued = 0;
       for (int kb = 0; kb < KB; ++kb) {
         const int i = kb % SA;
         if (kb >= SA && !mbar_wait_bounded(a_free(i), ((kb / SA) + 1) & 1)) { fail(); break; }
         if (*abort_flag) break;
-        mbar_arrive_expect_tx(in_full(i), PF_X_TILE + NW * SH::CTILE);
+        mbar_arrive_expect_tx(in_full(i), PF_X_TILE + SH::CTILE);
         tma_load_2d(smem_u32(xslot(i)), &xmap, kb * PF_KB, m0, in_full(i));
-        tma_load_2d(smem_u32(cslot(i, 0)), &wmap0, kb * SH::CB, n0, in_full(i));
-        if constexpr (NW == 2) tma_load_2d(smem_u32(cslot(i, 1)), &wmap1, kb * SH::CB, n0, in_full(i));
+        tma_load_2d(smem_u32(cslot(i)), &wmap0, kb * SH::CB, f0, in_full(i));
+        if constexpr (KIND == 0) tma_load_2d(smem_u32(cslot(i) + 64 * SH::CB), &wmap1, kb * SH::CB, f0, in_full(i));
         ++issued;
       }
       // copies still in flight (only after an abort) land before the CTA ends
@@ -363,16 +364,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     }
     __syncwarp();
   } else if (warp >= CONV0 && warp < MMA_WARP) {
-    // ---- converters: rows c, c + CONV, ... of each code tile into the fp16 tiles
+    // ---- converters: rows c, c + CONV of the code tile into the fp16 A tile
     const int c = tid - 32 * CONV0;
     for (int kb = 0; kb < KB; ++kb) {
       const int i = kb % SA, j = kb % SB;
       if (!mbar_wait_bounded(in_full(i), (kb / SA) & 1)) { fail(); break; }
       if (kb >= SB && !mbar_wait_bounded(b_free(j), ((kb / SB) + 1) & 1)) { fail(); break; }
 #pragma unroll
-      for (int r = c; r < PF_ROWS; r += CONV)
-#pragma unroll
-        for (int mat = 0; mat < NW; ++mat) pf_convert_row<FMT>(cslot(i, mat), wslot(j, mat), r);
+      for (int r = c; r < PF_ROWS; r += CONV) pf_convert_row<FMT>(cslot(i), wslot(j), r);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor core reads
       mbar_arrive(w_full(j));
       mbar_arrive(a_free(i));
@@ -390,9 +389,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       }
       tc_fence_after();
       const uint64_t xd = pf_desc_sw128(smem_u32(xslot(i)));
-      uint64_t wd[NW];
-#pragma unroll
-      for (int mat = 0; mat < NW; ++mat) wd[mat] = pf_desc_sw128(smem_u32(wslot(jb, mat)));
+      const uint64_t wd = pf_desc_sw128(smem_u32(wslot(jb)));
 #pragma unroll
       for (int j = 0; j < PF_KB / 16; ++j) {
         const int k = kb * PF_KB + 16 * j;
@@ -403,9 +400,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           tc_fence_after();
         }
         if (elect_one()) {
-#pragma unroll
-          for (int mat = 0; mat < NW; ++mat)
-            tc_mma(tbase + (uint32_t)((b * NW + mat) * PF_COLS), wd[mat] + 2 * j, xd + 2 * j, first ? 0u : 1u);
+          tc_mma(tbase + (uint32_t)(b * PF_COLS), wd + 2 * j, xd + 2 * j, first ? 0u : 1u);
           if (((k + 16) & (group - 1)) == 0) tc_commit(acc_full(b));
         }
         __syncwarp();
@@ -422,27 +417,24 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     __syncwarp();
     (void)mbar_wait_bounded(mma_done, 0);
   } else {
-    // ---- epilogue: two warpgroups, output row n0 + (tid & 127), tile columns
-    // [wg * 64, wg * 64 + 64)
-    const int wg = warp >> 2, rl = tid & 127;
-    const int n = n0 + rl;
+    // ---- epilogue: two warpgroups; thread (r, wg) owns A row r (tensor
+    // memory lane r) and the tile columns [wg * 128, wg * 128 + 128)
+    const int wg = warp >> 2, r = tid & 127;
+    const int mat = (KIND == 0 && r >= 64) ? 1 : 0;     // gate/up: rows 64-127 are the up matrix
+    const int n = f0 + (KIND == 0 ? (r & 63) : r);      // output feature
     const bool okr = n < a.N;
+    const uint16_t* sp = mat ? a.s1 : a.s0;
+    const uint16_t* bp = mat ? a.b1 : a.b0;
     const size_t sbo = (size_t)(okr ? n : 0) * G;
-    float acc[NW][HALF];
+    float acc[HALF];
 #pragma unroll
-    for (int mat = 0; mat < NW; ++mat)
-#pragma unroll
-      for (int j = 0; j < HALF; ++j) acc[mat][j] = 0.f;
+    for (int j = 0; j < HALF; ++j) acc[j] = 0.f;
     const uint32_t lane_base = tbase + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(wg * HALF);
     constexpr float TWO24 = 16777216.f;  // the codes enter the MMA as q * 2^-24
-    float sv[NW], bv[NW];
-#pragma unroll
-    for (int mat = 0; mat < NW; ++mat) {
-      sv[mat] = okr ? bf16f((mat ? a.s1 : a.s0)[sbo]) * TWO24 : 0.f;
-      bv[mat] = okr ? bf16f((mat ? a.b1 : a.b0)[sbo]) : 0.f;
-    }
+    float sv = okr ? bf16f(sp[sbo]) * TWO24 : 0.f;
+    float bv = okr ? bf16f(bp[sbo]) : 0.f;
     // X'_g of group gi for the tile's rows comes into xg_sh[gi & 1] by
-    // asynchronous copies one group ahead (threads 0-31, 16 bytes each)
+    // asynchronous copies one group ahead (threads 0-63, 16 bytes each)
     auto fetch_xg = [&](int gi) {
       if (tid < PF_COLS / 4) cp_async16(&xg_sh[gi & 1][4 * tid], a.XgT + (size_t)gi * Mp + m0 + 4 * tid);
       cp_async_commit();
@@ -450,14 +442,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     auto epi_sync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(EPI) : "memory"); };
     // barrier of the epilogue warps that also ORs a flag over them (a uniform decision)
     auto epi_sync_or = [&](bool v) -> bool {
-      uint32_t r;
+      uint32_t res;
       asm volatile(
           "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
           "barrier.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-          : "=r"(r)
+          : "=r"(res)
           : "r"((uint32_t)v), "n"(EPI)
           : "memory");
-      return r != 0;
+      return res != 0;
     };
     fetch_xg(0);
     cp_async_wait_all();
@@ -466,26 +458,18 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     for (int gi = 0; gi < G; ++gi) {
       const int b = gi & 1;
       if (gi + 1 < G) fetch_xg(gi + 1);
-      // the next group's scales and biases, ahead of the wait
-      float sn[NW], bn[NW];
-#pragma unroll
-      for (int mat = 0; mat < NW; ++mat) {
-        const bool more = okr && gi + 1 < G;
-        sn[mat] = more ? bf16f((mat ? a.s1 : a.s0)[sbo + gi + 1]) * TWO24 : 0.f;
-        bn[mat] = more ? bf16f((mat ? a.b1 : a.b0)[sbo + gi + 1]) : 0.f;
-      }
+      // the next group's scale and bias, ahead of the wait
+      const bool more = okr && gi + 1 < G;
+      const float sn = more ? bf16f(sp[sbo + gi + 1]) * TWO24 : 0.f;
+      const float bn = more ? bf16f(bp[sbo + gi + 1]) : 0.f;
       if (!mbar_wait_bounded(acc_full(b), (gi >> 1) & 1)) { fail(); aborted = true; }
       if (!aborted) {
         tc_fence_after();
         const float* xg = xg_sh[b] + wg * HALF;
 #pragma unroll
         for (int q = 0; q < HALF / 16; ++q) {
-          float d0[16], d1[16];
-          const uint32_t t0 = lane_base + (uint32_t)(b * NW * PF_COLS + q * 16);
-          if constexpr (NW == 2)
-            tc_ld16x2_wait(t0, t0 + PF_COLS, d0, d1);
-          else
-            tc_ld16_wait(t0, d0);
+          float d[16];
+          tc_ld16_wait(lane_base + (uint32_t)(b * PF_COLS + q * 16), d);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float4 X = *reinterpret_cast<const float4*>(xg + q * 16 + 4 * i);
@@ -493,40 +477,59 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int jj = q * 16 + 4 * i + e;
-              acc[0][jj] = fmaf(sv[0], d0[4 * i + e], fmaf(bv[0], Xv[e], acc[0][jj]));
-              if constexpr (NW == 2) acc[NW - 1][jj] = fmaf(sv[NW - 1], d1[4 * i + e], fmaf(bv[NW - 1], Xv[e], acc[NW - 1][jj]));
+              acc[jj] = fmaf(sv, d[4 * i + e], fmaf(bv, Xv[e], acc[jj]));
             }
           }
         }
         tc_fence_before();
         mbar_arrive(acc_free(b));
       }
-#pragma unroll
-      for (int mat = 0; mat < NW; ++mat) { sv[mat] = sn[mat]; bv[mat] = bn[mat]; }
+      sv = sn;
+      bv = bn;
       // the next group's X'_g has landed and every thread is done with this
       // one; the decision to stop is the same for every epilogue thread
       cp_async_wait_all();
       aborted = epi_sync_or(aborted || *abort_flag);
       if (aborted) break;
     }
-    if (!aborted && okr) {
-#pragma unroll
-      for (int j = 0; j < HALF; ++j) {
-        const int m = m0 + wg * HALF + j;
-        if (m < a.M) {
-          const float ei = a.einv[m];
-          const float v0 = acc[0][j] * ei;
-          float outv;
-          if constexpr (KIND == 0) {
-            const float v1 = acc[NW - 1][j] * ei;
-            outv = v0 / (1.0f + expf(-v0)) * v1;  // silu(gate) * up
-          } else {
-            outv = a.res ? v0 + bf16f(a.res[(size_t)m * a.res_ld + n]) : v0;  // + residual or bias
-          }
+    if (!aborted) {
+      const int cbase = wg * HALF;
+      auto store = [&](int j, float outv) {
+        const int m = m0 + cbase + j;
+        if (m < a.M && okr) {
           if (a.out_f32)
             static_cast<float*>(a.out)[(size_t)m * a.N + n] = outv;
           else
             static_cast<uint16_t*>(a.out)[(size_t)m * a.N + n] = f2bf(outv);
+        }
+      };
+      if constexpr (KIND == 0) {
+        // the up rows hand their totals to the gate rows through shared
+        // memory (ring A is idle now: every copy and MMA has completed),
+        // column-major so that consecutive rows hit consecutive banks
+        float* xch = reinterpret_cast<float*>(smem);  // [PF_COLS][64]
+        if (mat == 1) {
+#pragma unroll
+          for (int j = 0; j < HALF; ++j) xch[(cbase + j) * 64 + (r - 64)] = acc[j];
+        }
+        epi_sync();
+        if (mat == 0) {
+#pragma unroll
+          for (int j = 0; j < HALF; ++j) {
+            const int m = m0 + cbase + j;
+            const float ei = m < a.M ? a.einv[m] : 0.f;
+            const float g = acc[j] * ei, u = xch[(cbase + j) * 64 + r] * ei;
+            store(j, g / (1.0f + expf(-g)) * u);  // silu(gate) * up
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < HALF; ++j) {
+          const int m = m0 + cbase + j;
+          if (m < a.M && okr) {
+            const float v = acc[j] * a.einv[m];
+            store(j, a.res ? v + bf16f(a.res[(size_t)m * a.res_ld + n]) : v);  // + residual or bias
+          }
         }
       }
     }
@@ -571,7 +574,7 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   constexpr int NW = KIND == 0 ? 2 : 1;
   const int M = p.M, K = p.K, N = p.N, group = p.group;
   const int n_ctiles = (M + PF_COLS - 1) / PF_COLS, Mp = n_ctiles * PF_COLS;
-  const int n_rtiles = (N + PF_ROWS - 1) / PF_ROWS;
+  const int n_rtiles = (N + PfShape<FMT, KIND>::FT - 1) / PfShape<FMT, KIND>::FT;
   const int G = K / group;
   unsigned char* w = static_cast<unsigned char*>(ws);
   __half* x16 = reinterpret_cast<__half*>(w);
@@ -598,7 +601,7 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
     const void* W = (mat && NW == 2) ? p.W1 : p.W0;
     const cuuint64_t wdims[2] = {(cuuint64_t)(FMT == FMT_A8 ? K : K / 2), (cuuint64_t)N};
     const cuuint64_t wstr[1] = {wdims[0]};
-    const cuuint32_t wbox[2] = {(cuuint32_t)SH::CB, (cuuint32_t)PF_ROWS};
+    const cuuint32_t wbox[2] = {(cuuint32_t)SH::CB, (cuuint32_t)SH::FT};  // gate/up: 64 rows of each
     if (enc(&wmap[mat], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), wdims, wstr, wbox, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, FMT == FMT_A8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)

@@ -75,7 +75,8 @@ struct PrefillArgs {
   void* out;            // [M][N]
   int out_f32;
   int M, K, N, group, lg_group, G, KB, row_bytes;
-  int n_ctiles;         // ceil(M / 64)
+  int n_ctiles;         // ceil(M / 256)
+  int tma_store;        // 1: bf16 output written by one TMA store per tile (row stride a multiple of 16 B)
   int* err;             // device error word
 };
 
@@ -152,6 +153,26 @@ __device__ __forceinline__ void tc_ld16x2_wait(uint32_t ta, uint32_t tb, float (
     va[i] = __uint_as_float(r[i]);
     vb[i] = __uint_as_float(r[16 + i]);
   }
+}
+
+// Plain global stores as inline PTX: the compiler then knows they touch no
+// shared memory and keeps the loads of the store loops ahead of them.
+__device__ __forceinline__ void st_global_f32(float* p, float v) {
+  asm volatile("st.global.f32 [%0], %1;" ::"l"(p), "f"(v));
+}
+__device__ __forceinline__ void st_global_bf16(uint16_t* p, float v) {
+  asm volatile("st.global.b16 [%0], %1;" ::"l"(p), "h"(f2bf(v)));
+}
+
+// 2D tiled TMA store of a shared-memory tile at (x0, y0); the part outside
+// the tensor is not written.  Waits until the tile has been read out of
+// shared memory.
+__device__ __forceinline__ void tma_store_2d_wait(const CUtensorMap* map, int x0, int y0, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x0),
+               "r"(y0), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // 2D tiled TMA load of box {64 elements, 64 rows} at (k0, m0), completing on bar.
@@ -278,7 +299,8 @@ __device__ __forceinline__ bool elect_one() {
 template <int FMT, int KIND>
 __global__ void __launch_bounds__(PF_THREADS, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap0,
-                        const __grid_constant__ CUtensorMap wmap1, const PrefillArgs a) {
+                        const __grid_constant__ CUtensorMap wmap1, const __grid_constant__ CUtensorMap omap,
+                        const PrefillArgs a) {
   using SH = PfShape<FMT, KIND>;
   constexpr int SA = SH::SA, SB = SH::SB, FT = SH::FT;
   constexpr uint32_t NCOLS = 2 * PF_COLS;   // two accumulator buffers of 256 columns
@@ -293,6 +315,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
   __shared__ __align__(16) float xg_sh[2][PF_COLS];  // X'_g of the tile's rows, two groups
+  __shared__ __align__(16) float einv_sh[PF_COLS];   // 2^-e_m of the tile's rows
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rt = blockIdx.x / a.n_ctiles, ct = blockIdx.x - rt * a.n_ctiles;
@@ -451,6 +474,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           : "memory");
       return res != 0;
     };
+    // the tile's row scales (padded rows hold 0) with group 0's sums
+    if (tid < PF_COLS / 4) cp_async16(&einv_sh[4 * tid], a.einv + m0 + 4 * tid);
     fetch_xg(0);
     cp_async_wait_all();
     epi_sync();
@@ -494,43 +519,72 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     }
     if (!aborted) {
       const int cbase = wg * HALF;
-      auto store = [&](int j, float outv) {
-        const int m = m0 + cbase + j;
-        if (m < a.M && okr) {
-          if (a.out_f32)
-            static_cast<float*>(a.out)[(size_t)m * a.N + n] = outv;
-          else
-            static_cast<uint16_t*>(a.out)[(size_t)m * a.N + n] = f2bf(outv);
-        }
-      };
+      const float* ei = einv_sh + cbase;
+      const int jmax = min(HALF, a.M - m0 - cbase);
+      const size_t obase = (size_t)(m0 + cbase) * a.N + n;
+      // bf16 output tile [256 rows][FT features], row-major, for one TMA store
+      // (ring A is idle now: every copy and MMA has completed)
+      uint16_t* stg = reinterpret_cast<uint16_t*>(smem + (KIND == 0 ? 64 * 1024 : 0));
       if constexpr (KIND == 0) {
         // the up rows hand their totals to the gate rows through shared
-        // memory (ring A is idle now: every copy and MMA has completed),
-        // column-major so that consecutive rows hit consecutive banks
+        // memory, column-major so that consecutive rows hit consecutive banks
         float* xch = reinterpret_cast<float*>(smem);  // [PF_COLS][64]
         if (mat == 1) {
 #pragma unroll
           for (int j = 0; j < HALF; ++j) xch[(cbase + j) * 64 + (r - 64)] = acc[j];
         }
         epi_sync();
-        if (mat == 0) {
+        if (mat == 0 && a.tma_store) {
 #pragma unroll
           for (int j = 0; j < HALF; ++j) {
-            const int m = m0 + cbase + j;
-            const float ei = m < a.M ? a.einv[m] : 0.f;
-            const float g = acc[j] * ei, u = xch[(cbase + j) * 64 + r] * ei;
-            store(j, g / (1.0f + expf(-g)) * u);  // silu(gate) * up
+            const float g = acc[j] * ei[j], u = xch[(cbase + j) * 64 + r] * ei[j];
+            stg[(cbase + j) * FT + r] = f2bf(g / (1.0f + expf(-g)) * u);  // silu(gate) * up
           }
         }
-      } else {
+        if (mat == 0 && okr && !a.tma_store) {
 #pragma unroll
-        for (int j = 0; j < HALF; ++j) {
-          const int m = m0 + cbase + j;
-          if (m < a.M && okr) {
-            const float v = acc[j] * a.einv[m];
-            store(j, a.res ? v + bf16f(a.res[(size_t)m * a.res_ld + n]) : v);  // + residual or bias
+          for (int j = 0; j < HALF; ++j) {
+            const float g = acc[j] * ei[j], u = xch[(cbase + j) * 64 + r] * ei[j];
+            const float h = g / (1.0f + expf(-g)) * u;  // silu(gate) * up
+            if (j < jmax) {
+              if (a.out_f32)
+                st_global_f32(static_cast<float*>(a.out) + obase + (size_t)j * a.N, h);
+              else
+                st_global_bf16(static_cast<uint16_t*>(a.out) + obase + (size_t)j * a.N, h);
+            }
           }
         }
+      } else if (okr || a.tma_store) {
+        // down / projection: 16 columns at a time, their addends loaded
+        // together, then stored
+        const uint16_t* __restrict__ res = a.res;
+#pragma unroll
+        for (int q = 0; q < HALF / 16; ++q) {
+          float add[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int j = q * 16 + e;
+            add[e] = (res && okr && j < jmax) ? bf16f(__ldg(res + (size_t)(m0 + cbase + j) * a.res_ld + n)) : 0.f;
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int j = q * 16 + e;
+            const float v = acc[j] * ei[j] + add[e];  // + residual or bias
+            if (a.tma_store) {
+              stg[(cbase + j) * FT + r] = f2bf(v);
+            } else if (j < jmax) {
+              if (a.out_f32)
+                st_global_f32(static_cast<float*>(a.out) + obase + (size_t)j * a.N, v);
+              else
+                st_global_bf16(static_cast<uint16_t*>(a.out) + obase + (size_t)j * a.N, v);
+            }
+          }
+        }
+      }
+      if (a.tma_store) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // tile writes -> TMA reads
+        epi_sync();
+        if (tid == 0) tma_store_2d_wait(&omap, f0, m0, smem_u32(stg));
       }
     }
   }
@@ -608,7 +662,21 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
       return cuda_fail(cudaErrorInvalidValue);
   }
 
+  // bf16 output tiles go out by TMA when a row is a multiple of 16 bytes
+  CUtensorMap omap = xmap;
+  const bool tma_store = !p.out_f32 && N % 8 == 0;
+  if (tma_store) {
+    const cuuint64_t odims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    const cuuint64_t ostr[1] = {(cuuint64_t)N * 2};
+    const cuuint32_t obox[2] = {(cuuint32_t)SH::FT, (cuuint32_t)PF_COLS};
+    if (enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, odims, ostr, obox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+      return cuda_fail(cudaErrorInvalidValue);
+  }
+
   PrefillArgs a = {};
+  a.tma_store = tma_store ? 1 : 0;
   a.W0 = static_cast<const uint8_t*>(p.W0);
   a.W1 = static_cast<const uint8_t*>(p.W1);
   a.s0 = p.s0; a.b0 = p.b0; a.s1 = p.s1; a.b1 = p.b1;
@@ -643,7 +711,7 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
       if (dev < 64) attr_set[dev] = true;
     }
   }
-  return launch(kern, dim3((unsigned)(n_rtiles * n_ctiles)), dim3(PF_THREADS), smem, l, xmap, wmap[0], wmap[1], a);
+  return launch(kern, dim3((unsigned)(n_rtiles * n_ctiles)), dim3(PF_THREADS), smem, l, xmap, wmap[0], wmap[1], omap, a);
 }
 
 mt_status launch_prefill(const GemvProblem& p, void* ws, const Launch& l) {

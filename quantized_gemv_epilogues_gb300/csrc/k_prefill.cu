@@ -273,20 +273,21 @@ __device__ __forceinline__ void pf_convert_row(const unsigned char* ctile, unsig
 // Shared-memory plan of one (format, kind).  The MMA's A tile is 128 weight
 // rows: 128 output features (down / projection), or the gate rows (0-63) and
 // the up rows (64-127) of 64 output features (gate/up), so that one MMA per K
-// step covers both matrices.  Ring A (TMA): per slot the x tile (256 rows x
-// 128 B, 128-byte swizzle) and the code tile (128 rows x CB bytes); ring B:
-// the fp16 A tiles.
+// step covers both matrices.  Three rings: X, the x tiles (256 rows x 128 B,
+// 128-byte swizzle; TMA in, freed by the MMA); C, the code tiles (128 rows x
+// CB bytes; TMA in, freed by the converters, so they are fetched further
+// ahead); B, the fp16 A tiles (converters in, freed by the MMA).
 template <int FMT, int KIND>
 struct PfShape {
   static constexpr int FT = KIND == 0 ? 64 : 128;       // output features per tile
   static constexpr int CB = FMT == FMT_A8 ? 64 : 32;    // code bytes per row and K block
   static constexpr int CTILE = PF_ROWS * CB;            // 8 or 4 KB
-  static constexpr int SA = 4, SB = 3;                  // ring depths
-  static constexpr int SLOT_A = PF_X_TILE + CTILE;      // multiple of 1024
-  static constexpr int SLOT_B = PF_W_TILE;
-  static constexpr size_t SMEM = 1024 + (size_t)SA * SLOT_A + (size_t)SB * SLOT_B;
-  static_assert(SMEM <= 216 * 1024, "shared memory plan");
-  static_assert((size_t)SA * SLOT_A >= (size_t)64 * PF_COLS * 4, "gate/up exchange buffer");
+  static constexpr int SX = 5, SC = FMT == FMT_A8 ? 3 : 6, SB = 2;  // ring depths
+  static constexpr size_t OFF_C = (size_t)SX * PF_X_TILE;
+  static constexpr size_t OFF_B = OFF_C + (size_t)SC * CTILE;
+  static constexpr size_t SMEM = 1024 + OFF_B + (size_t)SB * PF_W_TILE;
+  static_assert(SMEM <= 218 * 1024, "shared memory plan");
+  static_assert(OFF_C >= (size_t)64 * PF_COLS * 4 + (size_t)PF_COLS * 128 * 2, "final-phase buffers in ring X");
 };
 
 // 1 in exactly one lane of the (converged) warp.
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                         const __grid_constant__ CUtensorMap wmap1, const __grid_constant__ CUtensorMap omap,
                         const PrefillArgs a) {
   using SH = PfShape<FMT, KIND>;
-  constexpr int SA = SH::SA, SB = SH::SB, FT = SH::FT;
+  constexpr int SX = SH::SX, SC = SH::SC, SB = SH::SB, FT = SH::FT;
   constexpr uint32_t NCOLS = 2 * PF_COLS;   // two accumulator buffers of 256 columns
   constexpr int EPI = 32 * PF_EPI_WARPS;    // epilogue threads
   constexpr int HALF = PF_COLS / 2;         // tile columns per epilogue warpgroup (128)
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   // 1024-byte aligned start, by an offset on the shared array itself (so the
   // compiler keeps shared-space loads and stores)
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) uint64_t bars[2 * SA + 2 * SB + 5];
+  __shared__ __align__(8) uint64_t bars[2 * (SX + SC + SB) + 5];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
   __shared__ __align__(16) float xg_sh[2][PF_COLS];  // X'_g of the tile's rows, two groups
@@ -321,25 +322,31 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const int rt = blockIdx.x / a.n_ctiles, ct = blockIdx.x - rt * a.n_ctiles;
   const int f0 = rt * FT, m0 = ct * PF_COLS;  // first output feature and activation row
   const int KB = a.KB, G = a.G, Mp = a.n_ctiles * PF_COLS;
-  auto in_full = [&](int i) { return smem_u32(&bars[i]); };            // TMA bytes of slot i of ring A
-  auto a_free = [&](int i) { return smem_u32(&bars[SA + i]); };        // converters + MMA done with it
-  auto w_full = [&](int i) { return smem_u32(&bars[2 * SA + i]); };    // converters wrote slot i of ring B
-  auto b_free = [&](int i) { return smem_u32(&bars[2 * SA + SB + i]); };  // MMA done with it
-  auto acc_full = [&](int b) { return smem_u32(&bars[2 * SA + 2 * SB + b]); };
-  auto acc_free = [&](int b) { return smem_u32(&bars[2 * SA + 2 * SB + 2 + b]); };
-  const uint32_t mma_done = smem_u32(&bars[2 * SA + 2 * SB + 4]);
-  auto xslot = [&](int i) { return smem + (size_t)i * SH::SLOT_A; };
-  auto cslot = [&](int i) { return smem + (size_t)i * SH::SLOT_A + PF_X_TILE; };
-  auto wslot = [&](int i) { return smem + (size_t)SA * SH::SLOT_A + (size_t)i * SH::SLOT_B; };
+  auto x_full = [&](int i) { return smem_u32(&bars[i]); };                  // TMA bytes of x slot i
+  auto x_free = [&](int i) { return smem_u32(&bars[SX + i]); };             // MMA done with it
+  auto c_full = [&](int i) { return smem_u32(&bars[2 * SX + i]); };         // TMA bytes of code slot i
+  auto c_free = [&](int i) { return smem_u32(&bars[2 * SX + SC + i]); };    // converters done with it
+  auto w_full = [&](int i) { return smem_u32(&bars[2 * (SX + SC) + i]); };  // converters wrote A slot i
+  auto b_free = [&](int i) { return smem_u32(&bars[2 * (SX + SC) + SB + i]); };  // MMA done with it
+  auto acc_full = [&](int b) { return smem_u32(&bars[2 * (SX + SC + SB) + b]); };
+  auto acc_free = [&](int b) { return smem_u32(&bars[2 * (SX + SC + SB) + 2 + b]); };
+  const uint32_t mma_done = smem_u32(&bars[2 * (SX + SC + SB) + 4]);
+  auto xslot = [&](int i) { return smem + (size_t)i * PF_X_TILE; };
+  auto cslot = [&](int i) { return smem + SH::OFF_C + (size_t)i * SH::CTILE; };
+  auto wslot = [&](int i) { return smem + SH::OFF_B + (size_t)i * PF_W_TILE; };
   constexpr int CONV0 = PF_EPI_WARPS;                   // first converter warp
   constexpr int MMA_WARP = PF_EPI_WARPS + PF_CONV_WARPS;
   constexpr int TMA_WARP = MMA_WARP + 1;
   constexpr int CONV = 32 * PF_CONV_WARPS;              // converter threads
 
   if (tid == 0) {
-    for (int i = 0; i < SA; ++i) {
-      mbar_init(in_full(i), 1);
-      mbar_init(a_free(i), CONV + 1);
+    for (int i = 0; i < SX; ++i) {
+      mbar_init(x_full(i), 1);
+      mbar_init(x_free(i), 1);
+    }
+    for (int i = 0; i < SC; ++i) {
+      mbar_init(c_full(i), 1);
+      mbar_init(c_free(i), CONV);
     }
     for (int i = 0; i < SB; ++i) {
       mbar_init(w_full(i), CONV);
@@ -369,35 +376,43 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   };
 
   if (warp == TMA_WARP) {
-    // ---- producer: x tile and code tile of each K block, SA blocks ahead
-    if (lane == 0) {
+    // ---- producers: lane 0 the x tiles (SX blocks ahead of the MMA), lane 1
+    // the code tiles (SC blocks ahead of the converters)
+    if (lane < 2) {
+      const int S = lane == 0 ? SX : SC;
       int issued = 0;
       for (int kb = 0; kb < KB; ++kb) {
-        const int i = kb % SA;
-        if (kb >= SA && !mbar_wait_bounded(a_free(i), ((kb / SA) + 1) & 1)) { fail(); break; }
+        const int i = kb % S;
+        const uint32_t full = lane == 0 ? x_full(i) : c_full(i), free_ = lane == 0 ? x_free(i) : c_free(i);
+        if (kb >= S && !mbar_wait_bounded(free_, ((kb / S) + 1) & 1)) { fail(); break; }
         if (*abort_flag) break;
-        mbar_arrive_expect_tx(in_full(i), PF_X_TILE + SH::CTILE);
-        tma_load_2d(smem_u32(xslot(i)), &xmap, kb * PF_KB, m0, in_full(i));
-        tma_load_2d(smem_u32(cslot(i)), &wmap0, kb * SH::CB, f0, in_full(i));
-        if constexpr (KIND == 0) tma_load_2d(smem_u32(cslot(i) + 64 * SH::CB), &wmap1, kb * SH::CB, f0, in_full(i));
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, PF_X_TILE);
+          tma_load_2d(smem_u32(xslot(i)), &xmap, kb * PF_KB, m0, full);
+        } else {
+          mbar_arrive_expect_tx(full, SH::CTILE);
+          tma_load_2d(smem_u32(cslot(i)), &wmap0, kb * SH::CB, f0, full);
+          if constexpr (KIND == 0) tma_load_2d(smem_u32(cslot(i) + 64 * SH::CB), &wmap1, kb * SH::CB, f0, full);
+        }
         ++issued;
       }
       // copies still in flight (only after an abort) land before the CTA ends
-      for (int kb = max(0, issued - SA); kb < issued; ++kb) (void)mbar_wait_bounded(in_full(kb % SA), (kb / SA) & 1);
+      for (int kb = max(0, issued - S); kb < issued; ++kb)
+        (void)mbar_wait_bounded(lane == 0 ? x_full(kb % S) : c_full(kb % S), (kb / S) & 1);
     }
     __syncwarp();
   } else if (warp >= CONV0 && warp < MMA_WARP) {
     // ---- converters: rows c, c + CONV of the code tile into the fp16 A tile
     const int c = tid - 32 * CONV0;
     for (int kb = 0; kb < KB; ++kb) {
-      const int i = kb % SA, j = kb % SB;
-      if (!mbar_wait_bounded(in_full(i), (kb / SA) & 1)) { fail(); break; }
+      const int i = kb % SC, j = kb % SB;
+      if (!mbar_wait_bounded(c_full(i), (kb / SC) & 1)) { fail(); break; }
       if (kb >= SB && !mbar_wait_bounded(b_free(j), ((kb / SB) + 1) & 1)) { fail(); break; }
 #pragma unroll
       for (int r = c; r < PF_ROWS; r += CONV) pf_convert_row<FMT>(cslot(i), wslot(j), r);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor core reads
       mbar_arrive(w_full(j));
-      mbar_arrive(a_free(i));
+      mbar_arrive(c_free(i));
       if (*abort_flag) break;
     }
   } else if (warp == MMA_WARP) {
@@ -405,8 +420,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int group = a.group;
     bool ok = true;
     for (int kb = 0; kb < KB && ok; ++kb) {
-      const int i = kb % SA, jb = kb % SB;
-      if (!mbar_wait_bounded(in_full(i), (kb / SA) & 1) || !mbar_wait_bounded(w_full(jb), (kb / SB) & 1)) {
+      const int i = kb % SX, jb = kb % SB;
+      if (!mbar_wait_bounded(x_full(i), (kb / SX) & 1) || !mbar_wait_bounded(w_full(jb), (kb / SB) & 1)) {
         ok = false;
         break;
       }
@@ -430,7 +445,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       }
       if (elect_one()) {
         tc_commit(b_free(jb));
-        tc_commit(a_free(i));
+        tc_commit(x_free(i));
       }
       __syncwarp();
       if (*abort_flag) break;
@@ -535,10 +550,18 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
         epi_sync();
         if (mat == 0 && a.tma_store) {
+          // 16 columns at a time: their loads, then their stores
 #pragma unroll
-          for (int j = 0; j < HALF; ++j) {
-            const float g = acc[j] * ei[j], u = xch[(cbase + j) * 64 + r] * ei[j];
-            stg[(cbase + j) * FT + r] = f2bf(g / (1.0f + expf(-g)) * u);  // silu(gate) * up
+          for (int q = 0; q < HALF / 16; ++q) {
+            float u[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) u[e] = xch[(cbase + q * 16 + e) * 64 + r];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int j = q * 16 + e;
+              const float g = acc[j] * ei[j];
+              stg[(cbase + j) * FT + r] = f2bf(g / (1.0f + expf(-g)) * (u[e] * ei[j]));  // silu(gate) * up
+            }
           }
         }
         if (mat == 0 && okr && !a.tma_store) {

@@ -692,7 +692,7 @@ def run_prefill(args, torch, synth, mt, dev):
         synth.device_bf16(res, synth.seed_for(wl.wid, M, synth.T_RES3), synth.ACT)
         h = torch.empty(M, f, dtype=bf, device=dev)
         y = torch.empty(M, d, dtype=bf, device=dev)
-        ws = torch.empty(max(mt.mt_prefill_workspace_bytes(M, d, g), mt.mt_prefill_workspace_bytes(M, f, g)),
+        ws = torch.empty(max(mt.mt_prefill_workspace_bytes(M, d, f, g), mt.mt_prefill_workspace_bytes(M, f, d, g)),
                          dtype=torch.uint8, device=dev)
 
         def gateup():

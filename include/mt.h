@@ -215,10 +215,12 @@ mt_status mt_linear_bias(const void* x, const void* W, const void* scales,
  * registers); "Compute-Graph Fusion", Automatic Gated Epilogues.
  *   Arguments, layouts and results as mt_swiglu_gateup / mt_down_residual /
  *   mt_linear_bias, plus a caller-owned device workspace of at least
- *   mt_prefill_workspace_bytes(M, K, group) bytes (16-byte aligned; K is d
- *   for gate/up, f for down) that holds the activations converted for the
- *   tensor cores; it must not overlap any argument.  The call allocates
- *   nothing and never synchronises.
+ *   mt_prefill_workspace_bytes(M, K, N, group) bytes (16-byte aligned; K, N
+ *   are d, f for gate/up and f, d for down) that holds the activations
+ *   converted for the tensor cores and, when the output tiles do not fill
+ *   the GPU, the partial sums of K slices (added in a fixed order by a second
+ *   kernel); it must not overlap any argument.  The call allocates nothing
+ *   and never synchronises.
  * Formats: MT_W_AFFINE8, MT_W_AFFINE4 (group 32, 64 or 128).
  * Limits: 1 <= M <= 2^20; K % 64 == 0 and K % group == 0; 64 <= K <= 65536;
  *         1 <= N <= 2^20.  A workspace below the required size is
@@ -229,7 +231,7 @@ mt_status mt_linear_bias(const void* x, const void* W, const void* scales,
  * value above 2^-28 of the row's maximum); scales, biases and the total are
  * fp32.
  */
-size_t mt_prefill_workspace_bytes(int M, int K, int group);
+size_t mt_prefill_workspace_bytes(int M, int K, int N, int group);
 mt_status mt_prefill_swiglu_gateup(const void* x, const void* Wg, const void* Wu,
                                    const void* scales, const void* biases, int group,
                                    void* out_h, int M, int d, int f, mt_wfmt fmt,

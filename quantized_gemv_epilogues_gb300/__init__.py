@@ -57,7 +57,7 @@ _SIGS = {
     "mt_pack_affine": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "mt_unpack_affine": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "mt_pack_mx": (_I, [_P, _I, _I, _I, _P, _P, _P]),
-    "mt_prefill_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
+    "mt_prefill_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "mt_prefill_swiglu_gateup": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, ctypes.c_size_t, _P]),
     "mt_prefill_down_residual": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, ctypes.c_size_t, _P]),
     "mt_prefill_linear_bias": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, ctypes.c_size_t, _P]),
@@ -188,12 +188,12 @@ def mt_linear_bias(x, W, scales, biases, group, bias, out_y, M=None, K=None, N=N
            "mt_linear_bias")
 
 
-def mt_prefill_workspace_bytes(M, K, group):
-    return int(_lib.mt_prefill_workspace_bytes(int(M), int(K), int(group)))
+def mt_prefill_workspace_bytes(M, K, N, group):
+    return int(_lib.mt_prefill_workspace_bytes(int(M), int(K), int(N), int(group)))
 
 
-def _ws(workspace, M, K, group):
-    need = mt_prefill_workspace_bytes(M, K, group)
+def _ws(workspace, M, K, N, group):
+    need = mt_prefill_workspace_bytes(M, K, N, group)
     if workspace is None:
         raise TypeError(f"a device workspace of at least {need} bytes is required")
     nbytes = workspace.numel() * workspace.element_size() if not isinstance(workspace, int) else need
@@ -209,7 +209,7 @@ def mt_prefill_swiglu_gateup(x, Wg, Wu, scales, biases, group, out_h, workspace,
     if fmt is None:
         raise TypeError("fmt (MT_W_AFFINE8 / MT_W_AFFINE4) is required")
     od = _odt(out_h, out_dtype) if not isinstance(out_h, int) else (out_dtype or MT_BF16)
-    wp, wb = _ws(workspace, M, d, group)
+    wp, wb = _ws(workspace, M, d, f, group)
     _check(_lib.mt_prefill_swiglu_gateup(_ptr(x), _ptr(Wg), _ptr(Wu), _ptr(scales), _ptr(biases), int(group),
                                          _ptr(out_h), M, d, f, int(fmt), od, wp,
                                          workspace_bytes if workspace_bytes is not None else wb, _stream(stream)),
@@ -225,7 +225,7 @@ def mt_prefill_down_residual(h, Wd, scales, biases, group, residual, out_y, work
     if fmt is None:
         raise TypeError("fmt (MT_W_AFFINE8 / MT_W_AFFINE4) is required")
     od = _odt(out_y, out_dtype) if not isinstance(out_y, int) else (out_dtype or MT_BF16)
-    wp, wb = _ws(workspace, M, f, group)
+    wp, wb = _ws(workspace, M, f, d, group)
     _check(_lib.mt_prefill_down_residual(_ptr(h), _ptr(Wd), _ptr(scales), _ptr(biases), int(group),
                                          _ptr(residual), _ptr(out_y), M, f, d, int(fmt), od, wp,
                                          workspace_bytes if workspace_bytes is not None else wb, _stream(stream)),
@@ -241,7 +241,7 @@ def mt_prefill_linear_bias(x, W, scales, biases, group, bias, out_y, workspace, 
     if fmt is None:
         raise TypeError("fmt (MT_W_AFFINE8 / MT_W_AFFINE4) is required")
     od = _odt(out_y, out_dtype) if not isinstance(out_y, int) else (out_dtype or MT_BF16)
-    wp, wb = _ws(workspace, M, K, group)
+    wp, wb = _ws(workspace, M, K, N, group)
     _check(_lib.mt_prefill_linear_bias(_ptr(x), _ptr(W), _ptr(scales), _ptr(biases), int(group), _ptr(bias),
                                        _ptr(out_y), M, K, N, int(fmt), od, wp,
                                        workspace_bytes if workspace_bytes is not None else wb, _stream(stream)),

@@ -46,6 +46,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "k_gemv.cuh"
@@ -53,12 +54,11 @@
 namespace mt {
 
 constexpr int PF_ROWS = 128;       // weight rows per tile (MMA M)
-constexpr int PF_COLS = 256;       // activation rows per tile (MMA N)
+constexpr int PF_COLS = 256;       // largest activation-row tile (MMA N); 64 and 128 for small M
 constexpr int PF_KB = 64;          // K per stage (one 128-byte swizzle row of fp16)
 constexpr int PF_EPI_WARPS = 8;    // warps 0-7: epilogue, two warpgroups (64 tile columns each)
 constexpr int PF_CONV_WARPS = 2;   // warps 8-9: converters
 constexpr int PF_THREADS = 32 * (PF_EPI_WARPS + PF_CONV_WARPS + 2);  // + warp 10: MMA, warp 11: TMA
-constexpr int PF_X_TILE = PF_COLS * PF_KB * 2;   // 32 KB
 constexpr int PF_W_TILE = PF_ROWS * PF_KB * 2;   // 16 KB
 
 struct PrefillArgs {
@@ -75,7 +75,10 @@ struct PrefillArgs {
   void* out;            // [M][N]
   int out_f32;
   int M, K, N, group, lg_group, G, KB, row_bytes;
-  int n_ctiles;         // ceil(M / 256)
+  int n_ctiles;         // ceil(M / NT)
+  int Mp;               // row stride of XgT (M rounded up to 256)
+  int ks, KBs;          // K slices (split K when the tiles do not fill the GPU) and K blocks per slice
+  float* part;          // ks > 1: partial sums [ks][NW][Mp][N] before the row scale and epilogue
   int tma_store;        // 1: bf16 output written by one TMA store per tile (row stride a multiple of 16 B)
   int* err;             // device error word
 };
@@ -97,14 +100,17 @@ __device__ __forceinline__ uint64_t pf_desc_sw128(uint32_t saddr) {
 
 // Instruction descriptor: fp32 accumulator, fp16 A and B, both K-major,
 // N = 64, M = 128.
-constexpr uint32_t PF_IDESC = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(PF_COLS >> 3) << 17) |
-                              ((uint32_t)(PF_ROWS >> 4) << 24);
+template <int NT>
+__host__ __device__ constexpr uint32_t pf_idesc() {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(PF_ROWS >> 4) << 24);
+}
 
+template <int NT>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(PF_IDESC), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(pf_idesc<NT>()), "r"(accumulate)
       : "memory");
 }
 
@@ -277,17 +283,22 @@ __device__ __forceinline__ void pf_convert_row(const unsigned char* ctile, unsig
 // 128-byte swizzle; TMA in, freed by the MMA); C, the code tiles (128 rows x
 // CB bytes; TMA in, freed by the converters, so they are fetched further
 // ahead); B, the fp16 A tiles (converters in, freed by the MMA).
-template <int FMT, int KIND>
+template <int FMT, int KIND, int NT>
 struct PfShape {
+  static constexpr int XT = NT * PF_KB * 2;             // x tile bytes (8, 16 or 32 KB)
   static constexpr int FT = KIND == 0 ? 64 : 128;       // output features per tile
   static constexpr int CB = FMT == FMT_A8 ? 64 : 32;    // code bytes per row and K block
   static constexpr int CTILE = PF_ROWS * CB;            // 8 or 4 KB
-  static constexpr int SX = 5, SC = FMT == FMT_A8 ? 3 : 6, SB = 2;  // ring depths
-  static constexpr size_t OFF_C = (size_t)SX * PF_X_TILE;
+  // ring depths: narrow tiles (small M, weights streamed from HBM once) keep
+  // more code tiles in flight; wide tiles more x tiles
+  static constexpr int SX = NT == 128 ? 5 : 4;
+  static constexpr int SC = (NT == 64 ? 96 : (NT == 128 ? 64 : 48)) * 1024 / CTILE;
+  static constexpr int SB = NT == 256 ? 2 : 4;
+  static constexpr size_t OFF_C = (size_t)SX * XT;
   static constexpr size_t OFF_B = OFF_C + (size_t)SC * CTILE;
   static constexpr size_t SMEM = 1024 + OFF_B + (size_t)SB * PF_W_TILE;
   static_assert(SMEM <= 218 * 1024, "shared memory plan");
-  static_assert(OFF_C >= (size_t)64 * PF_COLS * 4 + (size_t)PF_COLS * 128 * 2, "final-phase buffers in ring X");
+  static_assert(OFF_C >= (size_t)64 * NT * 4 + (size_t)NT * 128 * 2, "final-phase buffers in ring X");
 };
 
 // 1 in exactly one lane of the (converged) warp.
@@ -297,16 +308,16 @@ __device__ __forceinline__ bool elect_one() {
   return e != 0;
 }
 
-template <int FMT, int KIND>
+template <int FMT, int KIND, int NT>
 __global__ void __launch_bounds__(PF_THREADS, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap0,
                         const __grid_constant__ CUtensorMap wmap1, const __grid_constant__ CUtensorMap omap,
                         const PrefillArgs a) {
-  using SH = PfShape<FMT, KIND>;
+  using SH = PfShape<FMT, KIND, NT>;
   constexpr int SX = SH::SX, SC = SH::SC, SB = SH::SB, FT = SH::FT;
-  constexpr uint32_t NCOLS = 2 * PF_COLS;   // two accumulator buffers of 256 columns
+  constexpr uint32_t NCOLS = 2 * NT;        // two accumulator buffers of NT columns
   constexpr int EPI = 32 * PF_EPI_WARPS;    // epilogue threads
-  constexpr int HALF = PF_COLS / 2;         // tile columns per epilogue warpgroup (128)
+  constexpr int HALF = NT / 2;              // tile columns per epilogue warpgroup
 
   extern __shared__ unsigned char smem_raw[];
   // 1024-byte aligned start, by an offset on the shared array itself (so the
@@ -315,13 +326,16 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   __shared__ __align__(8) uint64_t bars[2 * (SX + SC + SB) + 5];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
-  __shared__ __align__(16) float xg_sh[2][PF_COLS];  // X'_g of the tile's rows, two groups
-  __shared__ __align__(16) float einv_sh[PF_COLS];   // 2^-e_m of the tile's rows
+  __shared__ __align__(16) float xg_sh[2][NT];  // X'_g of the tile's rows, two groups
+  __shared__ __align__(16) float einv_sh[NT];   // 2^-e_m of the tile's rows
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rt = blockIdx.x / a.n_ctiles, ct = blockIdx.x - rt * a.n_ctiles;
-  const int f0 = rt * FT, m0 = ct * PF_COLS;  // first output feature and activation row
-  const int KB = a.KB, G = a.G, Mp = a.n_ctiles * PF_COLS;
+  const int tile = blockIdx.x / a.ks, sk = blockIdx.x - tile * a.ks;
+  const int rt = tile / a.n_ctiles, ct = tile - rt * a.n_ctiles;
+  const int f0 = rt * FT, m0 = ct * NT;  // first output feature and activation row
+  // this CTA's K slice: K blocks [kb0, kb0 + KB) and groups [g0, g0 + G)
+  const int kb0 = sk * a.KBs, KB = min(a.KB - kb0, a.KBs);
+  const int g0 = kb0 * PF_KB / a.group, G = KB * PF_KB / a.group, Gall = a.G, Mp = a.Mp;
   auto x_full = [&](int i) { return smem_u32(&bars[i]); };                  // TMA bytes of x slot i
   auto x_free = [&](int i) { return smem_u32(&bars[SX + i]); };             // MMA done with it
   auto c_full = [&](int i) { return smem_u32(&bars[2 * SX + i]); };         // TMA bytes of code slot i
@@ -331,7 +345,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   auto acc_full = [&](int b) { return smem_u32(&bars[2 * (SX + SC + SB) + b]); };
   auto acc_free = [&](int b) { return smem_u32(&bars[2 * (SX + SC + SB) + 2 + b]); };
   const uint32_t mma_done = smem_u32(&bars[2 * (SX + SC + SB) + 4]);
-  auto xslot = [&](int i) { return smem + (size_t)i * PF_X_TILE; };
+  auto xslot = [&](int i) { return smem + (size_t)i * SH::XT; };
   auto cslot = [&](int i) { return smem + SH::OFF_C + (size_t)i * SH::CTILE; };
   auto wslot = [&](int i) { return smem + SH::OFF_B + (size_t)i * PF_W_TILE; };
   constexpr int CONV0 = PF_EPI_WARPS;                   // first converter warp
@@ -386,13 +400,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const uint32_t full = lane == 0 ? x_full(i) : c_full(i), free_ = lane == 0 ? x_free(i) : c_free(i);
         if (kb >= S && !mbar_wait_bounded(free_, ((kb / S) + 1) & 1)) { fail(); break; }
         if (*abort_flag) break;
+        const int kg = kb0 + kb;  // K block of the tensor
         if (lane == 0) {
-          mbar_arrive_expect_tx(full, PF_X_TILE);
-          tma_load_2d(smem_u32(xslot(i)), &xmap, kb * PF_KB, m0, full);
+          mbar_arrive_expect_tx(full, SH::XT);
+          tma_load_2d(smem_u32(xslot(i)), &xmap, kg * PF_KB, m0, full);
         } else {
           mbar_arrive_expect_tx(full, SH::CTILE);
-          tma_load_2d(smem_u32(cslot(i)), &wmap0, kb * SH::CB, f0, full);
-          if constexpr (KIND == 0) tma_load_2d(smem_u32(cslot(i) + 64 * SH::CB), &wmap1, kb * SH::CB, f0, full);
+          tma_load_2d(smem_u32(cslot(i)), &wmap0, kg * SH::CB, f0, full);
+          if constexpr (KIND == 0) tma_load_2d(smem_u32(cslot(i) + 64 * SH::CB), &wmap1, kg * SH::CB, f0, full);
         }
         ++issued;
       }
@@ -430,15 +445,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       const uint64_t wd = pf_desc_sw128(smem_u32(wslot(jb)));
 #pragma unroll
       for (int j = 0; j < PF_KB / 16; ++j) {
-        const int k = kb * PF_KB + 16 * j;
-        const int gi = k >> a.lg_group, b = gi & 1;
+        const int k = kb * PF_KB + 16 * j;       // K within the slice (slices start on a group)
+        const int gi = k >> a.lg_group, b = gi & 1;  // group within the slice
         const bool first = (k & (group - 1)) == 0;
         if (first && gi >= 2) {
           if (!mbar_wait_bounded(acc_free(b), ((gi >> 1) - 1) & 1)) { ok = false; break; }
           tc_fence_after();
         }
         if (elect_one()) {
-          tc_mma(tbase + (uint32_t)(b * PF_COLS), wd + 2 * j, xd + 2 * j, first ? 0u : 1u);
+          tc_mma<NT>(tbase + (uint32_t)(b * NT), wd + 2 * j, xd + 2 * j, first ? 0u : 1u);
           if (((k + 16) & (group - 1)) == 0) tc_commit(acc_full(b));
         }
         __syncwarp();
@@ -463,7 +478,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const bool okr = n < a.N;
     const uint16_t* sp = mat ? a.s1 : a.s0;
     const uint16_t* bp = mat ? a.b1 : a.b0;
-    const size_t sbo = (size_t)(okr ? n : 0) * G;
+    const size_t sbo = (size_t)(okr ? n : 0) * Gall + g0;
     float acc[HALF];
 #pragma unroll
     for (int j = 0; j < HALF; ++j) acc[j] = 0.f;
@@ -474,7 +489,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // X'_g of group gi for the tile's rows comes into xg_sh[gi & 1] by
     // asynchronous copies one group ahead (threads 0-63, 16 bytes each)
     auto fetch_xg = [&](int gi) {
-      if (tid < PF_COLS / 4) cp_async16(&xg_sh[gi & 1][4 * tid], a.XgT + (size_t)gi * Mp + m0 + 4 * tid);
+      if (tid < NT / 4) cp_async16(&xg_sh[gi & 1][4 * tid], a.XgT + (size_t)(g0 + gi) * Mp + m0 + 4 * tid);
       cp_async_commit();
     };
     auto epi_sync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(EPI) : "memory"); };
@@ -490,7 +505,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       return res != 0;
     };
     // the tile's row scales (padded rows hold 0) with group 0's sums
-    if (tid < PF_COLS / 4) cp_async16(&einv_sh[4 * tid], a.einv + m0 + 4 * tid);
+    if (tid < NT / 4) cp_async16(&einv_sh[4 * tid], a.einv + m0 + 4 * tid);
     fetch_xg(0);
     cp_async_wait_all();
     epi_sync();
@@ -509,7 +524,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 #pragma unroll
         for (int q = 0; q < HALF / 16; ++q) {
           float d[16];
-          tc_ld16_wait(lane_base + (uint32_t)(b * PF_COLS + q * 16), d);
+          tc_ld16_wait(lane_base + (uint32_t)(b * NT + q * 16), d);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float4 X = *reinterpret_cast<const float4*>(xg + q * 16 + 4 * i);
@@ -532,18 +547,25 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       aborted = epi_sync_or(aborted || *abort_flag);
       if (aborted) break;
     }
-    if (!aborted) {
+    if (!aborted && a.ks > 1) {
+      // split K: this slice's sums, before the row scale and the epilogue
+      if (okr) {
+        float* pp = a.part + ((size_t)(sk * (KIND == 0 ? 2 : 1) + mat) * Mp + m0 + wg * HALF) * a.N + n;
+#pragma unroll
+        for (int j = 0; j < HALF; ++j) st_global_f32(pp + (size_t)j * a.N, acc[j]);
+      }
+    } else if (!aborted) {
       const int cbase = wg * HALF;
       const float* ei = einv_sh + cbase;
       const int jmax = min(HALF, a.M - m0 - cbase);
       const size_t obase = (size_t)(m0 + cbase) * a.N + n;
       // bf16 output tile [256 rows][FT features], row-major, for one TMA store
       // (ring A is idle now: every copy and MMA has completed)
-      uint16_t* stg = reinterpret_cast<uint16_t*>(smem + (KIND == 0 ? 64 * 1024 : 0));
+      uint16_t* stg = reinterpret_cast<uint16_t*>(smem + (KIND == 0 ? NT * 64 * 4 : 0));
       if constexpr (KIND == 0) {
         // the up rows hand their totals to the gate rows through shared
         // memory, column-major so that consecutive rows hit consecutive banks
-        float* xch = reinterpret_cast<float*>(smem);  // [PF_COLS][64]
+        float* xch = reinterpret_cast<float*>(smem);  // [NT][64]
         if (mat == 1) {
 #pragma unroll
           for (int j = 0; j < HALF; ++j) xch[(cbase + j) * 64 + (r - 64)] = acc[j];
@@ -618,16 +640,71 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   if (warp == MMA_WARP) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(NCOLS));
 }
 
+// Split K: the slices' partial sums added in slice order, the row scale
+// undone and the epilogue applied (one thread per output element).
+template <int KIND>
+__global__ void __launch_bounds__(256) prefill_finalize_kernel(const float* __restrict__ part, int ks, int Mp,
+                                                               const float* __restrict__ einv, int M, int N,
+                                                               const uint16_t* __restrict__ res, int res_ld,
+                                                               void* out, int out_f32) {
+  constexpr int NW = KIND == 0 ? 2 : 1;
+  const long total = (long)M * N;
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const int m = (int)(i / N), n = (int)(i - (long)m * N);
+    float v[NW];
+#pragma unroll
+    for (int mat = 0; mat < NW; ++mat) {
+      float t = 0.f;
+      for (int s = 0; s < ks; ++s) t += part[((size_t)(s * NW + mat) * Mp + m) * N + n];
+      v[mat] = t * einv[m];
+    }
+    float o;
+    if constexpr (KIND == 0)
+      o = v[0] / (1.0f + expf(-v[0])) * v[NW - 1];  // silu(gate) * up
+    else
+      o = res ? v[0] + bf16f(res[(size_t)m * res_ld + n]) : v[0];  // + residual or bias
+    if (out_f32)
+      static_cast<float*>(out)[i] = o;
+    else
+      static_cast<uint16_t*>(out)[i] = f2bf(o);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 namespace {
 
 size_t al1k(size_t v) { return (v + 1023) / 1024 * 1024; }
 
-// Workspace: x16 [M][K] fp16, XgT [G][Mp] fp32, einv [Mp] fp32.
-size_t prefill_ws_bytes(long M, long K, long group) {
+// The activation-row tile for M rows: the smallest of 64, 128, 256 that holds them.
+int prefill_nt(long M) { return M <= 64 ? 64 : (M <= 128 ? 128 : 256); }
+
+// K slices for a grid of `tiles` CTAs on `sms` SMs: split K when the tiles
+// fill at most half of the SMs, into whole groups, at most 8 slices and at
+// least two groups (and two K blocks) each.  *kbs receives K blocks per slice.
+int prefill_ks(long tiles, long K, long group, int sms, int* kbs) {
+  const int KB = (int)(K / PF_KB);
+  const int gb = group > PF_KB ? (int)(group / PF_KB) : 1;  // K blocks per group (or 1)
+  int ks = 1;
+  if (tiles * 2 <= sms) ks = (int)std::min<long>(8, sms / tiles);
+  ks = std::max(1, std::min(ks, KB / std::max(2, 2 * gb)));
+  int per = (KB + ks - 1) / ks;
+  per = (per + gb - 1) / gb * gb;
+  *kbs = per;
+  return (KB + per - 1) / per;
+}
+
+// Workspace: x16 [M][K] fp16, XgT [G][Mp] fp32, einv [Mp] fp32, and with
+// split K the partial sums [ks][2][Mp][N] fp32 (sized for the larger of the
+// two tilings, gate/up and down / projection).
+size_t prefill_ws_bytes(long M, long K, long N, long group, int sms) {
   const long Mp = (M + PF_COLS - 1) / PF_COLS * PF_COLS;
-  return al1k((size_t)M * K * 2) + al1k((size_t)(K / group) * Mp * 4) + al1k((size_t)Mp * 4);
+  const long nct = (M + prefill_nt(M) - 1) / prefill_nt(M);
+  int kbs = 0;
+  const int ks = std::max(prefill_ks(nct * ((N + 63) / 64), K, group, sms, &kbs),
+                          prefill_ks(nct * ((N + 127) / 128), K, group, sms, &kbs));
+  const size_t part = ks > 1 ? (size_t)ks * 2 * Mp * N * 4 : 0;
+  return al1k((size_t)M * K * 2) + al1k((size_t)(K / group) * Mp * 4) + al1k((size_t)Mp * 4) + al1k(part);
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once.
@@ -646,17 +723,24 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace
 
-template <int FMT, int KIND>
+template <int FMT, int KIND, int NT>
 mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   constexpr int NW = KIND == 0 ? 2 : 1;
   const int M = p.M, K = p.K, N = p.N, group = p.group;
-  const int n_ctiles = (M + PF_COLS - 1) / PF_COLS, Mp = n_ctiles * PF_COLS;
-  const int n_rtiles = (N + PfShape<FMT, KIND>::FT - 1) / PfShape<FMT, KIND>::FT;
+  using SH = PfShape<FMT, KIND, NT>;
+  const int n_ctiles = (M + NT - 1) / NT, Mp = (M + PF_COLS - 1) / PF_COLS * PF_COLS;
+  const int n_rtiles = (N + SH::FT - 1) / SH::FT;
   const int G = K / group;
   unsigned char* w = static_cast<unsigned char*>(ws);
   __half* x16 = reinterpret_cast<__half*>(w);
   float* XgT = reinterpret_cast<float*>(w + al1k((size_t)M * K * 2));
   float* einv = reinterpret_cast<float*>(w + al1k((size_t)M * K * 2) + al1k((size_t)G * Mp * 4));
+  float* part = reinterpret_cast<float*>(w + al1k((size_t)M * K * 2) + al1k((size_t)G * Mp * 4) + al1k((size_t)Mp * 4));
+  int derr = 0;
+  const DeviceInfo* di = device_info(&derr);
+  if (!di) return cuda_fail((cudaError_t)derr);
+  int kbs = 0;
+  const int ks = prefill_ks((long)n_rtiles * n_ctiles, K, group, di->sm_count, &kbs);
   int* err = device_error_ptr();
   if (!err) return MT_ERR_CUDA;
 
@@ -665,14 +749,13 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   CUtensorMap xmap;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)PF_KB, (cuuint32_t)PF_COLS};
+  const cuuint32_t box[2] = {(cuuint32_t)PF_KB, (cuuint32_t)NT};
   const cuuint32_t estr[2] = {1, 1};
   if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
       CUDA_SUCCESS)
     return cuda_fail(cudaErrorInvalidValue);
   // code tiles: 128 rows x CB bytes, 64-byte (INT8) or 32-byte (INT4) swizzle
-  using SH = PfShape<FMT, KIND>;
   CUtensorMap wmap[2];
   for (int mat = 0; mat < 2; ++mat) {
     const void* W = (mat && NW == 2) ? p.W1 : p.W0;
@@ -691,7 +774,7 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   if (tma_store) {
     const cuuint64_t odims[2] = {(cuuint64_t)N, (cuuint64_t)M};
     const cuuint64_t ostr[1] = {(cuuint64_t)N * 2};
-    const cuuint32_t obox[2] = {(cuuint32_t)SH::FT, (cuuint32_t)PF_COLS};
+    const cuuint32_t obox[2] = {(cuuint32_t)SH::FT, (cuuint32_t)NT};
     if (enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, odims, ostr, obox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
         CUDA_SUCCESS)
@@ -715,12 +798,16 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   a.KB = K / PF_KB;
   a.row_bytes = FMT == FMT_A8 ? K : K / 2;
   a.n_ctiles = n_ctiles;
+  a.Mp = Mp;
+  a.ks = ks;
+  a.KBs = ks > 1 ? kbs : K / PF_KB;
+  a.part = part;
   a.err = err;
 
   mt_status st = launch(prefill_x_kernel, dim3(Mp), dim3(256), 0, l, p.x, M, K, group, x16, XgT, einv);
   if (st != MT_OK) return st;
   const size_t smem = SH::SMEM;
-  auto kern = prefill_gemm_kernel<FMT, KIND>;
+  auto kern = prefill_gemm_kernel<FMT, KIND, NT>;
   static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -734,14 +821,29 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
       if (dev < 64) attr_set[dev] = true;
     }
   }
-  return launch(kern, dim3((unsigned)(n_rtiles * n_ctiles)), dim3(PF_THREADS), smem, l, xmap, wmap[0], wmap[1], omap, a);
+  st = launch(kern, dim3((unsigned)(n_rtiles * n_ctiles * ks)), dim3(PF_THREADS), smem, l, xmap, wmap[0], wmap[1],
+              omap, a);
+  if (st != MT_OK || ks == 1) return st;
+  const long total = (long)M * N;
+  const unsigned fgrid = (unsigned)std::min<long>((total + 255) / 256, (long)di->sm_count * 16);
+  return launch(prefill_finalize_kernel<KIND>, dim3(fgrid), dim3(256), 0, l, (const float*)part, ks, Mp,
+                (const float*)einv, M, N, p.res, p.res_ld, p.out, p.out_f32 ? 1 : 0);
+}
+
+// The activation-row tile: the smallest of 64, 128, 256 that holds M (a
+// narrow tile moves fewer x bytes through shared memory per K block).
+template <int FMT, int KIND>
+mt_status run_prefill_nt(const GemvProblem& p, void* ws, const Launch& l) {
+  if (p.M <= 64) return run_prefill<FMT, KIND, 64>(p, ws, l);
+  if (p.M <= 128) return run_prefill<FMT, KIND, 128>(p, ws, l);
+  return run_prefill<FMT, KIND, 256>(p, ws, l);
 }
 
 mt_status launch_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   if (p.fmt == MT_W_AFFINE8)
-    return p.kind == Kind::GateUp ? run_prefill<FMT_A8, 0>(p, ws, l) : run_prefill<FMT_A8, 1>(p, ws, l);
+    return p.kind == Kind::GateUp ? run_prefill_nt<FMT_A8, 0>(p, ws, l) : run_prefill_nt<FMT_A8, 1>(p, ws, l);
   if (p.fmt == MT_W_AFFINE4)
-    return p.kind == Kind::GateUp ? run_prefill<FMT_A4, 0>(p, ws, l) : run_prefill<FMT_A4, 1>(p, ws, l);
+    return p.kind == Kind::GateUp ? run_prefill_nt<FMT_A4, 0>(p, ws, l) : run_prefill_nt<FMT_A4, 1>(p, ws, l);
   return MT_ERR_FORMAT;
 }
 
@@ -772,7 +874,10 @@ mt_status prefill_call(Kind kind, const void* x, const void* W0, const void* W1,
   if (group != 32 && group != 64 && group != 128) return MT_ERR_GROUP;
   if (M < 1 || M > (1 << 20) || K < PF_KB || K > 65536 || K % PF_KB || K % group || N < 1 || N > (1 << 20))
     return MT_ERR_SHAPE;
-  if (ws_bytes < prefill_ws_bytes(M, K, group)) return MT_ERR_SHAPE;
+  int derr = 0;
+  const DeviceInfo* di = device_info(&derr);
+  const size_t need = prefill_ws_bytes(M, K, N, group, di ? di->sm_count : 1);
+  if (ws_bytes < need) return MT_ERR_SHAPE;
   if (!al16(x) || !al16(W0) || !al16(W1) || !al16(scales) || !al16(biases) || !al16(out) || !al16(ws) ||
       !al16(addend))
     return MT_ERR_ALIGN;
@@ -780,7 +885,7 @@ mt_status prefill_call(Kind kind, const void* x, const void* W0, const void* W1,
   const size_t wb = (size_t)N * K / (fmt == MT_W_AFFINE8 ? 1 : 2);
   const size_t sbb = (size_t)NW * N * (K / group) * 2;
   const Rg ro = rg(out, (size_t)M * N * (out_dtype == MT_F32 ? 4 : 2));
-  const Rg rw = rg(ws, prefill_ws_bytes(M, K, group));
+  const Rg rw = rg(ws, need);
   const Rg rx = rg(x, (size_t)M * K * 2), rw0 = rg(W0, wb), rw1 = rg(W1, W1 ? wb : 0);
   const Rg rs = rg(scales, sbb), rb = rg(biases, sbb);
   const Rg ra = rg(addend, !addend ? 0 : (addend_ld ? (size_t)M * N * 2 : (size_t)N * 2));
@@ -812,9 +917,11 @@ mt_status prefill_call(Kind kind, const void* x, const void* W0, const void* W1,
 
 extern "C" {
 
-size_t mt_prefill_workspace_bytes(int M, int K, int group) {
-  if (M < 1 || K < 1 || (group != 32 && group != 64 && group != 128)) return 0;
-  return prefill_ws_bytes(M, K, group);
+size_t mt_prefill_workspace_bytes(int M, int K, int N, int group) {
+  if (M < 1 || K < PF_KB || N < 1 || (group != 32 && group != 64 && group != 128)) return 0;
+  int derr = 0;
+  const DeviceInfo* di = device_info(&derr);
+  return prefill_ws_bytes(M, K, N, group, di ? di->sm_count : 1);
 }
 
 mt_status mt_prefill_swiglu_gateup(const void* x, const void* Wg, const void* Wu, const void* scales,

@@ -36,8 +36,8 @@ def _pack(mt, W32, fmt, group):
     return q, s, bi
 
 
-def _ws(mt, M, K, group):
-    n = mt.mt_prefill_workspace_bytes(M, K, group)
+def _ws(mt, M, K, N, group):
+    n = mt.mt_prefill_workspace_bytes(M, K, N, group)
     assert n > 0
     return torch.empty(n, dtype=torch.uint8, device="cuda")
 
@@ -74,7 +74,7 @@ def test_prefill_epilogues(mt, shape):
     bias = synth.host_bf16(N, seed + 4, synth.PROJ_BIAS)
     refs = {"h": oracle.swiglu_gateup(x, og, ou), "y": oracle.down_residual(x, og, res),
             "y + bias": oracle.linear_bias(x, ou, bias), "y, no bias": oracle.linear_bias(x, og)}
-    ws = _ws(mt, M, K, group)
+    ws = _ws(mt, M, K, N, group)
     xd = dev_bf16(x)
     sgu, bgu = torch.stack([sg, su]).contiguous(), torch.stack([bg, bu]).contiguous()
     for out_f32 in (False, True):
@@ -108,7 +108,7 @@ def test_prefill_indexing_bit_exact(mt, bits, group, M, K, N):
     y = torch.empty(M, N, dtype=torch.float32, device="cuda")
     fmt = 1 if bits == 8 else 2
     mt.mt_prefill_down_residual(dev_bf16(x), torch.from_numpy(oracle.pack_codes(codes, bits)).cuda(), dev_bf16(s),
-                                dev_bf16(b), group, dev_bf16(res), y, _ws(mt, M, K, group), fmt=fmt)
+                                dev_bf16(b), group, dev_bf16(res), y, _ws(mt, M, K, N, group), fmt=fmt)
     torch.cuda.synchronize()
     ref = oracle.down_residual(x, oracle.Weight(oracle.FMT_CODES, codes, s, b, group), res)
     assert np.array_equal(y.cpu().numpy().astype(np.float64), ref)
@@ -121,7 +121,7 @@ def test_prefill_in_place_residual(mt):
     W = synth.host_f32(N * K, 12503, synth.WEIGHT).reshape(N, K)
     q, s, b = _pack(mt, W, 1, g)
     rd = dev_bf16(res)
-    mt.mt_prefill_down_residual(dev_bf16(x), q, s, b, g, rd, rd, _ws(mt, M, K, g), fmt=1)
+    mt.mt_prefill_down_residual(dev_bf16(x), q, s, b, g, rd, rd, _ws(mt, M, K, N, g), fmt=1)
     torch.cuda.synchronize()
     assert_bf16_close(host_bits(rd), oracle.down_residual(x, oracle.Weight.from_f32(W, 8, g), res), "in place")
 
@@ -138,8 +138,8 @@ def test_prefill_qwen3_8b_layer(mt, M):
     res = synth.host_bf16(M * d, synth.seed_for(wl.wid, 0, synth.T_RES3) + M, synth.ACT).reshape(M, d)
     h = torch.empty(M, f, dtype=torch.float32, device="cuda")
     y = torch.empty(M, d, dtype=torch.bfloat16, device="cuda")
-    mt.mt_prefill_swiglu_gateup(dev_bf16(x), L.Wg, L.Wu, L.sgu, L.bgu, g, h, _ws(mt, M, d, g), fmt=wl.fmt)
-    mt.mt_prefill_down_residual(dev_bf16(hin), L.Wd, L.sdn, L.bdn, g, dev_bf16(res), y, _ws(mt, M, f, g),
+    mt.mt_prefill_swiglu_gateup(dev_bf16(x), L.Wg, L.Wu, L.sgu, L.bgu, g, h, _ws(mt, M, d, f, g), fmt=wl.fmt)
+    mt.mt_prefill_down_residual(dev_bf16(hin), L.Wd, L.sdn, L.bdn, g, dev_bf16(res), y, _ws(mt, M, f, d, g),
                                 fmt=wl.fmt)
     torch.cuda.synchronize()
     rg = np.sort(np.random.default_rng(21).choice(f, 64, replace=False))

@@ -234,43 +234,52 @@ __global__ void __launch_bounds__(256) prefill_x_kernel(const uint16_t* __restri
 
 // ------------------------------------------------------------- the GEMM
 
-// Codes of weight row r for one K block of 64 (INT8: 64 bytes, INT4: 32),
-// read from the TMA-filled code tile (rows of CB bytes, 64- or 32-byte
-// swizzle: 16-byte chunk u of row r at u ^ ((r >> 1) & 3), resp. u ^ ((r >> 2)
-// & 1), so that eight consecutive rows read their chunk u from distinct
-// banks), written as fp16 subnormals q * 2^-24 into row r of the MMA tile
-// (128-byte rows, chunk j at j ^ (r & 7)).
-template <int FMT>
-__device__ __forceinline__ void pf_convert_row(const unsigned char* ctile, unsigned char* wtile, int r) {
-  unsigned char* rowp = wtile + r * 128;
-  const int sw = r & 7;
-  if constexpr (FMT == FMT_A8) {
-    const unsigned char* src = ctile + r * 64;
+// Codes of weight rows r0, r0 + step, ... (R rows) for one K block of 64
+// (INT8: 64 bytes a row, INT4: 32), read from the TMA-filled code tile (rows
+// of CB bytes, 64- or 32-byte swizzle: 16-byte chunk u of row r at
+// u ^ ((r >> 1) & 3), resp. u ^ ((r >> 2) & 1), so that eight consecutive
+// rows read their chunk u from distinct banks), written as fp16 subnormals
+// q * 2^-24 into the same rows of the MMA tile (128-byte rows, chunk j at
+// j ^ (r & 7)).  Every load of the R rows is issued before the first store.
+template <int FMT, int R>
+__device__ __forceinline__ void pf_convert_rows(const unsigned char* __restrict__ ctile,
+                                                unsigned char* __restrict__ wtile, int r0, int step) {
+  constexpr int U = FMT == FMT_A8 ? 4 : 2;  // 16-byte code chunks a row
+  uint4 v[R][U];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {  // 16 codes -> chunks 2u, 2u+1
-      const uint4 v = *reinterpret_cast<const uint4*>(src + ((u ^ ((r >> 1) & 3)) << 4));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int i = 0; i < R; ++i) {
+    const int r = r0 + i * step;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t a = w[2 * h], b = w[2 * h + 1];
-        const uint4 o = make_uint4(__byte_perm(a, 0u, 0x4140), __byte_perm(a, 0u, 0x4342),
-                                   __byte_perm(b, 0u, 0x4140), __byte_perm(b, 0u, 0x4342));
-        *reinterpret_cast<uint4*>(rowp + (((2 * u + h) ^ sw) << 4)) = o;
-      }
-    }
-  } else {
-    const unsigned char* src = ctile + r * 32;
+    for (int u = 0; u < U; ++u)
+      v[i][u] = FMT == FMT_A8
+                    ? *reinterpret_cast<const uint4*>(ctile + r * 64 + ((u ^ ((r >> 1) & 3)) << 4))
+                    : *reinterpret_cast<const uint4*>(ctile + r * 32 + ((u ^ ((r >> 2) & 1)) << 4));
+  }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {  // 32 codes -> chunks 4u .. 4u+3 (one word each)
-      const uint4 v = *reinterpret_cast<const uint4*>(src + ((u ^ ((r >> 2) & 1)) << 4));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int i = 0; i < R; ++i) {
+    const int r = r0 + i * step;
+    unsigned char* rowp = wtile + r * 128;
+    const int sw = r & 7;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        // byte j of w holds code 2j (bits 0..3) and 2j+1 (bits 4..7)
-        const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
-        const uint4 o = make_uint4(__byte_perm(lo, hi, 0x4400) & 0x00FF00FFu, __byte_perm(lo, hi, 0x5511) & 0x00FF00FFu,
-                                   __byte_perm(lo, hi, 0x6622) & 0x00FF00FFu, __byte_perm(lo, hi, 0x7733) & 0x00FF00FFu);
-        *reinterpret_cast<uint4*>(rowp + (((4 * u + i) ^ sw) << 4)) = o;
+    for (int u = 0; u < U; ++u) {
+      const uint32_t w[4] = {v[i][u].x, v[i][u].y, v[i][u].z, v[i][u].w};
+      if constexpr (FMT == FMT_A8) {  // 16 codes -> chunks 2u, 2u+1
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t a = w[2 * h], b = w[2 * h + 1];
+          const uint4 o = make_uint4(__byte_perm(a, 0u, 0x4140), __byte_perm(a, 0u, 0x4342),
+                                     __byte_perm(b, 0u, 0x4140), __byte_perm(b, 0u, 0x4342));
+          *reinterpret_cast<uint4*>(rowp + (((2 * u + h) ^ sw) << 4)) = o;
+        }
+      } else {  // 32 codes -> chunks 4u .. 4u+3 (one word each)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          // byte j of w holds code 2j (bits 0..3) and 2j+1 (bits 4..7)
+          const uint32_t lo = w[k] & 0x0F0F0F0Fu, hi = (w[k] >> 4) & 0x0F0F0F0Fu;
+          const uint4 o = make_uint4(__byte_perm(lo, hi, 0x4400) & 0x00FF00FFu, __byte_perm(lo, hi, 0x5511) & 0x00FF00FFu,
+                                     __byte_perm(lo, hi, 0x6622) & 0x00FF00FFu, __byte_perm(lo, hi, 0x7733) & 0x00FF00FFu);
+          *reinterpret_cast<uint4*>(rowp + (((4 * u + k) ^ sw) << 4)) = o;
+        }
       }
     }
   }
@@ -423,8 +432,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       const int i = kb % SC, j = kb % SB;
       if (!mbar_wait_bounded(c_full(i), (kb / SC) & 1)) { fail(); break; }
       if (kb >= SB && !mbar_wait_bounded(b_free(j), ((kb / SB) + 1) & 1)) { fail(); break; }
-#pragma unroll
-      for (int r = c; r < PF_ROWS; r += CONV) pf_convert_row<FMT>(cslot(i), wslot(j), r);
+      pf_convert_rows<FMT, PF_ROWS / CONV>(cslot(i), wslot(j), c, CONV);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor core reads
       mbar_arrive(w_full(j));
       mbar_arrive(c_free(i));

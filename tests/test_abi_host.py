@@ -185,6 +185,38 @@ def test_linear_bias_validation(lib):
     assert call(fmt=3, g=32, bi=None, y=sc + 16) == ALIAS   # E8M0 scales: N * K/32 bytes
 
 
+def test_prefill_validation(lib):
+    wsb = lib.mt_prefill_workspace_bytes
+    wsb.restype = ctypes.c_size_t
+    wsb.argtypes = [ctypes.c_int] * 4
+    assert wsb(100, 512, 256, 64) > 100 * 512 * 2      # at least the fp16 activations
+    assert wsb(0, 512, 256, 64) == 0 and wsb(10, 512, 256, 48) == 0 and wsb(10, 32, 256, 32) == 0
+    f = lib.mt_prefill_linear_bias
+    f.restype = ctypes.c_int
+    f.argtypes = [P, P, P, P, ctypes.c_int, P, P] + [ctypes.c_int] * 5 + [P, ctypes.c_size_t, P]
+    x, w, sc, bi, bias, y, ws = A[:7]
+    need = wsb(100, 512, 256, 64)
+
+    def call(x=x, w=w, sc=sc, bi=bi, g=64, bias=bias, y=y, M=100, K=512, N=256, fmt=1, od=0, ws=ws, wb=need):
+        return f(x, w, sc, bi, g, bias, y, M, K, N, fmt, od, ws, wb, None)
+
+    assert call(ws=None) == NULL
+    assert call(bi=None) == NULL
+    assert call(fmt=0, g=0, sc=None, bi=None) == FORMAT     # bf16 weights are decode-only
+    assert call(fmt=3, g=32, bi=None) == FORMAT             # MX weights are decode-only
+    assert call(g=96) == GROUP
+    assert call(K=480) == SHAPE                             # K % 64 != 0
+    assert call(M=0) == SHAPE
+    assert call(wb=need - 1) == SHAPE                       # workspace too small
+    assert call(ws=ws + 8) == ALIGN
+    assert call(y=ws + 64) == ALIAS                         # output inside the workspace
+    assert call(ws=x) == ALIAS                              # workspace over the activations
+    g = lib.mt_prefill_down_residual
+    g.restype = ctypes.c_int
+    g.argtypes = [P, P, P, P, ctypes.c_int, P, P] + [ctypes.c_int] * 5 + [P, ctypes.c_size_t, P]
+    assert g(x, w, sc, bi, 64, None, y, 100, 512, 256, 1, 0, ws, need, None) == NULL  # residual required
+
+
 def test_pack_mx_validation(lib):
     f = lib.mt_pack_mx
     f.restype = ctypes.c_int

@@ -149,3 +149,28 @@ def test_prefill_qwen3_8b_layer(mt, M):
     y_ref = oracle.down_residual(hin, L.oracle_rows(synth.T_WD, rd, d, f), res[:, rd])
     assert_f32_close(host_f64(h)[:, rg], h_ref, "h sampled")
     assert_bf16_close(host_bits(y)[:, rd], y_ref, "y sampled")
+
+
+@pytest.mark.parametrize("M", [40, 300])
+def test_prefill_llama_layer_int4(mt, M):
+    """The Llama-3.2-1B-shaped layer (d=2048, f=8192, affine INT4 g64) at M = 40
+    (narrow tile, split K) and M = 300 (two 256-row tiles): gate/up and down on
+    every activation row, 48 sampled output features each, bf16 outputs."""
+    wl = synth.LLAMA1B
+    d, f, g = wl.d, wl.f, wl.group
+    L = DevLayer(mt, wl, 0)
+    x = synth.host_bf16(M * d, synth.seed_for(wl.wid, 0, synth.T_X) + M, synth.ACT).reshape(M, d)
+    hin = synth.host_bf16(M * f, synth.seed_for(wl.wid, 0, synth.T_H) + M, synth.ACT).reshape(M, f)
+    res = synth.host_bf16(M * d, synth.seed_for(wl.wid, 0, synth.T_RES3) + M, synth.ACT).reshape(M, d)
+    h = torch.empty(M, f, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(M, d, dtype=torch.bfloat16, device="cuda")
+    mt.mt_prefill_swiglu_gateup(dev_bf16(x), L.Wg, L.Wu, L.sgu, L.bgu, g, h, _ws(mt, M, d, f, g), fmt=wl.fmt)
+    mt.mt_prefill_down_residual(dev_bf16(hin), L.Wd, L.sdn, L.bdn, g, dev_bf16(res), y, _ws(mt, M, f, d, g),
+                                fmt=wl.fmt)
+    torch.cuda.synchronize()
+    rg = np.sort(np.random.default_rng(31).choice(f, 48, replace=False))
+    rd = np.sort(np.random.default_rng(32).choice(d, 48, replace=False))
+    h_ref = oracle.swiglu_gateup(x, L.oracle_rows(synth.T_WG, rg, f, d), L.oracle_rows(synth.T_WU, rg, f, d))
+    y_ref = oracle.down_residual(hin, L.oracle_rows(synth.T_WD, rd, d, f), res[:, rd])
+    assert_bf16_close(host_bits(h)[:, rg], h_ref, "h sampled")
+    assert_bf16_close(host_bits(y)[:, rd], y_ref, "y sampled")

@@ -174,3 +174,43 @@ def test_prefill_llama_layer_int4(mt, M):
     y_ref = oracle.down_residual(hin, L.oracle_rows(synth.T_WD, rd, d, f), res[:, rd])
     assert_bf16_close(host_bits(h)[:, rg], h_ref, "h sampled")
     assert_bf16_close(host_bits(y)[:, rd], y_ref, "y sampled")
+
+
+@pytest.mark.parametrize("bits,M,K,N", [(8, 40, 512, 200), (8, 300, 1024, 136), (4, 70, 512, 129),
+                                        (4, 257, 256, 96)])
+def test_prefill_mx(mt, bits, M, K, N):
+    """MXFP8 / MXFP4 weights (E8M0 block scales per 32) on the prefill GEMMs:
+    gate/up, down and projection against the oracle, bf16 and fp32 outputs."""
+    fmt = 3 if bits == 8 else 4
+    seed = 13000 + bits + M + K + N
+    x = synth.host_bf16(M * K, seed, synth.ACT).reshape(M, K)
+    Wg = synth.host_f32(N * K, seed + 1, synth.WEIGHT).reshape(N, K)
+    Wu = synth.host_f32(N * K, seed + 2, synth.WEIGHT_OUTLIERS).reshape(N, K)
+
+    def pack(W):
+        q = torch.empty(N, K * bits // 8, dtype=torch.uint8, device="cuda")
+        s = torch.empty(N, K // 32, dtype=torch.uint8, device="cuda")
+        mt.mt_pack_mx(torch.from_numpy(np.ascontiguousarray(W)).cuda(), N, K, bits, q, s)
+        return q, s
+
+    (qg, sg), (qu, su) = pack(Wg), pack(Wu)
+    torch.cuda.synchronize()
+    og, ou = oracle.Weight.from_f32_mx(Wg, bits), oracle.Weight.from_f32_mx(Wu, bits)
+    res = synth.host_bf16(M * N, seed + 3, synth.ACT).reshape(M, N)
+    bias = synth.host_bf16(N, seed + 4, synth.PROJ_BIAS)
+    refs = {"h": oracle.swiglu_gateup(x, og, ou), "y": oracle.down_residual(x, og, res),
+            "y + bias": oracle.linear_bias(x, ou, bias)}
+    ws = _ws(mt, M, K, N, 32)
+    xd = dev_bf16(x)
+    sgu = torch.stack([sg, su]).contiguous()
+    for out_f32 in (False, True):
+        dt = torch.float32 if out_f32 else torch.bfloat16
+        check = assert_f32_close if out_f32 else assert_bf16_close
+        get = host_f64 if out_f32 else host_bits
+        outs = {k: torch.empty(M, N, dtype=dt, device="cuda") for k in refs}
+        mt.mt_prefill_swiglu_gateup(xd, qg, qu, sgu, None, 32, outs["h"], ws, fmt=fmt)
+        mt.mt_prefill_down_residual(xd, qg, sg, None, 32, dev_bf16(res), outs["y"], ws, fmt=fmt)
+        mt.mt_prefill_linear_bias(xd, qu, su, None, 32, dev_bf16(bias), outs["y + bias"], ws, fmt=fmt)
+        torch.cuda.synchronize()
+        for k, ref in refs.items():
+            check(get(outs[k]), ref, f"{k} ({'f32' if out_f32 else 'bf16'})")

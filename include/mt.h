@@ -222,7 +222,8 @@ mt_status mt_linear_bias(const void* x, const void* W, const void* scales,
  *   kernel); it must not overlap any argument.  The call allocates nothing
  *   and never synchronises.
  * Formats: MT_W_AFFINE8, MT_W_AFFINE4 (group 32, 64 or 128), MT_W_MXFP8,
- *          MT_W_MXFP4 (group 32, biases NULL).
+ *          MT_W_MXFP4 (group 32, biases NULL), MT_W_BF16 (group 0, scales
+ *          and biases NULL; x enters the MMA as stored).
  * Limits: 1 <= M <= 2^20; K % 64 == 0 and K % group == 0; 64 <= K <= 65536;
  *         1 <= N <= 2^20.  A workspace below the required size is
  *         MT_ERR_SHAPE.  out_y may equal residual (bf16 output).

@@ -51,6 +51,8 @@ mt_status launch_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   if (p.fmt == MT_W_AFFINE4)
     return p.kind == Kind::GateUp ? run_prefill_nt<FMT_A4, 0>(p, ws, l) : run_prefill_nt<FMT_A4, 1>(p, ws, l);
   if (p.fmt == MT_W_MXFP8 || p.fmt == MT_W_MXFP4) return launch_prefill_mx(p, ws, l);
+  if (p.fmt == MT_W_BF16)
+    return p.kind == Kind::GateUp ? run_prefill_nt<FMT_BF16, 0>(p, ws, l) : run_prefill_nt<FMT_BF16, 1>(p, ws, l);
   return MT_ERR_FORMAT;
 }
 
@@ -75,14 +77,21 @@ bool ovl(Rg a, Rg b) { return a.lo < b.hi && b.lo < a.hi; }
 mt_status prefill_call(Kind kind, const void* x, const void* W0, const void* W1, const void* scales,
                        const void* biases, int group, const void* addend, int addend_ld, void* out, int M,
                        int K, int N, mt_wfmt fmt, mt_dtype out_dtype, void* ws, size_t ws_bytes, void* stream) {
-  const bool mx = fmt == MT_W_MXFP8 || fmt == MT_W_MXFP4;
-  if (fmt != MT_W_AFFINE8 && fmt != MT_W_AFFINE4 && !mx) return MT_ERR_FORMAT;
+  const bool mx = fmt == MT_W_MXFP8 || fmt == MT_W_MXFP4, bf = fmt == MT_W_BF16;
+  if (fmt != MT_W_AFFINE8 && fmt != MT_W_AFFINE4 && !mx && !bf) return MT_ERR_FORMAT;
   if (out_dtype != MT_BF16 && out_dtype != MT_F32) return MT_ERR_FORMAT;
-  if (!x || !W0 || (kind == Kind::GateUp && !W1) || !scales || (!mx && !biases) || !out || !ws) return MT_ERR_NULL;
-  if (mx && biases) return MT_ERR_FORMAT;  // MX weights have no biases
-  if (group != 32 && group != 64 && group != 128) return MT_ERR_GROUP;
-  if (mx && group != 32) return MT_ERR_GROUP;
-  if (M < 1 || M > (1 << 20) || K < PF_KB || K > 65536 || K % PF_KB || K % group || N < 1 || N > (1 << 20))
+  if (!x || !W0 || (kind == Kind::GateUp && !W1) || (!bf && !scales) || (!mx && !bf && !biases) || !out || !ws)
+    return MT_ERR_NULL;
+  if ((mx || bf) && biases) return MT_ERR_FORMAT;  // MX and bf16 weights have no biases
+  if (bf && scales) return MT_ERR_FORMAT;           // nor bf16 weights scales
+  if (bf) {
+    if (group != 0) return MT_ERR_GROUP;
+  } else {
+    if (group != 32 && group != 64 && group != 128) return MT_ERR_GROUP;
+    if (mx && group != 32) return MT_ERR_GROUP;
+  }
+  if (M < 1 || M > (1 << 20) || K < PF_KB || K > 65536 || K % PF_KB || (group && K % group) || N < 1 ||
+      N > (1 << 20))
     return MT_ERR_SHAPE;
   int derr = 0;
   const DeviceInfo* di = device_info(&derr);
@@ -92,8 +101,8 @@ mt_status prefill_call(Kind kind, const void* x, const void* W0, const void* W1,
       !al16(addend))
     return MT_ERR_ALIGN;
   const int NW = kind == Kind::GateUp ? 2 : 1;
-  const size_t wb = (size_t)N * K / (fmt == MT_W_AFFINE8 || fmt == MT_W_MXFP8 ? 1 : 2);
-  const size_t sbb = (size_t)NW * N * (K / group) * (mx ? 1 : 2);  // scale (and bias) bytes
+  const size_t wb = bf ? (size_t)N * K * 2 : (size_t)N * K / (fmt == MT_W_AFFINE8 || fmt == MT_W_MXFP8 ? 1 : 2);
+  const size_t sbb = bf ? 0 : (size_t)NW * N * (K / group) * (mx ? 1 : 2);  // scale (and bias) bytes
   const Rg ro = rg(out, (size_t)M * N * (out_dtype == MT_F32 ? 4 : 2));
   const Rg rw = rg(ws, need);
   const Rg rx = rg(x, (size_t)M * K * 2), rw0 = rg(W0, wb), rw1 = rg(W1, W1 ? wb : 0);
@@ -109,10 +118,10 @@ mt_status prefill_call(Kind kind, const void* x, const void* W0, const void* W1,
   p.M = M; p.K = K; p.N = N; p.group = group;
   p.x = (const uint16_t*)x;
   p.W0 = W0; p.W1 = W1;
-  const size_t plane = (size_t)N * (K / group) * (mx ? 1 : 2);  // bytes of one scale plane
+  const size_t plane = bf ? 0 : (size_t)N * (K / group) * (mx ? 1 : 2);  // bytes of one scale plane
   p.s0 = (const uint16_t*)scales;
   p.b0 = (const uint16_t*)biases;
-  if (kind == Kind::GateUp) {
+  if (kind == Kind::GateUp && !bf) {
     p.s1 = (const uint16_t*)((const char*)scales + plane);
     p.b1 = biases ? (const uint16_t*)((const char*)biases + plane) : nullptr;
   }
@@ -128,7 +137,7 @@ mt_status prefill_call(Kind kind, const void* x, const void* W0, const void* W1,
 extern "C" {
 
 size_t mt_prefill_workspace_bytes(int M, int K, int N, int group) {
-  if (M < 1 || K < PF_KB || N < 1 || (group != 32 && group != 64 && group != 128)) return 0;
+  if (M < 1 || K < PF_KB || N < 1 || (group != 0 && group != 32 && group != 64 && group != 128)) return 0;
   int derr = 0;
   const DeviceInfo* di = device_info(&derr);
   return prefill_ws_bytes(M, K, N, group, di ? di->sm_count : 1);

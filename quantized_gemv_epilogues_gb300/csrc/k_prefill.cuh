@@ -101,17 +101,20 @@ __device__ __forceinline__ uint64_t pf_desc_sw128(uint32_t saddr) {
 
 // Instruction descriptor: fp32 accumulator, fp16 A and B, both K-major,
 // N = 64, M = 128.
-template <int NT>
+// Instruction descriptor: fp32 accumulator, A and B fp16 (BF = false) or
+// bf16 (BF = true), both K-major, N = NT, M = 128.
+template <int NT, bool BF>
 __host__ __device__ constexpr uint32_t pf_idesc() {
-  return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(PF_ROWS >> 4) << 24);
+  return (1u << 4) | ((BF ? 1u : 0u) << 7) | ((BF ? 1u : 0u) << 10) | ((uint32_t)(NT >> 3) << 17) |
+         ((uint32_t)(PF_ROWS >> 4) << 24);
 }
 
-template <int NT>
+template <int NT, bool BF>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(pf_idesc<NT>()), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(pf_idesc<NT, BF>()), "r"(accumulate)
       : "memory");
 }
 
@@ -303,9 +306,11 @@ struct PfShape {
   static constexpr int CTILE = PF_ROWS * CB;            // 8 or 4 KB
   // ring depths: narrow tiles (small M, weights streamed from HBM once) keep
   // more code tiles in flight; wide tiles more x tiles
+  // (dense bf16 weights skip the code ring: TMA fills the A ring itself)
+  static constexpr bool BFW = FMT == FMT_BF16;
   static constexpr int SX = NT == 128 ? 5 : 4;
-  static constexpr int SC = (NT == 64 ? 96 : (NT == 128 ? 64 : 48)) * 1024 / CTILE;
-  static constexpr int SB = NT == 256 ? 2 : 4;
+  static constexpr int SC = BFW ? 1 : (NT == 64 ? 96 : (NT == 128 ? 64 : 48)) * 1024 / CTILE;
+  static constexpr int SB = BFW ? (NT == 256 ? 4 : 6) : (NT == 256 ? 2 : 4);
   static constexpr size_t OFF_C = (size_t)SX * XT;
   static constexpr size_t OFF_B = OFF_C + (size_t)SC * CTILE;
   static constexpr size_t SMEM = 1024 + OFF_B + (size_t)SB * PF_W_TILE;
@@ -328,6 +333,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   using SH = PfShape<FMT, KIND, NT>;
   constexpr int SX = SH::SX, SC = SH::SC, SB = SH::SB, FT = SH::FT;
   constexpr uint32_t NCOLS = 2 * NT;        // two accumulator buffers of NT columns
+  constexpr bool BFW = SH::BFW;              // dense bf16 weights: no codes, no converters
   constexpr int EPI = 32 * PF_EPI_WARPS;    // epilogue threads
   constexpr int HALF = NT / 2;              // tile columns per epilogue warpgroup
 
@@ -375,7 +381,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       mbar_init(c_free(i), CONV);
     }
     for (int i = 0; i < SB; ++i) {
-      mbar_init(w_full(i), CONV);
+      mbar_init(w_full(i), BFW ? 1 : CONV);  // TMA (bf16 weights) or the converters
       mbar_init(b_free(i), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -405,17 +411,23 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // ---- producers: lane 0 the x tiles (SX blocks ahead of the MMA), lane 1
     // the code tiles (SC blocks ahead of the converters)
     if (lane < 2) {
-      const int S = lane == 0 ? SX : SC;
+      // bf16 weights: lane 1 fills the A ring directly
+      const int S = lane == 0 ? SX : (BFW ? SB : SC);
       int issued = 0;
       for (int kb = 0; kb < KB; ++kb) {
         const int i = kb % S;
-        const uint32_t full = lane == 0 ? x_full(i) : c_full(i), free_ = lane == 0 ? x_free(i) : c_free(i);
+        const uint32_t full = lane == 0 ? x_full(i) : (BFW ? w_full(i) : c_full(i));
+        const uint32_t free_ = lane == 0 ? x_free(i) : (BFW ? b_free(i) : c_free(i));
         if (kb >= S && !mbar_wait_bounded(free_, ((kb / S) + 1) & 1)) { fail(); break; }
         if (*abort_flag) break;
         const int kg = kb0 + kb;  // K block of the tensor
         if (lane == 0) {
           mbar_arrive_expect_tx(full, SH::XT);
           tma_load_2d(smem_u32(xslot(i)), &xmap, kg * PF_KB, m0, full);
+        } else if constexpr (BFW) {
+          mbar_arrive_expect_tx(full, PF_W_TILE);
+          tma_load_2d(smem_u32(wslot(i)), &wmap0, kg * PF_KB, f0, full);
+          if constexpr (KIND == 0) tma_load_2d(smem_u32(wslot(i) + 64 * 128), &wmap1, kg * PF_KB, f0, full);
         } else {
           mbar_arrive_expect_tx(full, SH::CTILE);
           tma_load_2d(smem_u32(cslot(i)), &wmap0, kg * SH::CB, f0, full);
@@ -425,11 +437,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       }
       // copies still in flight (only after an abort) land before the CTA ends
       for (int kb = max(0, issued - S); kb < issued; ++kb)
-        (void)mbar_wait_bounded(lane == 0 ? x_full(kb % S) : c_full(kb % S), (kb / S) & 1);
+        (void)mbar_wait_bounded(lane == 0 ? x_full(kb % S) : (BFW ? w_full(kb % S) : c_full(kb % S)), (kb / S) & 1);
     }
     __syncwarp();
   } else if (warp >= CONV0 && warp < MMA_WARP) {
     // ---- converters: rows c, c + CONV of the code tile into the fp16 A tile
+    // (none for bf16 weights)
+    if constexpr (!BFW) {
     const int c = tid - 32 * CONV0;
     for (int kb = 0; kb < KB; ++kb) {
       const int i = kb % SC, j = kb % SB;
@@ -440,6 +454,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       mbar_arrive(w_full(j));
       mbar_arrive(c_free(i));
       if (*abort_flag) break;
+    }
     }
   } else if (warp == MMA_WARP) {
     // ---- MMA issuer: the whole warp walks the loop, one elected lane issues
@@ -464,7 +479,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           tc_fence_after();
         }
         if (elect_one()) {
-          tc_mma<NT>(tbase + (uint32_t)(b * NT), wd + 2 * j, xd + 2 * j, first ? 0u : 1u);
+          tc_mma<NT, BFW>(tbase + (uint32_t)(b * NT), wd + 2 * j, xd + 2 * j, first ? 0u : 1u);
           if (((k + 16) & (group - 1)) == 0) tc_commit(acc_full(b));
         }
         __syncwarp();
@@ -498,7 +513,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // q * 2^-24) and b; MX the E8M0 block scale 2^(E - 127) and no bias
     constexpr bool MXF = FmtTraits<FMT>::MX;
     auto scale_of = [&](size_t i) -> float {
-      if constexpr (MXF) {
+      if constexpr (BFW) {
+        return 1.0f;  // dense bf16 weights: D is the dot product itself
+      } else if constexpr (MXF) {
         const uint32_t E = reinterpret_cast<const uint8_t*>(sp)[i];
         return E ? __int_as_float((int)(E << 23)) : __int_as_float(0x00400000);
       } else {
@@ -506,7 +523,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       }
     };
     auto bias_of = [&](size_t i) -> float {
-      if constexpr (MXF) return 0.f;
+      if constexpr (MXF || BFW) return 0.f;
       else return bf16f(bp[i]);
     };
     float sv = okr ? scale_of(sbo) : 0.f;
@@ -514,7 +531,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // X'_g of group gi for the tile's rows comes into xg_sh[gi & 1] by
     // asynchronous copies one group ahead (threads 0-63, 16 bytes each)
     auto fetch_xg = [&](int gi) {
-      if (tid < NT / 4) cp_async16(&xg_sh[gi & 1][4 * tid], a.XgT + (size_t)(g0 + gi) * Mp + m0 + 4 * tid);
+      if (!BFW && tid < NT / 4) cp_async16(&xg_sh[gi & 1][4 * tid], a.XgT + (size_t)(g0 + gi) * Mp + m0 + 4 * tid);
       cp_async_commit();
     };
     auto epi_sync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(EPI) : "memory"); };
@@ -530,7 +547,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       return res != 0;
     };
     // the tile's row scales (padded rows hold 0) with group 0's sums
-    if (tid < NT / 4) cp_async16(&einv_sh[4 * tid], a.einv + m0 + 4 * tid);
+    if constexpr (BFW) {  // x enters the MMA as stored: no row scale, no group sums
+      for (int i = tid; i < NT; i += EPI) einv_sh[i] = 1.0f;
+    } else {
+      if (tid < NT / 4) cp_async16(&einv_sh[4 * tid], a.einv + m0 + 4 * tid);
+    }
     fetch_xg(0);
     cp_async_wait_all();
     epi_sync();
@@ -557,7 +578,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int jj = q * 16 + 4 * i + e;
-              acc[jj] = fmaf(sv, d[4 * i + e], fmaf(bv, Xv[e], acc[jj]));
+              if constexpr (BFW || MXF)
+                acc[jj] = fmaf(sv, d[4 * i + e], acc[jj]);  // no bias term
+              else
+                acc[jj] = fmaf(sv, d[4 * i + e], fmaf(bv, Xv[e], acc[jj]));
             }
           }
         }
@@ -681,7 +705,7 @@ __global__ void __launch_bounds__(256) prefill_finalize_kernel(const float* __re
     for (int mat = 0; mat < NW; ++mat) {
       float t = 0.f;
       for (int s = 0; s < ks; ++s) t += part[((size_t)(s * NW + mat) * Mp + m) * N + n];
-      v[mat] = t * einv[m];
+      v[mat] = einv ? t * einv[m] : t;
     }
     float o;
     if constexpr (KIND == 0)
@@ -719,10 +743,21 @@ int prefill_ks(long tiles, long K, long group, int sms, int* kbs) {
   return (KB + per - 1) / per;
 }
 
+// The accumulation group of dense bf16 weights (they have no quantisation
+// groups): the largest power of two up to 512 that divides K (K % 64 == 0),
+// so that each group's sum is read out of tensor memory while the next one
+// accumulates, as for the affine groups.
+int prefill_bf16_group(long K) {
+  int g = 512;
+  while (K % g) g >>= 1;
+  return g;
+}
+
 // Workspace: x16 [M][K] fp16, XgT [G][Mp] fp32, einv [Mp] fp32, and with
 // split K the partial sums [ks][2][Mp][N] fp32 (sized for the larger of the
 // two tilings, gate/up and down / projection).
 size_t prefill_ws_bytes(long M, long K, long N, long group, int sms) {
+  if (group == 0) group = prefill_bf16_group(K);  // dense bf16 weights
   const long Mp = (M + PF_COLS - 1) / PF_COLS * PF_COLS;
   const long nct = (M + prefill_nt(M) - 1) / prefill_nt(M);
   int kbs = 0;
@@ -751,7 +786,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 template <int FMT, int KIND, int NT>
 mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   constexpr int NW = KIND == 0 ? 2 : 1;
-  const int M = p.M, K = p.K, N = p.N, group = p.group;
+  constexpr bool BFW = FMT == FMT_BF16;
+  const int M = p.M, K = p.K, N = p.N, group = BFW ? prefill_bf16_group(p.K) : p.group;
   using SH = PfShape<FMT, KIND, NT>;
   const int n_ctiles = (M + NT - 1) / NT, Mp = (M + PF_COLS - 1) / PF_COLS * PF_COLS;
   const int n_rtiles = (N + SH::FT - 1) / SH::FT;
@@ -776,14 +812,28 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
   const cuuint32_t box[2] = {(cuuint32_t)PF_KB, (cuuint32_t)NT};
   const cuuint32_t estr[2] = {1, 1};
-  if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  // x: the fp16 rows of the workspace, or (bf16 weights) the bf16 input as stored
+  if (enc(&xmap, BFW ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+          BFW ? const_cast<uint16_t*>(p.x) : static_cast<void*>(x16), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE,
           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
       CUDA_SUCCESS)
     return cuda_fail(cudaErrorInvalidValue);
-  // code tiles: 128 rows x CB bytes, 64-byte (INT8) or 32-byte (INT4) swizzle
+  // code tiles: 128 rows x CB bytes, 64-byte (INT8) or 32-byte (INT4) swizzle;
+  // bf16 weights: the A tile itself, 64 elements (128 B) a row, 128-byte swizzle
   CUtensorMap wmap[2];
   for (int mat = 0; mat < 2; ++mat) {
     const void* W = (mat && NW == 2) ? p.W1 : p.W0;
+    if constexpr (BFW) {
+      const cuuint64_t wdims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+      const cuuint64_t wstr[1] = {(cuuint64_t)K * 2};
+      const cuuint32_t wbox[2] = {(cuuint32_t)PF_KB, (cuuint32_t)SH::FT};
+      if (enc(&wmap[mat], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), wdims, wstr, wbox, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cuda_fail(cudaErrorInvalidValue);
+      continue;
+    }
     const cuuint64_t wdims[2] = {(cuuint64_t)(SH::CB == 64 ? K : K / 2), (cuuint64_t)N};
     const cuuint64_t wstr[1] = {wdims[0]};
     const cuuint32_t wbox[2] = {(cuuint32_t)SH::CB, (cuuint32_t)SH::FT};  // gate/up: 64 rows of each
@@ -812,13 +862,13 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   a.W1 = static_cast<const uint8_t*>(p.W1);
   a.s0 = p.s0; a.b0 = p.b0; a.s1 = p.s1; a.b1 = p.b1;
   a.XgT = XgT;
-  a.einv = einv;
+  a.einv = BFW ? nullptr : einv;
   a.res = p.res;
   a.res_ld = p.res_ld;
   a.out = p.out;
   a.out_f32 = p.out_f32 ? 1 : 0;
   a.M = M; a.K = K; a.N = N; a.group = group;
-  a.lg_group = group == 32 ? 5 : (group == 64 ? 6 : 7);
+  a.lg_group = 31 - __builtin_clz((unsigned)group);
   a.G = G;
   a.KB = K / PF_KB;
   a.row_bytes = SH::CB == 64 ? K : K / 2;
@@ -829,8 +879,11 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   a.part = part;
   a.err = err;
 
-  mt_status st = launch(prefill_x_kernel, dim3(Mp), dim3(256), 0, l, p.x, M, K, group, x16, XgT, einv);
-  if (st != MT_OK) return st;
+  mt_status st = MT_OK;
+  if (!BFW) {  // bf16 weights take x as stored
+    st = launch(prefill_x_kernel, dim3(Mp), dim3(256), 0, l, p.x, M, K, group, x16, XgT, einv);
+    if (st != MT_OK) return st;
+  }
   const size_t smem = SH::SMEM;
   auto kern = prefill_gemm_kernel<FMT, KIND, NT>;
   static std::mutex mu;
@@ -852,7 +905,7 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   const long total = (long)M * N;
   const unsigned fgrid = (unsigned)std::min<long>((total + 255) / 256, (long)di->sm_count * 16);
   return launch(prefill_finalize_kernel<KIND>, dim3(fgrid), dim3(256), 0, l, (const float*)part, ks, Mp,
-                (const float*)einv, M, N, p.res, p.res_ld, p.out, p.out_f32 ? 1 : 0);
+                (const float*)a.einv, M, N, p.res, p.res_ld, p.out, p.out_f32 ? 1 : 0);
 }
 
 // The activation-row tile: the smallest of 64, 128, 256 that holds M (a

@@ -202,7 +202,8 @@ def test_prefill_validation(lib):
 
     assert call(ws=None) == NULL
     assert call(bi=None) == NULL
-    assert call(fmt=0, g=0, sc=None, bi=None) == FORMAT     # bf16 weights are decode-only
+    assert call(fmt=0, g=64, sc=None, bi=None) == GROUP     # bf16 weights take group 0
+    assert call(fmt=0, g=0, bi=None) == FORMAT              # and no scales
     assert call(fmt=3, g=32) == FORMAT                      # MX weights take no biases
     assert call(fmt=4, g=64, bi=None) == GROUP               # MX blocks are 32
     assert call(g=96) == GROUP

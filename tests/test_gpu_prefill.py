@@ -214,3 +214,31 @@ def test_prefill_mx(mt, bits, M, K, N):
         torch.cuda.synchronize()
         for k, ref in refs.items():
             check(get(outs[k]), ref, f"{k} ({'f32' if out_f32 else 'bf16'})")
+
+
+@pytest.mark.parametrize("M,K,N", [(40, 512, 200), (130, 1536, 136), (300, 768, 64), (9, 64, 77)])
+def test_prefill_bf16_weights(mt, M, K, N):
+    """Dense bf16 weights on the prefill GEMMs (bf16 MMA operands, x as
+    stored): gate/up, down and projection against the oracle."""
+    seed = 14000 + M + K + N
+    x = synth.host_bf16(M * K, seed, synth.ACT).reshape(M, K)
+    Wg = synth.host_bf16(N * K, seed + 1, synth.WEIGHT).reshape(N, K)
+    Wu = synth.host_bf16(N * K, seed + 2, synth.WEIGHT).reshape(N, K)
+    og, ou = oracle.Weight(oracle.FMT_BF16, Wg), oracle.Weight(oracle.FMT_BF16, Wu)
+    res = synth.host_bf16(M * N, seed + 3, synth.ACT).reshape(M, N)
+    bias = synth.host_bf16(N, seed + 4, synth.PROJ_BIAS)
+    refs = {"h": oracle.swiglu_gateup(x, og, ou), "y": oracle.down_residual(x, og, res),
+            "y + bias": oracle.linear_bias(x, ou, bias)}
+    ws = _ws(mt, M, K, N, 0)
+    xd, gd, ud = dev_bf16(x), dev_bf16(Wg), dev_bf16(Wu)
+    for out_f32 in (False, True):
+        dt = torch.float32 if out_f32 else torch.bfloat16
+        check = assert_f32_close if out_f32 else assert_bf16_close
+        get = host_f64 if out_f32 else host_bits
+        outs = {k: torch.empty(M, N, dtype=dt, device="cuda") for k in refs}
+        mt.mt_prefill_swiglu_gateup(xd, gd, ud, None, None, 0, outs["h"], ws, fmt=0)
+        mt.mt_prefill_down_residual(xd, gd, None, None, 0, dev_bf16(res), outs["y"], ws, fmt=0)
+        mt.mt_prefill_linear_bias(xd, ud, None, None, 0, dev_bf16(bias), outs["y + bias"], ws, fmt=0)
+        torch.cuda.synchronize()
+        for k, ref in refs.items():
+            check(get(outs[k]), ref, f"{k} ({'f32' if out_f32 else 'bf16'})")

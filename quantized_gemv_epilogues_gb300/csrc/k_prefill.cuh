@@ -10,33 +10,38 @@
 // epilogues).
 //
 // GB300 design:
-//  * One CTA computes a tile of 128 weight rows (output features) x 64
-//    activation rows (tokens): D[128 x 64] = W_tile[128 x K] . X_tile[64 x K]^T
-//    with tcgen05.mma (cta_group::1, M = 128, N = 64, K = 16, fp16 operands,
-//    fp32 accumulators in tensor memory), one accumulator per weight matrix
-//    (two for gate/up).
-//  * The affine codes enter the MMA exactly: the fp16 bit pattern 0x00qq is
-//    q * 2^-24 (a subnormal), so one byte permute per two codes (INT8) or a
-//    mask and permute (INT4) builds the operand.  Four converter warps load
-//    the codes from global memory (one weight row per thread, one K block
-//    ahead in registers) and write them into shared memory in the MMA's
-//    128-byte-swizzled K-major layout.
-//  * The activations are converted once per call (prefill_x_kernel) to fp16
-//    scaled per token row by 2^e_m (max|x_m| 2^e_m in [2^14, 2^15): every
-//    bf16 value above 2^-28 of its row's maximum is exact), and their group
-//    sums X'_g = sum_{k in g} x 2^e_m are kept in fp32.  TMA (2D tiled,
-//    SWIZZLE_128B) brings each 64 x 64 fp16 tile into shared memory.
+//  * One CTA computes a tile of 128 A rows x NT activation rows (NT = 64,
+//    128 or 256 by M): D[128 x NT] = A[128 x K] . X[NT x K]^T with
+//    tcgen05.mma (cta_group::1, M = 128, N = NT, K = 16, fp32 accumulators
+//    in tensor memory).  The A rows are 128 output features (down /
+//    projection) or 64 gate rows over the same 64 up rows (gate/up), so one
+//    MMA per K step covers both matrices.
+//  * A operand: affine codes enter exactly as fp16 subnormals (the bit
+//    pattern 0x00qq is q * 2^-24: one byte permute per two INT8 codes, a
+//    mask and permute for INT4); MX elements as their exact fp16 values
+//    (cvt.rn.f16x2.e4m3x2 / .e2m1x2); two converter warps write them into
+//    the 128-byte-swizzled K-major layout from TMA-filled code tiles.  Dense
+//    bf16 weights go straight from TMA into the A tiles (bf16 MMA).
+//  * B operand: the activations, converted once per call (prefill_x_kernel)
+//    to fp16 scaled per row by 2^e_m (max|x_m| 2^e_m in [2^14, 2^15): every
+//    bf16 value above 2^-28 of its row's maximum is exact) with their group
+//    sums X'_g kept in fp32 (bf16 weights take x as stored); TMA
+//    (SWIZZLE_128B) brings each 64-element K block.
 //  * Each quantisation group accumulates into its own tensor-memory buffer
-//    (two buffers, alternating): the epilogue warpgroup reads a finished
-//    group's accumulator with tcgen05.ld while the MMA fills the other, and
-//    adds s * 2^24 * D + b * X'_g into fp32 registers (one output row per
-//    thread, 64 tokens each).  At the end the row scale 2^-e_m is undone and
-//    the SwiGLU, residual or bias epilogue is applied before the only store.
-//  * Pipeline: four shared-memory stages of (x tile, weight tiles) with
-//    mbarriers: x_full (TMA transaction bytes), w_full (converters),
-//    stage_free (tcgen05.commit after the MMAs that read the stage); two
-//    accumulator buffers with acc_full (tcgen05.commit) and acc_free
-//    (epilogue).  Every wait is bounded (~1 s): on expiry the thread records
+//    (two, alternating): the epilogue warpgroups read a finished group with
+//    tcgen05.ld while the MMA fills the other and add s * D + b * X'_g into
+//    fp32 registers (one A row per thread, NT / 2 activation rows per
+//    warpgroup).  At the end the row scale 2^-e_m is undone, the up rows
+//    hand their totals to the gate rows through shared memory for the
+//    SwiGLU (or the residual / bias is added), and the bf16 tile leaves by
+//    one TMA store.  With few tiles, K is split into slices whose fp32
+//    partial sums prefill_finalize_kernel adds in slice order.
+//  * Warp roles and rings: warp 11 lane 0 issues the x-tile copies (ring X),
+//    lane 1 the code-tile copies (ring C, deeper: they are freed as soon as
+//    converted); warps 8-9 convert ring C into ring B; warp 10 (converged,
+//    elect.sync) issues the MMAs and the tcgen05.commits that free ring X,
+//    ring B and fill the accumulator buffers; warps 0-7 are the epilogue.
+//    Every mbarrier wait is bounded (~1 s): on expiry the thread records
 //    MT_ERR_TIMEOUT in the device error word, the CTA stops, drains its
 //    outstanding copies and MMAs, frees its tensor memory and returns.
 #pragma once
@@ -131,9 +136,9 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// 16 consecutive fp32 columns of this thread's tensor-memory lane at taddr
-// (and at taddr2), the wait for the loads inside the same statement so that
-// no use of the registers can be scheduled before it.
+// 16 consecutive fp32 columns of this thread's tensor-memory lane at taddr,
+// the wait for the load inside the same statement so that no use of the
+// registers can be scheduled before it.
 __device__ __forceinline__ void tc_ld16_wait(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(
@@ -145,24 +150,6 @@ __device__ __forceinline__ void tc_ld16_wait(uint32_t taddr, float (&v)[16]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tc_ld16x2_wait(uint32_t ta, uint32_t tb, float (&va)[16], float (&vb)[16]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(ta), "r"(tb)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    va[i] = __uint_as_float(r[i]);
-    vb[i] = __uint_as_float(r[16 + i]);
-  }
 }
 
 // Plain global stores as inline PTX: the compiler then knows they touch no

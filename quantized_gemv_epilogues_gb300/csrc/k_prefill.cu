@@ -2,6 +2,7 @@
 // weights, the dispatch over weight formats and the C ABI of the prefill
 // calls.
 #include "k_prefill.cuh"
+#include "k_prefill_dq.cuh"
 
 namespace mt {
 
@@ -46,6 +47,12 @@ __global__ void __launch_bounds__(256) prefill_x_kernel(const uint16_t* __restri
 
 
 mt_status launch_prefill(const GemvProblem& p, void* ws, const Launch& l) {
+  // bf16 outputs: weights dequantised to fp16 tiles, one accumulator over K;
+  // fp32 outputs: exact operands, one tensor-memory sum per group
+  if (p.fmt == MT_W_AFFINE8 && !p.out_f32)
+    return p.kind == Kind::GateUp ? run_prefill_dq_nt<FMT_A8, 0>(p, ws, l) : run_prefill_dq_nt<FMT_A8, 1>(p, ws, l);
+  if (p.fmt == MT_W_AFFINE4 && !p.out_f32)
+    return p.kind == Kind::GateUp ? run_prefill_dq_nt<FMT_A4, 0>(p, ws, l) : run_prefill_dq_nt<FMT_A4, 1>(p, ws, l);
   if (p.fmt == MT_W_AFFINE8)
     return p.kind == Kind::GateUp ? run_prefill_nt<FMT_A8, 0>(p, ws, l) : run_prefill_nt<FMT_A8, 1>(p, ws, l);
   if (p.fmt == MT_W_AFFINE4)

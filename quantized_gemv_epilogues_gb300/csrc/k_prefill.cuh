@@ -62,10 +62,15 @@ namespace mt {
 constexpr int PF_ROWS = 128;       // weight rows per tile (MMA M)
 constexpr int PF_COLS = 256;       // largest activation-row tile (MMA N); 64 and 128 for small M
 constexpr int PF_KB = 64;          // K per stage (one 128-byte swizzle row of fp16)
-constexpr int PF_EPI_WARPS = 8;    // warps 0-7: epilogue, two warpgroups (64 tile columns each)
+constexpr int PF_EPI_WARPS = 8;    // warps 0-7: epilogue, two warpgroups (NT / 2 tile columns each)
 constexpr int PF_CONV_WARPS = 2;   // warps 8-9: converters
 constexpr int PF_THREADS = 32 * (PF_EPI_WARPS + PF_CONV_WARPS + 2);  // + warp 10: MMA, warp 11: TMA
 constexpr int PF_W_TILE = PF_ROWS * PF_KB * 2;   // 16 KB
+// Groups whose scale, bias and X'_g the epilogue has in flight ahead of use
+// (even): a group's MMAs take well under the latency of a global load under
+// the tensor-core stream, so one group ahead left the MMA waiting for the
+// epilogue.
+constexpr int PF_EPI_AHEAD = 4;
 
 struct PrefillArgs {
   const uint8_t* W0;  // gate (kind 0) or the weight (kind 1): codes [N][row_bytes]
@@ -87,6 +92,8 @@ struct PrefillArgs {
   float* part;          // ks > 1: partial sums [ks][NW][Mp][N] before the row scale and epilogue
   int tma_store;        // 1: bf16 output written by one TMA store per tile (row stride a multiple of 16 B)
   int* err;             // device error word
+  const float* tsc;     // dequantising kernel: 2^t_n of each weight row [NW][N]
+  const float* tinv;    // and 2^-t_n
 };
 
 // ------------------------------------------------------------- PTX wrappers
@@ -331,7 +338,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   __shared__ __align__(8) uint64_t bars[2 * (SX + SC + SB) + 5];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
-  __shared__ __align__(16) float xg_sh[2][NT];  // X'_g of the tile's rows, two groups
+  __shared__ __align__(16) float xg_sh[PF_EPI_AHEAD][NT];  // X'_g of the tile's rows, a ring of groups
   __shared__ __align__(16) float einv_sh[NT];   // 2^-e_m of the tile's rows
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -365,15 +372,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     }
     for (int i = 0; i < SC; ++i) {
       mbar_init(c_full(i), 1);
-      mbar_init(c_free(i), CONV);
+      mbar_init(c_free(i), PF_CONV_WARPS);  // one arrival per converter warp
     }
     for (int i = 0; i < SB; ++i) {
-      mbar_init(w_full(i), BFW ? 1 : CONV);  // TMA (bf16 weights) or the converters
+      mbar_init(w_full(i), BFW ? 1 : PF_CONV_WARPS);  // TMA (bf16 weights) or the converter warps
       mbar_init(b_free(i), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
-      mbar_init(acc_free(b), EPI);
+      mbar_init(acc_free(b), PF_EPI_WARPS);  // one arrival per epilogue warp
     }
     mbar_init(mma_done, 1);
     abort_sh = 0;
@@ -434,13 +441,19 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int c = tid - 32 * CONV0;
     for (int kb = 0; kb < KB; ++kb) {
       const int i = kb % SC, j = kb % SB;
-      if (!mbar_wait_bounded(c_full(i), (kb / SC) & 1)) { fail(); break; }
-      if (kb >= SB && !mbar_wait_bounded(b_free(j), ((kb / SB) + 1) & 1)) { fail(); break; }
+      bool ok = mbar_wait_bounded(c_full(i), (kb / SC) & 1);
+      if (ok && kb >= SB) ok = mbar_wait_bounded(b_free(j), ((kb / SB) + 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) { fail(); break; }
       pf_convert_rows<FMT, PF_ROWS / CONV>(cslot(i), wslot(j), c, CONV);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor core reads
-      mbar_arrive(w_full(j));
-      mbar_arrive(c_free(i));
-      if (*abort_flag) break;
+      // one arrival per warp (an mbarrier arrival is a shared-memory atomic:
+      // 32 of them on one word serialise)
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(w_full(j));
+        mbar_arrive(c_free(i));
+      }
+      if (__any_sync(0xffffffffu, *abort_flag)) break;
     }
     }
   } else if (warp == MMA_WARP) {
@@ -449,7 +462,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     bool ok = true;
     for (int kb = 0; kb < KB && ok; ++kb) {
       const int i = kb % SX, jb = kb % SB;
-      if (!mbar_wait_bounded(x_full(i), (kb / SX) & 1) || !mbar_wait_bounded(w_full(jb), (kb / SB) & 1)) {
+      // one decision for the whole warp (elect.sync below needs every lane)
+      const bool got = mbar_wait_bounded(x_full(i), (kb / SX) & 1) && mbar_wait_bounded(w_full(jb), (kb / SB) & 1);
+      if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
       }
@@ -462,7 +477,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const int gi = k >> a.lg_group, b = gi & 1;  // group within the slice
         const bool first = (k & (group - 1)) == 0;
         if (first && gi >= 2) {
-          if (!mbar_wait_bounded(acc_free(b), ((gi >> 1) - 1) & 1)) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(acc_free(b), ((gi >> 1) - 1) & 1))) { ok = false; break; }
           tc_fence_after();
         }
         if (elect_one()) {
@@ -476,7 +491,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         tc_commit(x_free(i));
       }
       __syncwarp();
-      if (*abort_flag) break;
+      if (__any_sync(0xffffffffu, *abort_flag)) break;
     }
     if (!ok) fail();
     if (elect_one()) tc_commit(mma_done);  // completes when every MMA issued above has
@@ -496,29 +511,39 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 #pragma unroll
     for (int j = 0; j < HALF; ++j) acc[j] = 0.f;
     const uint32_t lane_base = tbase + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(wg * HALF);
-    // group scale and bias: affine s * 2^24 (the codes enter the MMA as
+    // group scale and bias, loaded raw PD groups ahead of their use and
+    // converted there: affine s * 2^24 (the codes enter the MMA as
     // q * 2^-24) and b; MX the E8M0 block scale 2^(E - 127) and no bias
     constexpr bool MXF = FmtTraits<FMT>::MX;
-    auto scale_of = [&](size_t i) -> float {
+    constexpr int PD = PF_EPI_AHEAD;
+    auto raw_scale = [&](int gi) -> uint32_t {
+      if constexpr (BFW) return 0u;
+      else if constexpr (MXF) return (okr && gi < G) ? (uint32_t)__ldg(reinterpret_cast<const uint8_t*>(sp) + sbo + gi) : 0u;
+      else return (okr && gi < G) ? (uint32_t)__ldg(sp + sbo + gi) : 0u;
+    };
+    auto raw_bias = [&](int gi) -> uint32_t {
+      if constexpr (MXF || BFW) return 0u;
+      else return (okr && gi < G) ? (uint32_t)__ldg(bp + sbo + gi) : 0u;
+    };
+    auto scale_of = [&](uint32_t raw) -> float {
       if constexpr (BFW) {
         return 1.0f;  // dense bf16 weights: D is the dot product itself
       } else if constexpr (MXF) {
-        const uint32_t E = reinterpret_cast<const uint8_t*>(sp)[i];
-        return E ? __int_as_float((int)(E << 23)) : __int_as_float(0x00400000);
+        return raw ? __int_as_float((int)(raw << 23)) : __int_as_float(0x00400000);
       } else {
-        return bf16f(sp[i]) * 16777216.f;
+        return bf16f((uint16_t)raw) * 16777216.f;
       }
     };
-    auto bias_of = [&](size_t i) -> float {
+    auto bias_of = [&](uint32_t raw) -> float {
       if constexpr (MXF || BFW) return 0.f;
-      else return bf16f(bp[i]);
+      else return bf16f((uint16_t)raw);
     };
-    float sv = okr ? scale_of(sbo) : 0.f;
-    float bv = okr ? bias_of(sbo) : 0.f;
-    // X'_g of group gi for the tile's rows comes into xg_sh[gi & 1] by
-    // asynchronous copies one group ahead (threads 0-63, 16 bytes each)
+    // X'_g of group gi for the tile's rows comes into xg_sh[gi % PD] by
+    // asynchronous copies PD - 1 groups ahead (threads 0-63, 16 bytes each);
+    // one commit group per group index, empty past the slice's end
     auto fetch_xg = [&](int gi) {
-      if (!BFW && tid < NT / 4) cp_async16(&xg_sh[gi & 1][4 * tid], a.XgT + (size_t)(g0 + gi) * Mp + m0 + 4 * tid);
+      if (!BFW && gi < G && tid < NT / 4)
+        cp_async16(&xg_sh[gi % PD][4 * tid], a.XgT + (size_t)(g0 + gi) * Mp + m0 + 4 * tid);
       cp_async_commit();
     };
     auto epi_sync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(EPI) : "memory"); };
@@ -533,56 +558,69 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           : "memory");
       return res != 0;
     };
-    // the tile's row scales (padded rows hold 0) with group 0's sums
+    // the tile's row scales (padded rows hold 0), in the first commit group
     if constexpr (BFW) {  // x enters the MMA as stored: no row scale, no group sums
       for (int i = tid; i < NT; i += EPI) einv_sh[i] = 1.0f;
     } else {
       if (tid < NT / 4) cp_async16(&einv_sh[4 * tid], a.einv + m0 + 4 * tid);
     }
-    fetch_xg(0);
-    cp_async_wait_all();
+    uint32_t sq[PD], bq[PD];  // raw scale and bias of groups gi0 + u (then gi0 + PD + u)
+#pragma unroll
+    for (int u = 0; u < PD; ++u) {
+      sq[u] = raw_scale(u);
+      bq[u] = raw_bias(u);
+    }
+#pragma unroll
+    for (int u = 0; u < PD - 1; ++u) fetch_xg(u);
+    cp_async_wait_group<PD - 2>();  // group 0's sums and the row scales landed
     epi_sync();
     bool aborted = false;
-    for (int gi = 0; gi < G; ++gi) {
-      const int b = gi & 1;
-      if (gi + 1 < G) fetch_xg(gi + 1);
-      // the next group's scale and bias, ahead of the wait
-      const bool more = okr && gi + 1 < G;
-      const float sn = more ? scale_of(sbo + gi + 1) : 0.f;
-      const float bn = more ? bias_of(sbo + gi + 1) : 0.f;
-      if (!mbar_wait_bounded(acc_full(b), (gi >> 1) & 1)) { fail(); aborted = true; }
-      if (!aborted) {
-        tc_fence_after();
-        const float* xg = xg_sh[b] + wg * HALF;
+    for (int gi0 = 0; gi0 < G && !aborted; gi0 += PD) {
 #pragma unroll
-        for (int q = 0; q < HALF / 16; ++q) {
-          float d[16];
-          tc_ld16_wait(lane_base + (uint32_t)(b * NT + q * 16), d);
+      for (int u = 0; u < PD; ++u) {
+        const int gi = gi0 + u, b = u & 1;  // gi % PD == u, gi & 1 == b (PD even)
+        if (gi >= G) break;
+        fetch_xg(gi + PD - 1);
+        const float sv = scale_of(sq[u]), bv = bias_of(bq[u]);
+        sq[u] = raw_scale(gi + PD);
+        bq[u] = raw_bias(gi + PD);
+        if (!mbar_wait_bounded(acc_full(b), (gi >> 1) & 1)) { fail(); aborted = true; }
+        // the tensor-memory loads below are warp-wide: one decision per warp
+        aborted = __any_sync(0xffffffffu, aborted);
+        if (!aborted) {
+          tc_fence_after();
+          const float* xg = xg_sh[u] + wg * HALF;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 X = *reinterpret_cast<const float4*>(xg + q * 16 + 4 * i);
-            const float Xv[4] = {X.x, X.y, X.z, X.w};
+          for (int q = 0; q < HALF / 16; ++q) {
+            float d[16];
+            tc_ld16_wait(lane_base + (uint32_t)(b * NT + q * 16), d);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int jj = q * 16 + 4 * i + e;
-              if constexpr (BFW || MXF)
-                acc[jj] = fmaf(sv, d[4 * i + e], acc[jj]);  // no bias term
-              else
-                acc[jj] = fmaf(sv, d[4 * i + e], fmaf(bv, Xv[e], acc[jj]));
+            for (int i = 0; i < 4; ++i) {
+              const float4 X = *reinterpret_cast<const float4*>(xg + q * 16 + 4 * i);
+              const float Xv[4] = {X.x, X.y, X.z, X.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int jj = q * 16 + 4 * i + e;
+                if constexpr (BFW || MXF)
+                  acc[jj] = fmaf(sv, d[4 * i + e], acc[jj]);  // no bias term
+                else
+                  acc[jj] = fmaf(sv, d[4 * i + e], fmaf(bv, Xv[e], acc[jj]));
+              }
             }
           }
         }
+        // this warp is done reading the buffer: one arrival for the warp
         tc_fence_before();
-        mbar_arrive(acc_free(b));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_free(b));
+        // the next group's X'_g has landed and every thread is done with
+        // this one; the decision to stop is the same for every epilogue thread
+        cp_async_wait_group<PD - 2>();
+        aborted = epi_sync_or(aborted || *abort_flag);
+        if (aborted) break;
       }
-      sv = sn;
-      bv = bn;
-      // the next group's X'_g has landed and every thread is done with this
-      // one; the decision to stop is the same for every epilogue thread
-      cp_async_wait_all();
-      aborted = epi_sync_or(aborted || *abort_flag);
-      if (aborted) break;
     }
+    cp_async_wait_all();  // nothing left in flight (after an abort: copies of later groups)
     if (!aborted && a.ks > 1) {
       // split K: this slice's sums, before the row scale and the epilogue
       if (okr) {
@@ -676,11 +714,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   if (warp == MMA_WARP) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(NCOLS));
 }
 
-// Split K: the slices' partial sums added in slice order, the row scale
-// undone and the epilogue applied (one thread per output element).
+// Split K: the slices' partial sums added in slice order, the row scales
+// (2^-e_m of the activations; 2^-t_n of dequantised weight rows) undone and
+// the epilogue applied (one thread per output element).
 template <int KIND>
 __global__ void __launch_bounds__(256) prefill_finalize_kernel(const float* __restrict__ part, int ks, int Mp,
-                                                               const float* __restrict__ einv, int M, int N,
+                                                               const float* __restrict__ einv,
+                                                               const float* __restrict__ tinv, int M, int N,
                                                                const uint16_t* __restrict__ res, int res_ld,
                                                                void* out, int out_f32) {
   constexpr int NW = KIND == 0 ? 2 : 1;
@@ -692,7 +732,9 @@ __global__ void __launch_bounds__(256) prefill_finalize_kernel(const float* __re
     for (int mat = 0; mat < NW; ++mat) {
       float t = 0.f;
       for (int s = 0; s < ks; ++s) t += part[((size_t)(s * NW + mat) * Mp + m) * N + n];
-      v[mat] = einv ? t * einv[m] : t;
+      if (einv) t *= einv[m];
+      if (tinv) t *= tinv[(size_t)mat * N + n];  // 2^-t_n of the dequantised weight row
+      v[mat] = t;
     }
     float o;
     if constexpr (KIND == 0)
@@ -740,18 +782,31 @@ int prefill_bf16_group(long K) {
   return g;
 }
 
-// Workspace: x16 [M][K] fp16, XgT [G][Mp] fp32, einv [Mp] fp32, and with
-// split K the partial sums [ks][2][Mp][N] fp32 (sized for the larger of the
-// two tilings, gate/up and down / projection).
-size_t prefill_ws_bytes(long M, long K, long N, long group, int sms) {
+// Workspace: x16 [M][K] fp16, XgT [G][Mp] fp32, einv [Mp] fp32, the weight
+// rows' 2^t_n and 2^-t_n [2][2][N] fp32 (dequantising kernel), and with split
+// K the partial sums [ks][2][Mp][N] fp32 (sized for the largest split of both
+// tilings, gate/up and down / projection, and both kernels).
+struct PfWs {
+  size_t xg, einv, tw, part, total;  // byte offsets (x16 at 0) and the size
+};
+PfWs prefill_ws_layout(long M, long K, long N, long group, int sms) {
   if (group == 0) group = prefill_bf16_group(K);  // dense bf16 weights
   const long Mp = (M + PF_COLS - 1) / PF_COLS * PF_COLS;
   const long nct = (M + prefill_nt(M) - 1) / prefill_nt(M);
-  int kbs = 0;
-  const int ks = std::max(prefill_ks(nct * ((N + 63) / 64), K, group, sms, &kbs),
-                          prefill_ks(nct * ((N + 127) / 128), K, group, sms, &kbs));
+  int kbs = 0, ks = 1;
+  for (long g : {group, (long)PF_KB})
+    for (long ft : {64L, 128L}) ks = std::max(ks, prefill_ks(nct * ((N + ft - 1) / ft), K, g, sms, &kbs));
   const size_t part = ks > 1 ? (size_t)ks * 2 * Mp * N * 4 : 0;
-  return al1k((size_t)M * K * 2) + al1k((size_t)(K / group) * Mp * 4) + al1k((size_t)Mp * 4) + al1k(part);
+  PfWs w;
+  w.xg = al1k((size_t)M * K * 2);
+  w.einv = w.xg + al1k((size_t)(K / group) * Mp * 4);
+  w.tw = w.einv + al1k((size_t)Mp * 4);
+  w.part = w.tw + al1k((size_t)16 * N);
+  w.total = w.part + al1k(part);
+  return w;
+}
+size_t prefill_ws_bytes(long M, long K, long N, long group, int sms) {
+  return prefill_ws_layout(M, K, N, group, sms).total;
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once.
@@ -779,14 +834,15 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   const int n_ctiles = (M + NT - 1) / NT, Mp = (M + PF_COLS - 1) / PF_COLS * PF_COLS;
   const int n_rtiles = (N + SH::FT - 1) / SH::FT;
   const int G = K / group;
-  unsigned char* w = static_cast<unsigned char*>(ws);
-  __half* x16 = reinterpret_cast<__half*>(w);
-  float* XgT = reinterpret_cast<float*>(w + al1k((size_t)M * K * 2));
-  float* einv = reinterpret_cast<float*>(w + al1k((size_t)M * K * 2) + al1k((size_t)G * Mp * 4));
-  float* part = reinterpret_cast<float*>(w + al1k((size_t)M * K * 2) + al1k((size_t)G * Mp * 4) + al1k((size_t)Mp * 4));
   int derr = 0;
   const DeviceInfo* di = device_info(&derr);
   if (!di) return cuda_fail((cudaError_t)derr);
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  const PfWs wl = prefill_ws_layout(M, K, N, group, di->sm_count);
+  __half* x16 = reinterpret_cast<__half*>(w);
+  float* XgT = reinterpret_cast<float*>(w + wl.xg);
+  float* einv = reinterpret_cast<float*>(w + wl.einv);
+  float* part = reinterpret_cast<float*>(w + wl.part);
   int kbs = 0;
   const int ks = prefill_ks((long)n_rtiles * n_ctiles, K, group, di->sm_count, &kbs);
   int* err = device_error_ptr();
@@ -892,7 +948,7 @@ mt_status run_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   const long total = (long)M * N;
   const unsigned fgrid = (unsigned)std::min<long>((total + 255) / 256, (long)di->sm_count * 16);
   return launch(prefill_finalize_kernel<KIND>, dim3(fgrid), dim3(256), 0, l, (const float*)part, ks, Mp,
-                (const float*)a.einv, M, N, p.res, p.res_ld, p.out, p.out_f32 ? 1 : 0);
+                (const float*)a.einv, (const float*)nullptr, M, N, p.res, p.res_ld, p.out, p.out_f32 ? 1 : 0);
 }
 
 // The activation-row tile: the smallest of 64, 128, 256 that holds M (a

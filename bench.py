@@ -747,7 +747,8 @@ def run_prefill(args, torch, synth, mt, dev):
             "data": "synthetic",
             "config": {"workload": "qwen3-8b layer d4096 f12288 affine8 g128, M activation rows, 3 distinct layers cycled",
                        "l2": "weights of 3 layers (467 MB) exceed the L2"},
-            "roofline": {"bound": "tensor", "kernel": f"prefill_gemm_kernel (M = {top['M']})",
+            "roofline": {"bound": "tensor",
+                         "kernel": f"prefill_dq_kernel (bf16 outputs: fp16-dequantised weight tiles; M = {top['M']})",
                          "achieved": top["tflops"], "peak": tpk, "unit": "TFLOP/s",
                          "frac": top["frac_of_tensor_peak"], "peak_kind": tpk_kind},
             "hbm_peak": hbm, "hbm_peak_kind": hbm_kind, "points": points, "device_error": mt.mt_device_error()}

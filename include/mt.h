@@ -208,9 +208,9 @@ mt_status mt_linear_bias(const void* x, const void* W, const void* scales,
 /*
  * Multi-row prefill (M > 8 activation rows, any M >= 1) of the same three
  * GEMV epilogues as tensor-core GEMMs (tcgen05 with tensor-memory
- * accumulators, TMA-fed activation tiles): a 128-output x 64-row tile per
- * CTA, the gate and up tiles of a row range computed together and the SwiGLU
- * applied before the only store.  meTile docs, "MLX-LM Backend", Dispatch
+ * accumulators, TMA-fed activation tiles): a tile of 128 weight rows x 64,
+ * 128 or 256 activation rows per CTA, the gate and up rows of a feature range
+ * in one tile and the SwiGLU applied before the only store.  meTile docs, "MLX-LM Backend", Dispatch
  * Policy (multi-row shapes: a row-tiled dual GEMM with the SwiGLU in
  * registers); "Compute-Graph Fusion", Automatic Gated Epilogues.
  *   Arguments, layouts and results as mt_swiglu_gateup / mt_down_residual /
@@ -227,11 +227,17 @@ mt_status mt_linear_bias(const void* x, const void* W, const void* scales,
  * Limits: 1 <= M <= 2^20; K % 64 == 0 and K % group == 0; 64 <= K <= 65536;
  *         1 <= N <= 2^20.  A workspace below the required size is
  *         MT_ERR_SHAPE.  out_y may equal residual (bf16 output).
- * Accumulation: each quantisation group's code . x sum is exact products
- * with fp32 accumulation on the tensor cores (codes as fp16 q * 2^-24; x as
- * fp16 scaled per activation row by a power of two, exact for every bf16
- * value above 2^-28 of the row's maximum); scales, biases and the total are
- * fp32.
+ * Accumulation, fp32 outputs (and MX or bf16 weights): each quantisation
+ * group's code . x sum is exact products with fp32 accumulation on the
+ * tensor cores (codes as fp16 q * 2^-24; x as fp16 scaled per activation row
+ * by a power of two, exact for every bf16 value above 2^-28 of the row's
+ * maximum); scales, biases and the total are fp32.
+ * Accumulation, bf16 outputs over affine weights (the pages' multi-row path
+ * dequantises weight tiles into the activations' type before the matmul):
+ * each weight w = s q + b is formed in fp32 times a power of two 2^t_n per
+ * weight row (max |w| 2^t_n < 2^15) and rounded once to fp16 (relative error
+ * at most 2^-11), and the whole K range accumulates in fp32 on the tensor
+ * cores; the workspace also holds the rows' 2^t_n.
  */
 size_t mt_prefill_workspace_bytes(int M, int K, int N, int group);
 mt_status mt_prefill_swiglu_gateup(const void* x, const void* Wg, const void* Wu,

@@ -191,6 +191,13 @@ def test_prefill_validation(lib):
     wsb.argtypes = [ctypes.c_int] * 4
     assert wsb(100, 512, 256, 64) > 100 * 512 * 2      # at least the fp16 activations
     assert wsb(0, 512, 256, 64) == 0 and wsb(10, 512, 256, 48) == 0 and wsb(10, 32, 256, 32) == 0
+    # the documented parts: fp16 activations, group sums [K/g][Mp], 2^-e_m [Mp] and the
+    # dequantised weight rows' 2^t_n and 2^-t_n [2][2][N] (Mp: M rounded up to 256)
+    for M, K, N, g in ((100, 512, 256, 64), (4096, 4096, 12288, 128), (9, 256, 200, 32), (1, 64, 5, 0)):
+        Mp = -(-M // 256) * 256
+        gb = g or max(v for v in (64, 128, 256, 512) if K % v == 0)  # dense bf16: its accumulation group
+        G = K // gb
+        assert wsb(M, K, N, g) >= 2 * M * K + 4 * G * Mp + 4 * Mp + 16 * N, (M, K, N, g)
     f = lib.mt_prefill_linear_bias
     f.restype = ctypes.c_int
     f.argtypes = [P, P, P, P, ctypes.c_int, P, P] + [ctypes.c_int] * 5 + [P, ctypes.c_size_t, P]

@@ -98,6 +98,13 @@ struct PrefillArgs {
 
 // ------------------------------------------------------------- PTX wrappers
 
+// Waits until at most N of this thread's committed asynchronous copy groups
+// (cp.async) are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major fp16 tile whose rows are 128
 // bytes, stored with the 128-byte swizzle (16-byte chunk c of row r at chunk
 // c ^ (r & 7)); 8-row core groups 1024 bytes apart.  The tile starts on a

@@ -237,7 +237,8 @@ mt_status mt_linear_bias(const void* x, const void* W, const void* scales,
  * each weight w = s q + b is formed in fp32 times a power of two 2^t_n per
  * weight row (max |w| 2^t_n < 2^15) and rounded once to fp16 (relative error
  * at most 2^-11), and the whole K range accumulates in fp32 on the tensor
- * cores; the workspace also holds the rows' 2^t_n.
+ * cores; the workspace also holds the rows' 2^t_n.  Dense bf16 weights with
+ * bf16 outputs accumulate the whole K range the same way (exact operands).
  */
 size_t mt_prefill_workspace_bytes(int M, int K, int N, int group);
 mt_status mt_prefill_swiglu_gateup(const void* x, const void* Wg, const void* Wu,

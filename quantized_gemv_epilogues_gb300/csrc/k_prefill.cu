@@ -58,6 +58,8 @@ mt_status launch_prefill(const GemvProblem& p, void* ws, const Launch& l) {
   if (p.fmt == MT_W_AFFINE4)
     return p.kind == Kind::GateUp ? run_prefill_nt<FMT_A4, 0>(p, ws, l) : run_prefill_nt<FMT_A4, 1>(p, ws, l);
   if (p.fmt == MT_W_MXFP8 || p.fmt == MT_W_MXFP4) return launch_prefill_mx(p, ws, l);
+  if (p.fmt == MT_W_BF16 && !p.out_f32)  // one accumulator over K (the operands are exact either way)
+    return p.kind == Kind::GateUp ? run_prefill_dq_nt<FMT_BF16, 0>(p, ws, l) : run_prefill_dq_nt<FMT_BF16, 1>(p, ws, l);
   if (p.fmt == MT_W_BF16)
     return p.kind == Kind::GateUp ? run_prefill_nt<FMT_BF16, 0>(p, ws, l) : run_prefill_nt<FMT_BF16, 1>(p, ws, l);
   return MT_ERR_FORMAT;

@@ -49,16 +49,17 @@ struct PqShape {
   static constexpr int CB = FmtTraits<FMT>::EPW == 4 ? 64 : 32;
   static constexpr int CTILE = PF_ROWS * CB;
   static constexpr int SX = NT == 256 ? 4 : (NT == 128 ? 6 : 8);
-  static constexpr int SB = NT == 256 ? 3 : 4;
+  static constexpr bool BFW = FMT == FMT_BF16;  // dense bf16 weights: no code ring (TMA fills ring B)
+  static constexpr int SB = BFW ? (NT == 256 ? 5 : 6) : (NT == 256 ? 3 : 4);
   static constexpr int SC0 = (217 * 1024 - SX * XT - SB * PF_W_TILE) / CTILE;
-  static constexpr int SC = SC0 > 8 ? 8 : SC0;
+  static constexpr int SC = BFW ? 1 : (SC0 > 8 ? 8 : SC0);
   static constexpr size_t OFF_C = (size_t)SX * XT;
   static constexpr size_t OFF_B = OFF_C + (size_t)SC * CTILE;
   static constexpr size_t SMEM = 1024 + OFF_B + (size_t)SB * PF_W_TILE;
   // the final phase reuses the rings: gate/up the gate and up sums
   // [NT][64] fp32 each and the bf16 tile [NT][64]; otherwise the bf16 tile
   static constexpr size_t FINAL = KIND == 0 ? (size_t)NT * 64 * 4 * 2 + (size_t)NT * 64 * 2 : (size_t)NT * 128 * 2;
-  static_assert(SC >= 2, "code ring");
+  static_assert(BFW || SC >= 2, "code ring");
   static_assert(SMEM <= 218 * 1024, "shared memory plan");
   static_assert(FINAL + 1024 <= SMEM, "final-phase buffers in the rings");
 };
@@ -132,6 +133,7 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
   constexpr int HALF = NT / 2;               // accumulator columns per epilogue warpgroup
   constexpr int MMA_WARP = PQ_CONV_WARPS, TMA_WARP = PQ_CONV_WARPS + 1;
   constexpr bool W8 = CB == 64;              // INT8 codes (else INT4)
+  constexpr bool BFW = SH::BFW;              // dense bf16 weights: exact operands, no dequantising
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -166,7 +168,7 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
       mbar_init(c_free(i), PQ_CONV_WARPS);  // one arrival per dequantising warp
     }
     for (int i = 0; i < SB; ++i) {
-      mbar_init(w_full(i), PQ_CONV_WARPS);
+      mbar_init(w_full(i), BFW ? 1 : PQ_CONV_WARPS);  // TMA (bf16 weights) or the dequantising warps
       mbar_init(b_free(i), 1);
     }
     mbar_init(acc_full, 1);
@@ -191,18 +193,23 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
   if (warp == TMA_WARP) {
     // ---- producers: lane 0 the x tiles, lane 1 the code tiles
     if (lane < 2) {
-      const int S = lane == 0 ? SX : SC;
+      // bf16 weights: lane 1 fills ring B directly
+      const int S = lane == 0 ? SX : (BFW ? SB : SC);
       int issued = 0;
       for (int kb = 0; kb < KB; ++kb) {
         const int i = kb % S;
-        const uint32_t full = lane == 0 ? x_full(i) : c_full(i);
-        const uint32_t free_ = lane == 0 ? x_free(i) : c_free(i);
+        const uint32_t full = lane == 0 ? x_full(i) : (BFW ? w_full(i) : c_full(i));
+        const uint32_t free_ = lane == 0 ? x_free(i) : (BFW ? b_free(i) : c_free(i));
         if (kb >= S && !mbar_wait_bounded(free_, ((kb / S) + 1) & 1)) { fail(); break; }
         if (*abort_flag) break;
         const int kg = kb0 + kb;
         if (lane == 0) {
           mbar_arrive_expect_tx(full, SH::XT);
           tma_load_2d(smem_u32(xslot(i)), &xmap, kg * PF_KB, m0, full);
+        } else if constexpr (BFW) {
+          mbar_arrive_expect_tx(full, PF_W_TILE);
+          tma_load_2d(smem_u32(wslot(i)), &wmap0, kg * PF_KB, f0, full);
+          if constexpr (KIND == 0) tma_load_2d(smem_u32(wslot(i) + 64 * 128), &wmap1, kg * PF_KB, f0, full);
         } else {
           mbar_arrive_expect_tx(full, SH::CTILE);
           tma_load_2d(smem_u32(cslot(i)), &wmap0, kg * CB, f0, full);
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
         ++issued;
       }
       for (int kb = max(0, issued - S); kb < issued; ++kb)
-        (void)mbar_wait_bounded(lane == 0 ? x_full(kb % S) : c_full(kb % S), (kb / S) & 1);
+        (void)mbar_wait_bounded(lane == 0 ? x_full(kb % S) : (BFW ? w_full(kb % S) : c_full(kb % S)), (kb / S) & 1);
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
       const uint64_t wd = pf_desc_sw128(smem_u32(wslot(jb)));
       if (elect_one()) {
 #pragma unroll
-        for (int j = 0; j < PF_KB / 16; ++j) tc_mma<NT, false>(tbase, wd + 2 * j, xd + 2 * j, (kb | j) ? 1u : 0u);
+        for (int j = 0; j < PF_KB / 16; ++j) tc_mma<NT, BFW>(tbase, wd + 2 * j, xd + 2 * j, (kb | j) ? 1u : 0u);
         tc_commit(b_free(jb));
         tc_commit(x_free(i));
       }
@@ -252,13 +259,13 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
     const bool okr = n < a.N;
     const uint16_t* sp = (mat ? a.s1 : a.s0) + (size_t)(okr ? n : 0) * a.G;
     const uint16_t* bp = (mat ? a.b1 : a.b0) + (size_t)(okr ? n : 0) * a.G;
-    const float tsc = okr ? a.tsc[(size_t)mat * a.N + n] : 0.f;
+    const float tsc = (okr && !BFW) ? a.tsc[(size_t)mat * a.N + n] : 0.f;
     // raw bf16 scale and bias of this thread's group in K block kb of the slice
     auto raw_s = [&](int kb) -> uint32_t {
-      return (okr && kb < KB) ? (uint32_t)__ldg(sp + (((kb0 + kb) * PF_KB + 32 * h) >> a.lg_group)) : 0u;
+      return (okr && !BFW && kb < KB) ? (uint32_t)__ldg(sp + (((kb0 + kb) * PF_KB + 32 * h) >> a.lg_group)) : 0u;
     };
     auto raw_b = [&](int kb) -> uint32_t {
-      return (okr && kb < KB) ? (uint32_t)__ldg(bp + (((kb0 + kb) * PF_KB + 32 * h) >> a.lg_group)) : 0u;
+      return (okr && !BFW && kb < KB) ? (uint32_t)__ldg(bp + (((kb0 + kb) * PF_KB + 32 * h) >> a.lg_group)) : 0u;
     };
     uint32_t sq[PQ_AHEAD], bq[PQ_AHEAD];
 #pragma unroll
@@ -267,7 +274,7 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
       bq[u] = raw_b(u);
     }
     bool ok = true;
-    for (int kbu = 0; kbu < KB && ok; kbu += PQ_AHEAD) {
+    for (int kbu = 0; kbu < (BFW ? 0 : KB) && ok; kbu += PQ_AHEAD) {
 #pragma unroll
       for (int u = 0; u < PQ_AHEAD; ++u) {
         const int kb = kbu + u;
@@ -326,7 +333,8 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
           : "memory");
       return res != 0;
     };
-    for (int q = tid; q < NT; q += EPI) einv_sh[q] = a.einv[m0 + q];  // padded rows hold 0
+    // (bf16 weights: x enters as stored, no row scales)
+    for (int q = tid; q < NT; q += EPI) einv_sh[q] = BFW ? 1.0f : a.einv[m0 + q];  // padded rows hold 0
     bool aborted = epi_sync_or(!ok || *abort_flag);
     if (!aborted && !mbar_wait_bounded(acc_full, 0)) {
       fail();
@@ -337,7 +345,7 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
       tc_fence_after();
       const int wg = h, cbase = wg * HALF;
       const uint32_t lane_base = tbase + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)cbase;
-      const float ti = okr ? a.tinv[(size_t)mat * a.N + n] : 0.f;
+      const float ti = !okr ? 0.f : (BFW ? 1.0f : a.tinv[(size_t)mat * a.N + n]);
       const float* ei = einv_sh + cbase;
       constexpr int NW = KIND == 0 ? 2 : 1;
       if (a.ks > 1) {
@@ -439,14 +447,17 @@ template <int FMT, int KIND, int NT>
 mt_status run_prefill_dq(const GemvProblem& p, void* ws, const Launch& l) {
   constexpr int NW = KIND == 0 ? 2 : 1;
   using SH = PqShape<FMT, KIND, NT>;
-  const int M = p.M, K = p.K, N = p.N, group = p.group;
+  constexpr bool BFW = SH::BFW;
+  // (dense bf16 weights have no groups: group 0 in the workspace layout, and
+  // K blocks of 64 stand in for them in the arguments)
+  const int M = p.M, K = p.K, N = p.N, group = BFW ? PF_KB : p.group;
   const int n_ctiles = (M + NT - 1) / NT, Mp = (M + PF_COLS - 1) / PF_COLS * PF_COLS;
   const int n_rtiles = (N + SH::FT - 1) / SH::FT;
   int derr = 0;
   const DeviceInfo* di = device_info(&derr);
   if (!di) return cuda_fail((cudaError_t)derr);
   unsigned char* w = static_cast<unsigned char*>(ws);
-  const PfWs wl = prefill_ws_layout(M, K, N, group, di->sm_count);
+  const PfWs wl = prefill_ws_layout(M, K, N, p.group, di->sm_count);
   __half* x16 = reinterpret_cast<__half*>(w);
   float* XgT = reinterpret_cast<float*>(w + wl.xg);
   float* einv = reinterpret_cast<float*>(w + wl.einv);
@@ -466,7 +477,9 @@ mt_status run_prefill_dq(const GemvProblem& p, void* ws, const Launch& l) {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {(cuuint32_t)PF_KB, (cuuint32_t)NT};
-    if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, static_cast<void*>(x16), dims, strides, box, estr,
+    // x: the fp16 rows of the workspace, or (bf16 weights) the bf16 input as stored
+    if (enc(&xmap, BFW ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+            BFW ? const_cast<uint16_t*>(p.x) : static_cast<void*>(x16), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cuda_fail(cudaErrorInvalidValue);
@@ -476,6 +489,16 @@ mt_status run_prefill_dq(const GemvProblem& p, void* ws, const Launch& l) {
   CUtensorMap wmap[2];
   for (int mat = 0; mat < 2; ++mat) {
     const void* W = (mat && NW == 2) ? p.W1 : p.W0;
+    if constexpr (BFW) {  // the A tile itself: 64 elements (128 B) a row, 128-byte swizzle
+      const cuuint64_t wdims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+      const cuuint64_t wstr[1] = {(cuuint64_t)K * 2};
+      const cuuint32_t wbox[2] = {(cuuint32_t)PF_KB, (cuuint32_t)SH::FT};
+      if (enc(&wmap[mat], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), wdims, wstr, wbox, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cuda_fail(cudaErrorInvalidValue);
+      continue;
+    }
     const cuuint64_t wdims[2] = {(cuuint64_t)(SH::CB == 64 ? K : K / 2), (cuuint64_t)N};
     const cuuint64_t wstr[1] = {wdims[0]};
     const cuuint32_t wbox[2] = {(cuuint32_t)SH::CB, (cuuint32_t)SH::FT};
@@ -502,7 +525,7 @@ mt_status run_prefill_dq(const GemvProblem& p, void* ws, const Launch& l) {
   a.W1 = static_cast<const uint8_t*>(p.W1);
   a.s0 = p.s0; a.b0 = p.b0; a.s1 = p.s1; a.b1 = p.b1;
   a.XgT = XgT;
-  a.einv = einv;
+  a.einv = BFW ? nullptr : einv;
   a.res = p.res;
   a.res_ld = p.res_ld;
   a.out = p.out;
@@ -521,12 +544,15 @@ mt_status run_prefill_dq(const GemvProblem& p, void* ws, const Launch& l) {
   a.tsc = tsc;
   a.tinv = tinv;
 
-  mt_status st = launch(prefill_x_kernel, dim3(Mp), dim3(256), 0, l, p.x, M, K, group, x16, XgT, einv);
-  if (st != MT_OK) return st;
-  const float qmax = SH::CB == 64 ? 255.f : 15.f;
-  st = launch(prefill_wscale_kernel, dim3((unsigned)((NW * (long)N + 7) / 8)), dim3(256), 0, l, p.s0, p.b0,
-              NW == 2 ? p.s1 : p.s0, NW == 2 ? p.b1 : p.b0, N, K / group, NW, qmax, tsc, tinv);
-  if (st != MT_OK) return st;
+  mt_status st = MT_OK;
+  if (!BFW) {  // bf16 weights take x as stored and have no row scales
+    st = launch(prefill_x_kernel, dim3(Mp), dim3(256), 0, l, p.x, M, K, group, x16, XgT, einv);
+    if (st != MT_OK) return st;
+    const float qmax = SH::CB == 64 ? 255.f : 15.f;
+    st = launch(prefill_wscale_kernel, dim3((unsigned)((NW * (long)N + 7) / 8)), dim3(256), 0, l, p.s0, p.b0,
+                NW == 2 ? p.s1 : p.s0, NW == 2 ? p.b1 : p.b0, N, K / group, NW, qmax, tsc, tinv);
+    if (st != MT_OK) return st;
+  }
   const size_t smem = SH::SMEM;
   auto kern = prefill_dq_kernel<FMT, KIND, NT>;
   static std::mutex mu;
@@ -548,7 +574,8 @@ mt_status run_prefill_dq(const GemvProblem& p, void* ws, const Launch& l) {
   const long total = (long)M * N;
   const unsigned fgrid = (unsigned)std::min<long>((total + 255) / 256, (long)di->sm_count * 16);
   return launch(prefill_finalize_kernel<KIND>, dim3(fgrid), dim3(256), 0, l, (const float*)part, ks, Mp,
-                (const float*)einv, (const float*)tinv, M, N, p.res, p.res_ld, p.out, p.out_f32 ? 1 : 0);
+                (const float*)(BFW ? nullptr : einv), (const float*)(BFW ? nullptr : tinv), M, N, p.res, p.res_ld,
+                p.out, p.out_f32 ? 1 : 0);
 }
 
 template <int FMT, int KIND>

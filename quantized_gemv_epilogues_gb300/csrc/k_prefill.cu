@@ -1,6 +1,7 @@
-// k_prefill.cu - the prefill GEMMs (k_prefill.cuh) for affine INT8/INT4
-// weights, the dispatch over weight formats and the C ABI of the prefill
-// calls.
+// k_prefill.cu - the prefill GEMMs for affine INT8/INT4 and dense bf16
+// weights (exact-operand kernel, k_prefill.cuh; single-accumulator kernel
+// for bf16 outputs, k_prefill_dq.cuh), the dispatch over weight formats and
+// output types, and the C ABI of the prefill calls.
 #include "k_prefill.cuh"
 #include "k_prefill_dq.cuh"
 

@@ -38,13 +38,12 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
   sm.xs = reinterpret_cast<uint4*>(smem + (size_t)g.K * 2);
   phase_tail_carve<FMT, KIND>(g, smem + (size_t)g.K * 2 + xs_bytes<FMT>(g.K), sm);
   __shared__ int task_ctr;
+  __shared__ float red[WARP_TASK_WARPS];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PhaseCta c = phase_cta<KIND>(g, blockIdx.x);
 
   if (tid == 0) task_ctr = 2 * WARP_TASK_WARPS;  // tasks 0..2W-1 are taken statically
-  if constexpr (AFF)
-    for (int p = tid; p < g.P; p += WT_THREADS) sm.pmax[p] = 0;
   __syncthreads();
   pdl_trigger();
 
@@ -61,14 +60,28 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
   }
 
   pdl_wait();  // x, the residual and the output buffer follow the preceding kernel
-  for (int base = warp * 32; base < g.K / 8; base += WT_THREADS) {
-    const int i = base + lane < g.K / 8 ? base + lane : -1;
+  // x into shared memory and (affine) its largest |x|, then one staging pass
+  // with the vector's fixed-point scale
+  const int nu = g.K / 8;
+  float m = 0.f;
+  for (int i = tid; i < nu; i += WT_THREADS) {
     // plain (coherent) loads: x was written by the preceding kernel
-    const uint4 v = i >= 0 ? *reinterpret_cast<const uint4*>(a.x + (size_t)i * 8) : make_uint4(0, 0, 0, 0);
-    x_unit<FMT>(g, sm, i, v);
+    const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)i * 8);
+    reinterpret_cast<uint4*>(sm.xraw)[i] = v;
+    if constexpr (AFF) m = fmaxf(m, unit_absmax(v));
   }
+  int ex = 0;
+  if constexpr (AFF) ex = fx_exponent(cta_max(m, red, tid));  // its barrier also publishes xraw
+  else __syncthreads();
+  const float xscale = exp2i(ex);
+  for (int base = warp * 32; base < nu; base += WT_THREADS) {
+    const int i = base + lane < nu ? base + lane : -1;
+    x_stage_unit<FMT>(g, sm, i, i >= 0 ? reinterpret_cast<const uint4*>(sm.xraw)[i] : make_uint4(0, 0, 0, 0),
+                      xscale, false);
+  }
+  x_set_scale<FMT>(g, sm, ex, tid, WT_THREADS);
   cp_async_wait_all();  // scales and biases
-  x_convert<FMT>(g, sm, tid);
+  __syncthreads();
 
   wt_run<FMT, KIND>(g, a.w, c, sm, bufA, bufB, tA, tB, &task_ctr, pol, lane);
   __syncthreads();

@@ -28,18 +28,19 @@
 //    memory with cp.async 16-byte copies issued by every thread.
 //  * The affine term is factored as
 //      sum_k (s q_k + b) x_k = sum_chunks s * (sum q_k x_k) + sum_groups b * X_g
-//    with X_g the sum of x over group g (fp32, from the bf16 values).  The
-//    chunk sums sum q_k x_k are EXACT integer arithmetic: x is held as a
-//    24-bit fixed-point integer X = round(x * 2^e) (2^e chosen per piece of
-//    the row from that piece's max|x| so that |X| <= 2^22; every element
-//    within 2^14 of its piece's maximum is exact, smaller ones are rounded to
-//    2^-22 of that maximum) and split into
-//    three byte planes, X = 65536 X2 + 256 X1 + X0 (X2 signed).  The packed
-//    codes are used as they are stored: one dp4a (four u8 x s8/u8 products
-//    added to an int32) per weight word and plane, so a 16-byte chunk of INT8
-//    codes costs 12 dp4a; the three plane sums are combined in fp32 and the
-//    scale 2^-e is divided out of the partial sums.  INT4 words are split into
-//    their low and high nibbles (two masks) against even/odd element planes.
+//    with X_g the sum of x over group g (fp32, from the bf16 values).  x is
+//    held as a 24-bit fixed-point integer X = round(x * 2^e), one 2^e for the
+//    whole vector chosen from its max|x| so that |X| <= 2^22: every element
+//    within 2^14 of the vector's maximum is exact, smaller ones are rounded to
+//    2^-22 of that maximum.  X is split into three byte planes, X = 65536 X2 +
+//    256 X1 + X0 (X2 signed), and the packed codes are used as they are
+//    stored: one dp4a (four u8 x s8/u8 products added to an int32) per weight
+//    word and plane, so a 16-byte chunk of INT8 codes costs 12 dp4a.  The
+//    three plane sums of a chunk are exact integers; they are combined with
+//    one rounding in fp32 (256 S1 + S0 and 65536 S2 are each exact, their sum
+//    rounds once when it exceeds 2^24), and the scale 2^-e is divided out of
+//    the partial sums.  INT4 words are split into their low and high nibbles
+//    (two masks) against even/odd element planes.
 //    This replaced an fp16 exponent-bias dequant + mixed-precision FMA chain
 //    that was instruction-bound at ~4.6 instructions per weight.  Dense bf16
 //    weights use mixed-precision bf16 FMAs (exact products, fp32
@@ -72,8 +73,6 @@ struct PhaseGeom {
   unsigned long long p_mul;  // ceil(2^32 / P): t / P == (t * p_mul) >> 32 for t < 2^32 / P
   int B;                     // bytes per piece (multiple of 16)
   int CPP;                   // 16-byte chunks per piece (<= 32 * WT_CL)
-  int upp;                   // 8-element x units per piece (K / 8 / P)
-  unsigned long long upp_mul;  // ceil(2^32 / upp): i / upp == (i * upp_mul) >> 32 for i < K / 8
   int GPP;                   // groups per piece (affine)
   int sb_stride;             // elements per staged scale or bias array (multiple of 8)
   int sb_vec;                // 1: scales/biases are staged in 16-byte copies (G % 8 == 0)
@@ -94,14 +93,13 @@ struct PhaseSmem {
   uint16_t* xraw;  // [K] bf16 activations
   uint4* xs;       // staging layout of x (see below), xs_bytes<FMT>(K) bytes
   float* gsum;     // [G] X_g (affine)
-  int* pmax;       // [P] max |x| of each piece, as float bits (affine)
-  float* xinv;     // [P] 1 / 2^e_p, undoing the piece's x scale (affine)
+  float* xinv;     // [P] 2^-e, undoing the x scale (the same for every piece; affine)
   uint16_t* sbr;   // 2*NW arrays of sb_stride bf16: 2m = scales, 2m+1 = biases of matrix m
   float* parts;    // [rows][P][NW] partial sums of the pieces
 };
 
 // Bytes of a phase's shared arrays other than xraw and xs, in the order gsum,
-// pmax, xinv, sbr, parts (each a multiple of 16 bytes).
+// xinv, sbr, parts (each a multiple of 16 bytes).
 template <int FMT, int KIND>
 __host__ __device__ inline size_t phase_tail_bytes(const PhaseGeom& g) {
   constexpr bool AFF = FmtTraits<FMT>::AFFINE;
@@ -109,24 +107,23 @@ __host__ __device__ inline size_t phase_tail_bytes(const PhaseGeom& g) {
   size_t n = 0;
   if (AFF) {
     n += (size_t)(g.G + 3) / 4 * 16;
-    n += (size_t)(2 * g.P + 3) / 4 * 16;
+    n += (size_t)(g.P + 3) / 4 * 16;
     n += (size_t)2 * NW * g.sb_stride * 2;
   }
   n += ((size_t)g.rows_alloc * g.P * NW * 4 + 15) / 16 * 16;
   return n;
 }
 
-// Points sm's gsum, pmax, xinv, sbr and parts into the tail at p (16-byte
-// aligned, phase_tail_bytes long).
+// Points sm's gsum, xinv, sbr and parts into the tail at p (16-byte aligned,
+// phase_tail_bytes long).
 template <int FMT, int KIND>
 __device__ __forceinline__ void phase_tail_carve(const PhaseGeom& g, unsigned char* p, PhaseSmem& sm) {
   constexpr bool AFF = FmtTraits<FMT>::AFFINE;
   constexpr int NW = KIND == 0 ? 2 : 1;
   sm.gsum = reinterpret_cast<float*>(p);
   if (AFF) p += (size_t)(g.G + 3) / 4 * 16;
-  sm.pmax = reinterpret_cast<int*>(p);
-  sm.xinv = reinterpret_cast<float*>(p) + g.P;
-  if (AFF) p += (size_t)(2 * g.P + 3) / 4 * 16;
+  sm.xinv = reinterpret_cast<float*>(p);
+  if (AFF) p += (size_t)(g.P + 3) / 4 * 16;
   sm.sbr = reinterpret_cast<uint16_t*>(p);
   if (AFF) p += (size_t)2 * NW * g.sb_stride * 2;
   sm.parts = reinterpret_cast<float*>(p);
@@ -150,7 +147,7 @@ __device__ __forceinline__ PhaseCta phase_cta(const PhaseGeom& g, int cta) {
 // Staging layout of x, read by chunk_dot (16-byte units; CPR chunks per row):
 // A8:   unit p*CPR + c holds byte plane p (0: bits 16..23 of X, signed;
 //       1: bits 8..15; 2: bits 0..7) of the 16 elements of chunk c, in
-//       element order.  (X: the 24-bit fixed-point x, see x_convert.)
+//       element order.  (X: the 24-bit fixed-point x, see x_stage_unit.)
 // A4:   unit (2p + h)*CPR + c holds byte plane p of the even (h = 0) or odd
 //       (h = 1) elements of chunk c's 32: byte b of word wi is element
 //       8wi + 2b + h, matching the low / high nibbles of weight word wi.
@@ -171,7 +168,9 @@ __device__ __forceinline__ void dp4a_uu(uint32_t& s, uint32_t a, uint32_t b) {
 }
 
 // The plane sums of one chunk, S = 65536 S2 + 256 S1 + S0 = sum q_k X_k, in
-// fp32.  S1, S0 <= 255 * 255 * 32, so 256 S1 + S0 < 2^31.
+// fp32.  The plane sums are exact; S1, S0 <= 255 * 255 * 32, so 256 S1 + S0 <
+// 2^31 is exact in int32.  Its conversion to fp32 rounds when it exceeds 2^24
+// and the final fma rounds once more, so S carries at most two fp32 roundings.
 __device__ __forceinline__ float combine_planes(int s2, uint32_t s1, uint32_t s0) {
   return fmaf((float)s2, 65536.f, (float)(int)(s1 * 256u + s0));
 }
@@ -311,46 +310,23 @@ __device__ __forceinline__ void stage_sb(const PhaseGeom& g, const PhaseW& w, co
   }
 }
 
-// Staging of x, in two passes over 8-element units (one uint4 of bf16).
+// Staging of x, in 8-element units (one uint4 of bf16).
 //
-// The piece of x unit i.
-__device__ __forceinline__ int unit_piece(const PhaseGeom& g, int i) {
-  return (int)(((unsigned long long)(unsigned)i * g.upp_mul) >> 32);
+// The largest |x| of a unit (exact).
+__device__ __forceinline__ float unit_absmax(const uint4 v) {
+  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16lo(vw[j])), fabsf(bf16hi(vw[j]))));
+  return m;
 }
 
-// Pass 1, x_unit: unit i of x (0 <= i < K/8) is stored in sm.xraw and
-// (affine) its |x| folded into its piece's maximum sm.pmax (a shared-memory
-// max on the float bits, which order like the non-negative floats) and its
-// sum added into the group sum X_g (fp32).  sm.pmax must start at zero.
-// Every lane of a warp calls it together for units base + lane (base a
-// multiple of 32; i = -1 for a lane without a unit), so the group/8 units of a
-// group sit in consecutive lanes and are summed with a fixed shuffle tree.
-template <int FMT>
-__device__ __forceinline__ void x_unit(const PhaseGeom& g, const PhaseSmem& sm, int i, const uint4 v) {
-  if (i >= 0) reinterpret_cast<uint4*>(sm.xraw)[i] = v;
-  if constexpr (FmtTraits<FMT>::AFFINE) {
-    float sum = 0.f, m = 0.f;
-    if (i >= 0) {
-      const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float lo = bf16lo(vw[j]), hi = bf16hi(vw[j]);
-        sum += lo + hi;
-        m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
-      }
-    }
-    if (g.upp % 32 == 0) {  // the warp's 32 units lie in one piece
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      const int i0 = __shfl_sync(0xffffffffu, i, 0);
-      if ((threadIdx.x & 31) == 0 && i0 >= 0) atomicMax(sm.pmax + unit_piece(g, i0), __float_as_int(m));
-    } else if (i >= 0) {
-      atomicMax(sm.pmax + unit_piece(g, i), __float_as_int(m));
-    }
-    const int upg = g.group >> 3;  // units per group: 4, 8 or 16
-    for (int off = 1; off < upg; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if (i >= 0 && (i & (upg - 1)) == 0) sm.gsum[i / upg] = sum;
-  }
+// The exponent e with m * 2^e in [2^21, 2^22) for the largest |x| m of the
+// vector (a zero or subnormal m takes the largest exponent, 126): then X =
+// round(x * 2^e) has |X| <= 2^22 for every element.
+__device__ __forceinline__ int fx_exponent(float m) {
+  const int mb = __float_as_int(m);
+  return (mb >> 23) >= 255 ? 0 : max(-126, min(126, 21 - ((mb >> 23) - 127)));
 }
 
 // Byte k of each of a, b, c, d, packed as one word (a in the low byte).
@@ -359,67 +335,80 @@ __device__ __forceinline__ uint32_t byte_plane(uint32_t a, uint32_t b, uint32_t 
   return __byte_perm(__byte_perm(a, b, sel), __byte_perm(c, d, sel), 0x5410);
 }
 
-// Pass 2, after every thread's pass-1 calls: per piece p, the power-of-two
-// scale 2^e_p with max|x| * 2^e_p in [2^21, 2^22) (affine; the fixed-point X =
-// round(x * 2^e_p) then has |X| <= 2^22) and the staging layout of every unit;
-// sm.xinv[p] = 2^-e_p, and sm.pmax is reset to zero for the next use.  Begins
-// and ends with a CTA barrier (the reset follows the second).
+// Unit i of x (0 <= i < K/8): stored in sm.xraw (when store_raw), in the
+// staging layout sm.xs with the scale xscale = 2^e (affine), and its sum
+// added into the group sum X_g = sm.gsum[g] (fp32).  Every lane of a warp
+// calls it together for units base + lane (base a multiple of 32; i = -1 for
+// a lane without a unit), so the group/8 units of a quantisation group sit in
+// consecutive lanes and are summed with a fixed shuffle tree.  The caller ends
+// the staging with a CTA barrier before sm.xs is read.
 template <int FMT>
-__device__ __forceinline__ void x_convert(const PhaseGeom& g, const PhaseSmem& sm, int tid) {
-  using T = FmtTraits<FMT>;
-  const int CPR = g.CPR, NU = g.K / 8;
-  __syncthreads();
-  if constexpr (!T::AFFINE) {
+__device__ __forceinline__ void x_stage_unit(const PhaseGeom& g, const PhaseSmem& sm, int i, const uint4 v,
+                                             float xscale, bool store_raw) {
+  if (store_raw && i >= 0) reinterpret_cast<uint4*>(sm.xraw)[i] = v;
+  const int CPR = g.CPR;
+  if constexpr (!FmtTraits<FMT>::AFFINE) {
     // bf16: a unit is a chunk; its words 2u, 2u+1 go to 8-byte unit u*CPR + c
-    for (int i = tid; i < NU; i += WT_THREADS) {
-      const uint4 v = reinterpret_cast<const uint4*>(sm.xraw)[i];
+    if (i >= 0) {
       reinterpret_cast<uint2*>(sm.xs)[i] = make_uint2(v.x, v.y);
       reinterpret_cast<uint2*>(sm.xs)[CPR + i] = make_uint2(v.z, v.w);
     }
-    __syncthreads();
   } else {
-    // per piece: the exponent from the maximum's bits (a subnormal or zero
-    // maximum gives the largest exponent, 126), then pmax[p] holds the scale
-    for (int p = tid; p < g.P; p += WT_THREADS) {
-      const int mb = sm.pmax[p];
-      const int ex = (mb >> 23) >= 255 ? 0 : max(-126, min(126, 21 - ((mb >> 23) - 127)));
-      sm.xinv[p] = exp2i(-ex);
-      sm.pmax[p] = __float_as_int(exp2i(ex));
+    const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+    float sum = 0.f;
+    uint32_t X[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = bf16lo(vw[j]), hi = bf16hi(vw[j]);
+      sum += lo + hi;
+      // |x * xscale| < 2^22 by the choice of the scale
+      X[2 * j] = (uint32_t)round_small_to_int(lo * xscale);
+      X[2 * j + 1] = (uint32_t)round_small_to_int(hi * xscale);
     }
-    __syncthreads();
-    for (int i = tid; i < NU; i += WT_THREADS) {
-      const float xscale = __int_as_float(sm.pmax[unit_piece(g, i)]);
-      const uint4 v = reinterpret_cast<const uint4*>(sm.xraw)[i];
-      const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-      uint32_t X[8];
+    const int upg = g.group >> 3;  // units per group: 4, 8 or 16
+    for (int off = 1; off < upg; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (i < 0) return;
+    if ((i & (upg - 1)) == 0) sm.gsum[i >> (g.lg_group - 3)] = sum;
+    if constexpr (FMT == FMT_A8) {
+      // unit i = words 2(i&1), 2(i&1)+1 of chunk i>>1; plane p byte 2-p of X
+      uint2* xs2 = reinterpret_cast<uint2*>(sm.xs);
+      const int c = i >> 1, h = i & 1;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        // |x * xscale| < 2^22 by the choice of the piece's scale
-        X[2 * j] = (uint32_t)round_small_to_int(bf16lo(vw[j]) * xscale);
-        X[2 * j + 1] = (uint32_t)round_small_to_int(bf16hi(vw[j]) * xscale);
-      }
-      if constexpr (FMT == FMT_A8) {
-        // unit i = words 2(i&1), 2(i&1)+1 of chunk i>>1; plane p byte 2-p of X
-        uint2* xs2 = reinterpret_cast<uint2*>(sm.xs);
-        const int c = i >> 1, h = i & 1;
+      for (int p = 0; p < 3; ++p)
+        xs2[(size_t)(p * CPR + c) * 2 + h] =
+            make_uint2(byte_plane(X[0], X[1], X[2], X[3], 2 - p), byte_plane(X[4], X[5], X[6], X[7], 2 - p));
+    } else {
+      // unit i = word i&3 of chunk i>>2: even elements -> half 0, odd -> half 1
+      uint32_t* xs4 = reinterpret_cast<uint32_t*>(sm.xs);
+      const int c = i >> 2, wi = i & 3;
 #pragma unroll
-        for (int p = 0; p < 3; ++p)
-          xs2[(size_t)(p * CPR + c) * 2 + h] =
-              make_uint2(byte_plane(X[0], X[1], X[2], X[3], 2 - p), byte_plane(X[4], X[5], X[6], X[7], 2 - p));
-      } else {
-        // unit i = word i&3 of chunk i>>2: even elements -> half 0, odd -> half 1
-        uint32_t* xs4 = reinterpret_cast<uint32_t*>(sm.xs);
-        const int c = i >> 2, wi = i & 3;
-#pragma unroll
-        for (int p = 0; p < 3; ++p) {
-          xs4[(size_t)((2 * p) * CPR + c) * 4 + wi] = byte_plane(X[0], X[2], X[4], X[6], 2 - p);
-          xs4[(size_t)((2 * p + 1) * CPR + c) * 4 + wi] = byte_plane(X[1], X[3], X[5], X[7], 2 - p);
-        }
+      for (int p = 0; p < 3; ++p) {
+        xs4[(size_t)((2 * p) * CPR + c) * 4 + wi] = byte_plane(X[0], X[2], X[4], X[6], 2 - p);
+        xs4[(size_t)((2 * p + 1) * CPR + c) * 4 + wi] = byte_plane(X[1], X[3], X[5], X[7], 2 - p);
       }
     }
-    __syncthreads();
-    for (int p = tid; p < g.P; p += WT_THREADS) sm.pmax[p] = 0;
   }
+}
+
+// Records the scale 2^-e for every piece (affine; threads t < P of nt).
+template <int FMT>
+__device__ __forceinline__ void x_set_scale(const PhaseGeom& g, const PhaseSmem& sm, int ex, int t, int nt) {
+  if constexpr (FmtTraits<FMT>::AFFINE)
+    for (int p = t; p < g.P; p += nt) sm.xinv[p] = exp2i(-ex);
+}
+
+// The largest value over the CTA of one float per thread; every thread gets
+// it.  red: WARP_TASK_WARPS floats of shared memory, free on entry and not
+// reused before the next CTA barrier.
+__device__ __forceinline__ float cta_max(float v, float* red, int tid) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  if ((tid & 31) == 0) red[tid >> 5] = v;
+  __syncthreads();
+  float m = red[0];
+#pragma unroll
+  for (int w = 1; w < WARP_TASK_WARPS; ++w) m = fmaxf(m, red[w]);
+  return m;
 }
 
 // Computes task t from the weights in buf and stores its partial sums (one
@@ -558,8 +547,6 @@ bool plan_phase(int K, int N, int group, int grid, PhaseGeom* out, size_t* smem_
   g.p_mul = ((1ull << 32) + (unsigned long long)P - 1) / (unsigned long long)P;
   g.B = g.row_bytes / P;
   g.CPP = g.CPR / P;
-  g.upp = K / 8 / P;
-  g.upp_mul = ((1ull << 32) + (unsigned long long)g.upp - 1) / (unsigned long long)g.upp;
   g.GPP = AFF ? g.G / P : 0;
   g.row_unit = row_unit;
   g.rows_base = N / row_unit / grid;

@@ -35,9 +35,12 @@
 // error word and raises the abort flag that every other wait also watches,
 // and every CTA returns.
 //
-// Between hand-offs a CTA asks L2 for the first rows of its next phase's
-// weights with bulk (TMA) prefetches and stages that phase's scales, biases
-// and RMSNorm gain, so HBM keeps streaming while the hand-off completes.
+// As soon as its task loop ends, a CTA asks L2 for the first rows of its
+// next phase's weights with bulk (TMA) prefetches, and it stages that phase's
+// scales, biases and RMSNorm gain during the current loop, so HBM keeps
+// streaming while the hand-off completes.  x and h are staged in one pass with
+// one fixed-point scale per vector: the gate/up CTAs publish the largest |h|
+// of their rows next to h, and x's largest |x| is a CTA reduction.
 #include <math.h>
 
 #include <mutex>
@@ -86,6 +89,7 @@ struct StackArgs {
   uint16_t* hbuf;  // [f]    h of the current layer
   uint16_t* sbuf;  // [d]    summed of the next layer
   float* ssq;      // [grid] per-CTA partial sums of squares of sbuf
+  float* hmax;     // [grid] per-CTA largest |h| of its gate/up rows
   int* err;
   int pre_g, pre_d;   // bytes per weight stream asked of L2 ahead of a phase
   unsigned bar_extra; // arrivals a barrier waits for beyond the grid (0; > 0 only in tests)
@@ -157,6 +161,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int task_ctr;
   __shared__ float red[WARP_TASK_WARPS];
+  __shared__ float vec_max;  // the staged vector's largest |value|, or its sum of squares
   __shared__ __align__(16) StackLayerDev lay_s[2];  // layers l and l + 1
   static_assert(sizeof(StackLayerDev) % 16 == 0, "layer table entries are copied in 16-byte units");
   constexpr int LAY_UNITS = (int)(sizeof(StackLayerDev) / 16);
@@ -194,15 +199,14 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
     const uint32_t n = (uint32_t)(all < (size_t)pre ? all : (size_t)pre);
     if (n) bulk_prefetch_l2(W + (size_t)c.r_begin * g.row_bytes, n);
   };
-  // What a phase needs that does not depend on the hand-off before it is
-  // requested early, so that only the hand-off's own traffic is in flight
-  // while a CTA waits: its scales and biases and (gate/up) the RMSNorm gain
-  // go to shared memory at the start of the PREVIOUS phase's task loop
-  // (stage_*_smem; the copies are small next to the weight stream), and its
-  // first rows' weights go to L2 with bulk prefetches as soon as the
-  // hand-off's barrier has passed (prefetch_*; issued between the arrival
-  // and the barrier, their traffic slowed the barrier itself).  lay_s[l & 1]
-  // must be complete and visible.  The caller commits the copies.
+  // What a phase needs that does not depend on the hand-off is requested
+  // early: its scales and biases and (gate/up) the RMSNorm gain go to shared
+  // memory at the start of the PREVIOUS phase's task loop (stage_*_smem; the
+  // copies are small next to the weight stream), and its first rows' weights
+  // go to L2 with bulk prefetches as soon as the previous task loop ends
+  // (prefetch_*; issued after the arrival or after the barrier, the hand-off
+  // left HBM idle for longer).  lay_s[l & 1] must be complete and visible.
+  // The caller commits the copies.
   auto stage_gateup_smem = [&](int l) {
     const StackLayerDev& Ly = lay_s[l & 1];
     if constexpr (AFF) stage_sb<0>(a.gu, gateup_w(Ly), cg, smG.sbr, tid, WT_THREADS);
@@ -252,10 +256,6 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
   const int npair_d = cd.rows >> 1, npair_g = cg.rows >> 1;
 
   // ---- prologue: layer 0's table entry and staging, summed_0
-  if constexpr (AFF) {
-    for (int p = tid; p < a.gu.P; p += WT_THREADS) smG.pmax[p] = 0;
-    for (int p = tid; p < a.dn.P; p += WT_THREADS) smD.pmax[p] = 0;
-  }
   fetch_layer(0);
   cp_async_commit();
   cp_async_wait_all();
@@ -288,54 +288,56 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
     // ---- add + RMSNorm of the whole vector (every CTA)
     {
       const int nu = d / 8;  // x units of 8 elements
-      // the per-CTA partial sums of squares (every warp reads all of them,
-      // in one fixed order) and this thread's first two units of summed_l
-      float q[STACK_MAX_GRID / 32];
+      // the per-CTA partial sums of squares (warp 0 reads them, in one fixed
+      // order; read by every warp they piled up on a few L2 lines) and this
+      // thread's first two units of summed_l
+      float tot = 0.f;
+      if (warp == 0) {
+        float q[STACK_MAX_GRID / 32];
 #pragma unroll
-      for (int k = 0; k < STACK_MAX_GRID / 32; ++k) {
-        const int i = lane + 32 * k;
-        q[k] = i < (int)gridDim.x ? ldg_cg_f32(a.ssq + i) : 0.f;
+        for (int k = 0; k < STACK_MAX_GRID / 32; ++k) {
+          const int i = lane + 32 * k;
+          q[k] = i < (int)gridDim.x ? ldg_cg_f32(a.ssq + i) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < STACK_MAX_GRID / 32; ++k) tot += q[k];
       }
       uint4 u0 = make_uint4(0, 0, 0, 0), u1 = u0;
       if (tid < nu) u0 = ldg_cg(a.sbuf + (size_t)tid * 8);
       if (tid + WT_THREADS < nu) u1 = ldg_cg(a.sbuf + (size_t)(tid + WT_THREADS) * 8);
-      float tot = 0.f;
+      if (warp == 0) {
 #pragma unroll
-      for (int k = 0; k < STACK_MAX_GRID / 32; ++k) tot += q[k];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-      const float inv = rsqrtf(tot / (float)d + a.eps);
-      cp_async_wait_all();
-      __syncthreads();  // the RMSNorm gain, the scales and the next table entry
-      // x = bf16(summed * inv * w), unit by unit, into the first staging pass
-      auto norm_unit = [&](int base, const uint4 sv) {
-        const int i = base + lane < nu ? base + lane : -1;
-        uint4 o = make_uint4(0, 0, 0, 0);
-        if (i >= 0) {
-          const uint4 w = reinterpret_cast<const uint4*>(wn)[i];
-          const uint32_t* sp = &sv.x;
-          const uint32_t* wp = &w.x;
-          uint32_t* op = &o.x;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float lo = bf16lo(sp[j]) * inv * bf16lo(wp[j]);
-            const float hi = bf16hi(sp[j]) * inv * bf16hi(wp[j]);
-            op[j] = pack2(f2bf(lo), f2bf(hi));
-          }
-          reinterpret_cast<uint4*>(ssm)[i] = sv;
-        }
-        x_unit<FMT>(a.gu, smG, i, o);
-      };
-      if (warp * 32 < nu) norm_unit(warp * 32, u0);
-      if (warp * 32 + WT_THREADS < nu) norm_unit(warp * 32 + WT_THREADS, u1);
-      for (int base = warp * 32 + 2 * WT_THREADS; base < nu; base += WT_THREADS) {  // d > 8192
-        const int i = base + lane;
-        norm_unit(base, i < nu ? ldg_cg(a.sbuf + (size_t)i * 8) : make_uint4(0, 0, 0, 0));
+        for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+        if (lane == 0) vec_max = tot;
       }
+      cp_async_wait_all();
+      __syncthreads();  // the sum of squares, the RMSNorm gain, the scales and the next table entry
+      const float inv = rsqrtf(vec_max / (float)d + a.eps);
+      // x = bf16(summed * inv * w) into xraw, unit by unit, and its largest |x|
+      float m = 0.f;
+      auto norm_unit = [&](int i, const uint4 sv) {
+        const uint4 w = reinterpret_cast<const uint4*>(wn)[i];
+        const uint32_t* sp = &sv.x;
+        const uint32_t* wp = &w.x;
+        uint4 o;
+        uint32_t* op = &o.x;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = bf16lo(sp[j]) * inv * bf16lo(wp[j]);
+          const float hi = bf16hi(sp[j]) * inv * bf16hi(wp[j]);
+          op[j] = pack2(f2bf(lo), f2bf(hi));
+        }
+        reinterpret_cast<uint4*>(ssm)[i] = sv;
+        reinterpret_cast<uint4*>(smG.xraw)[i] = o;
+        m = fmaxf(m, unit_absmax(o));
+      };
+      if (tid < nu) norm_unit(tid, u0);
+      if (tid + WT_THREADS < nu) norm_unit(tid + WT_THREADS, u1);
+      for (int i = tid + 2 * WT_THREADS; i < nu; i += WT_THREADS)  // d > 8192
+        norm_unit(i, ldg_cg(a.sbuf + (size_t)i * 8));
       if (tid == 0) task_ctr = 2 * WARP_TASK_WARPS;  // tasks 0..2W-1 are taken statically
       // the first two gate/up tasks (mostly L2 hits after prefetch_gateup),
-      // in flight while x is converted (shared memory only; requested before
-      // the hand-off instead, they slowed the barrier itself)
+      // in flight while x is staged (shared memory only)
       {
         const PhaseW w = gateup_w(Ly);
         wt_load<0>(a.gu, w, cg, tA, bufA, pol, lane);
@@ -343,7 +345,18 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
         wt_prefetch<0>(a.gu, w, cg, tA + 2 * WARP_TASK_WARPS, lane);
         wt_prefetch<0>(a.gu, w, cg, tB + 2 * WARP_TASK_WARPS, lane);
       }
-      x_convert<FMT>(a.gu, smG, tid);
+      // one staging pass with the vector's fixed-point scale
+      int ex = 0;
+      if constexpr (AFF) ex = fx_exponent(cta_max(m, red, tid));  // its barrier also publishes xraw
+      else __syncthreads();
+      const float xscale = exp2i(ex);
+      for (int base = warp * 32; base < nu; base += WT_THREADS) {
+        const int i = base + lane < nu ? base + lane : -1;
+        x_stage_unit<FMT>(a.gu, smG, i, i >= 0 ? reinterpret_cast<const uint4*>(smG.xraw)[i] : make_uint4(0, 0, 0, 0),
+                          xscale, false);
+      }
+      x_set_scale<FMT>(a.gu, smG, ex, tid, WT_THREADS);
+      __syncthreads();
       stage_down_smem(l);  // for the next phase, during this one's loop
       cp_async_commit();
       if (a.tr_sum || a.tr_norm)
@@ -357,6 +370,8 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
     {
       wt_run<FMT, 0>(a.gu, gateup_w(Ly), cg, smG, bufA, bufB, tA, tB, &task_ctr, pol, lane);
       __syncthreads();
+      prefetch_down(l);  // HBM keeps streaming through the hand-off
+      float hm = 0.f;
       for (int j = tid; j < npair_g; j += WT_THREADS) {
         uint16_t hb[2];
 #pragma unroll
@@ -364,50 +379,71 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
           const float g = row_total<2>(a.gu, smG.parts, 2 * j + e, 0);
           const float u = row_total<2>(a.gu, smG.parts, 2 * j + e, 1);
           hb[e] = f2bf(g / (1.0f + expf(-g)) * u);
+          hm = fmaxf(hm, fabsf(bf16f(hb[e])));
         }
         *reinterpret_cast<uint32_t*>(a.hbuf + cg.r_begin + 2 * j) = pack2(hb[0], hb[1]);
         if (a.tr_h) *reinterpret_cast<uint32_t*>(a.tr_h + (size_t)l * f + cg.r_begin + 2 * j) = pack2(hb[0], hb[1]);
       }
-      __syncthreads();
-      if (tid == 0) grid_arrive(a.ctl);  // h is published
+      hm = cta_max(hm, red, tid);  // its barrier also orders the h stores before the release
+      if (tid == 0) {
+        a.hmax[cta] = hm;
+        grid_arrive(a.ctl);  // h and its largest |h| are published
+      }
     }
     // ---- down
     {
       if (tid == 0) task_ctr = 2 * WARP_TASK_WARPS;
       if (!grid_wait()) { cp_async_wait_all(); return; }
-      prefetch_down(l);  // after the barrier: its traffic would slow the barrier
-      // h (every unit of a batch read before it is used) and the first
-      // staging pass over it
+      // h (every unit of a batch read before it is used) and the largest |h|
+      // (warp 0 reads the per-CTA maxima); one staging pass per batch with
+      // the vector's fixed-point scale
       const PhaseW w = down_w(Ly);
       const int nu = f / 8;
       constexpr int HB = 4;  // units per thread and batch: f <= 16384 in one batch
-      for (int base0 = warp * 32; base0 < nu; base0 += HB * WT_THREADS) {
+      float hm = 0.f;
+      if (warp == 0)
+        for (int i = lane; i < (int)gridDim.x; i += 32) hm = fmaxf(hm, ldg_cg_f32(a.hmax + i));
+      int ex = 0;
+      for (int base0 = warp * 32, batch = 0;; base0 += HB * WT_THREADS, ++batch) {
         uint4 hv[HB];
 #pragma unroll
         for (int k = 0; k < HB; ++k) {
           const int i = base0 + k * WT_THREADS + lane;
           hv[k] = i < nu ? ldg_cg(a.hbuf + (size_t)i * 8) : make_uint4(0, 0, 0, 0);
         }
+        if (batch == 0) {
+          if (warp == 0) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, off));
+            if (lane == 0) vec_max = hm;
+          }
+          __syncthreads();
+          if constexpr (AFF) ex = fx_exponent(vec_max);
+        }
+        const float xscale = exp2i(ex);
 #pragma unroll
         for (int k = 0; k < HB; ++k) {
           const int base = base0 + k * WT_THREADS;
-          if (base < nu) x_unit<FMT>(a.dn, smD, base + lane < nu ? base + lane : -1, hv[k]);
+          if (base < nu) x_stage_unit<FMT>(a.dn, smD, base + lane < nu ? base + lane : -1, hv[k], xscale, true);
         }
+        if (base0 + HB * WT_THREADS >= nu) break;
       }
+      x_set_scale<FMT>(a.dn, smD, ex, tid, WT_THREADS);
       cp_async_wait_all();  // scales and biases (long complete)
-      // the first two tasks (mostly L2 hits after prefetch_down), in flight
-      // while h is converted (shared memory only)
+      // the first two tasks (mostly L2 hits after prefetch_down), then the
+      // staged h is published to the CTA
       wt_load<1>(a.dn, w, cd, tA, bufA, pol, lane);
       wt_load<1>(a.dn, w, cd, tB, bufB, pol, lane);
       wt_prefetch<1>(a.dn, w, cd, tA + 2 * WARP_TASK_WARPS, lane);
       wt_prefetch<1>(a.dn, w, cd, tB + 2 * WARP_TASK_WARPS, lane);
-      x_convert<FMT>(a.dn, smD, tid);
+      __syncthreads();
       if (l + 1 < a.L) {  // the next gate/up phase's, during this loop
         stage_gateup_smem(l + 1);
         cp_async_commit();
       }
       wt_run<FMT, 1>(a.dn, w, cd, smD, bufA, bufB, tA, tB, &task_ctr, pol, lane);
       __syncthreads();
+      if (l + 1 < a.L) prefetch_gateup(l + 1);  // HBM keeps streaming through the hand-off
       // epilogue: y = h . Wd[n] + summed_l[n]; summed_{l+1} = values_{l+1} + y
       const bool last = l + 1 == a.L;
       const bool have = tid < npair_d;
@@ -426,7 +462,6 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       if (last) break;
       publish_summed(vnx, y2, have);
       if (!grid_wait()) { cp_async_wait_all(); return; }
-      prefetch_gateup(l + 1);
     }
   }
 }
@@ -526,11 +561,12 @@ extern "C" mt_status mt_mlp_plan_create(const mt_mlp_layer* layers, int L, int d
   if (ce != cudaSuccess) return cuda_fail(ce);
   if (occ < 1) return MT_ERR_SHAPE;
 
-  // device memory: [layer table | control line | ssq | sbuf | hbuf]; the
-  // control line is zeroed before each run
+  // device memory: [layer table | control line | ssq | hmax | sbuf | hbuf];
+  // the control line is zeroed before each run
   const size_t tab = ((size_t)L * sizeof(StackLayerDev) + 127) / 128 * 128;
   const size_t o_ctl = tab, o_ssq = o_ctl + 128;
-  const size_t o_sbuf = o_ssq + ((size_t)P.grid * 4 + 127) / 128 * 128;
+  const size_t o_hmax = o_ssq + ((size_t)P.grid * 4 + 127) / 128 * 128;
+  const size_t o_sbuf = o_hmax + ((size_t)P.grid * 4 + 127) / 128 * 128;
   const size_t o_hbuf = o_sbuf + ((size_t)d * 2 + 127) / 128 * 128;
   const size_t total = o_hbuf + ((size_t)f * 2 + 127) / 128 * 128;
   StackLayerDev* host_tab = new (std::nothrow) StackLayerDev[L];
@@ -564,6 +600,7 @@ extern "C" mt_status mt_mlp_plan_create(const mt_mlp_layer* layers, int L, int d
   a.layers = reinterpret_cast<const StackLayerDev*>(base);
   a.ctl = reinterpret_cast<StackCtl*>(base + o_ctl);
   a.ssq = reinterpret_cast<float*>(base + o_ssq);
+  a.hmax = reinterpret_cast<float*>(base + o_hmax);
   a.sbuf = reinterpret_cast<uint16_t*>(base + o_sbuf);
   a.hbuf = reinterpret_cast<uint16_t*>(base + o_hbuf);
   P.run_state = base + o_ctl;
@@ -748,10 +785,11 @@ extern "C" mt_status mt_mlp_stack_run_noalloc(const mt_mlp_layer* layers, int L,
   if (!ok) return MT_ERR_SHAPE;
   const size_t budget = (size_t)di->max_smem_optin - 1024;  // static smem and slack
   if (P.smem > budget) return MT_ERR_SHAPE;
-  // scratch layout: [layer table | control line | ssq | sbuf | hbuf]
+  // scratch layout: [layer table | control line | ssq | hmax | sbuf | hbuf]
   const size_t o_ctl = round128((size_t)L * sizeof(StackLayerDev));
   const size_t o_ssq = o_ctl + 128;
-  const size_t o_sbuf = o_ssq + round128((size_t)P.grid * 4);
+  const size_t o_hmax = o_ssq + round128((size_t)P.grid * 4);
+  const size_t o_sbuf = o_hmax + round128((size_t)P.grid * 4);
   const size_t o_hbuf = o_sbuf + round128((size_t)d * 2);
   const size_t total = o_hbuf + round128((size_t)f * 2);
   if (total > (size_t)MT_STACK_SCRATCH_BYTES) return MT_ERR_SHAPE;
@@ -800,6 +838,7 @@ extern "C" mt_status mt_mlp_stack_run_noalloc(const mt_mlp_layer* layers, int L,
   a.layers = reinterpret_cast<const StackLayerDev*>(base);
   a.ctl = reinterpret_cast<StackCtl*>(base + o_ctl);
   a.ssq = reinterpret_cast<float*>(base + o_ssq);
+  a.hmax = reinterpret_cast<float*>(base + o_hmax);
   a.sbuf = reinterpret_cast<uint16_t*>(base + o_sbuf);
   a.hbuf = reinterpret_cast<uint16_t*>(base + o_hbuf);
   a.L = L; a.d = d; a.f = f; a.eps = eps;

@@ -96,8 +96,7 @@ typedef enum mt_status {
   MT_ERR_FORMAT = 5,  /* unknown weight format, dtype, bit width or option */
   MT_ERR_ALIAS = 6,   /* an output overlaps an input it may not overlap */
   MT_ERR_CUDA = 7,    /* a CUDA runtime call failed (see mt_last_cuda_error) */
-  MT_ERR_TIMEOUT = 8, /* a bounded device-side wait expired (mt_device_error) */
-  MT_ERR_RANGE = 9    /* a value left the executor's fixed-point range (mt_device_error) */
+  MT_ERR_TIMEOUT = 8  /* a bounded device-side wait expired (mt_device_error) */
 } mt_status;
 
 /* Output element type of a call.  Inputs are always bf16. */

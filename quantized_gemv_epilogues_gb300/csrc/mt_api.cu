@@ -365,7 +365,6 @@ const char* mt_status_string(mt_status s) {
     case MT_ERR_ALIAS: return "MT_ERR_ALIAS: output overlaps an input";
     case MT_ERR_CUDA: return "MT_ERR_CUDA: a CUDA runtime call failed";
     case MT_ERR_TIMEOUT: return "MT_ERR_TIMEOUT: a bounded device wait expired";
-    case MT_ERR_RANGE: return "MT_ERR_RANGE: a value left the executor's fixed-point range";
     default: return "unknown mt_status";
   }
 }

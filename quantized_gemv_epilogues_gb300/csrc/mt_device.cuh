@@ -40,17 +40,6 @@ __device__ __forceinline__ uint4 ldg_stream_pol(const void* p, uint64_t pol) {
   return v;
 }
 
-// 128-bit read-only load with an explicit L2 eviction policy that also
-// allocates in L1: for rows read as runs of 16-byte chunks by one lane, so the
-// second half of each 32-byte sector is served from L1.
-__device__ __forceinline__ uint4 ldg_nc_pol(const void* p, uint64_t pol) {
-  uint4 v;
-  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p), "l"(pol));
-  return v;
-}
-
 __device__ __forceinline__ uint4 ldg_nc(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -88,10 +77,6 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
 }
 __device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Integer atomic add at GPU scope without a return value.
-__device__ __forceinline__ void red_add_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
   int v;

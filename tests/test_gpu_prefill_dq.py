@@ -45,15 +45,11 @@ def _ws(mt, M, K, N, group):
     return torch.empty(mt.mt_prefill_workspace_bytes(M, K, N, group), dtype=torch.uint8, device="cuda")
 
 
-def _weight_from_device(q, s, b, fmt, group):
-    """The oracle's Weight of exactly the packed codes, scales and biases."""
-    bits = FMT_BITS[fmt]
-    N = s.shape[0]
-    codes = q.cpu().numpy()
-    if bits == 4:  # two codes a byte, low nibble first
-        codes = np.stack([codes & 15, codes >> 4], axis=-1).reshape(N, -1)
-    sb = host_bits(s), host_bits(b)
-    return oracle.Weight(oracle.FMT_CODES, codes.astype(np.uint8), sb[0], sb[1], group)
+def _oracle_weight(W32, fmt, group):
+    """The oracle's own quantisation of the same fp32 weights (the library's
+    packer is checked bit for bit against it elsewhere; nothing here is
+    read back from the device)."""
+    return oracle.Weight.from_f32(W32, FMT_BITS[fmt], group)
 
 
 @pytest.mark.parametrize("fmt,group,M,K,N", [(1, 128, 70, 1024, 200), (1, 64, 257, 512, 384),
@@ -63,7 +59,7 @@ def test_dq_error_bound(mt, fmt, group, M, K, N):
     x = synth.host_bf16(M * K, seed, synth.ACT).reshape(M, K)
     W32 = synth.host_f32(N * K, seed + 1, synth.WEIGHT_OUTLIERS).reshape(N, K)
     q, s, b = _pack(mt, W32, fmt, group)
-    W = _weight_from_device(q, s, b, fmt, group)
+    W = _oracle_weight(W32, fmt, group)
     y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     mt.mt_prefill_linear_bias(dev_bf16(x), q, s, b, group, None, y, _ws(mt, M, K, N, group), fmt=fmt)
     torch.cuda.synchronize()
@@ -83,7 +79,7 @@ def test_dq_rows_of_any_magnitude(mt, fmt):
     W32 = synth.host_f32(N * K, seed + 1, synth.WEIGHT).reshape(N, K)
     W32 = (W32 * np.exp2(np.linspace(-40, 40, N)).astype(np.float32)[:, None]).astype(np.float32)
     q, s, b = _pack(mt, W32, fmt, group)
-    W = _weight_from_device(q, s, b, fmt, group)
+    W = _oracle_weight(W32, fmt, group)
     res = np.zeros((M, N), dtype=np.uint16)  # zero addend: every row's own magnitude stays visible
     y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     mt.mt_prefill_down_residual(dev_bf16(x), q, s, b, group, dev_bf16(res), y, _ws(mt, M, K, N, group), fmt=fmt)
@@ -108,6 +104,6 @@ def test_dq_zero_rows(mt):
     torch.cuda.synchronize()
     got = host_bits(y)
     assert np.array_equal(got[:, ::3], res[:, ::3]), "a zero weight row must pass the residual through"
-    ref = oracle.down_residual(x, _weight_from_device(q, s, b, fmt, group), res)
+    ref = oracle.down_residual(x, _oracle_weight(W32, fmt, group), res)
     err = np.maximum(0.0, np.abs(oracle.f64_from_bf16(got) - ref) - 0.5 * ulp_bf16(ref)).max() / np.abs(ref).max()
     assert err <= TOL_BF16

@@ -641,3 +641,122 @@ def test_mlp_layer_and_stack_composition():
         assert np.array_equal(out[l]["y_x"], yx)
         r = oracle.bf16_from_f64(yx)
     assert not np.array_equal(out[0]["y"], out[1]["y"])
+
+
+# ------------------------------------------------- composition, closed forms
+# "Compute-Graph Fusion", Automatic Gated Epilogues: the down projection adds
+# the transformer residual (the layer's own summed row) in its epilogue, and
+# each tensor handed to the next call is bf16.  These cases fix the answer
+# without the oracle: dense bf16 weights with zeros or one non-zero entry
+# reduce every dot product to at most one exact product.
+
+def _dense(bits):
+    return oracle.Weight(oracle.FMT_BF16, np.ascontiguousarray(bits, dtype=np.uint16))
+
+
+def _torch_bf16_add(a_bits, b_bits):
+    """bf16(a + b) by torch (bf16 tensors on the CPU)."""
+    ta = torch.from_numpy(np.ascontiguousarray(a_bits, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+    tb = torch.from_numpy(np.ascontiguousarray(b_bits, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+    return (ta + tb).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_mlp_layer_zero_down_returns_summed():
+    """Wd = 0: y == out_sum bit for bit, and out_sum == torch's bf16(v + r),
+    so the residual of the down projection is the layer's own summed row
+    (not r, not the normalised row) and y is rounded once from it."""
+    d, f, M = 48, 80, 3
+    v = gen_bf16(M * d, 301).reshape(M, d)
+    r = gen_bf16(M * d, 302).reshape(M, d)
+    w = gen_bf16(d, 303, synth.NORM_W)
+    Wg = _dense(gen_bf16(f * d, 304, synth.WEIGHT).reshape(f, d))
+    Wu = _dense(gen_bf16(f * d, 305, synth.WEIGHT).reshape(f, d))
+    Wd = _dense(np.zeros((d, f), dtype=np.uint16))
+    out = oracle.mlp_layer(v, r, w, 1e-5, Wg, Wu, Wd)
+    assert np.array_equal(out["out_sum"], _torch_bf16_add(v, r))
+    assert np.array_equal(out["y"], out["out_sum"])
+    assert not np.array_equal(out["y"], r) and np.any(out["h"] != 0)
+
+
+@pytest.mark.parametrize("zero", ["gate", "up"])
+def test_mlp_layer_zero_gate_or_up_gives_zero_h(zero):
+    """Wg = 0 (silu(0) = 0) or Wu = 0: every h is zero and y == out_sum."""
+    d, f, M = 40, 56, 2
+    v = gen_bf16(M * d, 311).reshape(M, d)
+    r = gen_bf16(M * d, 312).reshape(M, d)
+    w = gen_bf16(d, 313, synth.NORM_W)
+    rnd = _dense(gen_bf16(f * d, 314, synth.WEIGHT).reshape(f, d))
+    zero_w = _dense(np.zeros((f, d), dtype=np.uint16))
+    Wg, Wu = (zero_w, rnd) if zero == "gate" else (rnd, zero_w)
+    Wd = _dense(gen_bf16(d * f, 315, synth.WEIGHT).reshape(d, f))
+    out = oracle.mlp_layer(v, r, w, 1e-5, Wg, Wu, Wd)
+    assert np.all(oracle.f64_from_bf16(out["h"]) == 0.0)
+    assert np.array_equal(out["y"], out["out_sum"])
+
+
+def test_mlp_stack_chains_y_into_the_next_residual():
+    """Two layers with Wg = Wd = 0: y_l = out_sum_l, so
+    y_1 = bf16(v_1 + bf16(v_0 + r_0)) (torch bf16 adds)."""
+    d, f, M = 32, 64, 2
+    v0 = gen_bf16(M * d, 321).reshape(M, d)
+    v1 = gen_bf16(M * d, 322).reshape(M, d)
+    r0 = gen_bf16(M * d, 323).reshape(M, d)
+    zg = _dense(np.zeros((f, d), dtype=np.uint16))
+    zd = _dense(np.zeros((d, f), dtype=np.uint16))
+    up = _dense(gen_bf16(f * d, 324, synth.WEIGHT).reshape(f, d))
+    layer = (gen_bf16(d, 325, synth.NORM_W), zg, up, zd)
+    out = oracle.mlp_stack([v0, v1], r0, [layer, layer], 1e-6)
+    y0 = _torch_bf16_add(v0, r0)
+    assert np.array_equal(out[0]["y"], y0)
+    assert np.array_equal(out[1]["y"], _torch_bf16_add(v1, y0))
+    assert not np.array_equal(out[1]["y"], _torch_bf16_add(v1, r0))
+
+
+def _one_hot_case(s0_bits, w0_bits, a_bits, b_bits, c_bits, d=8, f=4, n0=2, eps=1e-5):
+    """summed = (s0, 0, ..., 0); Wg[n][0] = a, Wu[n][0] = b for every n;
+    Wd[0][n0] = c, other weights 0.  Returns the oracle layer and the closed
+    form with Python floats: x0 = bf16(s0 w0 / sqrt(s0^2 / d + eps)),
+    h = bf16(silu(x0 a) * x0 b), y0 = bf16(h c + s0), and the variants that
+    skip the rounding of x0 or of h."""
+    f64 = lambda b: float(torch_f64_from_bf16(np.array([b], dtype=np.uint16))[0])
+    v = np.zeros((1, d), dtype=np.uint16)
+    v[0, 0] = s0_bits
+    r = np.zeros((1, d), dtype=np.uint16)  # summed = v + 0 = v exactly
+    w = np.full(d, 0x3F80, dtype=np.uint16)  # 1.0
+    w[0] = w0_bits
+    Wg = np.zeros((f, d), dtype=np.uint16)
+    Wu = np.zeros((f, d), dtype=np.uint16)
+    Wg[:, 0] = a_bits
+    Wu[:, 0] = b_bits
+    Wd = np.zeros((d, f), dtype=np.uint16)
+    Wd[0, n0] = c_bits
+    out = oracle.mlp_layer(v, r, w, eps, _dense(Wg), _dense(Wu), _dense(Wd))
+    s0, w0, a, b, c = (f64(t) for t in (s0_bits, w0_bits, a_bits, b_bits, c_bits))
+    bf = lambda x: int(oracle.bf16_from_f64(np.array([x]))[0])
+    nx = s0 * w0 / math.sqrt(s0 * s0 / d + eps)
+    silu = lambda g: g / (1.0 + math.exp(-g))
+    x0 = f64(bf(nx))
+    h = f64(bf(silu(x0 * a) * (x0 * b)))
+    y0 = bf(h * c + s0)
+    h_unrounded_x = f64(bf(silu(nx * a) * (nx * b)))
+    y_unrounded_h = bf(silu(x0 * a) * (x0 * b) * c + s0)
+    return out, bf(nx), h, y0, h_unrounded_x, y_unrounded_h
+
+
+def test_mlp_layer_one_hot_closed_form_rounds_each_handoff():
+    """One non-zero summed element and one-hot weights: out_norm, h and y
+    follow from a single bf16 element in closed form (math.sqrt and
+    math.exp in Python).  The case is chosen so that feeding the unrounded
+    normalised value into gate/up, or the unrounded h into down, gives a
+    different bf16 result: the oracle rounds both hand-offs."""
+    found = 0
+    for s0, w0, a, b, c in [(0x3FA0, 0x3F9A, 0x4040, 0x3FC8, 0x4120), (0x3F80, 0x3F8D, 0x40A3, 0x3FB1, 0x41F0),
+                            (0x4010, 0x3FB7, 0x3FD3, 0x4003, 0x4250), (0xBF90, 0x3FA9, 0x4071, 0x3F93, 0x4305)]:
+        out, x0_bits, h, y0, h_alt, y_alt = _one_hot_case(s0, w0, a, b, c)
+        assert out["out_norm"][0, 0] == x0_bits
+        assert np.all(oracle.f64_from_bf16(out["h"][0]) == h)
+        assert out["y"][0, 0] == y0
+        assert np.array_equal(out["y"][0, 1:], out["out_sum"][0, 1:])  # rows with no weights: the residual
+        if h_alt != h and y_alt != y0:
+            found += 1
+    assert found >= 1, "no case separates the rounded from the unrounded hand-offs"

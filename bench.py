@@ -30,6 +30,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -90,61 +91,110 @@ def profiled_traffic(kind: str):
 
 
 # ------------------------------------------------------------------ clocks
+# NVML clock event reason bits (nvml.h): software power cap, hardware
+# slowdown, software / hardware thermal slowdown.
+_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown"}
+
+
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+    """SM clock and clock-event reasons sampled DURING the timed region.
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Reads NVML in-process every ~2 ms from a thread (libnvidia-ml through
+    ctypes; reading clocks changes no setting), so a region of a few tens of
+    milliseconds gets several samples; falls back to nvidia-smi every 20 ms
+    when NVML cannot be loaded.  The GPU is found by its PCI bus id."""
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, torch=None):
         self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
+        self.torch = torch
+        self.samples = []  # (sm_mhz, reasons_mask)
+        self.sm_max = None
+        self.source = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+
+    # -- NVML
+    def _nvml_handle(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        ok = False
+        if self.torch is not None:
+            try:
+                pr = self.torch.cuda.get_device_properties(self.gpu)
+                bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0".encode()
+                ok = lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(h)) == 0
+            except Exception:
+                ok = False
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.gpu, ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+            self.sm_max = float(mx.value)
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, reasons
+
+    def _nvml_loop(self, lib, h, reasons):
+        import ctypes
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                r = rs.value if reasons(h, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((float(clk.value), int(r)))
+            time.sleep(0.002)
+
+    # -- nvidia-smi
+    def _smi_loop(self):
+        fields = "clocks.sm,clocks.max.sm,clocks_event_reasons.active"
+        self._proc = subprocess.Popen(
+            ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={fields}", "--format=csv,noheader,nounits",
+             "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        for line in self._proc.stdout:
+            parts = [t.strip() for t in line.split(",")]
+            try:
+                self.sm_max = float(parts[1])
+                self.samples.append((float(parts[0]), int(parts[2], 16)))
+            except (ValueError, IndexError):
+                pass
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
-        except OSError:
-            self.proc = None
+            lib, h, reasons = self._nvml_handle()
+            self.source = "nvml"
+            self._thread = threading.Thread(target=self._nvml_loop, args=(lib, h, reasons), daemon=True)
+        except (OSError, AttributeError):
+            self.source = "nvidia-smi"
+            self._thread = threading.Thread(target=self._smi_loop, daemon=True)
+        self._thread.start()
+        time.sleep(0.005)
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx = float(parts[1])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.sm_max, "reasons": ["no samples"], "samples": 0,
+                    "source": self.source}
+        mask = 0
+        for _, r in self.samples:
+            mask |= r
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.sm_max,
+                "reasons": sorted(n for bit, n in _REASONS.items() if mask & bit),
+                "samples": len(self.samples), "source": self.source}
 
 
 # ------------------------------------------------------------------ stack
@@ -316,16 +366,34 @@ def capture(fn, torch, direct=False):
 
 
 def time_graph(g, n, torch):
+    """Mean ms per replay of g over n back-to-back replays (CUDA events on
+    the launching stream)."""
+    return time_steps(g, n, torch)[0] / n
+
+
+def time_steps(g, n, torch):
+    """n replays of g on one stream, each bracketed by CUDA events recorded
+    on that stream: (total ms from the first start to the last end, per-step
+    ms)."""
     st = torch.cuda.Stream()
     with torch.cuda.stream(st):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
         torch.cuda.synchronize()
-        e0.record(st)
-        for _ in range(n):
+        ev[0].record(st)
+        for i in range(n):
             g.replay()
-        e1.record(st)
-        e1.synchronize()
-    return e0.elapsed_time(e1) / n  # ms
+            ev[i + 1].record(st)
+        ev[-1].synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+    return ev[0].elapsed_time(ev[-1]), per
+
+
+def step_stats(per_ms):
+    """Median, 10th and 90th percentile (nearest rank) of per-step times."""
+    v = sorted(per_ms)
+    q = lambda f: v[min(len(v) - 1, max(0, int(math.ceil(f * len(v))) - 1))]
+    return {"median": round(statistics.median(v), 4), "p10": round(q(0.10), 4), "p90": round(q(0.90), 4),
+            "n": len(v)}
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -352,8 +420,8 @@ class OracleLayer:
 
 
 def oracle_layer_timing(wl, budget_s: float = 12.0, max_reps: int = 64):
-    """Times the CPU oracle on one layer of `wl` for about `budget_s` seconds.
-    Returns (us_per_layer, reps)."""
+    """Times the CPU oracle on one layer of `wl` for about `budget_s` seconds
+    in this process (one thread).  Returns (us_per_layer, reps)."""
     lay = OracleLayer(wl)
     reps, t0 = 0, time.perf_counter()
     while True:
@@ -365,14 +433,96 @@ def oracle_layer_timing(wl, budget_s: float = 12.0, max_reps: int = 64):
     return el / reps * 1e6, reps
 
 
-def workload_config(wl, n_gpus):
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+# Worker state of OraclePool (one layer per process, built once).
+_POOL_LAYER = None
+_POOL_BARRIER = None
+
+
+def _pool_init(wl_args, barrier):
+    global _POOL_LAYER, _POOL_BARRIER
+    sys.path.insert(0, ROOT)
+    import synth
+    _POOL_LAYER = OracleLayer(synth.QWEN8B.with_(**wl_args))
+    _POOL_BARRIER = barrier
+
+
+def _pool_run(_):
+    # every worker waits for all the others, so each takes exactly one pass
+    _POOL_BARRIER.wait(timeout=600)
+    t0 = time.perf_counter()
+    _POOL_LAYER.run()
+    return time.perf_counter() - t0
+
+
+class OraclePool:
+    """The CPU oracle on all host cores: `procs` processes (started with
+    spawn, so no CUDA state is inherited), each holding one layer of the
+    workload quantised by the oracle; step() runs the layer once in every
+    process at the same time, i.e. `procs` layers per step."""
+
+    def __init__(self, wl, procs):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.procs = procs
+        self.barrier = ctx.Barrier(procs)
+        args = dict(d=wl.d, f=wl.f, M=wl.M, group=wl.group, fmt=wl.fmt, eps=wl.eps, wid=wl.wid)
+        self.pool = ctx.Pool(procs, initializer=_pool_init, initargs=(args, self.barrier))
+
+    def step(self):
+        t0 = time.perf_counter()
+        per = self.pool.map(_pool_run, range(self.procs), chunksize=1)
+        return time.perf_counter() - t0, per
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_pool_timing(wl, steps: int = 3):
+    """Layers per second of the oracle over every host core (one process
+    per core, one layer each per step); the first step warms up."""
+    procs = host_cores()
+    pool = OraclePool(wl, procs)
+    try:
+        pool.step()
+        walls = [pool.step()[0] for _ in range(steps)]
+    finally:
+        pool.close()
+    return procs * steps / sum(walls), procs
+
+
+def workload_config(wl):
+    """The workload only (shared by the GPU arm and the reference arm)."""
     return {"workload": wl.name, "d": wl.d, "f": wl.f, "rows_M": wl.M, "layers": wl.layers,
             "weights": {0: "bf16", 1: "affine8", 2: "affine4"}[wl.fmt], "group": wl.group,
-            "eps": wl.eps, "bytes_per_layer": wl.layer_bytes(),
-            "l2": "inputs larger than L2: each step streams all layers' weights once "
-                  f"({wl.layer_bytes() * wl.layers / 1e9:.2f} GB per step vs 129 MB L2)",
-            "graph": "one CUDA graph per step, PDL between kernels",  # overwritten below when direct
-            "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU"}
+            "eps": wl.eps, "bytes_per_layer": wl.layer_bytes()}
 
 
 def dist_env():
@@ -393,33 +543,37 @@ def reduce_max(value: float, ws: int, torch, device=None):
 
 
 def run_reference(args):
-    """The reference arm: the float64 CPU oracle, one layer of the Qwen3-8B
-    stack per step (a bounded sample of the workload), on the host cores."""
+    """The reference arm: the float64 CPU oracle over every host core (one
+    process per core), each step one layer of the Qwen3-8B stack in every
+    process at once -- a bounded sample of the workload; value = layers per
+    step / step time, in the GPU arm's unit.  Under torchrun only rank 0 runs."""
     import synth
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
     wl = synth.QWEN8B
-    lay = OracleLayer(wl)
-    for _ in range(max(0, args.warmup)):
-        lay.run()
-    times = []
-    for _ in range(max(1, args.steps)):
-        t0 = time.perf_counter()
-        lay.run()
-        times.append(time.perf_counter() - t0)
-    total = sum(times)
-    us = total / len(times) * 1e6
-    gbs = wl.layer_bytes() / (us * 1e-6) / 1e9
+    pool = OraclePool(wl, host_cores())
+    try:
+        for _ in range(max(0, args.warmup)):
+            pool.step()
+        walls = [pool.step()[0] for _ in range(max(1, args.steps))]
+    finally:
+        pool.close()
+    per_layer_s = sum(walls) / (len(walls) * pool.procs)  # wall time per layer over all cores
+    us = per_layer_s * 1e6
+    gbs = wl.layer_bytes() / per_layer_s / 1e9
+    sample = (f"{pool.procs} processes (one per host core), each one {wl.d}x{wl.f} affine8 g128 "
+              f"layer per step, of the {wl.layers}-layer stack; single-threaded binary64 C oracle")
     line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
-            "us_per_layer": round(us, 1), "n_gpus": args.gpus, "steps": len(times),
-            "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": True,
+            "us_per_layer": round(us, 1), "n_gpus": args.gpus, "steps": len(walls),
+            "warmup": args.warmup, "ms_per_step": round(sum(walls) / len(walls) * 1e3, 3),
+            "step_ms": step_stats([w * 1e3 for w in walls]), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(wl, 1),
-            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"one {wl.d}x{wl.f} affine8 g128 layer per step "
-                                       "(a bounded sample of the 36-layer stack), single-threaded "
-                                       "binary64 C oracle"},
+            "config": workload_config(wl),
+            "path": "float64 CPU oracle, one layer per process per step, host cores",
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": pool.procs,
+                             "threads": pool.procs, "nproc": os.cpu_count(), "cpu_model": cpu_model(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -624,7 +778,7 @@ def run_projections(args, torch, synth, mt, dev):
         for _ in range(max(3, args.warmup)):
             g.replay()
         steps = max(5, args.steps // 10)
-        with ClockSampler(dev.index or 0) as clk:
+        with ClockSampler(dev.index or 0, torch) as clk:
             ms = time_graph(g, steps, torch)
         del g
         pt.update({"us_per_step": round(ms * 1e3, 2),
@@ -718,7 +872,7 @@ def run_prefill(args, torch, synth, mt, dev):
             for _ in range(max(3, args.warmup)):
                 gk.replay()
             if name == "layer":
-                with ClockSampler(dev.index or 0) as clk:
+                with ClockSampler(dev.index or 0, torch) as clk:
                     res_us[name] = time_graph(gk, reps, torch) * 1e3 / n_layers
             else:
                 res_us[name] = time_graph(gk, reps, torch) * 1e3 / n_layers
@@ -865,14 +1019,14 @@ def main():
         g_step.replay()
     torch.cuda.synchronize()
 
-    # ---- timed region: K graph replays
+    # ---- timed region: K graph replays, each between its own CUDA events
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        ms = time_graph(g_step, args.steps, torch)
+    with ClockSampler(local, torch) as clk:
+        total_ms, per_step = time_steps(g_step, args.steps, torch)
     torch.cuda.synchronize()
-    ms = reduce_max(ms, ws, torch, dev)
+    ms = reduce_max(total_ms / args.steps, ws, torch, dev)
     step_bytes = wl.layer_bytes() * wl.layers
     value = ws * step_bytes / (ms * 1e-3) / 1e9
     us_layer = ms * 1e3 / wl.layers
@@ -943,9 +1097,13 @@ def main():
             "us_per_layer": round(us_layer, 3), "frac_of_8TBs": round(value / ws / 8000.0, 4),
             "frac_of_measured_hbm": round(value / ws / peak, 4),
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": round(ms, 4), "step_ms": step_stats(per_step),
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": {0: "bf16", 1: "u8", 2: "u4"}[wl.fmt] + "-weights/f32-acc",
-            "data": "synthetic", "config": workload_config(wl, ws),
+            "data": "synthetic", "config": workload_config(wl),
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+            "l2": "inputs larger than L2: each step streams all layers' weights once "
+                  f"({wl.layer_bytes() * wl.layers / 1e9:.2f} GB per step vs 129 MB L2)",
             "gpu_launches": (1 if use_exec else 3 * wl.layers) * args.steps,
             "device_error": mt.mt_device_error(),
             "roofline": roof,
@@ -959,19 +1117,24 @@ def main():
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "clocks": clk.summary()}
     if use_exec:
-        line["config"]["path"] = "warmed executor: mt_mlp_plan_run, one cooperative kernel per step"
+        line["path"] = "warmed executor: mt_mlp_plan_run, one cooperative kernel per step"
     else:
-        line["config"]["path"] = "single calls: mt_add_rmsnorm + mt_swiglu_gateup + mt_down_residual " \
-                                 "per layer" + (", no PDL" if args.no_pdl else ", PDL between kernels")
-    line["config"]["graph"] = "direct launches" if isinstance(g_step, DirectLaunch) else \
-        "one CUDA graph per step"
+        line["path"] = "single calls: mt_add_rmsnorm + mt_swiglu_gateup + mt_down_residual " \
+                       "per layer" + (", no PDL" if args.no_pdl else ", PDL between kernels")
+    line["graph"] = "direct launches" if isinstance(g_step, DirectLaunch) else "one CUDA graph per step"
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and wl.name == synth.QWEN8B.name:
+        # one thread, then one process per host core (spawned: no CUDA state)
         us_cpu, reps = oracle_layer_timing(wl)
-        line["cpu_baseline"] = {"value": round(wl.layer_bytes() / (us_cpu * 1e-6) / 1e9, 4),
-                                "unit": "GB/s", "us_per_layer": round(us_cpu, 1), "cores": 1,
-                                "kind": "oracle",
-                                "sample": f"{reps} passes of one layer ({wl.d}x{wl.f}, affine8 g128) "
-                                          "of the same workload, binary64 C oracle, one thread"}
+        lps, procs = oracle_pool_timing(wl)
+        line["cpu_baseline"] = {"value": round(wl.layer_bytes() * lps / 1e9, 4), "unit": "GB/s",
+                                "us_per_layer": round(1e6 / lps, 1), "cores": procs, "threads": procs,
+                                "nproc": os.cpu_count(), "cpu_model": cpu_model(), "kind": "oracle",
+                                "single_thread": {"value": round(wl.layer_bytes() / (us_cpu * 1e-6) / 1e9, 4),
+                                                  "us_per_layer": round(us_cpu, 1), "passes": reps},
+                                "sample": f"one {wl.d}x{wl.f} affine8 g128 layer of the same workload per "
+                                          f"process, {procs} processes at once (one per host core) for "
+                                          "3 rounds after one warm-up round; single-threaded binary64 C "
+                                          "oracle; single_thread: one process alone"}
     stack.close()
     if rank == 0:
         print(json.dumps(line), flush=True)

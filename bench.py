@@ -939,6 +939,33 @@ def run_mx(args, torch, synth, mt, dev):
     return 0
 
 
+def run_only(args, torch, synth, mt, dev):
+    """Profiling aid: the chosen kernels over the workload's layers, warm-up +
+    steps times, launched directly (no graph, no timing, no JSON line), so a
+    profiler sees plain launches in a known order."""
+    if args.workload == "sweep":
+        wl = synth.sweep_point(args.sweep_group or 128, args.sweep_rows or 1)
+    elif args.workload == "mx":
+        wl = {"fp8": synth.QWEN8B_MXFP8, "fp4": synth.QWEN8B_MXFP4}[args.mx].with_(M=args.rows or 1)
+    elif args.workload in ("qwen3-8b", "tiny", "llama1b", "qwen15"):
+        wl = {"qwen3-8b": synth.QWEN8B, "tiny": synth.TINY, "llama1b": synth.LLAMA1B,
+              "qwen15": synth.QWEN15}[args.workload]
+    else:
+        raise SystemExit(f"--only does not take --workload {args.workload}")
+    if args.layers:
+        wl = wl.with_(layers=args.layers)
+    stack = Stack(wl, dev)
+    fn = {"gateup": stack.gateup_only, "down": stack.down_only,
+          "executor": stack.step_executor}[args.only]
+    if args.only == "executor" and stack.plan is None:
+        raise SystemExit("the executor does not take this workload")
+    for _ in range(max(3, args.warmup) + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    stack.close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -968,8 +995,12 @@ def main():
     ap.add_argument("--gemv", default="default", choices=["default", "team", "mma"],
                     help="single-call GEMV kernels: default (warp-task kernel for one row, "
                          "tensor-core kernel for M > 1), team kernel, or tensor-core kernel for every M")
-    ap.add_argument("--only", default=None, choices=["gateup", "executor"],
-                    help="profiling aid: run only these kernels (no timing, no JSON line)")
+    ap.add_argument("--only", default=None, choices=["gateup", "down", "executor"],
+                    help="profiling aid: run only these kernels over the workload's layers "
+                         "(no timing, no JSON line); sweep takes one point (--sweep-group, "
+                         "--sweep-rows), mx one format (--mx) and --rows")
+    ap.add_argument("--mx", default="fp8", choices=["fp8", "fp4"],
+                    help="mx with --only: the MX format")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -988,6 +1019,8 @@ def main():
         mt.mt_set_option(mt.MT_OPT_PDL, 0)
     mt.mt_set_option(mt.MT_OPT_GEMV, {"default": 0, "team": 1, "mma": 2}[args.gemv])
 
+    if args.only:
+        return run_only(args, torch, synth, mt, dev)
     if args.workload == "sweep":
         return run_sweep(args, torch, synth, mt, dev)
     if args.workload == "configs":
@@ -1004,14 +1037,6 @@ def main():
         wl = wl.with_(layers=args.layers)
     stack = Stack(wl, dev)
     use_exec = args.path == "executor" and stack.plan is not None
-
-    if args.only:
-        fn = stack.gateup_only if args.only == "gateup" else stack.step_executor
-        for _ in range(max(3, args.warmup) + args.steps):
-            fn()
-        torch.cuda.synchronize()
-        stack.close()
-        return 0
 
     step_fn = stack.step_executor if use_exec else stack.step_calls
     g_step = capture(step_fn, torch, direct=args.no_graph)

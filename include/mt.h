@@ -76,6 +76,12 @@
  *   written by work still running on the stream (upload or pack them, then
  *   synchronise or record an event, before the first call that reads them).
  *   mt_set_option(MT_OPT_PDL, 0) turns this off.
+ * - Device reset.  The first launch of a kernel that uses more than 48 KB of
+ *   shared memory on a device sets its limit once per process.  A
+ *   cudaDeviceReset may drop that limit, and such a launch then returns
+ *   MT_ERR_CUDA (cudaErrorInvalidValue) instead of running; plans made
+ *   before the reset hold freed memory.  mt_mlp_stack_run_noalloc and
+ *   mt_device_error look everything up on each call and stay valid.
  */
 #ifndef MT_H
 #define MT_H
@@ -390,15 +396,21 @@ mt_status mt_mlp_plan_destroy(mt_mlp_plan* plan);
  *   values, residual, out_y, stream  : as for mt_mlp_plan_run (no trace)
  * Scratch.  The layer table and the hand-off words live in one static device
  * array of MT_STACK_SCRATCH_BYTES bytes per device:
- *   128*ceil(80 L / 128) + 128 + 128*ceil(4 S / 128)
+ *   128*ceil(80 L / 128) + 128 + 2*128*ceil(4 S / 128)
  *     + 128*ceil(2 d / 128) + 128*ceil(2 f / 128)      bytes, S = SM count
- * (36,480 bytes for 36 layers of d = 4096, f = 12288 on 152 SMs).  Larger
- * problems return MT_ERR_SHAPE.  Each call uploads the table
- * (cudaMemcpyAsync from host memory) and zeroes the barrier line (cudaMemsetAsync) on
- * `stream` before the kernel; it calls no allocating routine.
- * Set-up.  The first call on a device, made with that device current, looks
- * up the array's device address (cudaGetSymbolAddress) and sets the kernel's
- * shared-memory limit; make that first call before any stream capture.
+ * (37,120 bytes for 36 layers of d = 4096, f = 12288 on 152 SMs).  Larger
+ * problems return MT_ERR_SHAPE.
+ * Launches.  Each call launches a one-block kernel per 48 layers that takes
+ * the table as kernel parameters, writes it to the array and zeroes the
+ * barrier line, then the stack kernel, all on `stream`.  It makes no copy
+ * from host memory and calls no allocating or synchronising routine, so the
+ * call can be captured into a CUDA graph; the graph then replays the table
+ * and the pointers of the captured call.
+ * Set-up.  Every call looks up the array's device address
+ * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit
+ * (cudaFuncSetAttribute), so the call stays valid across a cudaDeviceReset.
+ * The first call in a process may load the library's device code: make it
+ * before any stream capture.
  * Concurrency.  Every call on a device uses the same array: calls that can
  * overlap in time (other streams, or calls not ordered by the caller) race
  * and give undefined results.

@@ -65,9 +65,14 @@ struct PqShape {
 };
 
 // One weight row's 2^t_n and 2^-t_n: warp per row, max over the row's groups
-// of |s| qmax + |b| (a bound on |w|), t_n = 14 - floor(log2 max) clamped to
-// [-100, 100] (0 for an all-zero row).  Rows of both matrices: row index
-// i in [0, NW * N), matrix i / N.
+// of |s| qmax + |b| (a bound on |w|, in binary64 so that it cannot overflow
+// for finite scales), t_n = 14 - floor(log2 max) clamped to [-126, 126] (0
+// for an all-zero row, and for a row whose scales or biases are not finite:
+// its weights are then infinite or NaN and so are its outputs, as in IEEE
+// arithmetic).  Every row whose bound is at least 2^-112 is scaled into
+// [2^14, 2^15); a smaller row is scaled by 2^126 and keeps full fp16
+// precision for every weight above 2^-140.  Rows of both matrices: row
+// index i in [0, NW * N), matrix i / N.
 __global__ void __launch_bounds__(256) prefill_wscale_kernel(const uint16_t* __restrict__ s0,
                                                              const uint16_t* __restrict__ b0,
                                                              const uint16_t* __restrict__ s1,
@@ -80,16 +85,17 @@ __global__ void __launch_bounds__(256) prefill_wscale_kernel(const uint16_t* __r
   const int mat = (int)(row / N), n = (int)(row - (long)mat * N);
   const uint16_t* sp = (mat ? s1 : s0) + (size_t)n * G;
   const uint16_t* bp = (mat ? b1 : b0) + (size_t)n * G;
-  float m = 0.f;
-  for (int g = lane; g < G; g += 32) m = fmaxf(m, fabsf(bf16f(sp[g])) * qmax + fabsf(bf16f(bp[g])));
+  double m = 0.0;
+  for (int g = lane; g < G; g += 32)
+    m = fmax(m, fabs((double)bf16f(sp[g])) * (double)qmax + fabs((double)bf16f(bp[g])));
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  for (int off = 16; off > 0; off >>= 1) m = fmax(m, __shfl_xor_sync(0xffffffffu, m, off));
   if (lane == 0) {
     int t = 0;
-    if (m > 0.f && m <= 3.0e38f) {
+    if (m > 0.0 && isfinite(m)) {
       int e;
-      (void)frexpf(m, &e);  // m = f 2^e, f in [0.5, 1): floor(log2 m) = e - 1
-      t = max(-100, min(100, 14 - (e - 1)));
+      (void)frexp(m, &e);  // m = f 2^e, f in [0.5, 1): floor(log2 m) = e - 1
+      t = max(-126, min(126, 14 - (e - 1)));
     }
     tsc[row] = exp2i(t);
     tinv[row] = exp2i(-t);

@@ -43,7 +43,6 @@
 // of their rows next to h, and x's largest |x| is a CTA reduction.
 #include <math.h>
 
-#include <mutex>
 #include <new>
 
 #include "k_phase.cuh"
@@ -703,32 +702,41 @@ static __device__ __align__(256) unsigned char g_stack_scratch[MT_STACK_SCRATCH_
 
 namespace mt {
 
-// Per-device one-time set-up: the scratch's device address (with the device
-// current) and the kernel's shared-memory limit.  Guarded by a mutex.
-struct NoallocState {
-  std::mutex mu;
-  void* scratch[64];
-  bool attr_set[3][64];
+// The layer table reaches the device as kernel parameters: a launch copies
+// its parameters when it is issued, so nothing on the host has to outlive the
+// call and the upload can be captured into a CUDA graph (a cudaMemcpyAsync
+// from pageable host memory can be neither).  48 entries of 80 bytes keep the
+// parameter block under the classic 4 KB limit.
+constexpr int TABLE_CHUNK = 48;
+struct TableChunk {
+  StackLayerDev t[TABLE_CHUNK];
 };
-static NoallocState g_noalloc;
+static_assert(sizeof(StackLayerDev) % 8 == 0, "table entries copied as 8-byte words");
+static_assert(sizeof(TableChunk) + 32 <= 4096, "table chunk within the parameter limit");
 
-static mt_status noalloc_setup(int dev, int fmt, const void* kernel, size_t smem_limit,
-                               void** scratch) {
-  if (dev < 0 || dev >= 64) return cuda_fail(cudaErrorInvalidDevice);
-  std::lock_guard<std::mutex> g(g_noalloc.mu);
-  if (!g_noalloc.scratch[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_stack_scratch);
-    if (e != cudaSuccess) return cuda_fail(e);
-    g_noalloc.scratch[dev] = p;
-  }
-  if (!g_noalloc.attr_set[fmt][dev]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_limit);
-    if (e != cudaSuccess) return cuda_fail(e);
-    g_noalloc.attr_set[fmt][dev] = true;
-  }
-  *scratch = g_noalloc.scratch[dev];
+// Writes n entries of the chunk to dst and, when ctl is given, zeroes the
+// control line (barrier counter, abort flag) that the stack kernel starts from.
+__global__ void __launch_bounds__(256) stack_table_kernel(const TableChunk c, int n,
+                                                          StackLayerDev* __restrict__ dst,
+                                                          StackCtl* __restrict__ ctl) {
+  constexpr int WPE = sizeof(StackLayerDev) / 8;
+  const unsigned long long* src = reinterpret_cast<const unsigned long long*>(c.t);
+  unsigned long long* out = reinterpret_cast<unsigned long long*>(dst);
+  for (int i = threadIdx.x; i < n * WPE; i += blockDim.x) out[i] = src[i];
+  if (ctl && threadIdx.x < (int)(sizeof(StackCtl) / 4)) reinterpret_cast<int*>(ctl)[threadIdx.x] = 0;
+}
+
+// Set-up done on every call, so that nothing cached outlives a
+// cudaDeviceReset (which reloads the module at new addresses and drops the
+// kernel's attributes): the scratch's device address and the kernel's
+// shared-memory limit.  Neither call allocates or synchronises.
+static mt_status noalloc_setup(const void* kernel, size_t smem_limit, void** scratch) {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_stack_scratch);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_limit);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *scratch = p;
   return MT_OK;
 }
 
@@ -794,9 +802,9 @@ extern "C" mt_status mt_mlp_stack_run_noalloc(const mt_mlp_layer* layers, int L,
   const size_t total = o_hbuf + round128((size_t)f * 2);
   if (total > (size_t)MT_STACK_SCRATCH_BYTES) return MT_ERR_SHAPE;
 
-  // ---- one-time set-up of this device, then the launch
+  // ---- set-up, the table upload, then the launch
   void* scratch = nullptr;
-  const mt_status st = noalloc_setup(P.dev, (int)fmt, P.kernel, budget, &scratch);
+  const mt_status st = noalloc_setup(P.kernel, budget, &scratch);
   if (st != MT_OK) return st;
   int occ = 0;
   ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, P.kernel, WT_THREADS, P.smem);
@@ -806,15 +814,12 @@ extern "C" mt_status mt_mlp_stack_run_noalloc(const mt_mlp_layer* layers, int L,
   if (!err) return cuda_fail(cudaErrorInvalidSymbol);
   cudaStream_t s = (cudaStream_t)stream;
   char* base = static_cast<char*>(scratch);
-  // the layer table, converted in chunks on the host stack; copies from
-  // pageable memory are staged before cudaMemcpyAsync returns
-  constexpr int CHUNK = 32;
-  for (int l0 = 0; l0 < L; l0 += CHUNK) {
-    StackLayerDev tab[CHUNK];
-    const int n = L - l0 < CHUNK ? L - l0 : CHUNK;
+  for (int l0 = 0; l0 < L; l0 += TABLE_CHUNK) {
+    TableChunk c;
+    const int n = L - l0 < TABLE_CHUNK ? L - l0 : TABLE_CHUNK;
     for (int i = 0; i < n; ++i) {
       const mt_mlp_layer& y = layers[l0 + i];
-      StackLayerDev& t = tab[i];
+      StackLayerDev& t = c.t[i];
       t.wn = (const uint16_t*)y.norm_weight;
       t.Wg = (const uint8_t*)y.Wg; t.Wu = (const uint8_t*)y.Wu; t.Wd = (const uint8_t*)y.Wd;
       if (aff) {
@@ -826,13 +831,14 @@ extern "C" mt_status mt_mlp_stack_run_noalloc(const mt_mlp_layer* layers, int L,
         t.sg = t.su = t.bg = t.bu = t.sd = t.bd = nullptr;
       }
     }
-    ce = cudaMemcpyAsync(base + (size_t)l0 * sizeof(StackLayerDev), tab,
-                         (size_t)n * sizeof(StackLayerDev), cudaMemcpyHostToDevice, s);
+    for (int i = n; i < TABLE_CHUNK; ++i) c.t[i] = StackLayerDev{};
+    StackLayerDev* dst = reinterpret_cast<StackLayerDev*>(base) + l0;
+    StackCtl* ctl = l0 == 0 ? reinterpret_cast<StackCtl*>(base + o_ctl) : nullptr;
+    int cnt = n;
+    void* targs[] = {&c, &cnt, &dst, &ctl};
+    ce = cudaLaunchKernel((const void*)stack_table_kernel, dim3(1), dim3(256), targs, 0, s);
     if (ce != cudaSuccess) return cuda_fail(ce);
   }
-  // the control line (barrier counter, abort flag) must start at zero
-  ce = cudaMemsetAsync(base + o_ctl, 0, 128, s);
-  if (ce != cudaSuccess) return cuda_fail(ce);
 
   StackArgs a = P.base;
   a.layers = reinterpret_cast<const StackLayerDev*>(base);

@@ -18,18 +18,12 @@ static std::atomic<int> g_opt_barrier_extra{0};
 // Device error word: kernels with bounded waits record MT_ERR_TIMEOUT here.
 __device__ int g_device_error;
 
+// Looked up on every call (no allocation, no synchronisation): a cached
+// address would dangle after a cudaDeviceReset reloads the module.
 int* device_error_ptr() {
-  static std::mutex mu;
-  static int* ptr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> g(mu);
-  if (!ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    ptr[dev] = static_cast<int*>(p);
-  }
-  return ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
 }
 
 int gemv_choice() { return g_opt_gemv.load(); }

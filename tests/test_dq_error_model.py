@@ -17,11 +17,13 @@ import oracle
 import synth
 
 
-def _pow2_scale(m):
-    """t with m 2^t in [2^14, 2^15) (0 for m == 0)."""
+def _pow2_scale(m, clamp=None):
+    """t with m 2^t in [2^14, 2^15) (0 for m == 0); clamp: the kernel's
+    range of t for the weight rows, [-126, 126] (2^t a normal fp32)."""
     m = np.asarray(m, dtype=np.float64)
     e = np.floor(np.log2(np.where(m > 0, m, 1.0)))
-    return np.where(m > 0, 14 - e, 0.0)
+    t = np.where(m > 0, 14 - e, 0.0)
+    return t if clamp is None else np.clip(t, -clamp, clamp)
 
 
 def _model(x_bits, W: oracle.Weight, bits: int):
@@ -29,7 +31,7 @@ def _model(x_bits, W: oracle.Weight, bits: int):
     s = oracle.f64_from_bf16(W.scales)
     b = oracle.f64_from_bf16(W.biases)
     bound = (np.abs(s) * (2 ** bits - 1) + np.abs(b)).max(axis=1)
-    t = _pow2_scale(bound)
+    t = _pow2_scale(bound, clamp=126)
     ws = w * np.exp2(t)[:, None]
     assert np.abs(ws).max() < 2.0 ** 15, "scaled weight beyond the fp16 plan"
     wq = ws.astype(np.float16).astype(np.float64) * np.exp2(-t)[:, None]
@@ -66,3 +68,19 @@ def test_dq_rows_far_apart():
     t_all = _pow2_scale(np.abs(w).max())
     wq = (w * 2.0 ** t_all).astype(np.float16).astype(np.float64) * 2.0 ** -t_all
     assert np.count_nonzero(wq[0]) == 0 and np.count_nonzero(w[0]) > 0
+
+
+def test_dq_rows_near_the_bottom_of_the_range():
+    """Rows scaled by 2^-120 (bf16 scales near the bottom of the normal range
+    and below): t is clamped to 126, and each row still keeps its relative
+    precision next to rows of ordinary and large magnitude."""
+    bits, group, M, K, N = 8, 64, 3, 256, 24
+    x = synth.host_bf16(M * K, 41950, synth.ACT).reshape(M, K)
+    W32 = synth.host_f32(N * K, 41951, synth.WEIGHT).reshape(N, K).astype(np.float64)
+    W32 = (W32 * np.exp2(np.linspace(-120, 60, N))[:, None]).astype(np.float32)
+    W = oracle.Weight.from_f32(W32, bits, group)
+    s = oracle.f64_from_bf16(W.scales)
+    assert s[0].max() < 2.0 ** -120  # the smallest row's scales are bf16 subnormals
+    y, mag = _model(x, W, bits)
+    ref = oracle.linear_bias(x, W)
+    assert np.all(np.abs(y - ref) <= 2.0 ** -10 * mag)

@@ -71,13 +71,15 @@ def test_dq_error_bound(mt, fmt, group, M, K, N):
     assert np.all(err <= bound), f"error {err[worst]:.3e} above the bound {bound[worst]:.3e} at {worst}"
 
 
-@pytest.mark.parametrize("fmt", [1, 2])
-def test_dq_rows_of_any_magnitude(mt, fmt):
+@pytest.mark.parametrize("fmt,lo,hi", [(1, -40, 40), (2, -40, 40), (1, -120, 60)])
+def test_dq_rows_of_any_magnitude(mt, fmt, lo, hi):
+    """Rows scaled by 2^lo .. 2^hi (down to bf16-subnormal scales) each keep
+    their own precision."""
     group, M, K, N = 64, 40, 512, 96
     seed = 32000 + fmt
     x = synth.host_bf16(M * K, seed, synth.ACT).reshape(M, K)
-    W32 = synth.host_f32(N * K, seed + 1, synth.WEIGHT).reshape(N, K)
-    W32 = (W32 * np.exp2(np.linspace(-40, 40, N)).astype(np.float32)[:, None]).astype(np.float32)
+    W32 = synth.host_f32(N * K, seed + 1, synth.WEIGHT).reshape(N, K).astype(np.float64)
+    W32 = (W32 * np.exp2(np.linspace(lo, hi, N))[:, None]).astype(np.float32)
     q, s, b = _pack(mt, W32, fmt, group)
     W = _oracle_weight(W32, fmt, group)
     res = np.zeros((M, N), dtype=np.uint16)  # zero addend: every row's own magnitude stays visible

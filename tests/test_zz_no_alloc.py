@@ -70,6 +70,58 @@ def test_noalloc_matches_plan(mt, wl):
         assert np.array_equal(host_bits(y), host_bits(ref)), f"call {call}: not bit-identical to the plan"
 
 
+def _plan_ref(mt, wl, layers, vals, r0):
+    ref = torch.empty(wl.d, dtype=torch.bfloat16, device="cuda")
+    plan = mt.mt_mlp_plan_create(layers, wl.d, wl.f, wl.group, wl.fmt, wl.eps)
+    try:
+        mt.mt_mlp_plan_run(plan, vals, r0, ref)
+        torch.cuda.synchronize()
+    finally:
+        mt.mt_mlp_plan_destroy(plan)
+    return ref
+
+
+def test_noalloc_table_in_two_chunks(mt):
+    """50 layers: the table reaches the device in two parameter blocks (48 + 2
+    entries); the result is the plan's, bit for bit."""
+    wl = synth.TINY.with_(layers=50)
+    layers = [plan_layer(DevLayer(mt, wl, l)) for l in range(wl.layers)]
+    vals, r0 = _inputs(wl, wl.layers)
+    ref = _plan_ref(mt, wl, layers, vals, r0)
+    y = torch.full((wl.d,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mt.mt_mlp_stack_run_noalloc(layers, wl.d, wl.f, wl.group, wl.fmt, wl.eps, vals, r0, y)
+    torch.cuda.synchronize()
+    assert mt.mt_device_error(False) == 0
+    assert np.array_equal(host_bits(y), host_bits(ref))
+
+
+def test_noalloc_captured_in_a_graph(mt):
+    """The call captured into a CUDA graph (after a first call outside any
+    capture) and replayed on new contents of the same input buffers: each
+    replay gives the plan's result on those contents, bit for bit."""
+    wl = synth.TINY.with_(wid=13, layers=3)
+    n = wl.layers
+    layers = [plan_layer(DevLayer(mt, wl, l)) for l in range(n)]
+    vals, r0 = _inputs(wl, n)
+    y = torch.empty(wl.d, dtype=torch.bfloat16, device="cuda")
+    mt.mt_mlp_stack_run_noalloc(layers, wl.d, wl.f, wl.group, wl.fmt, wl.eps, vals, r0, y)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        mt.mt_mlp_stack_run_noalloc(layers, wl.d, wl.f, wl.group, wl.fmt, wl.eps, vals, r0, y)
+    torch.cuda.synchronize()
+    for trial in range(2):
+        v = np.stack([synth.host_bf16(wl.d, 52000 + 10 * trial + l, synth.ACT) for l in range(n)])
+        vals.copy_(dev_bf16(v))
+        r0.copy_(dev_bf16(synth.host_bf16(wl.d, 52100 + trial, synth.ACT)))
+        y.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert mt.mt_device_error(False) == 0
+        ref = _plan_ref(mt, wl, layers, vals, r0)
+        assert np.array_equal(host_bits(y), host_bits(ref)), f"replay {trial}"
+
+
 def test_noalloc_rejects_scratch_overflow(mt):
     """A layer table larger than the static scratch is refused before any
     device work (4096 layers x 80 bytes > MT_STACK_SCRATCH_BYTES)."""

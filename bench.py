@@ -947,6 +947,16 @@ def run_only(args, torch, synth, mt, dev):
         wl = synth.sweep_point(args.sweep_group or 128, args.sweep_rows or 1)
     elif args.workload == "mx":
         wl = {"fp8": synth.QWEN8B_MXFP8, "fp4": synth.QWEN8B_MXFP4}[args.mx].with_(M=args.rows or 1)
+    elif args.workload == "projections":
+        # one model's vocabulary projection (--proj), launched warm-up + steps times
+        pw = {"qwen3-8b": synth.QWEN8B_PROJ, "qwen15": synth.QWEN15_PROJ,
+              "llama1b": synth.LLAMA1B_PROJ}[args.proj]
+        ps = ProjStack(pw, dev, args.rows or pw.M)
+        vocab = [p.name for p in pw.projs if not p.per_layer]
+        for _ in range(max(3, args.warmup) + args.steps):
+            ps.run(vocab)
+        torch.cuda.synchronize()
+        return 0
     elif args.workload in ("qwen3-8b", "tiny", "llama1b", "qwen15"):
         wl = {"qwen3-8b": synth.QWEN8B, "tiny": synth.TINY, "llama1b": synth.LLAMA1B,
               "qwen15": synth.QWEN15}[args.workload]
@@ -998,9 +1008,12 @@ def main():
     ap.add_argument("--only", default=None, choices=["gateup", "down", "executor"],
                     help="profiling aid: run only these kernels over the workload's layers "
                          "(no timing, no JSON line); sweep takes one point (--sweep-group, "
-                         "--sweep-rows), mx one format (--mx) and --rows")
+                         "--sweep-rows), mx one format (--mx) and --rows, projections one "
+                         "model's vocabulary projection (--proj; --only takes any value there)")
     ap.add_argument("--mx", default="fp8", choices=["fp8", "fp4"],
                     help="mx with --only: the MX format")
+    ap.add_argument("--proj", default="llama1b", choices=["qwen3-8b", "qwen15", "llama1b"],
+                    help="projections with --only: the model whose vocabulary projection runs")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

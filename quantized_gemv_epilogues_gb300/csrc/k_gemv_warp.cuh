@@ -26,7 +26,8 @@ struct WarpArgs {
   int out_f32;
 };
 
-template <int FMT, int KIND>
+// RS: rows per load stream (g.RS; 2 for rows of exactly 64 chunks).
+template <int FMT, int KIND, int RS>
 __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs a) {
   constexpr bool AFF = FmtTraits<FMT>::AFFINE;
   constexpr int NW = KIND == 0 ? 2 : 1;
@@ -41,7 +42,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
   __shared__ float red[WARP_TASK_WARPS];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const PhaseCta c = phase_cta<KIND>(g, blockIdx.x);
+  const PhaseCta c = phase_cta<KIND, RS>(g, blockIdx.x);
 
   if (tid == 0) task_ctr = 2 * WARP_TASK_WARPS;  // tasks 0..2W-1 are taken statically
   __syncthreads();
@@ -50,10 +51,10 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
   const uint64_t pol = l2_evict_first_policy();
   uint4 bufA[WT_NS][WT_CL], bufB[WT_NS][WT_CL];
   const int tA = warp, tB = warp + WARP_TASK_WARPS;
-  wt_load<KIND>(g, a.w, c, tA, bufA, pol, lane);
-  wt_load<KIND>(g, a.w, c, tB, bufB, pol, lane);
-  wt_prefetch<KIND>(g, a.w, c, tA + 2 * WARP_TASK_WARPS, lane);
-  wt_prefetch<KIND>(g, a.w, c, tB + 2 * WARP_TASK_WARPS, lane);
+  wt_load<KIND, RS>(g, a.w, c, tA, bufA, pol, lane);
+  wt_load<KIND, RS>(g, a.w, c, tB, bufB, pol, lane);
+  wt_prefetch<KIND, RS>(g, a.w, c, tA + 2 * WARP_TASK_WARPS, lane);
+  wt_prefetch<KIND, RS>(g, a.w, c, tB + 2 * WARP_TASK_WARPS, lane);
   if constexpr (AFF) {
     stage_sb<KIND>(g, a.w, c, sm.sbr, tid, WT_THREADS);
     cp_async_commit();
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
   cp_async_wait_all();  // scales and biases
   __syncthreads();
 
-  wt_run<FMT, KIND>(g, a.w, c, sm, bufA, bufB, tA, tB, &task_ctr, pol, lane);
+  wt_run<FMT, KIND, RS>(g, a.w, c, sm, bufA, bufB, tA, tB, &task_ctr, pol, lane);
   __syncthreads();
 
   // epilogue: one thread per row adds the pieces in a fixed order
@@ -134,13 +135,14 @@ mt_status run_gemv_warp(const GemvProblem& p, const Launch& l) {
   const size_t budget = (size_t)di->max_smem_optin - 1024;  // static smem and slack
   if (smem > budget) return MT_ERR_SHAPE;
 
-  auto kern = gemv_warp_kernel<FMT, KIND>;
+  auto kern = a.g.RS == 2 ? gemv_warp_kernel<FMT, KIND, 2> : gemv_warp_kernel<FMT, KIND, 1>;
   {
     std::lock_guard<std::mutex> g(cache.mu);
     if (dev < 64 && !cache.attr_set[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)budget);
-      if (e != cudaSuccess) return cuda_fail(e);
+      for (auto k : {gemv_warp_kernel<FMT, KIND, 1>, gemv_warp_kernel<FMT, KIND, 2>}) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
+        if (e != cudaSuccess) return cuda_fail(e);
+      }
       cache.attr_set[dev] = 1;
     }
   }

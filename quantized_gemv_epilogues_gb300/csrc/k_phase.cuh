@@ -12,8 +12,12 @@
 //  * One CTA of 16 warps per SM owns a contiguous range of output rows.  The
 //    range is cut into tasks of two weight streams of B bytes that share
 //    their activations: gate and up of one row (gate/up), or two consecutive
-//    rows (down).  Tasks are handed out through a shared-memory counter, so
-//    the warps of a CTA finish within about one task of each other.
+//    rows (down).  A row of exactly 64 chunks (INT4 K = 2048, INT8 K = 1024,
+//    bf16 K = 512) would fill only half of a lane's registers, so there a
+//    stream spans two consecutive rows (RS = 2): every task still moves 4 KB,
+//    which doubles the bytes in flight for those shapes.  Tasks are handed
+//    out through a shared-memory counter, so the warps of a CTA finish within
+//    about one task of each other.
 //  * A warp holds two tasks' weights in registers (128-bit evict-first
 //    loads, up to 8 x 16 B per lane per task): it computes one while the
 //    other is in flight, ~128 KB in flight per SM with no per-copy issue
@@ -76,6 +80,8 @@ struct PhaseGeom {
   int GPP;                   // groups per piece (affine)
   int sb_stride;             // elements per staged scale or bias array (multiple of 8)
   int sb_vec;                // 1: scales/biases are staged in 16-byte copies (G % 8 == 0)
+  int RS;                    // rows per stream: 1, or 2 when P == 1 and CPR == 16 * WT_CL
+                             // (the kernel instantiated for it is chosen on the host)
 };
 
 // Weights of one phase.  Gate/up: W0 = gate, W1 = up.  Down: W0 only.
@@ -134,9 +140,9 @@ struct PhaseCta {
   int r_begin, rows, T;
 };
 
-template <int KIND>
+template <int KIND, int RS = 1>
 __device__ __forceinline__ PhaseCta phase_cta(const PhaseGeom& g, int cta) {
-  constexpr int RW = KIND == 0 ? 1 : 2;  // rows per task
+  constexpr int RW = (KIND == 0 ? 1 : 2) * RS;  // rows per task (RS == g.RS)
   PhaseCta c;
   c.r_begin = g.row_unit * (cta * g.rows_base + min(cta, g.rows_extra));
   c.rows = g.row_unit * (g.rows_base + (cta < g.rows_extra ? 1 : 0));
@@ -241,7 +247,7 @@ __device__ __forceinline__ float chunk_dot(const uint4 w, const uint4* __restric
 
 // Asks L2 for the weights of task t (one 128-byte line per lane; no
 // registers are written).
-template <int KIND>
+template <int KIND, int RS = 1>
 __device__ __forceinline__ void wt_prefetch(const PhaseGeom& g, const PhaseW& w, const PhaseCta& c,
                                             int t, int lane) {
   constexpr int RW = KIND == 0 ? 1 : 2;
@@ -249,33 +255,51 @@ __device__ __forceinline__ void wt_prefetch(const PhaseGeom& g, const PhaseW& w,
   const int rg = (int)(((unsigned long long)(unsigned)t * g.p_mul) >> 32);
   const int p = t - rg * g.P;
   const int v = lane >> 4, line = lane & 15;  // lanes 0-15: stream 0, 16-31: stream 1
-  const int rl = rg * RW + (KIND == 0 ? 0 : v);
-  if (rl >= c.rows || line * 128 >= g.B) return;
+  // with RS = 2 the stream is two whole rows (P == 1): lines 0-7 and 8-15
+  const int rl = (rg * RW + (KIND == 0 ? 0 : v)) * RS + (RS == 2 ? line * 128 / g.row_bytes : 0);
+  if (rl >= c.rows || line * 128 >= g.B * RS) return;
   const uint8_t* src = (KIND == 0 && v ? w.W1 : w.W0) + (size_t)(c.r_begin + rl) * g.row_bytes +
-                       (size_t)p * g.B + (size_t)line * 128;
+                       (size_t)p * g.B + (size_t)(RS == 2 ? line * 128 % g.row_bytes : line * 128);
   prefetch_l2_normal(src);
 }
 
 // Requests the weights of task t into buf (zeros for t >= T or rows past the
 // CTA's range).  Stream v of a task: matrix v of row rg (gate/up) or row
 // 2*rg + v (down); piece p of the row.
-template <int KIND>
+template <int KIND, int RS = 1>
 __device__ __forceinline__ void wt_load(const PhaseGeom& g, const PhaseW& w, const PhaseCta& c,
                                         int t, uint4 (&buf)[WT_NS][WT_CL], uint64_t pol,
                                         int lane) {
   constexpr int RW = KIND == 0 ? 1 : 2;
   const int rg = (int)(((unsigned long long)(unsigned)t * g.p_mul) >> 32);
   const int p = t - rg * g.P;
+  if constexpr (RS == 1) {
 #pragma unroll
-  for (int v = 0; v < WT_NS; ++v) {
-    const int rl = rg * RW + (KIND == 0 ? 0 : v);
-    const bool ok = t < c.T && rl < c.rows;
-    const uint8_t* src = (KIND == 0 && v ? w.W1 : w.W0) +
-                         (size_t)(c.r_begin + (ok ? rl : 0)) * g.row_bytes + (size_t)p * g.B;
+    for (int v = 0; v < WT_NS; ++v) {
+      const int rl = rg * RW + (KIND == 0 ? 0 : v);
+      const bool ok = t < c.T && rl < c.rows;
+      const uint8_t* src = (KIND == 0 && v ? w.W1 : w.W0) +
+                           (size_t)(c.r_begin + (ok ? rl : 0)) * g.row_bytes + (size_t)p * g.B;
 #pragma unroll
-    for (int k = 0; k < WT_CL; ++k) {
-      const int j = lane + 32 * k;
-      buf[v][k] = (ok && j < g.CPP) ? ldg_stream_pol(src + (size_t)j * 16, pol) : make_uint4(0, 0, 0, 0);
+      for (int k = 0; k < WT_CL; ++k) {
+        const int j = lane + 32 * k;
+        buf[v][k] = (ok && j < g.CPP) ? ldg_stream_pol(src + (size_t)j * 16, pol) : make_uint4(0, 0, 0, 0);
+      }
+    }
+  } else {
+    // RS = 2: stream v is rows rl, rl + 1 (whole rows of 64 chunks, contiguous);
+    // chunks k = 0, 1 of a lane belong to row rl and k = 2, 3 to row rl + 1
+#pragma unroll
+    for (int v = 0; v < WT_NS; ++v) {
+      const int rl = (rg * RW + (KIND == 0 ? 0 : v)) * 2;
+      const uint8_t* src = (KIND == 0 && v ? w.W1 : w.W0) + (size_t)c.r_begin * g.row_bytes;
+#pragma unroll
+      for (int k = 0; k < WT_CL; ++k) {
+        const int r = rl + (k >> 1);
+        const bool ok = t < c.T && r < c.rows;
+        buf[v][k] = ok ? ldg_stream_pol(src + (size_t)r * g.row_bytes + (size_t)(lane + 32 * (k & 1)) * 16, pol)
+                       : make_uint4(0, 0, 0, 0);
+      }
     }
   }
 }
@@ -411,9 +435,84 @@ __device__ __forceinline__ float cta_max(float v, float* red, int tid) {
   return m;
 }
 
+// wt_compute for RS = 2 (P == 1, rows of 64 chunks): stream v holds rows
+// r_v and r_v + 1, r_v = 2 (t * RW + v) for down and 2t (both matrices) for
+// gate/up; a lane's chunks k = 0, 1 (chunk lane + 32 k) are row r_v and
+// k = 2, 3 (chunk lane + 32 (k - 2)) row r_v + 1.  Each row's partial sum is
+// formed exactly as in wt_compute (the same chunk, group and lane order, the
+// same reduction), so it does not depend on whether the row is the first or
+// second of its stream, and is stored as its single piece.
+template <int FMT, int KIND>
+__device__ __forceinline__ void wt_compute_rs2(const PhaseGeom& g, const PhaseCta& c,
+                                               const PhaseSmem& sm, int t,
+                                               const uint4 (&buf)[WT_NS][WT_CL], int lane) {
+  using T = FmtTraits<FMT>;
+  constexpr int EPC = T::EPC;
+  constexpr bool AFF = T::AFFINE;
+  constexpr int NW = KIND == 0 ? 2 : 1;
+  constexpr int RW = KIND == 0 ? 1 : 2;
+  static_assert(WT_CL == 4, "two rows of two chunks per lane");
+  auto row_of = [&](int v, int r) { return (t * RW + (KIND == 0 ? 0 : v)) * 2 + r; };
+  float acc[WT_NS][2];
+#pragma unroll
+  for (int v = 0; v < WT_NS; ++v) acc[v][0] = acc[v][1] = 0.f;
+#pragma unroll
+  for (int k = 0; k < WT_CL; ++k) {
+    const int r = k >> 1, ch = lane + 32 * (k & 1);
+#pragma unroll
+    for (int v = 0; v < WT_NS; ++v) {
+      const float d = chunk_dot<FMT>(buf[v][k], sm.xs, ch, g.CPR);
+      if constexpr (AFF) {
+        const int m = KIND == 0 ? v : 0, rl = min(row_of(v, r), c.rows - 1);
+        const int gi = (ch * EPC) >> g.lg_group;
+        acc[v][r] = fmaf(bf16f(sm.sbr[(size_t)(2 * m) * g.sb_stride + rl * g.G + gi]), d, acc[v][r]);
+      } else {
+        acc[v][r] += d;
+      }
+    }
+  }
+  float vals[WT_NS][2];
+#pragma unroll
+  for (int v = 0; v < WT_NS; ++v)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) vals[v][r] = AFF ? acc[v][r] * sm.xinv[0] : acc[v][r];
+  if constexpr (AFF) {
+    // bias terms: sum_g b_g * X_g over each row's groups, group g on lane
+    // g mod 32 for both rows, as in wt_compute, so a row's sum does not depend
+    // on its place in the stream (the partition of rows over CTAs may differ)
+    for (int gi = lane; gi < g.G; gi += 32) {
+      const float xg = sm.gsum[gi];
+#pragma unroll
+      for (int v = 0; v < WT_NS; ++v)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int m = KIND == 0 ? v : 0, rl = min(row_of(v, r), c.rows - 1);
+          vals[v][r] = fmaf(bf16f(sm.sbr[(size_t)(2 * m + 1) * g.sb_stride + rl * g.G + gi]), xg, vals[v][r]);
+        }
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < WT_NS; ++v)
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) vals[v][r] += __shfl_xor_sync(0xffffffffu, vals[v][r], off);
+  if (lane < 2 * WT_NS) {
+    const int v = lane >> 1, r = lane & 1;
+    float val = vals[0][0];
+#pragma unroll
+    for (int vv = 0; vv < WT_NS; ++vv)
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr)
+        if (lane == 2 * vv + rr) val = vals[vv][rr];
+    const int m = KIND == 0 ? v : 0, rl = row_of(v, r);
+    if (rl < c.rows) sm.parts[(size_t)rl * NW + m] = val;
+  }
+}
+
 // Computes task t from the weights in buf and stores its partial sums (one
 // per stream) in sm.parts.
-template <int FMT, int KIND>
+template <int FMT, int KIND, int RS = 1>
 __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c,
                                            const PhaseSmem& sm, int t,
                                            const uint4 (&buf)[WT_NS][WT_CL], int lane) {
@@ -422,6 +521,10 @@ __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c
   constexpr bool AFF = T::AFFINE;
   constexpr int NW = KIND == 0 ? 2 : 1;
   constexpr int RW = KIND == 0 ? 1 : 2;
+  if constexpr (RS == 2) {
+    wt_compute_rs2<FMT, KIND>(g, c, sm, t, buf, lane);
+    return;
+  }
   const int rg = (int)(((unsigned long long)(unsigned)t * g.p_mul) >> 32);
   const int p = t - rg * g.P;
   const int rl0 = rg * RW;
@@ -480,7 +583,7 @@ __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c
 // (wt_prefetch); task_ctr (shared) hands out the next task numbers.  Register
 // ping-pong: one task is in flight while the other is computed; two tasks per
 // iteration keep the buffer indices static.
-template <int FMT, int KIND>
+template <int FMT, int KIND, int RS = 1>
 __device__ __forceinline__ void wt_run(const PhaseGeom& g, const PhaseW& w, const PhaseCta& c,
                                        const PhaseSmem& sm, uint4 (&bufA)[WT_NS][WT_CL],
                                        uint4 (&bufB)[WT_NS][WT_CL], int tA, int tB, int* task_ctr,
@@ -493,15 +596,15 @@ __device__ __forceinline__ void wt_run(const PhaseGeom& g, const PhaseW& w, cons
   constexpr int AHEAD = 2 * WARP_TASK_WARPS;  // L2 lookahead in tasks
   for (;;) {
     if (tA >= c.T) break;  // tA < tB here
-    wt_compute<FMT, KIND>(g, c, sm, tA, bufA, lane);
+    wt_compute<FMT, KIND, RS>(g, c, sm, tA, bufA, lane);
     tA = next_task();
-    wt_load<KIND>(g, w, c, tA, bufA, pol, lane);
-    wt_prefetch<KIND>(g, w, c, tA + AHEAD, lane);
+    wt_load<KIND, RS>(g, w, c, tA, bufA, pol, lane);
+    wt_prefetch<KIND, RS>(g, w, c, tA + AHEAD, lane);
     if (tB >= c.T) break;  // tB < tA here
-    wt_compute<FMT, KIND>(g, c, sm, tB, bufB, lane);
+    wt_compute<FMT, KIND, RS>(g, c, sm, tB, bufB, lane);
     tB = next_task();
-    wt_load<KIND>(g, w, c, tB, bufB, pol, lane);
-    wt_prefetch<KIND>(g, w, c, tB + AHEAD, lane);
+    wt_load<KIND, RS>(g, w, c, tB, bufB, pol, lane);
+    wt_prefetch<KIND, RS>(g, w, c, tB + AHEAD, lane);
   }
 }
 
@@ -524,7 +627,7 @@ __device__ __forceinline__ float row_total(const PhaseGeom& g, const float* part
 // than x (phase_tail_bytes).
 template <int FMT, int KIND>
 bool plan_phase(int K, int N, int group, int grid, PhaseGeom* out, size_t* smem_parts,
-                int row_unit = 1) {
+                int row_unit = 1, int max_rs = 2) {
   using T = FmtTraits<FMT>;
   constexpr int EPC = T::EPC;
   constexpr bool AFF = T::AFFINE;
@@ -544,6 +647,7 @@ bool plan_phase(int K, int N, int group, int grid, PhaseGeom* out, size_t* smem_
   }
   if (P == 0 || grid < 1 || row_unit < 1 || N % row_unit) return false;
   g.P = P;
+  g.RS = (max_rs >= 2 && P == 1 && g.CPR == 16 * WT_CL) ? 2 : 1;
   g.p_mul = ((1ull << 32) + (unsigned long long)P - 1) / (unsigned long long)P;
   g.B = g.row_bytes / P;
   g.CPP = g.CPR / P;

@@ -154,7 +154,9 @@ __device__ __forceinline__ float cta_sum(float v, float* red, int tid) {
 
 __device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
 
-template <int FMT>
+// RSG: rows per load stream of the gate/up phase (a.gu.RS); the down phase
+// always has one.
+template <int FMT, int RSG>
 __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArgs a) {
   constexpr bool AFF = FmtTraits<FMT>::AFFINE;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -177,7 +179,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
   uint16_t* wn = reinterpret_cast<uint16_t*>(smem + a.off_wn);    // [d] RMSNorm gain
   uint16_t* ssm = reinterpret_cast<uint16_t*>(smem + a.off_ssm);  // [d] summed_l
 
-  const PhaseCta cg = phase_cta<0>(a.gu, cta);
+  const PhaseCta cg = phase_cta<0, RSG>(a.gu, cta);
   const PhaseCta cd = phase_cta<1>(a.dn, cta);
   const uint64_t pol = l2_evict_first_policy();
   uint4 bufA[WT_NS][WT_CL], bufB[WT_NS][WT_CL];
@@ -339,10 +341,10 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       // in flight while x is staged (shared memory only)
       {
         const PhaseW w = gateup_w(Ly);
-        wt_load<0>(a.gu, w, cg, tA, bufA, pol, lane);
-        wt_load<0>(a.gu, w, cg, tB, bufB, pol, lane);
-        wt_prefetch<0>(a.gu, w, cg, tA + 2 * WARP_TASK_WARPS, lane);
-        wt_prefetch<0>(a.gu, w, cg, tB + 2 * WARP_TASK_WARPS, lane);
+        wt_load<0, RSG>(a.gu, w, cg, tA, bufA, pol, lane);
+        wt_load<0, RSG>(a.gu, w, cg, tB, bufB, pol, lane);
+        wt_prefetch<0, RSG>(a.gu, w, cg, tA + 2 * WARP_TASK_WARPS, lane);
+        wt_prefetch<0, RSG>(a.gu, w, cg, tB + 2 * WARP_TASK_WARPS, lane);
       }
       // one staging pass with the vector's fixed-point scale
       int ex = 0;
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
     }
     // ---- gate/up with the SwiGLU epilogue; h rows published in pairs
     {
-      wt_run<FMT, 0>(a.gu, gateup_w(Ly), cg, smG, bufA, bufB, tA, tB, &task_ctr, pol, lane);
+      wt_run<FMT, 0, RSG>(a.gu, gateup_w(Ly), cg, smG, bufA, bufB, tA, tB, &task_ctr, pol, lane);
       __syncthreads();
       prefetch_down(l);  // HBM keeps streaming through the hand-off
       float hm = 0.f;
@@ -477,7 +479,7 @@ struct StackPlanImpl {
   void* alloc;          // device allocation owned by the plan
   void* run_state;      // what is zeroed before each run (the control line)
   size_t run_state_bytes;
-  const void* kernel;   // mlp_stack_kernel<FMT>
+  const void* kernel;   // mlp_stack_kernel<FMT, RSG>
 };
 
 template <int FMT>
@@ -488,7 +490,7 @@ static bool plan_stack(StackPlanImpl* P, const DeviceInfo* di) {
   StackArgs& a = P->base;
   // rows in pairs: every published word has one writer
   if (!plan_phase<FMT, 0>(P->d, P->f, P->group, grid, &a.gu, &pg, 2)) return false;
-  if (!plan_phase<FMT, 1>(P->f, P->d, P->group, grid, &a.dn, &pd, 2)) return false;
+  if (!plan_phase<FMT, 1>(P->f, P->d, P->group, grid, &a.dn, &pd, 2, 1)) return false;
   if (a.dn.rows_alloc > 2 * WT_THREADS) return false;  // one pair of down rows per thread
   const int Kmax = P->d > P->f ? P->d : P->f;
   size_t off = (size_t)Kmax * 2;  // xraw
@@ -499,7 +501,8 @@ static bool plan_stack(StackPlanImpl* P, const DeviceInfo* di) {
   a.off_ssm = (int)off; off += (size_t)P->d * 2;
   P->smem = off;
   P->grid = grid;
-  P->kernel = reinterpret_cast<const void*>(mlp_stack_kernel<FMT>);
+  P->kernel = a.gu.RS == 2 ? reinterpret_cast<const void*>(mlp_stack_kernel<FMT, 2>)
+                           : reinterpret_cast<const void*>(mlp_stack_kernel<FMT, 1>);
   return true;
 }
 

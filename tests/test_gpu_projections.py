@@ -56,6 +56,11 @@ SHAPES = [  # (fmt, group, M, K, N)
     (1, 128, 1, 512, 20000),    # long vocabulary-like row range per CTA
     (2, 128, 2, 768, 4999),
     (1, 64, 7, 256, 153),
+    # one row: rows of 64 chunks, two rows per load stream (odd N: a last task with one row)
+    (1, 64, 1, 1024, 1001),
+    (2, 128, 1, 2048, 1337),
+    (2, 32, 1, 2048, 153),
+    (0, 0, 1, 512, 999),
 ]
 
 

@@ -76,6 +76,9 @@ SMALL = [
     synth.TINY.with_(wid=13, name="stack d1024 f2816 affine8 g128", d=1024, f=2816, group=128,
                      eps=1e-6, layers=2),
     synth.TINY.with_(wid=14, name="stack d96 f224 affine8 g32", d=96, f=224, group=32, layers=2),
+    # gate/up rows of 64 chunks (two rows per load stream), down rows of 32
+    synth.TINY.with_(wid=15, name="stack d2048 f1024 affine4 g128", d=2048, f=1024,
+                     fmt=synth.FMT_AFFINE4, group=128, eps=1e-6, layers=2),
 ]
 
 

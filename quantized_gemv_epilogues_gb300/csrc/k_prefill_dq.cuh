@@ -42,23 +42,30 @@ constexpr int PQ_AHEAD = 4;                                // K blocks of scales
 
 // Shared-memory plan: ring X (x tiles, TMA), ring C (code tiles, TMA),
 // ring B (fp16 A tiles, written by the dequantising warps, read by the MMA).
-template <int FMT, int KIND, int NT>
+// NA: 128-row A sub-tiles per tile, each with its own accumulator of NT
+// columns; NA = 2 (with NT = 256) makes one x tile feed twice the MMAs, which
+// halves the K-block overhead (waits, commits, TMA latency) per flop.
+template <int FMT, int KIND, int NT, int NA = 1>
 struct PqShape {
+  static_assert(NA == 1 || (NA == 2 && NT == 256), "wide tiles take 256 activation rows");
   static constexpr int XT = NT * PF_KB * 2;
-  static constexpr int FT = KIND == 0 ? 64 : 128;
+  static constexpr int FT = (KIND == 0 ? 64 : 128) * NA;  // output rows (gate/up: of h) per tile
   static constexpr int CB = FmtTraits<FMT>::EPW == 4 ? 64 : 32;
-  static constexpr int CTILE = PF_ROWS * CB;
-  static constexpr int SX = NT == 256 ? 4 : (NT == 128 ? 6 : 8);
+  static constexpr int CTILE = PF_ROWS * NA * CB;
+  static constexpr int BTILE = PF_W_TILE * NA;             // one ring-B slot: NA sub-tiles
+  static constexpr int SX = NA == 2 ? 3 : (NT == 256 ? 4 : (NT == 128 ? 6 : 8));
   static constexpr bool BFW = FMT == FMT_BF16;  // dense bf16 weights: no code ring (TMA fills ring B)
-  static constexpr int SB = BFW ? (NT == 256 ? 5 : 6) : (NT == 256 ? 3 : 4);
-  static constexpr int SC0 = (217 * 1024 - SX * XT - SB * PF_W_TILE) / CTILE;
+  static constexpr int SB = NA == 2 ? (BFW ? 3 : 2) : (BFW ? (NT == 256 ? 5 : 6) : (NT == 256 ? 3 : 4));
+  static constexpr int SC0 = (217 * 1024 - SX * XT - SB * BTILE) / CTILE;
   static constexpr int SC = BFW ? 1 : (SC0 > 8 ? 8 : SC0);
   static constexpr size_t OFF_C = (size_t)SX * XT;
   static constexpr size_t OFF_B = OFF_C + (size_t)SC * CTILE;
-  static constexpr size_t SMEM = 1024 + OFF_B + (size_t)SB * PF_W_TILE;
-  // the final phase reuses the rings: gate/up the gate and up sums
+  static constexpr size_t SMEM = 1024 + OFF_B + (size_t)SB * BTILE;
+  // the final phase reuses the rings: narrow gate/up the gate and up sums
   // [NT][64] fp32 each and the bf16 tile [NT][64]; otherwise the bf16 tile
-  static constexpr size_t FINAL = KIND == 0 ? (size_t)NT * 64 * 4 * 2 + (size_t)NT * 64 * 2 : (size_t)NT * 128 * 2;
+  // [NT][FT]
+  static constexpr size_t FINAL = (KIND == 0 && NA == 1) ? (size_t)NT * 64 * 4 * 2 + (size_t)NT * 64 * 2
+                                                         : (size_t)NT * FT * 2;
   static_assert(BFW || SC >= 2, "code ring");
   static_assert(SMEM <= 218 * 1024, "shared memory plan");
   static_assert(FINAL + 1024 <= SMEM, "final-phase buffers in the rings");
@@ -128,12 +135,13 @@ __device__ __forceinline__ uint4 pq_chunk4(uint32_t w, float s, float c) {
   return pq_chunk8(a, b, s, c);
 }
 
-template <int FMT, int KIND, int NT>
+template <int FMT, int KIND, int NT, int NA>
 __global__ void __launch_bounds__(PQ_THREADS, 1)
     prefill_dq_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap0,
                       const __grid_constant__ CUtensorMap wmap1, const __grid_constant__ CUtensorMap omap,
                       const PrefillArgs a) {
-  using SH = PqShape<FMT, KIND, NT>;
+  using SH = PqShape<FMT, KIND, NT, NA>;
+  constexpr uint32_t TCOLS = (uint32_t)(NT * NA);  // tensor-memory columns: NA accumulators
   constexpr int SX = SH::SX, SC = SH::SC, SB = SH::SB, FT = SH::FT, CB = SH::CB;
   constexpr int EPI = 32 * PQ_CONV_WARPS;    // dequantising / epilogue threads
   constexpr int HALF = NT / 2;               // accumulator columns per epilogue warpgroup
@@ -162,7 +170,7 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
   const uint32_t acc_full = smem_u32(&bars[2 * (SX + SC + SB)]);
   auto xslot = [&](int i) { return smem + (size_t)i * SH::XT; };
   auto cslot = [&](int i) { return smem + SH::OFF_C + (size_t)i * SH::CTILE; };
-  auto wslot = [&](int i) { return smem + SH::OFF_B + (size_t)i * PF_W_TILE; };
+  auto wslot = [&](int i) { return smem + SH::OFF_B + (size_t)i * SH::BTILE; };
 
   if (tid == 0) {
     for (int i = 0; i < SX; ++i) {
@@ -183,7 +191,7 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
   }
   if (warp == MMA_WARP) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_sh)),
-                 "r"((uint32_t)NT));
+                 "r"(TCOLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
@@ -213,13 +221,14 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
           mbar_arrive_expect_tx(full, SH::XT);
           tma_load_2d(smem_u32(xslot(i)), &xmap, kg * PF_KB, m0, full);
         } else if constexpr (BFW) {
-          mbar_arrive_expect_tx(full, PF_W_TILE);
+          // gate/up: FT rows of each matrix, the up rows after the gate rows
+          mbar_arrive_expect_tx(full, SH::BTILE);
           tma_load_2d(smem_u32(wslot(i)), &wmap0, kg * PF_KB, f0, full);
-          if constexpr (KIND == 0) tma_load_2d(smem_u32(wslot(i) + 64 * 128), &wmap1, kg * PF_KB, f0, full);
+          if constexpr (KIND == 0) tma_load_2d(smem_u32(wslot(i) + FT * 128), &wmap1, kg * PF_KB, f0, full);
         } else {
           mbar_arrive_expect_tx(full, SH::CTILE);
           tma_load_2d(smem_u32(cslot(i)), &wmap0, kg * CB, f0, full);
-          if constexpr (KIND == 0) tma_load_2d(smem_u32(cslot(i) + 64 * CB), &wmap1, kg * CB, f0, full);
+          if constexpr (KIND == 0) tma_load_2d(smem_u32(cslot(i) + FT * CB), &wmap1, kg * CB, f0, full);
         }
         ++issued;
       }
@@ -240,10 +249,14 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
       }
       tc_fence_after();
       const uint64_t xd = pf_desc_sw128(smem_u32(xslot(i)));
-      const uint64_t wd = pf_desc_sw128(smem_u32(wslot(jb)));
       if (elect_one()) {
 #pragma unroll
-        for (int j = 0; j < PF_KB / 16; ++j) tc_mma<NT, BFW>(tbase, wd + 2 * j, xd + 2 * j, (kb | j) ? 1u : 0u);
+        for (int sa = 0; sa < NA; ++sa) {  // sub-tile sa: A rows 128 sa .. 128 sa + 127, accumulator sa
+          const uint64_t wd = pf_desc_sw128(smem_u32(wslot(jb) + sa * PF_W_TILE));
+#pragma unroll
+          for (int j = 0; j < PF_KB / 16; ++j)
+            tc_mma<NT, BFW>(tbase + (uint32_t)(sa * NT), wd + 2 * j, xd + 2 * j, (kb | j) ? 1u : 0u);
+        }
         tc_commit(b_free(jb));
         tc_commit(x_free(i));
       }
@@ -256,29 +269,44 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
     __syncwarp();
     (void)mbar_wait_bounded(acc_full, 0);
   } else {
-    // ---- dequantising warps, then the epilogue.  Thread (r, h): weight row r
-    // of the tile (tensor-memory lane r), codes [32 h, 32 h + 32) of each K
-    // block, and accumulator columns [h * NT / 2, (h + 1) * NT / 2).
+    // ---- dequantising warps, then the epilogue.  Thread (r, h): row r of
+    // each A sub-tile sa (tensor-memory lane r; tile row 128 sa + r), codes
+    // [32 h, 32 h + 32) of each K block, and accumulator columns
+    // [h * NT / 2, (h + 1) * NT / 2).  Narrow gate/up tiles stack 64 gate rows
+    // over the same 64 up rows; wide ones put 128 gate rows in sub-tile 0 and
+    // the same 128 up rows in sub-tile 1.
     const int r = tid & 127, h = tid >> 7;
-    const int mat = (KIND == 0 && r >= 64) ? 1 : 0;
-    const int n = f0 + (KIND == 0 ? (r & 63) : r);
-    const bool okr = n < a.N;
-    const uint16_t* sp = (mat ? a.s1 : a.s0) + (size_t)(okr ? n : 0) * a.G;
-    const uint16_t* bp = (mat ? a.b1 : a.b0) + (size_t)(okr ? n : 0) * a.G;
-    const float tsc = (okr && !BFW) ? a.tsc[(size_t)mat * a.N + n] : 0.f;
-    // raw bf16 scale and bias of this thread's group in K block kb of the slice
-    auto raw_s = [&](int kb) -> uint32_t {
-      return (okr && !BFW && kb < KB) ? (uint32_t)__ldg(sp + (((kb0 + kb) * PF_KB + 32 * h) >> a.lg_group)) : 0u;
-    };
-    auto raw_b = [&](int kb) -> uint32_t {
-      return (okr && !BFW && kb < KB) ? (uint32_t)__ldg(bp + (((kb0 + kb) * PF_KB + 32 * h) >> a.lg_group)) : 0u;
-    };
-    uint32_t sq[PQ_AHEAD], bq[PQ_AHEAD];
+    int mat[NA], n[NA];
+    bool okr[NA];
+    const uint16_t* sp[NA];
+    const uint16_t* bp[NA];
+    float tsc[NA];
 #pragma unroll
-    for (int u = 0; u < PQ_AHEAD; ++u) {
-      sq[u] = raw_s(u);
-      bq[u] = raw_b(u);
+    for (int sa = 0; sa < NA; ++sa) {
+      mat[sa] = KIND == 0 ? (NA == 2 ? sa : (r >= 64 ? 1 : 0)) : 0;
+      n[sa] = f0 + (KIND == 0 ? (NA == 2 ? r : (r & 63)) : 128 * sa + r);
+      okr[sa] = n[sa] < a.N;
+      sp[sa] = (mat[sa] ? a.s1 : a.s0) + (size_t)(okr[sa] ? n[sa] : 0) * a.G;
+      bp[sa] = (mat[sa] ? a.b1 : a.b0) + (size_t)(okr[sa] ? n[sa] : 0) * a.G;
+      tsc[sa] = (okr[sa] && !BFW) ? a.tsc[(size_t)mat[sa] * a.N + n[sa]] : 0.f;
     }
+    // raw bf16 scale and bias of sub-tile sa's group in K block kb of the slice
+    auto raw_s = [&](int sa, int kb) -> uint32_t {
+      return (okr[sa] && !BFW && kb < KB) ? (uint32_t)__ldg(sp[sa] + (((kb0 + kb) * PF_KB + 32 * h) >> a.lg_group))
+                                          : 0u;
+    };
+    auto raw_b = [&](int sa, int kb) -> uint32_t {
+      return (okr[sa] && !BFW && kb < KB) ? (uint32_t)__ldg(bp[sa] + (((kb0 + kb) * PF_KB + 32 * h) >> a.lg_group))
+                                          : 0u;
+    };
+    uint32_t sq[NA][PQ_AHEAD], bq[NA][PQ_AHEAD];
+#pragma unroll
+    for (int sa = 0; sa < NA; ++sa)
+#pragma unroll
+      for (int u = 0; u < PQ_AHEAD; ++u) {
+        sq[sa][u] = raw_s(sa, u);
+        bq[sa][u] = raw_b(sa, u);
+      }
     bool ok = true;
     for (int kbu = 0; kbu < (BFW ? 0 : KB) && ok; kbu += PQ_AHEAD) {
 #pragma unroll
@@ -286,9 +314,14 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
         const int kb = kbu + u;
         if (kb >= KB) break;
         const int i = kb % SC, j = kb % SB;
-        const float s = bf16f((uint16_t)sq[u]) * tsc, c = bf16f((uint16_t)bq[u]) * tsc;
-        sq[u] = raw_s(kb + PQ_AHEAD);
-        bq[u] = raw_b(kb + PQ_AHEAD);
+        float sv[NA], cv[NA];
+#pragma unroll
+        for (int sa = 0; sa < NA; ++sa) {
+          sv[sa] = bf16f((uint16_t)sq[sa][u]) * tsc[sa];
+          cv[sa] = bf16f((uint16_t)bq[sa][u]) * tsc[sa];
+          sq[sa][u] = raw_s(sa, kb + PQ_AHEAD);
+          bq[sa][u] = raw_b(sa, kb + PQ_AHEAD);
+        }
         bool w = mbar_wait_bounded(c_full(i), (kb / SC) & 1);
         if (w && kb >= SB) w = mbar_wait_bounded(b_free(j), ((kb / SB) + 1) & 1);
         if (!__all_sync(0xffffffffu, w)) {
@@ -297,25 +330,30 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
           break;
         }
         const unsigned char* ct = cslot(i);
-        uint4 o[4];
-        if constexpr (W8) {  // chunks 2h, 2h+1 of the 64-byte code row (64-byte swizzle)
-          const int swc = (r >> 1) & 3;
-          const uint4 v0 = *reinterpret_cast<const uint4*>(ct + r * 64 + (((2 * h) ^ swc) << 4));
-          const uint4 v1 = *reinterpret_cast<const uint4*>(ct + r * 64 + (((2 * h + 1) ^ swc) << 4));
-          o[0] = pq_chunk8(v0.x, v0.y, s, c);
-          o[1] = pq_chunk8(v0.z, v0.w, s, c);
-          o[2] = pq_chunk8(v1.x, v1.y, s, c);
-          o[3] = pq_chunk8(v1.z, v1.w, s, c);
-        } else {  // chunk h of the 32-byte code row (32-byte swizzle)
-          const uint4 v = *reinterpret_cast<const uint4*>(ct + r * 32 + ((h ^ ((r >> 2) & 1)) << 4));
-          o[0] = pq_chunk4(v.x, s, c);
-          o[1] = pq_chunk4(v.y, s, c);
-          o[2] = pq_chunk4(v.z, s, c);
-          o[3] = pq_chunk4(v.w, s, c);
-        }
-        unsigned char* rowp = wslot(j) + r * 128;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(rowp + (((4 * h + k) ^ (r & 7)) << 4)) = o[k];
+        for (int sa = 0; sa < NA; ++sa) {
+          const int R = 128 * sa + r;  // row of the code tile
+          const float s_ = sv[sa], c_ = cv[sa];
+          uint4 o[4];
+          if constexpr (W8) {  // chunks 2h, 2h+1 of the 64-byte code row (64-byte swizzle)
+            const int swc = (R >> 1) & 3;
+            const uint4 v0 = *reinterpret_cast<const uint4*>(ct + R * 64 + (((2 * h) ^ swc) << 4));
+            const uint4 v1 = *reinterpret_cast<const uint4*>(ct + R * 64 + (((2 * h + 1) ^ swc) << 4));
+            o[0] = pq_chunk8(v0.x, v0.y, s_, c_);
+            o[1] = pq_chunk8(v0.z, v0.w, s_, c_);
+            o[2] = pq_chunk8(v1.x, v1.y, s_, c_);
+            o[3] = pq_chunk8(v1.z, v1.w, s_, c_);
+          } else {  // chunk h of the 32-byte code row (32-byte swizzle)
+            const uint4 v = *reinterpret_cast<const uint4*>(ct + R * 32 + ((h ^ ((R >> 2) & 1)) << 4));
+            o[0] = pq_chunk4(v.x, s_, c_);
+            o[1] = pq_chunk4(v.y, s_, c_);
+            o[2] = pq_chunk4(v.z, s_, c_);
+            o[3] = pq_chunk4(v.w, s_, c_);
+          }
+          unsigned char* rowp = wslot(j) + sa * PF_W_TILE + r * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(rowp + (((4 * h + k) ^ (r & 7)) << 4)) = o[k];
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor core reads
         __syncwarp();
         if (lane == 0) {  // one arrival per warp
@@ -351,90 +389,184 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
       tc_fence_after();
       const int wg = h, cbase = wg * HALF;
       const uint32_t lane_base = tbase + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)cbase;
-      const float ti = !okr ? 0.f : (BFW ? 1.0f : a.tinv[(size_t)mat * a.N + n]);
-      const float* ei = einv_sh + cbase;
-      constexpr int NW = KIND == 0 ? 2 : 1;
-      if (a.ks > 1) {
-        // split K: this slice's sums of the tile, before any scaling
-        // (every lane takes part in the warp-wide tensor-memory loads; only
-        // rows inside the tensor store)
-        float* pp = a.part + ((size_t)(sk * NW + mat) * a.Mp + m0 + cbase) * a.N + (okr ? n : 0);
+      if constexpr (NA == 1) {
+        const float ti = !okr[0] ? 0.f : (BFW ? 1.0f : a.tinv[(size_t)mat[0] * a.N + n[0]]);
+        const float* ei = einv_sh + cbase;
+        constexpr int NW = KIND == 0 ? 2 : 1;
+        if (a.ks > 1) {
+          // split K: this slice's sums of the tile, before any scaling
+          // (every lane takes part in the warp-wide tensor-memory loads; only
+          // rows inside the tensor store)
+          float* pp = a.part + ((size_t)(sk * NW + mat[0]) * a.Mp + m0 + cbase) * a.N + (okr[0] ? n[0] : 0);
 #pragma unroll 1
-        for (int q = 0; q < HALF / 16; ++q) {
-          float d[16];
-          tc_ld16_wait(lane_base + (uint32_t)(q * 16), d);
-          if (okr) {
+          for (int q = 0; q < HALF / 16; ++q) {
+            float d[16];
+            tc_ld16_wait(lane_base + (uint32_t)(q * 16), d);
+            if (okr[0]) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) st_global_f32(pp + (size_t)(q * 16 + e) * a.N, d[e]);
-          }
-        }
-      } else if constexpr (KIND == 0) {
-        // gate and up sums [NT][64] each in shared memory, then silu(gate) * up
-        // over the whole tile by all 256 threads
-        float* gsh = reinterpret_cast<float*>(smem);
-        float* ush = gsh + NT * 64;
-        uint16_t* stg = reinterpret_cast<uint16_t*>(ush + NT * 64);
-        float* dst = (mat ? ush : gsh) + (r & 63);
-#pragma unroll 1
-        for (int q = 0; q < HALF / 16; ++q) {
-          float d[16];
-          tc_ld16_wait(lane_base + (uint32_t)(q * 16), d);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) dst[(cbase + q * 16 + e) * 64] = d[e] * ti * ei[q * 16 + e];
-        }
-        epi_sync();
-#pragma unroll 4
-        for (int idx = tid; idx < NT * 64; idx += EPI) {
-          const int col = idx >> 6, f = idx & 63;
-          const float g = gsh[idx], hv = g / (1.0f + __expf(-g)) * ush[idx];  // silu(gate) * up
-          if (a.tma_store) {
-            stg[idx] = f2bf(hv);
-          } else if (m0 + col < a.M && f0 + f < a.N) {
-            const size_t o = (size_t)(m0 + col) * a.N + f0 + f;
-            if (a.out_f32)
-              st_global_f32(static_cast<float*>(a.out) + o, hv);
-            else
-              st_global_bf16(static_cast<uint16_t*>(a.out) + o, hv);
-          }
-        }
-        if (a.tma_store) {
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // tile writes -> TMA reads
-          epi_sync();
-          if (tid == 0) tma_store_2d_wait(&omap, f0, m0, smem_u32(stg));
-        }
-      } else {
-        // down / projection: + residual or bias, 16 columns at a time
-        uint16_t* stg = reinterpret_cast<uint16_t*>(smem);  // [NT][128] bf16
-        const uint16_t* __restrict__ res = a.res;
-        const int jmax = min(HALF, a.M - m0 - cbase);
-        const size_t obase = (size_t)(m0 + cbase) * a.N + n;
-#pragma unroll 1
-        for (int q = 0; q < HALF / 16; ++q) {
-          float add[16], d[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int jj = q * 16 + e;
-            add[e] = (res && okr && jj < jmax) ? bf16f(__ldg(res + (size_t)(m0 + cbase + jj) * a.res_ld + n)) : 0.f;
-          }
-          tc_ld16_wait(lane_base + (uint32_t)(q * 16), d);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int jj = q * 16 + e;
-            const float v = d[e] * ti * ei[jj] + add[e];
-            if (a.tma_store) {
-              stg[(cbase + jj) * FT + r] = f2bf(v);
-            } else if (okr && jj < jmax) {
-              if (a.out_f32)
-                st_global_f32(static_cast<float*>(a.out) + obase + (size_t)jj * a.N, v);
-              else
-                st_global_bf16(static_cast<uint16_t*>(a.out) + obase + (size_t)jj * a.N, v);
+              for (int e = 0; e < 16; ++e) st_global_f32(pp + (size_t)(q * 16 + e) * a.N, d[e]);
             }
           }
-        }
-        if (a.tma_store) {
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        } else if constexpr (KIND == 0) {
+          // gate and up sums [NT][64] each in shared memory, then silu(gate) * up
+          // over the whole tile by all 256 threads
+          float* gsh = reinterpret_cast<float*>(smem);
+          float* ush = gsh + NT * 64;
+          uint16_t* stg = reinterpret_cast<uint16_t*>(ush + NT * 64);
+          float* dst = (mat[0] ? ush : gsh) + (r & 63);
+#pragma unroll 1
+          for (int q = 0; q < HALF / 16; ++q) {
+            float d[16];
+            tc_ld16_wait(lane_base + (uint32_t)(q * 16), d);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) dst[(cbase + q * 16 + e) * 64] = d[e] * ti * ei[q * 16 + e];
+          }
           epi_sync();
-          if (tid == 0) tma_store_2d_wait(&omap, f0, m0, smem_u32(stg));
+#pragma unroll 4
+          for (int idx = tid; idx < NT * 64; idx += EPI) {
+            const int col = idx >> 6, f = idx & 63;
+            const float g = gsh[idx], hv = g / (1.0f + __expf(-g)) * ush[idx];  // silu(gate) * up
+            if (a.tma_store) {
+              stg[idx] = f2bf(hv);
+            } else if (m0 + col < a.M && f0 + f < a.N) {
+              const size_t o = (size_t)(m0 + col) * a.N + f0 + f;
+              if (a.out_f32)
+                st_global_f32(static_cast<float*>(a.out) + o, hv);
+              else
+                st_global_bf16(static_cast<uint16_t*>(a.out) + o, hv);
+            }
+          }
+          if (a.tma_store) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // tile writes -> TMA reads
+            epi_sync();
+            if (tid == 0) tma_store_2d_wait(&omap, f0, m0, smem_u32(stg));
+          }
+        } else {
+          // down / projection: + residual or bias, 16 columns at a time
+          uint16_t* stg = reinterpret_cast<uint16_t*>(smem);  // [NT][128] bf16
+          const uint16_t* __restrict__ res = a.res;
+          const int jmax = min(HALF, a.M - m0 - cbase);
+          const size_t obase = (size_t)(m0 + cbase) * a.N + n[0];
+#pragma unroll 1
+          for (int q = 0; q < HALF / 16; ++q) {
+            float add[16], d[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int jj = q * 16 + e;
+              add[e] = (res && okr[0] && jj < jmax) ? bf16f(__ldg(res + (size_t)(m0 + cbase + jj) * a.res_ld + n[0])) : 0.f;
+            }
+            tc_ld16_wait(lane_base + (uint32_t)(q * 16), d);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int jj = q * 16 + e;
+              const float v = d[e] * ti * ei[jj] + add[e];
+              if (a.tma_store) {
+                stg[(cbase + jj) * FT + r] = f2bf(v);
+              } else if (okr[0] && jj < jmax) {
+                if (a.out_f32)
+                  st_global_f32(static_cast<float*>(a.out) + obase + (size_t)jj * a.N, v);
+                else
+                  st_global_bf16(static_cast<uint16_t*>(a.out) + obase + (size_t)jj * a.N, v);
+              }
+            }
+          }
+          if (a.tma_store) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            epi_sync();
+            if (tid == 0) tma_store_2d_wait(&omap, f0, m0, smem_u32(stg));
+          }
+        }
+      } else {
+        // wide tile: accumulator sa (columns sa * NT ...) holds sub-tile sa
+        const float* ei = einv_sh + cbase;
+        constexpr int NW = KIND == 0 ? 2 : 1;
+        float ti[NA];
+#pragma unroll
+        for (int sa = 0; sa < NA; ++sa) ti[sa] = !okr[sa] ? 0.f : (BFW ? 1.0f : a.tinv[(size_t)mat[sa] * a.N + n[sa]]);
+        if (a.ks > 1) {
+          // split K: this slice's sums of the tile, before any scaling
+#pragma unroll
+          for (int sa = 0; sa < NA; ++sa) {
+            float* pp = a.part + ((size_t)(sk * NW + mat[sa]) * a.Mp + m0 + cbase) * a.N + (okr[sa] ? n[sa] : 0);
+#pragma unroll 1
+            for (int q = 0; q < HALF / 16; ++q) {
+              float d[16];
+              tc_ld16_wait(lane_base + (uint32_t)(sa * NT + q * 16), d);
+              if (okr[sa]) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) st_global_f32(pp + (size_t)(q * 16 + e) * a.N, d[e]);
+              }
+            }
+          }
+        } else if constexpr (KIND == 0) {
+          // gate (accumulator 0) and up (accumulator 1) of the same row n:
+          // silu(gate) * up in registers, into the bf16 tile [NT][FT]
+          uint16_t* stg = reinterpret_cast<uint16_t*>(smem);
+#pragma unroll 1
+          for (int q = 0; q < HALF / 16; ++q) {
+            float dg[16], du[16];
+            tc_ld16_wait(lane_base + (uint32_t)(q * 16), dg);
+            tc_ld16_wait(lane_base + (uint32_t)(NT + q * 16), du);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int col = cbase + q * 16 + e;
+              const float g = dg[e] * ti[0] * ei[q * 16 + e], u = du[e] * ti[1] * ei[q * 16 + e];
+              const float hv = g / (1.0f + __expf(-g)) * u;  // silu(gate) * up
+              if (a.tma_store) {
+                stg[col * FT + r] = f2bf(hv);
+              } else if (m0 + col < a.M && okr[0]) {
+                const size_t o = (size_t)(m0 + col) * a.N + n[0];
+                if (a.out_f32)
+                  st_global_f32(static_cast<float*>(a.out) + o, hv);
+                else
+                  st_global_bf16(static_cast<uint16_t*>(a.out) + o, hv);
+              }
+            }
+          }
+          if (a.tma_store) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // tile writes -> TMA reads
+            epi_sync();
+            if (tid == 0) tma_store_2d_wait(&omap, f0, m0, smem_u32(stg));
+          }
+        } else {
+          // down / projection: + residual or bias, 16 columns at a time
+          uint16_t* stg = reinterpret_cast<uint16_t*>(smem);  // [NT][FT] bf16
+          const uint16_t* __restrict__ res = a.res;
+          const int jmax = min(HALF, a.M - m0 - cbase);
+#pragma unroll
+          for (int sa = 0; sa < NA; ++sa) {
+            const size_t obase = (size_t)(m0 + cbase) * a.N + n[sa];
+#pragma unroll 1
+            for (int q = 0; q < HALF / 16; ++q) {
+              float add[16], d[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int jj = q * 16 + e;
+                add[e] = (res && okr[sa] && jj < jmax)
+                             ? bf16f(__ldg(res + (size_t)(m0 + cbase + jj) * a.res_ld + n[sa]))
+                             : 0.f;
+              }
+              tc_ld16_wait(lane_base + (uint32_t)(sa * NT + q * 16), d);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int jj = q * 16 + e;
+                const float v = d[e] * ti[sa] * ei[jj] + add[e];
+                if (a.tma_store) {
+                  stg[(cbase + jj) * FT + 128 * sa + r] = f2bf(v);
+                } else if (okr[sa] && jj < jmax) {
+                  if (a.out_f32)
+                    st_global_f32(static_cast<float*>(a.out) + obase + (size_t)jj * a.N, v);
+                  else
+                    st_global_bf16(static_cast<uint16_t*>(a.out) + obase + (size_t)jj * a.N, v);
+                }
+              }
+            }
+          }
+          if (a.tma_store) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            epi_sync();
+            if (tid == 0) tma_store_2d_wait(&omap, f0, m0, smem_u32(stg));
+          }
         }
       }
     }
@@ -444,15 +576,15 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == MMA_WARP)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"((uint32_t)NT));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TCOLS));
 }
 
 // ---------------------------------------------------------------- host side
 
-template <int FMT, int KIND, int NT>
+template <int FMT, int KIND, int NT, int NA>
 mt_status run_prefill_dq(const GemvProblem& p, void* ws, const Launch& l) {
   constexpr int NW = KIND == 0 ? 2 : 1;
-  using SH = PqShape<FMT, KIND, NT>;
+  using SH = PqShape<FMT, KIND, NT, NA>;
   constexpr bool BFW = SH::BFW;
   // (dense bf16 weights have no groups: group 0 in the workspace layout, and
   // K blocks of 64 stand in for them in the arguments)
@@ -560,7 +692,7 @@ mt_status run_prefill_dq(const GemvProblem& p, void* ws, const Launch& l) {
     if (st != MT_OK) return st;
   }
   const size_t smem = SH::SMEM;
-  auto kern = prefill_dq_kernel<FMT, KIND, NT>;
+  auto kern = prefill_dq_kernel<FMT, KIND, NT, NA>;
   static std::mutex mu;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -586,9 +718,9 @@ mt_status run_prefill_dq(const GemvProblem& p, void* ws, const Launch& l) {
 
 template <int FMT, int KIND>
 mt_status run_prefill_dq_nt(const GemvProblem& p, void* ws, const Launch& l) {
-  if (p.M <= 64) return run_prefill_dq<FMT, KIND, 64>(p, ws, l);
-  if (p.M <= 128) return run_prefill_dq<FMT, KIND, 128>(p, ws, l);
-  return run_prefill_dq<FMT, KIND, 256>(p, ws, l);
+  if (p.M <= 64) return run_prefill_dq<FMT, KIND, 64, 1>(p, ws, l);
+  if (p.M <= 128) return run_prefill_dq<FMT, KIND, 128, 1>(p, ws, l);
+  return run_prefill_dq<FMT, KIND, 256, 2>(p, ws, l);  // wide tiles: 256 weight rows
 }
 
 }  // namespace mt

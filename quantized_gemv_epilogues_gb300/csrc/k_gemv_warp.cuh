@@ -38,6 +38,9 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
   sm.xraw = reinterpret_cast<uint16_t*>(smem);
   sm.xs = reinterpret_cast<uint4*>(smem + (size_t)g.K * 2);
   phase_tail_carve<FMT, KIND>(g, smem + (size_t)g.K * 2 + xs_bytes<FMT>(g.K), sm);
+  // down / projection: the addend of each of the CTA's rows, after the tail
+  uint16_t* res_s = reinterpret_cast<uint16_t*>(smem + (size_t)g.K * 2 + xs_bytes<FMT>(g.K) +
+                                                phase_tail_bytes<FMT, KIND>(g));
   __shared__ int task_ctr;
   __shared__ float red[WARP_TASK_WARPS];
 
@@ -61,15 +64,40 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
   }
 
   pdl_wait();  // x, the residual and the output buffer follow the preceding kernel
+  // the addends of the CTA's rows (residual or bias), requested with x so the
+  // epilogue does not wait on an L2 round trip; each row's addend is read
+  // here and its output written later by the same thread's row loop, so an
+  // output that is also the residual stays correct
+  if constexpr (KIND == 1)
+    if (a.res)
+      for (int rl = tid; rl < c.rows; rl += WT_THREADS) res_s[rl] = a.res[c.r_begin + rl];
   // x into shared memory and (affine) its largest |x|, then one staging pass
   // with the vector's fixed-point scale
   const int nu = g.K / 8;
   float m = 0.f;
-  for (int i = tid; i < nu; i += WT_THREADS) {
-    // plain (coherent) loads: x was written by the preceding kernel
-    const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)i * 8);
-    reinterpret_cast<uint4*>(sm.xraw)[i] = v;
-    if constexpr (AFF) m = fmaxf(m, unit_absmax(v));
+  {
+    // plain (coherent) loads, all of a thread's units requested before any is
+    // used (K <= 16384 in one batch): x was written by the preceding kernel
+    constexpr int XU = 4;
+    uint4 xv[XU];
+#pragma unroll
+    for (int k = 0; k < XU; ++k) {
+      const int i = tid + k * WT_THREADS;
+      xv[k] = i < nu ? *reinterpret_cast<const uint4*>(a.x + (size_t)i * 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < XU; ++k) {
+      const int i = tid + k * WT_THREADS;
+      if (i < nu) {
+        reinterpret_cast<uint4*>(sm.xraw)[i] = xv[k];
+        if constexpr (AFF) m = fmaxf(m, unit_absmax(xv[k]));
+      }
+    }
+    for (int i = tid + XU * WT_THREADS; i < nu; i += WT_THREADS) {
+      const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)i * 8);
+      reinterpret_cast<uint4*>(sm.xraw)[i] = v;
+      if constexpr (AFF) m = fmaxf(m, unit_absmax(v));
+    }
   }
   int ex = 0;
   if constexpr (AFF) ex = fx_exponent(cta_max(m, red, tid));  // its barrier also publishes xraw
@@ -96,7 +124,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
       const float v1 = row_total<NW>(g, sm.parts, rl, 1);
       outv = v0 / (1.0f + expf(-v0)) * v1;  // silu(gate) * up
     } else {
-      outv = a.res ? v0 + bf16f(a.res[n]) : v0;  // + residual or bias (one row)
+      outv = a.res ? v0 + bf16f(res_s[rl]) : v0;  // + residual or bias (one row)
     }
     if (a.out_f32)
       static_cast<float*>(a.out)[n] = outv;
@@ -131,7 +159,8 @@ mt_status run_gemv_warp(const GemvProblem& p, const Launch& l) {
   a.out = p.out;
   a.out_f32 = p.out_f32 ? 1 : 0;
 
-  const size_t smem = (size_t)p.K * 2 + xs_bytes<FMT>(p.K) + smem_parts;
+  const size_t smem = (size_t)p.K * 2 + xs_bytes<FMT>(p.K) + smem_parts +
+                      (KIND == 1 ? ((size_t)a.g.rows_alloc * 2 + 15) / 16 * 16 : 0);  // res_s
   const size_t budget = (size_t)di->max_smem_optin - 1024;  // static smem and slack
   if (smem > budget) return MT_ERR_SHAPE;
 

@@ -121,14 +121,15 @@ template <int FMT, int KIND>
 mt_status dispatch_mma(const GemvProblem& p, const Launch& l);
 
 // Chooses the kernel for one (format, kind) by MT_OPT_GEMV: 0 (default) the
-// warp-task kernel for one row and the tensor-core kernel for M > 1; 1 the
-// team kernel for every M; 2 the tensor-core kernel for every M.  A shape
-// that does not fit the chosen kernel's shared memory falls back to the team
-// kernel by row count.
+// warp-task kernel for one row (and for two rows over affine INT8, where it
+// measured faster than the tensor-core kernel) and the tensor-core kernel for
+// more rows; 1 the team kernel for every M; 2 the tensor-core kernel for every
+// M.  A shape that does not fit the chosen kernel's shared memory falls back
+// to the team kernel by row count.
 template <int FMT, int KIND>
 mt_status dispatch_rows(const GemvProblem& p, const Launch& l) {
   const int choice = gemv_choice();
-  if (p.M == 1 && choice == 0) {
+  if ((p.M == 1 || (p.M == 2 && FMT == FMT_A8)) && choice == 0) {
     const mt_status st = run_gemv_warp<FMT, KIND>(p, l);
     if (st != MT_ERR_SHAPE) return st;
   }

@@ -98,6 +98,7 @@ struct PhaseW {
 struct PhaseSmem {
   uint16_t* xraw;  // [K] bf16 activations
   uint4* xs;       // staging layout of x (see below), xs_bytes<FMT>(K) bytes
+  int xs_stride;   // 16-byte units between two activation rows' staging (MR = 2)
   float* gsum;     // [G] X_g (affine)
   float* xinv;     // [P] 2^-e, undoing the x scale (the same for every piece; affine)
   uint16_t* sbr;   // 2*NW arrays of sb_stride bf16: 2m = scales, 2m+1 = biases of matrix m
@@ -105,31 +106,33 @@ struct PhaseSmem {
 };
 
 // Bytes of a phase's shared arrays other than xraw and xs, in the order gsum,
-// xinv, sbr, parts (each a multiple of 16 bytes).
-template <int FMT, int KIND>
+// xinv, sbr, parts (each a multiple of 16 bytes).  MR: activation rows (the
+// one-row kernel also takes two): gsum [MR][G], xinv [MR][P], parts
+// [rows][P][NW][MR].
+template <int FMT, int KIND, int MR = 1>
 __host__ __device__ inline size_t phase_tail_bytes(const PhaseGeom& g) {
   constexpr bool AFF = FmtTraits<FMT>::AFFINE;
   constexpr int NW = KIND == 0 ? 2 : 1;
   size_t n = 0;
   if (AFF) {
-    n += (size_t)(g.G + 3) / 4 * 16;
-    n += (size_t)(g.P + 3) / 4 * 16;
+    n += (size_t)(MR * g.G + 3) / 4 * 16;
+    n += (size_t)(MR * g.P + 3) / 4 * 16;
     n += (size_t)2 * NW * g.sb_stride * 2;
   }
-  n += ((size_t)g.rows_alloc * g.P * NW * 4 + 15) / 16 * 16;
+  n += ((size_t)g.rows_alloc * g.P * NW * MR * 4 + 15) / 16 * 16;
   return n;
 }
 
 // Points sm's gsum, xinv, sbr and parts into the tail at p (16-byte aligned,
 // phase_tail_bytes long).
-template <int FMT, int KIND>
+template <int FMT, int KIND, int MR = 1>
 __device__ __forceinline__ void phase_tail_carve(const PhaseGeom& g, unsigned char* p, PhaseSmem& sm) {
   constexpr bool AFF = FmtTraits<FMT>::AFFINE;
   constexpr int NW = KIND == 0 ? 2 : 1;
   sm.gsum = reinterpret_cast<float*>(p);
-  if (AFF) p += (size_t)(g.G + 3) / 4 * 16;
+  if (AFF) p += (size_t)(MR * g.G + 3) / 4 * 16;
   sm.xinv = reinterpret_cast<float*>(p);
-  if (AFF) p += (size_t)(g.P + 3) / 4 * 16;
+  if (AFF) p += (size_t)(MR * g.P + 3) / 4 * 16;
   sm.sbr = reinterpret_cast<uint16_t*>(p);
   if (AFF) p += (size_t)2 * NW * g.sb_stride * 2;
   sm.parts = reinterpret_cast<float*>(p);
@@ -510,9 +513,82 @@ __device__ __forceinline__ void wt_compute_rs2(const PhaseGeom& g, const PhaseCt
   }
 }
 
+// wt_compute for two activation rows (MR = 2; affine INT8, one row per
+// stream): each weight chunk is multiplied with both rows' staged x (row m's
+// staging at sm.xs + m * xs_stride, its group sums at sm.gsum + m * G, its
+// scale at sm.xinv[m * P + p]).  Each row's sum is formed as in wt_compute;
+// parts hold [rows][P][NW][2].
+template <int FMT, int KIND>
+__device__ __forceinline__ void wt_compute_mr2(const PhaseGeom& g, const PhaseCta& c,
+                                               const PhaseSmem& sm, int t,
+                                               const uint4 (&buf)[WT_NS][WT_CL], int lane) {
+  using T = FmtTraits<FMT>;
+  constexpr int EPC = T::EPC;
+  constexpr int NW = KIND == 0 ? 2 : 1;
+  constexpr int RW = KIND == 0 ? 1 : 2;
+  static_assert(FMT == FMT_A8, "two activation rows: affine INT8");
+  const int rg = (int)(((unsigned long long)(unsigned)t * g.p_mul) >> 32);
+  const int p = t - rg * g.P;
+  const int rl0 = rg * RW;
+  float acc[WT_NS][2];
+#pragma unroll
+  for (int v = 0; v < WT_NS; ++v) acc[v][0] = acc[v][1] = 0.f;
+#pragma unroll
+  for (int k = 0; k < WT_CL; ++k) {
+    const int j = lane + 32 * k;
+    if (j < g.CPP) {
+      const int ch = p * g.CPP + j;
+      const int gi = (ch * EPC) >> g.lg_group;
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const uint4* xs = sm.xs + (size_t)m * sm.xs_stride;
+#pragma unroll
+        for (int v = 0; v < WT_NS; ++v) {
+          const float d = chunk_dot<FMT>(buf[v][k], xs, ch, g.CPR);
+          const int mt = KIND == 0 ? v : 0, rl = min(rl0 + (KIND == 0 ? 0 : v), c.rows - 1);
+          acc[v][m] = fmaf(bf16f(sm.sbr[(size_t)(2 * mt) * g.sb_stride + rl * g.G + gi]), d, acc[v][m]);
+        }
+      }
+    }
+  }
+  float vals[WT_NS][2];
+#pragma unroll
+  for (int v = 0; v < WT_NS; ++v)
+#pragma unroll
+    for (int m = 0; m < 2; ++m) vals[v][m] = acc[v][m] * sm.xinv[m * g.P + p];
+  // bias terms of the groups in this piece: sum_g b_g * X_g, per row of x
+  for (int gl = lane; gl < g.GPP; gl += 32) {
+    const int gi = p * g.GPP + gl;
+#pragma unroll
+    for (int v = 0; v < WT_NS; ++v) {
+      const int mt = KIND == 0 ? v : 0, rl = min(rl0 + (KIND == 0 ? 0 : v), c.rows - 1);
+      const float b = bf16f(sm.sbr[(size_t)(2 * mt + 1) * g.sb_stride + rl * g.G + gi]);
+#pragma unroll
+      for (int m = 0; m < 2; ++m) vals[v][m] = fmaf(b, sm.gsum[m * g.G + gi], vals[v][m]);
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < WT_NS; ++v)
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) vals[v][m] += __shfl_xor_sync(0xffffffffu, vals[v][m], off);
+  if (lane < 2 * WT_NS) {
+    const int v = lane >> 1, m = lane & 1;
+    float val = vals[0][0];
+#pragma unroll
+    for (int vv = 0; vv < WT_NS; ++vv)
+#pragma unroll
+      for (int mm = 0; mm < 2; ++mm)
+        if (lane == 2 * vv + mm) val = vals[vv][mm];
+    const int mt = KIND == 0 ? v : 0, rl = rl0 + (KIND == 0 ? 0 : v);
+    if (rl < c.rows) sm.parts[(((size_t)rl * g.P + p) * NW + mt) * 2 + m] = val;
+  }
+}
+
 // Computes task t from the weights in buf and stores its partial sums (one
 // per stream) in sm.parts.
-template <int FMT, int KIND, int RS = 1>
+template <int FMT, int KIND, int RS = 1, int MR = 1>
 __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c,
                                            const PhaseSmem& sm, int t,
                                            const uint4 (&buf)[WT_NS][WT_CL], int lane) {
@@ -523,6 +599,10 @@ __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c
   constexpr int RW = KIND == 0 ? 1 : 2;
   if constexpr (RS == 2) {
     wt_compute_rs2<FMT, KIND>(g, c, sm, t, buf, lane);
+    return;
+  }
+  if constexpr (MR == 2) {
+    wt_compute_mr2<FMT, KIND>(g, c, sm, t, buf, lane);
     return;
   }
   const int rg = (int)(((unsigned long long)(unsigned)t * g.p_mul) >> 32);
@@ -583,7 +663,7 @@ __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c
 // (wt_prefetch); task_ctr (shared) hands out the next task numbers.  Register
 // ping-pong: one task is in flight while the other is computed; two tasks per
 // iteration keep the buffer indices static.
-template <int FMT, int KIND, int RS = 1>
+template <int FMT, int KIND, int RS = 1, int MR = 1>
 __device__ __forceinline__ void wt_run(const PhaseGeom& g, const PhaseW& w, const PhaseCta& c,
                                        const PhaseSmem& sm, uint4 (&bufA)[WT_NS][WT_CL],
                                        uint4 (&bufB)[WT_NS][WT_CL], int tA, int tB, int* task_ctr,
@@ -596,23 +676,24 @@ __device__ __forceinline__ void wt_run(const PhaseGeom& g, const PhaseW& w, cons
   constexpr int AHEAD = 2 * WARP_TASK_WARPS;  // L2 lookahead in tasks
   for (;;) {
     if (tA >= c.T) break;  // tA < tB here
-    wt_compute<FMT, KIND, RS>(g, c, sm, tA, bufA, lane);
+    wt_compute<FMT, KIND, RS, MR>(g, c, sm, tA, bufA, lane);
     tA = next_task();
     wt_load<KIND, RS>(g, w, c, tA, bufA, pol, lane);
     wt_prefetch<KIND, RS>(g, w, c, tA + AHEAD, lane);
     if (tB >= c.T) break;  // tB < tA here
-    wt_compute<FMT, KIND, RS>(g, c, sm, tB, bufB, lane);
+    wt_compute<FMT, KIND, RS, MR>(g, c, sm, tB, bufB, lane);
     tB = next_task();
     wt_load<KIND, RS>(g, w, c, tB, bufB, pol, lane);
     wt_prefetch<KIND, RS>(g, w, c, tB + AHEAD, lane);
   }
 }
 
-// Sum of the pieces of CTA row rl of matrix m, in piece order.
-template <int NW>
-__device__ __forceinline__ float row_total(const PhaseGeom& g, const float* parts, int rl, int m) {
+// Sum of the pieces of CTA row rl of matrix m (for activation row r of MR),
+// in piece order.
+template <int NW, int MR = 1>
+__device__ __forceinline__ float row_total(const PhaseGeom& g, const float* parts, int rl, int m, int r = 0) {
   float v = 0.f;
-  for (int q = 0; q < g.P; ++q) v += parts[((size_t)rl * g.P + q) * NW + m];
+  for (int q = 0; q < g.P; ++q) v += parts[(((size_t)rl * g.P + q) * NW + m) * MR + r];
   return v;
 }
 
@@ -631,7 +712,6 @@ bool plan_phase(int K, int N, int group, int grid, PhaseGeom* out, size_t* smem_
   using T = FmtTraits<FMT>;
   constexpr int EPC = T::EPC;
   constexpr bool AFF = T::AFFINE;
-  constexpr int NW = KIND == 0 ? 2 : 1;
   PhaseGeom g = {};
   g.K = K;
   g.N = N;

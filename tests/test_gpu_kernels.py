@@ -30,8 +30,9 @@ def mt():
 @pytest.fixture(params=["default", "team", "mma"])
 def gemv(request, mt):
     """Runs a test with each GEMV kernel family: the default choice (warp-task
-    kernel for M = 1, tensor-core kernel for M > 1), the team kernel for every
-    M, and the tensor-core kernel for every M."""
+    kernel for M = 1 and for M = 2 over affine INT8, tensor-core kernel for
+    other M > 1), the team kernel for every M, and the tensor-core kernel for
+    every M."""
     mt.mt_set_option(mt.MT_OPT_GEMV, {"default": 0, "team": 1, "mma": 2}[request.param])
     yield request.param
     mt.mt_set_option(mt.MT_OPT_GEMV, 0)
@@ -203,6 +204,38 @@ def test_down_residual(mt, gemv, shape, out_f32):
         assert_f32_close(host_f64(y), ref, "y f32")
     else:
         assert_bf16_close(host_bits(y), ref, "y bf16")
+
+
+@pytest.mark.parametrize("group,K,N", [(128, 4096, 1000), (64, 12288, 333), (32, 1024, 257)])
+def test_two_rows_match_one_row_calls(mt, group, K, N):
+    """Two activation rows over affine INT8 weights (one kernel reading each
+    weight once): every output row equals the one-row call on that row alone,
+    bit for bit, for gate/up + SwiGLU, down + residual and a projection with
+    bias (each row keeps its own fixed-point scale and summation order)."""
+    seed = 61000 + K + N + group
+    x = synth.host_bf16(2 * K, seed, synth.ACT).reshape(2, K)
+    res = synth.host_bf16(2 * N, seed + 1, synth.ACT).reshape(2, N)
+    bias = synth.host_bf16(N, seed + 2, synth.PROJ_BIAS)
+    qg, sg, bg = gpu_pack(mt, gen_w32(N, K, seed + 3), 1, group)
+    qu, su, bu = gpu_pack(mt, gen_w32(N, K, seed + 4), 1, group)
+    sgu, bgu = torch.stack([sg, su]).contiguous(), torch.stack([bg, bu]).contiguous()
+    xd, rd, bd = dev_bf16(x), dev_bf16(res), dev_bf16(bias)
+    calls = {
+        "h": lambda xx, rr, out: mt.mt_swiglu_gateup(xx, qg, qu, sgu, bgu, group, out, fmt=1),
+        "y": lambda xx, rr, out: mt.mt_down_residual(xx, qg, sg, bg, group, rr, out, fmt=1),
+        "y + bias": lambda xx, rr, out: mt.mt_linear_bias(xx, qu, su, bu, group, bd, out, fmt=1),
+    }
+    for name, call in calls.items():
+        two = torch.empty(2, N, dtype=torch.bfloat16, device="cuda")
+        call(xd, rd, two)
+        ones = []
+        for r in range(2):
+            one = torch.empty(1, N, dtype=torch.bfloat16, device="cuda")
+            call(xd[r:r + 1].clone(), rd[r:r + 1].clone(), one)  # fresh 16-byte aligned rows
+            ones.append(one)
+        torch.cuda.synchronize()
+        for r in range(2):
+            assert torch.equal(two[r], ones[r][0]), f"{name}: row {r} differs from the one-row call"
 
 
 def test_down_residual_in_place(mt, gemv):

@@ -29,8 +29,9 @@ struct WarpArgs {
 
 // RS: rows per load stream (g.RS; 2 for rows of exactly 64 chunks).  MR:
 // activation rows (1, or 2 for affine INT8 with RS == 1): every weight chunk
-// is used for both rows, and each row's result is the one-row kernel's.
-template <int FMT, int KIND, int RS, int MR>
+// is used for both rows, and each row's result is the one-row kernel's.  PL:
+// bytes of the fixed-point x (affine; 2 for bf16 outputs, 3 for fp32).
+template <int FMT, int KIND, int RS, int MR, int PL>
 __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs a) {
   constexpr bool AFF = FmtTraits<FMT>::AFFINE;
   constexpr int NW = KIND == 0 ? 2 : 1;
@@ -40,7 +41,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
   // shared memory: xraw [MR][K] bf16, xs [MR] staging layouts, the phase
   // tail, then (down / projection) the addends [MR][rows]
   extern __shared__ __align__(128) unsigned char smem[];
-  const size_t xs_row = xs_bytes<FMT>(g.K);
+  const size_t xs_row = xs_bytes<FMT, PL>(g.K);
   PhaseSmem sm;
   sm.xraw = reinterpret_cast<uint16_t*>(smem);
   sm.xs = reinterpret_cast<uint4*>(smem + (size_t)MR * g.K * 2);
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
 #pragma unroll
   for (int r = 0; r < MR; ++r) {
     int ex = 0;
-    if constexpr (AFF) ex = fx_exponent(cta_max(mx[r], red, tid));  // its barrier also publishes xraw
+    if constexpr (AFF) ex = fx_exponent<PL>(cta_max(mx[r], red, tid));  // its barrier also publishes xraw
     else __syncthreads();
     const float xscale = exp2i(ex);
     PhaseSmem smr = sm;
@@ -130,7 +131,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
     smr.xinv = sm.xinv + (size_t)r * g.P;
     for (int base = warp * 32; base < nu; base += WT_THREADS) {
       const int i = base + lane < nu ? base + lane : -1;
-      x_stage_unit<FMT>(g, smr, i, i >= 0 ? reinterpret_cast<const uint4*>(smr.xraw)[i] : make_uint4(0, 0, 0, 0),
+      x_stage_unit<FMT, PL>(g, smr, i, i >= 0 ? reinterpret_cast<const uint4*>(smr.xraw)[i] : make_uint4(0, 0, 0, 0),
                         xscale, false);
     }
     x_set_scale<FMT>(g, smr, ex, tid, WT_THREADS);
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
   cp_async_wait_all();  // scales and biases
   __syncthreads();
 
-  wt_run<FMT, KIND, RS, MR>(g, a.w, c, sm, bufA, bufB, tA, tB, &task_ctr, pol, lane);
+  wt_run<FMT, KIND, PL, RS, MR, RS == 1>(g, a.w, c, sm, bufA, bufB, tA, tB, &task_ctr, pol, lane);
   __syncthreads();
 
   // epilogue: one thread per row adds the pieces in a fixed order
@@ -162,6 +163,16 @@ __global__ void __launch_bounds__(WT_THREADS, 1) gemv_warp_kernel(const WarpArgs
         static_cast<uint16_t*>(a.out)[o] = f2bf(outv);
     }
   }
+}
+
+using WarpKernT = void (*)(WarpArgs);
+
+// The instantiation for MR activation rows and RS rows per load stream.
+template <int FMT, int KIND, int PL>
+WarpKernT warp_kernel_for(int MR, int RS) {
+  constexpr int MR2 = FMT == FMT_A8 ? 2 : 1;  // the two-row instantiation (affine INT8 only)
+  return MR == 2 ? gemv_warp_kernel<FMT, KIND, 1, MR2, PL>
+                 : (RS == 2 ? gemv_warp_kernel<FMT, KIND, 2, 1, PL> : gemv_warp_kernel<FMT, KIND, 1, 1, PL>);
 }
 
 // Host plan and launch of the warp-task kernel for one (format, kind).
@@ -194,23 +205,29 @@ mt_status run_gemv_warp(const GemvProblem& p, const Launch& l) {
   a.out = p.out;
   a.out_f32 = p.out_f32 ? 1 : 0;
 
-  const size_t smem = (size_t)MR * ((size_t)p.K * 2 + xs_bytes<FMT>(p.K)) + smem_parts +
+  // affine weights with bf16 outputs: x in 16-bit fixed point (2 byte planes),
+  // with fp32 outputs in 24-bit (3 planes); dense bf16 weights: x as stored
+  constexpr bool AFF = FmtTraits<FMT>::AFFINE;
+  const bool pl2 = AFF && !p.out_f32;
+  const size_t smem = (size_t)MR * ((size_t)p.K * 2 + (pl2 ? xs_bytes<FMT, 2>(p.K) : xs_bytes<FMT, 3>(p.K))) +
+                      smem_parts +
                       (KIND == 1 ? ((size_t)MR * a.g.rows_alloc * 2 + 15) / 16 * 16 : 0);  // res_s
   const size_t budget = (size_t)di->max_smem_optin - 1024;  // static smem and slack
   if (smem > budget) return MT_ERR_SHAPE;
 
-  using KernT = void (*)(WarpArgs);
-  constexpr int MR2 = FMT == FMT_A8 ? 2 : 1;  // the two-row instantiation (affine INT8 only)
-  const KernT kern = MR == 2 ? gemv_warp_kernel<FMT, KIND, 1, MR2>
-                     : (a.g.RS == 2 ? gemv_warp_kernel<FMT, KIND, 2, 1> : gemv_warp_kernel<FMT, KIND, 1, 1>);
+  WarpKernT kern = warp_kernel_for<FMT, KIND, 3>(MR, a.g.RS);
+  if constexpr (AFF)
+    if (pl2) kern = warp_kernel_for<FMT, KIND, 2>(MR, a.g.RS);
   {
     std::lock_guard<std::mutex> g(cache.mu);
     if (dev < 64 && !cache.attr_set[dev]) {
-      for (KernT k : {gemv_warp_kernel<FMT, KIND, 1, 1>, gemv_warp_kernel<FMT, KIND, 2, 1>,
-                      gemv_warp_kernel<FMT, KIND, 1, MR2>}) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
-        if (e != cudaSuccess) return cuda_fail(e);
-      }
+      for (int mr = 1; mr <= 2; ++mr)
+        for (int rs = 1; rs <= 2; ++rs)
+          for (int pl = AFF ? 2 : 3; pl <= 3; ++pl) {
+            const WarpKernT k = pl == 2 ? warp_kernel_for<FMT, KIND, 2>(mr, rs) : warp_kernel_for<FMT, KIND, 3>(mr, rs);
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
+            if (e != cudaSuccess) return cuda_fail(e);
+          }
       cache.attr_set[dev] = 1;
     }
   }

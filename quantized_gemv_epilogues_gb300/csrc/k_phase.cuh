@@ -33,18 +33,21 @@
 //  * The affine term is factored as
 //      sum_k (s q_k + b) x_k = sum_chunks s * (sum q_k x_k) + sum_groups b * X_g
 //    with X_g the sum of x over group g (fp32, from the bf16 values).  x is
-//    held as a 24-bit fixed-point integer X = round(x * 2^e), one 2^e for the
-//    whole vector chosen from its max|x| so that |X| <= 2^22: every element
-//    within 2^14 of the vector's maximum is exact, smaller ones are rounded to
-//    2^-22 of that maximum.  X is split into three byte planes, X = 65536 X2 +
-//    256 X1 + X0 (X2 signed), and the packed codes are used as they are
-//    stored: one dp4a (four u8 x s8/u8 products added to an int32) per weight
-//    word and plane, so a 16-byte chunk of INT8 codes costs 12 dp4a.  The
-//    three plane sums of a chunk are exact integers; they are combined with
-//    one rounding in fp32 (256 S1 + S0 and 65536 S2 are each exact, their sum
-//    rounds once when it exceeds 2^24), and the scale 2^-e is divided out of
-//    the partial sums.  INT4 words are split into their low and high nibbles
-//    (two masks) against even/odd element planes.
+//    held as a fixed-point integer X = round(x * 2^e) of PL bytes, one 2^e
+//    for the whole vector chosen from its max|x|:
+//      PL = 2 (bf16 outputs): |X| <= 2^14; every element within 2^6 of the
+//        vector's maximum is exact, smaller ones are rounded to 2^-14 of it,
+//        below the outputs' own bf16 rounding (2^-9 relative);
+//      PL = 3 (fp32 outputs): |X| <= 2^22; every element within 2^14 of the
+//        maximum is exact, smaller ones are rounded to 2^-22 of it.
+//    X is split into PL byte planes (the top one signed), and the packed
+//    codes are used as they are stored: one dp4a (four u8 x s8/u8 products
+//    added to an int32) per weight word and plane, so a 16-byte chunk of INT8
+//    codes costs 4 PL dp4a.  The plane sums of a chunk are exact integers;
+//    combining them into fp32 rounds once (PL = 2) or at most twice (PL = 3),
+//    and the scale 2^-e is divided out of the partial sums.  INT4 words are
+//    split into their low and high nibbles (two masks) against even/odd
+//    element planes.
 //    This replaced an fp16 exponent-bias dequant + mixed-precision FMA chain
 //    that was instruction-bound at ~4.6 instructions per weight.  Dense bf16
 //    weights use mixed-precision bf16 FMAs (exact products, fp32
@@ -97,7 +100,7 @@ struct PhaseW {
 // Shared-memory arrays of one phase.
 struct PhaseSmem {
   uint16_t* xraw;  // [K] bf16 activations
-  uint4* xs;       // staging layout of x (see below), xs_bytes<FMT>(K) bytes
+  uint4* xs;       // staging layout of x (see below), xs_bytes<FMT, PL>(K) bytes
   int xs_stride;   // 16-byte units between two activation rows' staging (MR = 2)
   float* gsum;     // [G] X_g (affine)
   float* xinv;     // [P] 2^-e, undoing the x scale (the same for every piece; affine)
@@ -153,18 +156,21 @@ __device__ __forceinline__ PhaseCta phase_cta(const PhaseGeom& g, int cta) {
   return c;
 }
 
-// Staging layout of x, read by chunk_dot (16-byte units; CPR chunks per row):
-// A8:   unit p*CPR + c holds byte plane p (0: bits 16..23 of X, signed;
-//       1: bits 8..15; 2: bits 0..7) of the 16 elements of chunk c, in
-//       element order.  (X: the 24-bit fixed-point x, see x_stage_unit.)
+// Staging layout of x, read by chunk_dot (16-byte units; CPR chunks per row).
+// Affine formats hold x as a fixed-point integer X of PL bytes (PL = 3: 24
+// bits, for fp32 outputs; PL = 2: 16 bits, for bf16 outputs), stored as PL
+// byte planes; plane 0 is the most significant byte (signed), the others are
+// unsigned:
+// A8:   unit p*CPR + c holds byte plane p (byte PL-1-p of X) of the 16
+//       elements of chunk c, in element order.
 // A4:   unit (2p + h)*CPR + c holds byte plane p of the even (h = 0) or odd
 //       (h = 1) elements of chunk c's 32: byte b of word wi is element
 //       8wi + 2b + h, matching the low / high nibbles of weight word wi.
 // BF16: words 2u, 2u+1 of chunk c read 4 bf16 (elements 4u..4u+3) at 8-byte
 //       unit u*CPR + c.
-template <int FMT>
+template <int FMT, int PL>
 __host__ __device__ constexpr size_t xs_bytes(int K) {
-  return FMT == FMT_BF16 ? (size_t)K * 2 : (size_t)K * 3;
+  return FMT == FMT_BF16 ? (size_t)K * 2 : (size_t)K * PL;
 }
 
 // s += the four byte products of a (unsigned codes) and b (signed or
@@ -183,6 +189,11 @@ __device__ __forceinline__ void dp4a_uu(uint32_t& s, uint32_t a, uint32_t b) {
 __device__ __forceinline__ float combine_planes(int s2, uint32_t s1, uint32_t s0) {
   return fmaf((float)s2, 65536.f, (float)(int)(s1 * 256u + s0));
 }
+// Two planes (16-bit X): S = 256 S1 + S0 with |S1| <= 32 * 255 * 128 and S0 <=
+// 32 * 255 * 255, exact in int32; one rounding in the conversion to fp32.
+__device__ __forceinline__ float combine_planes(int s1, uint32_t s0) {
+  return (float)(s1 * 256 + (int)s0);
+}
 
 // acc_lo += lo(a) * lo(b), acc_hi += hi(a) * hi(b) for bf16 pairs: exact
 // products in fp32, fp32 accumulation.
@@ -195,13 +206,42 @@ __device__ __forceinline__ void fma2_bf16_f32(float& lo, float& hi, uint32_t a, 
 }
 
 // Dot product of one 16-byte weight chunk (chunk c of its row) with its
-// activations from the staging layout: sum of q * X (affine, exact, returned
-// in fp32) or of w * x (bf16, fp32 accumulation).
-template <int FMT>
+// activations from the staging layout: sum of q * X (affine, PL byte planes,
+// exact but for the final conversion, returned in fp32) or of w * x (bf16,
+// fp32 accumulation).
+template <int FMT, int PL>
 __device__ __forceinline__ float chunk_dot(const uint4 w, const uint4* __restrict__ xs, int c,
                                            int CPR) {
   const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-  if constexpr (FMT == FMT_A8) {
+  if constexpr (FMT == FMT_A8 && PL == 2) {
+    const uint4 p1 = xs[c], p0 = xs[CPR + c];
+    const uint32_t x1[4] = {p1.x, p1.y, p1.z, p1.w};
+    const uint32_t x0[4] = {p0.x, p0.y, p0.z, p0.w};
+    int s1 = 0;
+    uint32_t s0 = 0;
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      dp4a_us(s1, ww[wi], x1[wi]);
+      dp4a_uu(s0, ww[wi], x0[wi]);
+    }
+    return combine_planes(s1, s0);
+  } else if constexpr (FMT == FMT_A4 && PL == 2) {
+    const uint4 e1 = xs[c], o1 = xs[CPR + c], e0 = xs[2 * CPR + c], o0 = xs[3 * CPR + c];
+    const uint32_t xe1[4] = {e1.x, e1.y, e1.z, e1.w}, xo1[4] = {o1.x, o1.y, o1.z, o1.w};
+    const uint32_t xe0[4] = {e0.x, e0.y, e0.z, e0.w}, xo0[4] = {o0.x, o0.y, o0.z, o0.w};
+    int s1 = 0;
+    uint32_t s0 = 0;
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      const uint32_t lo = ww[wi] & 0x0F0F0F0Fu;         // codes 8wi + 0, 2, 4, 6
+      const uint32_t hi = (ww[wi] >> 4) & 0x0F0F0F0Fu;  // codes 8wi + 1, 3, 5, 7
+      dp4a_us(s1, lo, xe1[wi]);
+      dp4a_us(s1, hi, xo1[wi]);
+      dp4a_uu(s0, lo, xe0[wi]);
+      dp4a_uu(s0, hi, xo0[wi]);
+    }
+    return combine_planes(s1, s0);
+  } else if constexpr (FMT == FMT_A8) {
     const uint4 p2 = xs[c], p1 = xs[CPR + c], p0 = xs[2 * CPR + c];
     const uint32_t x2[4] = {p2.x, p2.y, p2.z, p2.w};
     const uint32_t x1[4] = {p1.x, p1.y, p1.z, p1.w};
@@ -266,45 +306,43 @@ __device__ __forceinline__ void wt_prefetch(const PhaseGeom& g, const PhaseW& w,
   prefetch_l2_normal(src);
 }
 
-// Requests the weights of task t into buf (zeros for t >= T or rows past the
-// CTA's range).  Stream v of a task: matrix v of row rg (gate/up) or row
-// 2*rg + v (down); piece p of the row.
+// Requests chunk slot k of every stream of task t into buf[.][k] (zeros
+// for t >= T or rows past the CTA's range).  Stream v of a task: matrix v of
+// row rg (gate/up) or row 2*rg + v (down); piece p of the row.  Lane chunk
+// slot k is chunk lane + 32 k of the piece (RS = 1), or chunk lane + 32 (k & 1)
+// of row k >> 1 of the stream's two rows (RS = 2: whole rows of 64 chunks).
+template <int KIND, int RS = 1>
+__device__ __forceinline__ void wt_load_chunk(const PhaseGeom& g, const PhaseW& w, const PhaseCta& c,
+                                              int t, uint4 (&buf)[WT_NS][WT_CL], int k, uint64_t pol,
+                                              int lane) {
+  constexpr int RW = KIND == 0 ? 1 : 2;
+  const int rg = (int)(((unsigned long long)(unsigned)t * g.p_mul) >> 32);
+  const int p = t - rg * g.P;
+#pragma unroll
+  for (int v = 0; v < WT_NS; ++v) {
+    const uint8_t* W = KIND == 0 && v ? w.W1 : w.W0;
+    if constexpr (RS == 1) {
+      const int rl = rg * RW + (KIND == 0 ? 0 : v);
+      const int j = lane + 32 * k;
+      const bool ok = t < c.T && rl < c.rows && j < g.CPP;
+      buf[v][k] = ok ? ldg_stream_pol(W + (size_t)(c.r_begin + rl) * g.row_bytes + (size_t)p * g.B + (size_t)j * 16, pol)
+                     : make_uint4(0, 0, 0, 0);
+    } else {
+      const int r = (rg * RW + (KIND == 0 ? 0 : v)) * 2 + (k >> 1);
+      const bool ok = t < c.T && r < c.rows;
+      buf[v][k] = ok ? ldg_stream_pol(W + (size_t)(c.r_begin + r) * g.row_bytes + (size_t)(lane + 32 * (k & 1)) * 16, pol)
+                     : make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+// Requests the weights of task t into buf (every chunk slot).
 template <int KIND, int RS = 1>
 __device__ __forceinline__ void wt_load(const PhaseGeom& g, const PhaseW& w, const PhaseCta& c,
                                         int t, uint4 (&buf)[WT_NS][WT_CL], uint64_t pol,
                                         int lane) {
-  constexpr int RW = KIND == 0 ? 1 : 2;
-  const int rg = (int)(((unsigned long long)(unsigned)t * g.p_mul) >> 32);
-  const int p = t - rg * g.P;
-  if constexpr (RS == 1) {
 #pragma unroll
-    for (int v = 0; v < WT_NS; ++v) {
-      const int rl = rg * RW + (KIND == 0 ? 0 : v);
-      const bool ok = t < c.T && rl < c.rows;
-      const uint8_t* src = (KIND == 0 && v ? w.W1 : w.W0) +
-                           (size_t)(c.r_begin + (ok ? rl : 0)) * g.row_bytes + (size_t)p * g.B;
-#pragma unroll
-      for (int k = 0; k < WT_CL; ++k) {
-        const int j = lane + 32 * k;
-        buf[v][k] = (ok && j < g.CPP) ? ldg_stream_pol(src + (size_t)j * 16, pol) : make_uint4(0, 0, 0, 0);
-      }
-    }
-  } else {
-    // RS = 2: stream v is rows rl, rl + 1 (whole rows of 64 chunks, contiguous);
-    // chunks k = 0, 1 of a lane belong to row rl and k = 2, 3 to row rl + 1
-#pragma unroll
-    for (int v = 0; v < WT_NS; ++v) {
-      const int rl = (rg * RW + (KIND == 0 ? 0 : v)) * 2;
-      const uint8_t* src = (KIND == 0 && v ? w.W1 : w.W0) + (size_t)c.r_begin * g.row_bytes;
-#pragma unroll
-      for (int k = 0; k < WT_CL; ++k) {
-        const int r = rl + (k >> 1);
-        const bool ok = t < c.T && r < c.rows;
-        buf[v][k] = ok ? ldg_stream_pol(src + (size_t)r * g.row_bytes + (size_t)(lane + 32 * (k & 1)) * 16, pol)
-                       : make_uint4(0, 0, 0, 0);
-      }
-    }
-  }
+  for (int k = 0; k < WT_CL; ++k) wt_load_chunk<KIND, RS>(g, w, c, t, buf, k, pol, lane);
 }
 
 // Stages the CTA's scales and biases (contiguous [rows][G] blocks) into
@@ -348,12 +386,14 @@ __device__ __forceinline__ float unit_absmax(const uint4 v) {
   return m;
 }
 
-// The exponent e with m * 2^e in [2^21, 2^22) for the largest |x| m of the
-// vector (a zero or subnormal m takes the largest exponent, 126): then X =
-// round(x * 2^e) has |X| <= 2^22 for every element.
+// The exponent e with m * 2^e in [2^(8 PL - 3), 2^(8 PL - 2)) for the
+// largest |x| m of the vector (a zero or subnormal m takes the largest
+// exponent, 126): then X = round(x * 2^e) has |X| <= 2^(8 PL - 2) for every
+// element, within the signed range of PL bytes (24 bits: 2^22; 16 bits: 2^14).
+template <int PL>
 __device__ __forceinline__ int fx_exponent(float m) {
   const int mb = __float_as_int(m);
-  return (mb >> 23) >= 255 ? 0 : max(-126, min(126, 21 - ((mb >> 23) - 127)));
+  return (mb >> 23) >= 255 ? 0 : max(-126, min(126, (8 * PL - 3) - ((mb >> 23) - 127)));
 }
 
 // Byte k of each of a, b, c, d, packed as one word (a in the low byte).
@@ -369,9 +409,10 @@ __device__ __forceinline__ uint32_t byte_plane(uint32_t a, uint32_t b, uint32_t 
 // a lane without a unit), so the group/8 units of a quantisation group sit in
 // consecutive lanes and are summed with a fixed shuffle tree.  The caller ends
 // the staging with a CTA barrier before sm.xs is read.
-template <int FMT>
+template <int FMT, int PL>
 __device__ __forceinline__ void x_stage_unit(const PhaseGeom& g, const PhaseSmem& sm, int i, const uint4 v,
                                              float xscale, bool store_raw) {
+  static_assert(PL == 2 || PL == 3, "16- or 24-bit fixed point");
   if (store_raw && i >= 0) reinterpret_cast<uint4*>(sm.xraw)[i] = v;
   const int CPR = g.CPR;
   if constexpr (!FmtTraits<FMT>::AFFINE) {
@@ -388,7 +429,7 @@ __device__ __forceinline__ void x_stage_unit(const PhaseGeom& g, const PhaseSmem
     for (int j = 0; j < 4; ++j) {
       const float lo = bf16lo(vw[j]), hi = bf16hi(vw[j]);
       sum += lo + hi;
-      // |x * xscale| < 2^22 by the choice of the scale
+      // |x * xscale| <= 2^(8 PL - 2) by the choice of the scale
       X[2 * j] = (uint32_t)round_small_to_int(lo * xscale);
       X[2 * j + 1] = (uint32_t)round_small_to_int(hi * xscale);
     }
@@ -397,21 +438,21 @@ __device__ __forceinline__ void x_stage_unit(const PhaseGeom& g, const PhaseSmem
     if (i < 0) return;
     if ((i & (upg - 1)) == 0) sm.gsum[i >> (g.lg_group - 3)] = sum;
     if constexpr (FMT == FMT_A8) {
-      // unit i = words 2(i&1), 2(i&1)+1 of chunk i>>1; plane p byte 2-p of X
+      // unit i = words 2(i&1), 2(i&1)+1 of chunk i>>1; plane p byte PL-1-p of X
       uint2* xs2 = reinterpret_cast<uint2*>(sm.xs);
       const int c = i >> 1, h = i & 1;
 #pragma unroll
-      for (int p = 0; p < 3; ++p)
-        xs2[(size_t)(p * CPR + c) * 2 + h] =
-            make_uint2(byte_plane(X[0], X[1], X[2], X[3], 2 - p), byte_plane(X[4], X[5], X[6], X[7], 2 - p));
+      for (int p = 0; p < PL; ++p)
+        xs2[(size_t)(p * CPR + c) * 2 + h] = make_uint2(byte_plane(X[0], X[1], X[2], X[3], PL - 1 - p),
+                                                        byte_plane(X[4], X[5], X[6], X[7], PL - 1 - p));
     } else {
       // unit i = word i&3 of chunk i>>2: even elements -> half 0, odd -> half 1
       uint32_t* xs4 = reinterpret_cast<uint32_t*>(sm.xs);
       const int c = i >> 2, wi = i & 3;
 #pragma unroll
-      for (int p = 0; p < 3; ++p) {
-        xs4[(size_t)((2 * p) * CPR + c) * 4 + wi] = byte_plane(X[0], X[2], X[4], X[6], 2 - p);
-        xs4[(size_t)((2 * p + 1) * CPR + c) * 4 + wi] = byte_plane(X[1], X[3], X[5], X[7], 2 - p);
+      for (int p = 0; p < PL; ++p) {
+        xs4[(size_t)((2 * p) * CPR + c) * 4 + wi] = byte_plane(X[0], X[2], X[4], X[6], PL - 1 - p);
+        xs4[(size_t)((2 * p + 1) * CPR + c) * 4 + wi] = byte_plane(X[1], X[3], X[5], X[7], PL - 1 - p);
       }
     }
   }
@@ -445,10 +486,11 @@ __device__ __forceinline__ float cta_max(float v, float* red, int tid) {
 // formed exactly as in wt_compute (the same chunk, group and lane order, the
 // same reduction), so it does not depend on whether the row is the first or
 // second of its stream, and is stored as its single piece.
-template <int FMT, int KIND>
+template <int FMT, int KIND, int PL, class AfterChunk>
 __device__ __forceinline__ void wt_compute_rs2(const PhaseGeom& g, const PhaseCta& c,
                                                const PhaseSmem& sm, int t,
-                                               const uint4 (&buf)[WT_NS][WT_CL], int lane) {
+                                               const uint4 (&buf)[WT_NS][WT_CL], int lane,
+                                               AfterChunk after) {
   using T = FmtTraits<FMT>;
   constexpr int EPC = T::EPC;
   constexpr bool AFF = T::AFFINE;
@@ -464,7 +506,7 @@ __device__ __forceinline__ void wt_compute_rs2(const PhaseGeom& g, const PhaseCt
     const int r = k >> 1, ch = lane + 32 * (k & 1);
 #pragma unroll
     for (int v = 0; v < WT_NS; ++v) {
-      const float d = chunk_dot<FMT>(buf[v][k], sm.xs, ch, g.CPR);
+      const float d = chunk_dot<FMT, PL>(buf[v][k], sm.xs, ch, g.CPR);
       if constexpr (AFF) {
         const int m = KIND == 0 ? v : 0, rl = min(row_of(v, r), c.rows - 1);
         const int gi = (ch * EPC) >> g.lg_group;
@@ -473,6 +515,7 @@ __device__ __forceinline__ void wt_compute_rs2(const PhaseGeom& g, const PhaseCt
         acc[v][r] += d;
       }
     }
+    after(k);
   }
   float vals[WT_NS][2];
 #pragma unroll
@@ -518,10 +561,11 @@ __device__ __forceinline__ void wt_compute_rs2(const PhaseGeom& g, const PhaseCt
 // staging at sm.xs + m * xs_stride, its group sums at sm.gsum + m * G, its
 // scale at sm.xinv[m * P + p]).  Each row's sum is formed as in wt_compute;
 // parts hold [rows][P][NW][2].
-template <int FMT, int KIND>
+template <int FMT, int KIND, int PL, class AfterChunk>
 __device__ __forceinline__ void wt_compute_mr2(const PhaseGeom& g, const PhaseCta& c,
                                                const PhaseSmem& sm, int t,
-                                               const uint4 (&buf)[WT_NS][WT_CL], int lane) {
+                                               const uint4 (&buf)[WT_NS][WT_CL], int lane,
+                                               AfterChunk after) {
   using T = FmtTraits<FMT>;
   constexpr int EPC = T::EPC;
   constexpr int NW = KIND == 0 ? 2 : 1;
@@ -544,12 +588,13 @@ __device__ __forceinline__ void wt_compute_mr2(const PhaseGeom& g, const PhaseCt
         const uint4* xs = sm.xs + (size_t)m * sm.xs_stride;
 #pragma unroll
         for (int v = 0; v < WT_NS; ++v) {
-          const float d = chunk_dot<FMT>(buf[v][k], xs, ch, g.CPR);
+          const float d = chunk_dot<FMT, PL>(buf[v][k], xs, ch, g.CPR);
           const int mt = KIND == 0 ? v : 0, rl = min(rl0 + (KIND == 0 ? 0 : v), c.rows - 1);
           acc[v][m] = fmaf(bf16f(sm.sbr[(size_t)(2 * mt) * g.sb_stride + rl * g.G + gi]), d, acc[v][m]);
         }
       }
     }
+    after(k);
   }
   float vals[WT_NS][2];
 #pragma unroll
@@ -587,22 +632,25 @@ __device__ __forceinline__ void wt_compute_mr2(const PhaseGeom& g, const PhaseCt
 }
 
 // Computes task t from the weights in buf and stores its partial sums (one
-// per stream) in sm.parts.
-template <int FMT, int KIND, int RS = 1, int MR = 1>
+// per stream) in sm.parts.  after(k) runs once chunk slot k of every stream
+// has been consumed, so that the slot's registers can be refilled while the
+// rest of the task is computed.
+template <int FMT, int KIND, int PL, int RS = 1, int MR = 1, class AfterChunk>
 __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c,
                                            const PhaseSmem& sm, int t,
-                                           const uint4 (&buf)[WT_NS][WT_CL], int lane) {
+                                           const uint4 (&buf)[WT_NS][WT_CL], int lane,
+                                           AfterChunk after) {
   using T = FmtTraits<FMT>;
   constexpr int EPC = T::EPC;
   constexpr bool AFF = T::AFFINE;
   constexpr int NW = KIND == 0 ? 2 : 1;
   constexpr int RW = KIND == 0 ? 1 : 2;
   if constexpr (RS == 2) {
-    wt_compute_rs2<FMT, KIND>(g, c, sm, t, buf, lane);
+    wt_compute_rs2<FMT, KIND, PL>(g, c, sm, t, buf, lane, after);
     return;
   }
   if constexpr (MR == 2) {
-    wt_compute_mr2<FMT, KIND>(g, c, sm, t, buf, lane);
+    wt_compute_mr2<FMT, KIND, PL>(g, c, sm, t, buf, lane, after);
     return;
   }
   const int rg = (int)(((unsigned long long)(unsigned)t * g.p_mul) >> 32);
@@ -618,7 +666,7 @@ __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c
       const int ch = p * g.CPP + j;
 #pragma unroll
       for (int v = 0; v < WT_NS; ++v) {
-        const float d = chunk_dot<FMT>(buf[v][k], sm.xs, ch, g.CPR);
+        const float d = chunk_dot<FMT, PL>(buf[v][k], sm.xs, ch, g.CPR);
         if constexpr (AFF) {
           const int m = KIND == 0 ? v : 0, rl = min(rl0 + (KIND == 0 ? 0 : v), c.rows - 1);
           const int gi = (ch * EPC) >> g.lg_group;
@@ -628,6 +676,7 @@ __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c
         }
       }
     }
+    after(k);
   }
   float vals[WT_NS];
 #pragma unroll
@@ -662,8 +711,13 @@ __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c
 // (tA < tB, both requested) and tasks tA + 2W, tB + 2W have been asked of L2
 // (wt_prefetch); task_ctr (shared) hands out the next task numbers.  Register
 // ping-pong: one task is in flight while the other is computed; two tasks per
-// iteration keep the buffer indices static.
-template <int FMT, int KIND, int RS = 1, int MR = 1>
+// iteration keep the buffer indices static.  EAGER: the task that replaces
+// the one being computed is drawn first, and each of its chunk slots is
+// requested as soon as the slot has been consumed, so the warp keeps nearly
+// two tasks of weights in flight while it computes; otherwise the whole task
+// is requested after the computation (one task in flight meanwhile, but the
+// computation's shared-memory reads do not queue behind weight loads).
+template <int FMT, int KIND, int PL, int RS = 1, int MR = 1, bool EAGER = false>
 __device__ __forceinline__ void wt_run(const PhaseGeom& g, const PhaseW& w, const PhaseCta& c,
                                        const PhaseSmem& sm, uint4 (&bufA)[WT_NS][WT_CL],
                                        uint4 (&bufB)[WT_NS][WT_CL], int tA, int tB, int* task_ctr,
@@ -674,17 +728,35 @@ __device__ __forceinline__ void wt_run(const PhaseGeom& g, const PhaseW& w, cons
     return __shfl_sync(0xffffffffu, t, 0);
   };
   constexpr int AHEAD = 2 * WARP_TASK_WARPS;  // L2 lookahead in tasks
+  auto no_op = [](int) {};
+  if constexpr (!EAGER) {
+    for (;;) {
+      if (tA >= c.T) break;  // tA < tB here
+      wt_compute<FMT, KIND, PL, RS, MR>(g, c, sm, tA, bufA, lane, no_op);
+      tA = next_task();
+      wt_load<KIND, RS>(g, w, c, tA, bufA, pol, lane);
+      wt_prefetch<KIND, RS>(g, w, c, tA + AHEAD, lane);
+      if (tB >= c.T) break;  // tB < tA here
+      wt_compute<FMT, KIND, PL, RS, MR>(g, c, sm, tB, bufB, lane, no_op);
+      tB = next_task();
+      wt_load<KIND, RS>(g, w, c, tB, bufB, pol, lane);
+      wt_prefetch<KIND, RS>(g, w, c, tB + AHEAD, lane);
+    }
+    return;
+  }
   for (;;) {
     if (tA >= c.T) break;  // tA < tB here
-    wt_compute<FMT, KIND, RS, MR>(g, c, sm, tA, bufA, lane);
-    tA = next_task();
-    wt_load<KIND, RS>(g, w, c, tA, bufA, pol, lane);
-    wt_prefetch<KIND, RS>(g, w, c, tA + AHEAD, lane);
+    const int nA = next_task();
+    wt_prefetch<KIND, RS>(g, w, c, nA + AHEAD, lane);
+    wt_compute<FMT, KIND, PL, RS, MR>(g, c, sm, tA, bufA, lane,
+                                  [&](int k) { wt_load_chunk<KIND, RS>(g, w, c, nA, bufA, k, pol, lane); });
+    tA = nA;
     if (tB >= c.T) break;  // tB < tA here
-    wt_compute<FMT, KIND, RS, MR>(g, c, sm, tB, bufB, lane);
-    tB = next_task();
-    wt_load<KIND, RS>(g, w, c, tB, bufB, pol, lane);
-    wt_prefetch<KIND, RS>(g, w, c, tB + AHEAD, lane);
+    const int nB = next_task();
+    wt_prefetch<KIND, RS>(g, w, c, nB + AHEAD, lane);
+    wt_compute<FMT, KIND, PL, RS, MR>(g, c, sm, tB, bufB, lane,
+                                  [&](int k) { wt_load_chunk<KIND, RS>(g, w, c, nB, bufB, k, pol, lane); });
+    tB = nB;
   }
 }
 

@@ -154,6 +154,10 @@ __device__ __forceinline__ float cta_sum(float v, float* red, int tid) {
 
 __device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
 
+// x and h are staged in 16-bit fixed point (two byte planes): every output
+// of the executor (h, y) is bf16.
+constexpr int STACK_PL = 2;
+
 // RSG: rows per load stream of the gate/up phase (a.gu.RS); the down phase
 // always has one.
 template <int FMT, int RSG>
@@ -348,12 +352,12 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       }
       // one staging pass with the vector's fixed-point scale
       int ex = 0;
-      if constexpr (AFF) ex = fx_exponent(cta_max(m, red, tid));  // its barrier also publishes xraw
+      if constexpr (AFF) ex = fx_exponent<STACK_PL>(cta_max(m, red, tid));  // its barrier also publishes xraw
       else __syncthreads();
       const float xscale = exp2i(ex);
       for (int base = warp * 32; base < nu; base += WT_THREADS) {
         const int i = base + lane < nu ? base + lane : -1;
-        x_stage_unit<FMT>(a.gu, smG, i, i >= 0 ? reinterpret_cast<const uint4*>(smG.xraw)[i] : make_uint4(0, 0, 0, 0),
+        x_stage_unit<FMT, STACK_PL>(a.gu, smG, i, i >= 0 ? reinterpret_cast<const uint4*>(smG.xraw)[i] : make_uint4(0, 0, 0, 0),
                           xscale, false);
       }
       x_set_scale<FMT>(a.gu, smG, ex, tid, WT_THREADS);
@@ -369,7 +373,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
     }
     // ---- gate/up with the SwiGLU epilogue; h rows published in pairs
     {
-      wt_run<FMT, 0, RSG>(a.gu, gateup_w(Ly), cg, smG, bufA, bufB, tA, tB, &task_ctr, pol, lane);
+      wt_run<FMT, 0, STACK_PL, RSG>(a.gu, gateup_w(Ly), cg, smG, bufA, bufB, tA, tB, &task_ctr, pol, lane);
       __syncthreads();
       prefetch_down(l);  // HBM keeps streaming through the hand-off
       float hm = 0.f;
@@ -419,13 +423,13 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
             if (lane == 0) vec_max = hm;
           }
           __syncthreads();
-          if constexpr (AFF) ex = fx_exponent(vec_max);
+          if constexpr (AFF) ex = fx_exponent<STACK_PL>(vec_max);
         }
         const float xscale = exp2i(ex);
 #pragma unroll
         for (int k = 0; k < HB; ++k) {
           const int base = base0 + k * WT_THREADS;
-          if (base < nu) x_stage_unit<FMT>(a.dn, smD, base + lane < nu ? base + lane : -1, hv[k], xscale, true);
+          if (base < nu) x_stage_unit<FMT, STACK_PL>(a.dn, smD, base + lane < nu ? base + lane : -1, hv[k], xscale, true);
         }
         if (base0 + HB * WT_THREADS >= nu) break;
       }
@@ -442,7 +446,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
         stage_gateup_smem(l + 1);
         cp_async_commit();
       }
-      wt_run<FMT, 1>(a.dn, w, cd, smD, bufA, bufB, tA, tB, &task_ctr, pol, lane);
+      wt_run<FMT, 1, STACK_PL>(a.dn, w, cd, smD, bufA, bufB, tA, tB, &task_ctr, pol, lane);
       __syncthreads();
       if (l + 1 < a.L) prefetch_gateup(l + 1);  // HBM keeps streaming through the hand-off
       // epilogue: y = h . Wd[n] + summed_l[n]; summed_{l+1} = values_{l+1} + y
@@ -494,7 +498,7 @@ static bool plan_stack(StackPlanImpl* P, const DeviceInfo* di) {
   if (a.dn.rows_alloc > 2 * WT_THREADS) return false;  // one pair of down rows per thread
   const int Kmax = P->d > P->f ? P->d : P->f;
   size_t off = (size_t)Kmax * 2;  // xraw
-  a.off_xs = (int)off; off += xs_bytes<FMT>(Kmax);
+  a.off_xs = (int)off; off += xs_bytes<FMT, STACK_PL>(Kmax);
   a.off_tail_g = (int)off; off += pg;  // plan_phase's phase_tail_bytes (16-byte multiples)
   a.off_tail_d = (int)off; off += pd;
   a.off_wn = (int)off; off += (size_t)P->d * 2;

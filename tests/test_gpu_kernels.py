@@ -303,6 +303,47 @@ def test_indexing_gateup_bit_exact(mt, gemv, bits, group, M, K, N):
     assert np.array_equal(h.cpu().numpy(), (g_ref * u_ref).astype(np.float32))
 
 
+@pytest.mark.parametrize("bits,group,M,K,N", [(8, 32, 1, 128, 45), (8, 64, 2, 512, 33), (8, 64, 1, 1024, 40),
+                                              (4, 32, 1, 256, 23), (4, 64, 1, 2048, 20), (4, 128, 2, 384, 9)])
+def test_indexing_down_bf16_out_bit_exact(mt, gemv, bits, group, M, K, N):
+    """bf16 outputs, which the one-row kernels compute from a 16-bit
+    fixed-point x: in the exact case every sum is exact in fp32, so each
+    output is the one nearest-even bf16 rounding of the exact value.  (K = 1024
+    INT8 and K = 2048 INT4 rows are 64 chunks: two rows per load stream.)"""
+    rng = np.random.default_rng(bits * 3000 + group + K + N + M)
+    codes, s, b = _exact_affine(N, K, group, bits, rng)
+    x = oracle.bf16_from_f64(rng.integers(-4, 5, size=(M, K)).astype(np.float64))
+    res = oracle.bf16_from_f64(rng.integers(-8, 9, size=(M, N)).astype(np.float64))
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    mt.mt_down_residual(dev_bf16(x), torch.from_numpy(oracle.pack_codes(codes, bits)).cuda(), dev_bf16(s),
+                        dev_bf16(b), group, dev_bf16(res), y, fmt=1 if bits == 8 else 2)
+    torch.cuda.synchronize()
+    ref = oracle.down_residual(x, oracle.Weight(oracle.FMT_CODES, codes, s, b, group), res)
+    assert np.array_equal(host_bits(y), oracle.bf16_from_f64(ref))
+
+
+@pytest.mark.parametrize("bits,group,M,K,N", [(8, 32, 1, 256, 31), (8, 128, 2, 512, 20), (8, 64, 1, 1024, 16),
+                                              (4, 64, 1, 512, 12), (4, 32, 1, 2048, 10)])
+def test_indexing_gateup_bf16_out_bit_exact(mt, gemv, bits, group, M, K, N):
+    # as the fp32 case (g >= 40, silu(g) == g in fp32); the kernel rounds the
+    # product g * u to fp32 and then to bf16
+    rng = np.random.default_rng(bits * 91 + group + K + N + M)
+    cg, sgb, bgb = _exact_affine(N, K, group, bits, rng, bias_lo=128, bias_hi=256)
+    cu, sub, bub = _exact_affine(N, K, group, bits, rng)
+    x = oracle.bf16_from_f64(rng.integers(1, 5, size=(M, K)).astype(np.float64))
+    Wg = oracle.Weight(oracle.FMT_CODES, cg, sgb, bgb, group)
+    Wu = oracle.Weight(oracle.FMT_CODES, cu, sub, bub, group)
+    _, g_ref, u_ref = oracle.swiglu_gateup(x, Wg, Wu, return_gu=True)
+    assert np.all(g_ref >= 40.0)
+    h = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    mt.mt_swiglu_gateup(dev_bf16(x), torch.from_numpy(oracle.pack_codes(cg, bits)).cuda(),
+                        torch.from_numpy(oracle.pack_codes(cu, bits)).cuda(), dev_bf16(np.stack([sgb, sub])),
+                        dev_bf16(np.stack([bgb, bub])), group, h, fmt=1 if bits == 8 else 2)
+    torch.cuda.synchronize()
+    want = oracle.bf16_from_f64((g_ref * u_ref).astype(np.float32).astype(np.float64))
+    assert np.array_equal(host_bits(h), want)
+
+
 def test_indexing_bf16_weights_bit_exact(mt, gemv):
     rng = np.random.default_rng(5)
     M, K, N = 2, 1000, 37

@@ -479,6 +479,23 @@ __device__ __forceinline__ float cta_max(float v, float* red, int tid) {
   return m;
 }
 
+// Sums four values over the warp in one butterfly: at step 16 a lane keeps
+// a, b (bit 4 clear) or c, d (set) and sends the other pair; at step 8 it
+// keeps the first (bit 3 clear) or second of its pair; steps 4, 2, 1 finish.
+// Lane l returns the warp sum of value 2 * bit4(l) + bit3(l) of (a, b, c, d),
+// added in the same tree as a full butterfly of that value.
+__device__ __forceinline__ float reduce4_lanes(float a, float b, float c, float d, int lane) {
+  const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0;
+  float x = h16 ? c : a, y = h16 ? d : b;
+  x += __shfl_xor_sync(0xffffffffu, h16 ? a : c, 16);
+  y += __shfl_xor_sync(0xffffffffu, h16 ? b : d, 16);
+  float z = h8 ? y : x;
+  z += __shfl_xor_sync(0xffffffffu, h8 ? x : y, 8);
+#pragma unroll
+  for (int off = 4; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+  return z;
+}
+
 // wt_compute for RS = 2 (P == 1, rows of 64 chunks): stream v holds rows
 // r_v and r_v + 1, r_v = 2 (t * RW + v) for down and 2t (both matrices) for
 // gate/up; a lane's chunks k = 0, 1 (chunk lane + 32 k) are row r_v and
@@ -498,6 +515,21 @@ __device__ __forceinline__ void wt_compute_rs2(const PhaseGeom& g, const PhaseCt
   constexpr int RW = KIND == 0 ? 1 : 2;
   static_assert(WT_CL == 4, "two rows of two chunks per lane");
   auto row_of = [&](int v, int r) { return (t * RW + (KIND == 0 ? 0 : v)) * 2 + r; };
+  // scales of stream v, row r: chunk lane + 32 (k & 1) is in group gi0 +
+  // (k & 1) * gstep (exact, as in wt_compute)
+  const uint16_t* sc[WT_NS][2];
+  int gstep = 0;
+  if constexpr (AFF) {
+    const int gi0 = (lane * EPC) >> g.lg_group;
+    gstep = (32 * EPC) >> g.lg_group;
+#pragma unroll
+    for (int v = 0; v < WT_NS; ++v)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int m = KIND == 0 ? v : 0, rl = min(row_of(v, r), c.rows - 1);
+        sc[v][r] = sm.sbr + (size_t)(2 * m) * g.sb_stride + rl * g.G + gi0;
+      }
+  }
   float acc[WT_NS][2];
 #pragma unroll
   for (int v = 0; v < WT_NS; ++v) acc[v][0] = acc[v][1] = 0.f;
@@ -507,13 +539,8 @@ __device__ __forceinline__ void wt_compute_rs2(const PhaseGeom& g, const PhaseCt
 #pragma unroll
     for (int v = 0; v < WT_NS; ++v) {
       const float d = chunk_dot<FMT, PL>(buf[v][k], sm.xs, ch, g.CPR);
-      if constexpr (AFF) {
-        const int m = KIND == 0 ? v : 0, rl = min(row_of(v, r), c.rows - 1);
-        const int gi = (ch * EPC) >> g.lg_group;
-        acc[v][r] = fmaf(bf16f(sm.sbr[(size_t)(2 * m) * g.sb_stride + rl * g.G + gi]), d, acc[v][r]);
-      } else {
-        acc[v][r] += d;
-      }
+      if constexpr (AFF) acc[v][r] = fmaf(bf16f(sc[v][r][(k & 1) * gstep]), d, acc[v][r]);
+      else acc[v][r] += d;
     }
     after(k);
   }
@@ -537,22 +564,13 @@ __device__ __forceinline__ void wt_compute_rs2(const PhaseGeom& g, const PhaseCt
         }
     }
   }
-#pragma unroll
-  for (int v = 0; v < WT_NS; ++v)
-#pragma unroll
-    for (int r = 0; r < 2; ++r)
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) vals[v][r] += __shfl_xor_sync(0xffffffffu, vals[v][r], off);
-  if (lane < 2 * WT_NS) {
-    const int v = lane >> 1, r = lane & 1;
-    float val = vals[0][0];
-#pragma unroll
-    for (int vv = 0; vv < WT_NS; ++vv)
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr)
-        if (lane == 2 * vv + rr) val = vals[vv][rr];
+  // the four warp sums in one butterfly: lanes keep stream v = bit 4 and row
+  // r = bit 3 of their index, sending the others at the first two steps
+  const float s = reduce4_lanes(vals[0][0], vals[0][1], vals[1][0], vals[1][1], lane);
+  if ((lane & 7) == 0) {
+    const int v = (lane >> 4) & 1, r = (lane >> 3) & 1;
     const int m = KIND == 0 ? v : 0, rl = row_of(v, r);
-    if (rl < c.rows) sm.parts[(size_t)rl * NW + m] = val;
+    if (rl < c.rows) sm.parts[(size_t)rl * NW + m] = s;
   }
 }
 
@@ -577,20 +595,26 @@ __device__ __forceinline__ void wt_compute_mr2(const PhaseGeom& g, const PhaseCt
   float acc[WT_NS][2];
 #pragma unroll
   for (int v = 0; v < WT_NS; ++v) acc[v][0] = acc[v][1] = 0.f;
+  // scales: slot k in group gi0 + k*gstep (exact, as in wt_compute)
+  const int gstep = (32 * EPC) >> g.lg_group;
+  const uint16_t* sc[WT_NS];
+#pragma unroll
+  for (int v = 0; v < WT_NS; ++v) {
+    const int mt = KIND == 0 ? v : 0, rl = min(rl0 + (KIND == 0 ? 0 : v), c.rows - 1);
+    sc[v] = sm.sbr + (size_t)(2 * mt) * g.sb_stride + rl * g.G + (((p * g.CPP + lane) * EPC) >> g.lg_group);
+  }
 #pragma unroll
   for (int k = 0; k < WT_CL; ++k) {
     const int j = lane + 32 * k;
     if (j < g.CPP) {
       const int ch = p * g.CPP + j;
-      const int gi = (ch * EPC) >> g.lg_group;
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const uint4* xs = sm.xs + (size_t)m * sm.xs_stride;
 #pragma unroll
         for (int v = 0; v < WT_NS; ++v) {
           const float d = chunk_dot<FMT, PL>(buf[v][k], xs, ch, g.CPR);
-          const int mt = KIND == 0 ? v : 0, rl = min(rl0 + (KIND == 0 ? 0 : v), c.rows - 1);
-          acc[v][m] = fmaf(bf16f(sm.sbr[(size_t)(2 * mt) * g.sb_stride + rl * g.G + gi]), d, acc[v][m]);
+          acc[v][m] = fmaf(bf16f(sc[v][k * gstep]), d, acc[v][m]);
         }
       }
     }
@@ -612,22 +636,13 @@ __device__ __forceinline__ void wt_compute_mr2(const PhaseGeom& g, const PhaseCt
       for (int m = 0; m < 2; ++m) vals[v][m] = fmaf(b, sm.gsum[m * g.G + gi], vals[v][m]);
     }
   }
-#pragma unroll
-  for (int v = 0; v < WT_NS; ++v)
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) vals[v][m] += __shfl_xor_sync(0xffffffffu, vals[v][m], off);
-  if (lane < 2 * WT_NS) {
-    const int v = lane >> 1, m = lane & 1;
-    float val = vals[0][0];
-#pragma unroll
-    for (int vv = 0; vv < WT_NS; ++vv)
-#pragma unroll
-      for (int mm = 0; mm < 2; ++mm)
-        if (lane == 2 * vv + mm) val = vals[vv][mm];
+  // the four warp sums in one butterfly (stream v = bit 4, activation row m
+  // = bit 3 of the lane that ends with the sum)
+  const float s = reduce4_lanes(vals[0][0], vals[0][1], vals[1][0], vals[1][1], lane);
+  if ((lane & 7) == 0) {
+    const int v = (lane >> 4) & 1, m = (lane >> 3) & 1;
     const int mt = KIND == 0 ? v : 0, rl = rl0 + (KIND == 0 ? 0 : v);
-    if (rl < c.rows) sm.parts[(((size_t)rl * g.P + p) * NW + mt) * 2 + m] = val;
+    if (rl < c.rows) sm.parts[(((size_t)rl * g.P + p) * NW + mt) * 2 + m] = s;
   }
 }
 
@@ -656,6 +671,19 @@ __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c
   const int rg = (int)(((unsigned long long)(unsigned)t * g.p_mul) >> 32);
   const int p = t - rg * g.P;
   const int rl0 = rg * RW;
+  // scales: chunk slot k of this lane is chunk p*CPP + lane + 32k of the row,
+  // in group gi0 + k*gstep (32 chunks span whole groups, so the step is exact)
+  const uint16_t* sc[WT_NS];
+  int gstep = 0;
+  if constexpr (AFF) {
+    const int gi0 = ((p * g.CPP + lane) * EPC) >> g.lg_group;
+    gstep = (32 * EPC) >> g.lg_group;
+#pragma unroll
+    for (int v = 0; v < WT_NS; ++v) {
+      const int m = KIND == 0 ? v : 0, rl = min(rl0 + (KIND == 0 ? 0 : v), c.rows - 1);
+      sc[v] = sm.sbr + (size_t)(2 * m) * g.sb_stride + rl * g.G + gi0;
+    }
+  }
   float acc[WT_NS];
 #pragma unroll
   for (int v = 0; v < WT_NS; ++v) acc[v] = 0.f;
@@ -667,13 +695,8 @@ __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c
 #pragma unroll
       for (int v = 0; v < WT_NS; ++v) {
         const float d = chunk_dot<FMT, PL>(buf[v][k], sm.xs, ch, g.CPR);
-        if constexpr (AFF) {
-          const int m = KIND == 0 ? v : 0, rl = min(rl0 + (KIND == 0 ? 0 : v), c.rows - 1);
-          const int gi = (ch * EPC) >> g.lg_group;
-          acc[v] = fmaf(bf16f(sm.sbr[(size_t)(2 * m) * g.sb_stride + rl * g.G + gi]), d, acc[v]);
-        } else {
-          acc[v] += d;
-        }
+        if constexpr (AFF) acc[v] = fmaf(bf16f(sc[v][k * gstep]), d, acc[v]);
+        else acc[v] += d;
       }
     }
     after(k);
@@ -693,17 +716,18 @@ __device__ __forceinline__ void wt_compute(const PhaseGeom& g, const PhaseCta& c
       }
     }
   }
+  // the two streams' warp sums in one butterfly: at its first step lanes
+  // 0-15 keep stream 0 and lanes 16-31 stream 1, each sending the other
+  static_assert(WT_NS == 2, "two streams per task");
+  const bool hi = (lane & 16) != 0;
+  float r = hi ? vals[1] : vals[0];
+  r += __shfl_xor_sync(0xffffffffu, hi ? vals[0] : vals[1], 16);
 #pragma unroll
-  for (int v = 0; v < WT_NS; ++v)
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) vals[v] += __shfl_xor_sync(0xffffffffu, vals[v], off);
-  if (lane < WT_NS) {
-    float val = vals[0];
-#pragma unroll
-    for (int v = 1; v < WT_NS; ++v)
-      if (lane == v) val = vals[v];
-    const int m = KIND == 0 ? lane : 0, rl = rl0 + (KIND == 0 ? 0 : lane);
-    if (rl < c.rows) sm.parts[((size_t)rl * g.P + p) * NW + m] = val;
+  for (int off = 8; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+  if ((lane & 15) == 0) {
+    const int v = lane >> 4;
+    const int m = KIND == 0 ? v : 0, rl = rl0 + (KIND == 0 ? 0 : v);
+    if (rl < c.rows) sm.parts[((size_t)rl * g.P + p) * NW + m] = r;
   }
 }
 
@@ -742,21 +766,21 @@ __device__ __forceinline__ void wt_run(const PhaseGeom& g, const PhaseW& w, cons
       wt_load<KIND, RS>(g, w, c, tB, bufB, pol, lane);
       wt_prefetch<KIND, RS>(g, w, c, tB + AHEAD, lane);
     }
-    return;
-  }
-  for (;;) {
-    if (tA >= c.T) break;  // tA < tB here
-    const int nA = next_task();
-    wt_prefetch<KIND, RS>(g, w, c, nA + AHEAD, lane);
-    wt_compute<FMT, KIND, PL, RS, MR>(g, c, sm, tA, bufA, lane,
-                                  [&](int k) { wt_load_chunk<KIND, RS>(g, w, c, nA, bufA, k, pol, lane); });
-    tA = nA;
-    if (tB >= c.T) break;  // tB < tA here
-    const int nB = next_task();
-    wt_prefetch<KIND, RS>(g, w, c, nB + AHEAD, lane);
-    wt_compute<FMT, KIND, PL, RS, MR>(g, c, sm, tB, bufB, lane,
-                                  [&](int k) { wt_load_chunk<KIND, RS>(g, w, c, nB, bufB, k, pol, lane); });
-    tB = nB;
+  } else {
+    for (;;) {
+      if (tA >= c.T) break;  // tA < tB here
+      const int nA = next_task();
+      wt_prefetch<KIND, RS>(g, w, c, nA + AHEAD, lane);
+      wt_compute<FMT, KIND, PL, RS, MR>(g, c, sm, tA, bufA, lane,
+                                    [&](int k) { wt_load_chunk<KIND, RS>(g, w, c, nA, bufA, k, pol, lane); });
+      tA = nA;
+      if (tB >= c.T) break;  // tB < tA here
+      const int nB = next_task();
+      wt_prefetch<KIND, RS>(g, w, c, nB + AHEAD, lane);
+      wt_compute<FMT, KIND, PL, RS, MR>(g, c, sm, tB, bufB, lane,
+                                    [&](int k) { wt_load_chunk<KIND, RS>(g, w, c, nB, bufB, k, pol, lane); });
+      tB = nB;
+    }
   }
 }
 

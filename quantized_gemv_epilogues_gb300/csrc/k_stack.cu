@@ -377,17 +377,21 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       __syncthreads();
       prefetch_down(l);  // HBM keeps streaming through the hand-off
       float hm = 0.f;
-      for (int j = tid; j < npair_g; j += WT_THREADS) {
-        uint16_t hb[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float g = row_total<2>(a.gu, smG.parts, 2 * j + e, 0);
-          const float u = row_total<2>(a.gu, smG.parts, 2 * j + e, 1);
-          hb[e] = f2bf(g / (1.0f + expf(-g)) * u);
-          hm = fmaxf(hm, fabsf(bf16f(hb[e])));
+      for (int i0 = 0; i0 < 2 * npair_g; i0 += WT_THREADS) {  // one row per thread, pairs stored by lane pairs
+        const int i = i0 + tid;
+        const bool ok = i < 2 * npair_g;
+        uint16_t hb = 0;
+        if (ok) {
+          const float g = row_total<2>(a.gu, smG.parts, i, 0);
+          const float u = row_total<2>(a.gu, smG.parts, i, 1);
+          hb = f2bf(g / (1.0f + expf(-g)) * u);
+          hm = fmaxf(hm, fabsf(bf16f(hb)));
         }
-        *reinterpret_cast<uint32_t*>(a.hbuf + cg.r_begin + 2 * j) = pack2(hb[0], hb[1]);
-        if (a.tr_h) *reinterpret_cast<uint32_t*>(a.tr_h + (size_t)l * f + cg.r_begin + 2 * j) = pack2(hb[0], hb[1]);
+        const uint16_t ho = (uint16_t)__shfl_down_sync(0xffffffffu, (uint32_t)hb, 1);
+        if (ok && (i & 1) == 0) {
+          *reinterpret_cast<uint32_t*>(a.hbuf + cg.r_begin + i) = pack2(hb, ho);
+          if (a.tr_h) *reinterpret_cast<uint32_t*>(a.tr_h + (size_t)l * f + cg.r_begin + i) = pack2(hb, ho);
+        }
       }
       hm = cta_max(hm, red, tid);  // its barrier also orders the h stores before the release
       if (tid == 0) {

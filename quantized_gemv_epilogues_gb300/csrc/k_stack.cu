@@ -341,14 +341,13 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       for (int i = tid + 2 * WT_THREADS; i < nu; i += WT_THREADS)  // d > 8192
         norm_unit(i, ldg_cg(a.sbuf + (size_t)i * 8));
       if (tid == 0) task_ctr = 2 * WARP_TASK_WARPS;  // tasks 0..2W-1 are taken statically
-      // the first two gate/up tasks (mostly L2 hits after prefetch_gateup),
-      // in flight while x is staged (shared memory only)
+      // the first gate/up task (mostly L2 hits after prefetch_gateup), in
+      // flight while x is staged; the second is requested after the staging
+      // (loads in flight slow the staging's shared-memory accesses)
       {
         const PhaseW w = gateup_w(Ly);
         wt_load<0, RSG>(a.gu, w, cg, tA, bufA, pol, lane);
-        wt_load<0, RSG>(a.gu, w, cg, tB, bufB, pol, lane);
         wt_prefetch<0, RSG>(a.gu, w, cg, tA + 2 * WARP_TASK_WARPS, lane);
-        wt_prefetch<0, RSG>(a.gu, w, cg, tB + 2 * WARP_TASK_WARPS, lane);
       }
       // one staging pass with the vector's fixed-point scale
       int ex = 0;
@@ -373,6 +372,8 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
     }
     // ---- gate/up with the SwiGLU epilogue; h rows published in pairs
     {
+      wt_load<0, RSG>(a.gu, gateup_w(Ly), cg, tB, bufB, pol, lane);
+      wt_prefetch<0, RSG>(a.gu, gateup_w(Ly), cg, tB + 2 * WARP_TASK_WARPS, lane);
       wt_run<FMT, 0, STACK_PL, RSG>(a.gu, gateup_w(Ly), cg, smG, bufA, bufB, tA, tB, &task_ctr, pol, lane);
       __syncthreads();
       prefetch_down(l);  // HBM keeps streaming through the hand-off

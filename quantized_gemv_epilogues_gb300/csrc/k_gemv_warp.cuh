@@ -224,7 +224,9 @@ mt_status run_gemv_warp(const GemvProblem& p, const Launch& l) {
       for (int mr = 1; mr <= 2; ++mr)
         for (int rs = 1; rs <= 2; ++rs)
           for (int pl = AFF ? 2 : 3; pl <= 3; ++pl) {
-            const WarpKernT k = pl == 2 ? warp_kernel_for<FMT, KIND, 2>(mr, rs) : warp_kernel_for<FMT, KIND, 3>(mr, rs);
+            WarpKernT k = warp_kernel_for<FMT, KIND, 3>(mr, rs);
+            if constexpr (AFF)
+              if (pl == 2) k = warp_kernel_for<FMT, KIND, 2>(mr, rs);
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
             if (e != cudaSuccess) return cuda_fail(e);
           }

@@ -197,13 +197,19 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       cp_async16(reinterpret_cast<uint4*>(&lay_s[l & 1]) + tid,
                  reinterpret_cast<const uint4*>(a.layers + l) + tid);
   };
-  // Asks L2 for the first `pre` bytes of the CTA's (contiguous) rows of W:
-  // one bulk prefetch, issued by the calling thread.
-  auto l2_ahead = [&](const PhaseGeom& g, const PhaseCta& c, const uint8_t* W, int pre) {
+  // Asks L2 for bytes [off, off + n) of the CTA's (contiguous) rows of W,
+  // clipped to the rows: one bulk prefetch, issued by the calling thread.
+  auto l2_range = [&](const PhaseGeom& g, const PhaseCta& c, const uint8_t* W, int off, int n) {
     const size_t all = (size_t)c.rows * g.row_bytes;
-    const uint32_t n = (uint32_t)(all < (size_t)pre ? all : (size_t)pre);
-    if (n) bulk_prefetch_l2(W + (size_t)c.r_begin * g.row_bytes, n);
+    if (n <= 0 || (size_t)off >= all) return;
+    const size_t m = all - (size_t)off < (size_t)n ? all - (size_t)off : (size_t)n;
+    bulk_prefetch_l2(W + (size_t)c.r_begin * g.row_bytes + off, (uint32_t)m);
   };
+  // A phase's prefetch is split: the first three quarters are issued when the
+  // previous task loop ends, the last quarter by thread 0 right after its
+  // arrival at the barrier (the arrival's release fence waits for the CTA's
+  // bulk prefetches in flight, so a smaller first part shortens it).
+  constexpr int pre_g1 = (STACK_PRE_GATEUP * 3 / 4) & ~15, pre_d1 = (STACK_PRE_DOWN * 3 / 4) & ~15;
   // What a phase needs that does not depend on the hand-off is requested
   // early: its scales and biases and (gate/up) the RMSNorm gain go to shared
   // memory at the start of the PREVIOUS phase's task loop (stage_*_smem; the
@@ -221,14 +227,19 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
     const StackLayerDev& Ly = lay_s[l & 1];
     if constexpr (AFF) stage_sb<1>(a.dn, down_w(Ly), cd, smD.sbr, tid, WT_THREADS);
   };
-  auto prefetch_gateup = [&](int l) {
+  auto prefetch_gateup = [&](int l, int n) {
     const StackLayerDev& Ly = lay_s[l & 1];
-    if (tid == 32) l2_ahead(a.gu, cg, Ly.Wg, a.pre_g);
-    if (tid == 64) l2_ahead(a.gu, cg, Ly.Wu, a.pre_g);
+    if (tid == 32) l2_range(a.gu, cg, Ly.Wg, 0, n);
+    if (tid == 64) l2_range(a.gu, cg, Ly.Wu, 0, n);
+  };
+  auto prefetch_gateup_rest = [&](int l) {  // thread 0, after its arrival
+    const StackLayerDev& Ly = lay_s[l & 1];
+    l2_range(a.gu, cg, Ly.Wg, pre_g1, a.pre_g - pre_g1);
+    l2_range(a.gu, cg, Ly.Wu, pre_g1, a.pre_g - pre_g1);
   };
   auto prefetch_down = [&](int l) {
     const StackLayerDev& Ly = lay_s[l & 1];
-    if (tid == 32) l2_ahead(a.dn, cd, Ly.Wd, a.pre_d);
+    if (tid == 32) l2_range(a.dn, cd, Ly.Wd, 0, pre_d1);
   };
   // Completes barrier nbar: thread 0 polls, then every thread learns the
   // verdict.  (Thread 0 issues no other loads between its arrival and here:
@@ -243,7 +254,9 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
   // rounding): pair j (rows 2j, 2j+1 of the CTA's down rows) is computed and
   // stored by thread j, its squares folded into the CTA's partial sum, which
   // thread 0 stores before arriving at the barrier.  r2: the pair of r.
-  auto publish_summed = [&](uint32_t v2, uint32_t r2, bool have) {
+  // next_l >= 0: thread 0 then asks L2 for the rest of that layer's gate/up
+  // prefetch.
+  auto publish_summed = [&](uint32_t v2, uint32_t r2, bool have, int next_l) {
     float ss = 0.f;
     if (have) {
       const uint16_t s0 = f2bf(bf16lo(v2) + bf16lo(r2));
@@ -255,6 +268,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
     if (tid == 0) {
       a.ssq[cta] = ss;
       grid_arrive(a.ctl);
+      if (next_l >= 0) prefetch_gateup_rest(next_l);
     }
   };
 
@@ -272,9 +286,9 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       v2 = *reinterpret_cast<const uint32_t*>(a.values + cd.r_begin + 2 * tid);
       r2 = *reinterpret_cast<const uint32_t*>(a.residual + cd.r_begin + 2 * tid);
     }
-    publish_summed(v2, r2, have);
+    publish_summed(v2, r2, have, -1);
   }
-  prefetch_gateup(0);
+  prefetch_gateup(0, a.pre_g);  // all of it: nothing waits on this arrival's fence
   if (warp > 0) stage_gateup_smem(0);
   cp_async_commit();
   if (!grid_wait()) { cp_async_wait_all(); return; }
@@ -398,6 +412,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       if (tid == 0) {
         a.hmax[cta] = hm;
         grid_arrive(a.ctl);  // h and its largest |h| are published
+        l2_range(a.dn, cd, Ly.Wd, pre_d1, a.pre_d - pre_d1);  // the rest of the down prefetch
       }
     }
     // ---- down
@@ -453,7 +468,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       }
       wt_run<FMT, 1, STACK_PL>(a.dn, w, cd, smD, bufA, bufB, tA, tB, &task_ctr, pol, lane);
       __syncthreads();
-      if (l + 1 < a.L) prefetch_gateup(l + 1);  // HBM keeps streaming through the hand-off
+      if (l + 1 < a.L) prefetch_gateup(l + 1, pre_g1);  // HBM keeps streaming through the hand-off
       // epilogue: y = h . Wd[n] + summed_l[n]; summed_{l+1} = values_{l+1} + y
       const bool last = l + 1 == a.L;
       const bool have = tid < npair_d;
@@ -470,7 +485,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
         if (last) *reinterpret_cast<uint32_t*>(a.out_y + cd.r_begin + 2 * tid) = y2;
       }
       if (last) break;
-      publish_summed(vnx, y2, have);
+      publish_summed(vnx, y2, have, l + 1);
       if (!grid_wait()) { cp_async_wait_all(); return; }
     }
   }

@@ -119,11 +119,24 @@ typedef enum mt_option {
                       M = 1 and tensor-core kernel for M > 1; 1 team kernel
                       for every M; 2 tensor-core kernel for every M (shapes
                       a kernel cannot hold fall back to the team kernel) */
-  MT_OPT_TEST_BARRIER_EXTRA = 2 /* test hook for failure detection, 0 (default)
+  MT_OPT_TEST_BARRIER_EXTRA = 2, /* test hook for failure detection, 0 (default)
                       to 8: executor runs started while it is n > 0 make
                       every grid barrier wait for n arrivals that never come,
                       so the bounded wait expires (~1 s) and the run ends with
                       MT_ERR_TIMEOUT in mt_device_error() */
+  MT_OPT_ACT_BITS = 3 /* bits of the fixed-point activation x = X 2^-e (one
+                      power of two per activation row) with which the one-row
+                      affine GEMVs with bf16 outputs and the executor compute
+                      their dot products: 16 (default) or 24.  fp32 outputs
+                      always use 24.  With 16 bits, elements more than 2^6
+                      below the row's largest |x| are rounded to 2^-14 of it:
+                      within the 2e-3 bf16 bound on activations whose
+                      max|x| / rms(x) stays below ~30, but a row with a channel
+                      ~1000x the others (one weight row's output dominated by
+                      the other channels) can exceed it; 24 bits keep such
+                      rows within the bound at ~1.5 us more per executor layer
+                      (Qwen3-8B shape).  A plan takes the value set when it is
+                      created. */
 } mt_option;
 
 /*

@@ -46,7 +46,7 @@ MT_OK, MT_ERR_NULL, MT_ERR_SHAPE, MT_ERR_GROUP, MT_ERR_ALIGN = 0, 1, 2, 3, 4
 MT_ERR_FORMAT, MT_ERR_ALIAS, MT_ERR_CUDA, MT_ERR_TIMEOUT = 5, 6, 7, 8
 MT_BF16, MT_F32 = 0, 1
 MT_W_BF16, MT_W_AFFINE8, MT_W_AFFINE4, MT_W_MXFP8, MT_W_MXFP4 = 0, 1, 2, 3, 4
-MT_OPT_PDL, MT_OPT_GEMV, MT_OPT_TEST_BARRIER_EXTRA = 0, 1, 2
+MT_OPT_PDL, MT_OPT_GEMV, MT_OPT_TEST_BARRIER_EXTRA, MT_OPT_ACT_BITS = 0, 1, 2, 3
 
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _SIGS = {

@@ -205,10 +205,11 @@ mt_status run_gemv_warp(const GemvProblem& p, const Launch& l) {
   a.out = p.out;
   a.out_f32 = p.out_f32 ? 1 : 0;
 
-  // affine weights with bf16 outputs: x in 16-bit fixed point (2 byte planes),
-  // with fp32 outputs in 24-bit (3 planes); dense bf16 weights: x as stored
+  // affine weights with bf16 outputs: x in 16-bit fixed point (2 byte planes)
+  // unless MT_OPT_ACT_BITS asks for 24; with fp32 outputs in 24-bit (3
+  // planes); dense bf16 weights: x as stored
   constexpr bool AFF = FmtTraits<FMT>::AFFINE;
-  const bool pl2 = AFF && !p.out_f32;
+  const bool pl2 = AFF && !p.out_f32 && act_bits() == 16;
   const size_t smem = (size_t)MR * ((size_t)p.K * 2 + (pl2 ? xs_bytes<FMT, 2>(p.K) : xs_bytes<FMT, 3>(p.K))) +
                       smem_parts +
                       (KIND == 1 ? ((size_t)MR * a.g.rows_alloc * 2 + 15) / 16 * 16 : 0);  // res_s

@@ -154,13 +154,11 @@ __device__ __forceinline__ float cta_sum(float v, float* red, int tid) {
 
 __device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
 
-// x and h are staged in 16-bit fixed point (two byte planes): every output
-// of the executor (h, y) is bf16.
-constexpr int STACK_PL = 2;
-
 // RSG: rows per load stream of the gate/up phase (a.gu.RS); the down phase
-// always has one.
-template <int FMT, int RSG>
+// always has one.  PL: bytes of the fixed-point x and h (every output of the
+// executor, h and y, is bf16: 2 by default, 3 when MT_OPT_ACT_BITS is 24 at
+// plan creation).
+template <int FMT, int RSG, int PL>
 __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArgs a) {
   constexpr bool AFF = FmtTraits<FMT>::AFFINE;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -365,12 +363,12 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
       }
       // one staging pass with the vector's fixed-point scale
       int ex = 0;
-      if constexpr (AFF) ex = fx_exponent<STACK_PL>(cta_max(m, red, tid));  // its barrier also publishes xraw
+      if constexpr (AFF) ex = fx_exponent<PL>(cta_max(m, red, tid));  // its barrier also publishes xraw
       else __syncthreads();
       const float xscale = exp2i(ex);
       for (int base = warp * 32; base < nu; base += WT_THREADS) {
         const int i = base + lane < nu ? base + lane : -1;
-        x_stage_unit<FMT, STACK_PL>(a.gu, smG, i, i >= 0 ? reinterpret_cast<const uint4*>(smG.xraw)[i] : make_uint4(0, 0, 0, 0),
+        x_stage_unit<FMT, PL>(a.gu, smG, i, i >= 0 ? reinterpret_cast<const uint4*>(smG.xraw)[i] : make_uint4(0, 0, 0, 0),
                           xscale, false);
       }
       x_set_scale<FMT>(a.gu, smG, ex, tid, WT_THREADS);
@@ -388,7 +386,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
     {
       wt_load<0, RSG>(a.gu, gateup_w(Ly), cg, tB, bufB, pol, lane);
       wt_prefetch<0, RSG>(a.gu, gateup_w(Ly), cg, tB + 2 * WARP_TASK_WARPS, lane);
-      wt_run<FMT, 0, STACK_PL, RSG>(a.gu, gateup_w(Ly), cg, smG, bufA, bufB, tA, tB, &task_ctr, pol, lane);
+      wt_run<FMT, 0, PL, RSG>(a.gu, gateup_w(Ly), cg, smG, bufA, bufB, tA, tB, &task_ctr, pol, lane);
       __syncthreads();
       prefetch_down(l);  // HBM keeps streaming through the hand-off
       float hm = 0.f;
@@ -443,13 +441,13 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
             if (lane == 0) vec_max = hm;
           }
           __syncthreads();
-          if constexpr (AFF) ex = fx_exponent<STACK_PL>(vec_max);
+          if constexpr (AFF) ex = fx_exponent<PL>(vec_max);
         }
         const float xscale = exp2i(ex);
 #pragma unroll
         for (int k = 0; k < HB; ++k) {
           const int base = base0 + k * WT_THREADS;
-          if (base < nu) x_stage_unit<FMT, STACK_PL>(a.dn, smD, base + lane < nu ? base + lane : -1, hv[k], xscale, true);
+          if (base < nu) x_stage_unit<FMT, PL>(a.dn, smD, base + lane < nu ? base + lane : -1, hv[k], xscale, true);
         }
         if (base0 + HB * WT_THREADS >= nu) break;
       }
@@ -466,7 +464,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1) mlp_stack_kernel(const StackArg
         stage_gateup_smem(l + 1);
         cp_async_commit();
       }
-      wt_run<FMT, 1, STACK_PL>(a.dn, w, cd, smD, bufA, bufB, tA, tB, &task_ctr, pol, lane);
+      wt_run<FMT, 1, PL>(a.dn, w, cd, smD, bufA, bufB, tA, tB, &task_ctr, pol, lane);
       __syncthreads();
       if (l + 1 < a.L) prefetch_gateup(l + 1, pre_g1);  // HBM keeps streaming through the hand-off
       // epilogue: y = h . Wd[n] + summed_l[n]; summed_{l+1} = values_{l+1} + y
@@ -503,7 +501,7 @@ struct StackPlanImpl {
   void* alloc;          // device allocation owned by the plan
   void* run_state;      // what is zeroed before each run (the control line)
   size_t run_state_bytes;
-  const void* kernel;   // mlp_stack_kernel<FMT, RSG>
+  const void* kernel;   // mlp_stack_kernel<FMT, RSG, PL>
 };
 
 template <int FMT>
@@ -518,15 +516,19 @@ static bool plan_stack(StackPlanImpl* P, const DeviceInfo* di) {
   if (a.dn.rows_alloc > 2 * WT_THREADS) return false;  // one pair of down rows per thread
   const int Kmax = P->d > P->f ? P->d : P->f;
   size_t off = (size_t)Kmax * 2;  // xraw
-  a.off_xs = (int)off; off += xs_bytes<FMT, STACK_PL>(Kmax);
+  a.off_xs = (int)off; off += xs_bytes<FMT, 3>(Kmax);  // room for either width
   a.off_tail_g = (int)off; off += pg;  // plan_phase's phase_tail_bytes (16-byte multiples)
   a.off_tail_d = (int)off; off += pd;
   a.off_wn = (int)off; off += (size_t)P->d * 2;
   a.off_ssm = (int)off; off += (size_t)P->d * 2;
   P->smem = off;
   P->grid = grid;
-  P->kernel = a.gu.RS == 2 ? reinterpret_cast<const void*>(mlp_stack_kernel<FMT, 2>)
-                           : reinterpret_cast<const void*>(mlp_stack_kernel<FMT, 1>);
+  P->kernel = a.gu.RS == 2 ? reinterpret_cast<const void*>(mlp_stack_kernel<FMT, 2, 2>)
+                           : reinterpret_cast<const void*>(mlp_stack_kernel<FMT, 1, 2>);
+  if constexpr (FmtTraits<FMT>::AFFINE)  // dense bf16 weights stage x as stored
+    if (act_bits() == 24)
+      P->kernel = a.gu.RS == 2 ? reinterpret_cast<const void*>(mlp_stack_kernel<FMT, 2, 3>)
+                               : reinterpret_cast<const void*>(mlp_stack_kernel<FMT, 1, 3>);
   return true;
 }
 

@@ -14,6 +14,7 @@ static thread_local int g_last_cuda_error = 0;
 static std::atomic<int> g_opt_pdl{1};
 static std::atomic<int> g_opt_gemv{0};
 static std::atomic<int> g_opt_barrier_extra{0};
+static std::atomic<int> g_opt_act_bits{16};
 
 // Device error word: kernels with bounded waits record MT_ERR_TIMEOUT here.
 __device__ int g_device_error;
@@ -28,6 +29,7 @@ int* device_error_ptr() {
 
 int gemv_choice() { return g_opt_gemv.load(); }
 int test_barrier_extra() { return g_opt_barrier_extra.load(); }
+int act_bits() { return g_opt_act_bits.load(); }
 
 mt_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = (int)e;
@@ -328,6 +330,11 @@ mt_status mt_set_option(mt_option opt, int value) {
     g_opt_barrier_extra.store(value);
     return MT_OK;
   }
+  if (opt == MT_OPT_ACT_BITS) {
+    if (value != 16 && value != 24) return MT_ERR_FORMAT;
+    g_opt_act_bits.store(value);
+    return MT_OK;
+  }
   return MT_ERR_FORMAT;
 }
 
@@ -335,6 +342,7 @@ int mt_get_option(mt_option opt) {
   if (opt == MT_OPT_PDL) return g_opt_pdl.load();
   if (opt == MT_OPT_GEMV) return g_opt_gemv.load();
   if (opt == MT_OPT_TEST_BARRIER_EXTRA) return g_opt_barrier_extra.load();
+  if (opt == MT_OPT_ACT_BITS) return g_opt_act_bits.load();
   return -1;
 }
 

@@ -34,6 +34,9 @@ int gemv_choice();
 // (MT_OPT_TEST_BARRIER_EXTRA; 0 except in failure-detection tests).
 int test_barrier_extra();
 
+// MT_OPT_ACT_BITS: 16 or 24 (fixed-point activation bits for bf16 outputs).
+int act_bits();
+
 // Launches `kernel` with (grid, block, smem) on l.stream, adding the
 // programmatic-stream-serialization attribute when l.pdl is set.
 template <typename... KArgs, typename... Args>

@@ -265,6 +265,10 @@ def test_status_strings_and_options(lib):
     assert lib.mt_set_option(1, 0) == 0
     assert lib.mt_set_option(2, 9) == FORMAT and lib.mt_set_option(2, -1) == FORMAT
     assert lib.mt_set_option(2, 0) == 0 and lib.mt_get_option(2) == 0
+    assert lib.mt_get_option(3) == 16  # fixed-point activation bits, default
+    assert lib.mt_set_option(3, 20) == FORMAT and lib.mt_get_option(3) == 16
+    assert lib.mt_set_option(3, 24) == 0 and lib.mt_get_option(3) == 24
+    assert lib.mt_set_option(3, 16) == 0 and lib.mt_get_option(3) == 16
     assert lib.mt_version() >> 16 == 1
 
 

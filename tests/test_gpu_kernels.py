@@ -206,6 +206,43 @@ def test_down_residual(mt, gemv, shape, out_f32):
         assert_bf16_close(host_bits(y), ref, "y bf16")
 
 
+@pytest.mark.parametrize("fmt,group", [(1, 128), (2, 64)])
+def test_act_bits_24_massive_channel(mt, fmt, group):
+    """An activation row with one channel 1000x the others (the case the
+    16-bit fixed-point x cannot hold within the bf16 bound): with
+    MT_OPT_ACT_BITS = 24 the one-row gate/up and down calls with bf16 outputs
+    meet it, and 16 bits remain the default."""
+    assert mt.mt_get_option(mt.MT_OPT_ACT_BITS) == 16
+    d, f, N = 4096, 12288, 512
+    seed = 71000 + fmt * 10 + group
+    x = oracle.f64_from_bf16(synth.host_bf16(d, seed, synth.ACT))
+    x[17] = 1000.0
+    x = oracle.bf16_from_f64(x)[None]
+    h = oracle.f64_from_bf16(synth.host_bf16(f, seed + 1, synth.ACT))
+    h[4321] = 1000.0
+    h = oracle.bf16_from_f64(h)[None]
+    res = synth.host_bf16(N, seed + 2, synth.ACT)[None]
+    Wg, Wu = gen_w32(N, d, seed + 3, synth.WEIGHT_OUTLIERS), gen_w32(N, d, seed + 4, synth.WEIGHT_OUTLIERS)
+    Wd = gen_w32(N, f, seed + 5, synth.WEIGHT_OUTLIERS)
+    qg, sg, bg = gpu_pack(mt, Wg, fmt, group)
+    qu, su, bu = gpu_pack(mt, Wu, fmt, group)
+    qd, sd, bd = gpu_pack(mt, Wd, fmt, group)
+    sgu, bgu = torch.stack([sg, su]).contiguous(), torch.stack([bg, bu]).contiguous()
+    hout = torch.empty(1, N, dtype=torch.bfloat16, device="cuda")
+    yout = torch.empty(1, N, dtype=torch.bfloat16, device="cuda")
+    mt.mt_set_option(mt.MT_OPT_ACT_BITS, 24)
+    try:
+        mt.mt_swiglu_gateup(dev_bf16(x), qg, qu, sgu, bgu, group, hout, fmt=fmt)
+        mt.mt_down_residual(dev_bf16(h), qd, sd, bd, group, dev_bf16(res), yout, fmt=fmt)
+        torch.cuda.synchronize()
+    finally:
+        mt.mt_set_option(mt.MT_OPT_ACT_BITS, 16)
+    h_ref = oracle.swiglu_gateup(x, orc_weight(Wg, fmt, group), orc_weight(Wu, fmt, group))
+    y_ref = oracle.down_residual(h, orc_weight(Wd, fmt, group), res)
+    assert_bf16_close(host_bits(hout), h_ref, "h bf16, 24-bit x")
+    assert_bf16_close(host_bits(yout), y_ref, "y bf16, 24-bit h")
+
+
 @pytest.mark.parametrize("group,K,N", [(128, 4096, 1000), (64, 12288, 333), (32, 1024, 257)])
 def test_two_rows_match_one_row_calls(mt, group, K, N):
     """Two activation rows over affine INT8 weights (one kernel reading each

@@ -84,6 +84,22 @@ SMALL = [
 
 @pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name.replace(" ", "-"))
 def test_stack_small(mt, wl):
+    _check_stack(mt, wl)
+
+
+@pytest.mark.parametrize("wl", [SMALL[1], SMALL[3]], ids=lambda w: w.name.replace(" ", "-"))
+def test_stack_act_bits_24(mt, wl):
+    """A plan created while MT_OPT_ACT_BITS is 24 stages x and h in 24-bit
+    fixed point: parity, and bit-identity with the single calls made with the
+    same option."""
+    mt.mt_set_option(mt.MT_OPT_ACT_BITS, 24)
+    try:
+        _check_stack(mt, wl)
+    finally:
+        mt.mt_set_option(mt.MT_OPT_ACT_BITS, 16)
+
+
+def _check_stack(mt, wl):
     n = wl.layers
     layers = [DevLayer(mt, wl, l) for l in range(n)]
     vals, r0 = _acts(wl, n)

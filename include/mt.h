@@ -136,7 +136,8 @@ typedef enum mt_option {
                       the other channels) can exceed it; 24 bits keep such
                       rows within the bound at ~1.5 us more per executor layer
                       (Qwen3-8B shape).  A plan takes the value set when it is
-                      created. */
+                      created; mt_mlp_stack_run_noalloc the value set when it
+                      is called. */
 } mt_option;
 
 /*
